@@ -1,0 +1,143 @@
+/*
+ * ida.h -- C ABI of the GB300 (sm_103a) Interdomain Attention token mixer.
+ *
+ * The operation is the token mixer of "Interdomain Attention: Beyond
+ * Token-Level Key-Value Memory" (arXiv 2605.24330) in its scalable form, as
+ * the German technical summary of that paper states it in the section
+ * "Skalierbare Implementierung" (the Dutch summary, "Schaalbare
+ * Implementatie", says the same).  Per batch row b and head h, with
+ * x_t in R^R the raw query or key row and v_t in R^d the value row:
+ *
+ *   feature map     xi(x) = SiLU(SC(x)) / ||SiLU(SC(x))||^2, SC a causal
+ *                   depthwise conv of width W (own taps for q and for k);
+ *   normalisation   kt = RMSNorm(xi(k)) * w_k + b_k,  vt = RMSNorm(v) * w_v + b_v
+ *                   (per-head weights and biases on the key and value halves);
+ *   recurrent core  one complex diagonal S4D recurrence over z_t = [kt_t ; vt_t]:
+ *                   X_t = lambda o X_{t-1} + B o z_t, X_{-1} = 0, with
+ *                   U_t = X_t[:, :R] (M x R) and Gamma_t = X_t[:, R:] (M x d),
+ *                   the state shapes of the paper's Fig. 1 caption;
+ *   readout         o_t = Re( xi(q_t)^T U_t^T Gamma_t )  (denominator-free), or
+ *                   with IDA_READOUT_ETA the ratio form of the summary's
+ *                   "Theoretische Herleitung": o_t /= Re( xi(q_t)^T U_t^T eta_t ),
+ *                   eta_t = lambda o eta_{t-1} + B.
+ *
+ * Readings where the pages are silent: ||.||^2 is the squared Euclidean norm
+ * plus IDA_EPS_FEAT; RMSNorm uses mean square + IDA_EPS_RMS; conv taps in
+ * cross-correlation order (tap W-1 on the current token), zero left padding,
+ * no conv bias, v not convolved, q not RMS-normed; lambda and B are the
+ * discretised complex parameters (no conjugation, real part taken last, no
+ * factor 2); the eta division has no epsilon.
+ *
+ * Conventions for every call:
+ *   - All data pointers are device pointers owned by the caller, 16-byte
+ *     aligned.  The library allocates no device memory per call.
+ *   - Calls are asynchronous on `stream` and never synchronise.  The return
+ *     value reports argument errors (nothing is launched) and launch errors.
+ *   - Kernels never trap.  A device-side fault detected by a kernel (e.g. a
+ *     bounded wait that ran out) is recorded in a device error word and
+ *     returned as IDA_ERR_DEVICE by the next call (or by ida_device_error).
+ *   - Outputs must not alias inputs.
+ *   - Supported: 8 <= R,d <= 256 with R % 8 == 0 and d % 8 == 0,
+ *     1 <= M <= 128, 1 <= W <= 4.  Other shapes return IDA_ERR_UNSUPPORTED.
+ */
+#ifndef IDA_H
+#define IDA_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define IDA_API __attribute__((visibility("default")))
+#else
+#define IDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *ida_stream_t;
+
+typedef enum {
+    IDA_OK = 0,
+    IDA_ERR_ARG = 1,          /* null/misaligned pointer, negative size, bad enum */
+    IDA_ERR_UNSUPPORTED = 2,  /* valid but outside the supported shape set       */
+    IDA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed             */
+    IDA_ERR_DEVICE = 4        /* a kernel recorded a device-side error            */
+} ida_status;
+
+enum { IDA_F32 = 0, IDA_BF16 = 1 };            /* dtype of q, k, v and out */
+
+enum {
+    IDA_READOUT_ETA = 1,        /* eta-normalised readout instead of denominator-free */
+    IDA_PATH_SEQUENTIAL = 256   /* force the token-sequential CUDA-core prefill kernel */
+};
+
+#define IDA_EPS_FEAT 1e-6f
+#define IDA_EPS_RMS 1e-6f
+
+/*
+ * Number of floats of one (b,h) recurrent state, the format shared by
+ * ida_forward's final_state and ida_decode_step's state_inout:
+ *   [2M][R+d]  planar complex state: rows 0..M-1 hold Re, rows M..2M-1 hold Im;
+ *              columns 0..R-1 are U, columns R..R+d-1 are Gamma;
+ *   [2M]       eta (Re then Im), maintained whichever readout is used;
+ *   [W-1][R]   raw q rows of the last W-1 positions (conv tail), oldest first;
+ *   [W-1][R]   raw k rows, same;
+ *   0..3       padding floats so that every unit starts on a 16-byte boundary.
+ * Positions before the first token are zero.  Returns 0 for invalid sizes.
+ */
+IDA_API size_t ida_state_floats(int d, int R, int M, int W);
+
+/*
+ * Prefill: run the mixer over N positions of B x H independent (b,h) units,
+ * starting from the zero state.
+ *   q, k    [B, N, H, R]  dtype (IDA_F32: float, IDA_BF16: bfloat16)
+ *   v       [B, N, H, d]  dtype
+ *   conv_w  [2, H, R, W]  float; [0] = query taps, [1] = key taps
+ *   norm_w  [H, R + d]    float; RMSNorm weights, key half first
+ *   bias    [H, R + d]    float; RMSNorm biases, key half first
+ *   lambda  [H, M, 2]     float; complex modes (re, im)
+ *   Bvec    [H, M, 2]     float; complex input gains (re, im)
+ *   out     [B, N, H, d]  dtype; written
+ *   final_state  NULL, or [B, H] x ida_state_floats(d, R, M, W) floats:
+ *           receives the state after the last position.
+ *   flags   IDA_READOUT_ETA and/or IDA_PATH_SEQUENTIAL.
+ * N == 0 writes nothing but the zero final_state (if given).
+ */
+IDA_API ida_status ida_forward(const void *q, const void *k, const void *v,
+                       const float *conv_w, const float *norm_w,
+                       const float *bias, const float *lambda,
+                       const float *Bvec, void *out, float *final_state,
+                       int B, int H, int N, int d, int R, int M, int dtype,
+                       int W, int flags, ida_stream_t stream);
+
+/*
+ * One recurrent decode step (one new position per (b,h) unit).
+ *   q, k [B, H, R], v [B, H, d] in dtype; parameters as for ida_forward;
+ *   state_inout [B, H] x ida_state_floats(...) floats, read and updated in
+ *   place (state, eta and the conv tails); out [B, H, d] in dtype.
+ * A prefill's final_state is a valid state_inout.
+ */
+IDA_API ida_status ida_decode_step(const void *q, const void *k, const void *v,
+                           const float *conv_w, const float *norm_w,
+                           const float *bias, const float *lambda,
+                           const float *Bvec, float *state_inout, void *out,
+                           int B, int H, int d, int R, int M, int dtype,
+                           int W, int flags, ida_stream_t stream);
+
+/* Reads and clears the device error word without synchronising; returns
+ * IDA_OK or IDA_ERR_DEVICE.  *code (nullable) receives the raw word. */
+IDA_API ida_status ida_device_error(unsigned *code);
+
+/* Static text for a status code. */
+IDA_API const char *ida_status_str(ida_status s);
+
+/* Human-readable reason of the last non-OK status on the calling thread. */
+IDA_API const char *ida_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDA_H */

@@ -1,0 +1,179 @@
+"""Python binding of the C ABI in ``include/ida.h`` (``_lib/libida.so``).
+
+Argument marshalling only: every step of the mixer runs in the library's CUDA
+kernels.  Torch supplies device memory and the stream.  There is no fallback:
+if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from pathlib import Path
+
+import torch
+
+LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libida.so"
+
+IDA_OK, IDA_ERR_ARG, IDA_ERR_UNSUPPORTED, IDA_ERR_CUDA, IDA_ERR_DEVICE = range(5)
+IDA_F32, IDA_BF16 = 0, 1
+IDA_READOUT_ETA = 1
+IDA_PATH_SEQUENTIAL = 256
+
+EXPORTED = ("ida_state_floats", "ida_forward", "ida_decode_step", "ida_device_error",
+            "ida_status_str", "ida_last_error")
+
+_lock = threading.Lock()
+_lib = None
+_vp, _fp, _i = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
+
+
+class IdaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load ``libida.so``; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not LIB_PATH.exists():
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with linear_token_mixer_sc_gb300.build.build()")
+            L = ctypes.CDLL(str(LIB_PATH))
+            L.ida_state_floats.restype = ctypes.c_size_t
+            L.ida_state_floats.argtypes = [_i, _i, _i, _i]
+            L.ida_forward.restype = _i
+            L.ida_forward.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _fp,
+                                      _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]
+            L.ida_decode_step.restype = _i
+            L.ida_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _fp, _vp,
+                                          _i, _i, _i, _i, _i, _i, _i, _i, _vp]
+            L.ida_device_error.restype = _i
+            L.ida_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+            L.ida_status_str.restype = ctypes.c_char_p
+            L.ida_status_str.argtypes = [_i]
+            L.ida_last_error.restype = ctypes.c_char_p
+            L.ida_last_error.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != IDA_OK:
+        L = load()
+        raise IdaError(status, f"{what}: {L.ida_status_str(status).decode()} "
+                               f"({L.ida_last_error().decode()})")
+
+
+def ida_state_floats(d: int, R: int, M: int, W: int) -> int:
+    return int(load().ida_state_floats(d, R, M, W))
+
+
+def ida_status_str(status: int) -> str:
+    return load().ida_status_str(status).decode()
+
+
+def ida_last_error() -> str:
+    return load().ida_last_error().decode()
+
+
+def ida_device_error() -> int:
+    code = ctypes.c_uint(0)
+    load().ida_device_error(ctypes.byref(code))
+    return int(code.value)
+
+
+def _p(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return IDA_F32
+    if t.dtype == torch.bfloat16:
+        return IDA_BF16
+    raise TypeError(f"q/k/v must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _params(p: dict):
+    out = []
+    for key in ("conv_w", "norm_w", "bias", "lambda", "Bvec"):
+        t = p[key]
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise ValueError(f"parameter {key} must be a contiguous float32 CUDA tensor")
+        out.append(t)
+    return out
+
+
+def ida_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,
+                out: torch.Tensor | None = None, final_state: torch.Tensor | bool | None = None,
+                flags: int = 0, stream=None):
+    """Prefill.  q, k [B,N,H,R], v [B,N,H,d] CUDA tensors (fp32/bf16, contiguous).
+
+    ``params``: dict of float32 CUDA tensors conv_w [2,H,R,W], norm_w/bias
+    [H,R+d], lambda/Bvec [H,M,2].  ``final_state``: a [B,H,S] float32 tensor to
+    fill, True to allocate one, or None.  Returns (out, final_state).
+    """
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    B, N, H, R = q.shape
+    d = v.shape[3]
+    cw, nw, bs, lam, bv = _params(params)
+    M, W = lam.shape[1], cw.shape[3]
+    if tuple(k.shape) != (B, N, H, R) or tuple(v.shape[:3]) != (B, N, H):
+        raise ValueError("shape mismatch between q, k and v")
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=q.dtype, device=q.device)
+    S = ida_state_floats(d, R, M, W)
+    if final_state is True:
+        final_state = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    elif final_state is False:
+        final_state = None
+    if final_state is not None and (final_state.dtype != torch.float32 or final_state.numel() < B * H * S):
+        raise ValueError("final_state must be float32 with B*H*ida_state_floats elements")
+    st = load().ida_forward(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv), _p(out),
+                            _p(final_state), B, H, N, d, R, M, dt, W, int(flags),
+                            _stream_handle(stream))
+    _check(st, "ida_forward")
+    return out, final_state
+
+
+def ida_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,
+                    state: torch.Tensor, out: torch.Tensor | None = None, flags: int = 0,
+                    stream=None) -> torch.Tensor:
+    """One decode step.  q, k [B,H,R], v [B,H,d]; ``state`` [B,H,S] float32 updated in place."""
+    for t in (q, k, v, state):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("q, k, v and state must be contiguous CUDA tensors")
+    dt = _dtype_code(q)
+    B, H, R = q.shape
+    d = v.shape[2]
+    cw, nw, bs, lam, bv = _params(params)
+    M, W = lam.shape[1], cw.shape[3]
+    if state.dtype != torch.float32 or state.numel() < B * H * ida_state_floats(d, R, M, W):
+        raise ValueError("state must be float32 with B*H*ida_state_floats elements")
+    if out is None:
+        out = torch.empty((B, H, d), dtype=q.dtype, device=q.device)
+    st = load().ida_decode_step(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv),
+                                _p(state), _p(out), B, H, d, R, M, dt, W, int(flags),
+                                _stream_handle(stream))
+    _check(st, "ida_decode_step")
+    return out
+
+
+def params_to_device(p: dict, device="cuda") -> dict:
+    """float32 parameter arrays (e.g. from ``inputs.make_params``) as CUDA tensors."""
+    keys = ("conv_w", "norm_w", "bias", "lambda", "Bvec")
+    return {k: torch.as_tensor(p[k], dtype=torch.float32).contiguous().to(device) for k in keys}

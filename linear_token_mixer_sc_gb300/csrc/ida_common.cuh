@@ -1,0 +1,82 @@
+// ida_common.cuh -- device helpers shared by the mixer's CUDA kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ida.h"
+
+namespace ida {
+
+// Plain argument bundle handed to every prefill kernel.
+struct PrefillArgs {
+    const void *q, *k, *v;
+    const float *conv_w, *norm_w, *bias, *lambda, *Bvec;
+    void *out;
+    float *final_state;
+    int B, H, N, d, R, M, W, dtype, flags;
+    size_t state_floats;
+    unsigned *err;  // device-visible error word (host-mapped)
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v;
+    const float *conv_w, *norm_w, *bias, *lambda, *Bvec;
+    float *state;
+    void *out;
+    int B, H, d, R, M, W, dtype, flags;
+    size_t state_floats;
+    unsigned *err;
+};
+
+// Error codes written to the device error word (first writer wins).
+enum : unsigned {
+    kErrNone = 0,
+    kErrWaitTimeout = 1,
+    kErrTmemAlloc = 2,
+    kErrShape = 3,
+};
+
+__device__ __forceinline__ void report_error(unsigned *err, unsigned code) {
+    if (err) atomicCAS(err, 0u, code);
+}
+
+__device__ __forceinline__ float load_in(const void *base, int dtype, size_t i) {
+    if (dtype == IDA_BF16)
+        return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
+    return reinterpret_cast<const float *>(base)[i];
+}
+
+__device__ __forceinline__ void store_out(void *base, int dtype, size_t i, float x) {
+    if (dtype == IDA_BF16)
+        reinterpret_cast<__nv_bfloat16 *>(base)[i] = __float2bfloat16_rn(x);
+    else
+        reinterpret_cast<float *>(base)[i] = x;
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+struct cplx {
+    float re, im;
+};
+
+__device__ __forceinline__ cplx cmul(cplx a, cplx b) {
+    return {a.re * b.re - a.im * b.im, a.re * b.im + a.im * b.re};
+}
+
+// x <- lam * x + g * z   (z real)
+__device__ __forceinline__ void cstep(float &xr, float &xi, cplx lam, cplx g, float z) {
+    float nr = fmaf(lam.re, xr, fmaf(-lam.im, xi, g.re * z));
+    float ni = fmaf(lam.re, xi, fmaf(lam.im, xr, g.im * z));
+    xr = nr;
+    xi = ni;
+}
+
+}  // namespace ida

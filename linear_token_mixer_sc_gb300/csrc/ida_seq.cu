@@ -1,0 +1,298 @@
+// ida_seq.cu -- token-sequential prefill on CUDA cores (fp32 throughout).
+//
+// This is the exact-arithmetic path of the mixer ("Interdomain Attention:
+// Beyond Token-Level Key-Value Memory", German technical summary,
+// "Skalierbare Implementierung"): it walks the recurrence X_t = lambda X_{t-1}
+// + B z_t one position at a time, reads out a_t = xi(q_t) U_t^T and
+// o_t = Re(a_t Gamma_t) after every step, and keeps the whole complex state in
+// shared memory.  It serves fp32 inputs (where tensor-core rounding would
+// break a 1e-5 relative tolerance) and any shape the chunked tensor-core
+// kernel does not take.
+//
+// Work split: one thread-block cluster of G CTAs per (b,h) unit.  The M
+// modes are independent in the recurrence, so CTA r of the cluster owns modes
+// [r*Mg, (r+1)*Mg) and produces a partial readout over them; the G partials
+// of each position are summed through distributed shared memory.  Positions
+// are processed in tiles of SEQ_T: the prologue (conv, SiLU feature map,
+// RMSNorm) of a tile runs one warp per position, then every warp walks the
+// tile's positions for its modes with the mode's state row in registers.
+#include <cooperative_groups.h>
+
+#include <string>
+
+#include "ida_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace ida {
+
+constexpr int SEQ_WARPS = 16;
+constexpr int SEQ_THREADS = SEQ_WARPS * 32;
+constexpr int SEQ_T = 16;  // positions per tile (one per warp in the prologue)
+
+static size_t seq_smem_bytes(int Mg, int R, int d) {
+    size_t RD = (size_t)R + d;
+    return (size_t)Mg * RD * sizeof(float2)  // X
+           + (size_t)Mg * sizeof(float2)     // eta
+           + (size_t)SEQ_T * R * 4           // xi(q)
+           + (size_t)SEQ_T * RD * 4          // z = [kt ; vt]
+           + (size_t)SEQ_T * d * 4           // partial outputs
+           + (size_t)SEQ_T * 4;              // partial denominators
+}
+
+// Prologue of one position (one warp): xi(q) -> xq_row, [kt ; vt] -> z_row.
+template <int NC>
+__device__ __forceinline__ void seq_prologue(const PrefillArgs &a, int h, size_t base_qk,
+                                             size_t base_v, int t, float *xq_row,
+                                             float *z_row, int lane) {
+    const int R = a.R, d = a.d, W = a.W, H = a.H;
+    const size_t sqk = (size_t)H * R, sv = (size_t)H * d;
+    const float *nw = a.norm_w + (size_t)h * (R + d);
+    const float *bs = a.bias + (size_t)h * (R + d);
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {  // 0: query, 1: key
+        const void *x = which == 0 ? a.q : a.k;
+        const float *cw = a.conv_w + ((size_t)which * H + h) * R * W;
+        float f[NC];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
+            int c = lane + 32 * i;
+            f[i] = 0.f;
+            if (c < R) {
+                float s = 0.f;
+                for (int j = 0; j < W; ++j) {
+                    int p = t - (W - 1) + j;
+                    if (p >= 0) s = fmaf(cw[(size_t)c * W + j], load_in(x, a.dtype, base_qk + (size_t)p * sqk + c), s);
+                }
+                f[i] = silu(s);
+                ss = fmaf(f[i], f[i], ss);
+            }
+        }
+        float inv = 1.f / (warp_sum(ss) + IDA_EPS_FEAT);
+        if (which == 0) {
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                int c = lane + 32 * i;
+                if (c < R) xq_row[c] = f[i] * inv;
+            }
+        } else {
+            float ms = 0.f;
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                f[i] *= inv;
+                ms = fmaf(f[i], f[i], ms);
+            }
+            float r = rsqrtf(warp_sum(ms) / R + IDA_EPS_RMS);
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                int c = lane + 32 * i;
+                if (c < R) z_row[c] = fmaf(f[i] * r, nw[c], bs[c]);
+            }
+        }
+    }
+    float vv[NC];
+    float ms = 0.f;
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        int j = lane + 32 * i;
+        vv[i] = j < d ? load_in(a.v, a.dtype, base_v + (size_t)t * sv + j) : 0.f;
+        ms = fmaf(vv[i], vv[i], ms);
+    }
+    float r = rsqrtf(warp_sum(ms) / d + IDA_EPS_RMS);
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        int j = lane + 32 * i;
+        if (j < d) z_row[R + j] = fmaf(vv[i] * r, nw[R + j], bs[R + j]);
+    }
+}
+
+template <int NC>
+__global__ void __launch_bounds__(SEQ_THREADS, 1) seq_prefill_kernel(PrefillArgs a, int G, int Mg) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int R = a.R, d = a.d, RD = R + d, M = a.M, W = a.W, H = a.H, N = a.N;
+    const int rank = blockIdx.x % G;
+    const int unit = blockIdx.x / G;
+    const int b = unit / H, h = unit % H;
+    const int m0 = rank * Mg;
+    const int mcount = max(0, min(Mg, M - m0));
+    float2 *X = reinterpret_cast<float2 *>(smem);
+    float2 *eta = X + (size_t)Mg * RD;
+    float *xq = reinterpret_cast<float *>(eta + Mg);
+    float *z = xq + SEQ_T * R;
+    float *opart = z + SEQ_T * RD;
+    float *dpart = opart + SEQ_T * d;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t sqk = (size_t)H * R, sv = (size_t)H * d;
+    const size_t base_qk = ((size_t)b * N * H + h) * R;
+    const size_t base_v = ((size_t)b * N * H + h) * d;
+    const bool eta_ro = (a.flags & IDA_READOUT_ETA) != 0;
+
+    for (int i = threadIdx.x; i < Mg * RD; i += SEQ_THREADS) X[i] = make_float2(0.f, 0.f);
+    for (int i = threadIdx.x; i < Mg; i += SEQ_THREADS) eta[i] = make_float2(0.f, 0.f);
+
+    for (int t0 = 0; t0 < N; t0 += SEQ_T) {
+        const int tn = min(SEQ_T, N - t0);
+        // Phase A: prologue, one warp per position; clear the partials.
+        if (warp < tn) {
+            seq_prologue<NC>(a, h, base_qk, base_v, t0 + warp, xq + warp * R, z + warp * RD, lane);
+            for (int j = lane; j < d; j += 32) opart[warp * d + j] = 0.f;
+            if (lane == 0) dpart[warp] = 0.f;
+        }
+        __syncthreads();
+        // Phase B: recurrence + per-mode readout, one warp per mode.
+        for (int ml = warp; ml < mcount; ml += SEQ_WARPS) {
+            const int m = m0 + ml;
+            const cplx lam = {a.lambda[((size_t)h * M + m) * 2], a.lambda[((size_t)h * M + m) * 2 + 1]};
+            const cplx g = {a.Bvec[((size_t)h * M + m) * 2], a.Bvec[((size_t)h * M + m) * 2 + 1]};
+            float ur[NC], ui[NC], gr[NC], gi[NC];
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                int c = lane + 32 * i;
+                float2 u = c < R ? X[(size_t)ml * RD + c] : make_float2(0.f, 0.f);
+                float2 w = c < d ? X[(size_t)ml * RD + R + c] : make_float2(0.f, 0.f);
+                ur[i] = u.x; ui[i] = u.y; gr[i] = w.x; gi[i] = w.y;
+            }
+            float er = eta[ml].x, ei = eta[ml].y;
+            for (int tt = 0; tt < tn; ++tt) {
+                float ar = 0.f, ai = 0.f;
+#pragma unroll
+                for (int i = 0; i < NC; ++i) {
+                    int c = lane + 32 * i;
+                    if (c < R) {
+                        cstep(ur[i], ui[i], lam, g, z[tt * RD + c]);
+                        float xv = xq[tt * R + c];
+                        ar = fmaf(xv, ur[i], ar);
+                        ai = fmaf(xv, ui[i], ai);
+                    }
+                    if (c < d) cstep(gr[i], gi[i], lam, g, z[tt * RD + R + c]);
+                }
+                cstep(er, ei, lam, g, 1.f);
+                ar = warp_sum(ar);
+                ai = warp_sum(ai);
+#pragma unroll
+                for (int i = 0; i < NC; ++i) {
+                    int j = lane + 32 * i;
+                    if (j < d) atomicAdd(&opart[tt * d + j], ar * gr[i] - ai * gi[i]);
+                }
+                if (lane == 0) atomicAdd(&dpart[tt], ar * er - ai * ei);
+            }
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                int c = lane + 32 * i;
+                if (c < R) X[(size_t)ml * RD + c] = make_float2(ur[i], ui[i]);
+                if (c < d) X[(size_t)ml * RD + R + c] = make_float2(gr[i], gi[i]);
+            }
+            if (lane == 0) eta[ml] = make_float2(er, ei);
+        }
+        // Phase C: sum the cluster's partials; CTA r writes positions tt = r (mod G).
+        if (G == 1) {
+            __syncthreads();
+        } else {
+            cg::this_cluster().sync();
+        }
+        for (int tt = rank + G * warp; tt < tn; tt += G * SEQ_WARPS) {
+            float dn = 0.f;
+            if (eta_ro) {
+                for (int r = 0; r < G; ++r) {
+                    const float *pd = G == 1 ? dpart : cg::this_cluster().map_shared_rank(dpart, r);
+                    dn += pd[tt];
+                }
+            }
+            for (int j = lane; j < d; j += 32) {
+                float o = 0.f;
+                for (int r = 0; r < G; ++r) {
+                    const float *po = G == 1 ? opart : cg::this_cluster().map_shared_rank(opart, r);
+                    o += po[tt * d + j];
+                }
+                if (eta_ro) o = o / dn;
+                store_out(a.out, a.dtype, base_v + (size_t)(t0 + tt) * sv + j, o);
+            }
+        }
+        if (G == 1) {
+            __syncthreads();
+        } else {
+            cg::this_cluster().sync();
+        }
+    }
+
+    if (a.final_state) {
+        float *fs = a.final_state + (size_t)unit * a.state_floats;
+        const size_t plane = (size_t)M * RD;
+        for (int i = threadIdx.x; i < mcount * RD; i += SEQ_THREADS) {
+            int ml = i / RD, c = i % RD;
+            float2 x = X[i];
+            fs[(size_t)(m0 + ml) * RD + c] = x.x;
+            fs[plane + (size_t)(m0 + ml) * RD + c] = x.y;
+        }
+        for (int ml = threadIdx.x; ml < mcount; ml += SEQ_THREADS) {
+            fs[2 * plane + m0 + ml] = eta[ml].x;
+            fs[2 * plane + M + m0 + ml] = eta[ml].y;
+        }
+        if (rank == 0) {
+            float *tq = fs + 2 * plane + 2 * M;
+            float *tk = tq + (size_t)(W - 1) * R;
+            for (int i = threadIdx.x; i < (W - 1) * R; i += SEQ_THREADS) {
+                int r = i / R, c = i % R;
+                int p = N - (W - 1) + r;
+                tq[i] = p >= 0 ? load_in(a.q, a.dtype, base_qk + (size_t)p * sqk + c) : 0.f;
+                tk[i] = p >= 0 ? load_in(a.k, a.dtype, base_qk + (size_t)p * sqk + c) : 0.f;
+            }
+            size_t used = 2 * plane + 2 * M + 2 * (size_t)(W - 1) * R;
+            for (size_t i = used + threadIdx.x; i < a.state_floats; i += SEQ_THREADS) fs[i] = 0.f;
+        }
+    }
+}
+
+template <int NC>
+static cudaError_t launch_seq_nc(const PrefillArgs &a, int G, int Mg, size_t smem, cudaStream_t st) {
+    auto kern = seq_prefill_kernel<NC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)G * (unsigned)(a.B * a.H), 1, 1);
+    cfg.blockDim = dim3(SEQ_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, G, Mg);
+}
+
+// Chooses the cluster size: the smallest G whose per-CTA state fits in shared
+// memory, then doubled while the grid stays within one wave of SMs.
+ida_status launch_seq_prefill(const PrefillArgs &a, cudaStream_t st, int num_sms, std::string &why) {
+    const size_t kMaxSmem = 227 * 1024;
+    int G = 1;
+    while (G < 8 && seq_smem_bytes((a.M + G - 1) / G, a.R, a.d) > kMaxSmem) G *= 2;
+    if (seq_smem_bytes((a.M + G - 1) / G, a.R, a.d) > kMaxSmem) {
+        why = "state of M x (R+d) does not fit a cluster of 8 CTAs";
+        return IDA_ERR_UNSUPPORTED;
+    }
+    const long units = (long)a.B * a.H;
+    while (G < 8 && 2 * G <= a.M && units * 2 * G <= num_sms) G *= 2;
+    const int Mg = (a.M + G - 1) / G;
+    const size_t smem = seq_smem_bytes(Mg, a.R, a.d);
+    const int nc_need = ((a.R > a.d ? a.R : a.d) + 31) / 32;
+    cudaError_t e;
+    if (nc_need <= 1)
+        e = launch_seq_nc<1>(a, G, Mg, smem, st);
+    else if (nc_need <= 2)
+        e = launch_seq_nc<2>(a, G, Mg, smem, st);
+    else if (nc_need <= 4)
+        e = launch_seq_nc<4>(a, G, Mg, smem, st);
+    else
+        e = launch_seq_nc<8>(a, G, Mg, smem, st);
+    if (e != cudaSuccess) {
+        why = std::string("sequential prefill launch: ") + cudaGetErrorString(e);
+        return IDA_ERR_CUDA;
+    }
+    return IDA_OK;
+}
+
+}  // namespace ida

@@ -1,0 +1,116 @@
+"""C ABI checks that need no GPU: symbols, state size, argument validation.
+
+Every call here is rejected by the host-side checks before the library
+touches CUDA, so it runs on a machine without a GPU.
+"""
+import ctypes
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+from linear_token_mixer_sc_gb300 import binding, build
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _declared_symbols():
+    text = (ROOT / "include" / "ida.h").read_text()
+    return sorted(set(re.findall(r"IDA_API\s+[\w\s\*]*?\b(ida_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_exported_api():
+    assert set(_declared_symbols()) == set(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_state_floats(lib):
+    for d, R, M, W in [(32, 32, 16, 4), (128, 128, 64, 4), (64, 64, 64, 1), (24, 16, 15, 3)]:
+        n = 2 * M * (R + d) + 2 * M + 2 * (W - 1) * R
+        assert binding.ida_state_floats(d, R, M, W) == (n + 3) // 4 * 4
+    assert binding.ida_state_floats(0, 32, 16, 4) == 0
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert binding.ida_status_str(s).startswith("IDA_")
+
+
+class _Bufs:
+    """Aligned host buffers standing in for device pointers (never dereferenced)."""
+
+    def __init__(self):
+        self.mem = np.zeros(64, dtype=np.float32)
+        base = self.mem.ctypes.data
+        self.p = ctypes.c_void_p((base + 15) // 16 * 16)
+        self.mis = ctypes.c_void_p((base + 15) // 16 * 16 + 4)
+
+
+def _fwd(lib, b, B=1, H=2, N=8, d=32, R=32, M=16, dtype=0, W=4, flags=0, **over):
+    args = dict(q=b.p, k=b.p, v=b.p, cw=b.p, nw=b.p, bs=b.p, lam=b.p, bv=b.p, out=b.p, fs=None)
+    args.update(over)
+    return lib.ida_forward(args["q"], args["k"], args["v"], args["cw"], args["nw"], args["bs"],
+                           args["lam"], args["bv"], args["out"], args["fs"], B, H, N, d, R, M,
+                           dtype, W, flags, None)
+
+
+def _dec(lib, b, B=1, H=2, d=32, R=32, M=16, dtype=0, W=4, flags=0, **over):
+    args = dict(q=b.p, k=b.p, v=b.p, cw=b.p, nw=b.p, bs=b.p, lam=b.p, bv=b.p, st=b.p, out=b.p)
+    args.update(over)
+    return lib.ida_decode_step(args["q"], args["k"], args["v"], args["cw"], args["nw"],
+                               args["bs"], args["lam"], args["bv"], args["st"], args["out"],
+                               B, H, d, R, M, dtype, W, flags, None)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    b = _Bufs()
+    assert _fwd(lib, b, q=None) == binding.IDA_ERR_ARG
+    assert _fwd(lib, b, out=None) == binding.IDA_ERR_ARG
+    assert _fwd(lib, b, lam=b.mis) == binding.IDA_ERR_ARG
+    assert _fwd(lib, b, fs=b.mis) == binding.IDA_ERR_ARG
+    assert _fwd(lib, b, N=-1) == binding.IDA_ERR_ARG
+    assert _fwd(lib, b, B=-2) == binding.IDA_ERR_ARG
+    assert _fwd(lib, b, dtype=7) == binding.IDA_ERR_ARG
+    assert _fwd(lib, b, flags=2) == binding.IDA_ERR_ARG
+    assert _fwd(lib, b, M=0) == binding.IDA_ERR_ARG
+    assert "pointer" in binding.ida_last_error() or "must" in binding.ida_last_error()
+
+
+def test_forward_rejects_unsupported_shapes(lib):
+    b = _Bufs()
+    for over in (dict(R=264), dict(d=12), dict(R=4), dict(M=129), dict(W=5), dict(d=512)):
+        assert _fwd(lib, b, **over) == binding.IDA_ERR_UNSUPPORTED, over
+
+
+def test_forward_empty_work_is_a_noop(lib):
+    b = _Bufs()
+    assert _fwd(lib, b, N=0) == binding.IDA_OK
+    assert _fwd(lib, b, B=0) == binding.IDA_OK
+    assert _fwd(lib, b, H=0, q=None, out=None) == binding.IDA_OK
+
+
+def test_decode_rejects_bad_arguments(lib):
+    b = _Bufs()
+    assert _dec(lib, b, st=None) == binding.IDA_ERR_ARG
+    assert _dec(lib, b, st=b.mis) == binding.IDA_ERR_ARG
+    assert _dec(lib, b, dtype=3) == binding.IDA_ERR_ARG
+    assert _dec(lib, b, R=100) == binding.IDA_ERR_UNSUPPORTED
+    assert _dec(lib, b, B=0) == binding.IDA_OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "LIB_PATH", tmp_path / "missing.so")
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.load()

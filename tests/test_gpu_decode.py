@@ -1,0 +1,121 @@
+"""GPU parity of ida_decode_step against the fp64 CPU oracle.
+
+The decode kernel is checked on its own (starting from the oracle's state
+rounded to fp32), chained after a GPU prefill, and at the full recurrent
+decode workload (batch 256, 16 heads, R = d = 128, M = 64: a 4096-position
+prefill then 512 steps) on sampled (b,h) units.
+"""
+import numpy as np
+import pytest
+import torch
+
+from linear_token_mixer_sc_gb300 import binding, build, configs, inputs
+from oracle import ida_oracle as orc
+from tests.helpers import (BF16_REL_L2, F32_MAX_ABS, F32_REL_L2, head_params, max_abs, problem,
+                           rel_l2, to_np, unpadded_state)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    binding.load()
+
+
+def _pad_state(st64: np.ndarray, S: int) -> torch.Tensor:
+    B, H, n = st64.shape
+    out = np.zeros((B, H, S), dtype=np.float32)
+    out[..., :n] = st64
+    return torch.from_numpy(out).cuda()
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 32, 32, 16, 4, "f32"), (3, 2, 24, 40, 7, 3, "f32"),
+                                   (2, 3, 128, 128, 64, 4, "bf16"), (1, 1, 256, 256, 128, 4, "f32"),
+                                   (2, 2, 16, 8, 5, 1, "f32")],
+                         ids=lambda s: "B{}H{}d{}R{}M{}W{}{}".format(*s))
+@pytest.mark.parametrize("eta", [0, binding.IDA_READOUT_ETA])
+def test_decode_from_oracle_state(shape, eta):
+    """Decode kernel alone: same fp32 state in, compare out and state over 6 steps."""
+    B, H, d, R, M, W, dt = shape
+    N0 = 11
+    q, k, v, p = problem(B, N0, H, R, d, M, W, dt, seed=200 + d)
+    ref = orc.forward(q, k, v, p, flags=eta, final_state=True)
+    S = binding.ida_state_floats(d, R, M, W)
+    # the device starts from the oracle's state rounded to fp32; so does the oracle
+    st32 = ref["final_state"].astype(np.float32)
+    st_dev = _pad_state(st32, S)
+    st_ref = st32.astype(np.float64)
+    pd = binding.params_to_device(p)
+    for step in range(6):
+        qt, kt, vt = inputs.make_tokens(B, H, R, d, dt, seed=7, step=step)
+        out = binding.ida_decode_step(qt.cuda(), kt.cuda(), vt.cuda(), pd, st_dev, flags=eta)
+        r = orc.decode_step(qt, kt, vt, p, st_ref, flags=eta)
+        torch.cuda.synchronize()
+        got = to_np(out)
+        if dt == "f32":
+            assert rel_l2(got, r["out"]) <= F32_REL_L2 and max_abs(got, r["out"]) <= F32_MAX_ABS
+        else:
+            assert rel_l2(got, r["out"]) <= BF16_REL_L2
+    got_st = unpadded_state(to_np(st_dev), d, R, M, W)
+    assert rel_l2(got_st, st_ref) <= 1e-5
+    assert binding.ida_device_error() == 0
+
+
+def test_prefill_then_decode_chain_tiny():
+    """GPU prefill(N-j) + j GPU decode steps == oracle prefill(N) (fp32)."""
+    w = configs.TINY_F32
+    q, k, v, p = problem(w.B, w.N, w.H, w.R, w.d, w.M, w.W, w.dtype, w.seed)
+    j = 9
+    N = w.N
+    pd = binding.params_to_device(p)
+    _, st = binding.ida_forward(q[:, :N - j].contiguous().cuda(), k[:, :N - j].contiguous().cuda(),
+                                v[:, :N - j].contiguous().cuda(), pd, final_state=True)
+    ref = orc.forward(q, k, v, p, final_state=True)
+    for i in range(N - j, N):
+        out = binding.ida_decode_step(q[:, i].contiguous().cuda(), k[:, i].contiguous().cuda(),
+                                      v[:, i].contiguous().cuda(), pd, st)
+        got = to_np(out)
+        assert rel_l2(got, ref["out"][:, i]) <= F32_REL_L2
+    torch.cuda.synchronize()
+    got_st = unpadded_state(to_np(st), w.d, w.R, w.M, w.W)
+    assert rel_l2(got_st, ref["final_state"]) <= F32_REL_L2
+
+
+def test_decode_full_workload_sampled():
+    """Batch 256 x 16 heads: GPU prefill of 4096 positions, then 512 GPU decode
+    steps; sampled units checked step by step against the oracle."""
+    w = configs.DECODE
+    dev = torch.device("cuda")
+    p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
+    pd = binding.params_to_device(p)
+    q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed, device=dev)
+    _, st = binding.ida_forward(q, k, v, pd, final_state=True)
+    units = [(0, 0), (77, 5), (255, 15)]
+    ref_states, hp = {}, {}
+    for (b, h) in units:
+        hp[(b, h)] = head_params(p, h)
+        r = orc.forward(q[b:b + 1, :, h:h + 1].cpu(), k[b:b + 1, :, h:h + 1].cpu(),
+                        v[b:b + 1, :, h:h + 1].cpu(), hp[(b, h)], final_state=True)
+        ref_states[(b, h)] = r["final_state"]
+    del q, k, v
+    torch.cuda.synchronize()
+    for (b, h) in units:
+        got = unpadded_state(to_np(st[b, h]), w.d, w.R, w.M, w.W)
+        assert rel_l2(got, ref_states[(b, h)][0, 0]) <= 1e-4
+    errs = {u: [] for u in units}
+    sq = {u: [] for u in units}
+    for step in range(w.decode_steps):
+        qt, kt, vt = inputs.make_tokens(w.B, w.H, w.R, w.d, w.dtype, w.seed, step, device=dev)
+        out = binding.ida_decode_step(qt, kt, vt, pd, st)
+        o = to_np(out)
+        for (b, h) in units:
+            r = orc.decode_step(qt[b:b + 1, h:h + 1].cpu(), kt[b:b + 1, h:h + 1].cpu(),
+                                vt[b:b + 1, h:h + 1].cpu(), hp[(b, h)], ref_states[(b, h)])
+            diff = o[b, h] - r["out"][0, 0]
+            errs[(b, h)].append(float(diff @ diff))
+            sq[(b, h)].append(float(r["out"][0, 0] @ r["out"][0, 0]))
+    assert binding.ida_device_error() == 0
+    for u in units:
+        rl = (sum(errs[u]) / sum(sq[u])) ** 0.5
+        assert rl <= BF16_REL_L2, (u, rl)

@@ -1,0 +1,143 @@
+"""GPU parity of ida_forward (prefill) against the fp64 CPU oracle.
+
+Element-by-element comparison on the same seeded input bytes.  Small cases
+cover every kernel path, ragged tails and degenerate shapes; the full-size
+workloads are checked on sampled (b,h) units that the oracle computes one by
+one, in the same launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+from linear_token_mixer_sc_gb300 import binding, build, configs, inputs
+from oracle import ida_oracle as orc
+from tests.helpers import (BF16_REL_L2, F32_MAX_ABS, F32_REL_L2, max_abs, problem, rel_l2,
+                           to_np, unpadded_state)
+
+pytestmark = pytest.mark.gpu
+
+PATHS = {"default": 0, "sequential": binding.IDA_PATH_SEQUENTIAL}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    binding.load()
+
+
+def _run(q, k, v, p, flags=0, final_state=False):
+    dev = torch.device("cuda")
+    pd = binding.params_to_device(p)
+    out, fs = binding.ida_forward(q.to(dev), k.to(dev), v.to(dev), pd, flags=flags,
+                                  final_state=final_state)
+    torch.cuda.synchronize()
+    assert binding.ida_device_error() == 0
+    return out, fs
+
+
+def _check(got, ref, dtype):
+    if dtype == "f32":
+        assert rel_l2(got, ref) <= F32_REL_L2, rel_l2(got, ref)
+        assert max_abs(got, ref) <= F32_MAX_ABS, max_abs(got, ref)
+    else:
+        assert rel_l2(got, ref) <= BF16_REL_L2, rel_l2(got, ref)
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("eta", [False, True])
+def test_tiny_f32_workload(path, eta):
+    w = configs.TINY_F32
+    q, k, v, p = problem(w.B, w.N, w.H, w.R, w.d, w.M, w.W, w.dtype, w.seed)
+    flags = PATHS[path] | (binding.IDA_READOUT_ETA if eta else 0)
+    out, fs = _run(q, k, v, p, flags=flags, final_state=True)
+    ref = orc.forward(q, k, v, p, flags=flags & binding.IDA_READOUT_ETA, final_state=True)
+    _check(to_np(out), ref["out"], "f32")
+    got_st = unpadded_state(to_np(fs), w.d, w.R, w.M, w.W)
+    assert rel_l2(got_st, ref["final_state"]) <= F32_REL_L2
+
+
+# (B, N, H, R, d, M, W, dtype): ragged lengths, d != R, odd M, W < 4, max sizes
+EDGE = [
+    (1, 1, 1, 32, 32, 16, 4, "f32"),
+    (2, 37, 3, 32, 64, 15, 4, "f32"),
+    (1, 70, 2, 64, 32, 7, 2, "f32"),
+    (3, 19, 1, 16, 8, 5, 1, "f32"),
+    (1, 50, 2, 40, 24, 9, 3, "f32"),
+    (1, 33, 1, 256, 256, 128, 4, "f32"),
+    (2, 131, 2, 128, 128, 64, 4, "bf16"),
+    (1, 65, 3, 64, 64, 33, 4, "bf16"),
+]
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("shape", EDGE, ids=lambda s: "B{}N{}H{}R{}d{}M{}W{}{}".format(*s))
+def test_edge_shapes(shape, path):
+    B, N, H, R, d, M, W, dt = shape
+    q, k, v, p = problem(B, N, H, R, d, M, W, dt, seed=100 + N)
+    for eta in (0, binding.IDA_READOUT_ETA):
+        out, fs = _run(q, k, v, p, flags=PATHS[path] | eta, final_state=True)
+        ref = orc.forward(q, k, v, p, flags=eta, final_state=True)
+        _check(to_np(out), ref["out"], dt)
+        got_st = unpadded_state(to_np(fs), d, R, M, W)
+        assert rel_l2(got_st, ref["final_state"]) <= (F32_REL_L2 if dt == "f32" else 1e-4)
+
+
+def test_zero_length_gives_zero_state():
+    q, k, v, p = problem(2, 0, 3, 32, 32, 8, 4, "f32", seed=5)
+    fs = torch.full((2, 3, binding.ida_state_floats(32, 32, 8, 4)), 7.0, device="cuda")
+    out, fs = _run(q, k, v, p, final_state=fs)
+    assert out.numel() == 0
+    assert torch.count_nonzero(fs).item() == 0
+
+
+def test_state_padding_is_zero():
+    q, k, v, p = problem(1, 9, 2, 32, 32, 15, 3, "f32", seed=6)
+    _, fs = _run(q, k, v, p, final_state=True)
+    n = 2 * 15 * 64 + 2 * 15 + 2 * 2 * 32
+    assert fs.shape[-1] > n
+    assert torch.count_nonzero(fs[..., n:]).item() == 0
+
+
+def _sampled(w, units, flags, final_state=False, path=0):
+    """Full-size workload on the GPU, oracle on the sampled units only."""
+    dev = torch.device("cuda")
+    p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
+    q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed)
+    pd = binding.params_to_device(p)
+    out, fs = binding.ida_forward(q.to(dev), k.to(dev), v.to(dev), pd, flags=flags | path,
+                                  final_state=final_state)
+    torch.cuda.synchronize()
+    assert binding.ida_device_error() == 0
+    ref = orc.forward(q, k, v, p, flags=flags, final_state=final_state, units=units, want_den=True)
+    got = to_np(out)
+    errs = []
+    for u in units:
+        b, h = divmod(u, w.H)
+        errs.append(rel_l2(got[b, :, h], ref["out"][b, :, h]))
+        if final_state:
+            st = unpadded_state(to_np(fs[b, h]), w.d, w.R, w.M, w.W)
+            assert rel_l2(st, ref["final_state"][b, h]) <= 1e-4
+    return errs, ref
+
+
+def test_prefill_125m_full_size_sampled():
+    w = configs.PREFILL_125M
+    units = [0, 17, 50, w.B * w.H - 1]
+    errs, _ = _sampled(w, units, 0)
+    assert max(errs) <= BF16_REL_L2, errs
+
+
+@pytest.mark.parametrize("eta", [False, True])
+def test_prefill_1p3b_full_size_sampled(eta):
+    w = configs.PREFILL_1P3B
+    units = [0, 21, w.B * w.H - 1]
+    flags = binding.IDA_READOUT_ETA if eta else 0
+    errs, ref = _sampled(w, units, flags)
+    assert max(errs) <= BF16_REL_L2, errs
+
+
+def test_prefill_14k_full_size_sampled_with_final_state():
+    w = configs.PREFILL_14K
+    units = [0, 9, w.B * w.H - 1]
+    errs, _ = _sampled(w, units, 0, final_state=True)
+    assert max(errs) <= BF16_REL_L2, errs
