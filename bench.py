@@ -1,0 +1,482 @@
+"""Throughput benchmark of the Interdomain Attention token mixer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one pass of the mixer over one batch of synthetic input: a
+prefill (``ida_forward``) for the prefill workloads, one ``ida_decode_step``
+over the whole batch for the decode workload.  The default workload is the
+125M-like prefill (B=8, H=12, N=2048, R=d=64, M=64, bf16); the JSON line also
+carries a ``decode`` object measured in the same run on the recurrent decode
+workload (batch 256, H=16, R=d=128, M=64, state seeded by a 4096-position
+prefill).
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream; between timed steps the L2 is flushed (a 512 MB
+write) when the step's inputs fit in L2.  ``value`` is whole-job tokens/s
+(a token is one position of one batch row, through all H heads).
+``--impl reference`` times the CPU oracle instead (bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import platform
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from linear_token_mixer_sc_gb300 import configs, inputs  # noqa: E402
+
+METRIC = "mixer tokens/s (prefill & decode) at 1 GB300; % of roofline (HBM/TC)"
+L2_BYTES = 126 * 1024 * 1024
+FLUSH_BYTES = 512 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal GB300 unit counts for the FP32 CUDA-core peak (decode arithmetic):
+# 152 SMs x 128 FP32 lanes x 2 flops (FMA) x 2.07 GHz max SM clock.
+FP32_TFLOPS_NOMINAL = 152 * 128 * 2 * 2.07e9 / 1e12
+PREFILL_SOURCES = ["ida_chunk.cu", "ida_seq.cu", "ida_common.cuh", "ida_api.cu"]
+DECODE_SOURCES = ["ida_decode.cu", "ida_common.cuh", "ida_api.cu"]
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sources_sha(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        h.update((ROOT / "linear_token_mixer_sc_gb300" / "csrc" / n).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(workload: str, names):
+    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    rec = json.loads(p.read_text()).get(workload)
+    if not rec or rec.get("source_sha") != sources_sha(names):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def elem_bytes(dtype: str) -> int:
+    return 4 if dtype == "f32" else 2
+
+
+def prefill_bytes(w) -> int:
+    """Compulsory HBM bytes of one prefill launch: read q, k, v once, write out once
+    (plus the final state when it is returned)."""
+    s = elem_bytes(w.dtype)
+    b = w.B * w.H * w.N * ((2 * w.R + w.d) * s + w.d * s)
+    if w.final_state:
+        b += w.B * w.H * state_floats(w) * 4
+    return b
+
+
+def state_floats(w) -> int:
+    n = 2 * w.M * (w.R + w.d) + 2 * w.M + 2 * (w.W - 1) * w.R
+    return (n + 3) // 4 * 4
+
+
+def decode_bytes(w) -> int:
+    """One decode step: state read + write, q, k, v read, out written."""
+    s = elem_bytes(w.dtype)
+    return w.B * w.H * (2 * state_floats(w) * 4 + (2 * w.R + w.d) * s + w.d * s)
+
+
+def mixer_flops(w, positions: int) -> float:
+    """Algorithmic flops of the recurrent form: 12 M (R+d) per position and head
+    (a 6-flop complex update of each state element, 2 flops per element for
+    a = xi(q) U^T and 2 for Re(a Gamma))."""
+    return 12.0 * w.M * (w.R + w.d) * positions
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.idx = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+
+class Prefill:
+    def __init__(self, w, dev, flags=0):
+        from linear_token_mixer_sc_gb300 import binding
+        self.b = binding
+        self.w, self.dev, self.flags = w, dev, flags
+        p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
+        self.params_host = p
+        self.pd = binding.params_to_device(p, dev)
+        q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed)
+        self.host = [t.pin_memory() for t in (q, k, v)]
+        self.q, self.k, self.v = (t.to(dev) for t in self.host)
+        self.out = torch.empty((w.B, w.N, w.H, w.d), dtype=self.q.dtype, device=dev)
+        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.fs = (torch.empty((w.B, w.H, state_floats(w)), dtype=torch.float32, device=dev)
+                   if w.final_state else None)
+        self.in_bytes = sum(t.numel() * t.element_size() for t in self.host)
+        self.launches_per_step = 1
+
+    def step(self):
+        self.b.ida_forward(self.q, self.k, self.v, self.pd, out=self.out, final_state=self.fs,
+                           flags=self.flags)
+
+    def step_e2e(self):
+        for src, dst in zip(self.host, (self.q, self.k, self.v)):
+            dst.copy_(src, non_blocking=True)
+        self.step()
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        return self.in_bytes, self.out.numel() * self.out.element_size()
+
+    def tokens(self):
+        return self.w.B * self.w.N
+
+    def alg_bytes(self):
+        return prefill_bytes(self.w)
+
+    def flops(self):
+        return mixer_flops(self.w, self.w.B * self.w.H * self.w.N)
+
+    def resident_bytes(self):
+        return self.in_bytes + self.out.numel() * self.out.element_size()
+
+
+class Decode:
+    def __init__(self, w, dev, flags=0):
+        from linear_token_mixer_sc_gb300 import binding
+        self.b = binding
+        self.w, self.dev, self.flags = w, dev, flags
+        p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
+        self.pd = binding.params_to_device(p, dev)
+        q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed, device=dev)
+        _, self.state = binding.ida_forward(q, k, v, self.pd, final_state=True)
+        del q, k, v
+        # a ring of pre-drawn tokens so that no generator runs inside the timed region
+        self.ring = [inputs.make_tokens(w.B, w.H, w.R, w.d, w.dtype, w.seed, s, device=dev)
+                     for s in range(8)]
+        self.host_ring = [tuple(t.cpu().pin_memory() for t in r) for r in self.ring[:2]]
+        self.dq, self.dk, self.dv = (torch.empty_like(t) for t in self.ring[0])
+        self.out = torch.empty((w.B, w.H, w.d), dtype=self.ring[0][0].dtype, device=dev)
+        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.i = 0
+        self.launches_per_step = 1
+        torch.cuda.synchronize(dev)
+
+    def step(self):
+        q, k, v = self.ring[self.i % len(self.ring)]
+        self.i += 1
+        self.b.ida_decode_step(q, k, v, self.pd, self.state, out=self.out, flags=self.flags)
+
+    def step_e2e(self):
+        q, k, v = self.host_ring[self.i % 2]
+        self.i += 1
+        self.dq.copy_(q, non_blocking=True)
+        self.dk.copy_(k, non_blocking=True)
+        self.dv.copy_(v, non_blocking=True)
+        self.b.ida_decode_step(self.dq, self.dk, self.dv, self.pd, self.state, out=self.out,
+                               flags=self.flags)
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        r = self.host_ring[0]
+        return sum(t.numel() * t.element_size() for t in r), self.out.numel() * self.out.element_size()
+
+    def tokens(self):
+        return self.w.B
+
+    def alg_bytes(self):
+        return decode_bytes(self.w)
+
+    def flops(self):
+        return mixer_flops(self.w, self.w.B * self.w.H)
+
+    def resident_bytes(self):
+        return self.state.numel() * 4
+
+
+def time_steps(runner, steps, warmup, dev, flush, e2e=False):
+    """Per-step CUDA-event times (ms) on the launching stream."""
+    stream = torch.cuda.current_stream(dev)
+    fn = runner.step_e2e if e2e else runner.step
+    scratch = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for s, e in evs:
+        if scratch is not None:
+            scratch.fill_(1.0)
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def roofline(runner, ms_avg, peaks, peak_kind, traffic, kernel_bound=None):
+    alg_b = runner.alg_bytes()
+    fl = runner.flops()
+    t_b = alg_b / (peaks["hbm_gbs"] * 1e9)
+    t_f = fl / (peaks["bf16_tflops"] * 1e12)
+    bound = kernel_bound or ("hbm" if t_b >= t_f else "tensor")
+    if bound == "hbm":
+        ach = alg_b / (ms_avg * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "algorithmic_bytes": alg_b, "peak_source": f"hbm_gbs ({peak_kind})"}
+    ach = fl / (ms_avg * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
+            "algorithmic_flops": fl, "peak_source": f"bf16_tflops ({peak_kind})"}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, budget_s: float, cores: int, flags: int = 0):
+    """Time the fp64 oracle on a bounded sample of the workload.
+
+    Returns (tokens/s, description, seconds).  Prefill: the first k (b,h)
+    units over all N positions; decode: k units for a few steps.
+    """
+    from oracle import ida_oracle as orc
+    if w.decode_steps:
+        B = min(w.B, max(1, cores))
+        p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
+        st = torch.zeros((B, w.H, orc.state_doubles(w.d, w.R, w.M, w.W)), dtype=torch.float64).numpy()
+        n, t0 = 0, time.perf_counter()
+        while True:
+            q, k, v = inputs.make_tokens(B, w.H, w.R, w.d, w.dtype, w.seed, n)
+            orc.decode_step(q, k, v, p, st, flags=flags, nthreads=cores)
+            n += 1
+            if time.perf_counter() - t0 > budget_s or n >= w.decode_steps:
+                break
+        dt = time.perf_counter() - t0
+        return B * n / dt, f"{n} decode steps of batch {B} x {w.H} heads (of {w.B})", dt
+    p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
+    # calibrate on one unit, then size the sample to the budget
+    Bq = 1
+    q, k, v = inputs.make_qkv(Bq, w.N, 1, w.R, w.d, w.dtype, w.seed)
+    hp = {kk: vv[:, :1] if kk == "conv_w" else vv[:1] for kk, vv in p.items() if kk != "delta"}
+    t0 = time.perf_counter()
+    orc.forward(q, k, v, hp, flags=flags, nthreads=1)
+    t1 = time.perf_counter() - t0
+    units = max(1, min(w.B * w.H, int(budget_s * cores / max(t1, 1e-6))))
+    Bs = max(1, min(w.B, math.ceil(units / w.H)))
+    q, k, v = inputs.make_qkv(Bs, w.N, w.H, w.R, w.d, w.dtype, w.seed)
+    ids = list(range(min(units, Bs * w.H)))
+    t0 = time.perf_counter()
+    orc.forward(q, k, v, p, flags=flags, units=ids, nthreads=cores)
+    dt = time.perf_counter() - t0
+    tok = len(ids) * w.N / w.H
+    return tok / dt, f"{len(ids)} of {w.B * w.H} (b,h) units x {w.N} positions", dt
+
+
+# ---------------------------------------------------------------- main
+
+def dist_setup(n_gpus):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        lr = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(lr)
+        dist.init_process_group("nccl")
+        return dist, dist.get_rank(), ws, lr
+    return None, 0, 1, 0
+
+
+def max_over_ranks(dist, x: float, dev) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e2e=True):
+    runner = (Decode if w.decode_steps else Prefill)(w, dev, flags)
+    flush = runner.resident_bytes() < 2 * L2_BYTES
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    times = time_steps(runner, steps, warmup, dev, flush)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    ms = sum(times) / len(times)
+    ms_all = max_over_ranks(dist, ms, dev)
+    value = ws * runner.tokens() / (ms_all * 1e-3)
+    res = {"value": value, "ms_per_step": ms_all, "tokens_per_step": runner.tokens(),
+           "flush_l2": flush, "wall_s": wall,
+           "roofline": roofline(runner, ms, peaks, peak_kind, traffic_record(w.name, sources)),
+           "gpu_launches": runner.launches_per_step * steps}
+    if e2e:
+        et = time_steps(runner, max(3, steps // 2), 2, dev, False, e2e=True)
+        ems = max_over_ranks(dist, sum(et) / len(et), dev)
+        bi, bo = runner.e2e_bytes()
+        res["e2e"] = {"value": ws * runner.tokens() / (ems * 1e-3), "unit": "tokens/s",
+                      "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                      "ms_per_step": ems}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=configs.PREFILL_125M.name, choices=sorted(configs.ALL))
+    ap.add_argument("--eta", action="store_true", help="eta-normalised readout")
+    ap.add_argument("--no-decode", action="store_true", help="skip the secondary decode line")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle CPU work")
+    args = ap.parse_args()
+    w = configs.ALL[args.workload]
+    flags = 1 if args.eta else 0
+
+    dist, rank, ws, lr = dist_setup(args.gpus)
+    cores = os.cpu_count() or 1
+    config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "R": w.R, "d": w.d, "M": w.M,
+              "W": w.W, "readout": "eta" if args.eta else "denominator-free",
+              "parallelism": f"replicas x{ws} (independent (b,h) units, no collective)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals, desc, spent = [], "", 0.0
+        budget = max(2.0, min(args.cpu_budget, 120.0 / max(1, args.steps + args.warmup)))
+        for i in range(args.warmup + args.steps):
+            v, desc, dt = oracle_sample(w, budget, cores, flags)
+            if i >= args.warmup:
+                vals.append(v)
+                spent += dt
+        value = sum(vals) / len(vals)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * spent / max(1, len(vals)), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config,
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                                 "kind": "oracle", "sample": desc,
+                                 "host": f"{platform.machine()} x{cores}"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    dev = torch.device("cuda", lr)
+    torch.cuda.set_device(dev)
+    from linear_token_mixer_sc_gb300 import binding, build
+    if rank == 0 or dist is None:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    binding.load()
+    peaks, peak_kind = load_peaks()
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    main_res = measure(w, dev, args.steps, args.warmup, flags, dist, ws, peaks, peak_kind,
+                       DECODE_SOURCES if w.decode_steps else PREFILL_SOURCES)
+    clocks = sampler.stop()
+    decode_res = None
+    if not w.decode_steps and not args.no_decode:
+        dw = configs.DECODE
+        sampler2 = ClockSampler(dev.index if dev.index is not None else 0)
+        sampler2.start()
+        decode_res = measure(dw, dev, max(args.steps, 64), args.warmup, 0, dist, ws, peaks,
+                             peak_kind, DECODE_SOURCES, e2e=True)
+        decode_res["clocks"] = sampler2.stop()
+        decode_res["config"] = {"workload": dw.name, "B": dw.B, "H": dw.H, "R": dw.R, "d": dw.d,
+                                "M": dw.M, "seed_prefill_N": dw.N}
+    if binding.ida_device_error() != 0:
+        raise RuntimeError("a kernel reported a device error")
+
+    if rank != 0:
+        return
+    cpu = None
+    if ws == 1 or rank == 0:
+        cv, desc, _ = oracle_sample(w, args.cpu_budget, cores, flags)
+        cpu = {"value": cv, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "host": f"{platform.machine()} x{cores}"}
+    config["l2"] = ("flushed between timed steps" if main_res["flush_l2"]
+                    else "inputs larger than L2")
+    line = {"metric": METRIC, "value": main_res["value"], "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main_res["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded; shapes of the pages' workloads)",
+            "config": config, "roofline": main_res["roofline"], "cpu_baseline": cpu,
+            "e2e": main_res["e2e"], "gpu_launches": main_res["gpu_launches"], "clocks": clocks}
+    if decode_res is not None:
+        line["decode"] = {k: decode_res[k] for k in ("value", "ms_per_step", "roofline", "e2e",
+                                                     "gpu_launches", "clocks", "config")}
+        line["decode"]["unit"] = "tokens/s"
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

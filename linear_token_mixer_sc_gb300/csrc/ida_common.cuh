@@ -56,11 +56,25 @@ __device__ __forceinline__ void store_out(void *base, int dtype, size_t i, float
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+__device__ __forceinline__ double silu(double x) { return x / (1.0 + exp(-x)); }
 
-__device__ __forceinline__ float warp_sum(float x) {
+__device__ __forceinline__ float rsqrt_t(float x) { return rsqrtf(x); }
+__device__ __forceinline__ double rsqrt_t(double x) { return 1.0 / sqrt(x); }
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
+}
+
+// x <- lam * x + g * z for complex x, lam, g and real z, in arithmetic type T.
+template <typename T>
+__device__ __forceinline__ void cstep_t(T &xr, T &xi, T lr, T li, T gr, T gi, T z) {
+    T nr = fma(lr, xr, fma(-li, xi, gr * z));
+    T ni = fma(lr, xi, fma(li, xr, gi * z));
+    xr = nr;
+    xi = ni;
 }
 
 struct cplx {

@@ -13,7 +13,9 @@
 // coalesced accesses.  One CTA per (b,h) unit; each warp owns a strided set
 // of modes, lanes own 4-float column slices, the per-mode dot product is a
 // warp-shuffle reduction and the per-warp partial outputs are summed through
-// shared memory at the end.
+// shared memory at the end.  Arithmetic is fp64 for fp32 inputs (see the
+// sequential prefill for why) and fp32 for bf16 inputs; the state is stored
+// as fp32 either way.
 #include <string>
 
 #include "ida_common.cuh"
@@ -26,8 +28,9 @@ constexpr int DEC_UNROLL = 2;  // modes in flight per warp
 
 // Features of one new position for one unit, one warp each (q, k, v).
 // Shifts the raw conv tails of q and k in the state.
+template <typename T>
 __device__ __forceinline__ void decode_prologue(const DecodeArgs &a, int unit, int h, float *st,
-                                                float *xq_s, float *z_s, int warp, int lane) {
+                                                T *xq_s, T *z_s, int warp, int lane) {
     const int R = a.R, d = a.d, W = a.W, H = a.H, M = a.M, RD = R + d;
     const float *nw = a.norm_w + (size_t)h * RD;
     const float *bs = a.bias + (size_t)h * RD;
@@ -36,24 +39,24 @@ __device__ __forceinline__ void decode_prologue(const DecodeArgs &a, int unit, i
         const void *x = which == 0 ? a.q : a.k;
         const float *cw = a.conv_w + ((size_t)which * H + h) * R * W;
         float *tail = st + 2 * (size_t)M * RD + 2 * M + (size_t)which * (W - 1) * R;
-        float f[8];
-        float ss = 0.f;
+        T f[8];
+        T ss = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             int c = lane + 32 * i;
-            f[i] = 0.f;
+            f[i] = 0;
             if (c < R) {
                 float xc = load_in(x, a.dtype, (size_t)unit * R + c);
-                float s = cw[(size_t)c * W + (W - 1)] * xc;
-                for (int j = 0; j < W - 1; ++j) s = fmaf(cw[(size_t)c * W + j], tail[(size_t)j * R + c], s);
+                T s = (T)cw[(size_t)c * W + (W - 1)] * (T)xc;
+                for (int j = 0; j < W - 1; ++j) s = fma((T)cw[(size_t)c * W + j], (T)tail[(size_t)j * R + c], s);
                 // shift: drop the oldest row, append this position (each lane owns column c)
                 for (int j = 0; j + 1 < W - 1; ++j) tail[(size_t)j * R + c] = tail[(size_t)(j + 1) * R + c];
                 if (W > 1) tail[(size_t)(W - 2) * R + c] = xc;
                 f[i] = silu(s);
-                ss = fmaf(f[i], f[i], ss);
+                ss = fma(f[i], f[i], ss);
             }
         }
-        float inv = 1.f / (warp_sum(ss) + IDA_EPS_FEAT);
+        T inv = T(1) / (warp_sum(ss) + (T)IDA_EPS_FEAT);
         if (which == 0) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -61,44 +64,63 @@ __device__ __forceinline__ void decode_prologue(const DecodeArgs &a, int unit, i
                 if (c < R) xq_s[c] = f[i] * inv;
             }
         } else {
-            float ms = 0.f;
+            T ms = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 f[i] *= inv;
-                ms = fmaf(f[i], f[i], ms);
+                ms = fma(f[i], f[i], ms);
             }
-            float r = rsqrtf(warp_sum(ms) / R + IDA_EPS_RMS);
+            T r = rsqrt_t(warp_sum(ms) / R + (T)IDA_EPS_RMS);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 int c = lane + 32 * i;
-                if (c < R) z_s[c] = fmaf(f[i] * r, nw[c], bs[c]);
+                if (c < R) z_s[c] = fma(f[i] * r, (T)nw[c], (T)bs[c]);
             }
         }
     } else if (warp == 2) {
-        float vv[8];
-        float ms = 0.f;
+        T vv[8];
+        T ms = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             int j = lane + 32 * i;
-            vv[i] = j < d ? load_in(a.v, a.dtype, (size_t)unit * d + j) : 0.f;
-            ms = fmaf(vv[i], vv[i], ms);
+            vv[i] = j < d ? (T)load_in(a.v, a.dtype, (size_t)unit * d + j) : T(0);
+            ms = fma(vv[i], vv[i], ms);
         }
-        float r = rsqrtf(warp_sum(ms) / d + IDA_EPS_RMS);
+        T r = rsqrt_t(warp_sum(ms) / d + (T)IDA_EPS_RMS);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             int j = lane + 32 * i;
-            if (j < d) z_s[R + j] = fmaf(vv[i] * r, nw[R + j], bs[R + j]);
+            if (j < d) z_s[R + j] = fma(vv[i] * r, (T)nw[R + j], (T)bs[R + j]);
         }
     }
 }
 
+__device__ __forceinline__ float4 ld_state(const float *p) {
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+
+template <typename T>
+__device__ __forceinline__ void st_state(float *p, const T v[4]) {
+    __stcs(reinterpret_cast<float4 *>(p), make_float4((float)v[0], (float)v[1], (float)v[2], (float)v[3]));
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack4(float4 f, T v[4]) {
+    v[0] = f.x;
+    v[1] = f.y;
+    v[2] = f.z;
+    v[3] = f.w;
+}
+
 // NV: float4 slices per lane per row half (ceil(max(R, d) / 128)).
-template <int NV>
+// T: arithmetic type (double for fp32 inputs, float for bf16 inputs); the
+// state itself is always stored as fp32.
+template <int NV, typename T>
 __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(DecodeArgs a) {
-    __shared__ __align__(16) float xq_s[256];
-    __shared__ __align__(16) float z_s[512];
-    __shared__ __align__(16) float ored[DEC_WARPS][256];
-    __shared__ float dred[DEC_WARPS];
+    __shared__ __align__(16) T xq_s[256];
+    __shared__ __align__(16) T z_s[512];
+    __shared__ __align__(16) T ored[DEC_WARPS][256];
+    __shared__ T dred[DEC_WARPS];
     const int R = a.R, d = a.d, RD = R + d, M = a.M, H = a.H;
     const int unit = blockIdx.x;
     const int h = unit % H;
@@ -106,22 +128,23 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(DecodeArgs a) {
     float *st = a.state + (size_t)unit * a.state_floats;
     const size_t plane = (size_t)M * RD;
 
-    decode_prologue(a, unit, h, st, xq_s, z_s, warp, lane);
+    decode_prologue<T>(a, unit, h, st, xq_s, z_s, warp, lane);
     __syncthreads();
 
     // Per-lane slices of xi(q) and z, reused for every mode.
-    float4 xq4[NV], zk4[NV], zv4[NV];
+    T xq[NV][4], zk[NV][4], zv[NV][4], oacc[NV][4];
 #pragma unroll
     for (int iv = 0; iv < NV; ++iv) {
-        int c = 4 * (lane + 32 * iv);
-        xq4[iv] = c < R ? *reinterpret_cast<const float4 *>(xq_s + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        zk4[iv] = c < R ? *reinterpret_cast<const float4 *>(z_s + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        zv4[iv] = c < d ? *reinterpret_cast<const float4 *>(z_s + R + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float4 oacc[NV];
+        const int c = 4 * (lane + 32 * iv);
 #pragma unroll
-    for (int iv = 0; iv < NV; ++iv) oacc[iv] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float dacc = 0.f;
+        for (int e = 0; e < 4; ++e) {
+            xq[iv][e] = c < R ? xq_s[c + e] : T(0);
+            zk[iv][e] = c < R ? z_s[c + e] : T(0);
+            zv[iv][e] = c < d ? z_s[R + c + e] : T(0);
+            oacc[iv][e] = T(0);
+        }
+    }
+    T dacc = 0;
 
     for (int mb = warp; mb < M; mb += DEC_WARPS * DEC_UNROLL) {
         float4 ur[DEC_UNROLL][NV], ui[DEC_UNROLL][NV], gr[DEC_UNROLL][NV], gi[DEC_UNROLL][NV];
@@ -134,89 +157,95 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(DecodeArgs a) {
                 const int c = 4 * (lane + 32 * iv);
                 const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
                 const bool okm = m < M;
-                ur[u][iv] = okm && c < R ? __ldcs(reinterpret_cast<const float4 *>(st + (size_t)m * RD + c)) : zero;
-                ui[u][iv] = okm && c < R ? __ldcs(reinterpret_cast<const float4 *>(st + plane + (size_t)m * RD + c)) : zero;
-                gr[u][iv] = okm && c < d ? __ldcs(reinterpret_cast<const float4 *>(st + (size_t)m * RD + R + c)) : zero;
-                gi[u][iv] = okm && c < d ? __ldcs(reinterpret_cast<const float4 *>(st + plane + (size_t)m * RD + R + c)) : zero;
+                ur[u][iv] = okm && c < R ? ld_state(st + (size_t)m * RD + c) : zero;
+                ui[u][iv] = okm && c < R ? ld_state(st + plane + (size_t)m * RD + c) : zero;
+                gr[u][iv] = okm && c < d ? ld_state(st + (size_t)m * RD + R + c) : zero;
+                gi[u][iv] = okm && c < d ? ld_state(st + plane + (size_t)m * RD + R + c) : zero;
             }
         }
 #pragma unroll
         for (int u = 0; u < DEC_UNROLL; ++u) {
             const int m = mb + u * DEC_WARPS;
             if (m >= M) break;
-            const cplx lam = {a.lambda[((size_t)h * M + m) * 2], a.lambda[((size_t)h * M + m) * 2 + 1]};
-            const cplx g = {a.Bvec[((size_t)h * M + m) * 2], a.Bvec[((size_t)h * M + m) * 2 + 1]};
-            float ar = 0.f, ai = 0.f;
+            const T lr = a.lambda[((size_t)h * M + m) * 2], li = a.lambda[((size_t)h * M + m) * 2 + 1];
+            const T br = a.Bvec[((size_t)h * M + m) * 2], bi = a.Bvec[((size_t)h * M + m) * 2 + 1];
+            T ar = 0, ai = 0;
+            T yr[NV][4], yi[NV][4];
 #pragma unroll
             for (int iv = 0; iv < NV; ++iv) {
-                float4 &xr = ur[u][iv], &xi = ui[u][iv];
-                cstep(xr.x, xi.x, lam, g, zk4[iv].x);
-                cstep(xr.y, xi.y, lam, g, zk4[iv].y);
-                cstep(xr.z, xi.z, lam, g, zk4[iv].z);
-                cstep(xr.w, xi.w, lam, g, zk4[iv].w);
-                ar = fmaf(xq4[iv].x, xr.x, fmaf(xq4[iv].y, xr.y, fmaf(xq4[iv].z, xr.z, fmaf(xq4[iv].w, xr.w, ar))));
-                ai = fmaf(xq4[iv].x, xi.x, fmaf(xq4[iv].y, xi.y, fmaf(xq4[iv].z, xi.z, fmaf(xq4[iv].w, xi.w, ai))));
-                float4 &yr = gr[u][iv], &yi = gi[u][iv];
-                cstep(yr.x, yi.x, lam, g, zv4[iv].x);
-                cstep(yr.y, yi.y, lam, g, zv4[iv].y);
-                cstep(yr.z, yi.z, lam, g, zv4[iv].z);
-                cstep(yr.w, yi.w, lam, g, zv4[iv].w);
+                const int c = 4 * (lane + 32 * iv);
+                T xr[4], xi[4];
+                unpack4(ur[u][iv], xr);
+                unpack4(ui[u][iv], xi);
+                unpack4(gr[u][iv], yr[iv]);
+                unpack4(gi[u][iv], yi[iv]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    cstep_t(xr[e], xi[e], lr, li, br, bi, zk[iv][e]);
+                    ar = fma(xq[iv][e], xr[e], ar);
+                    ai = fma(xq[iv][e], xi[e], ai);
+                    cstep_t(yr[iv][e], yi[iv][e], lr, li, br, bi, zv[iv][e]);
+                }
+                if (c < R) {
+                    st_state(st + (size_t)m * RD + c, xr);
+                    st_state(st + plane + (size_t)m * RD + c, xi);
+                }
+                if (c < d) {
+                    st_state(st + (size_t)m * RD + R + c, yr[iv]);
+                    st_state(st + plane + (size_t)m * RD + R + c, yi[iv]);
+                }
             }
             ar = warp_sum(ar);
             ai = warp_sum(ai);
 #pragma unroll
-            for (int iv = 0; iv < NV; ++iv) {
-                const float4 yr = gr[u][iv], yi = gi[u][iv];
-                oacc[iv].x += ar * yr.x - ai * yi.x;
-                oacc[iv].y += ar * yr.y - ai * yi.y;
-                oacc[iv].z += ar * yr.z - ai * yi.z;
-                oacc[iv].w += ar * yr.w - ai * yi.w;
-                const int c = 4 * (lane + 32 * iv);
-                if (c < R) {
-                    __stcs(reinterpret_cast<float4 *>(st + (size_t)m * RD + c), ur[u][iv]);
-                    __stcs(reinterpret_cast<float4 *>(st + plane + (size_t)m * RD + c), ui[u][iv]);
-                }
-                if (c < d) {
-                    __stcs(reinterpret_cast<float4 *>(st + (size_t)m * RD + R + c), yr);
-                    __stcs(reinterpret_cast<float4 *>(st + plane + (size_t)m * RD + R + c), yi);
-                }
-            }
-            float er = st[2 * plane + m], ei = st[2 * plane + M + m];
-            cstep(er, ei, lam, g, 1.f);
+            for (int iv = 0; iv < NV; ++iv)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) oacc[iv][e] += ar * yr[iv][e] - ai * yi[iv][e];
+            T er = st[2 * plane + m], ei = st[2 * plane + M + m];
+            cstep_t(er, ei, lr, li, br, bi, T(1));
             dacc += ar * er - ai * ei;
             __syncwarp();
             if (lane == 0) {
-                st[2 * plane + m] = er;
-                st[2 * plane + M + m] = ei;
+                st[2 * plane + m] = (float)er;
+                st[2 * plane + M + m] = (float)ei;
             }
         }
     }
 #pragma unroll
     for (int iv = 0; iv < NV; ++iv) {
-        int c = 4 * (lane + 32 * iv);
-        if (c < d) *reinterpret_cast<float4 *>(&ored[warp][c]) = oacc[iv];
+        const int c = 4 * (lane + 32 * iv);
+        if (c < d)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ored[warp][c + e] = oacc[iv][e];
     }
     if (lane == 0) dred[warp] = dacc;
     __syncthreads();
     const bool eta_ro = (a.flags & IDA_READOUT_ETA) != 0;
-    float dn = 0.f;
+    T dn = 0;
     if (eta_ro)
         for (int w = 0; w < DEC_WARPS; ++w) dn += dred[w];
     for (int j = threadIdx.x; j < d; j += DEC_THREADS) {
-        float o = 0.f;
+        T o = 0;
         for (int w = 0; w < DEC_WARPS; ++w) o += ored[w][j];
         if (eta_ro) o = o / dn;
-        store_out(a.out, a.dtype, (size_t)unit * d + j, o);
+        store_out(a.out, a.dtype, (size_t)unit * d + j, (float)o);
     }
 }
 
 ida_status launch_decode(const DecodeArgs &a, cudaStream_t st, std::string &why) {
     const int need = ((a.R > a.d ? a.R : a.d) + 127) / 128;
     const unsigned grid = (unsigned)(a.B * a.H);
-    if (need <= 1)
-        decode_kernel<1><<<grid, DEC_THREADS, 0, st>>>(a);
-    else
-        decode_kernel<2><<<grid, DEC_THREADS, 0, st>>>(a);
+    if (a.dtype == IDA_F32) {
+        if (need <= 1)
+            decode_kernel<1, double><<<grid, DEC_THREADS, 0, st>>>(a);
+        else
+            decode_kernel<2, double><<<grid, DEC_THREADS, 0, st>>>(a);
+    } else {
+        if (need <= 1)
+            decode_kernel<1, float><<<grid, DEC_THREADS, 0, st>>>(a);
+        else
+            decode_kernel<2, float><<<grid, DEC_THREADS, 0, st>>>(a);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         why = std::string("decode launch: ") + cudaGetErrorString(e);
