@@ -1,12 +1,659 @@
-// ida_chunk.cu -- chunked tensor-core prefill (placeholder: not yet taken).
+// ida_chunk.cu -- chunked prefill on the tcgen05 tensor cores.
+//
+// The recurrence X_t = lambda X_{t-1} + B z_t and the readout
+// o_t = Re(xi(q_t)^T U_t^T Gamma_t) of "Interdomain Attention: Beyond
+// Token-Level Key-Value Memory" (German technical summary, "Skalierbare
+// Implementierung"; state shapes from the paper's Fig. 1 caption) are
+// re-associated over chunks of C = 64 positions.  With X_p the state before
+// a chunk and i, j in [0, C) local positions:
+//
+//   P[i,m]   = xi(q_i) . U_p[m]                           (state read-out)
+//   G[i,j]   = xi(q_i) . kt_j,     G'[i,k] = G[i,i-k] for k <= i, else 0
+//   L[i,m]   = sum_k G'[i,k] lambda_m^k = sum_{j<=i} lambda_m^{i-j} G[i,j]
+//   a[i,m]   = lambda_m^{i+1} P[i,m] + B_m L[i,m]         (= xi(q_i) . U_i[m])
+//   A2'[i,k] = Re sum_m a[i,m] B_m lambda_m^k,  A2[i,j] = A2'[i,i-j] (j <= i)
+//   o_i      = sum_j A2[i,j] vt_j + Re sum_m a[i,m] lambda_m^{i+1} Gamma_p[m]
+//   X_end    = lambda^L X_p + sum_j B lambda^{L-1-j} z_j   (L = chunk length)
+//
+// Skewing the Gram matrix (G' and A2') makes every intra-chunk decay factor
+// a power lambda^k with 0 <= k < C, so no operand grows beyond |lambda| <= 1
+// for any stable mode.  Every contraction above is an MMA:
+//
+//   G     [128 x 64]  = [xiQ ; Kt] . Kt^T          kind::f16  (rows 64..127 unused)
+//   P^T   [2M x 64]   = U . xiQ^T                  kind::tf32, U read from TMEM
+//   L^T   [2M x 64]   = T_L . G'^T                 kind::f16
+//   A2'   [128 x 64]  = Ya . T_A^T                 kind::f16  (rows 64..127 unused)
+//   O1    [128 x 64]  = Vt^T . A2^T                kind::f16  (lanes = value channel)
+//   O2    [128 x 64]  = Gamma^T . a'^T             kind::tf32, Gamma^T read from TMEM
+//   U    += Coef . Kt^T-chunk,  Gamma^T += Vt^T . Coef^T      kind::f16
+//
+// The complex state never leaves the SM: U (lanes = mode planes 2m / 2m+1 for
+// Re / Im, columns = key channels) and Gamma^T (lanes = value channels,
+// columns = mode planes) are fp32 MMA accumulators in TMEM; each chunk first
+// scales them by lambda^L on the CUDA cores, then accumulates the chunk's
+// contribution with two MMAs.  Operands that are unbounded (Ya, A2) are
+// stored as fp16 with a power-of-two scale per column / row, undone exactly
+// in the matching table or epilogue.
+//
+// One CTA of 128 threads per (b,h) unit; thread t owns TMEM lane t; thread 0
+// issues the MMAs.  Every wait on an MMA completion is bounded; on timeout
+// the kernel records kErrWaitTimeout, stops, frees its TMEM and returns.
+#include <cuda_fp16.h>
+
 #include <string>
 
 #include "ida_common.cuh"
+#include "tc_sm103.cuh"
 
 namespace ida {
 
-ida_status launch_chunk_prefill(const PrefillArgs &, cudaStream_t, int, std::string &, bool *taken) {
+using namespace tc;
+
+constexpr int CH = 64;    // positions per chunk
+constexpr int NTH = 128;  // threads per CTA
+constexpr int MP = 128;   // mode planes (2M, M = 64)
+constexpr int PADLBO = 144;  // core-matrix stride along K for column-wise (transposed) writers
+
+template <int R, int D>
+struct ChunkSmem {
+    // All operands are K-major, no-swizzle core-matrix layouts (8 rows x 16 B).
+    static constexpr int XQ16 = 0;                               // [64][R] f16   LBO 128, SBO 16R
+    static constexpr int KT16 = XQ16 + CH * R * 2;               // [64][R] f16   (follows XQ16: A rows 64..127)
+    static constexpr int XQ32 = KT16 + CH * R * 2;               // [64][R] tf32  LBO 128, SBO 32R; skew scratch
+    static constexpr int ZT16 = XQ32 + CH * R * 4;               // [R+D][64] f16 LBO 144, SBO 1152
+    static constexpr int ZT_SBO = 8 * PADLBO;
+    static constexpr int GP16 = ZT16 + (R + D) / 8 * ZT_SBO;     // [64][64] f16  LBO 128, SBO 1024
+    static constexpr int A216 = GP16 + CH * CH * 2;              // [64][64] f16
+    static constexpr int TL16 = A216 + CH * CH * 2;              // [128][64] f16 LBO 128, SBO 1024
+    static constexpr int CF16 = TL16 + MP * CH * 2;              // [128][64] f16
+    static constexpr int TA16 = CF16 + MP * CH * 2;              // [64][128] f16 LBO 144, SBO 2304
+    static constexpr int TY_SBO = 16 * PADLBO;
+    static constexpr int YA16 = TA16 + 8 * TY_SBO;               // [64][128] f16 LBO 144, SBO 2304
+    static constexpr int AP32 = YA16 + 8 * TY_SBO;               // [64][128] tf32 LBO 144, SBO 4608
+    static constexpr int AP_SBO = 32 * PADLBO;
+    static constexpr int MISC = AP32 + 8 * AP_SBO;
+    static constexpr int BARS = MISC;                            // 5 mbarriers
+    static constexpr int TSLOT = BARS + 64;                      // TMEM base address
+    static constexpr int FLAG = TSLOT + 16;                      // abort flag
+    static constexpr int OSC = FLAG + 16;                        // [64] float: row scales of A2
+    static constexpr int LAML = OSC + CH * 4;                    // [64] float2: lambda^L per mode
+    static constexpr int TOTAL = LAML + 64 * 8;
+};
+
+// TMEM column map (512 columns allocated).
+template <int R>
+struct ChunkTmem {
+    static constexpr uint32_t U = 0;        // [2M lanes][R]
+    static constexpr uint32_t GT = R;       // [value lanes][2M]
+    static constexpr uint32_t G = 256;      // [64 lanes][64], later A2'
+    static constexpr uint32_t PT = 320;     // [2M lanes][64], later O1
+    static constexpr uint32_t LT = 384;     // [2M lanes][64], later O2
+};
+
+// byte offset of element (row, k) in a K-major no-swizzle operand
+__device__ __forceinline__ int kmaj_off(int row, int k, int esize, int lbo, int sbo) {
+    const int T = 16 / esize;
+    return (row >> 3) * sbo + (k / T) * lbo + (row & 7) * 16 + (k % T) * esize;
+}
+
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// exponent e >= 0 such that x * 2^-e <= 2^14 (fp16 headroom), for x >= 0
+__device__ __forceinline__ int down_exp(float x) {
+    if (!(x > 16384.f)) return 0;
+    int ex = ((__float_as_int(x) >> 23) & 0xFF) - 127;  // floor(log2 x)
+    int e = ex - 13;
+    return e > 15 ? 15 : e;
+}
+
+template <int R, int D>
+__global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
+    using S = ChunkSmem<R, D>;
+    using T = ChunkTmem<R>;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S::BARS);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S::TSLOT);
+    int *flag = reinterpret_cast<int *>(sm + S::FLAG);
+    float *osc = reinterpret_cast<float *>(sm + S::OSC);
+    float2 *laml = reinterpret_cast<float2 *>(sm + S::LAML);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H, N = a.N, M = 64, W = a.W;
+    const int unit = blockIdx.x, b = unit / H, h = unit % H;
+    const size_t sqk = (size_t)H * R, sv = (size_t)H * D;
+    const size_t base_qk = ((size_t)b * N * H + h) * R;
+    const size_t base_v = ((size_t)b * N * H + h) * D;
+    const __nv_bfloat16 *gq = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+    const __nv_bfloat16 *gk = reinterpret_cast<const __nv_bfloat16 *>(a.k);
+    const __nv_bfloat16 *gv = reinterpret_cast<const __nv_bfloat16 *>(a.v);
+    __nv_bfloat16 *gout = reinterpret_cast<__nv_bfloat16 *>(a.out);
+
+    // my mode plane (thread mp = tid): m = tid / 2, Re (even) / Im (odd)
+    const int mp = tid, mm = tid >> 1, is_im = tid & 1;
+    const float lam_r = a.lambda[((size_t)h * M + mm) * 2], lam_i = a.lambda[((size_t)h * M + mm) * 2 + 1];
+    const float b_r = a.Bvec[((size_t)h * M + mm) * 2], b_i = a.Bvec[((size_t)h * M + mm) * 2 + 1];
+
+    // ---- set-up: barriers, TMEM, constant tables ----------------------------
+    if (tid == 0) {
+        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
+        *flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    {
+        // T_L row mp: component of lambda_m^k, k = 0..63; Coef row mp: component of
+        // B_m lambda_m^(C-1-j).  Powers in fp64 to keep the tables exact to fp16.
+        double pr = 1.0, pi = 0.0;
+        __half tl[CH], cf[CH];
+        for (int k = 0; k < CH; ++k) {
+            tl[k] = __float2half_rn((float)(is_im ? pi : pr));
+            double cr = b_r * pr - b_i * pi, ci = b_r * pi + b_i * pr;  // B lambda^k
+            cf[CH - 1 - k] = __float2half_rn((float)(is_im ? ci : cr));
+            double nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
+            pr = nr;
+            pi = ni;
+        }
+        if (!is_im) laml[mm] = make_float2((float)pr, (float)pi);  // lambda^C
+        for (int k8 = 0; k8 < CH / 8; ++k8) {
+            *reinterpret_cast<uint4 *>(sm + S::TL16 + kmaj_off(mp, k8 * 8, 2, 128, 1024)) =
+                *reinterpret_cast<const uint4 *>(&tl[k8 * 8]);
+            *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(mp, k8 * 8, 2, 128, 1024)) =
+                *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *tslot;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    {
+        // zero state: U (cols [0,R)) and Gamma^T (cols [R, R+128)) in every lane
+        float z[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) z[i] = 0.f;
+        for (int c0 = 0; c0 < R + MP; c0 += 16) tmem_st16(tb + lane_base + c0, z);
+        tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // eta_p (for the final state): complex per mode, kept by the Re thread
+    float eta_r = 0.f, eta_i = 0.f;
+    const int nchunks = (N + CH - 1) / CH;
+    bool ok = true;
+
+    // conv weights / norm params of this lane's channels (prologue: lanes = channels)
+    constexpr int RS = R / 32, DS = D / 32;
+    const float *cwq = a.conv_w + ((size_t)0 * H + h) * R * W;
+    const float *cwk = a.conv_w + ((size_t)1 * H + h) * R * W;
+    const float *nw = a.norm_w + (size_t)h * (R + D);
+    const float *bs = a.bias + (size_t)h * (R + D);
+
+    for (int ci = 0; ci < nchunks && ok; ++ci) {
+        const int t0 = ci * CH;
+        const int L = min(CH, N - t0);
+        const uint32_t par = ci & 1;
+
+        // wait for the previous chunk's state-update MMAs (they read ZT16 / CF16)
+        if (ci > 0) {
+            ok = mbar_wait(&bar[4], par ^ 1);
+            tc_fence_after();
+        }
+        if (__syncthreads_or(!ok)) break;
+
+        // ---- S1: prologue, warp w handles positions 16w .. 16w+15 -------------
+        {
+            float qw[3][RS], kw[3][RS];  // raw rows t-3, t-2, t-1 (oldest first)
+            const int i0 = 16 * warp;
+#pragma unroll
+            for (int s = 0; s < 3; ++s) {
+                const int p = t0 + i0 - 3 + s;
+#pragma unroll
+                for (int r = 0; r < RS; ++r) {
+                    const int c = lane + 32 * r;
+                    qw[s][r] = (p >= 0 && p < N) ? __bfloat162float(gq[base_qk + (size_t)p * sqk + c]) : 0.f;
+                    kw[s][r] = (p >= 0 && p < N) ? __bfloat162float(gk[base_qk + (size_t)p * sqk + c]) : 0.f;
+                }
+            }
+            for (int ii = 0; ii < 16; ++ii) {
+                const int i = i0 + ii, t = t0 + i;
+                const bool valid = i < L;
+                float xq[RS], xk[RS], xv[DS];
+#pragma unroll
+                for (int r = 0; r < RS; ++r) {
+                    const int c = lane + 32 * r;
+                    xq[r] = valid ? __bfloat162float(gq[base_qk + (size_t)t * sqk + c]) : 0.f;
+                    xk[r] = valid ? __bfloat162float(gk[base_qk + (size_t)t * sqk + c]) : 0.f;
+                }
+#pragma unroll
+                for (int r = 0; r < DS; ++r)
+                    xv[r] = valid ? __bfloat162float(gv[base_v + (size_t)t * sv + lane + 32 * r]) : 0.f;
+                // conv + SiLU for q and k
+                float fq[RS], fk[RS], ssq = 0.f, ssk = 0.f;
+#pragma unroll
+                for (int r = 0; r < RS; ++r) {
+                    const int c = lane + 32 * r;
+                    float sq = cwq[c * W + (W - 1)] * xq[r], sk = cwk[c * W + (W - 1)] * xk[r];
+                    for (int j = 0; j < W - 1; ++j) {
+                        sq = fmaf(cwq[c * W + j], qw[3 - (W - 1) + j][r], sq);
+                        sk = fmaf(cwk[c * W + j], kw[3 - (W - 1) + j][r], sk);
+                    }
+                    fq[r] = silu(sq);
+                    fk[r] = silu(sk);
+                    ssq = fmaf(fq[r], fq[r], ssq);
+                    ssk = fmaf(fk[r], fk[r], ssk);
+                    qw[0][r] = qw[1][r]; qw[1][r] = qw[2][r]; qw[2][r] = xq[r];
+                    kw[0][r] = kw[1][r]; kw[1][r] = kw[2][r]; kw[2][r] = xk[r];
+                }
+                const float invq = 1.f / (warp_sum(ssq) + IDA_EPS_FEAT);
+                const float invk = 1.f / (warp_sum(ssk) + IDA_EPS_FEAT);
+                float msk = 0.f, msv = 0.f;
+#pragma unroll
+                for (int r = 0; r < RS; ++r) {
+                    fq[r] *= invq;
+                    fk[r] *= invk;
+                    msk = fmaf(fk[r], fk[r], msk);
+                }
+#pragma unroll
+                for (int r = 0; r < DS; ++r) msv = fmaf(xv[r], xv[r], msv);
+                const float rk = rsqrtf(warp_sum(msk) / R + IDA_EPS_RMS);
+                const float rv = rsqrtf(warp_sum(msv) / D + IDA_EPS_RMS);
+#pragma unroll
+                for (int r = 0; r < RS; ++r) {
+                    const int c = lane + 32 * r;
+                    const float kt = valid ? fmaf(fk[r] * rk, nw[c], bs[c]) : 0.f;
+                    const float xqv = valid ? fq[r] : 0.f;
+                    *reinterpret_cast<__half *>(sm + S::XQ16 + kmaj_off(i, c, 2, 128, 16 * R)) = __float2half_rn(xqv);
+                    *reinterpret_cast<float *>(sm + S::XQ32 + kmaj_off(i, c, 4, 128, 32 * R)) = to_tf32(xqv);
+                    *reinterpret_cast<__half *>(sm + S::KT16 + kmaj_off(i, c, 2, 128, 16 * R)) = __float2half_rn(kt);
+                    *reinterpret_cast<__half *>(sm + S::ZT16 + kmaj_off(c, i, 2, PADLBO, S::ZT_SBO)) =
+                        __float2half_rn(kt);
+                }
+#pragma unroll
+                for (int r = 0; r < DS; ++r) {
+                    const int jv = lane + 32 * r;
+                    const float vt = valid ? fmaf(xv[r] * rv, nw[R + jv], bs[R + jv]) : 0.f;
+                    *reinterpret_cast<__half *>(sm + S::ZT16 + kmaj_off(R + jv, i, 2, PADLBO, S::ZT_SBO)) =
+                        __float2half_rn(vt);
+                }
+            }
+        }
+        if (L < CH && tid < MP) {
+            // ragged last chunk: Coef row mp = component of B lambda^(L-1-j) for j < L, else 0
+            double pr = 1.0, pi = 0.0;
+            __half cf[CH];
+            for (int j = 0; j < CH; ++j) cf[j] = __float2half_rn(0.f);
+            for (int k = 0; k < L; ++k) {
+                double cr = b_r * pr - b_i * pi, cim = b_r * pi + b_i * pr;
+                cf[L - 1 - k] = __float2half_rn((float)(is_im ? cim : cr));
+                double nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
+                pr = nr;
+                pi = ni;
+            }
+            for (int k8 = 0; k8 < CH / 8; ++k8)
+                *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(mp, k8 * 8, 2, 128, 1024)) =
+                    *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
+            if (!is_im) laml[mm] = make_float2((float)pr, (float)pi);  // lambda^L
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- S2: G and P^T ----------------------------------------------------
+        if (tid == 0) {
+            const uint32_t idg = idesc(128, 64, 0, 0);
+            for (int s = 0; s < R / 16; ++s)
+                mma_f16_ss(tb + T::G, sdesc(sm + S::XQ16 + s * 256, 128, 16 * R),
+                           sdesc(sm + S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
+            const uint32_t idp = idesc(128, 64, 2, 2);
+            for (int s = 0; s < R / 8; ++s)
+                mma_tf32_ts(tb + T::PT, tb + T::U + 8 * s, sdesc(sm + S::XQ32 + s * 256, 128, 32 * R), idp, s > 0);
+            mma_commit(&bar[0]);
+        }
+        __syncwarp();
+        ok = mbar_wait(&bar[0], par);
+        tc_fence_after();
+        if (__syncthreads_or(!ok)) break;
+
+        // ---- S3: G' = skewed, masked G (rows i < 64) ---------------------------
+        float *scr = reinterpret_cast<float *>(sm + S::XQ32);  // [64][64], rotated by row
+        if (warp < 2) {
+            const int i = tid;
+            for (int c0 = 0; c0 < CH; c0 += 16) {
+                float v[16];
+                tmem_ld16(tb + lane_base + T::G + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) scr[i * 64 + ((c0 + j + i) & 63)] = v[j];
+            }
+        }
+        __syncthreads();
+        if (warp < 2) {
+            const int i = tid;
+            for (int k8 = 0; k8 < CH / 8; ++k8) {
+                __align__(16) __half g8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int k = k8 * 8 + e;
+                    const float g = k <= i ? scr[i * 64 + ((2 * i - k) & 63)] : 0.f;
+                    g8[e] = __float2half_rn(g);
+                }
+                *reinterpret_cast<uint4 *>(sm + S::GP16 + kmaj_off(i, k8 * 8, 2, 128, 1024)) =
+                    *reinterpret_cast<const uint4 *>(g8);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- S4: L^T = T_L . G'^T ---------------------------------------------
+        if (tid == 0) {
+            const uint32_t id = idesc(128, 64, 0, 0);
+            for (int s = 0; s < CH / 16; ++s)
+                mma_f16_ss(tb + T::LT, sdesc(sm + S::TL16 + s * 256, 128, 1024),
+                           sdesc(sm + S::GP16 + s * 256, 128, 1024), id, s > 0);
+            mma_commit(&bar[1]);
+        }
+        __syncwarp();
+        ok = mbar_wait(&bar[1], par);
+        tc_fence_after();
+        if (__syncthreads_or(!ok)) break;
+
+        // ---- S5: a, Ya (scaled fp16, with T_A rescaled to match), a' (tf32) -----
+        {
+            float ya[CH];
+            float wr = lam_r, wi = lam_i;  // lambda^(i+1)
+            float ymax = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < CH; c0 += 16) {
+                float pv[16], lv[16];
+                tmem_ld16(tb + lane_base + T::PT + c0, pv);
+                tmem_ld16(tb + lane_base + T::LT + c0, lv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int i = c0 + j;
+                    const float po = __shfl_xor_sync(0xffffffffu, pv[j], 1);
+                    const float lo = __shfl_xor_sync(0xffffffffu, lv[j], 1);
+                    const float pr = is_im ? po : pv[j], pim = is_im ? pv[j] : po;
+                    const float lr = is_im ? lo : lv[j], lim = is_im ? lv[j] : lo;
+                    // a = lambda^(i+1) P + B L
+                    const float ar = wr * pr - wi * pim + b_r * lr - b_i * lim;
+                    const float ai = wr * pim + wi * pr + b_r * lim + b_i * lr;
+                    // Ya = a B ; a' = a lambda^(i+1); operands hold (Re, -Im) per mode
+                    const float yr = ar * b_r - ai * b_i, yi = ar * b_i + ai * b_r;
+                    const float qr = ar * wr - ai * wi, qi = ar * wi + ai * wr;
+                    ya[i] = is_im ? -yi : yr;
+                    ymax = fmaxf(ymax, fabsf(ya[i]));
+                    *reinterpret_cast<float *>(sm + S::AP32 + kmaj_off(i, mp, 4, PADLBO, S::AP_SBO)) =
+                        to_tf32(is_im ? -qi : qr);
+                    const float nr = wr * lam_r - wi * lam_i, ni = wr * lam_i + wi * lam_r;
+                    wr = nr;
+                    wi = ni;
+                }
+            }
+            const int e = down_exp(ymax);
+            const float sdown = pow2i(-e), sup = pow2i(e);
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+                *reinterpret_cast<__half *>(sm + S::YA16 + kmaj_off(i, mp, 2, PADLBO, S::TY_SBO)) =
+                    __float2half_rn(ya[i] * sdown);
+            // T_A column mp = T_L row mp scaled by 2^e (exact in fp16)
+            for (int k8 = 0; k8 < CH / 8; ++k8) {
+                __align__(16) __half t8[8];
+                *reinterpret_cast<uint4 *>(t8) =
+                    *reinterpret_cast<const uint4 *>(sm + S::TL16 + kmaj_off(mp, k8 * 8, 2, 128, 1024));
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<__half *>(sm + S::TA16 + kmaj_off(k8 * 8 + u, mp, 2, PADLBO, S::TY_SBO)) =
+                        __float2half_rn(__half2float(t8[u]) * sup);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- S6: A2' = Ya . T_A^T -------------------------------------------------
+        if (tid == 0) {
+            const uint32_t id = idesc(128, 64, 0, 0);
+            for (int s = 0; s < MP / 16; ++s)
+                mma_f16_ss(tb + T::G, sdesc(sm + S::YA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO),
+                           sdesc(sm + S::TA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO), id, s > 0);
+            mma_commit(&bar[2]);
+        }
+        __syncwarp();
+        ok = mbar_wait(&bar[2], par);
+        tc_fence_after();
+        if (__syncthreads_or(!ok)) break;
+
+        // ---- S7: A2 = unskewed, masked A2' (scaled fp16 rows) ----------------------
+        if (warp < 2) {
+            const int i = tid;
+            for (int c0 = 0; c0 < CH; c0 += 16) {
+                float v[16];
+                tmem_ld16(tb + lane_base + T::G + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) scr[i * 64 + ((c0 + j + i) & 63)] = v[j];
+            }
+        }
+        __syncthreads();
+        if (warp < 2) {
+            const int i = tid;
+            float amax = 0.f;
+            for (int j = 0; j <= i; ++j) amax = fmaxf(amax, fabsf(scr[i * 64 + ((2 * i - j) & 63)]));
+            const int e = down_exp(amax);
+            const float sdown = pow2i(-e);
+            osc[i] = pow2i(e);
+            for (int j8 = 0; j8 < CH / 8; ++j8) {
+                __align__(16) __half g8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int j = j8 * 8 + u;
+                    const float g = j <= i ? scr[i * 64 + ((2 * i - j) & 63)] * sdown : 0.f;
+                    g8[u] = __float2half_rn(g);
+                }
+                *reinterpret_cast<uint4 *>(sm + S::A216 + kmaj_off(i, j8 * 8, 2, 128, 1024)) =
+                    *reinterpret_cast<const uint4 *>(g8);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- S8: O1 = Vt^T . A2^T ; O2 = Gamma^T . a'^T ---------------------------
+        if (tid == 0) {
+            const uint32_t id16 = idesc(128, 64, 0, 0);
+            const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;  // value rows R .. R+127
+            for (int s = 0; s < CH / 16; ++s)
+                mma_f16_ss(tb + T::PT, sdesc(sm + vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
+                           sdesc(sm + S::A216 + s * 256, 128, 1024), id16, s > 0);
+            const uint32_t id32 = idesc(128, 64, 2, 2);
+            for (int s = 0; s < MP / 8; ++s)
+                mma_tf32_ts(tb + T::LT, tb + T::GT + 8 * s, sdesc(sm + S::AP32 + s * 2 * PADLBO, PADLBO, S::AP_SBO),
+                            id32, s > 0);
+            mma_commit(&bar[3]);
+        }
+        __syncwarp();
+        ok = mbar_wait(&bar[3], par);
+        tc_fence_after();
+        if (__syncthreads_or(!ok)) break;
+
+        // ---- S9: outputs; scale the state by lambda^L --------------------------------
+        {
+            const int jv = tid;  // value channel lane
+            for (int c0 = 0; c0 < CH; c0 += 16) {
+                float o1[16], o2[16];
+                tmem_ld16(tb + lane_base + T::PT + c0, o1);
+                tmem_ld16(tb + lane_base + T::LT + c0, o2);
+                tmem_wait_ld();
+                if (jv < D) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int i = c0 + j;
+                        if (i < L)
+                            gout[base_v + (size_t)(t0 + i) * sv + jv] = __float2bfloat16_rn(fmaf(o1[j], osc[i], o2[j]));
+                    }
+                }
+            }
+            // eta_p <- lambda^L eta_p + B sum_{k<L} lambda^k  (Re thread of each mode)
+            if (!is_im) {
+                float sr = 0.f, si = 0.f, pr = 1.f, pi = 0.f;
+                for (int k = 0; k < L; ++k) {
+                    sr += pr;
+                    si += pi;
+                    const float nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
+                    pr = nr;
+                    pi = ni;
+                }
+                const float2 ll = laml[mm];
+                const float er = ll.x * eta_r - ll.y * eta_i + b_r * sr - b_i * si;
+                const float ei = ll.x * eta_i + ll.y * eta_r + b_r * si + b_i * sr;
+                eta_r = er;
+                eta_i = ei;
+            }
+            // U (lanes = mode planes): partner lane holds the other component
+            const float2 lm = laml[mm];
+            for (int c0 = 0; c0 < R; c0 += 16) {
+                float v[16];
+                tmem_ld16(tb + lane_base + T::U + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float o = __shfl_xor_sync(0xffffffffu, v[j], 1);
+                    const float xr = is_im ? o : v[j], xi = is_im ? v[j] : o;
+                    v[j] = is_im ? (lm.x * xi + lm.y * xr) : (lm.x * xr - lm.y * xi);
+                }
+                tmem_st16(tb + lane_base + T::U + c0, v);
+            }
+            // Gamma^T (lanes = value channels, columns = (Re, Im) per mode)
+            for (int c0 = 0; c0 < MP; c0 += 16) {
+                float v[16];
+                tmem_ld16(tb + lane_base + T::GT + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    const float2 l2 = laml[(c0 + j) >> 1];
+                    const float xr = v[j], xi = v[j + 1];
+                    v[j] = l2.x * xr - l2.y * xi;
+                    v[j + 1] = l2.x * xi + l2.y * xr;
+                }
+                tmem_st16(tb + lane_base + T::GT + c0, v);
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- S10: U += Coef . Kt ; Gamma^T += Vt^T . Coef^T ---------------------------
+        if (tid == 0) {
+            const uint32_t idu = idesc(128, R, 0, 0);
+            for (int s = 0; s < CH / 16; ++s)
+                mma_f16_ss(tb + T::U, sdesc(sm + S::CF16 + s * 256, 128, 1024),
+                           sdesc(sm + S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, 1);
+            const uint32_t idg = idesc(128, MP, 0, 0);
+            const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;
+            for (int s = 0; s < CH / 16; ++s)
+                mma_f16_ss(tb + T::GT, sdesc(sm + vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
+                           sdesc(sm + S::CF16 + s * 256, 128, 1024), idg, 1);
+            mma_commit(&bar[4]);
+        }
+        __syncwarp();
+    }
+
+    // ---- final state ------------------------------------------------------------
+    if (ok && nchunks > 0) {
+        ok = mbar_wait(&bar[4], (nchunks - 1) & 1);
+        tc_fence_after();
+    }
+    ok = !__syncthreads_or(!ok);
+    if (ok && a.final_state) {
+        float *fs = a.final_state + (size_t)unit * a.state_floats;
+        const int RD = R + D;
+        const size_t plane = (size_t)M * RD;
+        // U: thread mp writes row (is_im ? M + m : m), columns 0..R-1
+        for (int c0 = 0; c0 < R; c0 += 16) {
+            float v[16];
+            tmem_ld16(tb + lane_base + T::U + c0, v);
+            tmem_wait_ld();
+            float *row = fs + (is_im ? plane : 0) + (size_t)mm * RD + c0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) row[j] = v[j];
+        }
+        // Gamma^T: thread jv writes column R + jv of every row
+        for (int c0 = 0; c0 < MP; c0 += 16) {
+            float v[16];
+            tmem_ld16(tb + lane_base + T::GT + c0, v);
+            tmem_wait_ld();
+            if (tid < D) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int pl = c0 + j, m = pl >> 1;
+                    fs[((pl & 1) ? plane : 0) + (size_t)m * RD + R + tid] = v[j];
+                }
+            }
+        }
+        if (!is_im) {
+            fs[2 * plane + mm] = eta_r;
+            fs[2 * plane + M + mm] = eta_i;
+        }
+        float *tq = fs + 2 * plane + 2 * M;
+        float *tk = tq + (size_t)(W - 1) * R;
+        for (int x = tid; x < (W - 1) * R; x += NTH) {
+            const int r = x / R, c = x % R;
+            const int p = N - (W - 1) + r;
+            tq[x] = p >= 0 ? __bfloat162float(gq[base_qk + (size_t)p * sqk + c]) : 0.f;
+            tk[x] = p >= 0 ? __bfloat162float(gk[base_qk + (size_t)p * sqk + c]) : 0.f;
+        }
+        const size_t used = 2 * plane + 2 * M + 2 * (size_t)(W - 1) * R;
+        for (size_t x = used + tid; x < a.state_floats; x += NTH) fs[x] = 0.f;
+    }
+    if (!ok && tid == 0) report_error(a.err, kErrWaitTimeout);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+template <int R, int D>
+static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st) {
+    using S = ChunkSmem<R, D>;
+    auto kern = chunk_prefill_kernel<R, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)(a.B * a.H), NTH, S::TOTAL, st>>>(a);
+    return cudaGetLastError();
+}
+
+// Takes bf16 prefill with M = 64 modes and R, d in {64, 128}; the eta readout
+// and every other shape go to the sequential kernel.
+ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int, std::string &why, bool *taken) {
     *taken = false;
+    if (a.dtype != IDA_BF16 || a.M != 64 || (a.flags & IDA_READOUT_ETA) || a.W > 4) return IDA_OK;
+    if (!((a.R == 64 || a.R == 128) && (a.d == 64 || a.d == 128))) return IDA_OK;
+    *taken = true;
+    cudaError_t e;
+    if (a.R == 128 && a.d == 128)
+        e = launch_chunk_rd<128, 128>(a, st);
+    else if (a.R == 64 && a.d == 64)
+        e = launch_chunk_rd<64, 64>(a, st);
+    else if (a.R == 128 && a.d == 64)
+        e = launch_chunk_rd<128, 64>(a, st);
+    else
+        e = launch_chunk_rd<64, 128>(a, st);
+    if (e != cudaSuccess) {
+        why = std::string("chunked prefill launch: ") + cudaGetErrorString(e);
+        return IDA_ERR_CUDA;
+    }
     return IDA_OK;
 }
 

@@ -67,6 +67,12 @@ EDGE = [
     (1, 33, 1, 256, 256, 128, 4, "f32"),
     (2, 131, 2, 128, 128, 64, 4, "bf16"),
     (1, 65, 3, 64, 64, 33, 4, "bf16"),
+    # shapes the chunked tensor-core kernel takes (bf16, M = 64, R, d in {64, 128})
+    (1, 1, 2, 64, 64, 64, 4, "bf16"),
+    (3, 70, 2, 128, 64, 64, 3, "bf16"),
+    (1, 200, 2, 64, 128, 64, 2, "bf16"),
+    (2, 64, 1, 64, 64, 64, 1, "bf16"),
+    (1, 257, 3, 128, 128, 64, 4, "bf16"),
 ]
 
 
@@ -80,7 +86,7 @@ def test_edge_shapes(shape, path):
         ref = orc.forward(q, k, v, p, flags=eta, final_state=True)
         _check(to_np(out), ref["out"], dt)
         got_st = unpadded_state(to_np(fs), d, R, M, W)
-        assert rel_l2(got_st, ref["final_state"]) <= (F32_REL_L2 if dt == "f32" else 1e-4)
+        assert rel_l2(got_st, ref["final_state"]) <= (F32_REL_L2 if dt == "f32" else BF16_REL_L2)
 
 
 def test_zero_length_gives_zero_state():
@@ -117,7 +123,7 @@ def _sampled(w, units, flags, final_state=False, path=0):
         errs.append(rel_l2(got[b, :, h], ref["out"][b, :, h]))
         if final_state:
             st = unpadded_state(to_np(fs[b, h]), w.d, w.R, w.M, w.W)
-            assert rel_l2(st, ref["final_state"][b, h]) <= 1e-4
+            assert rel_l2(st, ref["final_state"][b, h]) <= BF16_REL_L2
     return errs, ref
 
 
