@@ -35,11 +35,20 @@
 // stored as fp16 with a power-of-two scale per column / row, undone exactly
 // in the matching table or epilogue.
 //
-// One CTA of 128 threads per (b,h) unit; thread t owns TMEM lane t; thread 0
-// issues the MMAs.  Every wait on an MMA completion is bounded; on timeout
-// the kernel records kErrWaitTimeout, stops, frees its TMEM and returns.
+// One CTA of 256 threads per (b,h) unit.  Warp w reaches TMEM lanes
+// 32*(w%4) .. +31, so warps w and w+4 share a lane quarter and split the
+// columns (or positions) of every TMEM-side stage; thread 0 issues the MMAs.
+// The raw q, k, v rows of a chunk (with the W-1 = 3 row conv halo) arrive by
+// TMA one chunk ahead, into shared memory that is dead between the output
+// MMAs and the next a / Ya stage; out-of-range rows (before position 0 or
+// past N) are zero-filled by the copy itself.  Every wait (MMA completion or
+// TMA arrival) is bounded; on timeout the kernel records kErrWaitTimeout,
+// stops issuing, waits (bounded) for its own copy in flight, frees its TMEM
+// and returns.
+#include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
 #include <string>
 
 #include "ida_common.cuh"
@@ -49,20 +58,23 @@ namespace ida {
 
 using namespace tc;
 
-constexpr int CH = 64;    // positions per chunk
-constexpr int NTH = 128;  // threads per CTA
-constexpr int MP = 128;   // mode planes (2M, M = 64)
+constexpr int CH = 64;       // positions per chunk
+constexpr int HALO = 3;      // conv halo rows staged before a chunk (W <= 4)
+constexpr int NTH = 256;     // threads per CTA
+constexpr int MP = 128;      // mode planes (2M, M = 64)
 constexpr int PADLBO = 144;  // core-matrix stride along K for column-wise (transposed) writers
+
+__host__ __device__ constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
 
 template <int R, int D>
 struct ChunkSmem {
-    // All operands are K-major, no-swizzle core-matrix layouts (8 rows x 16 B).
+    // All MMA operands are K-major, no-swizzle core-matrix layouts (8 rows x 16 B).
     static constexpr int XQ16 = 0;                               // [64][R] f16   LBO 128, SBO 16R
     static constexpr int KT16 = XQ16 + CH * R * 2;               // [64][R] f16   (follows XQ16: A rows 64..127)
     static constexpr int XQ32 = KT16 + CH * R * 2;               // [64][R] tf32  LBO 128, SBO 32R; skew scratch
     static constexpr int ZT16 = XQ32 + CH * R * 4;               // [R+D][64] f16 LBO 144, SBO 1152
     static constexpr int ZT_SBO = 8 * PADLBO;
-    static constexpr int GP16 = ZT16 + (R + D) / 8 * ZT_SBO;     // [64][64] f16  LBO 128, SBO 1024
+    static constexpr int GP16 = ZT16 + (R + D) / 8 * ZT_SBO;     // [64][64] f16  LBO 128, SBO 1024; S5 scratch
     static constexpr int A216 = GP16 + CH * CH * 2;              // [64][64] f16
     static constexpr int TL16 = A216 + CH * CH * 2;              // [128][64] f16 LBO 128, SBO 1024
     static constexpr int CF16 = TL16 + MP * CH * 2;              // [128][64] f16
@@ -72,22 +84,32 @@ struct ChunkSmem {
     static constexpr int AP32 = YA16 + 8 * TY_SBO;               // [64][128] tf32 LBO 144, SBO 4608
     static constexpr int AP_SBO = 32 * PADLBO;
     static constexpr int MISC = AP32 + 8 * AP_SBO;
-    static constexpr int BARS = MISC;                            // 5 mbarriers
-    static constexpr int TSLOT = BARS + 64;                      // TMEM base address
-    static constexpr int FLAG = TSLOT + 16;                      // abort flag
-    static constexpr int OSC = FLAG + 16;                        // [64] float: row scales of A2
+    // raw bf16 rows of the next chunk, staged over YA16 / AP32 (dead while they land)
+    static constexpr int RAWQ_BYTES = align1k((CH + HALO) * R * 2);
+    static constexpr int RAWQ = YA16;                            // [67][R] bf16, row r = position t0-3+r
+    static constexpr int RAWK = RAWQ + RAWQ_BYTES;               // [67][R] bf16
+    static constexpr int RAWV = RAWK + RAWQ_BYTES;               // [64][D] bf16
+    static_assert(YA16 % 1024 == 0 && RAWV + CH * D * 2 <= MISC, "raw staging must fit over YA16/AP32");
+    static constexpr int BARS = MISC;                            // 6 mbarriers
+    static constexpr int TSLOT = BARS + 64;
+    static constexpr int OSC = TSLOT + 16;                       // [64] float: row scales of A2
     static constexpr int LAML = OSC + CH * 4;                    // [64] float2: lambda^L per mode
-    static constexpr int TOTAL = LAML + 64 * 8;
+    static constexpr int CWQ = LAML + 64 * 8;                    // [R][4] float conv taps (q)
+    static constexpr int CWK = CWQ + R * 16;                     // [R][4] float conv taps (k)
+    static constexpr int NWS = CWK + R * 16;                     // [R+D] float RMSNorm weights
+    static constexpr int BSS = NWS + (R + D) * 4;                // [R+D] float RMSNorm biases
+    static constexpr int TOTAL = BSS + (R + D) * 4;
+    static_assert(TOTAL <= 227 * 1024, "shared memory budget");
 };
 
 // TMEM column map (512 columns allocated).
 template <int R>
 struct ChunkTmem {
-    static constexpr uint32_t U = 0;        // [2M lanes][R]
-    static constexpr uint32_t GT = R;       // [value lanes][2M]
-    static constexpr uint32_t G = 256;      // [64 lanes][64], later A2'
-    static constexpr uint32_t PT = 320;     // [2M lanes][64], later O1
-    static constexpr uint32_t LT = 384;     // [2M lanes][64], later O2
+    static constexpr uint32_t U = 0;     // [2M lanes][R]
+    static constexpr uint32_t GT = R;    // [value lanes][2M]
+    static constexpr uint32_t G = 256;   // [64 lanes][64], later A2'
+    static constexpr uint32_t PT = 320;  // [2M lanes][64], later O1
+    static constexpr uint32_t LT = 384;  // [2M lanes][64], later O2
 };
 
 // byte offset of element (row, k) in a K-major no-swizzle operand
@@ -106,18 +128,44 @@ __device__ __forceinline__ int down_exp(float x) {
     return e > 15 ? 15 : e;
 }
 
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
+__device__ __forceinline__ void unpack_bf16x8(uint4 u, float x[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 pack_f16x8(const float x[8]) {
+    __align__(16) __half h[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) h[e] = __float2half_rn(x[e]);
+    return *reinterpret_cast<const uint4 *>(h);
+}
+
 template <int R, int D>
-__global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(NTH, 1)
+    chunk_prefill_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
     using S = ChunkSmem<R, D>;
     using T = ChunkTmem<R>;
     extern __shared__ __align__(1024) unsigned char sm[];
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S::BARS);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S::BARS);  // 0..4 MMA stages, 5 TMA
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S::TSLOT);
-    int *flag = reinterpret_cast<int *>(sm + S::FLAG);
     float *osc = reinterpret_cast<float *>(sm + S::OSC);
     float2 *laml = reinterpret_cast<float2 *>(sm + S::LAML);
+    float *cwq = reinterpret_cast<float *>(sm + S::CWQ);
+    float *cwk = reinterpret_cast<float *>(sm + S::CWK);
+    float *nws = reinterpret_cast<float *>(sm + S::NWS);
+    float *bss = reinterpret_cast<float *>(sm + S::BSS);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hsel = warp >> 2;        // TMEM lane quarter, column / position half
+    const int tl = 32 * q4 + lane;                    // my TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const int H = a.H, N = a.N, M = 64, W = a.W;
     const int unit = blockIdx.x, b = unit / H, h = unit % H;
     const size_t sqk = (size_t)H * R, sv = (size_t)H * D;
@@ -125,178 +173,232 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
     const size_t base_v = ((size_t)b * N * H + h) * D;
     const __nv_bfloat16 *gq = reinterpret_cast<const __nv_bfloat16 *>(a.q);
     const __nv_bfloat16 *gk = reinterpret_cast<const __nv_bfloat16 *>(a.k);
-    const __nv_bfloat16 *gv = reinterpret_cast<const __nv_bfloat16 *>(a.v);
     __nv_bfloat16 *gout = reinterpret_cast<__nv_bfloat16 *>(a.out);
+    const uint32_t raw_bytes = 2u * (CH + HALO) * R * 2 + (uint32_t)CH * D * 2;
 
-    // my mode plane (thread mp = tid): m = tid / 2, Re (even) / Im (odd)
-    const int mp = tid, mm = tid >> 1, is_im = tid & 1;
+    // my mode plane in the lane-side stages: plane tl = 2m + (0: Re, 1: Im)
+    const int mm = tl >> 1, is_im = tl & 1;
     const float lam_r = a.lambda[((size_t)h * M + mm) * 2], lam_i = a.lambda[((size_t)h * M + mm) * 2 + 1];
     const float b_r = a.Bvec[((size_t)h * M + mm) * 2], b_i = a.Bvec[((size_t)h * M + mm) * 2 + 1];
+    float l33r = lam_r, l33i = lam_i;  // lambda^(32*hsel+1): first decay of my position half
 
-    // ---- set-up: barriers, TMEM, constant tables ----------------------------
+    // TMA destinations need 1 KB-aligned shared memory; refuse rather than fault
+    if ((smem_u32(sm) & 1023u) != 0u) {
+        if (tid == 0) report_error(a.err, kErrShape);
+        return;
+    }
+
+    // ---- set-up: barriers, TMEM, per-head constants -----------------------------
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
-        *flag = 0;
+        for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
     }
     if (warp == 0) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
-    {
-        // T_L row mp: component of lambda_m^k, k = 0..63; Coef row mp: component of
-        // B_m lambda_m^(C-1-j).  Powers in fp64 to keep the tables exact to fp16.
+    for (int x = tid; x < R * 4; x += NTH) {
+        const int c = x >> 2, j = x & 3;
+        cwq[x] = j < W ? a.conv_w[((size_t)(0 * H + h) * R + c) * W + j] : 0.f;
+        cwk[x] = j < W ? a.conv_w[((size_t)(1 * H + h) * R + c) * W + j] : 0.f;
+    }
+    for (int x = tid; x < R + D; x += NTH) {
+        nws[x] = a.norm_w[(size_t)h * (R + D) + x];
+        bss[x] = a.bias[(size_t)h * (R + D) + x];
+    }
+    if (hsel == 0) {
+        // T_L row (plane tl): component of lambda_m^k, k = 0..63; Coef row: component
+        // of B_m lambda_m^(C-1-j); T_A column tl = T_L row (unscaled).  Powers in fp64.
         double pr = 1.0, pi = 0.0;
-        __half tl[CH], cf[CH];
+        __align__(16) __half tl16[CH], cf[CH];
         for (int k = 0; k < CH; ++k) {
-            tl[k] = __float2half_rn((float)(is_im ? pi : pr));
-            double cr = b_r * pr - b_i * pi, ci = b_r * pi + b_i * pr;  // B lambda^k
+            tl16[k] = __float2half_rn((float)(is_im ? pi : pr));
+            const double cr = b_r * pr - b_i * pi, ci = b_r * pi + b_i * pr;
             cf[CH - 1 - k] = __float2half_rn((float)(is_im ? ci : cr));
-            double nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
+            const double nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
             pr = nr;
             pi = ni;
         }
         if (!is_im) laml[mm] = make_float2((float)pr, (float)pi);  // lambda^C
+#pragma unroll
         for (int k8 = 0; k8 < CH / 8; ++k8) {
-            *reinterpret_cast<uint4 *>(sm + S::TL16 + kmaj_off(mp, k8 * 8, 2, 128, 1024)) =
-                *reinterpret_cast<const uint4 *>(&tl[k8 * 8]);
-            *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(mp, k8 * 8, 2, 128, 1024)) =
+            *reinterpret_cast<uint4 *>(sm + S::TL16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
+                *reinterpret_cast<const uint4 *>(&tl16[k8 * 8]);
+            *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
                 *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
         }
+        for (int k = 0; k < CH; ++k)
+            *reinterpret_cast<__half *>(sm + S::TA16 + kmaj_off(k, tl, 2, PADLBO, S::TY_SBO)) = tl16[k];
+    } else {
+        double pr = lam_r, pi = lam_i;
+        for (int k = 1; k < 33; ++k) {
+            const double nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
+            pr = nr;
+            pi = ni;
+        }
+        l33r = (float)pr;
+        l33i = (float)pi;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *tslot;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     {
-        // zero state: U (cols [0,R)) and Gamma^T (cols [R, R+128)) in every lane
+        // zero state: U (cols [0,R)) and Gamma^T (cols [R, R+128)), split by column half
         float z[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[i] = 0.f;
-        for (int c0 = 0; c0 < R + MP; c0 += 16) tmem_st16(tb + lane_base + c0, z);
+        for (int c0 = hsel * 16; c0 < R + MP; c0 += 32) tmem_st16(tb + lane_base + c0, z);
         tmem_wait_st();
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[5], raw_bytes);
+        tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, -HALO, b, &bar[5]);
+        tma_load_4d(sm + S::RAWK, &tm_k, 0, h, -HALO, b, &bar[5]);
+        tma_load_4d(sm + S::RAWV, &tm_v, 0, h, 0, b, &bar[5]);
+    }
 
-    // eta_p (for the final state): complex per mode, kept by the Re thread
-    float eta_r = 0.f, eta_i = 0.f;
+    float eta_r = 0.f, eta_i = 0.f;  // eta of my mode (kept by hsel == 0, Re thread)
+    int ya_exp = 0;                  // scale exponent of my T_A column currently stored
     const int nchunks = (N + CH - 1) / CH;
     bool ok = true;
+    int tma_pending = 1;  // TMA copies issued and not yet waited for
+    int ci = 0;
 
-    // conv weights / norm params of this lane's channels (prologue: lanes = channels)
-    constexpr int RS = R / 32, DS = D / 32;
-    const float *cwq = a.conv_w + ((size_t)0 * H + h) * R * W;
-    const float *cwk = a.conv_w + ((size_t)1 * H + h) * R * W;
-    const float *nw = a.norm_w + (size_t)h * (R + D);
-    const float *bs = a.bias + (size_t)h * (R + D);
-
-    for (int ci = 0; ci < nchunks && ok; ++ci) {
+    for (; ci < nchunks; ++ci) {
         const int t0 = ci * CH;
         const int L = min(CH, N - t0);
         const uint32_t par = ci & 1;
 
-        // wait for the previous chunk's state-update MMAs (they read ZT16 / CF16)
-        if (ci > 0) {
-            ok = mbar_wait(&bar[4], par ^ 1);
-            tc_fence_after();
-        }
+        // previous chunk's state update (reads ZT16 / CF16), then this chunk's raw rows
+        if (ci > 0) ok = mbar_wait(&bar[4], par ^ 1);
+        if (ok) ok = mbar_wait(&bar[5], par);
+        if (ok) tma_pending = 0;
+        tc_fence_after();
         if (__syncthreads_or(!ok)) break;
 
-        // ---- S1: prologue, warp w handles positions 16w .. 16w+15 -------------
+        // ---- S1: prologue, thread = (position i, quarter p) --------------------
         {
-            float qw[3][RS], kw[3][RS];  // raw rows t-3, t-2, t-1 (oldest first)
-            const int i0 = 16 * warp;
+            const int i = tid >> 2, p = tid & 3;
+            const bool valid = i < L;
+            constexpr int NGQ = R / 32, NGV = D / 32;
+            float fk[NGQ][8];
+            float ss[2] = {0.f, 0.f};
 #pragma unroll
-            for (int s = 0; s < 3; ++s) {
-                const int p = t0 + i0 - 3 + s;
+            for (int which = 0; which < 2; ++which) {
+                const unsigned char *raw = sm + (which == 0 ? S::RAWQ : S::RAWK);
+                const float *cw = which == 0 ? cwq : cwk;
+                float f[NGQ][8];
+                float acc = 0.f;
 #pragma unroll
-                for (int r = 0; r < RS; ++r) {
-                    const int c = lane + 32 * r;
-                    qw[s][r] = (p >= 0 && p < N) ? __bfloat162float(gq[base_qk + (size_t)p * sqk + c]) : 0.f;
-                    kw[s][r] = (p >= 0 && p < N) ? __bfloat162float(gk[base_qk + (size_t)p * sqk + c]) : 0.f;
+                for (int gg = 0; gg < NGQ; ++gg) {
+                    const int c0 = 8 * (4 * gg + p);
+                    float s8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s8[e] = 0.f;
+                    for (int j = 0; j < W; ++j) {
+                        const int row = i + HALO + 1 - W + j;
+                        float x8[8];
+                        unpack_bf16x8(*reinterpret_cast<const uint4 *>(raw + ((size_t)row * R + c0) * 2), x8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) s8[e] = fmaf(cw[(c0 + e) * 4 + j], x8[e], s8[e]);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        f[gg][e] = silu_fast(s8[e]);
+                        acc = fmaf(f[gg][e], f[gg][e], acc);
+                    }
+                }
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                const float inv = 1.f / (acc + IDA_EPS_FEAT);
+                if (which == 0) {
+#pragma unroll
+                    for (int gg = 0; gg < NGQ; ++gg) {
+                        const int c0 = 8 * (4 * gg + p);
+                        float x8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x8[e] = valid ? f[gg][e] * inv : 0.f;
+                        *reinterpret_cast<uint4 *>(sm + S::XQ16 + kmaj_off(i, c0, 2, 128, 16 * R)) = pack_f16x8(x8);
+                        uint4 t0v, t1v;
+                        t0v.x = __float_as_uint(to_tf32(x8[0])); t0v.y = __float_as_uint(to_tf32(x8[1]));
+                        t0v.z = __float_as_uint(to_tf32(x8[2])); t0v.w = __float_as_uint(to_tf32(x8[3]));
+                        t1v.x = __float_as_uint(to_tf32(x8[4])); t1v.y = __float_as_uint(to_tf32(x8[5]));
+                        t1v.z = __float_as_uint(to_tf32(x8[6])); t1v.w = __float_as_uint(to_tf32(x8[7]));
+                        *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0, 4, 128, 32 * R)) = t0v;
+                        *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0 + 4, 4, 128, 32 * R)) = t1v;
+                    }
+                } else {
+#pragma unroll
+                    for (int gg = 0; gg < NGQ; ++gg)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            fk[gg][e] = f[gg][e] * inv;
+                            ss[1] = fmaf(fk[gg][e], fk[gg][e], ss[1]);
+                        }
                 }
             }
-            for (int ii = 0; ii < 16; ++ii) {
-                const int i = i0 + ii, t = t0 + i;
-                const bool valid = i < L;
-                float xq[RS], xk[RS], xv[DS];
+            float msk = ss[1];
+            msk += __shfl_xor_sync(0xffffffffu, msk, 1);
+            msk += __shfl_xor_sync(0xffffffffu, msk, 2);
+            const float rk = rsqrtf(msk / R + IDA_EPS_RMS);
 #pragma unroll
-                for (int r = 0; r < RS; ++r) {
-                    const int c = lane + 32 * r;
-                    xq[r] = valid ? __bfloat162float(gq[base_qk + (size_t)t * sqk + c]) : 0.f;
-                    xk[r] = valid ? __bfloat162float(gk[base_qk + (size_t)t * sqk + c]) : 0.f;
-                }
+            for (int gg = 0; gg < NGQ; ++gg) {
+                const int c0 = 8 * (4 * gg + p);
+                float x8[8];
 #pragma unroll
-                for (int r = 0; r < DS; ++r)
-                    xv[r] = valid ? __bfloat162float(gv[base_v + (size_t)t * sv + lane + 32 * r]) : 0.f;
-                // conv + SiLU for q and k
-                float fq[RS], fk[RS], ssq = 0.f, ssk = 0.f;
+                for (int e = 0; e < 8; ++e) x8[e] = valid ? fmaf(fk[gg][e] * rk, nws[c0 + e], bss[c0 + e]) : 0.f;
+                *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) = pack_f16x8(x8);
 #pragma unroll
-                for (int r = 0; r < RS; ++r) {
-                    const int c = lane + 32 * r;
-                    float sq = cwq[c * W + (W - 1)] * xq[r], sk = cwk[c * W + (W - 1)] * xk[r];
-                    for (int j = 0; j < W - 1; ++j) {
-                        sq = fmaf(cwq[c * W + j], qw[3 - (W - 1) + j][r], sq);
-                        sk = fmaf(cwk[c * W + j], kw[3 - (W - 1) + j][r], sk);
-                    }
-                    fq[r] = silu(sq);
-                    fk[r] = silu(sk);
-                    ssq = fmaf(fq[r], fq[r], ssq);
-                    ssk = fmaf(fk[r], fk[r], ssk);
-                    qw[0][r] = qw[1][r]; qw[1][r] = qw[2][r]; qw[2][r] = xq[r];
-                    kw[0][r] = kw[1][r]; kw[1][r] = kw[2][r]; kw[2][r] = xk[r];
-                }
-                const float invq = 1.f / (warp_sum(ssq) + IDA_EPS_FEAT);
-                const float invk = 1.f / (warp_sum(ssk) + IDA_EPS_FEAT);
-                float msk = 0.f, msv = 0.f;
+                for (int e = 0; e < 8; ++e)
+                    *reinterpret_cast<__half *>(sm + S::ZT16 + kmaj_off(c0 + e, i, 2, PADLBO, S::ZT_SBO)) =
+                        __float2half_rn(x8[e]);
+            }
+            float xv[NGV][8];
+            float msv = 0.f;
 #pragma unroll
-                for (int r = 0; r < RS; ++r) {
-                    fq[r] *= invq;
-                    fk[r] *= invk;
-                    msk = fmaf(fk[r], fk[r], msk);
-                }
+            for (int gg = 0; gg < NGV; ++gg) {
+                const int j0 = 8 * (4 * gg + p);
+                unpack_bf16x8(*reinterpret_cast<const uint4 *>(sm + S::RAWV + ((size_t)i * D + j0) * 2), xv[gg]);
 #pragma unroll
-                for (int r = 0; r < DS; ++r) msv = fmaf(xv[r], xv[r], msv);
-                const float rk = rsqrtf(warp_sum(msk) / R + IDA_EPS_RMS);
-                const float rv = rsqrtf(warp_sum(msv) / D + IDA_EPS_RMS);
+                for (int e = 0; e < 8; ++e) msv = fmaf(xv[gg][e], xv[gg][e], msv);
+            }
+            msv += __shfl_xor_sync(0xffffffffu, msv, 1);
+            msv += __shfl_xor_sync(0xffffffffu, msv, 2);
+            const float rv = rsqrtf(msv / D + IDA_EPS_RMS);
 #pragma unroll
-                for (int r = 0; r < RS; ++r) {
-                    const int c = lane + 32 * r;
-                    const float kt = valid ? fmaf(fk[r] * rk, nw[c], bs[c]) : 0.f;
-                    const float xqv = valid ? fq[r] : 0.f;
-                    *reinterpret_cast<__half *>(sm + S::XQ16 + kmaj_off(i, c, 2, 128, 16 * R)) = __float2half_rn(xqv);
-                    *reinterpret_cast<float *>(sm + S::XQ32 + kmaj_off(i, c, 4, 128, 32 * R)) = to_tf32(xqv);
-                    *reinterpret_cast<__half *>(sm + S::KT16 + kmaj_off(i, c, 2, 128, 16 * R)) = __float2half_rn(kt);
-                    *reinterpret_cast<__half *>(sm + S::ZT16 + kmaj_off(c, i, 2, PADLBO, S::ZT_SBO)) =
-                        __float2half_rn(kt);
-                }
+            for (int gg = 0; gg < NGV; ++gg) {
+                const int j0 = 8 * (4 * gg + p);
 #pragma unroll
-                for (int r = 0; r < DS; ++r) {
-                    const int jv = lane + 32 * r;
-                    const float vt = valid ? fmaf(xv[r] * rv, nw[R + jv], bs[R + jv]) : 0.f;
-                    *reinterpret_cast<__half *>(sm + S::ZT16 + kmaj_off(R + jv, i, 2, PADLBO, S::ZT_SBO)) =
+                for (int e = 0; e < 8; ++e) {
+                    const float vt = valid ? fmaf(xv[gg][e] * rv, nws[R + j0 + e], bss[R + j0 + e]) : 0.f;
+                    *reinterpret_cast<__half *>(sm + S::ZT16 + kmaj_off(R + j0 + e, i, 2, PADLBO, S::ZT_SBO)) =
                         __float2half_rn(vt);
                 }
             }
         }
-        if (L < CH && tid < MP) {
-            // ragged last chunk: Coef row mp = component of B lambda^(L-1-j) for j < L, else 0
+        if (L < CH && hsel == 0) {
+            // ragged last chunk: Coef row = component of B lambda^(L-1-j) for j < L, else 0
             double pr = 1.0, pi = 0.0;
-            __half cf[CH];
+            __align__(16) __half cf[CH];
             for (int j = 0; j < CH; ++j) cf[j] = __float2half_rn(0.f);
             for (int k = 0; k < L; ++k) {
-                double cr = b_r * pr - b_i * pi, cim = b_r * pi + b_i * pr;
+                const double cr = b_r * pr - b_i * pi, cim = b_r * pi + b_i * pr;
                 cf[L - 1 - k] = __float2half_rn((float)(is_im ? cim : cr));
-                double nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
+                const double nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
                 pr = nr;
                 pi = ni;
             }
+#pragma unroll
             for (int k8 = 0; k8 < CH / 8; ++k8)
-                *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(mp, k8 * 8, 2, 128, 1024)) =
+                *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
                     *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
             if (!is_im) laml[mm] = make_float2((float)pr, (float)pi);  // lambda^L
         }
@@ -305,13 +407,15 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         __syncthreads();
         tc_fence_after();
 
-        // ---- S2: G and P^T ----------------------------------------------------
+        // ---- S2: G and P^T ------------------------------------------------------
         if (tid == 0) {
             const uint32_t idg = idesc(128, 64, 0, 0);
+#pragma unroll
             for (int s = 0; s < R / 16; ++s)
                 mma_f16_ss(tb + T::G, sdesc(sm + S::XQ16 + s * 256, 128, 16 * R),
                            sdesc(sm + S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
             const uint32_t idp = idesc(128, 64, 2, 2);
+#pragma unroll
             for (int s = 0; s < R / 8; ++s)
                 mma_tf32_ts(tb + T::PT, tb + T::U + 8 * s, sdesc(sm + S::XQ32 + s * 256, 128, 32 * R), idp, s > 0);
             mma_commit(&bar[0]);
@@ -321,11 +425,12 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
 
-        // ---- S3: G' = skewed, masked G (rows i < 64) ---------------------------
-        float *scr = reinterpret_cast<float *>(sm + S::XQ32);  // [64][64], rotated by row
-        if (warp < 2) {
-            const int i = tid;
-            for (int c0 = 0; c0 < CH; c0 += 16) {
+        // ---- S3: G' = skewed, masked G -----------------------------------------------
+        float *scr = reinterpret_cast<float *>(sm + S::XQ32);  // [64][64] rotated by row; XQ32 is consumed
+        if (q4 < 2) {
+            const int i = tl;
+#pragma unroll
+            for (int c0 = 32 * hsel; c0 < 32 * hsel + 32; c0 += 16) {
                 float v[16];
                 tmem_ld16(tb + lane_base + T::G + c0, v);
                 tmem_wait_ld();
@@ -334,18 +439,17 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
             }
         }
         __syncthreads();
-        if (warp < 2) {
-            const int i = tid;
-            for (int k8 = 0; k8 < CH / 8; ++k8) {
-                __align__(16) __half g8[8];
+        {
+            const int i = tid >> 2, p = tid & 3;
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {
+                float g8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int k = k8 * 8 + e;
-                    const float g = k <= i ? scr[i * 64 + ((2 * i - k) & 63)] : 0.f;
-                    g8[e] = __float2half_rn(g);
+                    const int k = 16 * p + 8 * h8 + e;
+                    g8[e] = k <= i ? scr[i * 64 + ((2 * i - k) & 63)] : 0.f;
                 }
-                *reinterpret_cast<uint4 *>(sm + S::GP16 + kmaj_off(i, k8 * 8, 2, 128, 1024)) =
-                    *reinterpret_cast<const uint4 *>(g8);
+                *reinterpret_cast<uint4 *>(sm + S::GP16 + kmaj_off(i, 16 * p + 8 * h8, 2, 128, 1024)) = pack_f16x8(g8);
             }
         }
         fence_proxy_async_smem();
@@ -353,9 +457,10 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         __syncthreads();
         tc_fence_after();
 
-        // ---- S4: L^T = T_L . G'^T ---------------------------------------------
+        // ---- S4: L^T = T_L . G'^T -----------------------------------------------------
         if (tid == 0) {
             const uint32_t id = idesc(128, 64, 0, 0);
+#pragma unroll
             for (int s = 0; s < CH / 16; ++s)
                 mma_f16_ss(tb + T::LT, sdesc(sm + S::TL16 + s * 256, 128, 1024),
                            sdesc(sm + S::GP16 + s * 256, 128, 1024), id, s > 0);
@@ -366,13 +471,19 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
 
-        // ---- S5: a, Ya (scaled fp16, with T_A rescaled to match), a' (tf32) -----
+        // ---- S5: a, Ya (fp16, column-scaled), a' (tf32); plane tl, positions of my half
         {
-            float ya[CH];
-            float wr = lam_r, wi = lam_i;  // lambda^(i+1)
+            float *ymx = reinterpret_cast<float *>(sm + S::GP16);  // [2][128]; GP16 is consumed
+            float ya[32];
+            float wr = l33r, wi = l33i;  // lambda^(i+1)
+            if (hsel == 0) {
+                wr = lam_r;
+                wi = lam_i;
+            }
             float ymax = 0.f;
 #pragma unroll
-            for (int c0 = 0; c0 < CH; c0 += 16) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = 32 * hsel + 16 * cc;
                 float pv[16], lv[16];
                 tmem_ld16(tb + lane_base + T::PT + c0, pv);
                 tmem_ld16(tb + lane_base + T::LT + c0, lv);
@@ -390,30 +501,38 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
                     // Ya = a B ; a' = a lambda^(i+1); operands hold (Re, -Im) per mode
                     const float yr = ar * b_r - ai * b_i, yi = ar * b_i + ai * b_r;
                     const float qr = ar * wr - ai * wi, qi = ar * wi + ai * wr;
-                    ya[i] = is_im ? -yi : yr;
-                    ymax = fmaxf(ymax, fabsf(ya[i]));
-                    *reinterpret_cast<float *>(sm + S::AP32 + kmaj_off(i, mp, 4, PADLBO, S::AP_SBO)) =
+                    ya[16 * cc + j] = is_im ? -yi : yr;
+                    ymax = fmaxf(ymax, fabsf(ya[16 * cc + j]));
+                    *reinterpret_cast<float *>(sm + S::AP32 + kmaj_off(i, tl, 4, PADLBO, S::AP_SBO)) =
                         to_tf32(is_im ? -qi : qr);
                     const float nr = wr * lam_r - wi * lam_i, ni = wr * lam_i + wi * lam_r;
                     wr = nr;
                     wi = ni;
                 }
             }
-            const int e = down_exp(ymax);
-            const float sdown = pow2i(-e), sup = pow2i(e);
+            ymx[hsel * 128 + tl] = ymax;
+            __syncthreads();
+            const int e = down_exp(fmaxf(ymx[tl], ymx[128 + tl]));
+            const float sdown = pow2i(-e);
 #pragma unroll
-            for (int i = 0; i < CH; ++i)
-                *reinterpret_cast<__half *>(sm + S::YA16 + kmaj_off(i, mp, 2, PADLBO, S::TY_SBO)) =
-                    __float2half_rn(ya[i] * sdown);
-            // T_A column mp = T_L row mp scaled by 2^e (exact in fp16)
-            for (int k8 = 0; k8 < CH / 8; ++k8) {
-                __align__(16) __half t8[8];
-                *reinterpret_cast<uint4 *>(t8) =
-                    *reinterpret_cast<const uint4 *>(sm + S::TL16 + kmaj_off(mp, k8 * 8, 2, 128, 1024));
+            for (int j = 0; j < 32; ++j)
+                *reinterpret_cast<__half *>(sm + S::YA16 + kmaj_off(32 * hsel + j, tl, 2, PADLBO, S::TY_SBO)) =
+                    __float2half_rn(ya[j] * sdown);
+            if (e != ya_exp) {
+                // T_A column tl = T_L row tl scaled by 2^e (exact in fp16); my half of k
+                const float sup = pow2i(e);
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<__half *>(sm + S::TA16 + kmaj_off(k8 * 8 + u, mp, 2, PADLBO, S::TY_SBO)) =
-                        __float2half_rn(__half2float(t8[u]) * sup);
+                for (int k8 = 0; k8 < 4; ++k8) {
+                    const int k0 = 32 * hsel + 8 * k8;
+                    __align__(16) __half t8[8];
+                    *reinterpret_cast<uint4 *>(t8) =
+                        *reinterpret_cast<const uint4 *>(sm + S::TL16 + kmaj_off(tl, k0, 2, 128, 1024));
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<__half *>(sm + S::TA16 + kmaj_off(k0 + u, tl, 2, PADLBO, S::TY_SBO)) =
+                            __float2half_rn(__half2float(t8[u]) * sup);
+                }
+                ya_exp = e;
             }
         }
         fence_proxy_async_smem();
@@ -421,9 +540,10 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         __syncthreads();
         tc_fence_after();
 
-        // ---- S6: A2' = Ya . T_A^T -------------------------------------------------
+        // ---- S6: A2' = Ya . T_A^T -----------------------------------------------------
         if (tid == 0) {
             const uint32_t id = idesc(128, 64, 0, 0);
+#pragma unroll
             for (int s = 0; s < MP / 16; ++s)
                 mma_f16_ss(tb + T::G, sdesc(sm + S::YA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO),
                            sdesc(sm + S::TA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO), id, s > 0);
@@ -434,10 +554,11 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
 
-        // ---- S7: A2 = unskewed, masked A2' (scaled fp16 rows) ----------------------
-        if (warp < 2) {
-            const int i = tid;
-            for (int c0 = 0; c0 < CH; c0 += 16) {
+        // ---- S7: A2 = unskewed, masked A2' (row-scaled fp16) ------------------------------
+        if (q4 < 2) {
+            const int i = tl;
+#pragma unroll
+            for (int c0 = 32 * hsel; c0 < 32 * hsel + 32; c0 += 16) {
                 float v[16];
                 tmem_ld16(tb + lane_base + T::G + c0, v);
                 tmem_wait_ld();
@@ -446,23 +567,27 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
             }
         }
         __syncthreads();
-        if (warp < 2) {
-            const int i = tid;
+        {
+            const int i = tid >> 2, p = tid & 3;
+            float v16[16];
             float amax = 0.f;
-            for (int j = 0; j <= i; ++j) amax = fmaxf(amax, fabsf(scr[i * 64 + ((2 * i - j) & 63)]));
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int j = 16 * p + u;
+                v16[u] = j <= i ? scr[i * 64 + ((2 * i - j) & 63)] : 0.f;
+                amax = fmaxf(amax, fabsf(v16[u]));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             const int e = down_exp(amax);
             const float sdown = pow2i(-e);
-            osc[i] = pow2i(e);
-            for (int j8 = 0; j8 < CH / 8; ++j8) {
-                __align__(16) __half g8[8];
+            if (p == 0) osc[i] = pow2i(e);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int j = j8 * 8 + u;
-                    const float g = j <= i ? scr[i * 64 + ((2 * i - j) & 63)] * sdown : 0.f;
-                    g8[u] = __float2half_rn(g);
-                }
-                *reinterpret_cast<uint4 *>(sm + S::A216 + kmaj_off(i, j8 * 8, 2, 128, 1024)) =
-                    *reinterpret_cast<const uint4 *>(g8);
+            for (int h8 = 0; h8 < 2; ++h8) {
+                float g8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) g8[u] = v16[8 * h8 + u] * sdown;
+                *reinterpret_cast<uint4 *>(sm + S::A216 + kmaj_off(i, 16 * p + 8 * h8, 2, 128, 1024)) = pack_f16x8(g8);
             }
         }
         fence_proxy_async_smem();
@@ -470,14 +595,16 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         __syncthreads();
         tc_fence_after();
 
-        // ---- S8: O1 = Vt^T . A2^T ; O2 = Gamma^T . a'^T ---------------------------
+        // ---- S8: O1 = Vt^T . A2^T ; O2 = Gamma^T . a'^T -------------------------------------
         if (tid == 0) {
             const uint32_t id16 = idesc(128, 64, 0, 0);
             const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;  // value rows R .. R+127
+#pragma unroll
             for (int s = 0; s < CH / 16; ++s)
                 mma_f16_ss(tb + T::PT, sdesc(sm + vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
                            sdesc(sm + S::A216 + s * 256, 128, 1024), id16, s > 0);
             const uint32_t id32 = idesc(128, 64, 2, 2);
+#pragma unroll
             for (int s = 0; s < MP / 8; ++s)
                 mma_tf32_ts(tb + T::LT, tb + T::GT + 8 * s, sdesc(sm + S::AP32 + s * 2 * PADLBO, PADLBO, S::AP_SBO),
                             id32, s > 0);
@@ -488,10 +615,23 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
 
-        // ---- S9: outputs; scale the state by lambda^L --------------------------------
+        // ---- S9: next chunk's raw rows; outputs; state scaled by lambda^L -------------------
+        if (ci + 1 < nchunks) {
+            tma_pending = 1;
+            if (tid == 0) {
+                // YA16 / AP32 were last read by the S6 / S8 MMAs, both complete
+                const int tn = t0 + CH;
+                mbar_arrive_expect_tx(&bar[5], raw_bytes);
+                tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, tn - HALO, b, &bar[5]);
+                tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[5]);
+                tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[5]);
+            }
+        }
         {
-            const int jv = tid;  // value channel lane
-            for (int c0 = 0; c0 < CH; c0 += 16) {
+            const int jv = tl;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = 32 * hsel + 16 * cc;
                 float o1[16], o2[16];
                 tmem_ld16(tb + lane_base + T::PT + c0, o1);
                 tmem_ld16(tb + lane_base + T::LT + c0, o2);
@@ -505,8 +645,8 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
                     }
                 }
             }
-            // eta_p <- lambda^L eta_p + B sum_{k<L} lambda^k  (Re thread of each mode)
-            if (!is_im) {
+            if (hsel == 0 && !is_im) {
+                // eta <- lambda^L eta + B sum_{k<L} lambda^k
                 float sr = 0.f, si = 0.f, pr = 1.f, pi = 0.f;
                 for (int k = 0; k < L; ++k) {
                     sr += pr;
@@ -521,9 +661,10 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
                 eta_r = er;
                 eta_i = ei;
             }
-            // U (lanes = mode planes): partner lane holds the other component
+            // U (lanes = mode planes): the partner lane holds the other component
             const float2 lm = laml[mm];
-            for (int c0 = 0; c0 < R; c0 += 16) {
+#pragma unroll
+            for (int c0 = hsel * (R / 2); c0 < (hsel + 1) * (R / 2); c0 += 16) {
                 float v[16];
                 tmem_ld16(tb + lane_base + T::U + c0, v);
                 tmem_wait_ld();
@@ -536,7 +677,8 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
                 tmem_st16(tb + lane_base + T::U + c0, v);
             }
             // Gamma^T (lanes = value channels, columns = (Re, Im) per mode)
-            for (int c0 = 0; c0 < MP; c0 += 16) {
+#pragma unroll
+            for (int c0 = 64 * hsel; c0 < 64 * hsel + 64; c0 += 16) {
                 float v[16];
                 tmem_ld16(tb + lane_base + T::GT + c0, v);
                 tmem_wait_ld();
@@ -555,14 +697,16 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         __syncthreads();
         tc_fence_after();
 
-        // ---- S10: U += Coef . Kt ; Gamma^T += Vt^T . Coef^T ---------------------------
+        // ---- S10: U += Coef . Kt ; Gamma^T += Vt^T . Coef^T -----------------------------------
         if (tid == 0) {
             const uint32_t idu = idesc(128, R, 0, 0);
+#pragma unroll
             for (int s = 0; s < CH / 16; ++s)
                 mma_f16_ss(tb + T::U, sdesc(sm + S::CF16 + s * 256, 128, 1024),
                            sdesc(sm + S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, 1);
             const uint32_t idg = idesc(128, MP, 0, 0);
             const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;
+#pragma unroll
             for (int s = 0; s < CH / 16; ++s)
                 mma_f16_ss(tb + T::GT, sdesc(sm + vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
                            sdesc(sm + S::CF16 + s * 256, 128, 1024), idg, 1);
@@ -571,18 +715,24 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         __syncwarp();
     }
 
-    // ---- final state ------------------------------------------------------------
+    // ---- final state ------------------------------------------------------------------
     if (ok && nchunks > 0) {
         ok = mbar_wait(&bar[4], (nchunks - 1) & 1);
         tc_fence_after();
     }
     ok = !__syncthreads_or(!ok);
+    if (!ok) {
+        // error path: let a copy still in flight land before the CTA exits
+        if (tma_pending) mbar_wait(&bar[5], (uint32_t)(ci & 1), 200000000LL);
+        if (tid == 0) report_error(a.err, kErrWaitTimeout);
+    }
     if (ok && a.final_state) {
         float *fs = a.final_state + (size_t)unit * a.state_floats;
         const int RD = R + D;
         const size_t plane = (size_t)M * RD;
-        // U: thread mp writes row (is_im ? M + m : m), columns 0..R-1
-        for (int c0 = 0; c0 < R; c0 += 16) {
+        // U: plane tl -> row (Re: m, Im: M + m), my half of the columns
+#pragma unroll
+        for (int c0 = hsel * (R / 2); c0 < (hsel + 1) * (R / 2); c0 += 16) {
             float v[16];
             tmem_ld16(tb + lane_base + T::U + c0, v);
             tmem_wait_ld();
@@ -590,20 +740,21 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) row[j] = v[j];
         }
-        // Gamma^T: thread jv writes column R + jv of every row
-        for (int c0 = 0; c0 < MP; c0 += 16) {
+        // Gamma^T: value lane tl writes column R + tl of every row, my half of the modes
+#pragma unroll
+        for (int c0 = 64 * hsel; c0 < 64 * hsel + 64; c0 += 16) {
             float v[16];
             tmem_ld16(tb + lane_base + T::GT + c0, v);
             tmem_wait_ld();
-            if (tid < D) {
+            if (tl < D) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int pl = c0 + j, m = pl >> 1;
-                    fs[((pl & 1) ? plane : 0) + (size_t)m * RD + R + tid] = v[j];
+                    fs[((pl & 1) ? plane : 0) + (size_t)m * RD + R + tl] = v[j];
                 }
             }
         }
-        if (!is_im) {
+        if (hsel == 0 && !is_im) {
             fs[2 * plane + mm] = eta_r;
             fs[2 * plane + M + mm] = eta_i;
         }
@@ -618,19 +769,55 @@ __global__ void __launch_bounds__(NTH, 1) chunk_prefill_kernel(PrefillArgs a) {
         const size_t used = 2 * plane + 2 * M + 2 * (size_t)(W - 1) * R;
         for (size_t x = used + tid; x < a.state_floats; x += NTH) fs[x] = 0.f;
     }
-    if (!ok && tid == 0) report_error(a.err, kErrWaitTimeout);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
+// ---- host side ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn(std::string &why) {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    static std::string err;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+            err = "cuTensorMapEncodeTiled is not available from the driver";
+        else
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!fn) why = err;
+    return fn;
+}
+
+// [B, N, H, C] bf16 tensor as a 4-D map (C, H, N, B) with a box of `rows`
+// positions of one head: box (C, 1, rows, 1).
+static bool make_map(EncodeTiledFn fn, CUtensorMap *m, const void *ptr, int B, int N, int H, int C, int rows) {
+    cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)H * C * 2, (cuuint64_t)N * H * C * 2};
+    cuuint32_t box[4] = {(cuuint32_t)C, 1, (cuuint32_t)rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int R, int D>
-static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st) {
+static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const CUtensorMap &mq,
+                                   const CUtensorMap &mk, const CUtensorMap &mv) {
     using S = ChunkSmem<R, D>;
     auto kern = chunk_prefill_kernel<R, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(a.B * a.H), NTH, S::TOTAL, st>>>(a);
+    kern<<<(unsigned)(a.B * a.H), NTH, S::TOTAL, st>>>(a, mq, mk, mv);
     return cudaGetLastError();
 }
 
@@ -640,16 +827,24 @@ ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int, std:
     *taken = false;
     if (a.dtype != IDA_BF16 || a.M != 64 || (a.flags & IDA_READOUT_ETA) || a.W > 4) return IDA_OK;
     if (!((a.R == 64 || a.R == 128) && (a.d == 64 || a.d == 128))) return IDA_OK;
+    EncodeTiledFn fn = encode_fn(why);
+    if (!fn) return IDA_OK;  // no tensor-map support: the sequential kernel serves
+    CUtensorMap mq, mk, mv;
+    if (!make_map(fn, &mq, a.q, a.B, a.N, a.H, a.R, CH + HALO) ||
+        !make_map(fn, &mk, a.k, a.B, a.N, a.H, a.R, CH + HALO) || !make_map(fn, &mv, a.v, a.B, a.N, a.H, a.d, CH)) {
+        why = "cuTensorMapEncodeTiled rejected the q/k/v layout";
+        return IDA_OK;
+    }
     *taken = true;
     cudaError_t e;
     if (a.R == 128 && a.d == 128)
-        e = launch_chunk_rd<128, 128>(a, st);
+        e = launch_chunk_rd<128, 128>(a, st, mq, mk, mv);
     else if (a.R == 64 && a.d == 64)
-        e = launch_chunk_rd<64, 64>(a, st);
+        e = launch_chunk_rd<64, 64>(a, st, mq, mk, mv);
     else if (a.R == 128 && a.d == 64)
-        e = launch_chunk_rd<128, 64>(a, st);
+        e = launch_chunk_rd<128, 64>(a, st, mq, mk, mv);
     else
-        e = launch_chunk_rd<64, 128>(a, st);
+        e = launch_chunk_rd<64, 128>(a, st, mq, mk, mv);
     if (e != cudaSuccess) {
         why = std::string("chunked prefill launch: ") + cudaGetErrorString(e);
         return IDA_ERR_CUDA;
