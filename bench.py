@@ -393,7 +393,8 @@ def main():
     ap.add_argument("--workload", default=configs.PREFILL_125M.name, choices=sorted(configs.ALL))
     ap.add_argument("--eta", action="store_true", help="eta-normalised readout")
     ap.add_argument("--no-decode", action="store_true", help="skip the secondary decode line")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle CPU work")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle CPU work for cpu_baseline (0: skip the CPU leg)")
     args = ap.parse_args()
     w = configs.ALL[args.workload]
     flags = 1 if args.eta else 0
@@ -459,7 +460,7 @@ def main():
     if rank != 0:
         return
     cpu = None
-    if ws == 1 or rank == 0:
+    if args.cpu_budget > 0:
         cv, desc, _ = oracle_sample(w, args.cpu_budget, cores, flags)
         cpu = {"value": cv, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
                "host": f"{platform.machine()} x{cores}"}

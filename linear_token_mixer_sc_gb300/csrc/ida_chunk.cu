@@ -72,13 +72,13 @@ struct ChunkSmem {
     static constexpr int XQ16 = 0;                               // [64][R] f16   LBO 128, SBO 16R
     static constexpr int KT16 = XQ16 + CH * R * 2;               // [64][R] f16   (follows XQ16: A rows 64..127)
     static constexpr int XQ32 = KT16 + CH * R * 2;               // [64][R] tf32  LBO 128, SBO 32R; skew scratch
-    static constexpr int ZT16 = XQ32 + CH * R * 4;               // [R+D][64] f16 LBO 144, SBO 1152
-    static constexpr int ZT_SBO = 8 * PADLBO;
+    static constexpr int ZT16 = XQ32 + CH * R * 4;               // [R+D][64] f16 LBO 144, SBO 1168
+    static constexpr int ZT_SBO = 8 * PADLBO + 16;               // +16: row blocks start on different banks
     static constexpr int GP16 = ZT16 + (R + D) / 8 * ZT_SBO;     // [64][64] f16  LBO 128, SBO 1024; S5 scratch
     static constexpr int A216 = GP16 + CH * CH * 2;              // [64][64] f16
     static constexpr int TL16 = A216 + CH * CH * 2;              // [128][64] f16 LBO 128, SBO 1024
     static constexpr int CF16 = TL16 + MP * CH * 2;              // [128][64] f16
-    static constexpr int TA16 = CF16 + MP * CH * 2;              // [64][128] f16 LBO 144, SBO 2304
+    static constexpr int TA16 = align1k(CF16 + MP * CH * 2);     // [64][128] f16 LBO 144, SBO 2304
     static constexpr int TY_SBO = 16 * PADLBO;
     static constexpr int YA16 = TA16 + 8 * TY_SBO;               // [64][128] f16 LBO 144, SBO 2304
     static constexpr int AP32 = YA16 + 8 * TY_SBO;               // [64][128] tf32 LBO 144, SBO 4608
@@ -89,14 +89,14 @@ struct ChunkSmem {
     static constexpr int RAWQ = YA16;                            // [67][R] bf16, row r = position t0-3+r
     static constexpr int RAWK = RAWQ + RAWQ_BYTES;               // [67][R] bf16
     static constexpr int RAWV = RAWK + RAWQ_BYTES;               // [64][D] bf16
-    static_assert(YA16 % 1024 == 0 && RAWV + CH * D * 2 <= MISC, "raw staging must fit over YA16/AP32");
+    static constexpr int CWS = RAWV + CH * D * 2;                // [2][R][W] float conv taps of this head
+    static_assert(YA16 % 1024 == 0 && CWS + 2 * R * 4 * 4 <= MISC, "raw staging must fit over YA16/AP32");
     static constexpr int BARS = MISC;                            // 6 mbarriers
     static constexpr int TSLOT = BARS + 64;
     static constexpr int OSC = TSLOT + 16;                       // [64] float: row scales of A2
     static constexpr int LAML = OSC + CH * 4;                    // [64] float2: lambda^L per mode
-    static constexpr int CWQ = LAML + 64 * 8;                    // [R][4] float conv taps (q)
-    static constexpr int CWK = CWQ + R * 16;                     // [R][4] float conv taps (k)
-    static constexpr int NWS = CWK + R * 16;                     // [R+D] float RMSNorm weights
+    static constexpr int SUML = LAML + 64 * 8;                   // [64] float2: sum_{k<L} lambda^k per mode
+    static constexpr int NWS = SUML + 64 * 8;                    // [R+D] float RMSNorm weights
     static constexpr int BSS = NWS + (R + D) * 4;                // [R+D] float RMSNorm biases
     static constexpr int TOTAL = BSS + (R + D) * 4;
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
@@ -157,8 +157,7 @@ __global__ void __launch_bounds__(NTH, 1)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S::TSLOT);
     float *osc = reinterpret_cast<float *>(sm + S::OSC);
     float2 *laml = reinterpret_cast<float2 *>(sm + S::LAML);
-    float *cwq = reinterpret_cast<float *>(sm + S::CWQ);
-    float *cwk = reinterpret_cast<float *>(sm + S::CWK);
+    float2 *suml = reinterpret_cast<float2 *>(sm + S::SUML);
     float *nws = reinterpret_cast<float *>(sm + S::NWS);
     float *bss = reinterpret_cast<float *>(sm + S::BSS);
 
@@ -174,7 +173,10 @@ __global__ void __launch_bounds__(NTH, 1)
     const __nv_bfloat16 *gq = reinterpret_cast<const __nv_bfloat16 *>(a.q);
     const __nv_bfloat16 *gk = reinterpret_cast<const __nv_bfloat16 *>(a.k);
     __nv_bfloat16 *gout = reinterpret_cast<__nv_bfloat16 *>(a.out);
-    const uint32_t raw_bytes = 2u * (CH + HALO) * R * 2 + (uint32_t)CH * D * 2;
+    const uint32_t tap_bytes = (uint32_t)R * W * 4;  // one head's conv taps for q (or k)
+    const uint32_t raw_bytes = 2u * (CH + HALO) * R * 2 + (uint32_t)CH * D * 2 + 2 * tap_bytes;
+    const float *taps_q = a.conv_w + (size_t)(0 * H + h) * R * W;
+    const float *taps_k = a.conv_w + (size_t)(1 * H + h) * R * W;
 
     // my mode plane in the lane-side stages: plane tl = 2m + (0: Re, 1: Im)
     const int mm = tl >> 1, is_im = tl & 1;
@@ -200,29 +202,38 @@ __global__ void __launch_bounds__(NTH, 1)
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
-    for (int x = tid; x < R * 4; x += NTH) {
-        const int c = x >> 2, j = x & 3;
-        cwq[x] = j < W ? a.conv_w[((size_t)(0 * H + h) * R + c) * W + j] : 0.f;
-        cwk[x] = j < W ? a.conv_w[((size_t)(1 * H + h) * R + c) * W + j] : 0.f;
-    }
     for (int x = tid; x < R + D; x += NTH) {
         nws[x] = a.norm_w[(size_t)h * (R + D) + x];
         bss[x] = a.bias[(size_t)h * (R + D) + x];
     }
     if (hsel == 0) {
         // T_L row (plane tl): component of lambda_m^k, k = 0..63; Coef row: component
-        // of B_m lambda_m^(C-1-j); T_A column tl = T_L row (unscaled).  Powers in fp64.
-        double pr = 1.0, pi = 0.0;
+        // of B_m lambda_m^(C-1-j); T_A column tl = T_L row (unscaled).
+        float pr = 1.f, pi = 0.f, sr = 0.f, si = 0.f;
         __align__(16) __half tl16[CH], cf[CH];
+#pragma unroll
         for (int k = 0; k < CH; ++k) {
-            tl16[k] = __float2half_rn((float)(is_im ? pi : pr));
-            const double cr = b_r * pr - b_i * pi, ci = b_r * pi + b_i * pr;
-            cf[CH - 1 - k] = __float2half_rn((float)(is_im ? ci : cr));
-            const double nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
+            sr += pr;
+            si += pi;
+            tl16[k] = __float2half_rn(is_im ? pi : pr);
+            const float cr = b_r * pr - b_i * pi, ci = b_r * pi + b_i * pr;
+            cf[CH - 1 - k] = __float2half_rn(is_im ? ci : cr);
+            const float nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
             pr = nr;
             pi = ni;
         }
-        if (!is_im) laml[mm] = make_float2((float)pr, (float)pi);  // lambda^C
+        // lambda^C by repeated squaring (fewer roundings than the running product)
+        float qr = lam_r, qi = lam_i;
+#pragma unroll
+        for (int sq = 0; sq < 6; ++sq) {
+            const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
+            qr = nr;
+            qi = ni;
+        }
+        if (!is_im) {
+            laml[mm] = make_float2(qr, qi);  // lambda^C
+            suml[mm] = make_float2(sr, si);  // sum_{k<C} lambda^k
+        }
 #pragma unroll
         for (int k8 = 0; k8 < CH / 8; ++k8) {
             *reinterpret_cast<uint4 *>(sm + S::TL16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
@@ -230,17 +241,20 @@ __global__ void __launch_bounds__(NTH, 1)
             *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
                 *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
         }
+#pragma unroll
         for (int k = 0; k < CH; ++k)
             *reinterpret_cast<__half *>(sm + S::TA16 + kmaj_off(k, tl, 2, PADLBO, S::TY_SBO)) = tl16[k];
     } else {
-        double pr = lam_r, pi = lam_i;
-        for (int k = 1; k < 33; ++k) {
-            const double nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
-            pr = nr;
-            pi = ni;
+        // lambda^33 = (lambda^32) lambda
+        float qr = lam_r, qi = lam_i;
+#pragma unroll
+        for (int sq = 0; sq < 5; ++sq) {
+            const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
+            qr = nr;
+            qi = ni;
         }
-        l33r = (float)pr;
-        l33i = (float)pi;
+        l33r = qr * lam_r - qi * lam_i;
+        l33i = qr * lam_i + qi * lam_r;
     }
     tc_fence_before();
     __syncthreads();
@@ -263,6 +277,8 @@ __global__ void __launch_bounds__(NTH, 1)
         tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, -HALO, b, &bar[5]);
         tma_load_4d(sm + S::RAWK, &tm_k, 0, h, -HALO, b, &bar[5]);
         tma_load_4d(sm + S::RAWV, &tm_v, 0, h, 0, b, &bar[5]);
+        bulk_load(sm + S::CWS, taps_q, tap_bytes, &bar[5]);
+        bulk_load(sm + S::CWS + R * 16, taps_k, tap_bytes, &bar[5]);
     }
 
     float eta_r = 0.f, eta_i = 0.f;  // eta of my mode (kept by hsel == 0, Re thread)
@@ -284,48 +300,62 @@ __global__ void __launch_bounds__(NTH, 1)
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
 
-        // ---- S1: prologue, thread = (position i, quarter p) --------------------
+        // ---- S1: prologue, thread = (8-channel block, block of consecutive positions)
         {
-            const int i = tid >> 2, p = tid & 3;
-            const bool valid = i < L;
-            constexpr int NGQ = R / 32, NGV = D / 32;
-            float fk[NGQ][8];
-            float ss[2] = {0.f, 0.f};
+            // query / key: R/8 channel blocks x (64 R/8 / 256) positions per thread
+            constexpr int CBQ = R / 8, PPQ = CH * CBQ / NTH;
+            const int cb = tid % CBQ, i0 = (tid / CBQ) * PPQ, c0 = 8 * cb;
+            float fk[PPQ][8];
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 const unsigned char *raw = sm + (which == 0 ? S::RAWQ : S::RAWK);
-                const float *cw = which == 0 ? cwq : cwk;
-                float f[NGQ][8];
-                float acc = 0.f;
+                const float *cwg = reinterpret_cast<const float *>(sm + S::CWS + which * R * 16) + c0 * W;
+                // taps right-aligned: w8[e][jj] multiplies position i - 3 + jj (zero for jj < 4 - W)
+                float w8[8][4];
 #pragma unroll
-                for (int gg = 0; gg < NGQ; ++gg) {
-                    const int c0 = 8 * (4 * gg + p);
-                    float s8[8];
+                for (int e = 0; e < 8; ++e)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) s8[e] = 0.f;
-                    for (int j = 0; j < W; ++j) {
-                        const int row = i + HALO + 1 - W + j;
-                        float x8[8];
-                        unpack_bf16x8(*reinterpret_cast<const uint4 *>(raw + ((size_t)row * R + c0) * 2), x8);
+                    for (int jj = 0; jj < 4; ++jj) w8[e][jj] = jj >= 4 - W ? cwg[e * W + jj - (4 - W)] : 0.f;
+                // rows i0 .. i0+PPQ+2 of the staged tile = positions i0-3 .. i0+PPQ-1
+                float f[PPQ][8];
+                float acc[PPQ];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) s8[e] = fmaf(cw[(c0 + e) * 4 + j], x8[e], s8[e]);
-                    }
+                for (int pp = 0; pp < PPQ; ++pp) {
+                    acc[pp] = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        f[gg][e] = silu_fast(s8[e]);
-                        acc = fmaf(f[gg][e], f[gg][e], acc);
+                    for (int e = 0; e < 8; ++e) f[pp][e] = 0.f;
+                }
+#pragma unroll
+                for (int r = 0; r < PPQ + HALO; ++r) {
+                    float x8[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(raw + ((size_t)(i0 + r) * R + c0) * 2), x8);
+                    // tile row r holds position i0 + r - 3: right-aligned tap jj = r - pp of position pp
+#pragma unroll
+                    for (int pp = 0; pp < PPQ; ++pp) {
+                        const int jj = r - pp;
+                        if (jj >= 0 && jj < 4)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) f[pp][e] = fmaf(w8[e][jj], x8[e], f[pp][e]);
                     }
                 }
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                const float inv = 1.f / (acc + IDA_EPS_FEAT);
-                if (which == 0) {
 #pragma unroll
-                    for (int gg = 0; gg < NGQ; ++gg) {
-                        const int c0 = 8 * (4 * gg + p);
-                        float x8[8];
+                for (int pp = 0; pp < PPQ; ++pp)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x8[e] = valid ? f[gg][e] * inv : 0.f;
+                    for (int e = 0; e < 8; ++e) {
+                        f[pp][e] = silu_fast(f[pp][e]);
+                        acc[pp] = fmaf(f[pp][e], f[pp][e], acc[pp]);
+                    }
+#pragma unroll
+                for (int pp = 0; pp < PPQ; ++pp) {
+#pragma unroll
+                    for (int o = 1; o < CBQ; o <<= 1) acc[pp] += __shfl_xor_sync(0xffffffffu, acc[pp], o);
+                    const float inv = 1.f / (acc[pp] + IDA_EPS_FEAT);
+                    const int i = i0 + pp;
+                    const bool valid = i < L;
+                    float x8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x8[e] = valid ? f[pp][e] * inv : 0.f;
+                    if (which == 0) {
                         *reinterpret_cast<uint4 *>(sm + S::XQ16 + kmaj_off(i, c0, 2, 128, 16 * R)) = pack_f16x8(x8);
                         uint4 t0v, t1v;
                         t0v.x = __float_as_uint(to_tf32(x8[0])); t0v.y = __float_as_uint(to_tf32(x8[1]));
@@ -334,65 +364,83 @@ __global__ void __launch_bounds__(NTH, 1)
                         t1v.z = __float_as_uint(to_tf32(x8[6])); t1v.w = __float_as_uint(to_tf32(x8[7]));
                         *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0, 4, 128, 32 * R)) = t0v;
                         *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0 + 4, 4, 128, 32 * R)) = t1v;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) fk[pp][e] = x8[e];
                     }
-                } else {
-#pragma unroll
-                    for (int gg = 0; gg < NGQ; ++gg)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            fk[gg][e] = f[gg][e] * inv;
-                            ss[1] = fmaf(fk[gg][e], fk[gg][e], ss[1]);
-                        }
                 }
             }
-            float msk = ss[1];
-            msk += __shfl_xor_sync(0xffffffffu, msk, 1);
-            msk += __shfl_xor_sync(0xffffffffu, msk, 2);
-            const float rk = rsqrtf(msk / R + IDA_EPS_RMS);
+            // key RMSNorm + affine; Kt rows and the transposed key rows of Z^T
+            __align__(16) __half kt_t[8][PPQ];
 #pragma unroll
-            for (int gg = 0; gg < NGQ; ++gg) {
-                const int c0 = 8 * (4 * gg + p);
+            for (int pp = 0; pp < PPQ; ++pp) {
+                float ms = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ms = fmaf(fk[pp][e], fk[pp][e], ms);
+#pragma unroll
+                for (int o = 1; o < CBQ; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
+                const float rk = rsqrtf(ms / R + IDA_EPS_RMS);
+                const int i = i0 + pp;
+                const bool valid = i < L;
                 float x8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x8[e] = valid ? fmaf(fk[gg][e] * rk, nws[c0 + e], bss[c0 + e]) : 0.f;
+                for (int e = 0; e < 8; ++e) {
+                    x8[e] = valid ? fmaf(fk[pp][e] * rk, nws[c0 + e], bss[c0 + e]) : 0.f;
+                    kt_t[e][pp] = __float2half_rn(x8[e]);
+                }
                 *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) = pack_f16x8(x8);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                unsigned char *dst = sm + S::ZT16 + kmaj_off(c0 + e, i0, 2, PADLBO, S::ZT_SBO);
+                if (PPQ == 4)
+                    *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(kt_t[e]);
+                else
+                    *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(kt_t[e]);
+            }
+        }
+        {
+            // value: D/8 channel blocks x (64 D/8 / 256) positions per thread
+            constexpr int CBV = D / 8, PPV = CH * CBV / NTH;
+            const int cb = tid % CBV, i0 = (tid / CBV) * PPV, j0 = 8 * cb;
+            __align__(16) __half vt_t[8][PPV];
+#pragma unroll
+            for (int pp = 0; pp < PPV; ++pp) {
+                const int i = i0 + pp;
+                float x8[8];
+                unpack_bf16x8(*reinterpret_cast<const uint4 *>(sm + S::RAWV + ((size_t)i * D + j0) * 2), x8);
+                float ms = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ms = fmaf(x8[e], x8[e], ms);
+#pragma unroll
+                for (int o = 1; o < CBV; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
+                const float rv = rsqrtf(ms / D + IDA_EPS_RMS);
+                const bool valid = i < L;
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    *reinterpret_cast<__half *>(sm + S::ZT16 + kmaj_off(c0 + e, i, 2, PADLBO, S::ZT_SBO)) =
-                        __float2half_rn(x8[e]);
+                    vt_t[e][pp] = __float2half_rn(valid ? fmaf(x8[e] * rv, nws[R + j0 + e], bss[R + j0 + e]) : 0.f);
             }
-            float xv[NGV][8];
-            float msv = 0.f;
 #pragma unroll
-            for (int gg = 0; gg < NGV; ++gg) {
-                const int j0 = 8 * (4 * gg + p);
-                unpack_bf16x8(*reinterpret_cast<const uint4 *>(sm + S::RAWV + ((size_t)i * D + j0) * 2), xv[gg]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) msv = fmaf(xv[gg][e], xv[gg][e], msv);
-            }
-            msv += __shfl_xor_sync(0xffffffffu, msv, 1);
-            msv += __shfl_xor_sync(0xffffffffu, msv, 2);
-            const float rv = rsqrtf(msv / D + IDA_EPS_RMS);
-#pragma unroll
-            for (int gg = 0; gg < NGV; ++gg) {
-                const int j0 = 8 * (4 * gg + p);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float vt = valid ? fmaf(xv[gg][e] * rv, nws[R + j0 + e], bss[R + j0 + e]) : 0.f;
-                    *reinterpret_cast<__half *>(sm + S::ZT16 + kmaj_off(R + j0 + e, i, 2, PADLBO, S::ZT_SBO)) =
-                        __float2half_rn(vt);
-                }
+            for (int e = 0; e < 8; ++e) {
+                unsigned char *dst = sm + S::ZT16 + kmaj_off(R + j0 + e, i0, 2, PADLBO, S::ZT_SBO);
+                if (PPV == 4)
+                    *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(vt_t[e]);
+                else
+                    *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(vt_t[e]);
             }
         }
         if (L < CH && hsel == 0) {
             // ragged last chunk: Coef row = component of B lambda^(L-1-j) for j < L, else 0
-            double pr = 1.0, pi = 0.0;
+            float pr = 1.f, pi = 0.f, sr = 0.f, si = 0.f;
             __align__(16) __half cf[CH];
+#pragma unroll
             for (int j = 0; j < CH; ++j) cf[j] = __float2half_rn(0.f);
             for (int k = 0; k < L; ++k) {
-                const double cr = b_r * pr - b_i * pi, cim = b_r * pi + b_i * pr;
-                cf[L - 1 - k] = __float2half_rn((float)(is_im ? cim : cr));
-                const double nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
+                sr += pr;
+                si += pi;
+                const float cr = b_r * pr - b_i * pi, cim = b_r * pi + b_i * pr;
+                cf[L - 1 - k] = __float2half_rn(is_im ? cim : cr);
+                const float nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
                 pr = nr;
                 pi = ni;
             }
@@ -400,7 +448,10 @@ __global__ void __launch_bounds__(NTH, 1)
             for (int k8 = 0; k8 < CH / 8; ++k8)
                 *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
                     *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
-            if (!is_im) laml[mm] = make_float2((float)pr, (float)pi);  // lambda^L
+            if (!is_im) {
+                laml[mm] = make_float2(pr, pi);  // lambda^L
+                suml[mm] = make_float2(sr, si);  // sum_{k<L} lambda^k
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -625,6 +676,8 @@ __global__ void __launch_bounds__(NTH, 1)
                 tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, tn - HALO, b, &bar[5]);
                 tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[5]);
                 tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[5]);
+                bulk_load(sm + S::CWS, taps_q, tap_bytes, &bar[5]);
+                bulk_load(sm + S::CWS + R * 16, taps_k, tap_bytes, &bar[5]);
             }
         }
         {
@@ -647,15 +700,8 @@ __global__ void __launch_bounds__(NTH, 1)
             }
             if (hsel == 0 && !is_im) {
                 // eta <- lambda^L eta + B sum_{k<L} lambda^k
-                float sr = 0.f, si = 0.f, pr = 1.f, pi = 0.f;
-                for (int k = 0; k < L; ++k) {
-                    sr += pr;
-                    si += pi;
-                    const float nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
-                    pr = nr;
-                    pi = ni;
-                }
-                const float2 ll = laml[mm];
+                const float2 ll = laml[mm], sl = suml[mm];
+                const float sr = sl.x, si = sl.y;
                 const float er = ll.x * eta_r - ll.y * eta_i + b_r * sr - b_i * si;
                 const float ei = ll.x * eta_i + ll.y * eta_r + b_r * si + b_i * sr;
                 eta_r = er;
@@ -821,8 +867,11 @@ static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const 
     return cudaGetLastError();
 }
 
-// Takes bf16 prefill with M = 64 modes and R, d in {64, 128}; the eta readout
-// and every other shape go to the sequential kernel.
+// Takes bf16 prefill with M = 64 modes and R, d in {64, 128}, denominator-free
+// readout.  The eta readout divides by Re(xi(q)^T U^T eta), which on the
+// synthetic workloads comes within 1e-5 of its scale; fp16 / tf32 operand
+// rounding then dominates the quotient, so that readout, and every other
+// shape, is served by the fp32 sequential kernel.
 ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int, std::string &why, bool *taken) {
     *taken = false;
     if (a.dtype != IDA_BF16 || a.M != 64 || (a.flags & IDA_READOUT_ETA) || a.W > 4) return IDA_OK;

@@ -148,3 +148,18 @@ def test_prefill_14k_full_size_sampled_with_final_state():
     units = [0, 9, w.B * w.H - 1]
     errs, _ = _sampled(w, units, 0, final_state=True)
     assert max(errs) <= BF16_REL_L2, errs
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_eta_readout_constant_values_on_gpu(path):
+    """eta readout with the same v row at every position returns that row's
+    normalised value (the oracle's constant-value pin, on the device)."""
+    B, N, H, R, d, M, W = 1, 150, 2, 64, 64, 64, 4
+    q, k, v, p = problem(B, N, H, R, d, M, W, "bf16", seed=31)
+    v = v[:, :1].expand(B, N, H, d).contiguous()
+    out, _ = _run(q, k, v, p, flags=PATHS[path] | binding.IDA_READOUT_ETA)
+    ref = orc.forward(q, k, v, p, flags=binding.IDA_READOUT_ETA)
+    assert rel_l2(to_np(out), ref["out"]) <= BF16_REL_L2
+    # and the oracle's value is the constant row itself
+    np.testing.assert_allclose(ref["out"], np.broadcast_to(ref["out"][:, :1], ref["out"].shape),
+                               rtol=1e-6, atol=1e-8)
