@@ -204,13 +204,14 @@ class Prefill:
 
 
 class Decode:
-    def __init__(self, w, dev, flags=0):
+    def __init__(self, w, dev, flags=0, seed_len=None):
         from linear_token_mixer_sc_gb300 import binding
         self.b = binding
         self.w, self.dev, self.flags = w, dev, flags
         p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
         self.pd = binding.params_to_device(p, dev)
-        q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed, device=dev)
+        n0 = w.N if seed_len is None else seed_len
+        q, k, v = inputs.make_qkv(w.B, n0, w.H, w.R, w.d, w.dtype, w.seed, device=dev)
         _, self.state = binding.ida_forward(q, k, v, self.pd, final_state=True)
         del q, k, v
         # a ring of pre-drawn tokens so that no generator runs inside the timed region
@@ -355,8 +356,8 @@ def max_over_ranks(dist, x: float, dev) -> float:
     return float(t.item())
 
 
-def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e2e=True):
-    runner = (Decode if w.decode_steps else Prefill)(w, dev, flags)
+def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e2e=True, seed_len=None):
+    runner = Decode(w, dev, flags, seed_len) if w.decode_steps else Prefill(w, dev, flags)
     flush = runner.resident_bytes() < 2 * L2_BYTES
     if dist is not None:
         dist.barrier()
@@ -393,6 +394,8 @@ def main():
     ap.add_argument("--workload", default=configs.PREFILL_125M.name, choices=sorted(configs.ALL))
     ap.add_argument("--eta", action="store_true", help="eta-normalised readout")
     ap.add_argument("--no-decode", action="store_true", help="skip the secondary decode line")
+    ap.add_argument("--seed-len", type=int, default=None,
+                    help="decode workload: length of the seeding prefill (default: the workload's 4096)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle CPU work for cpu_baseline (0: skip the CPU leg)")
     args = ap.parse_args()
@@ -442,7 +445,7 @@ def main():
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     main_res = measure(w, dev, args.steps, args.warmup, flags, dist, ws, peaks, peak_kind,
-                       DECODE_SOURCES if w.decode_steps else PREFILL_SOURCES)
+                       DECODE_SOURCES if w.decode_steps else PREFILL_SOURCES, seed_len=args.seed_len)
     clocks = sampler.stop()
     decode_res = None
     if not w.decode_steps and not args.no_decode:
@@ -450,7 +453,7 @@ def main():
         sampler2 = ClockSampler(dev.index if dev.index is not None else 0)
         sampler2.start()
         decode_res = measure(dw, dev, max(args.steps, 64), args.warmup, 0, dist, ws, peaks,
-                             peak_kind, DECODE_SOURCES, e2e=True)
+                             peak_kind, DECODE_SOURCES, e2e=True, seed_len=args.seed_len)
         decode_res["clocks"] = sampler2.stop()
         decode_res["config"] = {"workload": dw.name, "B": dw.B, "H": dw.H, "R": dw.R, "d": dw.d,
                                 "M": dw.M, "seed_prefill_N": dw.N}

@@ -22,7 +22,7 @@
 
 namespace ida {
 
-constexpr int DEC_WARPS = 8;
+constexpr int DEC_WARPS = 4;
 constexpr int DEC_THREADS = DEC_WARPS * 32;
 constexpr int DEC_UNROLL = 2;  // modes in flight per warp
 
@@ -112,11 +112,95 @@ __device__ __forceinline__ void unpack4(float4 f, T v[4]) {
     v[3] = f.w;
 }
 
+// State slices of DEC_UNROLL modes of one warp: [mode][plane: Re U, Im U, Re G, Im G][slice].
+template <int NV>
+struct ModeGroup {
+    float4 v[DEC_UNROLL][4][NV];
+};
+
+template <int NV>
+__device__ __forceinline__ void load_group(ModeGroup<NV> &g, const float *st, int mb, int M, int R, int d,
+                                           int RD, size_t plane, int lane) {
+#pragma unroll
+    for (int u = 0; u < DEC_UNROLL; ++u) {
+        const int m = mb + u * DEC_WARPS;
+#pragma unroll
+        for (int iv = 0; iv < NV; ++iv) {
+            const int c = 4 * (lane + 32 * iv);
+            const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+            const bool okm = m < M;
+            g.v[u][0][iv] = okm && c < R ? ld_state(st + (size_t)m * RD + c) : zero;
+            g.v[u][1][iv] = okm && c < R ? ld_state(st + plane + (size_t)m * RD + c) : zero;
+            g.v[u][2][iv] = okm && c < d ? ld_state(st + (size_t)m * RD + R + c) : zero;
+            g.v[u][3][iv] = okm && c < d ? ld_state(st + plane + (size_t)m * RD + R + c) : zero;
+        }
+    }
+}
+
+// Update the group's modes, store them, accumulate the readout.
+template <int NV, typename T>
+__device__ __forceinline__ void step_group(const ModeGroup<NV> &g, float *st, int mb, const DecodeArgs &a,
+                                           int h, int RD, size_t plane, int lane, const T (&xq)[NV][4],
+                                           const T (&zk)[NV][4], const T (&zv)[NV][4], T (&oacc)[NV][4],
+                                           T &dacc) {
+    const int M = a.M, R = a.R, d = a.d;
+#pragma unroll
+    for (int u = 0; u < DEC_UNROLL; ++u) {
+        const int m = mb + u * DEC_WARPS;
+        if (m >= M) break;
+        const T lr = a.lambda[((size_t)h * M + m) * 2], li = a.lambda[((size_t)h * M + m) * 2 + 1];
+        const T br = a.Bvec[((size_t)h * M + m) * 2], bi = a.Bvec[((size_t)h * M + m) * 2 + 1];
+        T ar = 0, ai = 0;
+        T yr[NV][4], yi[NV][4];
+#pragma unroll
+        for (int iv = 0; iv < NV; ++iv) {
+            const int c = 4 * (lane + 32 * iv);
+            T xr[4], xi[4];
+            unpack4(g.v[u][0][iv], xr);
+            unpack4(g.v[u][1][iv], xi);
+            unpack4(g.v[u][2][iv], yr[iv]);
+            unpack4(g.v[u][3][iv], yi[iv]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                cstep_t(xr[e], xi[e], lr, li, br, bi, zk[iv][e]);
+                ar = fma(xq[iv][e], xr[e], ar);
+                ai = fma(xq[iv][e], xi[e], ai);
+                cstep_t(yr[iv][e], yi[iv][e], lr, li, br, bi, zv[iv][e]);
+            }
+            if (c < R) {
+                st_state(st + (size_t)m * RD + c, xr);
+                st_state(st + plane + (size_t)m * RD + c, xi);
+            }
+            if (c < d) {
+                st_state(st + (size_t)m * RD + R + c, yr[iv]);
+                st_state(st + plane + (size_t)m * RD + R + c, yi[iv]);
+            }
+        }
+        ar = warp_sum(ar);
+        ai = warp_sum(ai);
+#pragma unroll
+        for (int iv = 0; iv < NV; ++iv)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[iv][e] += ar * yr[iv][e] - ai * yi[iv][e];
+        T er = st[2 * plane + m], ei = st[2 * plane + M + m];
+        cstep_t(er, ei, lr, li, br, bi, T(1));
+        dacc += ar * er - ai * ei;
+        __syncwarp();
+        if (lane == 0) {
+            st[2 * plane + m] = (float)er;
+            st[2 * plane + M + m] = (float)ei;
+        }
+    }
+}
+
 // NV: float4 slices per lane per row half (ceil(max(R, d) / 128)).
 // T: arithmetic type (double for fp32 inputs, float for bf16 inputs); the
-// state itself is always stored as fp32.
+// state itself is always stored as fp32.  The state loads of a warp's first
+// mode group are issued before the feature prologue, and every later group
+// is loaded while the previous one is being updated, so that each warp keeps
+// its next loads in flight through the arithmetic.
 template <int NV, typename T>
-__global__ void __launch_bounds__(DEC_THREADS) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(DEC_THREADS, 3) decode_kernel(DecodeArgs a) {
     __shared__ __align__(16) T xq_s[256];
     __shared__ __align__(16) T z_s[512];
     __shared__ __align__(16) T ored[DEC_WARPS][256];
@@ -127,6 +211,10 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(DecodeArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float *st = a.state + (size_t)unit * a.state_floats;
     const size_t plane = (size_t)M * RD;
+    constexpr int STRIDE = DEC_WARPS * DEC_UNROLL;  // modes between a warp's consecutive groups
+
+    ModeGroup<NV> ga, gb;
+    load_group(ga, st, warp, M, R, d, RD, plane, lane);
 
     decode_prologue<T>(a, unit, h, st, xq_s, z_s, warp, lane);
     __syncthreads();
@@ -146,70 +234,12 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(DecodeArgs a) {
     }
     T dacc = 0;
 
-    for (int mb = warp; mb < M; mb += DEC_WARPS * DEC_UNROLL) {
-        float4 ur[DEC_UNROLL][NV], ui[DEC_UNROLL][NV], gr[DEC_UNROLL][NV], gi[DEC_UNROLL][NV];
-        // issue every load of this group of modes before any arithmetic
-#pragma unroll
-        for (int u = 0; u < DEC_UNROLL; ++u) {
-            const int m = mb + u * DEC_WARPS;
-#pragma unroll
-            for (int iv = 0; iv < NV; ++iv) {
-                const int c = 4 * (lane + 32 * iv);
-                const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-                const bool okm = m < M;
-                ur[u][iv] = okm && c < R ? ld_state(st + (size_t)m * RD + c) : zero;
-                ui[u][iv] = okm && c < R ? ld_state(st + plane + (size_t)m * RD + c) : zero;
-                gr[u][iv] = okm && c < d ? ld_state(st + (size_t)m * RD + R + c) : zero;
-                gi[u][iv] = okm && c < d ? ld_state(st + plane + (size_t)m * RD + R + c) : zero;
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < DEC_UNROLL; ++u) {
-            const int m = mb + u * DEC_WARPS;
-            if (m >= M) break;
-            const T lr = a.lambda[((size_t)h * M + m) * 2], li = a.lambda[((size_t)h * M + m) * 2 + 1];
-            const T br = a.Bvec[((size_t)h * M + m) * 2], bi = a.Bvec[((size_t)h * M + m) * 2 + 1];
-            T ar = 0, ai = 0;
-            T yr[NV][4], yi[NV][4];
-#pragma unroll
-            for (int iv = 0; iv < NV; ++iv) {
-                const int c = 4 * (lane + 32 * iv);
-                T xr[4], xi[4];
-                unpack4(ur[u][iv], xr);
-                unpack4(ui[u][iv], xi);
-                unpack4(gr[u][iv], yr[iv]);
-                unpack4(gi[u][iv], yi[iv]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    cstep_t(xr[e], xi[e], lr, li, br, bi, zk[iv][e]);
-                    ar = fma(xq[iv][e], xr[e], ar);
-                    ai = fma(xq[iv][e], xi[e], ai);
-                    cstep_t(yr[iv][e], yi[iv][e], lr, li, br, bi, zv[iv][e]);
-                }
-                if (c < R) {
-                    st_state(st + (size_t)m * RD + c, xr);
-                    st_state(st + plane + (size_t)m * RD + c, xi);
-                }
-                if (c < d) {
-                    st_state(st + (size_t)m * RD + R + c, yr[iv]);
-                    st_state(st + plane + (size_t)m * RD + R + c, yi[iv]);
-                }
-            }
-            ar = warp_sum(ar);
-            ai = warp_sum(ai);
-#pragma unroll
-            for (int iv = 0; iv < NV; ++iv)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) oacc[iv][e] += ar * yr[iv][e] - ai * yi[iv][e];
-            T er = st[2 * plane + m], ei = st[2 * plane + M + m];
-            cstep_t(er, ei, lr, li, br, bi, T(1));
-            dacc += ar * er - ai * ei;
-            __syncwarp();
-            if (lane == 0) {
-                st[2 * plane + m] = (float)er;
-                st[2 * plane + M + m] = (float)ei;
-            }
-        }
+    for (int mb = warp; mb < M; mb += 2 * STRIDE) {
+        if (mb + STRIDE < M) load_group(gb, st, mb + STRIDE, M, R, d, RD, plane, lane);
+        step_group<NV, T>(ga, st, mb, a, h, RD, plane, lane, xq, zk, zv, oacc, dacc);
+        if (mb + STRIDE >= M) break;
+        if (mb + 2 * STRIDE < M) load_group(ga, st, mb + 2 * STRIDE, M, R, d, RD, plane, lane);
+        step_group<NV, T>(gb, st, mb + STRIDE, a, h, RD, plane, lane, xq, zk, zv, oacc, dacc);
     }
 #pragma unroll
     for (int iv = 0; iv < NV; ++iv) {
