@@ -89,8 +89,7 @@ struct ChunkSmem {
     static constexpr int RAWQ = YA16;                            // [67][R] bf16, row r = position t0-3+r
     static constexpr int RAWK = RAWQ + RAWQ_BYTES;               // [67][R] bf16
     static constexpr int RAWV = RAWK + RAWQ_BYTES;               // [64][D] bf16
-    static constexpr int CWS = RAWV + CH * D * 2;                // [2][R][W] float conv taps of this head
-    static_assert(YA16 % 1024 == 0 && CWS + 2 * R * 4 * 4 <= MISC, "raw staging must fit over YA16/AP32");
+    static_assert(YA16 % 1024 == 0 && RAWV + CH * D * 2 <= MISC, "raw staging must fit over YA16/AP32");
     static constexpr int BARS = MISC;                            // 6 mbarriers
     static constexpr int TSLOT = BARS + 64;
     static constexpr int OSC = TSLOT + 16;                       // [64] float: row scales of A2
@@ -110,6 +109,7 @@ struct ChunkTmem {
     static constexpr uint32_t G = 256;   // [64 lanes][64], later A2'
     static constexpr uint32_t PT = 320;  // [2M lanes][64], later O1
     static constexpr uint32_t LT = 384;  // [2M lanes][64], later O2
+    static constexpr uint32_t TAPS = 448;  // [lane][64]: conv taps (q then k) of channel block lane % (R/8)
 };
 
 // byte offset of element (row, k) in a K-major no-swizzle operand
@@ -173,10 +173,7 @@ __global__ void __launch_bounds__(NTH, 1)
     const __nv_bfloat16 *gq = reinterpret_cast<const __nv_bfloat16 *>(a.q);
     const __nv_bfloat16 *gk = reinterpret_cast<const __nv_bfloat16 *>(a.k);
     __nv_bfloat16 *gout = reinterpret_cast<__nv_bfloat16 *>(a.out);
-    const uint32_t tap_bytes = (uint32_t)R * W * 4;  // one head's conv taps for q (or k)
-    const uint32_t raw_bytes = 2u * (CH + HALO) * R * 2 + (uint32_t)CH * D * 2 + 2 * tap_bytes;
-    const float *taps_q = a.conv_w + (size_t)(0 * H + h) * R * W;
-    const float *taps_k = a.conv_w + (size_t)(1 * H + h) * R * W;
+    const uint32_t raw_bytes = 2u * (CH + HALO) * R * 2 + (uint32_t)CH * D * 2;
 
     // my mode plane in the lane-side stages: plane tl = 2m + (0: Re, 1: Im)
     const int mm = tl >> 1, is_im = tl & 1;
@@ -266,6 +263,22 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[i] = 0.f;
         for (int c0 = hsel * 16; c0 < R + MP; c0 += 32) tmem_st16(tb + lane_base + c0, z);
+        if (hsel == 0) {
+            // conv taps of channels 8*(tl % (R/8)) .. +7, right-aligned: column 32*which + 4*e + jj
+            // multiplies position i - 3 + jj (zero for jj < 4 - W)
+            const int cbl = tl % (R / 8);
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const float *cwg = a.conv_w + ((size_t)(which * H + h) * R + 8 * cbl) * W;
+                float t32[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) t32[4 * e + jj] = jj >= 4 - W ? cwg[e * W + jj - (4 - W)] : 0.f;
+                tmem_st16(tb + lane_base + T::TAPS + 32 * which, t32);
+                tmem_st16(tb + lane_base + T::TAPS + 32 * which + 16, t32 + 16);
+            }
+        }
         tmem_wait_st();
     }
     fence_proxy_async_smem();
@@ -277,8 +290,6 @@ __global__ void __launch_bounds__(NTH, 1)
         tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, -HALO, b, &bar[5]);
         tma_load_4d(sm + S::RAWK, &tm_k, 0, h, -HALO, b, &bar[5]);
         tma_load_4d(sm + S::RAWV, &tm_v, 0, h, 0, b, &bar[5]);
-        bulk_load(sm + S::CWS, taps_q, tap_bytes, &bar[5]);
-        bulk_load(sm + S::CWS + R * 16, taps_k, tap_bytes, &bar[5]);
     }
 
     float eta_r = 0.f, eta_i = 0.f;  // eta of my mode (kept by hsel == 0, Re thread)
@@ -305,26 +316,31 @@ __global__ void __launch_bounds__(NTH, 1)
             // query / key: R/8 channel blocks x (64 R/8 / 256) positions per thread
             constexpr int CBQ = R / 8, PPQ = CH * CBQ / NTH;
             const int cb = tid % CBQ, i0 = (tid / CBQ) * PPQ, c0 = 8 * cb;
+            // rows are stored rotated: at step pp this thread writes position i0 + (pp + rot) % PPQ,
+            // so the channel-block threads of one position hit different banks
+            const int rot = cb % PPQ;
+            float tq[32], tk[32];  // taps of my channel block (TMEM lane tl holds block tl % CBQ == cb)
+            tmem_ld16(tb + lane_base + T::TAPS, tq);
+            tmem_ld16(tb + lane_base + T::TAPS + 16, tq + 16);
+            tmem_ld16(tb + lane_base + T::TAPS + 32, tk);
+            tmem_ld16(tb + lane_base + T::TAPS + 48, tk + 16);
+            float nwk[8], bsk[8];
+            *reinterpret_cast<float4 *>(nwk) = *reinterpret_cast<const float4 *>(nws + c0);
+            *reinterpret_cast<float4 *>(nwk + 4) = *reinterpret_cast<const float4 *>(nws + c0 + 4);
+            *reinterpret_cast<float4 *>(bsk) = *reinterpret_cast<const float4 *>(bss + c0);
+            *reinterpret_cast<float4 *>(bsk + 4) = *reinterpret_cast<const float4 *>(bss + c0 + 4);
+            tmem_wait_ld();
             float fk[PPQ][8];
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 const unsigned char *raw = sm + (which == 0 ? S::RAWQ : S::RAWK);
-                const float *cwg = reinterpret_cast<const float *>(sm + S::CWS + which * R * 16) + c0 * W;
-                // taps right-aligned: w8[e][jj] multiplies position i - 3 + jj (zero for jj < 4 - W)
-                float w8[8][4];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) w8[e][jj] = jj >= 4 - W ? cwg[e * W + jj - (4 - W)] : 0.f;
+                const float *w8 = which == 0 ? tq : tk;
                 // rows i0 .. i0+PPQ+2 of the staged tile = positions i0-3 .. i0+PPQ-1
                 float f[PPQ][8];
-                float acc[PPQ];
 #pragma unroll
-                for (int pp = 0; pp < PPQ; ++pp) {
-                    acc[pp] = 0.f;
+                for (int pp = 0; pp < PPQ; ++pp)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[pp][e] = 0.f;
-                }
 #pragma unroll
                 for (int r = 0; r < PPQ + HALO; ++r) {
                     float x8[8];
@@ -335,27 +351,39 @@ __global__ void __launch_bounds__(NTH, 1)
                         const int jj = r - pp;
                         if (jj >= 0 && jj < 4)
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) f[pp][e] = fmaf(w8[e][jj], x8[e], f[pp][e]);
+                            for (int e = 0; e < 8; ++e) f[pp][e] = fmaf(w8[4 * e + jj], x8[e], f[pp][e]);
                     }
                 }
+                float acc[PPQ];
 #pragma unroll
-                for (int pp = 0; pp < PPQ; ++pp)
+                for (int pp = 0; pp < PPQ; ++pp) {
+                    acc[pp] = 0.f;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         f[pp][e] = silu_fast(f[pp][e]);
                         acc[pp] = fmaf(f[pp][e], f[pp][e], acc[pp]);
                     }
+                }
 #pragma unroll
                 for (int pp = 0; pp < PPQ; ++pp) {
 #pragma unroll
                     for (int o = 1; o < CBQ; o <<= 1) acc[pp] += __shfl_xor_sync(0xffffffffu, acc[pp], o);
-                    const float inv = 1.f / (acc[pp] + IDA_EPS_FEAT);
-                    const int i = i0 + pp;
-                    const bool valid = i < L;
-                    float x8[8];
+                    const float inv = (i0 + pp < L) ? 1.f / (acc[pp] + IDA_EPS_FEAT) : 0.f;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x8[e] = valid ? f[pp][e] * inv : 0.f;
-                    if (which == 0) {
+                    for (int e = 0; e < 8; ++e) f[pp][e] *= inv;
+                }
+                if (which == 0) {
+#pragma unroll
+                    for (int pp = 0; pp < PPQ; ++pp) {
+                        const int q = (pp + rot) % PPQ, i = i0 + q;
+                        float x8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            float v = f[0][e];
+#pragma unroll
+                            for (int u = 1; u < PPQ; ++u) v = q == u ? f[u][e] : v;
+                            x8[e] = v;
+                        }
                         *reinterpret_cast<uint4 *>(sm + S::XQ16 + kmaj_off(i, c0, 2, 128, 16 * R)) = pack_f16x8(x8);
                         uint4 t0v, t1v;
                         t0v.x = __float_as_uint(to_tf32(x8[0])); t0v.y = __float_as_uint(to_tf32(x8[1]));
@@ -364,13 +392,15 @@ __global__ void __launch_bounds__(NTH, 1)
                         t1v.z = __float_as_uint(to_tf32(x8[6])); t1v.w = __float_as_uint(to_tf32(x8[7]));
                         *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0, 4, 128, 32 * R)) = t0v;
                         *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0 + 4, 4, 128, 32 * R)) = t1v;
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) fk[pp][e] = x8[e];
                     }
+                } else {
+#pragma unroll
+                    for (int pp = 0; pp < PPQ; ++pp)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) fk[pp][e] = f[pp][e];
                 }
             }
-            // key RMSNorm + affine; Kt rows and the transposed key rows of Z^T
+            // key RMSNorm + affine; Kt rows (rotated) and the transposed key rows of Z^T
             __align__(16) __half kt_t[8][PPQ];
 #pragma unroll
             for (int pp = 0; pp < PPQ; ++pp) {
@@ -380,13 +410,23 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
                 for (int o = 1; o < CBQ; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
                 const float rk = rsqrtf(ms / R + IDA_EPS_RMS);
-                const int i = i0 + pp;
-                const bool valid = i < L;
+                const bool valid = i0 + pp < L;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    fk[pp][e] = valid ? fmaf(fk[pp][e] * rk, nwk[e], bsk[e]) : 0.f;
+                    kt_t[e][pp] = __float2half_rn(fk[pp][e]);
+                }
+            }
+#pragma unroll
+            for (int pp = 0; pp < PPQ; ++pp) {
+                const int q = (pp + rot) % PPQ, i = i0 + q;
                 float x8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    x8[e] = valid ? fmaf(fk[pp][e] * rk, nws[c0 + e], bss[c0 + e]) : 0.f;
-                    kt_t[e][pp] = __float2half_rn(x8[e]);
+                    float v = fk[0][e];
+#pragma unroll
+                    for (int u = 1; u < PPQ; ++u) v = q == u ? fk[u][e] : v;
+                    x8[e] = v;
                 }
                 *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) = pack_f16x8(x8);
             }
@@ -403,6 +443,11 @@ __global__ void __launch_bounds__(NTH, 1)
             // value: D/8 channel blocks x (64 D/8 / 256) positions per thread
             constexpr int CBV = D / 8, PPV = CH * CBV / NTH;
             const int cb = tid % CBV, i0 = (tid / CBV) * PPV, j0 = 8 * cb;
+            float nwv[8], bsv[8];
+            *reinterpret_cast<float4 *>(nwv) = *reinterpret_cast<const float4 *>(nws + R + j0);
+            *reinterpret_cast<float4 *>(nwv + 4) = *reinterpret_cast<const float4 *>(nws + R + j0 + 4);
+            *reinterpret_cast<float4 *>(bsv) = *reinterpret_cast<const float4 *>(bss + R + j0);
+            *reinterpret_cast<float4 *>(bsv + 4) = *reinterpret_cast<const float4 *>(bss + R + j0 + 4);
             __align__(16) __half vt_t[8][PPV];
 #pragma unroll
             for (int pp = 0; pp < PPV; ++pp) {
@@ -418,7 +463,7 @@ __global__ void __launch_bounds__(NTH, 1)
                 const bool valid = i < L;
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    vt_t[e][pp] = __float2half_rn(valid ? fmaf(x8[e] * rv, nws[R + j0 + e], bss[R + j0 + e]) : 0.f);
+                    vt_t[e][pp] = __float2half_rn(valid ? fmaf(x8[e] * rv, nwv[e], bsv[e]) : 0.f);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -676,8 +721,6 @@ __global__ void __launch_bounds__(NTH, 1)
                 tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, tn - HALO, b, &bar[5]);
                 tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[5]);
                 tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[5]);
-                bulk_load(sm + S::CWS, taps_q, tap_bytes, &bar[5]);
-                bulk_load(sm + S::CWS + R * 16, taps_k, tap_bytes, &bar[5]);
             }
         }
         {
@@ -709,33 +752,40 @@ __global__ void __launch_bounds__(NTH, 1)
             }
             // U (lanes = mode planes): the partner lane holds the other component
             const float2 lm = laml[mm];
+            {
+                constexpr int NB = R / 32;  // 16-column blocks in my half of U
+                float v[NB][16];
 #pragma unroll
-            for (int c0 = hsel * (R / 2); c0 < (hsel + 1) * (R / 2); c0 += 16) {
-                float v[16];
-                tmem_ld16(tb + lane_base + T::U + c0, v);
+                for (int bb = 0; bb < NB; ++bb) tmem_ld16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float o = __shfl_xor_sync(0xffffffffu, v[j], 1);
-                    const float xr = is_im ? o : v[j], xi = is_im ? v[j] : o;
-                    v[j] = is_im ? (lm.x * xi + lm.y * xr) : (lm.x * xr - lm.y * xi);
+                for (int bb = 0; bb < NB; ++bb) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float o = __shfl_xor_sync(0xffffffffu, v[bb][j], 1);
+                        const float xr = is_im ? o : v[bb][j], xi = is_im ? v[bb][j] : o;
+                        v[bb][j] = is_im ? (lm.x * xi + lm.y * xr) : (lm.x * xr - lm.y * xi);
+                    }
+                    tmem_st16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
                 }
-                tmem_st16(tb + lane_base + T::U + c0, v);
             }
             // Gamma^T (lanes = value channels, columns = (Re, Im) per mode)
+            {
+                float v[4][16];
 #pragma unroll
-            for (int c0 = 64 * hsel; c0 < 64 * hsel + 64; c0 += 16) {
-                float v[16];
-                tmem_ld16(tb + lane_base + T::GT + c0, v);
+                for (int bb = 0; bb < 4; ++bb) tmem_ld16(tb + lane_base + T::GT + 64 * hsel + 16 * bb, v[bb]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    const float2 l2 = laml[(c0 + j) >> 1];
-                    const float xr = v[j], xi = v[j + 1];
-                    v[j] = l2.x * xr - l2.y * xi;
-                    v[j + 1] = l2.x * xi + l2.y * xr;
+                for (int bb = 0; bb < 4; ++bb) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        const float2 l2 = laml[(64 * hsel + 16 * bb + j) >> 1];
+                        const float xr = v[bb][j], xi = v[bb][j + 1];
+                        v[bb][j] = l2.x * xr - l2.y * xi;
+                        v[bb][j + 1] = l2.x * xi + l2.y * xr;
+                    }
+                    tmem_st16(tb + lane_base + T::GT + 64 * hsel + 16 * bb, v[bb]);
                 }
-                tmem_st16(tb + lane_base + T::GT + c0, v);
             }
             tmem_wait_st();
         }

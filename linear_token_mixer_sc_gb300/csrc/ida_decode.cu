@@ -200,7 +200,7 @@ __device__ __forceinline__ void step_group(const ModeGroup<NV> &g, float *st, in
 // is loaded while the previous one is being updated, so that each warp keeps
 // its next loads in flight through the arithmetic.
 template <int NV, typename T>
-__global__ void __launch_bounds__(DEC_THREADS, 3) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(DecodeArgs a) {
     __shared__ __align__(16) T xq_s[256];
     __shared__ __align__(16) T z_s[512];
     __shared__ __align__(16) T ored[DEC_WARPS][256];
