@@ -90,7 +90,7 @@ struct ChunkSmem {
     static constexpr int RAWK = RAWQ + RAWQ_BYTES;               // [67][R] bf16
     static constexpr int RAWV = RAWK + RAWQ_BYTES;               // [64][D] bf16
     static_assert(YA16 % 1024 == 0 && RAWV + CH * D * 2 <= MISC, "raw staging must fit over YA16/AP32");
-    static constexpr int BARS = MISC;                            // 6 mbarriers
+    static constexpr int BARS = MISC;                            // 8 mbarriers
     static constexpr int TSLOT = BARS + 64;
     static constexpr int OSC = TSLOT + 16;                       // [64] float: row scales of A2
     static constexpr int LAML = OSC + CH * 4;                    // [64] float2: lambda^L per mode
@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(NTH, 1)
     using S = ChunkSmem<R, D>;
     using T = ChunkTmem<R>;
     extern __shared__ __align__(1024) unsigned char sm[];
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S::BARS);  // 0..4 MMA stages, 5 TMA
+    // mbarriers: 0 G, 1 L^T, 2 A2', 3 O2, 4 state update, 5 TMA, 6 P^T, 7 O1
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S::BARS);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S::TSLOT);
     float *osc = reinterpret_cast<float *>(sm + S::OSC);
     float2 *laml = reinterpret_cast<float2 *>(sm + S::LAML);
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(NTH, 1)
 
     // ---- set-up: barriers, TMEM, per-head constants -----------------------------
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
@@ -304,9 +305,9 @@ __global__ void __launch_bounds__(NTH, 1)
         const int L = min(CH, N - t0);
         const uint32_t par = ci & 1;
 
-        // previous chunk's state update (reads ZT16 / CF16), then this chunk's raw rows
-        if (ci > 0) ok = mbar_wait(&bar[4], par ^ 1);
-        if (ok) ok = mbar_wait(&bar[5], par);
+        // this chunk's raw rows (the previous chunk's state-update MMAs, which read ZT16 and
+        // CF16, are waited for inside the prologue, just before ZT16 is rewritten)
+        ok = mbar_wait(&bar[5], par);
         if (ok) tma_pending = 0;
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
@@ -430,6 +431,7 @@ __global__ void __launch_bounds__(NTH, 1)
                 }
                 *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) = pack_f16x8(x8);
             }
+            if (ci > 0 && !mbar_wait(&bar[4], par ^ 1)) ok = false;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 unsigned char *dst = sm + S::ZT16 + kmaj_off(c0 + e, i0, 2, PADLBO, S::ZT_SBO);
@@ -500,7 +502,7 @@ __global__ void __launch_bounds__(NTH, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        if (__syncthreads_or(!ok)) break;  // also carries a timeout of the in-prologue wait
         tc_fence_after();
 
         // ---- S2: G and P^T ------------------------------------------------------
@@ -510,11 +512,14 @@ __global__ void __launch_bounds__(NTH, 1)
             for (int s = 0; s < R / 16; ++s)
                 mma_f16_ss(tb + T::G, sdesc(sm + S::XQ16 + s * 256, 128, 16 * R),
                            sdesc(sm + S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
+            mma_commit(&bar[0]);
+        } else if (tid == 32) {
+            // P^T from a second issuing thread, so that G's completion is not queued behind it
             const uint32_t idp = idesc(128, 64, 2, 2);
 #pragma unroll
             for (int s = 0; s < R / 8; ++s)
                 mma_tf32_ts(tb + T::PT, tb + T::U + 8 * s, sdesc(sm + S::XQ32 + s * 256, 128, 32 * R), idp, s > 0);
-            mma_commit(&bar[0]);
+            mma_commit(&bar[6]);
         }
         __syncwarp();
         ok = mbar_wait(&bar[0], par);
@@ -522,7 +527,9 @@ __global__ void __launch_bounds__(NTH, 1)
         if (__syncthreads_or(!ok)) break;
 
         // ---- S3: G' = skewed, masked G -----------------------------------------------
-        float *scr = reinterpret_cast<float *>(sm + S::XQ32);  // [64][64] rotated by row; XQ32 is consumed
+        // scratch [64][64] rotated by row, over YA16: the raw tile there is consumed and
+        // YA16 is not rewritten before S5 (XQ32 may still be read by the P^T MMA)
+        float *scr = reinterpret_cast<float *>(sm + S::YA16);
         if (q4 < 2) {
             const int i = tl;
 #pragma unroll
@@ -563,7 +570,7 @@ __global__ void __launch_bounds__(NTH, 1)
             mma_commit(&bar[1]);
         }
         __syncwarp();
-        ok = mbar_wait(&bar[1], par);
+        ok = mbar_wait(&bar[1], par) && mbar_wait(&bar[6], par);
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
 
@@ -644,6 +651,14 @@ __global__ void __launch_bounds__(NTH, 1)
                 mma_f16_ss(tb + T::G, sdesc(sm + S::YA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO),
                            sdesc(sm + S::TA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO), id, s > 0);
             mma_commit(&bar[2]);
+        } else if (tid == 32) {
+            // O2 = Gamma^T . a'^T needs only S5's a' and the state: it runs under S7
+            const uint32_t id32 = idesc(128, 64, 2, 2);
+#pragma unroll
+            for (int s = 0; s < MP / 8; ++s)
+                mma_tf32_ts(tb + T::LT, tb + T::GT + 8 * s, sdesc(sm + S::AP32 + s * 2 * PADLBO, PADLBO, S::AP_SBO),
+                            id32, s > 0);
+            mma_commit(&bar[3]);
         }
         __syncwarp();
         ok = mbar_wait(&bar[2], par);
@@ -651,6 +666,8 @@ __global__ void __launch_bounds__(NTH, 1)
         if (__syncthreads_or(!ok)) break;
 
         // ---- S7: A2 = unskewed, masked A2' (row-scaled fp16) ------------------------------
+        // scratch over XQ32 (P^T, its last reader, is complete)
+        scr = reinterpret_cast<float *>(sm + S::XQ32);
         if (q4 < 2) {
             const int i = tl;
 #pragma unroll
@@ -691,7 +708,7 @@ __global__ void __launch_bounds__(NTH, 1)
         __syncthreads();
         tc_fence_after();
 
-        // ---- S8: O1 = Vt^T . A2^T ; O2 = Gamma^T . a'^T -------------------------------------
+        // ---- S8: O1 = Vt^T . A2^T (O2 was issued with A2') -----------------------------------
         if (tid == 0) {
             const uint32_t id16 = idesc(128, 64, 0, 0);
             const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;  // value rows R .. R+127
@@ -699,15 +716,10 @@ __global__ void __launch_bounds__(NTH, 1)
             for (int s = 0; s < CH / 16; ++s)
                 mma_f16_ss(tb + T::PT, sdesc(sm + vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
                            sdesc(sm + S::A216 + s * 256, 128, 1024), id16, s > 0);
-            const uint32_t id32 = idesc(128, 64, 2, 2);
-#pragma unroll
-            for (int s = 0; s < MP / 8; ++s)
-                mma_tf32_ts(tb + T::LT, tb + T::GT + 8 * s, sdesc(sm + S::AP32 + s * 2 * PADLBO, PADLBO, S::AP_SBO),
-                            id32, s > 0);
-            mma_commit(&bar[3]);
+            mma_commit(&bar[7]);
         }
         __syncwarp();
-        ok = mbar_wait(&bar[3], par);
+        ok = mbar_wait(&bar[7], par) && mbar_wait(&bar[3], par);
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
 
