@@ -174,12 +174,14 @@ class Prefill:
         self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         self.fs = (torch.empty((w.B, w.H, state_floats(w)), dtype=torch.float32, device=dev)
                    if w.final_state else None)
+        # the workspace the library asks for (sequence segments on separate SMs); allocated once
+        self.ws = binding.forward_workspace(self.q, self.v, self.pd, flags)
         self.in_bytes = sum(t.numel() * t.element_size() for t in self.host)
-        self.launches_per_step = 1
+        self.launches_per_step = 1 if self.ws is None else 3  # state pass, segment scan, readout
 
     def step(self):
         self.b.ida_forward(self.q, self.k, self.v, self.pd, out=self.out, final_state=self.fs,
-                           flags=self.flags)
+                           flags=self.flags, workspace=self.ws)
 
     def step_e2e(self):
         for src, dst in zip(self.host, (self.q, self.k, self.v)):

@@ -113,6 +113,34 @@ IDA_API ida_status ida_forward(const void *q, const void *k, const void *v,
                        int W, int flags, ida_stream_t stream);
 
 /*
+ * Prefill with a caller-provided device workspace.  Same arguments and
+ * results as ida_forward, plus:
+ *   workspace        NULL, or a 16-byte aligned device buffer owned by the
+ *                    caller, not shared with a concurrent call;
+ *   workspace_bytes  its size.
+ * With a workspace of at least ida_forward_workspace_bytes(...) bytes the
+ * tensor-core path splits each (b,h) sequence into segments that run on
+ * separate SMs (their local end states, then their start states, are kept
+ * in the workspace); with a smaller or NULL workspace it runs as
+ * ida_forward.  The workspace's contents on entry are ignored.
+ */
+IDA_API ida_status ida_forward_ws(const void *q, const void *k, const void *v,
+                          const float *conv_w, const float *norm_w,
+                          const float *bias, const float *lambda,
+                          const float *Bvec, void *out, float *final_state,
+                          int B, int H, int N, int d, int R, int M, int dtype,
+                          int W, int flags, void *workspace,
+                          size_t workspace_bytes, ida_stream_t stream);
+
+/*
+ * Workspace bytes that let ida_forward_ws split sequences across the SMs of
+ * the current device for this shape; 0 when no split applies (the call then
+ * needs no workspace).  Queries the device (no other CUDA work).
+ */
+IDA_API size_t ida_forward_workspace_bytes(int B, int H, int N, int d, int R,
+                                           int M, int dtype, int W, int flags);
+
+/*
  * One recurrent decode step (one new position per (b,h) unit).
  *   q, k [B, H, R], v [B, H, d] in dtype; parameters as for ida_forward;
  *   state_inout [B, H] x ida_state_floats(...) floats, read and updated in

@@ -19,8 +19,8 @@ IDA_F32, IDA_BF16 = 0, 1
 IDA_READOUT_ETA = 1
 IDA_PATH_SEQUENTIAL = 256
 
-EXPORTED = ("ida_state_floats", "ida_forward", "ida_decode_step", "ida_device_error",
-            "ida_status_str", "ida_last_error")
+EXPORTED = ("ida_state_floats", "ida_forward", "ida_forward_ws", "ida_forward_workspace_bytes",
+            "ida_decode_step", "ida_device_error", "ida_status_str", "ida_last_error")
 
 _lock = threading.Lock()
 _lib = None
@@ -47,6 +47,11 @@ def load() -> ctypes.CDLL:
             L.ida_forward.restype = _i
             L.ida_forward.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _fp,
                                       _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]
+            L.ida_forward_ws.restype = _i
+            L.ida_forward_ws.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _fp,
+                                         _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp]
+            L.ida_forward_workspace_bytes.restype = ctypes.c_size_t
+            L.ida_forward_workspace_bytes.argtypes = [_i] * 9
             L.ida_decode_step.restype = _i
             L.ida_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _fp, _vp,
                                           _i, _i, _i, _i, _i, _i, _i, _i, _vp]
@@ -113,14 +118,20 @@ def _params(p: dict):
     return out
 
 
+def ida_forward_workspace_bytes(B: int, H: int, N: int, d: int, R: int, M: int, dtype: int,
+                                W: int, flags: int = 0) -> int:
+    return int(load().ida_forward_workspace_bytes(B, H, N, d, R, M, dtype, W, flags))
+
+
 def ida_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,
                 out: torch.Tensor | None = None, final_state: torch.Tensor | bool | None = None,
-                flags: int = 0, stream=None):
+                flags: int = 0, stream=None, workspace: torch.Tensor | None = None):
     """Prefill.  q, k [B,N,H,R], v [B,N,H,d] CUDA tensors (fp32/bf16, contiguous).
 
     ``params``: dict of float32 CUDA tensors conv_w [2,H,R,W], norm_w/bias
     [H,R+d], lambda/Bvec [H,M,2].  ``final_state``: a [B,H,S] float32 tensor to
-    fill, True to allocate one, or None.  Returns (out, final_state).
+    fill, True to allocate one, or None.  ``workspace``: optional CUDA tensor
+    (any dtype) handed to ``ida_forward_ws``.  Returns (out, final_state).
     """
     for t in (q, k, v):
         if not (t.is_cuda and t.is_contiguous()):
@@ -143,11 +154,29 @@ def ida_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,
         final_state = None
     if final_state is not None and (final_state.dtype != torch.float32 or final_state.numel() < B * H * S):
         raise ValueError("final_state must be float32 with B*H*ida_state_floats elements")
-    st = load().ida_forward(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv), _p(out),
-                            _p(final_state), B, H, N, d, R, M, dt, W, int(flags),
-                            _stream_handle(stream))
-    _check(st, "ida_forward")
+    if workspace is None:
+        st = load().ida_forward(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv), _p(out),
+                                _p(final_state), B, H, N, d, R, M, dt, W, int(flags),
+                                _stream_handle(stream))
+        _check(st, "ida_forward")
+    else:
+        if not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor")
+        nbytes = workspace.numel() * workspace.element_size()
+        st = load().ida_forward_ws(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv),
+                                   _p(out), _p(final_state), B, H, N, d, R, M, dt, W, int(flags),
+                                   _p(workspace), nbytes, _stream_handle(stream))
+        _check(st, "ida_forward_ws")
     return out, final_state
+
+
+def forward_workspace(q: torch.Tensor, v: torch.Tensor, params: dict, flags: int = 0):
+    """A device workspace sized by ``ida_forward_workspace_bytes`` (None when none applies)."""
+    B, N, H, R = q.shape
+    d = v.shape[3]
+    M, W = params["lambda"].shape[1], params["conv_w"].shape[3]
+    n = ida_forward_workspace_bytes(B, H, N, d, R, M, _dtype_code(q), W, flags)
+    return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=q.device)
 
 
 def ida_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,

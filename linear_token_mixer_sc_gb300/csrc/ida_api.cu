@@ -11,7 +11,8 @@
 namespace ida {
 ida_status launch_seq_prefill(const PrefillArgs &a, cudaStream_t st, int num_sms, std::string &why);
 ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int num_sms, std::string &why,
-                                bool *taken);
+                                bool *taken, void *workspace, size_t workspace_bytes);
+size_t chunk_workspace_bytes(const PrefillArgs &a, int num_sms);
 ida_status launch_decode(const DecodeArgs &a, cudaStream_t st, std::string &why);
 }  // namespace ida
 
@@ -118,10 +119,11 @@ ida_status ida_device_error(unsigned *code) {
     return c ? IDA_ERR_DEVICE : IDA_OK;
 }
 
-ida_status ida_forward(const void *q, const void *k, const void *v, const float *conv_w,
-                       const float *norm_w, const float *bias, const float *lambda,
-                       const float *Bvec, void *out, float *final_state, int B, int H, int N,
-                       int d, int R, int M, int dtype, int W, int flags, ida_stream_t stream) {
+static ida_status forward_impl(const void *q, const void *k, const void *v, const float *conv_w,
+                               const float *norm_w, const float *bias, const float *lambda, const float *Bvec,
+                               void *out, float *final_state, int B, int H, int N, int d, int R, int M,
+                               int dtype, int W, int flags, void *workspace, size_t workspace_bytes,
+                               ida_stream_t stream) {
     std::string why;
     if (B < 0 || H < 0 || N < 0) return fail(IDA_ERR_ARG, "B, H and N must be >= 0");
     ida_status s = check_shape(d, R, M, W, dtype, flags, why);
@@ -137,6 +139,7 @@ ida_status ida_forward(const void *q, const void *k, const void *v, const float 
             if (!aligned16(p)) return fail(IDA_ERR_ARG, "pointers must be 16-byte aligned");
     }
     if (final_state && !aligned16(final_state)) return fail(IDA_ERR_ARG, "final_state must be 16-byte aligned");
+    if (workspace && !aligned16(workspace)) return fail(IDA_ERR_ARG, "workspace must be 16-byte aligned");
     if ((long long)B * H == 0 || (N == 0 && !final_state)) return IDA_OK;
     int num_sms = 0;
     s = device_setup(&num_sms, why);
@@ -157,11 +160,41 @@ ida_status ida_forward(const void *q, const void *k, const void *v, const float 
     a.err = g_err_dev;
     if (!(flags & IDA_PATH_SEQUENTIAL)) {
         bool taken = false;
-        s = ida::launch_chunk_prefill(a, st, num_sms, why, &taken);
+        s = ida::launch_chunk_prefill(a, st, num_sms, why, &taken, workspace, workspace_bytes);
         if (taken) return s == IDA_OK ? IDA_OK : fail(s, why);
     }
     s = ida::launch_seq_prefill(a, st, num_sms, why);
     return s == IDA_OK ? IDA_OK : fail(s, why);
+}
+
+ida_status ida_forward(const void *q, const void *k, const void *v, const float *conv_w,
+                       const float *norm_w, const float *bias, const float *lambda,
+                       const float *Bvec, void *out, float *final_state, int B, int H, int N,
+                       int d, int R, int M, int dtype, int W, int flags, ida_stream_t stream) {
+    return forward_impl(q, k, v, conv_w, norm_w, bias, lambda, Bvec, out, final_state, B, H, N, d, R, M, dtype, W,
+                        flags, nullptr, 0, stream);
+}
+
+ida_status ida_forward_ws(const void *q, const void *k, const void *v, const float *conv_w,
+                          const float *norm_w, const float *bias, const float *lambda,
+                          const float *Bvec, void *out, float *final_state, int B, int H, int N,
+                          int d, int R, int M, int dtype, int W, int flags, void *workspace,
+                          size_t workspace_bytes, ida_stream_t stream) {
+    return forward_impl(q, k, v, conv_w, norm_w, bias, lambda, Bvec, out, final_state, B, H, N, d, R, M, dtype, W,
+                        flags, workspace, workspace_bytes, stream);
+}
+
+size_t ida_forward_workspace_bytes(int B, int H, int N, int d, int R, int M, int dtype, int W, int flags) {
+    std::string why;
+    if (B < 0 || H < 0 || N < 0 || check_shape(d, R, M, W, dtype, flags, why) != IDA_OK) return 0;
+    if (flags & IDA_PATH_SEQUENTIAL) return 0;
+    int dev = 0, num_sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    ida::PrefillArgs a = {};
+    a.B = B; a.H = H; a.N = N; a.d = d; a.R = R; a.M = M; a.W = W; a.dtype = dtype; a.flags = flags;
+    return ida::chunk_workspace_bytes(a, num_sms);
 }
 
 ida_status ida_decode_step(const void *q, const void *k, const void *v, const float *conv_w,

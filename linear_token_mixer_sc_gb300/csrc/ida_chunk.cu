@@ -149,7 +149,8 @@ __device__ __forceinline__ uint4 pack_f16x8(const float x[8]) {
 template <int R, int D>
 __global__ void __launch_bounds__(NTH, 1)
     chunk_prefill_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_q,
-                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         int nseg, int seg_chunks, const float *seg_start) {
     using S = ChunkSmem<R, D>;
     using T = ChunkTmem<R>;
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -167,7 +168,10 @@ __global__ void __launch_bounds__(NTH, 1)
     const int tl = 32 * q4 + lane;                    // my TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const int H = a.H, N = a.N, M = 64, W = a.W;
-    const int unit = blockIdx.x, b = unit / H, h = unit % H;
+    // sequence segment of this CTA: chunks [c_begin, c_end) of unit `unit`
+    const int unit = blockIdx.x / nseg, seg = blockIdx.x % nseg, b = unit / H, h = unit % H;
+    const int nchunks = (N + CH - 1) / CH;
+    const int c_begin = seg * seg_chunks, c_end = min(nchunks, c_begin + seg_chunks);
     const size_t sqk = (size_t)H * R, sv = (size_t)H * D;
     const size_t base_qk = ((size_t)b * N * H + h) * R;
     const size_t base_v = ((size_t)b * N * H + h) * D;
@@ -259,11 +263,15 @@ __global__ void __launch_bounds__(NTH, 1)
     tc_fence_after();
     const uint32_t tb = *tslot;
     {
-        // zero state: U (cols [0,R)) and Gamma^T (cols [R, R+128)), split by column half
-        float z[16];
+        // start state: zero for the first segment, else the state after the previous
+        // segments ([R+128 columns][128 lanes] floats, columns as in TMEM), split by column half
+        const float *x0 = seg > 0 ? seg_start + ((size_t)unit * (nseg - 1) + (seg - 1)) * (size_t)(R + MP) * 128 : nullptr;
+        for (int c0 = hsel * 16; c0 < R + MP; c0 += 32) {
+            float z[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) z[i] = 0.f;
-        for (int c0 = hsel * 16; c0 < R + MP; c0 += 32) tmem_st16(tb + lane_base + c0, z);
+            for (int i = 0; i < 16; ++i) z[i] = x0 ? x0[(size_t)(c0 + i) * 128 + tl] : 0.f;
+            tmem_st16(tb + lane_base + c0, z);
+        }
         if (hsel == 0) {
             // conv taps of channels 8*(tl % (R/8)) .. +7, right-aligned: column 32*which + 4*e + jj
             // multiplies position i - 3 + jj (zero for jj < 4 - W)
@@ -287,23 +295,33 @@ __global__ void __launch_bounds__(NTH, 1)
     __syncthreads();
     tc_fence_after();
     if (tid == 0) {
+        const int tb0 = c_begin * CH;
         mbar_arrive_expect_tx(&bar[5], raw_bytes);
-        tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, -HALO, b, &bar[5]);
-        tma_load_4d(sm + S::RAWK, &tm_k, 0, h, -HALO, b, &bar[5]);
-        tma_load_4d(sm + S::RAWV, &tm_v, 0, h, 0, b, &bar[5]);
+        tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, tb0 - HALO, b, &bar[5]);
+        tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tb0 - HALO, b, &bar[5]);
+        tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tb0, b, &bar[5]);
     }
 
-    float eta_r = 0.f, eta_i = 0.f;  // eta of my mode (kept by hsel == 0, Re thread)
-    int ya_exp = 0;                  // scale exponent of my T_A column currently stored
-    const int nchunks = (N + CH - 1) / CH;
+    // eta of my mode at the segment start, B sum_{k < t_begin} lambda^k (hsel == 0, Re thread)
+    float eta_r = 0.f, eta_i = 0.f;
+    if (hsel == 0 && !is_im) {
+        const float2 ll = laml[mm], sl = suml[mm];
+        for (int c = 0; c < c_begin; ++c) {
+            const float er = ll.x * eta_r - ll.y * eta_i + b_r * sl.x - b_i * sl.y;
+            const float ei = ll.x * eta_i + ll.y * eta_r + b_r * sl.y + b_i * sl.x;
+            eta_r = er;
+            eta_i = ei;
+        }
+    }
+    int ya_exp = 0;  // scale exponent of my T_A column currently stored
     bool ok = true;
     int tma_pending = 1;  // TMA copies issued and not yet waited for
-    int ci = 0;
+    int ci = c_begin;
 
-    for (; ci < nchunks; ++ci) {
+    for (; ci < c_end; ++ci) {
         const int t0 = ci * CH;
         const int L = min(CH, N - t0);
-        const uint32_t par = ci & 1;
+        const uint32_t par = (ci - c_begin) & 1;  // barrier phases count this CTA's chunks
 
         // this chunk's raw rows (the previous chunk's state-update MMAs, which read ZT16 and
         // CF16, are waited for inside the prologue, just before ZT16 is rewritten)
@@ -724,7 +742,7 @@ __global__ void __launch_bounds__(NTH, 1)
         if (__syncthreads_or(!ok)) break;
 
         // ---- S9: next chunk's raw rows; outputs; state scaled by lambda^L -------------------
-        if (ci + 1 < nchunks) {
+        if (ci + 1 < c_end) {
             tma_pending = 1;
             if (tid == 0) {
                 // YA16 / AP32 were last read by the S6 / S8 MMAs, both complete
@@ -824,17 +842,17 @@ __global__ void __launch_bounds__(NTH, 1)
     }
 
     // ---- final state ------------------------------------------------------------------
-    if (ok && nchunks > 0) {
-        ok = mbar_wait(&bar[4], (nchunks - 1) & 1);
+    if (ok && c_end > c_begin) {
+        ok = mbar_wait(&bar[4], (c_end - 1 - c_begin) & 1);
         tc_fence_after();
     }
     ok = !__syncthreads_or(!ok);
     if (!ok) {
         // error path: let a copy still in flight land before the CTA exits
-        if (tma_pending) mbar_wait(&bar[5], (uint32_t)(ci & 1), 200000000LL);
+        if (tma_pending) mbar_wait(&bar[5], (uint32_t)((ci - c_begin) & 1), 200000000LL);
         if (tid == 0) report_error(a.err, kErrWaitTimeout);
     }
-    if (ok && a.final_state) {
+    if (ok && a.final_state && seg == nseg - 1) {
         float *fs = a.final_state + (size_t)unit * a.state_floats;
         const int RD = R + D;
         const size_t plane = (size_t)M * RD;
@@ -882,6 +900,355 @@ __global__ void __launch_bounds__(NTH, 1)
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
+
+// ---- sequence segments: local end states, then their prefix (start states) ----------------
+//
+// With S segments of a unit's sequence, segment s's start state is
+//   X_start(s) = sum_{s' < s} lambda^(positions between the end of s' and the start of s) X_local(s')
+// where X_local(s') is the state segment s' reaches from zero.  chunk_state_kernel
+// computes X_local of every segment but the last (feature prologue for k and v and the
+// state-update MMAs only), segment_scan_kernel turns them into start states in place,
+// and chunk_prefill_kernel then runs every segment of every unit in parallel.  States
+// are kept as [R + 128 columns][128 lanes] floats, the TMEM image of U and Gamma^T.
+
+template <int R, int D>
+struct StateSmem {
+    static constexpr int RAWK = 0;                                    // [67][R] bf16
+    static constexpr int RAWV = align1k((CH + HALO) * R * 2);         // [64][D] bf16
+    static constexpr int ZT16 = RAWV + align1k(CH * D * 2);           // [R+D][64] f16, as in ChunkSmem
+    static constexpr int ZT_SBO = ChunkSmem<R, D>::ZT_SBO;
+    static constexpr int CF16 = ZT16 + (R + D) / 8 * ZT_SBO;          // [128][64] f16 (follows ZT16)
+    static constexpr int BARS = CF16 + MP * CH * 2;                   // 2 mbarriers: TMA, MMA
+    static constexpr int TSLOT = BARS + 16;
+    static constexpr int LAML = TSLOT + 16;                           // [64] float2 lambda^C
+    static constexpr int NWS = LAML + 64 * 8;                         // [R+D] float
+    static constexpr int BSS = NWS + (R + D) * 4;                     // [R+D] float
+    static constexpr int TOTAL = BSS + (R + D) * 4;
+    static_assert(RAWV % 1024 == 0 && TOTAL <= 113 * 1024, "two state-pass CTAs per SM");
+};
+
+template <int R, int D>
+__global__ void __launch_bounds__(NTH, 2)
+    chunk_state_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, int nseg, int seg_chunks, float *seg_state) {
+    using S = StateSmem<R, D>;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S::BARS);  // 0 TMA, 1 MMA
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S::TSLOT);
+    float2 *laml = reinterpret_cast<float2 *>(sm + S::LAML);
+    float *nws = reinterpret_cast<float *>(sm + S::NWS);
+    float *bss = reinterpret_cast<float *>(sm + S::BSS);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hsel = warp >> 2, tl = 32 * q4 + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const int H = a.H, M = 64, W = a.W;
+    const int nloc = nseg - 1;
+    const int unit = blockIdx.x / nloc, sgi = blockIdx.x % nloc, b = unit / H, h = unit % H;
+    const int c_begin = sgi * seg_chunks, c_end = c_begin + seg_chunks;  // full chunks only
+    const uint32_t raw_bytes = (uint32_t)(CH + HALO) * R * 2 + (uint32_t)CH * D * 2;
+    const int mm = tl >> 1, is_im = tl & 1;
+    const float lam_r = a.lambda[((size_t)h * M + mm) * 2], lam_i = a.lambda[((size_t)h * M + mm) * 2 + 1];
+    const float b_r = a.Bvec[((size_t)h * M + mm) * 2], b_i = a.Bvec[((size_t)h * M + mm) * 2 + 1];
+    constexpr uint32_t TU = 0, TG = R;  // TMEM columns of U and Gamma^T
+
+    if ((smem_u32(sm) & 1023u) != 0u) {
+        if (tid == 0) report_error(a.err, kErrShape);
+        return;
+    }
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, 256);
+        tmem_relinquish();
+    }
+    for (int x = tid; x < R + D; x += NTH) {
+        nws[x] = a.norm_w[(size_t)h * (R + D) + x];
+        bss[x] = a.bias[(size_t)h * (R + D) + x];
+    }
+    if (hsel == 0) {
+        float pr = 1.f, pi = 0.f;
+        __align__(16) __half cf[CH];
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const float cr = b_r * pr - b_i * pi, ci = b_r * pi + b_i * pr;
+            cf[CH - 1 - k] = __float2half_rn(is_im ? ci : cr);
+            const float nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
+            pr = nr;
+            pi = ni;
+        }
+        float qr = lam_r, qi = lam_i;
+#pragma unroll
+        for (int sq = 0; sq < 6; ++sq) {
+            const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
+            qr = nr;
+            qi = ni;
+        }
+        if (!is_im) laml[mm] = make_float2(qr, qi);
+#pragma unroll
+        for (int k8 = 0; k8 < CH / 8; ++k8)
+            *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
+                *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
+    }
+    // key conv taps of my channel block, right-aligned (as in the readout kernel)
+    constexpr int CBQ = R / 8, PPQ = CH * CBQ / NTH;
+    const int cb = tid % CBQ, i0 = (tid / CBQ) * PPQ, c0 = 8 * cb;
+    float tk[32];
+    {
+        const float *cwg = a.conv_w + ((size_t)(1 * H + h) * R + c0) * W;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) tk[4 * e + jj] = jj >= 4 - W ? cwg[e * W + jj - (4 - W)] : 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *tslot;
+    {
+        float z[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) z[i] = 0.f;
+        for (int cc = hsel * 16; cc < R + MP; cc += 32) tmem_st16(tb + lane_base + cc, z);
+        tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[0], raw_bytes);
+        tma_load_4d(sm + S::RAWK, &tm_k, 0, h, c_begin * CH - HALO, b, &bar[0]);
+        tma_load_4d(sm + S::RAWV, &tm_v, 0, h, c_begin * CH, b, &bar[0]);
+    }
+    float nwk[8], bsk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        nwk[e] = nws[c0 + e];
+        bsk[e] = bss[c0 + e];
+    }
+    bool ok = true;
+    int tma_pending = 1;
+    int ci = c_begin;
+    for (; ci < c_end; ++ci) {
+        const uint32_t par = (ci - c_begin) & 1;
+        ok = mbar_wait(&bar[0], par);
+        if (ok) tma_pending = 0;
+        if (__syncthreads_or(!ok)) break;
+        // key features: conv, SiLU, squared-norm normalisation, RMSNorm + affine
+        float fk[PPQ][8];
+#pragma unroll
+        for (int pp = 0; pp < PPQ; ++pp)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) fk[pp][e] = 0.f;
+#pragma unroll
+        for (int r = 0; r < PPQ + HALO; ++r) {
+            float x8[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(sm + S::RAWK + ((size_t)(i0 + r) * R + c0) * 2), x8);
+#pragma unroll
+            for (int pp = 0; pp < PPQ; ++pp) {
+                const int jj = r - pp;
+                if (jj >= 0 && jj < 4)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) fk[pp][e] = fmaf(tk[4 * e + jj], x8[e], fk[pp][e]);
+            }
+        }
+        __align__(16) __half kt_t[8][PPQ];
+#pragma unroll
+        for (int pp = 0; pp < PPQ; ++pp) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                fk[pp][e] = silu_fast(fk[pp][e]);
+                acc = fmaf(fk[pp][e], fk[pp][e], acc);
+            }
+#pragma unroll
+            for (int o = 1; o < CBQ; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            const float inv = 1.f / (acc + IDA_EPS_FEAT);
+            float ms = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                fk[pp][e] *= inv;
+                ms = fmaf(fk[pp][e], fk[pp][e], ms);
+            }
+#pragma unroll
+            for (int o = 1; o < CBQ; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
+            const float rk = rsqrtf(ms / R + IDA_EPS_RMS);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) kt_t[e][pp] = __float2half_rn(fmaf(fk[pp][e] * rk, nwk[e], bsk[e]));
+        }
+        // value RMSNorm + affine
+        constexpr int CBV = D / 8, PPV = CH * CBV / NTH;
+        const int cbv = tid % CBV, iv0 = (tid / CBV) * PPV, j0 = 8 * cbv;
+        __align__(16) __half vt_t[8][PPV];
+#pragma unroll
+        for (int pp = 0; pp < PPV; ++pp) {
+            float x8[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(sm + S::RAWV + ((size_t)(iv0 + pp) * D + j0) * 2), x8);
+            float ms = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ms = fmaf(x8[e], x8[e], ms);
+#pragma unroll
+            for (int o = 1; o < CBV; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
+            const float rv = rsqrtf(ms / D + IDA_EPS_RMS);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                vt_t[e][pp] = __float2half_rn(fmaf(x8[e] * rv, nws[R + j0 + e], bss[R + j0 + e]));
+        }
+        // the previous chunk's MMAs read ZT16: wait for them before rewriting it
+        if (ci > c_begin && !mbar_wait(&bar[1], par ^ 1)) ok = false;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            unsigned char *dst = sm + S::ZT16 + kmaj_off(c0 + e, i0, 2, PADLBO, S::ZT_SBO);
+            if (PPQ == 4)
+                *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(kt_t[e]);
+            else
+                *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(kt_t[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            unsigned char *dst = sm + S::ZT16 + kmaj_off(R + j0 + e, iv0, 2, PADLBO, S::ZT_SBO);
+            if (PPV == 4)
+                *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(vt_t[e]);
+            else
+                *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(vt_t[e]);
+        }
+        tc_fence_after();
+        // scale the state by lambda^C (the previous chunk's accumulation is complete)
+        const float2 lm = laml[mm];
+        {
+            constexpr int NB = R / 32;
+            float v[NB][16];
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb) tmem_ld16(tb + lane_base + TU + hsel * (R / 2) + 16 * bb, v[bb]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float o = __shfl_xor_sync(0xffffffffu, v[bb][j], 1);
+                    const float xr = is_im ? o : v[bb][j], xi = is_im ? v[bb][j] : o;
+                    v[bb][j] = is_im ? (lm.x * xi + lm.y * xr) : (lm.x * xr - lm.y * xi);
+                }
+                tmem_st16(tb + lane_base + TU + hsel * (R / 2) + 16 * bb, v[bb]);
+            }
+        }
+        {
+            float v[4][16];
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb) tmem_ld16(tb + lane_base + TG + 64 * hsel + 16 * bb, v[bb]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb) {
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    const float2 l2 = laml[(64 * hsel + 16 * bb + j) >> 1];
+                    const float xr = v[bb][j], xi = v[bb][j + 1];
+                    v[bb][j] = l2.x * xr - l2.y * xi;
+                    v[bb][j + 1] = l2.x * xi + l2.y * xr;
+                }
+                tmem_st16(tb + lane_base + TG + 64 * hsel + 16 * bb, v[bb]);
+            }
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        if (tid == 0) {
+            if (ci + 1 < c_end) {
+                // the raw tiles are consumed: fetch the next chunk's
+                const int tn = (ci + 1) * CH;
+                mbar_arrive_expect_tx(&bar[0], raw_bytes);
+                tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[0]);
+                tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[0]);
+            }
+            const uint32_t idu = idesc(128, R, 0, 0);
+#pragma unroll
+            for (int s = 0; s < CH / 16; ++s)
+                mma_f16_ss(tb + TU, sdesc(sm + S::CF16 + s * 256, 128, 1024),
+                           sdesc(sm + S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, 1);
+            const uint32_t idg = idesc(128, MP, 0, 0);
+            const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;
+#pragma unroll
+            for (int s = 0; s < CH / 16; ++s)
+                mma_f16_ss(tb + TG, sdesc(sm + vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
+                           sdesc(sm + S::CF16 + s * 256, 128, 1024), idg, 1);
+            mma_commit(&bar[1]);
+        }
+        if (ci + 1 < c_end) tma_pending = 1;
+        __syncwarp();
+    }
+    if (ok) {
+        ok = mbar_wait(&bar[1], (c_end - 1 - c_begin) & 1);
+        tc_fence_after();
+    }
+    ok = !__syncthreads_or(!ok);
+    if (!ok) {
+        if (tma_pending) mbar_wait(&bar[0], (uint32_t)((ci - c_begin) & 1), 200000000LL);
+        if (tid == 0) report_error(a.err, kErrWaitTimeout);
+    } else {
+        float *dst = seg_state + ((size_t)unit * nloc + sgi) * (size_t)(R + MP) * 128;
+        for (int cc = hsel * 16; cc < R + MP; cc += 32) {
+            float v[16];
+            tmem_ld16(tb + lane_base + cc, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dst[(size_t)(cc + j) * 128 + tl] = v[j];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 256);
+}
+
+// In place over [unit][segment][R+128][128]: slot s becomes X_start(s + 1).
+__global__ void segment_scan_kernel(const float *lambda, int H, int R, int units, int nseg, int seg_chunks,
+                                    float *seg_state) {
+    const int pairs = 64 * (R + MP);  // complex pairs of one state image
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)units * pairs) return;
+    const int unit = (int)(idx / pairs), r = (int)(idx % pairs), h = unit % H;
+    int m;
+    size_t re, im;
+    if (r < 64 * R) {  // U: column c, lanes 2m (Re) and 2m+1 (Im)
+        const int c = r / 64;
+        m = r % 64;
+        re = (size_t)c * 128 + 2 * m;
+        im = re + 1;
+    } else {  // Gamma^T: lane jv, columns R+2m (Re) and R+2m+1 (Im)
+        const int r2 = r - 64 * R, jv = r2 / 64;
+        m = r2 % 64;
+        re = (size_t)(R + 2 * m) * 128 + jv;
+        im = re + 128;
+    }
+    // g = lambda^(C * seg_chunks) by binary exponentiation
+    float gr = 1.f, gi = 0.f, pr = lambda[((size_t)h * 64 + m) * 2], pi = lambda[((size_t)h * 64 + m) * 2 + 1];
+    for (unsigned e = (unsigned)(CH * seg_chunks); e; e >>= 1) {
+        if (e & 1u) {
+            const float nr = gr * pr - gi * pi, ni = gr * pi + gi * pr;
+            gr = nr;
+            gi = ni;
+        }
+        const float nr = pr * pr - pi * pi, ni = 2.f * pr * pi;
+        pr = nr;
+        pi = ni;
+    }
+    float xr = 0.f, xi = 0.f;
+    for (int s = 0; s < nseg - 1; ++s) {
+        float *p = seg_state + ((size_t)unit * (nseg - 1) + s) * (size_t)(R + MP) * 128;
+        const float nr = gr * xr - gi * xi + p[re], ni = gr * xi + gi * xr + p[im];
+        xr = nr;
+        xi = ni;
+        p[re] = xr;
+        p[im] = xi;
+    }
+}
+
 // ---- host side ---------------------------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -920,24 +1287,65 @@ static bool make_map(EncodeTiledFn fn, CUtensorMap *m, const void *ptr, int B, i
 
 template <int R, int D>
 static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const CUtensorMap &mq,
-                                   const CUtensorMap &mk, const CUtensorMap &mv) {
+                                   const CUtensorMap &mk, const CUtensorMap &mv, int nseg, int seg_chunks,
+                                   float *ws) {
+    const unsigned units = (unsigned)(a.B * a.H);
+    cudaError_t e;
+    if (nseg > 1) {
+        using SS = StateSmem<R, D>;
+        auto sk = chunk_state_kernel<R, D>;
+        e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::TOTAL);
+        if (e != cudaSuccess) return e;
+        sk<<<units * (unsigned)(nseg - 1), NTH, SS::TOTAL, st>>>(a, mk, mv, nseg, seg_chunks, ws);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        const long long pairs = (long long)units * 64 * (R + MP);
+        segment_scan_kernel<<<(unsigned)((pairs + 255) / 256), 256, 0, st>>>(a.lambda, a.H, R, (int)units, nseg,
+                                                                          seg_chunks, ws);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     using S = ChunkSmem<R, D>;
     auto kern = chunk_prefill_kernel<R, D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(a.B * a.H), NTH, S::TOTAL, st>>>(a, mq, mk, mv);
+    kern<<<units * (unsigned)nseg, NTH, S::TOTAL, st>>>(a, mq, mk, mv, nseg, seg_chunks, ws);
     return cudaGetLastError();
+}
+
+static bool chunk_path_takes(const PrefillArgs &a) {
+    if (a.dtype != IDA_BF16 || a.M != 64 || (a.flags & IDA_READOUT_ETA) || a.W > 4) return false;
+    return (a.R == 64 || a.R == 128) && (a.d == 64 || a.d == 128);
+}
+
+// Segments per unit: enough to cover the SMs with one CTA each, at least 8 chunks per segment.
+static void choose_segments(const PrefillArgs &a, int num_sms, int *nseg, int *seg_chunks) {
+    const int nchunks = (a.N + CH - 1) / CH;
+    const long long units = (long long)a.B * a.H;
+    int s = (int)(num_sms / (units > 0 ? units : 1));
+    if (s > nchunks / 8) s = nchunks / 8;
+    if (s < 1) s = 1;
+    const int sc = (nchunks + s - 1) / s;
+    *seg_chunks = sc;
+    *nseg = (nchunks + sc - 1) / sc;
+}
+
+size_t chunk_workspace_bytes(const PrefillArgs &a, int num_sms) {
+    if (!chunk_path_takes(a) || a.N <= 0) return 0;
+    int nseg, sc;
+    choose_segments(a, num_sms, &nseg, &sc);
+    return (size_t)a.B * a.H * (size_t)(nseg - 1) * (size_t)(a.R + MP) * 128 * sizeof(float);
 }
 
 // Takes bf16 prefill with M = 64 modes and R, d in {64, 128}, denominator-free
 // readout.  The eta readout divides by Re(xi(q)^T U^T eta), which on the
 // synthetic workloads comes within 1e-5 of its scale; fp16 / tf32 operand
 // rounding then dominates the quotient, so that readout, and every other
-// shape, is served by the fp32 sequential kernel.
-ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int, std::string &why, bool *taken) {
+// shape, is served by the fp32 sequential kernel.  With a workspace of
+// chunk_workspace_bytes() the sequence of each unit is split into segments
+// that run on separate SMs; without one, one CTA walks each unit.
+ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int num_sms, std::string &why, bool *taken,
+                                void *workspace, size_t workspace_bytes) {
     *taken = false;
-    if (a.dtype != IDA_BF16 || a.M != 64 || (a.flags & IDA_READOUT_ETA) || a.W > 4) return IDA_OK;
-    if (!((a.R == 64 || a.R == 128) && (a.d == 64 || a.d == 128))) return IDA_OK;
+    if (!chunk_path_takes(a)) return IDA_OK;
     EncodeTiledFn fn = encode_fn(why);
     if (!fn) return IDA_OK;  // no tensor-map support: the sequential kernel serves
     CUtensorMap mq, mk, mv;
@@ -946,16 +1354,20 @@ ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int, std:
         why = "cuTensorMapEncodeTiled rejected the q/k/v layout";
         return IDA_OK;
     }
+    int nseg = 1, seg_chunks = (a.N + CH - 1) / CH;
+    if (workspace && workspace_bytes >= chunk_workspace_bytes(a, num_sms) && chunk_workspace_bytes(a, num_sms) > 0)
+        choose_segments(a, num_sms, &nseg, &seg_chunks);
+    float *ws = nseg > 1 ? static_cast<float *>(workspace) : nullptr;
     *taken = true;
     cudaError_t e;
     if (a.R == 128 && a.d == 128)
-        e = launch_chunk_rd<128, 128>(a, st, mq, mk, mv);
+        e = launch_chunk_rd<128, 128>(a, st, mq, mk, mv, nseg, seg_chunks, ws);
     else if (a.R == 64 && a.d == 64)
-        e = launch_chunk_rd<64, 64>(a, st, mq, mk, mv);
+        e = launch_chunk_rd<64, 64>(a, st, mq, mk, mv, nseg, seg_chunks, ws);
     else if (a.R == 128 && a.d == 64)
-        e = launch_chunk_rd<128, 64>(a, st, mq, mk, mv);
+        e = launch_chunk_rd<128, 64>(a, st, mq, mk, mv, nseg, seg_chunks, ws);
     else
-        e = launch_chunk_rd<64, 128>(a, st, mq, mk, mv);
+        e = launch_chunk_rd<64, 128>(a, st, mq, mk, mv, nseg, seg_chunks, ws);
     if (e != cudaSuccess) {
         why = std::string("chunked prefill launch: ") + cudaGetErrorString(e);
         return IDA_ERR_CUDA;

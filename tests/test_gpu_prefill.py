@@ -105,14 +105,17 @@ def test_state_padding_is_zero():
     assert torch.count_nonzero(fs[..., n:]).item() == 0
 
 
-def _sampled(w, units, flags, final_state=False, path=0):
-    """Full-size workload on the GPU, oracle on the sampled units only."""
+def _sampled(w, units, flags, final_state=False, path=0, workspace=True):
+    """Full-size workload on the GPU (through ida_forward_ws with the workspace
+    the library asks for, as the benchmark runs it), oracle on the sampled units."""
     dev = torch.device("cuda")
     p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
     q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed)
     pd = binding.params_to_device(p)
-    out, fs = binding.ida_forward(q.to(dev), k.to(dev), v.to(dev), pd, flags=flags | path,
-                                  final_state=final_state)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    ws = binding.forward_workspace(qd, vd, pd, flags | path) if workspace else None
+    out, fs = binding.ida_forward(qd, kd, vd, pd, flags=flags | path, final_state=final_state,
+                                  workspace=ws)
     torch.cuda.synchronize()
     assert binding.ida_device_error() == 0
     ref = orc.forward(q, k, v, p, flags=flags, final_state=final_state, units=units, want_den=True)
@@ -163,3 +166,32 @@ def test_eta_readout_constant_values_on_gpu(path):
     # and the oracle's value is the constant row itself
     np.testing.assert_allclose(ref["out"], np.broadcast_to(ref["out"][:, :1], ref["out"].shape),
                                rtol=1e-6, atol=1e-8)
+
+
+@pytest.mark.parametrize("shape", [(1, 64 * 40 + 17, 2, 128, 128), (2, 64 * 33, 1, 64, 128),
+                                   (1, 64 * 24 + 1, 3, 128, 64)],
+                         ids=lambda s: "B{}N{}H{}R{}d{}".format(*s))
+def test_segmented_prefill(shape):
+    """Sequences split into segments on separate SMs (workspace path) match the
+    oracle, including a ragged last chunk and the final state."""
+    B, N, H, R, d = shape
+    q, k, v, p = problem(B, N, H, R, d, 64, 4, "bf16", seed=300 + N)
+    dev = torch.device("cuda")
+    pd = binding.params_to_device(p)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    nbytes = binding.ida_forward_workspace_bytes(B, H, N, d, R, 64, binding.IDA_BF16, 4)
+    assert nbytes > 0, "this shape should be split into segments"
+    ws = torch.full((nbytes,), 255, dtype=torch.uint8, device=dev)  # contents on entry are ignored
+    out, fs = binding.ida_forward(qd, kd, vd, pd, final_state=True, workspace=ws)
+    out1, fs1 = binding.ida_forward(qd, kd, vd, pd, final_state=True)
+    torch.cuda.synchronize()
+    assert binding.ida_device_error() == 0
+    ref = orc.forward(q, k, v, p, final_state=True)
+    assert rel_l2(to_np(out), ref["out"]) <= BF16_REL_L2
+    assert rel_l2(unpadded_state(to_np(fs), d, R, 64, 4), ref["final_state"]) <= BF16_REL_L2
+    # the single-CTA-per-unit path computes the same thing
+    assert rel_l2(to_np(out), to_np(out1)) <= 2e-3
+    # a too-small workspace falls back to one CTA per unit
+    out2, _ = binding.ida_forward(qd, kd, vd, pd, workspace=ws[:16])
+    torch.cuda.synchronize()
+    assert rel_l2(to_np(out2), to_np(out1)) == 0.0
