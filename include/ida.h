@@ -141,6 +141,35 @@ IDA_API size_t ida_forward_workspace_bytes(int B, int H, int N, int d, int R,
                                            int M, int dtype, int W, int flags);
 
 /*
+ * Prefill for callers that cannot allocate device memory.  (The paper has no
+ * counterpart: this is a property of the library, not of the method.)
+ *
+ * Same arguments and results as ida_forward; it runs what ida_forward_ws
+ * runs with a sufficient workspace, but takes that workspace from one array
+ * of static device memory built into this library instead of from the
+ * caller.  Use it where the calling code may not allocate: a plug-in that a
+ * host framework hands only its input and output buffers, a serving loop
+ * that must not touch the allocator after start-up, code with no allocator
+ * in reach.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Limit: the array holds 32 MiB on every GPU that loads the library,
+ *     kept until the process exits.  A shape whose scratch need
+ *     (ida_forward_workspace_bytes) exceeds it returns IDA_ERR_UNSUPPORTED
+ *     with the sizes in ida_last_error().
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; nothing in it needs to start at zero, but calls that overlap
+ *     on the GPU (e.g. on two streams) race on it.
+ */
+IDA_API ida_status ida_forward_noalloc(const void *q, const void *k, const void *v,
+                               const float *conv_w, const float *norm_w,
+                               const float *bias, const float *lambda,
+                               const float *Bvec, void *out, float *final_state,
+                               int B, int H, int N, int d, int R, int M,
+                               int dtype, int W, int flags, ida_stream_t stream);
+
+/*
  * One recurrent decode step (one new position per (b,h) unit).
  *   q, k [B, H, R], v [B, H, d] in dtype; parameters as for ida_forward;
  *   state_inout [B, H] x ida_state_floats(...) floats, read and updated in

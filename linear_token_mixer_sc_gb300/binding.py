@@ -20,7 +20,8 @@ IDA_READOUT_ETA = 1
 IDA_PATH_SEQUENTIAL = 256
 
 EXPORTED = ("ida_state_floats", "ida_forward", "ida_forward_ws", "ida_forward_workspace_bytes",
-            "ida_decode_step", "ida_device_error", "ida_status_str", "ida_last_error")
+            "ida_forward_noalloc", "ida_decode_step", "ida_device_error", "ida_status_str",
+            "ida_last_error")
 
 _lock = threading.Lock()
 _lib = None
@@ -52,6 +53,9 @@ def load() -> ctypes.CDLL:
                                          _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp]
             L.ida_forward_workspace_bytes.restype = ctypes.c_size_t
             L.ida_forward_workspace_bytes.argtypes = [_i] * 9
+            L.ida_forward_noalloc.restype = _i
+            L.ida_forward_noalloc.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _fp,
+                                              _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]
             L.ida_decode_step.restype = _i
             L.ida_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _fp, _vp,
                                           _i, _i, _i, _i, _i, _i, _i, _i, _vp]
@@ -167,6 +171,27 @@ def ida_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,
                                    _p(out), _p(final_state), B, H, N, d, R, M, dt, W, int(flags),
                                    _p(workspace), nbytes, _stream_handle(stream))
         _check(st, "ida_forward_ws")
+    return out, final_state
+
+
+def ida_forward_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,
+                        out: torch.Tensor, final_state: torch.Tensor | None = None, flags: int = 0,
+                        stream=None):
+    """Prefill through ``ida_forward_noalloc``: for callers that may not allocate device
+    memory, so ``out`` (and ``final_state``, if wanted) must be passed in; the scratch is
+    the library's static device array.  Marshalling only, like ``ida_forward``."""
+    for t in (q, k, v, out):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("q, k, v and out must be contiguous CUDA tensors")
+    dt = _dtype_code(q)
+    B, N, H, R = q.shape
+    d = v.shape[3]
+    cw, nw, bs, lam, bv = _params(params)
+    M, W = lam.shape[1], cw.shape[3]
+    st = load().ida_forward_noalloc(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv),
+                                    _p(out), _p(final_state), B, H, N, d, R, M, dt, W, int(flags),
+                                    _stream_handle(stream))
+    _check(st, "ida_forward_noalloc")
     return out, final_state
 
 

@@ -88,6 +88,15 @@ ida_status check_shape(int d, int R, int M, int W, int dtype, int flags, std::st
 
 }  // namespace
 
+namespace ida {
+// Library-internal hooks for entry points defined in other files.
+ida_status forward_entry(const void *q, const void *k, const void *v, const float *conv_w, const float *norm_w,
+                         const float *bias, const float *lambda, const float *Bvec, void *out, float *final_state,
+                         int B, int H, int N, int d, int R, int M, int dtype, int W, int flags, void *workspace,
+                         size_t workspace_bytes, ida_stream_t stream);
+ida_status fail_with(ida_status s, const std::string &why) { return fail(s, why); }
+}  // namespace ida
+
 extern "C" {
 
 size_t ida_state_floats(int d, int R, int M, int W) {
@@ -119,11 +128,12 @@ ida_status ida_device_error(unsigned *code) {
     return c ? IDA_ERR_DEVICE : IDA_OK;
 }
 
-static ida_status forward_impl(const void *q, const void *k, const void *v, const float *conv_w,
-                               const float *norm_w, const float *bias, const float *lambda, const float *Bvec,
-                               void *out, float *final_state, int B, int H, int N, int d, int R, int M,
-                               int dtype, int W, int flags, void *workspace, size_t workspace_bytes,
-                               ida_stream_t stream) {
+}  // extern "C"
+
+ida_status ida::forward_entry(const void *q, const void *k, const void *v, const float *conv_w,
+                              const float *norm_w, const float *bias, const float *lambda, const float *Bvec,
+                              void *out, float *final_state, int B, int H, int N, int d, int R, int M, int dtype,
+                              int W, int flags, void *workspace, size_t workspace_bytes, ida_stream_t stream) {
     std::string why;
     if (B < 0 || H < 0 || N < 0) return fail(IDA_ERR_ARG, "B, H and N must be >= 0");
     ida_status s = check_shape(d, R, M, W, dtype, flags, why);
@@ -167,12 +177,14 @@ static ida_status forward_impl(const void *q, const void *k, const void *v, cons
     return s == IDA_OK ? IDA_OK : fail(s, why);
 }
 
+extern "C" {
+
 ida_status ida_forward(const void *q, const void *k, const void *v, const float *conv_w,
                        const float *norm_w, const float *bias, const float *lambda,
                        const float *Bvec, void *out, float *final_state, int B, int H, int N,
                        int d, int R, int M, int dtype, int W, int flags, ida_stream_t stream) {
-    return forward_impl(q, k, v, conv_w, norm_w, bias, lambda, Bvec, out, final_state, B, H, N, d, R, M, dtype, W,
-                        flags, nullptr, 0, stream);
+    return ida::forward_entry(q, k, v, conv_w, norm_w, bias, lambda, Bvec, out, final_state, B, H, N, d, R, M,
+                              dtype, W, flags, nullptr, 0, stream);
 }
 
 ida_status ida_forward_ws(const void *q, const void *k, const void *v, const float *conv_w,
@@ -180,8 +192,8 @@ ida_status ida_forward_ws(const void *q, const void *k, const void *v, const flo
                           const float *Bvec, void *out, float *final_state, int B, int H, int N,
                           int d, int R, int M, int dtype, int W, int flags, void *workspace,
                           size_t workspace_bytes, ida_stream_t stream) {
-    return forward_impl(q, k, v, conv_w, norm_w, bias, lambda, Bvec, out, final_state, B, H, N, d, R, M, dtype, W,
-                        flags, workspace, workspace_bytes, stream);
+    return ida::forward_entry(q, k, v, conv_w, norm_w, bias, lambda, Bvec, out, final_state, B, H, N, d, R, M,
+                              dtype, W, flags, workspace, workspace_bytes, stream);
 }
 
 size_t ida_forward_workspace_bytes(int B, int H, int N, int d, int R, int M, int dtype, int W, int flags) {
