@@ -340,6 +340,9 @@ def oracle_sample(w, budget_s: float, cores: int, flags: int = 0):
 # ---------------------------------------------------------------- main
 
 def dist_setup(n_gpus):
+    """One process per GPU under torchrun: every rank runs the same per-GPU
+    workload (weak scaling over independent (b,h) units); ranks exchange only
+    their timings, never data."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
         import torch.distributed as dist
@@ -351,11 +354,17 @@ def dist_setup(n_gpus):
 
 
 def max_over_ranks(dist, x: float, dev) -> float:
+    """The slowest rank's time (the job's time), on every rank."""
     if dist is None:
         return x
     t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(world_size: int, tokens_per_rank: int, ms_max: float) -> float:
+    """Whole-job tokens/s: all ranks' tokens over the slowest rank's step time."""
+    return world_size * tokens_per_rank / (ms_max * 1e-3)
 
 
 def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e2e=True, seed_len=None):
@@ -372,7 +381,7 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e
     wall = time.perf_counter() - wall0
     ms = sum(times) / len(times)
     ms_all = max_over_ranks(dist, ms, dev)
-    value = ws * runner.tokens() / (ms_all * 1e-3)
+    value = job_value(ws, runner.tokens(), ms_all)
     res = {"value": value, "ms_per_step": ms_all, "tokens_per_step": runner.tokens(),
            "flush_l2": flush, "wall_s": wall,
            "roofline": roofline(runner, ms, peaks, peak_kind, traffic_record(w.name, sources)),
@@ -381,7 +390,7 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e
         et = time_steps(runner, max(3, steps // 2), 2, dev, False, e2e=True)
         ems = max_over_ranks(dist, sum(et) / len(et), dev)
         bi, bo = runner.e2e_bytes()
-        res["e2e"] = {"value": ws * runner.tokens() / (ems * 1e-3), "unit": "tokens/s",
+        res["e2e"] = {"value": job_value(ws, runner.tokens(), ems), "unit": "tokens/s",
                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                       "ms_per_step": ems}
     return res
