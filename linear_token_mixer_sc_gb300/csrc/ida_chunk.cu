@@ -90,6 +90,7 @@ struct ChunkSmem {
     static constexpr int RAWK = RAWQ + RAWQ_BYTES;               // [67][R] bf16
     static constexpr int RAWV = RAWK + RAWQ_BYTES;               // [64][D] bf16
     static_assert(YA16 % 1024 == 0 && RAWV + CH * D * 2 <= MISC, "raw staging must fit over YA16/AP32");
+    static_assert(XQ32 % 1024 == 0 && CH * D * 2 <= CH * R * 4, "the [64][D] output tile is staged over XQ32");
     static constexpr int BARS = MISC;                            // 8 mbarriers
     static constexpr int TSLOT = BARS + 64;
     static constexpr int OSC = TSLOT + 16;                       // [64] float: row scales of A2
@@ -150,7 +151,8 @@ template <int R, int D>
 __global__ void __launch_bounds__(NTH, 1)
     chunk_prefill_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                         int nseg, int seg_chunks, const float *seg_start) {
+                         const __grid_constant__ CUtensorMap tm_o, int nseg, int seg_chunks,
+                         const float *seg_start) {
     using S = ChunkSmem<R, D>;
     using T = ChunkTmem<R>;
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -172,12 +174,10 @@ __global__ void __launch_bounds__(NTH, 1)
     const int unit = blockIdx.x / nseg, seg = blockIdx.x % nseg, b = unit / H, h = unit % H;
     const int nchunks = (N + CH - 1) / CH;
     const int c_begin = seg * seg_chunks, c_end = min(nchunks, c_begin + seg_chunks);
-    const size_t sqk = (size_t)H * R, sv = (size_t)H * D;
+    const size_t sqk = (size_t)H * R;
     const size_t base_qk = ((size_t)b * N * H + h) * R;
-    const size_t base_v = ((size_t)b * N * H + h) * D;
     const __nv_bfloat16 *gq = reinterpret_cast<const __nv_bfloat16 *>(a.q);
     const __nv_bfloat16 *gk = reinterpret_cast<const __nv_bfloat16 *>(a.k);
-    __nv_bfloat16 *gout = reinterpret_cast<__nv_bfloat16 *>(a.out);
     const uint32_t raw_bytes = 2u * (CH + HALO) * R * 2 + (uint32_t)CH * D * 2;
 
     // my mode plane in the lane-side stages: plane tl = 2m + (0: Re, 1: Im)
@@ -327,6 +327,7 @@ __global__ void __launch_bounds__(NTH, 1)
         // CF16, are waited for inside the prologue, just before ZT16 is rewritten)
         ok = mbar_wait(&bar[5], par);
         if (ok) tma_pending = 0;
+        if (tid == 0) bulk_wait_read_all();  // the previous output tile has left XQ32
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
 
@@ -595,11 +596,18 @@ __global__ void __launch_bounds__(NTH, 1)
         // ---- S5: a, Ya (fp16, column-scaled), a' (tf32); plane tl, positions of my half
         {
             float *ymx = reinterpret_cast<float *>(sm + S::GP16);  // [2][128]; GP16 is consumed
+            // Complex products in (own, partner) components: this lane's plane and its partner
+            // lane's.  With s = +1 on an Im plane and -1 on a Re plane, for z = (zo, zp) and
+            // w = (wr, wi):  own(z w) = zo wr + zp (s wi),  partner(z w) = zp wr - zo (s wi).
+            // The operands hold (Re, -Im) per mode, i.e. -s times the own component.
+            const float sg = is_im ? 1.f : -1.f;
+            const float bs = sg * b_i, ls = sg * lam_i;
+            const float ya_r = -sg * b_r, ya_p = -b_i;  // Ya = -s own(a B)
             float ya[32];
-            float wr = l33r, wi = l33i;  // lambda^(i+1)
+            float wr = l33r, ws = sg * l33i;  // lambda^(i+1) as (Re, s Im)
             if (hsel == 0) {
                 wr = lam_r;
-                wi = lam_i;
+                ws = ls;
             }
             float ymax = 0.f;
 #pragma unroll
@@ -614,21 +622,17 @@ __global__ void __launch_bounds__(NTH, 1)
                     const int i = c0 + j;
                     const float po = __shfl_xor_sync(0xffffffffu, pv[j], 1);
                     const float lo = __shfl_xor_sync(0xffffffffu, lv[j], 1);
-                    const float pr = is_im ? po : pv[j], pim = is_im ? pv[j] : po;
-                    const float lr = is_im ? lo : lv[j], lim = is_im ? lv[j] : lo;
                     // a = lambda^(i+1) P + B L
-                    const float ar = wr * pr - wi * pim + b_r * lr - b_i * lim;
-                    const float ai = wr * pim + wi * pr + b_r * lim + b_i * lr;
-                    // Ya = a B ; a' = a lambda^(i+1); operands hold (Re, -Im) per mode
-                    const float yr = ar * b_r - ai * b_i, yi = ar * b_i + ai * b_r;
-                    const float qr = ar * wr - ai * wi, qi = ar * wi + ai * wr;
-                    ya[16 * cc + j] = is_im ? -yi : yr;
+                    const float ao = fmaf(pv[j], wr, fmaf(po, ws, fmaf(lv[j], b_r, lo * bs)));
+                    const float ap = fmaf(po, wr, fmaf(-pv[j], ws, fmaf(lo, b_r, -lv[j] * bs)));
+                    // Ya = a B ; a' = a lambda^(i+1)
+                    ya[16 * cc + j] = fmaf(ao, ya_r, ap * ya_p);
                     ymax = fmaxf(ymax, fabsf(ya[16 * cc + j]));
                     *reinterpret_cast<float *>(sm + S::AP32 + kmaj_off(i, tl, 4, PADLBO, S::AP_SBO)) =
-                        to_tf32(is_im ? -qi : qr);
-                    const float nr = wr * lam_r - wi * lam_i, ni = wr * lam_i + wi * lam_r;
+                        to_tf32(-sg * fmaf(ao, wr, ap * ws));
+                    const float nr = fmaf(wr, lam_r, -ws * ls), ns = fmaf(wr, ls, ws * lam_r);
                     wr = nr;
-                    wi = ni;
+                    ws = ns;
                 }
             }
             ymx[hsel * 128 + tl] = ymax;
@@ -754,23 +758,26 @@ __global__ void __launch_bounds__(NTH, 1)
             }
         }
         {
+            // outputs o[i][jv] into the [64][D] bf16 store tile over XQ32 (free until the next
+            // prologue; thread 0 waits for the tile's bulk store before that prologue starts)
             const int jv = tl;
+            __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + S::XQ32);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c0 = 32 * hsel + 16 * cc;
-                float o1[16], o2[16];
+                float o1[16], o2[16], s16[16];
                 tmem_ld16(tb + lane_base + T::PT + c0, o1);
                 tmem_ld16(tb + lane_base + T::LT + c0, o2);
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4)
+                    *reinterpret_cast<float4 *>(s16 + 4 * j4) = *reinterpret_cast<const float4 *>(osc + c0 + 4 * j4);
                 tmem_wait_ld();
                 if (jv < D) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int i = c0 + j;
-                        if (i < L)
-                            gout[base_v + (size_t)(t0 + i) * sv + jv] = __float2bfloat16_rn(fmaf(o1[j], osc[i], o2[j]));
-                    }
+                    for (int j = 0; j < 16; ++j) otile[(c0 + j) * D + jv] = __float2bfloat16_rn(fmaf(o1[j], s16[j], o2[j]));
                 }
             }
+            fence_proxy_async_smem();
             if (hsel == 0 && !is_im) {
                 // eta <- lambda^L eta + B sum_{k<L} lambda^k
                 const float2 ll = laml[mm], sl = suml[mm];
@@ -788,13 +795,14 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
                 for (int bb = 0; bb < NB; ++bb) tmem_ld16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
                 tmem_wait_ld();
+                // own(lambda^L x) = own(x) Re lambda^L + partner(x) s Im lambda^L, s = +1 on Im planes
+                const float lms = is_im ? lm.y : -lm.y;
 #pragma unroll
                 for (int bb = 0; bb < NB; ++bb) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const float o = __shfl_xor_sync(0xffffffffu, v[bb][j], 1);
-                        const float xr = is_im ? o : v[bb][j], xi = is_im ? v[bb][j] : o;
-                        v[bb][j] = is_im ? (lm.x * xi + lm.y * xr) : (lm.x * xr - lm.y * xi);
+                        v[bb][j] = fmaf(v[bb][j], lm.x, o * lms);
                     }
                     tmem_st16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
                 }
@@ -825,6 +833,9 @@ __global__ void __launch_bounds__(NTH, 1)
 
         // ---- S10: U += Coef . Kt ; Gamma^T += Vt^T . Coef^T -----------------------------------
         if (tid == 0) {
+            // the chunk's output rows; rows past N are clipped by the copy
+            tma_store_4d(&tm_o, 0, h, t0, b, sm + S::XQ32);
+            bulk_commit();
             const uint32_t idu = idesc(128, R, 0, 0);
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
@@ -842,6 +853,7 @@ __global__ void __launch_bounds__(NTH, 1)
     }
 
     // ---- final state ------------------------------------------------------------------
+    if (tid == 0) bulk_wait_all();  // output stores complete before shared memory is released
     if (ok && c_end > c_begin) {
         ok = mbar_wait(&bar[4], (c_end - 1 - c_begin) & 1);
         tc_fence_after();
@@ -1287,8 +1299,8 @@ static bool make_map(EncodeTiledFn fn, CUtensorMap *m, const void *ptr, int B, i
 
 template <int R, int D>
 static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const CUtensorMap &mq,
-                                   const CUtensorMap &mk, const CUtensorMap &mv, int nseg, int seg_chunks,
-                                   float *ws) {
+                                   const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo, int nseg,
+                                   int seg_chunks, float *ws) {
     const unsigned units = (unsigned)(a.B * a.H);
     cudaError_t e;
     if (nseg > 1) {
@@ -1307,7 +1319,7 @@ static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const 
     auto kern = chunk_prefill_kernel<R, D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
     if (e != cudaSuccess) return e;
-    kern<<<units * (unsigned)nseg, NTH, S::TOTAL, st>>>(a, mq, mk, mv, nseg, seg_chunks, ws);
+    kern<<<units * (unsigned)nseg, NTH, S::TOTAL, st>>>(a, mq, mk, mv, mo, nseg, seg_chunks, ws);
     return cudaGetLastError();
 }
 
@@ -1348,10 +1360,11 @@ ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int num_s
     if (!chunk_path_takes(a)) return IDA_OK;
     EncodeTiledFn fn = encode_fn(why);
     if (!fn) return IDA_OK;  // no tensor-map support: the sequential kernel serves
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(fn, &mq, a.q, a.B, a.N, a.H, a.R, CH + HALO) ||
-        !make_map(fn, &mk, a.k, a.B, a.N, a.H, a.R, CH + HALO) || !make_map(fn, &mv, a.v, a.B, a.N, a.H, a.d, CH)) {
-        why = "cuTensorMapEncodeTiled rejected the q/k/v layout";
+        !make_map(fn, &mk, a.k, a.B, a.N, a.H, a.R, CH + HALO) || !make_map(fn, &mv, a.v, a.B, a.N, a.H, a.d, CH) ||
+        !make_map(fn, &mo, a.out, a.B, a.N, a.H, a.d, CH)) {
+        why = "cuTensorMapEncodeTiled rejected the q/k/v/out layout";
         return IDA_OK;
     }
     int nseg = 1, seg_chunks = (a.N + CH - 1) / CH;
@@ -1361,13 +1374,13 @@ ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int num_s
     *taken = true;
     cudaError_t e;
     if (a.R == 128 && a.d == 128)
-        e = launch_chunk_rd<128, 128>(a, st, mq, mk, mv, nseg, seg_chunks, ws);
+        e = launch_chunk_rd<128, 128>(a, st, mq, mk, mv, mo, nseg, seg_chunks, ws);
     else if (a.R == 64 && a.d == 64)
-        e = launch_chunk_rd<64, 64>(a, st, mq, mk, mv, nseg, seg_chunks, ws);
+        e = launch_chunk_rd<64, 64>(a, st, mq, mk, mv, mo, nseg, seg_chunks, ws);
     else if (a.R == 128 && a.d == 64)
-        e = launch_chunk_rd<128, 64>(a, st, mq, mk, mv, nseg, seg_chunks, ws);
+        e = launch_chunk_rd<128, 64>(a, st, mq, mk, mv, mo, nseg, seg_chunks, ws);
     else
-        e = launch_chunk_rd<64, 128>(a, st, mq, mk, mv, nseg, seg_chunks, ws);
+        e = launch_chunk_rd<64, 128>(a, st, mq, mk, mv, mo, nseg, seg_chunks, ws);
     if (e != cudaSuccess) {
         why = std::string("chunked prefill launch: ") + cudaGetErrorString(e);
         return IDA_ERR_CUDA;
