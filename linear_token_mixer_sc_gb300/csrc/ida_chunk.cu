@@ -129,7 +129,24 @@ __device__ __forceinline__ int down_exp(float x) {
     return e > 15 ? 15 : e;
 }
 
-__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+// SiLU with one special-function op: x sigmoid(x) = h + h tanh(h), h = x / 2, through the
+// hardware tanh approximation (relative error about 2^-11, below the fp16 rounding of every
+// operand built from it)
+__device__ __forceinline__ float silu_tanh(float x) {
+    const float h = 0.5f * x;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
+
+// x rounded to the tf32 grid (10 mantissa bits), nearest with ties away from zero, as bits
+__device__ __forceinline__ uint32_t tf32_bits(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
+
+// two floats as one fp16 pair (lo in the low half), one conversion instruction
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
 
 __device__ __forceinline__ void unpack_bf16x8(uint4 u, float x[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -141,10 +158,7 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 u, float x[8]) {
 }
 
 __device__ __forceinline__ uint4 pack_f16x8(const float x[8]) {
-    __align__(16) __half h[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) h[e] = __float2half_rn(x[e]);
-    return *reinterpret_cast<const uint4 *>(h);
+    return make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]), pack_h2(x[6], x[7]));
 }
 
 template <int R, int D>
@@ -184,7 +198,28 @@ __global__ void __launch_bounds__(NTH, 1)
     const int mm = tl >> 1, is_im = tl & 1;
     const float lam_r = a.lambda[((size_t)h * M + mm) * 2], lam_i = a.lambda[((size_t)h * M + mm) * 2 + 1];
     const float b_r = a.Bvec[((size_t)h * M + mm) * 2], b_i = a.Bvec[((size_t)h * M + mm) * 2 + 1];
-    float l33r = lam_r, l33i = lam_i;  // lambda^(32*hsel+1): first decay of my position half
+    // lambda^(32 hsel + 16 is_im + 1): the decay at this lane's first position in the a / Ya stage
+    float w0r = lam_r, w0i = lam_i;
+    {
+        float qr = lam_r, qi = lam_i;
+#pragma unroll
+        for (int sq = 0; sq < 4; ++sq) {  // lambda^16
+            const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
+            qr = nr;
+            qi = ni;
+        }
+        if (is_im) {
+            const float nr = w0r * qr - w0i * qi, ni = w0r * qi + w0i * qr;
+            w0r = nr;
+            w0i = ni;
+        }
+        const float q2r = qr * qr - qi * qi, q2i = 2.f * qr * qi;  // lambda^32
+        if (hsel) {
+            const float nr = w0r * q2r - w0i * q2i, ni = w0r * q2i + w0i * q2r;
+            w0r = nr;
+            w0i = ni;
+        }
+    }
 
     // TMA destinations need 1 KB-aligned shared memory; refuse rather than fault
     if ((smem_u32(sm) & 1023u) != 0u) {
@@ -246,17 +281,6 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
         for (int k = 0; k < CH; ++k)
             *reinterpret_cast<__half *>(sm + S::TA16 + kmaj_off(k, tl, 2, PADLBO, S::TY_SBO)) = tl16[k];
-    } else {
-        // lambda^33 = (lambda^32) lambda
-        float qr = lam_r, qi = lam_i;
-#pragma unroll
-        for (int sq = 0; sq < 5; ++sq) {
-            const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
-            qr = nr;
-            qi = ni;
-        }
-        l33r = qr * lam_r - qi * lam_i;
-        l33i = qr * lam_i + qi * lam_r;
     }
     tc_fence_before();
     __syncthreads();
@@ -380,7 +404,7 @@ __global__ void __launch_bounds__(NTH, 1)
                     acc[pp] = 0.f;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        f[pp][e] = silu_fast(f[pp][e]);
+                        f[pp][e] = silu_tanh(f[pp][e]);
                         acc[pp] = fmaf(f[pp][e], f[pp][e], acc[pp]);
                     }
                 }
@@ -388,30 +412,44 @@ __global__ void __launch_bounds__(NTH, 1)
                 for (int pp = 0; pp < PPQ; ++pp) {
 #pragma unroll
                     for (int o = 1; o < CBQ; o <<= 1) acc[pp] += __shfl_xor_sync(0xffffffffu, acc[pp], o);
-                    const float inv = (i0 + pp < L) ? 1.f / (acc[pp] + IDA_EPS_FEAT) : 0.f;
+                    const float inv = (i0 + pp < L) ? __fdividef(1.f, acc[pp] + IDA_EPS_FEAT) : 0.f;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[pp][e] *= inv;
                 }
                 if (which == 0) {
+                    // xi(q) rows: fp16 for the Gram MMA, tf32 for the state read-out MMA
+                    uint32_t h16[PPQ][4], t32[PPQ][8];
+#pragma unroll
+                    for (int pp = 0; pp < PPQ; ++pp) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) h16[pp][e] = pack_h2(f[pp][2 * e], f[pp][2 * e + 1]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) t32[pp][e] = tf32_bits(f[pp][e]);
+                    }
 #pragma unroll
                     for (int pp = 0; pp < PPQ; ++pp) {
                         const int q = (pp + rot) % PPQ, i = i0 + q;
-                        float x8[8];
+                        uint32_t hs[4], ts[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint32_t v = h16[0][e];
+#pragma unroll
+                            for (int u = 1; u < PPQ; ++u) v = q == u ? h16[u][e] : v;
+                            hs[e] = v;
+                        }
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
-                            float v = f[0][e];
+                            uint32_t v = t32[0][e];
 #pragma unroll
-                            for (int u = 1; u < PPQ; ++u) v = q == u ? f[u][e] : v;
-                            x8[e] = v;
+                            for (int u = 1; u < PPQ; ++u) v = q == u ? t32[u][e] : v;
+                            ts[e] = v;
                         }
-                        *reinterpret_cast<uint4 *>(sm + S::XQ16 + kmaj_off(i, c0, 2, 128, 16 * R)) = pack_f16x8(x8);
-                        uint4 t0v, t1v;
-                        t0v.x = __float_as_uint(to_tf32(x8[0])); t0v.y = __float_as_uint(to_tf32(x8[1]));
-                        t0v.z = __float_as_uint(to_tf32(x8[2])); t0v.w = __float_as_uint(to_tf32(x8[3]));
-                        t1v.x = __float_as_uint(to_tf32(x8[4])); t1v.y = __float_as_uint(to_tf32(x8[5]));
-                        t1v.z = __float_as_uint(to_tf32(x8[6])); t1v.w = __float_as_uint(to_tf32(x8[7]));
-                        *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0, 4, 128, 32 * R)) = t0v;
-                        *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0 + 4, 4, 128, 32 * R)) = t1v;
+                        *reinterpret_cast<uint4 *>(sm + S::XQ16 + kmaj_off(i, c0, 2, 128, 16 * R)) =
+                            make_uint4(hs[0], hs[1], hs[2], hs[3]);
+                        *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0, 4, 128, 32 * R)) =
+                            make_uint4(ts[0], ts[1], ts[2], ts[3]);
+                        *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0 + 4, 4, 128, 32 * R)) =
+                            make_uint4(ts[4], ts[5], ts[6], ts[7]);
                     }
                 } else {
 #pragma unroll
@@ -420,8 +458,9 @@ __global__ void __launch_bounds__(NTH, 1)
                         for (int e = 0; e < 8; ++e) fk[pp][e] = f[pp][e];
                 }
             }
-            // key RMSNorm + affine; Kt rows (rotated) and the transposed key rows of Z^T
-            __align__(16) __half kt_t[8][PPQ];
+            // key RMSNorm + affine, packed to fp16 once for the Kt rows (rotated) and the
+            // transposed key rows of Z^T
+            uint32_t hk[PPQ][4];
 #pragma unroll
             for (int pp = 0; pp < PPQ; ++pp) {
                 float ms = 0.f;
@@ -432,32 +471,35 @@ __global__ void __launch_bounds__(NTH, 1)
                 const float rk = rsqrtf(ms / R + IDA_EPS_RMS);
                 const bool valid = i0 + pp < L;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    fk[pp][e] = valid ? fmaf(fk[pp][e] * rk, nwk[e], bsk[e]) : 0.f;
-                    kt_t[e][pp] = __float2half_rn(fk[pp][e]);
-                }
+                for (int e = 0; e < 8; ++e) fk[pp][e] = valid ? fmaf(fk[pp][e] * rk, nwk[e], bsk[e]) : 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) hk[pp][e] = pack_h2(fk[pp][2 * e], fk[pp][2 * e + 1]);
             }
 #pragma unroll
             for (int pp = 0; pp < PPQ; ++pp) {
                 const int q = (pp + rot) % PPQ, i = i0 + q;
-                float x8[8];
+                uint32_t hs[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float v = fk[0][e];
+                for (int e = 0; e < 4; ++e) {
+                    uint32_t v = hk[0][e];
 #pragma unroll
-                    for (int u = 1; u < PPQ; ++u) v = q == u ? fk[u][e] : v;
-                    x8[e] = v;
+                    for (int u = 1; u < PPQ; ++u) v = q == u ? hk[u][e] : v;
+                    hs[e] = v;
                 }
-                *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) = pack_f16x8(x8);
+                *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) =
+                    make_uint4(hs[0], hs[1], hs[2], hs[3]);
             }
             if (ci > 0 && !mbar_wait(&bar[4], par ^ 1)) ok = false;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
+                // channel c0 + e at positions i0 .. i0 + PPQ - 1: pairs of halves from hk
+                const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
                 unsigned char *dst = sm + S::ZT16 + kmaj_off(c0 + e, i0, 2, PADLBO, S::ZT_SBO);
-                if (PPQ == 4)
-                    *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(kt_t[e]);
+                const uint32_t w01 = __byte_perm(hk[0][e >> 1], hk[1][e >> 1], sel);
+                if constexpr (PPQ == 4)
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(w01, __byte_perm(hk[2][e >> 1], hk[3][e >> 1], sel));
                 else
-                    *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(kt_t[e]);
+                    *reinterpret_cast<uint32_t *>(dst) = w01;
             }
         }
         {
@@ -469,7 +511,7 @@ __global__ void __launch_bounds__(NTH, 1)
             *reinterpret_cast<float4 *>(nwv + 4) = *reinterpret_cast<const float4 *>(nws + R + j0 + 4);
             *reinterpret_cast<float4 *>(bsv) = *reinterpret_cast<const float4 *>(bss + R + j0);
             *reinterpret_cast<float4 *>(bsv + 4) = *reinterpret_cast<const float4 *>(bss + R + j0 + 4);
-            __align__(16) __half vt_t[8][PPV];
+            float vt[PPV][8];
 #pragma unroll
             for (int pp = 0; pp < PPV; ++pp) {
                 const int i = i0 + pp;
@@ -483,16 +525,16 @@ __global__ void __launch_bounds__(NTH, 1)
                 const float rv = rsqrtf(ms / D + IDA_EPS_RMS);
                 const bool valid = i < L;
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    vt_t[e][pp] = __float2half_rn(valid ? fmaf(x8[e] * rv, nwv[e], bsv[e]) : 0.f);
+                for (int e = 0; e < 8; ++e) vt[pp][e] = valid ? fmaf(x8[e] * rv, nwv[e], bsv[e]) : 0.f;
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 unsigned char *dst = sm + S::ZT16 + kmaj_off(R + j0 + e, i0, 2, PADLBO, S::ZT_SBO);
-                if (PPV == 4)
-                    *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(vt_t[e]);
+                const uint32_t w01 = pack_h2(vt[0][e], vt[1][e]);
+                if constexpr (PPV == 4)
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(w01, pack_h2(vt[2][e], vt[3][e]));
                 else
-                    *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(vt_t[e]);
+                    *reinterpret_cast<uint32_t *>(dst) = w01;
             }
         }
         if (L < CH && hsel == 0) {
@@ -593,56 +635,67 @@ __global__ void __launch_bounds__(NTH, 1)
         tc_fence_after();
         if (__syncthreads_or(!ok)) break;
 
-        // ---- S5: a, Ya (fp16, column-scaled), a' (tf32); plane tl, positions of my half
+        // ---- S5: a, Ya (fp16, column-scaled), a' (tf32) ------------------------------------
+        // Lanes 2m, 2m+1 (planes Re / Im of mode m) split the 32 positions of the warp's half:
+        // the Re lane takes 32 hsel + p, the Im lane 32 hsel + 16 + p (p < 16), and each computes
+        // both planes there, so a mode's two planes are stored as one pair.  Complex values are
+        // held as (own, partner) components; with s = +1 on the Im lane and -1 on the Re lane,
+        // for z = (zo, zp) and w = (wr, wi): own(z w) = zo wr + zp (s wi), partner(z w) =
+        // zp wr - zo (s wi).  The operands hold (Re, -Im) per mode: -s own and +s partner.
         {
             float *ymx = reinterpret_cast<float *>(sm + S::GP16);  // [2][128]; GP16 is consumed
-            // Complex products in (own, partner) components: this lane's plane and its partner
-            // lane's.  With s = +1 on an Im plane and -1 on a Re plane, for z = (zo, zp) and
-            // w = (wr, wi):  own(z w) = zo wr + zp (s wi),  partner(z w) = zp wr - zo (s wi).
-            // The operands hold (Re, -Im) per mode, i.e. -s times the own component.
             const float sg = is_im ? 1.f : -1.f;
             const float bs = sg * b_i, ls = sg * lam_i;
-            const float ya_r = -sg * b_r, ya_p = -b_i;  // Ya = -s own(a B)
-            float ya[32];
-            float wr = l33r, ws = sg * l33i;  // lambda^(i+1) as (Re, s Im)
-            if (hsel == 0) {
-                wr = lam_r;
-                ws = ls;
-            }
-            float ymax = 0.f;
+            float pv[32], lv[32];
+            tmem_ld16(tb + lane_base + T::PT + 32 * hsel, pv);
+            tmem_ld16(tb + lane_base + T::PT + 32 * hsel + 16, pv + 16);
+            tmem_ld16(tb + lane_base + T::LT + 32 * hsel, lv);
+            tmem_ld16(tb + lane_base + T::LT + 32 * hsel + 16, lv + 16);
+            float wr = w0r, ws = sg * w0i;  // lambda^(i+1) at my first position, as (Re, s Im)
+            float yo[16], yq[16];           // Ya of my plane / of the partner plane, unscaled
+            float mo = 0.f, mq = 0.f;
+            const int ib = 32 * hsel + 16 * is_im;  // my first position
+            tmem_wait_ld();
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c0 = 32 * hsel + 16 * cc;
-                float pv[16], lv[16];
-                tmem_ld16(tb + lane_base + T::PT + c0, pv);
-                tmem_ld16(tb + lane_base + T::LT + c0, lv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int i = c0 + j;
-                    const float po = __shfl_xor_sync(0xffffffffu, pv[j], 1);
-                    const float lo = __shfl_xor_sync(0xffffffffu, lv[j], 1);
-                    // a = lambda^(i+1) P + B L
-                    const float ao = fmaf(pv[j], wr, fmaf(po, ws, fmaf(lv[j], b_r, lo * bs)));
-                    const float ap = fmaf(po, wr, fmaf(-pv[j], ws, fmaf(lo, b_r, -lv[j] * bs)));
-                    // Ya = a B ; a' = a lambda^(i+1)
-                    ya[16 * cc + j] = fmaf(ao, ya_r, ap * ya_p);
-                    ymax = fmaxf(ymax, fabsf(ya[16 * cc + j]));
-                    *reinterpret_cast<float *>(sm + S::AP32 + kmaj_off(i, tl, 4, PADLBO, S::AP_SBO)) =
-                        to_tf32(-sg * fmaf(ao, wr, ap * ws));
-                    const float nr = fmaf(wr, lam_r, -ws * ls), ns = fmaf(wr, ls, ws * lam_r);
-                    wr = nr;
-                    ws = ns;
-                }
+            for (int p = 0; p < 16; ++p) {
+                // my plane at my position; the partner needs mine at its position
+                const float pm = is_im ? pv[16 + p] : pv[p], ps = is_im ? pv[p] : pv[16 + p];
+                const float lm = is_im ? lv[16 + p] : lv[p], lsd = is_im ? lv[p] : lv[16 + p];
+                const float po = __shfl_xor_sync(0xffffffffu, ps, 1);
+                const float lo = __shfl_xor_sync(0xffffffffu, lsd, 1);
+                // a = lambda^(i+1) P + B L
+                const float ao = fmaf(pm, wr, fmaf(po, ws, fmaf(lm, b_r, lo * bs)));
+                const float ap = fmaf(po, wr, fmaf(-pm, ws, fmaf(lo, b_r, -lm * bs)));
+                // Ya = a B: -s own(a B) = -s b_r ao - b_i ap ; s partner(a B) = s b_r ap - b_i ao
+                yo[p] = fmaf(ao, -sg * b_r, -b_i * ap);
+                yq[p] = fmaf(ap, sg * b_r, -b_i * ao);
+                mo = fmaxf(mo, fabsf(yo[p]));
+                mq = fmaxf(mq, fabsf(yq[p]));
+                // a' = a lambda^(i+1), both planes, Re plane first
+                const float qo = -sg * fmaf(ao, wr, ap * ws), qq = sg * fmaf(ap, wr, -ao * ws);
+                const uint32_t t_re = tf32_bits(is_im ? qq : qo), t_im = tf32_bits(is_im ? qo : qq);
+                *reinterpret_cast<uint2 *>(sm + S::AP32 + kmaj_off(ib + p, 2 * mm, 4, PADLBO, S::AP_SBO)) =
+                    make_uint2(t_re, t_im);
+                const float nr = fmaf(wr, lam_r, -ws * ls), ns = fmaf(wr, ls, ws * lam_r);
+                wr = nr;
+                ws = ns;
             }
-            ymx[hsel * 128 + tl] = ymax;
+            // column (plane) maxima over the 64 positions: partner lane, then the other half
+            mo = fmaxf(mo, __shfl_xor_sync(0xffffffffu, mq, 1));
+            ymx[hsel * 128 + tl] = mo;
             __syncthreads();
             const int e = down_exp(fmaxf(ymx[tl], ymx[128 + tl]));
-            const float sdown = pow2i(-e);
+            const int eq = __shfl_xor_sync(0xffffffffu, e, 1);
+            const float so = pow2i(-e), sq = pow2i(-eq);
+            // the Im lane writes its positions rotated by 4 so that a pair's stores hit other banks
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                *reinterpret_cast<__half *>(sm + S::YA16 + kmaj_off(32 * hsel + j, tl, 2, PADLBO, S::TY_SBO)) =
-                    __float2half_rn(ya[j] * sdown);
+            for (int p = 0; p < 16; ++p) {
+                const int pr = is_im ? ((p + 4) & 15) : p;
+                const float vo = (is_im ? yo[(p + 4) & 15] : yo[p]) * so;
+                const float vq = (is_im ? yq[(p + 4) & 15] : yq[p]) * sq;
+                *reinterpret_cast<uint32_t *>(sm + S::YA16 + kmaj_off(ib + pr, 2 * mm, 2, PADLBO, S::TY_SBO)) =
+                    is_im ? pack_h2(vq, vo) : pack_h2(vo, vq);
+            }
             if (e != ya_exp) {
                 // T_A column tl = T_L row tl scaled by 2^e (exact in fp16); my half of k
                 const float sup = pow2i(e);
@@ -1069,18 +1122,17 @@ __global__ void __launch_bounds__(NTH, 2)
                     for (int e = 0; e < 8; ++e) fk[pp][e] = fmaf(tk[4 * e + jj], x8[e], fk[pp][e]);
             }
         }
-        __align__(16) __half kt_t[8][PPQ];
 #pragma unroll
         for (int pp = 0; pp < PPQ; ++pp) {
             float acc = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                fk[pp][e] = silu_fast(fk[pp][e]);
+                fk[pp][e] = silu_tanh(fk[pp][e]);
                 acc = fmaf(fk[pp][e], fk[pp][e], acc);
             }
 #pragma unroll
             for (int o = 1; o < CBQ; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            const float inv = 1.f / (acc + IDA_EPS_FEAT);
+            const float inv = __fdividef(1.f, acc + IDA_EPS_FEAT);
             float ms = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -1091,12 +1143,12 @@ __global__ void __launch_bounds__(NTH, 2)
             for (int o = 1; o < CBQ; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
             const float rk = rsqrtf(ms / R + IDA_EPS_RMS);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) kt_t[e][pp] = __float2half_rn(fmaf(fk[pp][e] * rk, nwk[e], bsk[e]));
+            for (int e = 0; e < 8; ++e) fk[pp][e] = fmaf(fk[pp][e] * rk, nwk[e], bsk[e]);
         }
         // value RMSNorm + affine
         constexpr int CBV = D / 8, PPV = CH * CBV / NTH;
         const int cbv = tid % CBV, iv0 = (tid / CBV) * PPV, j0 = 8 * cbv;
-        __align__(16) __half vt_t[8][PPV];
+        float vt[PPV][8];
 #pragma unroll
         for (int pp = 0; pp < PPV; ++pp) {
             float x8[8];
@@ -1108,26 +1160,27 @@ __global__ void __launch_bounds__(NTH, 2)
             for (int o = 1; o < CBV; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
             const float rv = rsqrtf(ms / D + IDA_EPS_RMS);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                vt_t[e][pp] = __float2half_rn(fmaf(x8[e] * rv, nws[R + j0 + e], bss[R + j0 + e]));
+            for (int e = 0; e < 8; ++e) vt[pp][e] = fmaf(x8[e] * rv, nws[R + j0 + e], bss[R + j0 + e]);
         }
         // the previous chunk's MMAs read ZT16: wait for them before rewriting it
         if (ci > c_begin && !mbar_wait(&bar[1], par ^ 1)) ok = false;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             unsigned char *dst = sm + S::ZT16 + kmaj_off(c0 + e, i0, 2, PADLBO, S::ZT_SBO);
-            if (PPQ == 4)
-                *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(kt_t[e]);
+            const uint32_t w01 = pack_h2(fk[0][e], fk[1][e]);
+            if constexpr (PPQ == 4)
+                *reinterpret_cast<uint2 *>(dst) = make_uint2(w01, pack_h2(fk[2][e], fk[3][e]));
             else
-                *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(kt_t[e]);
+                *reinterpret_cast<uint32_t *>(dst) = w01;
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             unsigned char *dst = sm + S::ZT16 + kmaj_off(R + j0 + e, iv0, 2, PADLBO, S::ZT_SBO);
-            if (PPV == 4)
-                *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(vt_t[e]);
+            const uint32_t w01 = pack_h2(vt[0][e], vt[1][e]);
+            if constexpr (PPV == 4)
+                *reinterpret_cast<uint2 *>(dst) = make_uint2(w01, pack_h2(vt[2][e], vt[3][e]));
             else
-                *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(vt_t[e]);
+                *reinterpret_cast<uint32_t *>(dst) = w01;
         }
         tc_fence_after();
         // scale the state by lambda^C (the previous chunk's accumulation is complete)
