@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(NTH, 1)
     using S = ChunkSmem<R, D>;
     using T = ChunkTmem<R>;
     extern __shared__ __align__(1024) unsigned char sm[];
+    const uint32_t s16 = smem_u32(sm) >> 4;  // shared base for MMA descriptors
     // mbarriers: 0 G, 1 L^T, 2 A2', 3 O2, 4 state update, 5 TMA, 6 P^T, 7 O1
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S::BARS);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S::TSLOT);
@@ -567,19 +568,19 @@ __global__ void __launch_bounds__(NTH, 1)
         tc_fence_after();
 
         // ---- S2: G and P^T ------------------------------------------------------
-        if (tid == 0) {
+        if (warp == 0 && elect_one()) {
             const uint32_t idg = idesc(128, 64, 0, 0);
 #pragma unroll
             for (int s = 0; s < R / 16; ++s)
-                mma_f16_ss(tb + T::G, sdesc(sm + S::XQ16 + s * 256, 128, 16 * R),
-                           sdesc(sm + S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
+                mma_f16(tb + T::G, sdesc_at(s16, S::XQ16 + s * 256, 128, 16 * R),
+                           sdesc_at(s16, S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
             mma_commit(&bar[0]);
-        } else if (tid == 32) {
+        } else if (warp == 1 && elect_one()) {
             // P^T from a second issuing thread, so that G's completion is not queued behind it
             const uint32_t idp = idesc(128, 64, 2, 2);
 #pragma unroll
             for (int s = 0; s < R / 8; ++s)
-                mma_tf32_ts(tb + T::PT, tb + T::U + 8 * s, sdesc(sm + S::XQ32 + s * 256, 128, 32 * R), idp, s > 0);
+                mma_tf32_t(tb + T::PT, tb + T::U + 8 * s, sdesc_at(s16, S::XQ32 + s * 256, 128, 32 * R), idp, s > 0);
             mma_commit(&bar[6]);
         }
         __syncwarp();
@@ -622,12 +623,12 @@ __global__ void __launch_bounds__(NTH, 1)
         tc_fence_after();
 
         // ---- S4: L^T = T_L . G'^T -----------------------------------------------------
-        if (tid == 0) {
+        if (warp == 0 && elect_one()) {
             const uint32_t id = idesc(128, 64, 0, 0);
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
-                mma_f16_ss(tb + T::LT, sdesc(sm + S::TL16 + s * 256, 128, 1024),
-                           sdesc(sm + S::GP16 + s * 256, 128, 1024), id, s > 0);
+                mma_f16(tb + T::LT, sdesc_at(s16, S::TL16 + s * 256, 128, 1024),
+                           sdesc_at(s16, S::GP16 + s * 256, 128, 1024), id, s > 0);
             mma_commit(&bar[1]);
         }
         __syncwarp();
@@ -719,19 +720,19 @@ __global__ void __launch_bounds__(NTH, 1)
         tc_fence_after();
 
         // ---- S6: A2' = Ya . T_A^T -----------------------------------------------------
-        if (tid == 0) {
+        if (warp == 0 && elect_one()) {
             const uint32_t id = idesc(128, 64, 0, 0);
 #pragma unroll
             for (int s = 0; s < MP / 16; ++s)
-                mma_f16_ss(tb + T::G, sdesc(sm + S::YA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO),
-                           sdesc(sm + S::TA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO), id, s > 0);
+                mma_f16(tb + T::G, sdesc_at(s16, S::YA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO),
+                           sdesc_at(s16, S::TA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO), id, s > 0);
             mma_commit(&bar[2]);
-        } else if (tid == 32) {
+        } else if (warp == 1 && elect_one()) {
             // O2 = Gamma^T . a'^T needs only S5's a' and the state: it runs under S7
             const uint32_t id32 = idesc(128, 64, 2, 2);
 #pragma unroll
             for (int s = 0; s < MP / 8; ++s)
-                mma_tf32_ts(tb + T::LT, tb + T::GT + 8 * s, sdesc(sm + S::AP32 + s * 2 * PADLBO, PADLBO, S::AP_SBO),
+                mma_tf32_t(tb + T::LT, tb + T::GT + 8 * s, sdesc_at(s16, S::AP32 + s * 2 * PADLBO, PADLBO, S::AP_SBO),
                             id32, s > 0);
             mma_commit(&bar[3]);
         }
@@ -784,13 +785,13 @@ __global__ void __launch_bounds__(NTH, 1)
         tc_fence_after();
 
         // ---- S8: O1 = Vt^T . A2^T (O2 was issued with A2') -----------------------------------
-        if (tid == 0) {
+        if (warp == 0 && elect_one()) {
             const uint32_t id16 = idesc(128, 64, 0, 0);
             const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;  // value rows R .. R+127
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
-                mma_f16_ss(tb + T::PT, sdesc(sm + vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
-                           sdesc(sm + S::A216 + s * 256, 128, 1024), id16, s > 0);
+                mma_f16(tb + T::PT, sdesc_at(s16, vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
+                           sdesc_at(s16, S::A216 + s * 256, 128, 1024), id16, s > 0);
             mma_commit(&bar[7]);
         }
         __syncwarp();
@@ -886,20 +887,23 @@ __global__ void __launch_bounds__(NTH, 1)
 
         // ---- S10: U += Coef . Kt ; Gamma^T += Vt^T . Coef^T -----------------------------------
         if (tid == 0) {
-            // the chunk's output rows; rows past N are clipped by the copy
+            // the chunk's output rows; rows past N are clipped by the copy (thread 0 owns the
+            // bulk group it waits on before the next prologue)
             tma_store_4d(&tm_o, 0, h, t0, b, sm + S::XQ32);
             bulk_commit();
+        }
+        if (warp == 0 && elect_one()) {
             const uint32_t idu = idesc(128, R, 0, 0);
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
-                mma_f16_ss(tb + T::U, sdesc(sm + S::CF16 + s * 256, 128, 1024),
-                           sdesc(sm + S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, 1);
+                mma_f16(tb + T::U, sdesc_at(s16, S::CF16 + s * 256, 128, 1024),
+                           sdesc_at(s16, S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, 1);
             const uint32_t idg = idesc(128, MP, 0, 0);
             const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
-                mma_f16_ss(tb + T::GT, sdesc(sm + vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
-                           sdesc(sm + S::CF16 + s * 256, 128, 1024), idg, 1);
+                mma_f16(tb + T::GT, sdesc_at(s16, vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
+                           sdesc_at(s16, S::CF16 + s * 256, 128, 1024), idg, 1);
             mma_commit(&bar[4]);
         }
         __syncwarp();
@@ -998,6 +1002,7 @@ __global__ void __launch_bounds__(NTH, 2)
                        const __grid_constant__ CUtensorMap tm_v, int nseg, int seg_chunks, float *seg_state) {
     using S = StateSmem<R, D>;
     extern __shared__ __align__(1024) unsigned char sm[];
+    const uint32_t s16 = smem_u32(sm) >> 4;  // shared base for MMA descriptors
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S::BARS);  // 0 TMA, 1 MMA
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S::TSLOT);
     float2 *laml = reinterpret_cast<float2 *>(sm + S::LAML);
@@ -1232,17 +1237,19 @@ __global__ void __launch_bounds__(NTH, 2)
                 tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[0]);
                 tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[0]);
             }
+        }
+        if (warp == 0 && elect_one()) {
             const uint32_t idu = idesc(128, R, 0, 0);
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
-                mma_f16_ss(tb + TU, sdesc(sm + S::CF16 + s * 256, 128, 1024),
-                           sdesc(sm + S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, 1);
+                mma_f16(tb + TU, sdesc_at(s16, S::CF16 + s * 256, 128, 1024),
+                           sdesc_at(s16, S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, 1);
             const uint32_t idg = idesc(128, MP, 0, 0);
             const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
-                mma_f16_ss(tb + TG, sdesc(sm + vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
-                           sdesc(sm + S::CF16 + s * 256, 128, 1024), idg, 1);
+                mma_f16(tb + TG, sdesc_at(s16, vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
+                           sdesc_at(s16, S::CF16 + s * 256, 128, 1024), idg, 1);
             mma_commit(&bar[1]);
         }
         if (ci + 1 < c_end) tma_pending = 1;

@@ -159,19 +159,6 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 // ---- descriptors ------------------------------------------------------------
 
-// Shared-memory matrix descriptor, no swizzle.  The operand is stored as
-// 8-row x 16-byte "core matrices"; `lbo` is the byte distance between core
-// matrices adjacent along K, `sbo` between core matrices adjacent along M/N.
-__device__ __forceinline__ uint64_t sdesc(const void *smem_ptr, uint32_t lbo, uint32_t sbo) {
-    const uint32_t a = smem_u32(smem_ptr);
-    uint64_t d = 0;
-    d |= (uint64_t)((a >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;  // descriptor version for the sm_100 family
-    return d;                // base offset 0, layout type 0 (no swizzle)
-}
-
 // Instruction descriptor for kind::f16 / kind::tf32 with an fp32 accumulator.
 // fmt: 0 = f16, 1 = bf16 (kind::f16); 2 = tf32 (kind::tf32).
 __host__ __device__ constexpr uint32_t idesc(int M, int N, int afmt, int bfmt, int a_mn = 0, int b_mn = 0) {
@@ -179,30 +166,41 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, int afmt, int bfmt, i
            ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Shared-memory matrix descriptor (no swizzle, sm_100-family version 1) of the operand
+// at byte offset `off` from a shared base whose address >> 4 is `s16`.  The operand is
+// stored as 8-row x 16-byte core matrices; `lbo` is the byte distance between core
+// matrices adjacent along K, `sbo` between core matrices adjacent along M/N.  Kept as
+// 32-bit halves so that a K step is one add on the low word.
+struct SmemDesc {
+    uint32_t lo, hi;
+};
+__device__ __forceinline__ SmemDesc sdesc_at(uint32_t s16, uint32_t off, uint32_t lbo, uint32_t sbo) {
+    return {((s16 + (off >> 4)) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16), ((sbo >> 4) & 0x3FFFu) | (1u << 14)};
+}
+
+// One lane of a fully active warp (every lane must execute it).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
 // ---- MMA issue (single thread) ---------------------------------------------
 
-__device__ __forceinline__ void mma_f16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+__device__ __forceinline__ void mma_f16(uint32_t d, SmemDesc a, SmemDesc b, uint32_t id, uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(id), "r"(acc)
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tmov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d),
+        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(id), "r"(acc)
         : "memory");
 }
 
-__device__ __forceinline__ void mma_tf32_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+// A operand read from TMEM (lanes = rows of A, columns = K), B from shared memory.
+__device__ __forceinline__ void mma_tf32_t(uint32_t d, uint32_t a_tmem, SmemDesc b, uint32_t id, uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(id), "r"(acc)
-        : "memory");
-}
-
-// A operand read from TMEM (lanes = rows of A, columns = K).
-__device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-        "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\tmov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\ttcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], db, %4, p;\n\t}" ::"r"(d),
+        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(id), "r"(acc)
         : "memory");
 }
 
@@ -210,14 +208,6 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a_tmem, uint64_
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
-}
-
-// fp32 -> tf32 with round-to-nearest (ties away), low 13 bits cleared, so
-// that the tensor core's read of the operand adds no further rounding.
-__device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
 }
 
 }  // namespace tc
