@@ -12,7 +12,7 @@ namespace ida {
 ida_status launch_seq_prefill(const PrefillArgs &a, cudaStream_t st, int num_sms, std::string &why);
 ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int num_sms, std::string &why,
                                 bool *taken, void *workspace, size_t workspace_bytes);
-size_t chunk_workspace_bytes(const PrefillArgs &a, int num_sms);
+size_t chunk_workspace_bytes(const PrefillArgs &a, int num_sms, size_t budget);
 ida_status launch_decode(const DecodeArgs &a, cudaStream_t st, std::string &why);
 }  // namespace ida
 
@@ -196,7 +196,12 @@ ida_status ida_forward_ws(const void *q, const void *k, const void *v, const flo
                               dtype, W, flags, workspace, workspace_bytes, stream);
 }
 
-size_t ida_forward_workspace_bytes(int B, int H, int N, int d, int R, int M, int dtype, int W, int flags) {
+}  // extern "C"
+
+namespace ida {
+// Workspace bytes of the prefill plan chosen within `budget` bytes on the current device.
+size_t forward_workspace_within(int B, int H, int N, int d, int R, int M, int dtype, int W, int flags,
+                                size_t budget) {
     std::string why;
     if (B < 0 || H < 0 || N < 0 || check_shape(d, R, M, W, dtype, flags, why) != IDA_OK) return 0;
     if (flags & IDA_PATH_SEQUENTIAL) return 0;
@@ -204,9 +209,16 @@ size_t ida_forward_workspace_bytes(int B, int H, int N, int d, int R, int M, int
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
-    ida::PrefillArgs a = {};
+    PrefillArgs a = {};
     a.B = B; a.H = H; a.N = N; a.d = d; a.R = R; a.M = M; a.W = W; a.dtype = dtype; a.flags = flags;
-    return ida::chunk_workspace_bytes(a, num_sms);
+    return chunk_workspace_bytes(a, num_sms, budget);
+}
+}  // namespace ida
+
+extern "C" {
+
+size_t ida_forward_workspace_bytes(int B, int H, int N, int d, int R, int M, int dtype, int W, int flags) {
+    return ida::forward_workspace_within(B, H, N, d, R, M, dtype, W, flags, ida::kPreferredWorkspace);
 }
 
 ida_status ida_decode_step(const void *q, const void *k, const void *v, const float *conv_w,

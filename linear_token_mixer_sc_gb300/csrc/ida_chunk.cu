@@ -161,12 +161,31 @@ __device__ __forceinline__ uint4 pack_f16x8(const float x[8]) {
     return make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]), pack_h2(x[6], x[7]));
 }
 
+// Work split of a batch of sequences across CTAs.  Each unit's chunks are grouped into
+// nb blocks of fs chunks (the last block may be shorter); the units' blocks, taken in
+// order, are dealt to the readout CTAs q at a time.  A CTA runs its blocks as pieces, one
+// per unit they fall in; every piece not at a sequence start needs the state before its
+// first block, which the block state pass and the block scan provide.
+struct SegPlan {
+    int fs;     // chunks per block
+    int nb;     // blocks per unit
+    int q;      // blocks per readout CTA
+    int total;  // units * nb
+};
+
+// Block (within unit u) at which u's last piece starts: the blocks before it are the ones
+// whose local end states the scan composes.
+__host__ __device__ inline int plan_last_start(const SegPlan &p, int u) {
+    const int f_last = (u + 1) * p.nb - 1;
+    const int start = (f_last / p.q) * p.q;
+    return start > u * p.nb ? start - u * p.nb : 0;
+}
+
 template <int R, int D>
 __global__ void __launch_bounds__(NTH, 1)
     chunk_prefill_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_o, int nseg, int seg_chunks,
-                         const float *seg_start) {
+                         const __grid_constant__ CUtensorMap tm_o, SegPlan plan, const float *seg_start) {
     using S = ChunkSmem<R, D>;
     using T = ChunkTmem<R>;
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -185,42 +204,13 @@ __global__ void __launch_bounds__(NTH, 1)
     const int tl = 32 * q4 + lane;                    // my TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const int H = a.H, N = a.N, M = 64, W = a.W;
-    // sequence segment of this CTA: chunks [c_begin, c_end) of unit `unit`
-    const int unit = blockIdx.x / nseg, seg = blockIdx.x % nseg, b = unit / H, h = unit % H;
     const int nchunks = (N + CH - 1) / CH;
-    const int c_begin = seg * seg_chunks, c_end = min(nchunks, c_begin + seg_chunks);
     const size_t sqk = (size_t)H * R;
-    const size_t base_qk = ((size_t)b * N * H + h) * R;
     const __nv_bfloat16 *gq = reinterpret_cast<const __nv_bfloat16 *>(a.q);
     const __nv_bfloat16 *gk = reinterpret_cast<const __nv_bfloat16 *>(a.k);
     const uint32_t raw_bytes = 2u * (CH + HALO) * R * 2 + (uint32_t)CH * D * 2;
-
     // my mode plane in the lane-side stages: plane tl = 2m + (0: Re, 1: Im)
     const int mm = tl >> 1, is_im = tl & 1;
-    const float lam_r = a.lambda[((size_t)h * M + mm) * 2], lam_i = a.lambda[((size_t)h * M + mm) * 2 + 1];
-    const float b_r = a.Bvec[((size_t)h * M + mm) * 2], b_i = a.Bvec[((size_t)h * M + mm) * 2 + 1];
-    // lambda^(32 hsel + 16 is_im + 1): the decay at this lane's first position in the a / Ya stage
-    float w0r = lam_r, w0i = lam_i;
-    {
-        float qr = lam_r, qi = lam_i;
-#pragma unroll
-        for (int sq = 0; sq < 4; ++sq) {  // lambda^16
-            const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
-            qr = nr;
-            qi = ni;
-        }
-        if (is_im) {
-            const float nr = w0r * qr - w0i * qi, ni = w0r * qi + w0i * qr;
-            w0r = nr;
-            w0i = ni;
-        }
-        const float q2r = qr * qr - qi * qi, q2i = 2.f * qr * qi;  // lambda^32
-        if (hsel) {
-            const float nr = w0r * q2r - w0i * q2i, ni = w0r * q2i + w0i * q2r;
-            w0r = nr;
-            w0i = ni;
-        }
-    }
 
     // TMA destinations need 1 KB-aligned shared memory; refuse rather than fault
     if ((smem_u32(sm) & 1023u) != 0u) {
@@ -228,741 +218,795 @@ __global__ void __launch_bounds__(NTH, 1)
         return;
     }
 
-    // ---- set-up: barriers, TMEM, per-head constants -----------------------------
+    // ---- set-up: barriers, TMEM ---------------------------------------------------
     if (tid == 0) {
         for (int i = 0; i < 8; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_o);
     }
     if (warp == 0) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
-    for (int x = tid; x < R + D; x += NTH) {
-        nws[x] = a.norm_w[(size_t)h * (R + D) + x];
-        bss[x] = a.bias[(size_t)h * (R + D) + x];
-    }
-    if (hsel == 0) {
-        // T_L row (plane tl): component of lambda_m^k, k = 0..63; Coef row: component
-        // of B_m lambda_m^(C-1-j); T_A column tl = T_L row (unscaled).
-        float pr = 1.f, pi = 0.f, sr = 0.f, si = 0.f;
-        __align__(16) __half tl16[CH], cf[CH];
-#pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            sr += pr;
-            si += pi;
-            tl16[k] = __float2half_rn(is_im ? pi : pr);
-            const float cr = b_r * pr - b_i * pi, ci = b_r * pi + b_i * pr;
-            cf[CH - 1 - k] = __float2half_rn(is_im ? ci : cr);
-            const float nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
-            pr = nr;
-            pi = ni;
-        }
-        // lambda^C by repeated squaring (fewer roundings than the running product)
-        float qr = lam_r, qi = lam_i;
-#pragma unroll
-        for (int sq = 0; sq < 6; ++sq) {
-            const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
-            qr = nr;
-            qi = ni;
-        }
-        if (!is_im) {
-            laml[mm] = make_float2(qr, qi);  // lambda^C
-            suml[mm] = make_float2(sr, si);  // sum_{k<C} lambda^k
-        }
-#pragma unroll
-        for (int k8 = 0; k8 < CH / 8; ++k8) {
-            *reinterpret_cast<uint4 *>(sm + S::TL16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
-                *reinterpret_cast<const uint4 *>(&tl16[k8 * 8]);
-            *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
-                *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
-        }
-#pragma unroll
-        for (int k = 0; k < CH; ++k)
-            *reinterpret_cast<__half *>(sm + S::TA16 + kmaj_off(k, tl, 2, PADLBO, S::TY_SBO)) = tl16[k];
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *tslot;
-    {
-        // start state: zero for the first segment, else the state after the previous
-        // segments ([R+128 columns][128 lanes] floats, columns as in TMEM), split by column half
-        const float *x0 = seg > 0 ? seg_start + ((size_t)unit * (nseg - 1) + (seg - 1)) * (size_t)(R + MP) * 128 : nullptr;
-        for (int c0 = hsel * 16; c0 < R + MP; c0 += 32) {
-            float z[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) z[i] = x0 ? x0[(size_t)(c0 + i) * 128 + tl] : 0.f;
-            tmem_st16(tb + lane_base + c0, z);
+
+    bool ok = true;
+    int it = 0;           // chunks this CTA has run so far: the phase parity of every barrier
+    int tma_pending = 0;  // TMA copies issued and not yet waited for
+    int ci = 0;
+    // This CTA's blocks of the (unit, block) sequence, split at unit boundaries into pieces
+    // that run one after the other; a piece starting past block 0 takes its start state
+    // from the block scan.
+    int fb = blockIdx.x * plan.q;
+    const int fb_end = min(fb + plan.q, plan.total);
+    while (ok && fb < fb_end) {
+        const int unit = fb / plan.nb, j0 = fb % plan.nb;
+        const int j1 = min(plan.nb, j0 + (fb_end - fb));
+        fb += j1 - j0;
+        const int b = unit / H, h = unit % H;
+        const int c_begin = j0 * plan.fs, c_end = min(nchunks, j1 * plan.fs);
+        const size_t base_qk = ((size_t)b * N * H + h) * R;
+        const float lam_r = a.lambda[((size_t)h * M + mm) * 2], lam_i = a.lambda[((size_t)h * M + mm) * 2 + 1];
+        const float b_r = a.Bvec[((size_t)h * M + mm) * 2], b_i = a.Bvec[((size_t)h * M + mm) * 2 + 1];
+        // lambda^(32 hsel + 16 is_im + 1): the decay at this lane's first position in the a / Ya stage
+        float w0r = lam_r, w0i = lam_i;
+        {
+            float qr = lam_r, qi = lam_i;
+    #pragma unroll
+            for (int sq = 0; sq < 4; ++sq) {  // lambda^16
+                const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
+                qr = nr;
+                qi = ni;
+            }
+            if (is_im) {
+                const float nr = w0r * qr - w0i * qi, ni = w0r * qi + w0i * qr;
+                w0r = nr;
+                w0i = ni;
+            }
+            const float q2r = qr * qr - qi * qi, q2i = 2.f * qr * qi;  // lambda^32
+            if (hsel) {
+                const float nr = w0r * q2r - w0i * q2i, ni = w0r * q2i + w0i * q2r;
+                w0r = nr;
+                w0i = ni;
+            }
+        }
+
+
+        // ---- per-head constants of the piece ----------------------------------------
+        for (int x = tid; x < R + D; x += NTH) {
+            nws[x] = a.norm_w[(size_t)h * (R + D) + x];
+            bss[x] = a.bias[(size_t)h * (R + D) + x];
         }
         if (hsel == 0) {
-            // conv taps of channels 8*(tl % (R/8)) .. +7, right-aligned: column 32*which + 4*e + jj
-            // multiplies position i - 3 + jj (zero for jj < 4 - W)
-            const int cbl = tl % (R / 8);
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const float *cwg = a.conv_w + ((size_t)(which * H + h) * R + 8 * cbl) * W;
-                float t32[32];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) t32[4 * e + jj] = jj >= 4 - W ? cwg[e * W + jj - (4 - W)] : 0.f;
-                tmem_st16(tb + lane_base + T::TAPS + 32 * which, t32);
-                tmem_st16(tb + lane_base + T::TAPS + 32 * which + 16, t32 + 16);
-            }
-        }
-        tmem_wait_st();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-        const int tb0 = c_begin * CH;
-        mbar_arrive_expect_tx(&bar[5], raw_bytes);
-        tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, tb0 - HALO, b, &bar[5]);
-        tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tb0 - HALO, b, &bar[5]);
-        tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tb0, b, &bar[5]);
-    }
-
-    // eta of my mode at the segment start, B sum_{k < t_begin} lambda^k (hsel == 0, Re thread)
-    float eta_r = 0.f, eta_i = 0.f;
-    if (hsel == 0 && !is_im) {
-        const float2 ll = laml[mm], sl = suml[mm];
-        for (int c = 0; c < c_begin; ++c) {
-            const float er = ll.x * eta_r - ll.y * eta_i + b_r * sl.x - b_i * sl.y;
-            const float ei = ll.x * eta_i + ll.y * eta_r + b_r * sl.y + b_i * sl.x;
-            eta_r = er;
-            eta_i = ei;
-        }
-    }
-    int ya_exp = 0;  // scale exponent of my T_A column currently stored
-    bool ok = true;
-    int tma_pending = 1;  // TMA copies issued and not yet waited for
-    int ci = c_begin;
-
-    for (; ci < c_end; ++ci) {
-        const int t0 = ci * CH;
-        const int L = min(CH, N - t0);
-        const uint32_t par = (ci - c_begin) & 1;  // barrier phases count this CTA's chunks
-
-        // this chunk's raw rows (the previous chunk's state-update MMAs, which read ZT16 and
-        // CF16, are waited for inside the prologue, just before ZT16 is rewritten)
-        ok = mbar_wait(&bar[5], par);
-        if (ok) tma_pending = 0;
-        if (tid == 0) bulk_wait_read_all();  // the previous output tile has left XQ32
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) break;
-
-        // ---- S1: prologue, thread = (8-channel block, block of consecutive positions)
-        {
-            // query / key: R/8 channel blocks x (64 R/8 / 256) positions per thread
-            constexpr int CBQ = R / 8, PPQ = CH * CBQ / NTH;
-            const int cb = tid % CBQ, i0 = (tid / CBQ) * PPQ, c0 = 8 * cb;
-            // rows are stored rotated: at step pp this thread writes position i0 + (pp + rot) % PPQ,
-            // so the channel-block threads of one position hit different banks
-            const int rot = cb % PPQ;
-            float tq[32], tk[32];  // taps of my channel block (TMEM lane tl holds block tl % CBQ == cb)
-            tmem_ld16(tb + lane_base + T::TAPS, tq);
-            tmem_ld16(tb + lane_base + T::TAPS + 16, tq + 16);
-            tmem_ld16(tb + lane_base + T::TAPS + 32, tk);
-            tmem_ld16(tb + lane_base + T::TAPS + 48, tk + 16);
-            float nwk[8], bsk[8];
-            *reinterpret_cast<float4 *>(nwk) = *reinterpret_cast<const float4 *>(nws + c0);
-            *reinterpret_cast<float4 *>(nwk + 4) = *reinterpret_cast<const float4 *>(nws + c0 + 4);
-            *reinterpret_cast<float4 *>(bsk) = *reinterpret_cast<const float4 *>(bss + c0);
-            *reinterpret_cast<float4 *>(bsk + 4) = *reinterpret_cast<const float4 *>(bss + c0 + 4);
-            tmem_wait_ld();
-            float fk[PPQ][8];
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const unsigned char *raw = sm + (which == 0 ? S::RAWQ : S::RAWK);
-                const float *w8 = which == 0 ? tq : tk;
-                // rows i0 .. i0+PPQ+2 of the staged tile = positions i0-3 .. i0+PPQ-1
-                float f[PPQ][8];
-#pragma unroll
-                for (int pp = 0; pp < PPQ; ++pp)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[pp][e] = 0.f;
-#pragma unroll
-                for (int r = 0; r < PPQ + HALO; ++r) {
-                    float x8[8];
-                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(raw + ((size_t)(i0 + r) * R + c0) * 2), x8);
-                    // tile row r holds position i0 + r - 3: right-aligned tap jj = r - pp of position pp
-#pragma unroll
-                    for (int pp = 0; pp < PPQ; ++pp) {
-                        const int jj = r - pp;
-                        if (jj >= 0 && jj < 4)
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) f[pp][e] = fmaf(w8[4 * e + jj], x8[e], f[pp][e]);
-                    }
-                }
-                float acc[PPQ];
-#pragma unroll
-                for (int pp = 0; pp < PPQ; ++pp) {
-                    acc[pp] = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        f[pp][e] = silu_tanh(f[pp][e]);
-                        acc[pp] = fmaf(f[pp][e], f[pp][e], acc[pp]);
-                    }
-                }
-#pragma unroll
-                for (int pp = 0; pp < PPQ; ++pp) {
-#pragma unroll
-                    for (int o = 1; o < CBQ; o <<= 1) acc[pp] += __shfl_xor_sync(0xffffffffu, acc[pp], o);
-                    const float inv = (i0 + pp < L) ? __fdividef(1.f, acc[pp] + IDA_EPS_FEAT) : 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[pp][e] *= inv;
-                }
-                if (which == 0) {
-                    // xi(q) rows: fp16 for the Gram MMA, tf32 for the state read-out MMA
-                    uint32_t h16[PPQ][4], t32[PPQ][8];
-#pragma unroll
-                    for (int pp = 0; pp < PPQ; ++pp) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) h16[pp][e] = pack_h2(f[pp][2 * e], f[pp][2 * e + 1]);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) t32[pp][e] = tf32_bits(f[pp][e]);
-                    }
-#pragma unroll
-                    for (int pp = 0; pp < PPQ; ++pp) {
-                        const int q = (pp + rot) % PPQ, i = i0 + q;
-                        uint32_t hs[4], ts[8];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            uint32_t v = h16[0][e];
-#pragma unroll
-                            for (int u = 1; u < PPQ; ++u) v = q == u ? h16[u][e] : v;
-                            hs[e] = v;
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            uint32_t v = t32[0][e];
-#pragma unroll
-                            for (int u = 1; u < PPQ; ++u) v = q == u ? t32[u][e] : v;
-                            ts[e] = v;
-                        }
-                        *reinterpret_cast<uint4 *>(sm + S::XQ16 + kmaj_off(i, c0, 2, 128, 16 * R)) =
-                            make_uint4(hs[0], hs[1], hs[2], hs[3]);
-                        *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0, 4, 128, 32 * R)) =
-                            make_uint4(ts[0], ts[1], ts[2], ts[3]);
-                        *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0 + 4, 4, 128, 32 * R)) =
-                            make_uint4(ts[4], ts[5], ts[6], ts[7]);
-                    }
-                } else {
-#pragma unroll
-                    for (int pp = 0; pp < PPQ; ++pp)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) fk[pp][e] = f[pp][e];
-                }
-            }
-            // key RMSNorm + affine, packed to fp16 once for the Kt rows (rotated) and the
-            // transposed key rows of Z^T
-            uint32_t hk[PPQ][4];
-#pragma unroll
-            for (int pp = 0; pp < PPQ; ++pp) {
-                float ms = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ms = fmaf(fk[pp][e], fk[pp][e], ms);
-#pragma unroll
-                for (int o = 1; o < CBQ; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
-                const float rk = rsqrtf(ms / R + IDA_EPS_RMS);
-                const bool valid = i0 + pp < L;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) fk[pp][e] = valid ? fmaf(fk[pp][e] * rk, nwk[e], bsk[e]) : 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) hk[pp][e] = pack_h2(fk[pp][2 * e], fk[pp][2 * e + 1]);
-            }
-#pragma unroll
-            for (int pp = 0; pp < PPQ; ++pp) {
-                const int q = (pp + rot) % PPQ, i = i0 + q;
-                uint32_t hs[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    uint32_t v = hk[0][e];
-#pragma unroll
-                    for (int u = 1; u < PPQ; ++u) v = q == u ? hk[u][e] : v;
-                    hs[e] = v;
-                }
-                *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) =
-                    make_uint4(hs[0], hs[1], hs[2], hs[3]);
-            }
-            if (ci > 0 && !mbar_wait(&bar[4], par ^ 1)) ok = false;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                // channel c0 + e at positions i0 .. i0 + PPQ - 1: pairs of halves from hk
-                const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-                unsigned char *dst = sm + S::ZT16 + kmaj_off(c0 + e, i0, 2, PADLBO, S::ZT_SBO);
-                const uint32_t w01 = __byte_perm(hk[0][e >> 1], hk[1][e >> 1], sel);
-                if constexpr (PPQ == 4)
-                    *reinterpret_cast<uint2 *>(dst) = make_uint2(w01, __byte_perm(hk[2][e >> 1], hk[3][e >> 1], sel));
-                else
-                    *reinterpret_cast<uint32_t *>(dst) = w01;
-            }
-        }
-        {
-            // value: D/8 channel blocks x (64 D/8 / 256) positions per thread
-            constexpr int CBV = D / 8, PPV = CH * CBV / NTH;
-            const int cb = tid % CBV, i0 = (tid / CBV) * PPV, j0 = 8 * cb;
-            float nwv[8], bsv[8];
-            *reinterpret_cast<float4 *>(nwv) = *reinterpret_cast<const float4 *>(nws + R + j0);
-            *reinterpret_cast<float4 *>(nwv + 4) = *reinterpret_cast<const float4 *>(nws + R + j0 + 4);
-            *reinterpret_cast<float4 *>(bsv) = *reinterpret_cast<const float4 *>(bss + R + j0);
-            *reinterpret_cast<float4 *>(bsv + 4) = *reinterpret_cast<const float4 *>(bss + R + j0 + 4);
-            float vt[PPV][8];
-#pragma unroll
-            for (int pp = 0; pp < PPV; ++pp) {
-                const int i = i0 + pp;
-                float x8[8];
-                unpack_bf16x8(*reinterpret_cast<const uint4 *>(sm + S::RAWV + ((size_t)i * D + j0) * 2), x8);
-                float ms = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ms = fmaf(x8[e], x8[e], ms);
-#pragma unroll
-                for (int o = 1; o < CBV; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
-                const float rv = rsqrtf(ms / D + IDA_EPS_RMS);
-                const bool valid = i < L;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) vt[pp][e] = valid ? fmaf(x8[e] * rv, nwv[e], bsv[e]) : 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                unsigned char *dst = sm + S::ZT16 + kmaj_off(R + j0 + e, i0, 2, PADLBO, S::ZT_SBO);
-                const uint32_t w01 = pack_h2(vt[0][e], vt[1][e]);
-                if constexpr (PPV == 4)
-                    *reinterpret_cast<uint2 *>(dst) = make_uint2(w01, pack_h2(vt[2][e], vt[3][e]));
-                else
-                    *reinterpret_cast<uint32_t *>(dst) = w01;
-            }
-        }
-        if (L < CH && hsel == 0) {
-            // ragged last chunk: Coef row = component of B lambda^(L-1-j) for j < L, else 0
+            // T_L row (plane tl): component of lambda_m^k, k = 0..63; Coef row: component
+            // of B_m lambda_m^(C-1-j); T_A column tl = T_L row (unscaled).
             float pr = 1.f, pi = 0.f, sr = 0.f, si = 0.f;
-            __align__(16) __half cf[CH];
-#pragma unroll
-            for (int j = 0; j < CH; ++j) cf[j] = __float2half_rn(0.f);
-            for (int k = 0; k < L; ++k) {
+            __align__(16) __half tl16[CH], cf[CH];
+    #pragma unroll
+            for (int k = 0; k < CH; ++k) {
                 sr += pr;
                 si += pi;
-                const float cr = b_r * pr - b_i * pi, cim = b_r * pi + b_i * pr;
-                cf[L - 1 - k] = __float2half_rn(is_im ? cim : cr);
+                tl16[k] = __float2half_rn(is_im ? pi : pr);
+                const float cr = b_r * pr - b_i * pi, ci = b_r * pi + b_i * pr;
+                cf[CH - 1 - k] = __float2half_rn(is_im ? ci : cr);
                 const float nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
                 pr = nr;
                 pi = ni;
             }
-#pragma unroll
-            for (int k8 = 0; k8 < CH / 8; ++k8)
+            // lambda^C by repeated squaring (fewer roundings than the running product)
+            float qr = lam_r, qi = lam_i;
+    #pragma unroll
+            for (int sq = 0; sq < 6; ++sq) {
+                const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
+                qr = nr;
+                qi = ni;
+            }
+            if (!is_im) {
+                laml[mm] = make_float2(qr, qi);  // lambda^C
+                suml[mm] = make_float2(sr, si);  // sum_{k<C} lambda^k
+            }
+    #pragma unroll
+            for (int k8 = 0; k8 < CH / 8; ++k8) {
+                *reinterpret_cast<uint4 *>(sm + S::TL16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
+                    *reinterpret_cast<const uint4 *>(&tl16[k8 * 8]);
                 *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
                     *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
-            if (!is_im) {
-                laml[mm] = make_float2(pr, pi);  // lambda^L
-                suml[mm] = make_float2(sr, si);  // sum_{k<L} lambda^k
             }
+    #pragma unroll
+            for (int k = 0; k < CH; ++k)
+                *reinterpret_cast<__half *>(sm + S::TA16 + kmaj_off(k, tl, 2, PADLBO, S::TY_SBO)) = tl16[k];
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) break;  // also carries a timeout of the in-prologue wait
-        tc_fence_after();
-
-        // ---- S2: G and P^T ------------------------------------------------------
-        if (warp == 0 && elect_one()) {
-            const uint32_t idg = idesc(128, 64, 0, 0);
-#pragma unroll
-            for (int s = 0; s < R / 16; ++s)
-                mma_f16(tb + T::G, sdesc_at(s16, S::XQ16 + s * 256, 128, 16 * R),
-                           sdesc_at(s16, S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
-            mma_commit(&bar[0]);
-        } else if (warp == 1 && elect_one()) {
-            // P^T from a second issuing thread, so that G's completion is not queued behind it
-            const uint32_t idp = idesc(128, 64, 2, 2);
-#pragma unroll
-            for (int s = 0; s < R / 8; ++s)
-                mma_tf32_t(tb + T::PT, tb + T::U + 8 * s, sdesc_at(s16, S::XQ32 + s * 256, 128, 32 * R), idp, s > 0);
-            mma_commit(&bar[6]);
-        }
-        __syncwarp();
-        ok = mbar_wait(&bar[0], par);
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) break;
-
-        // ---- S3: G' = skewed, masked G -----------------------------------------------
-        // scratch [64][64] rotated by row, over YA16: the raw tile there is consumed and
-        // YA16 is not rewritten before S5 (XQ32 may still be read by the P^T MMA)
-        float *scr = reinterpret_cast<float *>(sm + S::YA16);
-        if (q4 < 2) {
-            const int i = tl;
-#pragma unroll
-            for (int c0 = 32 * hsel; c0 < 32 * hsel + 32; c0 += 16) {
-                float v[16];
-                tmem_ld16(tb + lane_base + T::G + c0, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) scr[i * 64 + ((c0 + j + i) & 63)] = v[j];
-            }
-        }
-        __syncthreads();
-        {
-            const int i = tid >> 2, p = tid & 3;
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-                float g8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int k = 16 * p + 8 * h8 + e;
-                    g8[e] = k <= i ? scr[i * 64 + ((2 * i - k) & 63)] : 0.f;
-                }
-                *reinterpret_cast<uint4 *>(sm + S::GP16 + kmaj_off(i, 16 * p + 8 * h8, 2, 128, 1024)) = pack_f16x8(g8);
-            }
-        }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-
-        // ---- S4: L^T = T_L . G'^T -----------------------------------------------------
-        if (warp == 0 && elect_one()) {
-            const uint32_t id = idesc(128, 64, 0, 0);
-#pragma unroll
-            for (int s = 0; s < CH / 16; ++s)
-                mma_f16(tb + T::LT, sdesc_at(s16, S::TL16 + s * 256, 128, 1024),
-                           sdesc_at(s16, S::GP16 + s * 256, 128, 1024), id, s > 0);
-            mma_commit(&bar[1]);
-        }
-        __syncwarp();
-        ok = mbar_wait(&bar[1], par) && mbar_wait(&bar[6], par);
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) break;
-
-        // ---- S5: a, Ya (fp16, column-scaled), a' (tf32) ------------------------------------
-        // Lanes 2m, 2m+1 (planes Re / Im of mode m) split the 32 positions of the warp's half:
-        // the Re lane takes 32 hsel + p, the Im lane 32 hsel + 16 + p (p < 16), and each computes
-        // both planes there, so a mode's two planes are stored as one pair.  Complex values are
-        // held as (own, partner) components; with s = +1 on the Im lane and -1 on the Re lane,
-        // for z = (zo, zp) and w = (wr, wi): own(z w) = zo wr + zp (s wi), partner(z w) =
-        // zp wr - zo (s wi).  The operands hold (Re, -Im) per mode: -s own and +s partner.
         {
-            float *ymx = reinterpret_cast<float *>(sm + S::GP16);  // [2][128]; GP16 is consumed
-            const float sg = is_im ? 1.f : -1.f;
-            const float bs = sg * b_i, ls = sg * lam_i;
-            float pv[32], lv[32];
-            tmem_ld16(tb + lane_base + T::PT + 32 * hsel, pv);
-            tmem_ld16(tb + lane_base + T::PT + 32 * hsel + 16, pv + 16);
-            tmem_ld16(tb + lane_base + T::LT + 32 * hsel, lv);
-            tmem_ld16(tb + lane_base + T::LT + 32 * hsel + 16, lv + 16);
-            float wr = w0r, ws = sg * w0i;  // lambda^(i+1) at my first position, as (Re, s Im)
-            float yo[16], yq[16];           // Ya of my plane / of the partner plane, unscaled
-            float mo = 0.f, mq = 0.f;
-            const int ib = 32 * hsel + 16 * is_im;  // my first position
-            tmem_wait_ld();
-#pragma unroll
-            for (int p = 0; p < 16; ++p) {
-                // my plane at my position; the partner needs mine at its position
-                const float pm = is_im ? pv[16 + p] : pv[p], ps = is_im ? pv[p] : pv[16 + p];
-                const float lm = is_im ? lv[16 + p] : lv[p], lsd = is_im ? lv[p] : lv[16 + p];
-                const float po = __shfl_xor_sync(0xffffffffu, ps, 1);
-                const float lo = __shfl_xor_sync(0xffffffffu, lsd, 1);
-                // a = lambda^(i+1) P + B L
-                const float ao = fmaf(pm, wr, fmaf(po, ws, fmaf(lm, b_r, lo * bs)));
-                const float ap = fmaf(po, wr, fmaf(-pm, ws, fmaf(lo, b_r, -lm * bs)));
-                // Ya = a B: -s own(a B) = -s b_r ao - b_i ap ; s partner(a B) = s b_r ap - b_i ao
-                yo[p] = fmaf(ao, -sg * b_r, -b_i * ap);
-                yq[p] = fmaf(ap, sg * b_r, -b_i * ao);
-                mo = fmaxf(mo, fabsf(yo[p]));
-                mq = fmaxf(mq, fabsf(yq[p]));
-                // a' = a lambda^(i+1), both planes, Re plane first
-                const float qo = -sg * fmaf(ao, wr, ap * ws), qq = sg * fmaf(ap, wr, -ao * ws);
-                const uint32_t t_re = tf32_bits(is_im ? qq : qo), t_im = tf32_bits(is_im ? qo : qq);
-                *reinterpret_cast<uint2 *>(sm + S::AP32 + kmaj_off(ib + p, 2 * mm, 4, PADLBO, S::AP_SBO)) =
-                    make_uint2(t_re, t_im);
-                const float nr = fmaf(wr, lam_r, -ws * ls), ns = fmaf(wr, ls, ws * lam_r);
-                wr = nr;
-                ws = ns;
+            // start state: zero at the sequence start, else the state before block j0 from the
+            // block scan ([R+128 columns][128 lanes] floats, columns as in TMEM), by column half
+            const float *x0 = j0 > 0 ? seg_start + ((size_t)unit * (plan.nb - 1) + (j0 - 1)) * (size_t)(R + MP) * 128
+                                     : nullptr;
+            for (int c0 = hsel * 16; c0 < R + MP; c0 += 32) {
+                float z[16];
+    #pragma unroll
+                for (int i = 0; i < 16; ++i) z[i] = x0 ? x0[(size_t)(c0 + i) * 128 + tl] : 0.f;
+                tmem_st16(tb + lane_base + c0, z);
             }
-            // column (plane) maxima over the 64 positions: partner lane, then the other half
-            mo = fmaxf(mo, __shfl_xor_sync(0xffffffffu, mq, 1));
-            ymx[hsel * 128 + tl] = mo;
-            __syncthreads();
-            const int e = down_exp(fmaxf(ymx[tl], ymx[128 + tl]));
-            const int eq = __shfl_xor_sync(0xffffffffu, e, 1);
-            const float so = pow2i(-e), sq = pow2i(-eq);
-            // the Im lane writes its positions rotated by 4 so that a pair's stores hit other banks
-#pragma unroll
-            for (int p = 0; p < 16; ++p) {
-                const int pr = is_im ? ((p + 4) & 15) : p;
-                const float vo = (is_im ? yo[(p + 4) & 15] : yo[p]) * so;
-                const float vq = (is_im ? yq[(p + 4) & 15] : yq[p]) * sq;
-                *reinterpret_cast<uint32_t *>(sm + S::YA16 + kmaj_off(ib + pr, 2 * mm, 2, PADLBO, S::TY_SBO)) =
-                    is_im ? pack_h2(vq, vo) : pack_h2(vo, vq);
-            }
-            if (e != ya_exp) {
-                // T_A column tl = T_L row tl scaled by 2^e (exact in fp16); my half of k
-                const float sup = pow2i(e);
-#pragma unroll
-                for (int k8 = 0; k8 < 4; ++k8) {
-                    const int k0 = 32 * hsel + 8 * k8;
-                    __align__(16) __half t8[8];
-                    *reinterpret_cast<uint4 *>(t8) =
-                        *reinterpret_cast<const uint4 *>(sm + S::TL16 + kmaj_off(tl, k0, 2, 128, 1024));
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        *reinterpret_cast<__half *>(sm + S::TA16 + kmaj_off(k0 + u, tl, 2, PADLBO, S::TY_SBO)) =
-                            __float2half_rn(__half2float(t8[u]) * sup);
-                }
-                ya_exp = e;
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-
-        // ---- S6: A2' = Ya . T_A^T -----------------------------------------------------
-        if (warp == 0 && elect_one()) {
-            const uint32_t id = idesc(128, 64, 0, 0);
-#pragma unroll
-            for (int s = 0; s < MP / 16; ++s)
-                mma_f16(tb + T::G, sdesc_at(s16, S::YA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO),
-                           sdesc_at(s16, S::TA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO), id, s > 0);
-            mma_commit(&bar[2]);
-        } else if (warp == 1 && elect_one()) {
-            // O2 = Gamma^T . a'^T needs only S5's a' and the state: it runs under S7
-            const uint32_t id32 = idesc(128, 64, 2, 2);
-#pragma unroll
-            for (int s = 0; s < MP / 8; ++s)
-                mma_tf32_t(tb + T::LT, tb + T::GT + 8 * s, sdesc_at(s16, S::AP32 + s * 2 * PADLBO, PADLBO, S::AP_SBO),
-                            id32, s > 0);
-            mma_commit(&bar[3]);
-        }
-        __syncwarp();
-        ok = mbar_wait(&bar[2], par);
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) break;
-
-        // ---- S7: A2 = unskewed, masked A2' (row-scaled fp16) ------------------------------
-        // scratch over XQ32 (P^T, its last reader, is complete)
-        scr = reinterpret_cast<float *>(sm + S::XQ32);
-        if (q4 < 2) {
-            const int i = tl;
-#pragma unroll
-            for (int c0 = 32 * hsel; c0 < 32 * hsel + 32; c0 += 16) {
-                float v[16];
-                tmem_ld16(tb + lane_base + T::G + c0, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) scr[i * 64 + ((c0 + j + i) & 63)] = v[j];
-            }
-        }
-        __syncthreads();
-        {
-            const int i = tid >> 2, p = tid & 3;
-            float v16[16];
-            float amax = 0.f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int j = 16 * p + u;
-                v16[u] = j <= i ? scr[i * 64 + ((2 * i - j) & 63)] : 0.f;
-                amax = fmaxf(amax, fabsf(v16[u]));
-            }
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            const int e = down_exp(amax);
-            const float sdown = pow2i(-e);
-            if (p == 0) osc[i] = pow2i(e);
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-                float g8[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) g8[u] = v16[8 * h8 + u] * sdown;
-                *reinterpret_cast<uint4 *>(sm + S::A216 + kmaj_off(i, 16 * p + 8 * h8, 2, 128, 1024)) = pack_f16x8(g8);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-
-        // ---- S8: O1 = Vt^T . A2^T (O2 was issued with A2') -----------------------------------
-        if (warp == 0 && elect_one()) {
-            const uint32_t id16 = idesc(128, 64, 0, 0);
-            const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;  // value rows R .. R+127
-#pragma unroll
-            for (int s = 0; s < CH / 16; ++s)
-                mma_f16(tb + T::PT, sdesc_at(s16, vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
-                           sdesc_at(s16, S::A216 + s * 256, 128, 1024), id16, s > 0);
-            mma_commit(&bar[7]);
-        }
-        __syncwarp();
-        ok = mbar_wait(&bar[7], par) && mbar_wait(&bar[3], par);
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) break;
-
-        // ---- S9: next chunk's raw rows; outputs; state scaled by lambda^L -------------------
-        if (ci + 1 < c_end) {
-            tma_pending = 1;
-            if (tid == 0) {
-                // YA16 / AP32 were last read by the S6 / S8 MMAs, both complete
-                const int tn = t0 + CH;
-                mbar_arrive_expect_tx(&bar[5], raw_bytes);
-                tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, tn - HALO, b, &bar[5]);
-                tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[5]);
-                tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[5]);
-            }
-        }
-        {
-            // outputs o[i][jv] into the [64][D] bf16 store tile over XQ32 (free until the next
-            // prologue; thread 0 waits for the tile's bulk store before that prologue starts)
-            const int jv = tl;
-            __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + S::XQ32);
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c0 = 32 * hsel + 16 * cc;
-                float o1[16], o2[16], s16[16];
-                tmem_ld16(tb + lane_base + T::PT + c0, o1);
-                tmem_ld16(tb + lane_base + T::LT + c0, o2);
-#pragma unroll
-                for (int j4 = 0; j4 < 4; ++j4)
-                    *reinterpret_cast<float4 *>(s16 + 4 * j4) = *reinterpret_cast<const float4 *>(osc + c0 + 4 * j4);
-                tmem_wait_ld();
-                if (jv < D) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) otile[(c0 + j) * D + jv] = __float2bfloat16_rn(fmaf(o1[j], s16[j], o2[j]));
-                }
-            }
-            fence_proxy_async_smem();
-            if (hsel == 0 && !is_im) {
-                // eta <- lambda^L eta + B sum_{k<L} lambda^k
-                const float2 ll = laml[mm], sl = suml[mm];
-                const float sr = sl.x, si = sl.y;
-                const float er = ll.x * eta_r - ll.y * eta_i + b_r * sr - b_i * si;
-                const float ei = ll.x * eta_i + ll.y * eta_r + b_r * si + b_i * sr;
-                eta_r = er;
-                eta_i = ei;
-            }
-            // U (lanes = mode planes): the partner lane holds the other component
-            const float2 lm = laml[mm];
-            {
-                constexpr int NB = R / 32;  // 16-column blocks in my half of U
-                float v[NB][16];
-#pragma unroll
-                for (int bb = 0; bb < NB; ++bb) tmem_ld16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
-                tmem_wait_ld();
-                // own(lambda^L x) = own(x) Re lambda^L + partner(x) s Im lambda^L, s = +1 on Im planes
-                const float lms = is_im ? lm.y : -lm.y;
-#pragma unroll
-                for (int bb = 0; bb < NB; ++bb) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float o = __shfl_xor_sync(0xffffffffu, v[bb][j], 1);
-                        v[bb][j] = fmaf(v[bb][j], lm.x, o * lms);
-                    }
-                    tmem_st16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
-                }
-            }
-            // Gamma^T (lanes = value channels, columns = (Re, Im) per mode)
-            {
-                float v[4][16];
-#pragma unroll
-                for (int bb = 0; bb < 4; ++bb) tmem_ld16(tb + lane_base + T::GT + 64 * hsel + 16 * bb, v[bb]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int bb = 0; bb < 4; ++bb) {
-#pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const float2 l2 = laml[(64 * hsel + 16 * bb + j) >> 1];
-                        const float xr = v[bb][j], xi = v[bb][j + 1];
-                        v[bb][j] = l2.x * xr - l2.y * xi;
-                        v[bb][j + 1] = l2.x * xi + l2.y * xr;
-                    }
-                    tmem_st16(tb + lane_base + T::GT + 64 * hsel + 16 * bb, v[bb]);
+            if (hsel == 0) {
+                // conv taps of channels 8*(tl % (R/8)) .. +7, right-aligned: column 32*which + 4*e + jj
+                // multiplies position i - 3 + jj (zero for jj < 4 - W)
+                const int cbl = tl % (R / 8);
+    #pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    const float *cwg = a.conv_w + ((size_t)(which * H + h) * R + 8 * cbl) * W;
+                    float t32[32];
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e)
+    #pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) t32[4 * e + jj] = jj >= 4 - W ? cwg[e * W + jj - (4 - W)] : 0.f;
+                    tmem_st16(tb + lane_base + T::TAPS + 32 * which, t32);
+                    tmem_st16(tb + lane_base + T::TAPS + 32 * which + 16, t32 + 16);
                 }
             }
             tmem_wait_st();
         }
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-
-        // ---- S10: U += Coef . Kt ; Gamma^T += Vt^T . Coef^T -----------------------------------
+        tma_pending = 1;
         if (tid == 0) {
-            // the chunk's output rows; rows past N are clipped by the copy (thread 0 owns the
-            // bulk group it waits on before the next prologue)
-            tma_store_4d(&tm_o, 0, h, t0, b, sm + S::XQ32);
-            bulk_commit();
+            const int tb0 = c_begin * CH;
+            mbar_arrive_expect_tx(&bar[5], raw_bytes);
+            tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, tb0 - HALO, b, &bar[5]);
+            tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tb0 - HALO, b, &bar[5]);
+            tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tb0, b, &bar[5]);
         }
-        if (warp == 0 && elect_one()) {
-            const uint32_t idu = idesc(128, R, 0, 0);
-#pragma unroll
-            for (int s = 0; s < CH / 16; ++s)
-                mma_f16(tb + T::U, sdesc_at(s16, S::CF16 + s * 256, 128, 1024),
-                           sdesc_at(s16, S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, 1);
-            const uint32_t idg = idesc(128, MP, 0, 0);
-            const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;
-#pragma unroll
-            for (int s = 0; s < CH / 16; ++s)
-                mma_f16(tb + T::GT, sdesc_at(s16, vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
-                           sdesc_at(s16, S::CF16 + s * 256, 128, 1024), idg, 1);
-            mma_commit(&bar[4]);
-        }
-        __syncwarp();
-    }
 
-    // ---- final state ------------------------------------------------------------------
-    if (tid == 0) bulk_wait_all();  // output stores complete before shared memory is released
-    if (ok && c_end > c_begin) {
-        ok = mbar_wait(&bar[4], (c_end - 1 - c_begin) & 1);
-        tc_fence_after();
-    }
-    ok = !__syncthreads_or(!ok);
-    if (!ok) {
-        // error path: let a copy still in flight land before the CTA exits
-        if (tma_pending) mbar_wait(&bar[5], (uint32_t)((ci - c_begin) & 1), 200000000LL);
-        if (tid == 0) report_error(a.err, kErrWaitTimeout);
-    }
-    if (ok && a.final_state && seg == nseg - 1) {
-        float *fs = a.final_state + (size_t)unit * a.state_floats;
-        const int RD = R + D;
-        const size_t plane = (size_t)M * RD;
-        // U: plane tl -> row (Re: m, Im: M + m), my half of the columns
-#pragma unroll
-        for (int c0 = hsel * (R / 2); c0 < (hsel + 1) * (R / 2); c0 += 16) {
-            float v[16];
-            tmem_ld16(tb + lane_base + T::U + c0, v);
-            tmem_wait_ld();
-            float *row = fs + (is_im ? plane : 0) + (size_t)mm * RD + c0;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) row[j] = v[j];
-        }
-        // Gamma^T: value lane tl writes column R + tl of every row, my half of the modes
-#pragma unroll
-        for (int c0 = 64 * hsel; c0 < 64 * hsel + 64; c0 += 16) {
-            float v[16];
-            tmem_ld16(tb + lane_base + T::GT + c0, v);
-            tmem_wait_ld();
-            if (tl < D) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int pl = c0 + j, m = pl >> 1;
-                    fs[((pl & 1) ? plane : 0) + (size_t)m * RD + R + tl] = v[j];
-                }
+
+        // eta of my mode at the piece start, B sum_{k < t_begin} lambda^k (hsel == 0, Re thread)
+        float eta_r = 0.f, eta_i = 0.f;
+        if (hsel == 0 && !is_im) {
+            const float2 ll = laml[mm], sl = suml[mm];
+            for (int c = 0; c < c_begin; ++c) {
+                const float er = ll.x * eta_r - ll.y * eta_i + b_r * sl.x - b_i * sl.y;
+                const float ei = ll.x * eta_i + ll.y * eta_r + b_r * sl.y + b_i * sl.x;
+                eta_r = er;
+                eta_i = ei;
             }
         }
-        if (hsel == 0 && !is_im) {
-            fs[2 * plane + mm] = eta_r;
-            fs[2 * plane + M + mm] = eta_i;
+        int ya_exp = 0;  // scale exponent of my T_A column currently stored
+        ci = c_begin;
+
+        for (; ci < c_end; ++ci, ++it) {
+            const int t0 = ci * CH;
+            const int L = min(CH, N - t0);
+            const uint32_t par = it & 1;
+
+            // this chunk's raw rows (the previous chunk's state-update MMAs, which read ZT16 and
+            // CF16, are waited for inside the prologue, just before ZT16 is rewritten)
+            ok = mbar_wait(&bar[5], par);
+            if (ok) tma_pending = 0;
+            if (tid == 0) bulk_wait_read_all();  // the previous output tile has left XQ32
+            tc_fence_after();
+            if (__syncthreads_or(!ok)) break;
+
+            // ---- S1: prologue, thread = (8-channel block, block of consecutive positions)
+            {
+                // query / key: R/8 channel blocks x (64 R/8 / 256) positions per thread
+                constexpr int CBQ = R / 8, PPQ = CH * CBQ / NTH;
+                const int cb = tid % CBQ, i0 = (tid / CBQ) * PPQ, c0 = 8 * cb;
+                // rows are stored rotated: at step pp this thread writes position i0 + (pp + rot) % PPQ,
+                // so the channel-block threads of one position hit different banks
+                const int rot = cb % PPQ;
+                float tq[32], tk[32];  // taps of my channel block (TMEM lane tl holds block tl % CBQ == cb)
+                tmem_ld16(tb + lane_base + T::TAPS, tq);
+                tmem_ld16(tb + lane_base + T::TAPS + 16, tq + 16);
+                tmem_ld16(tb + lane_base + T::TAPS + 32, tk);
+                tmem_ld16(tb + lane_base + T::TAPS + 48, tk + 16);
+                float nwk[8], bsk[8];
+                *reinterpret_cast<float4 *>(nwk) = *reinterpret_cast<const float4 *>(nws + c0);
+                *reinterpret_cast<float4 *>(nwk + 4) = *reinterpret_cast<const float4 *>(nws + c0 + 4);
+                *reinterpret_cast<float4 *>(bsk) = *reinterpret_cast<const float4 *>(bss + c0);
+                *reinterpret_cast<float4 *>(bsk + 4) = *reinterpret_cast<const float4 *>(bss + c0 + 4);
+                tmem_wait_ld();
+                float fk[PPQ][8];
+    #pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    const unsigned char *raw = sm + (which == 0 ? S::RAWQ : S::RAWK);
+                    const float *w8 = which == 0 ? tq : tk;
+                    // rows i0 .. i0+PPQ+2 of the staged tile = positions i0-3 .. i0+PPQ-1
+                    float f[PPQ][8];
+    #pragma unroll
+                    for (int pp = 0; pp < PPQ; ++pp)
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) f[pp][e] = 0.f;
+    #pragma unroll
+                    for (int r = 0; r < PPQ + HALO; ++r) {
+                        float x8[8];
+                        unpack_bf16x8(*reinterpret_cast<const uint4 *>(raw + ((size_t)(i0 + r) * R + c0) * 2), x8);
+                        // tile row r holds position i0 + r - 3: right-aligned tap jj = r - pp of position pp
+    #pragma unroll
+                        for (int pp = 0; pp < PPQ; ++pp) {
+                            const int jj = r - pp;
+                            if (jj >= 0 && jj < 4)
+    #pragma unroll
+                                for (int e = 0; e < 8; ++e) f[pp][e] = fmaf(w8[4 * e + jj], x8[e], f[pp][e]);
+                        }
+                    }
+                    float acc[PPQ];
+    #pragma unroll
+                    for (int pp = 0; pp < PPQ; ++pp) {
+                        acc[pp] = 0.f;
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            f[pp][e] = silu_tanh(f[pp][e]);
+                            acc[pp] = fmaf(f[pp][e], f[pp][e], acc[pp]);
+                        }
+                    }
+    #pragma unroll
+                    for (int pp = 0; pp < PPQ; ++pp) {
+    #pragma unroll
+                        for (int o = 1; o < CBQ; o <<= 1) acc[pp] += __shfl_xor_sync(0xffffffffu, acc[pp], o);
+                        const float inv = (i0 + pp < L) ? __fdividef(1.f, acc[pp] + IDA_EPS_FEAT) : 0.f;
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) f[pp][e] *= inv;
+                    }
+                    if (which == 0) {
+                        // xi(q) rows: fp16 for the Gram MMA, tf32 for the state read-out MMA
+                        uint32_t h16[PPQ][4], t32[PPQ][8];
+    #pragma unroll
+                        for (int pp = 0; pp < PPQ; ++pp) {
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e) h16[pp][e] = pack_h2(f[pp][2 * e], f[pp][2 * e + 1]);
+    #pragma unroll
+                            for (int e = 0; e < 8; ++e) t32[pp][e] = tf32_bits(f[pp][e]);
+                        }
+    #pragma unroll
+                        for (int pp = 0; pp < PPQ; ++pp) {
+                            const int q = (pp + rot) % PPQ, i = i0 + q;
+                            uint32_t hs[4], ts[8];
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                uint32_t v = h16[0][e];
+    #pragma unroll
+                                for (int u = 1; u < PPQ; ++u) v = q == u ? h16[u][e] : v;
+                                hs[e] = v;
+                            }
+    #pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                uint32_t v = t32[0][e];
+    #pragma unroll
+                                for (int u = 1; u < PPQ; ++u) v = q == u ? t32[u][e] : v;
+                                ts[e] = v;
+                            }
+                            *reinterpret_cast<uint4 *>(sm + S::XQ16 + kmaj_off(i, c0, 2, 128, 16 * R)) =
+                                make_uint4(hs[0], hs[1], hs[2], hs[3]);
+                            *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0, 4, 128, 32 * R)) =
+                                make_uint4(ts[0], ts[1], ts[2], ts[3]);
+                            *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0 + 4, 4, 128, 32 * R)) =
+                                make_uint4(ts[4], ts[5], ts[6], ts[7]);
+                        }
+                    } else {
+    #pragma unroll
+                        for (int pp = 0; pp < PPQ; ++pp)
+    #pragma unroll
+                            for (int e = 0; e < 8; ++e) fk[pp][e] = f[pp][e];
+                    }
+                }
+                // key RMSNorm + affine, packed to fp16 once for the Kt rows (rotated) and the
+                // transposed key rows of Z^T
+                uint32_t hk[PPQ][4];
+    #pragma unroll
+                for (int pp = 0; pp < PPQ; ++pp) {
+                    float ms = 0.f;
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) ms = fmaf(fk[pp][e], fk[pp][e], ms);
+    #pragma unroll
+                    for (int o = 1; o < CBQ; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
+                    const float rk = rsqrtf(ms / R + IDA_EPS_RMS);
+                    const bool valid = i0 + pp < L;
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) fk[pp][e] = valid ? fmaf(fk[pp][e] * rk, nwk[e], bsk[e]) : 0.f;
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) hk[pp][e] = pack_h2(fk[pp][2 * e], fk[pp][2 * e + 1]);
+                }
+    #pragma unroll
+                for (int pp = 0; pp < PPQ; ++pp) {
+                    const int q = (pp + rot) % PPQ, i = i0 + q;
+                    uint32_t hs[4];
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t v = hk[0][e];
+    #pragma unroll
+                        for (int u = 1; u < PPQ; ++u) v = q == u ? hk[u][e] : v;
+                        hs[e] = v;
+                    }
+                    *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) =
+                        make_uint4(hs[0], hs[1], hs[2], hs[3]);
+                }
+                if (it > 0 && !mbar_wait(&bar[4], par ^ 1)) ok = false;
+    #pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    // channel c0 + e at positions i0 .. i0 + PPQ - 1: pairs of halves from hk
+                    const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+                    unsigned char *dst = sm + S::ZT16 + kmaj_off(c0 + e, i0, 2, PADLBO, S::ZT_SBO);
+                    const uint32_t w01 = __byte_perm(hk[0][e >> 1], hk[1][e >> 1], sel);
+                    if constexpr (PPQ == 4)
+                        *reinterpret_cast<uint2 *>(dst) = make_uint2(w01, __byte_perm(hk[2][e >> 1], hk[3][e >> 1], sel));
+                    else
+                        *reinterpret_cast<uint32_t *>(dst) = w01;
+                }
+            }
+            {
+                // value: D/8 channel blocks x (64 D/8 / 256) positions per thread
+                constexpr int CBV = D / 8, PPV = CH * CBV / NTH;
+                const int cb = tid % CBV, i0 = (tid / CBV) * PPV, j0 = 8 * cb;
+                float nwv[8], bsv[8];
+                *reinterpret_cast<float4 *>(nwv) = *reinterpret_cast<const float4 *>(nws + R + j0);
+                *reinterpret_cast<float4 *>(nwv + 4) = *reinterpret_cast<const float4 *>(nws + R + j0 + 4);
+                *reinterpret_cast<float4 *>(bsv) = *reinterpret_cast<const float4 *>(bss + R + j0);
+                *reinterpret_cast<float4 *>(bsv + 4) = *reinterpret_cast<const float4 *>(bss + R + j0 + 4);
+                float vt[PPV][8];
+    #pragma unroll
+                for (int pp = 0; pp < PPV; ++pp) {
+                    const int i = i0 + pp;
+                    float x8[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(sm + S::RAWV + ((size_t)i * D + j0) * 2), x8);
+                    float ms = 0.f;
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) ms = fmaf(x8[e], x8[e], ms);
+    #pragma unroll
+                    for (int o = 1; o < CBV; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
+                    const float rv = rsqrtf(ms / D + IDA_EPS_RMS);
+                    const bool valid = i < L;
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) vt[pp][e] = valid ? fmaf(x8[e] * rv, nwv[e], bsv[e]) : 0.f;
+                }
+    #pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    unsigned char *dst = sm + S::ZT16 + kmaj_off(R + j0 + e, i0, 2, PADLBO, S::ZT_SBO);
+                    const uint32_t w01 = pack_h2(vt[0][e], vt[1][e]);
+                    if constexpr (PPV == 4)
+                        *reinterpret_cast<uint2 *>(dst) = make_uint2(w01, pack_h2(vt[2][e], vt[3][e]));
+                    else
+                        *reinterpret_cast<uint32_t *>(dst) = w01;
+                }
+            }
+            if (L < CH && hsel == 0) {
+                // ragged last chunk: Coef row = component of B lambda^(L-1-j) for j < L, else 0
+                float pr = 1.f, pi = 0.f, sr = 0.f, si = 0.f;
+                __align__(16) __half cf[CH];
+    #pragma unroll
+                for (int j = 0; j < CH; ++j) cf[j] = __float2half_rn(0.f);
+                for (int k = 0; k < L; ++k) {
+                    sr += pr;
+                    si += pi;
+                    const float cr = b_r * pr - b_i * pi, cim = b_r * pi + b_i * pr;
+                    cf[L - 1 - k] = __float2half_rn(is_im ? cim : cr);
+                    const float nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
+                    pr = nr;
+                    pi = ni;
+                }
+    #pragma unroll
+                for (int k8 = 0; k8 < CH / 8; ++k8)
+                    *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
+                        *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
+                if (!is_im) {
+                    laml[mm] = make_float2(pr, pi);  // lambda^L
+                    suml[mm] = make_float2(sr, si);  // sum_{k<L} lambda^k
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (__syncthreads_or(!ok)) break;  // also carries a timeout of the in-prologue wait
+            tc_fence_after();
+
+            // ---- S2: G and P^T ------------------------------------------------------
+            if (warp == 0 && elect_one()) {
+                const uint32_t idg = idesc(128, 64, 0, 0);
+    #pragma unroll
+                for (int s = 0; s < R / 16; ++s)
+                    mma_f16(tb + T::G, sdesc_at(s16, S::XQ16 + s * 256, 128, 16 * R),
+                               sdesc_at(s16, S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
+                mma_commit(&bar[0]);
+            } else if (warp == 1 && elect_one()) {
+                // P^T from a second issuing thread, so that G's completion is not queued behind it
+                const uint32_t idp = idesc(128, 64, 2, 2);
+    #pragma unroll
+                for (int s = 0; s < R / 8; ++s)
+                    mma_tf32_t(tb + T::PT, tb + T::U + 8 * s, sdesc_at(s16, S::XQ32 + s * 256, 128, 32 * R), idp, s > 0);
+                mma_commit(&bar[6]);
+            }
+            __syncwarp();
+            ok = mbar_wait(&bar[0], par);
+            tc_fence_after();
+            if (__syncthreads_or(!ok)) break;
+
+            // ---- S3: G' = skewed, masked G -----------------------------------------------
+            // scratch [64][64] rotated by row, over YA16: the raw tile there is consumed and
+            // YA16 is not rewritten before S5 (XQ32 may still be read by the P^T MMA)
+            float *scr = reinterpret_cast<float *>(sm + S::YA16);
+            if (q4 < 2) {
+                const int i = tl;
+    #pragma unroll
+                for (int c0 = 32 * hsel; c0 < 32 * hsel + 32; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(tb + lane_base + T::G + c0, v);
+                    tmem_wait_ld();
+    #pragma unroll
+                    for (int j = 0; j < 16; ++j) scr[i * 64 + ((c0 + j + i) & 63)] = v[j];
+                }
+            }
+            __syncthreads();
+            {
+                const int i = tid >> 2, p = tid & 3;
+    #pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    float g8[8];
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int k = 16 * p + 8 * h8 + e;
+                        g8[e] = k <= i ? scr[i * 64 + ((2 * i - k) & 63)] : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(sm + S::GP16 + kmaj_off(i, 16 * p + 8 * h8, 2, 128, 1024)) = pack_f16x8(g8);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+
+            // ---- S4: L^T = T_L . G'^T -----------------------------------------------------
+            if (warp == 0 && elect_one()) {
+                const uint32_t id = idesc(128, 64, 0, 0);
+    #pragma unroll
+                for (int s = 0; s < CH / 16; ++s)
+                    mma_f16(tb + T::LT, sdesc_at(s16, S::TL16 + s * 256, 128, 1024),
+                               sdesc_at(s16, S::GP16 + s * 256, 128, 1024), id, s > 0);
+                mma_commit(&bar[1]);
+            }
+            __syncwarp();
+            ok = mbar_wait(&bar[1], par) && mbar_wait(&bar[6], par);
+            tc_fence_after();
+            if (__syncthreads_or(!ok)) break;
+
+            // ---- S5: a, Ya (fp16, column-scaled), a' (tf32) ------------------------------------
+            // Lanes 2m, 2m+1 (planes Re / Im of mode m) split the 32 positions of the warp's half:
+            // the Re lane takes 32 hsel + p, the Im lane 32 hsel + 16 + p (p < 16), and each computes
+            // both planes there, so a mode's two planes are stored as one pair.  Complex values are
+            // held as (own, partner) components; with s = +1 on the Im lane and -1 on the Re lane,
+            // for z = (zo, zp) and w = (wr, wi): own(z w) = zo wr + zp (s wi), partner(z w) =
+            // zp wr - zo (s wi).  The operands hold (Re, -Im) per mode: -s own and +s partner.
+            {
+                float *ymx = reinterpret_cast<float *>(sm + S::GP16);  // [2][128]; GP16 is consumed
+                const float sg = is_im ? 1.f : -1.f;
+                const float bs = sg * b_i, ls = sg * lam_i;
+                float pv[32], lv[32];
+                tmem_ld16(tb + lane_base + T::PT + 32 * hsel, pv);
+                tmem_ld16(tb + lane_base + T::PT + 32 * hsel + 16, pv + 16);
+                tmem_ld16(tb + lane_base + T::LT + 32 * hsel, lv);
+                tmem_ld16(tb + lane_base + T::LT + 32 * hsel + 16, lv + 16);
+                float wr = w0r, ws = sg * w0i;  // lambda^(i+1) at my first position, as (Re, s Im)
+                float yo[16], yq[16];           // Ya of my plane / of the partner plane, unscaled
+                float mo = 0.f, mq = 0.f;
+                const int ib = 32 * hsel + 16 * is_im;  // my first position
+                tmem_wait_ld();
+    #pragma unroll
+                for (int p = 0; p < 16; ++p) {
+                    // my plane at my position; the partner needs mine at its position
+                    const float pm = is_im ? pv[16 + p] : pv[p], ps = is_im ? pv[p] : pv[16 + p];
+                    const float lm = is_im ? lv[16 + p] : lv[p], lsd = is_im ? lv[p] : lv[16 + p];
+                    const float po = __shfl_xor_sync(0xffffffffu, ps, 1);
+                    const float lo = __shfl_xor_sync(0xffffffffu, lsd, 1);
+                    // a = lambda^(i+1) P + B L
+                    const float ao = fmaf(pm, wr, fmaf(po, ws, fmaf(lm, b_r, lo * bs)));
+                    const float ap = fmaf(po, wr, fmaf(-pm, ws, fmaf(lo, b_r, -lm * bs)));
+                    // Ya = a B: -s own(a B) = -s b_r ao - b_i ap ; s partner(a B) = s b_r ap - b_i ao
+                    yo[p] = fmaf(ao, -sg * b_r, -b_i * ap);
+                    yq[p] = fmaf(ap, sg * b_r, -b_i * ao);
+                    mo = fmaxf(mo, fabsf(yo[p]));
+                    mq = fmaxf(mq, fabsf(yq[p]));
+                    // a' = a lambda^(i+1), both planes, Re plane first
+                    const float qo = -sg * fmaf(ao, wr, ap * ws), qq = sg * fmaf(ap, wr, -ao * ws);
+                    const uint32_t t_re = tf32_bits(is_im ? qq : qo), t_im = tf32_bits(is_im ? qo : qq);
+                    *reinterpret_cast<uint2 *>(sm + S::AP32 + kmaj_off(ib + p, 2 * mm, 4, PADLBO, S::AP_SBO)) =
+                        make_uint2(t_re, t_im);
+                    const float nr = fmaf(wr, lam_r, -ws * ls), ns = fmaf(wr, ls, ws * lam_r);
+                    wr = nr;
+                    ws = ns;
+                }
+                // column (plane) maxima over the 64 positions: partner lane, then the other half
+                mo = fmaxf(mo, __shfl_xor_sync(0xffffffffu, mq, 1));
+                ymx[hsel * 128 + tl] = mo;
+                __syncthreads();
+                const int e = down_exp(fmaxf(ymx[tl], ymx[128 + tl]));
+                const int eq = __shfl_xor_sync(0xffffffffu, e, 1);
+                const float so = pow2i(-e), sq = pow2i(-eq);
+                // the Im lane writes its positions rotated by 4 so that a pair's stores hit other banks
+    #pragma unroll
+                for (int p = 0; p < 16; ++p) {
+                    const int pr = is_im ? ((p + 4) & 15) : p;
+                    const float vo = (is_im ? yo[(p + 4) & 15] : yo[p]) * so;
+                    const float vq = (is_im ? yq[(p + 4) & 15] : yq[p]) * sq;
+                    *reinterpret_cast<uint32_t *>(sm + S::YA16 + kmaj_off(ib + pr, 2 * mm, 2, PADLBO, S::TY_SBO)) =
+                        is_im ? pack_h2(vq, vo) : pack_h2(vo, vq);
+                }
+                if (e != ya_exp) {
+                    // T_A column tl = T_L row tl scaled by 2^e (exact in fp16); my half of k
+                    const float sup = pow2i(e);
+    #pragma unroll
+                    for (int k8 = 0; k8 < 4; ++k8) {
+                        const int k0 = 32 * hsel + 8 * k8;
+                        __align__(16) __half t8[8];
+                        *reinterpret_cast<uint4 *>(t8) =
+                            *reinterpret_cast<const uint4 *>(sm + S::TL16 + kmaj_off(tl, k0, 2, 128, 1024));
+    #pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            *reinterpret_cast<__half *>(sm + S::TA16 + kmaj_off(k0 + u, tl, 2, PADLBO, S::TY_SBO)) =
+                                __float2half_rn(__half2float(t8[u]) * sup);
+                    }
+                    ya_exp = e;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+
+            // ---- S6: A2' = Ya . T_A^T -----------------------------------------------------
+            if (warp == 0 && elect_one()) {
+                const uint32_t id = idesc(128, 64, 0, 0);
+    #pragma unroll
+                for (int s = 0; s < MP / 16; ++s)
+                    mma_f16(tb + T::G, sdesc_at(s16, S::YA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO),
+                               sdesc_at(s16, S::TA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO), id, s > 0);
+                mma_commit(&bar[2]);
+            } else if (warp == 1 && elect_one()) {
+                // O2 = Gamma^T . a'^T needs only S5's a' and the state: it runs under S7
+                const uint32_t id32 = idesc(128, 64, 2, 2);
+    #pragma unroll
+                for (int s = 0; s < MP / 8; ++s)
+                    mma_tf32_t(tb + T::LT, tb + T::GT + 8 * s, sdesc_at(s16, S::AP32 + s * 2 * PADLBO, PADLBO, S::AP_SBO),
+                                id32, s > 0);
+                mma_commit(&bar[3]);
+            }
+            __syncwarp();
+            ok = mbar_wait(&bar[2], par);
+            tc_fence_after();
+            if (__syncthreads_or(!ok)) break;
+
+            // ---- S7: A2 = unskewed, masked A2' (row-scaled fp16) ------------------------------
+            // scratch over XQ32 (P^T, its last reader, is complete)
+            scr = reinterpret_cast<float *>(sm + S::XQ32);
+            if (q4 < 2) {
+                const int i = tl;
+    #pragma unroll
+                for (int c0 = 32 * hsel; c0 < 32 * hsel + 32; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(tb + lane_base + T::G + c0, v);
+                    tmem_wait_ld();
+    #pragma unroll
+                    for (int j = 0; j < 16; ++j) scr[i * 64 + ((c0 + j + i) & 63)] = v[j];
+                }
+            }
+            __syncthreads();
+            {
+                const int i = tid >> 2, p = tid & 3;
+                float v16[16];
+                float amax = 0.f;
+    #pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int j = 16 * p + u;
+                    v16[u] = j <= i ? scr[i * 64 + ((2 * i - j) & 63)] : 0.f;
+                    amax = fmaxf(amax, fabsf(v16[u]));
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const int e = down_exp(amax);
+                const float sdown = pow2i(-e);
+                if (p == 0) osc[i] = pow2i(e);
+    #pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    float g8[8];
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) g8[u] = v16[8 * h8 + u] * sdown;
+                    *reinterpret_cast<uint4 *>(sm + S::A216 + kmaj_off(i, 16 * p + 8 * h8, 2, 128, 1024)) = pack_f16x8(g8);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+
+            // ---- S8: O1 = Vt^T . A2^T (O2 was issued with A2') -----------------------------------
+            if (warp == 0 && elect_one()) {
+                const uint32_t id16 = idesc(128, 64, 0, 0);
+                const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;  // value rows R .. R+127
+    #pragma unroll
+                for (int s = 0; s < CH / 16; ++s)
+                    mma_f16(tb + T::PT, sdesc_at(s16, vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
+                               sdesc_at(s16, S::A216 + s * 256, 128, 1024), id16, s > 0);
+                mma_commit(&bar[7]);
+            }
+            __syncwarp();
+            ok = mbar_wait(&bar[7], par) && mbar_wait(&bar[3], par);
+            tc_fence_after();
+            if (__syncthreads_or(!ok)) break;
+
+            // ---- S9: next chunk's raw rows; outputs; state scaled by lambda^L -------------------
+            if (ci + 1 < c_end) {
+                tma_pending = 1;
+                if (tid == 0) {
+                    // YA16 / AP32 were last read by the S6 / S8 MMAs, both complete
+                    const int tn = t0 + CH;
+                    mbar_arrive_expect_tx(&bar[5], raw_bytes);
+                    tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, tn - HALO, b, &bar[5]);
+                    tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[5]);
+                    tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[5]);
+                }
+            }
+            {
+                // outputs o[i][jv] into the [64][D] bf16 store tile over XQ32 (free until the next
+                // prologue; thread 0 waits for the tile's bulk store before that prologue starts)
+                const int jv = tl;
+                __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + S::XQ32);
+    #pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c0 = 32 * hsel + 16 * cc;
+                    float o1[16], o2[16], s16[16];
+                    tmem_ld16(tb + lane_base + T::PT + c0, o1);
+                    tmem_ld16(tb + lane_base + T::LT + c0, o2);
+    #pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        *reinterpret_cast<float4 *>(s16 + 4 * j4) = *reinterpret_cast<const float4 *>(osc + c0 + 4 * j4);
+                    tmem_wait_ld();
+                    if (jv < D) {
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) otile[(c0 + j) * D + jv] = __float2bfloat16_rn(fmaf(o1[j], s16[j], o2[j]));
+                    }
+                }
+                fence_proxy_async_smem();
+                if (hsel == 0 && !is_im) {
+                    // eta <- lambda^L eta + B sum_{k<L} lambda^k
+                    const float2 ll = laml[mm], sl = suml[mm];
+                    const float sr = sl.x, si = sl.y;
+                    const float er = ll.x * eta_r - ll.y * eta_i + b_r * sr - b_i * si;
+                    const float ei = ll.x * eta_i + ll.y * eta_r + b_r * si + b_i * sr;
+                    eta_r = er;
+                    eta_i = ei;
+                }
+                // U (lanes = mode planes): the partner lane holds the other component
+                const float2 lm = laml[mm];
+                {
+                    constexpr int NB = R / 32;  // 16-column blocks in my half of U
+                    float v[NB][16];
+    #pragma unroll
+                    for (int bb = 0; bb < NB; ++bb) tmem_ld16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
+                    tmem_wait_ld();
+                    // own(lambda^L x) = own(x) Re lambda^L + partner(x) s Im lambda^L, s = +1 on Im planes
+                    const float lms = is_im ? lm.y : -lm.y;
+    #pragma unroll
+                    for (int bb = 0; bb < NB; ++bb) {
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float o = __shfl_xor_sync(0xffffffffu, v[bb][j], 1);
+                            v[bb][j] = fmaf(v[bb][j], lm.x, o * lms);
+                        }
+                        tmem_st16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
+                    }
+                }
+                // Gamma^T (lanes = value channels, columns = (Re, Im) per mode)
+                {
+                    float v[4][16];
+    #pragma unroll
+                    for (int bb = 0; bb < 4; ++bb) tmem_ld16(tb + lane_base + T::GT + 64 * hsel + 16 * bb, v[bb]);
+                    tmem_wait_ld();
+    #pragma unroll
+                    for (int bb = 0; bb < 4; ++bb) {
+    #pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            const float2 l2 = laml[(64 * hsel + 16 * bb + j) >> 1];
+                            const float xr = v[bb][j], xi = v[bb][j + 1];
+                            v[bb][j] = l2.x * xr - l2.y * xi;
+                            v[bb][j + 1] = l2.x * xi + l2.y * xr;
+                        }
+                        tmem_st16(tb + lane_base + T::GT + 64 * hsel + 16 * bb, v[bb]);
+                    }
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+
+            // ---- S10: U += Coef . Kt ; Gamma^T += Vt^T . Coef^T -----------------------------------
+            if (tid == 0) {
+                // the chunk's output rows; rows past N are clipped by the copy (thread 0 owns the
+                // bulk group it waits on before the next prologue)
+                tma_store_4d(&tm_o, 0, h, t0, b, sm + S::XQ32);
+                bulk_commit();
+            }
+            if (warp == 0 && elect_one()) {
+                const uint32_t idu = idesc(128, R, 0, 0);
+    #pragma unroll
+                for (int s = 0; s < CH / 16; ++s)
+                    mma_f16(tb + T::U, sdesc_at(s16, S::CF16 + s * 256, 128, 1024),
+                               sdesc_at(s16, S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, 1);
+                const uint32_t idg = idesc(128, MP, 0, 0);
+                const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;
+    #pragma unroll
+                for (int s = 0; s < CH / 16; ++s)
+                    mma_f16(tb + T::GT, sdesc_at(s16, vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
+                               sdesc_at(s16, S::CF16 + s * 256, 128, 1024), idg, 1);
+                mma_commit(&bar[4]);
+            }
+            __syncwarp();
         }
-        float *tq = fs + 2 * plane + 2 * M;
-        float *tk = tq + (size_t)(W - 1) * R;
-        for (int x = tid; x < (W - 1) * R; x += NTH) {
-            const int r = x / R, c = x % R;
-            const int p = N - (W - 1) + r;
-            tq[x] = p >= 0 ? __bfloat162float(gq[base_qk + (size_t)p * sqk + c]) : 0.f;
-            tk[x] = p >= 0 ? __bfloat162float(gk[base_qk + (size_t)p * sqk + c]) : 0.f;
+
+        // ---- end of the piece: its last state update; the final state ----------------------
+        if (tid == 0) bulk_wait_all();  // output stores complete before shared memory is released
+        if (ok && c_end > c_begin) {
+            ok = mbar_wait(&bar[4], (it - 1) & 1);
+            tc_fence_after();
         }
-        const size_t used = 2 * plane + 2 * M + 2 * (size_t)(W - 1) * R;
-        for (size_t x = used + tid; x < a.state_floats; x += NTH) fs[x] = 0.f;
+        ok = !__syncthreads_or(!ok);
+        if (!ok) {
+            // error path: let a copy still in flight land before the CTA exits
+            if (tma_pending) mbar_wait(&bar[5], (uint32_t)(it & 1), 200000000LL);
+            if (tid == 0) report_error(a.err, kErrWaitTimeout);
+        }
+        if (ok && a.final_state && c_end == nchunks) {
+            float *fs = a.final_state + (size_t)unit * a.state_floats;
+            const int RD = R + D;
+            const size_t plane = (size_t)M * RD;
+            // U: plane tl -> row (Re: m, Im: M + m), my half of the columns
+    #pragma unroll
+            for (int c0 = hsel * (R / 2); c0 < (hsel + 1) * (R / 2); c0 += 16) {
+                float v[16];
+                tmem_ld16(tb + lane_base + T::U + c0, v);
+                tmem_wait_ld();
+                float *row = fs + (is_im ? plane : 0) + (size_t)mm * RD + c0;
+    #pragma unroll
+                for (int j = 0; j < 16; ++j) row[j] = v[j];
+            }
+            // Gamma^T: value lane tl writes column R + tl of every row, my half of the modes
+    #pragma unroll
+            for (int c0 = 64 * hsel; c0 < 64 * hsel + 64; c0 += 16) {
+                float v[16];
+                tmem_ld16(tb + lane_base + T::GT + c0, v);
+                tmem_wait_ld();
+                if (tl < D) {
+    #pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int pl = c0 + j, m = pl >> 1;
+                        fs[((pl & 1) ? plane : 0) + (size_t)m * RD + R + tl] = v[j];
+                    }
+                }
+            }
+            if (hsel == 0 && !is_im) {
+                fs[2 * plane + mm] = eta_r;
+                fs[2 * plane + M + mm] = eta_i;
+            }
+            float *tq = fs + 2 * plane + 2 * M;
+            float *tk = tq + (size_t)(W - 1) * R;
+            for (int x = tid; x < (W - 1) * R; x += NTH) {
+                const int r = x / R, c = x % R;
+                const int p = N - (W - 1) + r;
+                tq[x] = p >= 0 ? __bfloat162float(gq[base_qk + (size_t)p * sqk + c]) : 0.f;
+                tk[x] = p >= 0 ? __bfloat162float(gk[base_qk + (size_t)p * sqk + c]) : 0.f;
+            }
+            const size_t used = 2 * plane + 2 * M + 2 * (size_t)(W - 1) * R;
+            for (size_t x = used + tid; x < a.state_floats; x += NTH) fs[x] = 0.f;
+        }
+        // the next piece rewrites the tables, the TMEM state and the taps
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     }
     tc_fence_before();
     __syncthreads();
@@ -970,15 +1014,23 @@ __global__ void __launch_bounds__(NTH, 1)
 }
 
 
-// ---- sequence segments: local end states, then their prefix (start states) ----------------
+// ---- sequence blocks: local end states, then the states before each block ----------------
 //
-// With S segments of a unit's sequence, segment s's start state is
-//   X_start(s) = sum_{s' < s} lambda^(positions between the end of s' and the start of s) X_local(s')
-// where X_local(s') is the state segment s' reaches from zero.  chunk_state_kernel
-// computes X_local of every segment but the last (feature prologue for k and v and the
-// state-update MMAs only), segment_scan_kernel turns them into start states in place,
-// and chunk_prefill_kernel then runs every segment of every unit in parallel.  States
-// are kept as [R + 128 columns][128 lanes] floats, the TMEM image of U and Gamma^T.
+// A unit's sequence is cut into blocks of fs chunks (P = 64 fs positions).  The state
+// before block j is
+//   X_start(j) = sum_{j' < j} lambda^(P (j - 1 - j')) X_local(j')
+// where X_local(j') = sum_{t in j'} B lambda^(P - 1 - t') z_t (t' the position inside the
+// block) is the state block j' reaches from zero.  chunk_state_kernel computes X_local of
+// every block before the unit's last piece, segment_scan_kernel turns them into start
+// states in place, and chunk_prefill_kernel then runs all pieces in parallel.  States are
+// kept as [R + 128 columns][128 lanes] floats, the TMEM image of U and Gamma^T.
+//
+// X_local is one contraction over the block's positions: per chunk c of the block, the
+// state-update MMAs accumulate Coef_c . Kt_c and Vt_c^T . Coef_c^T with
+//   Coef_c[j] = lambda^(64 (fs - 1 - c)) B lambda^(63 - j)
+// so the accumulator is never rescaled between chunks.  Coefficients of old chunks of
+// fast modes underflow in fp16; they are below 2^-24 of the newest ones, beneath the
+// accumulator's own precision.
 
 template <int R, int D>
 struct StateSmem {
@@ -989,8 +1041,7 @@ struct StateSmem {
     static constexpr int CF16 = ZT16 + (R + D) / 8 * ZT_SBO;          // [128][64] f16 (follows ZT16)
     static constexpr int BARS = CF16 + MP * CH * 2;                   // 2 mbarriers: TMA, MMA
     static constexpr int TSLOT = BARS + 16;
-    static constexpr int LAML = TSLOT + 16;                           // [64] float2 lambda^C
-    static constexpr int NWS = LAML + 64 * 8;                         // [R+D] float
+    static constexpr int NWS = TSLOT + 16;                            // [R+D] float
     static constexpr int BSS = NWS + (R + D) * 4;                     // [R+D] float
     static constexpr int TOTAL = BSS + (R + D) * 4;
     static_assert(RAWV % 1024 == 0 && TOTAL <= 113 * 1024, "two state-pass CTAs per SM");
@@ -999,22 +1050,23 @@ struct StateSmem {
 template <int R, int D>
 __global__ void __launch_bounds__(NTH, 2)
     chunk_state_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, int nseg, int seg_chunks, float *seg_state) {
+                       const __grid_constant__ CUtensorMap tm_v, SegPlan plan, float *seg_state) {
     using S = StateSmem<R, D>;
     extern __shared__ __align__(1024) unsigned char sm[];
     const uint32_t s16 = smem_u32(sm) >> 4;  // shared base for MMA descriptors
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S::BARS);  // 0 TMA, 1 MMA
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S::TSLOT);
-    float2 *laml = reinterpret_cast<float2 *>(sm + S::LAML);
     float *nws = reinterpret_cast<float *>(sm + S::NWS);
     float *bss = reinterpret_cast<float *>(sm + S::BSS);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hsel = warp >> 2, tl = 32 * q4 + lane;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const int H = a.H, M = 64, W = a.W;
-    const int nloc = nseg - 1;
+    // block sgi of unit `unit` (blocks before the unit's last piece are full)
+    const int nloc = plan.nb - 1;
     const int unit = blockIdx.x / nloc, sgi = blockIdx.x % nloc, b = unit / H, h = unit % H;
-    const int c_begin = sgi * seg_chunks, c_end = c_begin + seg_chunks;  // full chunks only
+    if (sgi >= plan_last_start(plan, unit)) return;  // no piece starts after this block
+    const int c_begin = sgi * plan.fs, c_end = c_begin + plan.fs;
     const uint32_t raw_bytes = (uint32_t)(CH + HALO) * R * 2 + (uint32_t)CH * D * 2;
     const int mm = tl >> 1, is_im = tl & 1;
     const float lam_r = a.lambda[((size_t)h * M + mm) * 2], lam_i = a.lambda[((size_t)h * M + mm) * 2 + 1];
@@ -1040,29 +1092,25 @@ __global__ void __launch_bounds__(NTH, 2)
         nws[x] = a.norm_w[(size_t)h * (R + D) + x];
         bss[x] = a.bias[(size_t)h * (R + D) + x];
     }
-    if (hsel == 0) {
-        float pr = 1.f, pi = 0.f;
-        __align__(16) __half cf[CH];
-#pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            const float cr = b_r * pr - b_i * pi, ci = b_r * pi + b_i * pr;
-            cf[CH - 1 - k] = __float2half_rn(is_im ? ci : cr);
-            const float nr = pr * lam_r - pi * lam_i, ni = pr * lam_i + pi * lam_r;
-            pr = nr;
-            pi = ni;
-        }
+    // Coef row of plane tl, my half of the positions j: B lambda^(63 - j) for j in
+    // [32 hsel, 32 hsel + 32), i.e. B lambda^k from k0 = 32 (1 - hsel) down the row;
+    // and lambda^64, the decay across one chunk
+    float c0r = b_r, c0i = b_i, l64r = lam_r, l64i = lam_i;
+    {
         float qr = lam_r, qi = lam_i;
 #pragma unroll
-        for (int sq = 0; sq < 6; ++sq) {
+        for (int sq = 0; sq < 5; ++sq) {  // lambda^32
             const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
             qr = nr;
             qi = ni;
         }
-        if (!is_im) laml[mm] = make_float2(qr, qi);
-#pragma unroll
-        for (int k8 = 0; k8 < CH / 8; ++k8)
-            *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
-                *reinterpret_cast<const uint4 *>(&cf[k8 * 8]);
+        if (hsel == 0) {
+            const float nr = c0r * qr - c0i * qi, ni = c0r * qi + c0i * qr;
+            c0r = nr;
+            c0i = ni;
+        }
+        l64r = qr * qr - qi * qi;
+        l64i = 2.f * qr * qi;
     }
     // key conv taps of my channel block, right-aligned (as in the readout kernel)
     constexpr int CBQ = R / 8, PPQ = CH * CBQ / NTH;
@@ -1079,17 +1127,6 @@ __global__ void __launch_bounds__(NTH, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *tslot;
-    {
-        float z[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) z[i] = 0.f;
-        for (int cc = hsel * 16; cc < R + MP; cc += 32) tmem_st16(tb + lane_base + cc, z);
-        tmem_wait_st();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     if (tid == 0) {
         mbar_arrive_expect_tx(&bar[0], raw_bytes);
         tma_load_4d(sm + S::RAWK, &tm_k, 0, h, c_begin * CH - HALO, b, &bar[0]);
@@ -1101,15 +1138,18 @@ __global__ void __launch_bounds__(NTH, 2)
         nwk[e] = nws[c0 + e];
         bsk[e] = bss[c0 + e];
     }
+    constexpr int CBV = D / 8, PPV = CH * CBV / NTH;
+    const int cbv = tid % CBV, iv0 = (tid / CBV) * PPV, j0 = 8 * cbv;
     bool ok = true;
     int tma_pending = 1;
     int ci = c_begin;
     for (; ci < c_end; ++ci) {
-        const uint32_t par = (ci - c_begin) & 1;
+        const int lc = ci - c_begin;
+        const uint32_t par = lc & 1;
         ok = mbar_wait(&bar[0], par);
         if (ok) tma_pending = 0;
         if (__syncthreads_or(!ok)) break;
-        // key features: conv, SiLU, squared-norm normalisation, RMSNorm + affine
+        // key conv and the raw value rows: the staged tiles are then free for the next chunk
         float fk[PPQ][8];
 #pragma unroll
         for (int pp = 0; pp < PPQ; ++pp)
@@ -1127,6 +1167,19 @@ __global__ void __launch_bounds__(NTH, 2)
                     for (int e = 0; e < 8; ++e) fk[pp][e] = fmaf(tk[4 * e + jj], x8[e], fk[pp][e]);
             }
         }
+        uint4 vraw[PPV];
+#pragma unroll
+        for (int pp = 0; pp < PPV; ++pp)
+            vraw[pp] = *reinterpret_cast<const uint4 *>(sm + S::RAWV + ((size_t)(iv0 + pp) * D + j0) * 2);
+        __syncthreads();
+        if (tid == 0 && ci + 1 < c_end) {
+            const int tn = (ci + 1) * CH;
+            mbar_arrive_expect_tx(&bar[0], raw_bytes);
+            tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[0]);
+            tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[0]);
+        }
+        if (ci + 1 < c_end) tma_pending = 1;
+        // key features: SiLU, squared-norm normalisation, RMSNorm + affine
 #pragma unroll
         for (int pp = 0; pp < PPQ; ++pp) {
             float acc = 0.f;
@@ -1151,13 +1204,11 @@ __global__ void __launch_bounds__(NTH, 2)
             for (int e = 0; e < 8; ++e) fk[pp][e] = fmaf(fk[pp][e] * rk, nwk[e], bsk[e]);
         }
         // value RMSNorm + affine
-        constexpr int CBV = D / 8, PPV = CH * CBV / NTH;
-        const int cbv = tid % CBV, iv0 = (tid / CBV) * PPV, j0 = 8 * cbv;
         float vt[PPV][8];
 #pragma unroll
         for (int pp = 0; pp < PPV; ++pp) {
             float x8[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4 *>(sm + S::RAWV + ((size_t)(iv0 + pp) * D + j0) * 2), x8);
+            unpack_bf16x8(vraw[pp], x8);
             float ms = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) ms = fmaf(x8[e], x8[e], ms);
@@ -1167,8 +1218,37 @@ __global__ void __launch_bounds__(NTH, 2)
 #pragma unroll
             for (int e = 0; e < 8; ++e) vt[pp][e] = fmaf(x8[e] * rv, nws[R + j0 + e], bss[R + j0 + e]);
         }
-        // the previous chunk's MMAs read ZT16: wait for them before rewriting it
-        if (ci > c_begin && !mbar_wait(&bar[1], par ^ 1)) ok = false;
+        // Coef_c row: mu = lambda^(64 (fs - 1 - lc)) by squaring, times B lambda^k
+        float mr = 1.f, mi = 0.f;
+        {
+            float pr = l64r, pi = l64i;
+            for (unsigned e = (unsigned)(plan.fs - 1 - lc); e; e >>= 1) {
+                if (e & 1u) {
+                    const float nr = mr * pr - mi * pi, ni = mr * pi + mi * pr;
+                    mr = nr;
+                    mi = ni;
+                }
+                const float nr = pr * pr - pi * pi, ni = 2.f * pr * pi;
+                pr = nr;
+                pi = ni;
+            }
+        }
+        uint32_t cfw[16];  // my plane's Coef entries at j = 32 hsel + 2u, +1
+        {
+            float wr = mr * c0r - mi * c0i, wi = mr * c0i + mi * c0r;  // at j = 32 hsel + 31
+            float cj[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                cj[31 - k] = is_im ? wi : wr;
+                const float nr = wr * lam_r - wi * lam_i, ni = wr * lam_i + wi * lam_r;
+                wr = nr;
+                wi = ni;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) cfw[u] = pack_h2(cj[2 * u], cj[2 * u + 1]);
+        }
+        // the previous chunk's MMAs read ZT16 and CF16: wait for them before rewriting
+        if (lc > 0 && !mbar_wait(&bar[1], par ^ 1)) ok = false;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             unsigned char *dst = sm + S::ZT16 + kmaj_off(c0 + e, i0, 2, PADLBO, S::ZT_SBO);
@@ -1187,72 +1267,28 @@ __global__ void __launch_bounds__(NTH, 2)
             else
                 *reinterpret_cast<uint32_t *>(dst) = w01;
         }
-        tc_fence_after();
-        // scale the state by lambda^C (the previous chunk's accumulation is complete)
-        const float2 lm = laml[mm];
-        {
-            constexpr int NB = R / 32;
-            float v[NB][16];
 #pragma unroll
-            for (int bb = 0; bb < NB; ++bb) tmem_ld16(tb + lane_base + TU + hsel * (R / 2) + 16 * bb, v[bb]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int bb = 0; bb < NB; ++bb) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float o = __shfl_xor_sync(0xffffffffu, v[bb][j], 1);
-                    const float xr = is_im ? o : v[bb][j], xi = is_im ? v[bb][j] : o;
-                    v[bb][j] = is_im ? (lm.x * xi + lm.y * xr) : (lm.x * xr - lm.y * xi);
-                }
-                tmem_st16(tb + lane_base + TU + hsel * (R / 2) + 16 * bb, v[bb]);
-            }
-        }
-        {
-            float v[4][16];
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) tmem_ld16(tb + lane_base + TG + 64 * hsel + 16 * bb, v[bb]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) {
-#pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    const float2 l2 = laml[(64 * hsel + 16 * bb + j) >> 1];
-                    const float xr = v[bb][j], xi = v[bb][j + 1];
-                    v[bb][j] = l2.x * xr - l2.y * xi;
-                    v[bb][j + 1] = l2.x * xi + l2.y * xr;
-                }
-                tmem_st16(tb + lane_base + TG + 64 * hsel + 16 * bb, v[bb]);
-            }
-        }
-        tmem_wait_st();
+        for (int k8 = 0; k8 < 4; ++k8)
+            *reinterpret_cast<uint4 *>(sm + S::CF16 + kmaj_off(tl, 32 * hsel + 8 * k8, 2, 128, 1024)) =
+                make_uint4(cfw[4 * k8], cfw[4 * k8 + 1], cfw[4 * k8 + 2], cfw[4 * k8 + 3]);
         fence_proxy_async_smem();
         tc_fence_before();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
-        if (tid == 0) {
-            if (ci + 1 < c_end) {
-                // the raw tiles are consumed: fetch the next chunk's
-                const int tn = (ci + 1) * CH;
-                mbar_arrive_expect_tx(&bar[0], raw_bytes);
-                tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[0]);
-                tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[0]);
-            }
-        }
         if (warp == 0 && elect_one()) {
             const uint32_t idu = idesc(128, R, 0, 0);
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
                 mma_f16(tb + TU, sdesc_at(s16, S::CF16 + s * 256, 128, 1024),
-                           sdesc_at(s16, S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, 1);
+                        sdesc_at(s16, S::ZT16 + s * 2 * PADLBO, PADLBO, S::ZT_SBO), idu, lc > 0 || s > 0);
             const uint32_t idg = idesc(128, MP, 0, 0);
             const int vrow = S::ZT16 + (R / 8) * S::ZT_SBO;
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
                 mma_f16(tb + TG, sdesc_at(s16, vrow + s * 2 * PADLBO, PADLBO, S::ZT_SBO),
-                           sdesc_at(s16, S::CF16 + s * 256, 128, 1024), idg, 1);
+                        sdesc_at(s16, S::CF16 + s * 256, 128, 1024), idg, lc > 0 || s > 0);
             mma_commit(&bar[1]);
         }
-        if (ci + 1 < c_end) tma_pending = 1;
         __syncwarp();
     }
     if (ok) {
@@ -1278,29 +1314,35 @@ __global__ void __launch_bounds__(NTH, 2)
     if (warp == 0) tmem_dealloc(tb, 256);
 }
 
-// In place over [unit][segment][R+128][128]: slot s becomes X_start(s + 1).
-__global__ void segment_scan_kernel(const float *lambda, int H, int R, int units, int nseg, int seg_chunks,
+// In place over [unit][block][R+128][128]: slot j becomes the state before block j + 1, for
+// the blocks before the unit's last piece.  Threads walk consecutive floats of one column
+// (U: a complex pair per thread, adjacent lanes; Gamma^T: one value lane, Re and Im in two
+// columns), and each loads a batch of slots before running the recurrence through them.
+__global__ void segment_scan_kernel(const float *lambda, int H, int R, int D, int units, SegPlan plan,
                                     float *seg_state) {
-    const int pairs = 64 * (R + MP);  // complex pairs of one state image
+    const int upairs = 64 * R, pairs = upairs + 64 * D;  // complex pairs of one state image
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long long)units * pairs) return;
     const int unit = (int)(idx / pairs), r = (int)(idx % pairs), h = unit % H;
+    const int nscan = plan_last_start(plan, unit);
+    if (nscan == 0) return;
     int m;
     size_t re, im;
-    if (r < 64 * R) {  // U: column c, lanes 2m (Re) and 2m+1 (Im)
+    if (r < upairs) {  // U column c, lanes 2m (Re) and 2m+1 (Im)
         const int c = r / 64;
         m = r % 64;
         re = (size_t)c * 128 + 2 * m;
         im = re + 1;
-    } else {  // Gamma^T: lane jv, columns R+2m (Re) and R+2m+1 (Im)
-        const int r2 = r - 64 * R, jv = r2 / 64;
-        m = r2 % 64;
+    } else {  // Gamma^T lane jv, columns R+2m (Re) and R+2m+1 (Im)
+        const int r2 = r - upairs;
+        m = r2 / D;
+        const int jv = r2 % D;
         re = (size_t)(R + 2 * m) * 128 + jv;
         im = re + 128;
     }
-    // g = lambda^(C * seg_chunks) by binary exponentiation
+    // g = lambda^(C * fs), the decay across one block, by binary exponentiation
     float gr = 1.f, gi = 0.f, pr = lambda[((size_t)h * 64 + m) * 2], pi = lambda[((size_t)h * 64 + m) * 2 + 1];
-    for (unsigned e = (unsigned)(CH * seg_chunks); e; e >>= 1) {
+    for (unsigned e = (unsigned)(CH * plan.fs); e; e >>= 1) {
         if (e & 1u) {
             const float nr = gr * pr - gi * pi, ni = gr * pi + gi * pr;
             gr = nr;
@@ -1310,14 +1352,29 @@ __global__ void segment_scan_kernel(const float *lambda, int H, int R, int units
         pr = nr;
         pi = ni;
     }
+    constexpr int BATCH = 8;
+    const size_t slot = (size_t)(R + MP) * 128;
+    float *base = seg_state + (size_t)unit * (plan.nb - 1) * slot;
     float xr = 0.f, xi = 0.f;
-    for (int s = 0; s < nseg - 1; ++s) {
-        float *p = seg_state + ((size_t)unit * (nseg - 1) + s) * (size_t)(R + MP) * 128;
-        const float nr = gr * xr - gi * xi + p[re], ni = gr * xi + gi * xr + p[im];
-        xr = nr;
-        xi = ni;
-        p[re] = xr;
-        p[im] = xi;
+    for (int j0 = 0; j0 < nscan; j0 += BATCH) {
+        float lr[BATCH], li[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            if (j0 + u < nscan) {
+                lr[u] = base[(j0 + u) * slot + re];
+                li[u] = base[(j0 + u) * slot + im];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            if (j0 + u < nscan) {
+                const float nr = gr * xr - gi * xi + lr[u], ni = gr * xi + gi * xr + li[u];
+                xr = nr;
+                xi = ni;
+                base[(j0 + u) * slot + re] = xr;
+                base[(j0 + u) * slot + im] = xi;
+            }
+        }
     }
 }
 
@@ -1359,27 +1416,28 @@ static bool make_map(EncodeTiledFn fn, CUtensorMap *m, const void *ptr, int B, i
 
 template <int R, int D>
 static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const CUtensorMap &mq,
-                                   const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo, int nseg,
-                                   int seg_chunks, float *ws) {
+                                   const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+                                   const SegPlan &plan, float *ws) {
     const unsigned units = (unsigned)(a.B * a.H);
     cudaError_t e;
-    if (nseg > 1) {
+    if (plan.nb > 1) {
         using SS = StateSmem<R, D>;
         auto sk = chunk_state_kernel<R, D>;
         e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::TOTAL);
         if (e != cudaSuccess) return e;
-        sk<<<units * (unsigned)(nseg - 1), NTH, SS::TOTAL, st>>>(a, mk, mv, nseg, seg_chunks, ws);
+        sk<<<units * (unsigned)(plan.nb - 1), NTH, SS::TOTAL, st>>>(a, mk, mv, plan, ws);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        const long long pairs = (long long)units * 64 * (R + MP);
-        segment_scan_kernel<<<(unsigned)((pairs + 255) / 256), 256, 0, st>>>(a.lambda, a.H, R, (int)units, nseg,
-                                                                          seg_chunks, ws);
+        const long long pairs = (long long)units * 64 * (R + D);
+        segment_scan_kernel<<<(unsigned)((pairs + 255) / 256), 256, 0, st>>>(a.lambda, a.H, R, D, (int)units, plan,
+                                                                          ws);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     using S = ChunkSmem<R, D>;
     auto kern = chunk_prefill_kernel<R, D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
     if (e != cudaSuccess) return e;
-    kern<<<units * (unsigned)nseg, NTH, S::TOTAL, st>>>(a, mq, mk, mv, mo, nseg, seg_chunks, ws);
+    const unsigned grid = (unsigned)((plan.total + plan.q - 1) / plan.q);
+    kern<<<grid, NTH, S::TOTAL, st>>>(a, mq, mk, mv, mo, plan, ws);
     return cudaGetLastError();
 }
 
@@ -1388,23 +1446,70 @@ static bool chunk_path_takes(const PrefillArgs &a) {
     return (a.R == 64 || a.R == 128) && (a.d == 64 || a.d == 128);
 }
 
-// Segments per unit: enough to cover the SMs with one CTA each, at least 8 chunks per segment.
-static void choose_segments(const PrefillArgs &a, int num_sms, int *nseg, int *seg_chunks) {
-    const int nchunks = (a.N + CH - 1) / CH;
-    const long long units = (long long)a.B * a.H;
-    int s = (int)(num_sms / (units > 0 ? units : 1));
-    if (s > nchunks / 8) s = nchunks / 8;
-    if (s < 1) s = 1;
-    const int sc = (nchunks + s - 1) / s;
-    *seg_chunks = sc;
-    *nseg = (nchunks + sc - 1) / sc;
+// One CTA per unit, whole sequences: the plan without a workspace.
+static SegPlan whole_plan(long long units, int nchunks) {
+    SegPlan p;
+    p.fs = nchunks;
+    p.nb = 1;
+    p.q = 1;
+    p.total = (int)units;
+    return p;
 }
 
-size_t chunk_workspace_bytes(const PrefillArgs &a, int num_sms) {
+static SegPlan block_plan(long long units, int nchunks, int fs, int num_sms) {
+    SegPlan p;
+    p.fs = fs;
+    p.nb = (nchunks + fs - 1) / fs;
+    p.total = (int)(units * p.nb);
+    p.q = (p.total + num_sms - 1) / num_sms;
+    return p;
+}
+
+static size_t plan_workspace_bytes(const SegPlan &p, long long units, int R) {
+    return p.nb > 1 ? (size_t)units * (size_t)(p.nb - 1) * (size_t)(R + MP) * 128 * sizeof(float) : 0;
+}
+
+// Modelled time of a plan in readout chunk times (a readout chunk is about 8 us): the
+// busiest readout CTA's chunks, plus, when sequences are split, the block state pass
+// (blocks of fs chunks, two CTAs per SM, a block chunk costing about kStateChunk of a
+// readout chunk), the scan (reads and writes the workspace once, about kScanBytes per
+// readout chunk time) and the two extra launches.
+constexpr double kStateChunk = 0.35;
+constexpr double kScanBytes = 40e6;
+constexpr double kSplitOverhead = 0.5;
+static double plan_cost(const SegPlan &p, long long units, int nchunks, int num_sms, int R) {
+    if (p.nb == 1) return (double)((units + num_sms - 1) / num_sms) * nchunks;
+    long long nstate = 0;
+    for (long long u = 0; u < units; ++u) nstate += plan_last_start(p, (int)u);
+    const long long waves = (nstate + 2LL * num_sms - 1) / (2LL * num_sms);
+    const double scan = 2.0 * (double)nstate * (R + MP) * 128 * sizeof(float) / kScanBytes;
+    return (double)p.q * p.fs + (double)waves * p.fs * kStateChunk + scan + kSplitOverhead;
+}
+
+// The cheapest plan whose workspace fits `budget` bytes (block sizes 1, 2, 4, ... chunks;
+// ties go to the larger block, i.e. the smaller workspace).
+static SegPlan choose_plan(const PrefillArgs &a, int num_sms, size_t budget) {
+    const int nchunks = (a.N + CH - 1) / CH;
+    const long long units = (long long)a.B * a.H;
+    SegPlan best = whole_plan(units, nchunks);
+    double best_cost = plan_cost(best, units, nchunks, num_sms, a.R);
+    if (units <= 0 || nchunks < 2 || units * (long long)nchunks > (1LL << 30)) return best;
+    for (int fs = 1; fs < nchunks; fs *= 2) {
+        const SegPlan p = block_plan(units, nchunks, fs, num_sms);
+        if (p.nb < 2 || plan_workspace_bytes(p, units, a.R) > budget) continue;
+        const double c = plan_cost(p, units, nchunks, num_sms, a.R);
+        if (c <= best_cost) {
+            best = p;
+            best_cost = c;
+        }
+    }
+    return best;
+}
+
+// Workspace of the plan chosen within `budget` bytes (0 when no split pays off).
+size_t chunk_workspace_bytes(const PrefillArgs &a, int num_sms, size_t budget) {
     if (!chunk_path_takes(a) || a.N <= 0) return 0;
-    int nseg, sc;
-    choose_segments(a, num_sms, &nseg, &sc);
-    return (size_t)a.B * a.H * (size_t)(nseg - 1) * (size_t)(a.R + MP) * 128 * sizeof(float);
+    return plan_workspace_bytes(choose_plan(a, num_sms, budget), (long long)a.B * a.H, a.R);
 }
 
 // Takes bf16 prefill with M = 64 modes and R, d in {64, 128}, denominator-free
@@ -1427,20 +1532,18 @@ ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int num_s
         why = "cuTensorMapEncodeTiled rejected the q/k/v/out layout";
         return IDA_OK;
     }
-    int nseg = 1, seg_chunks = (a.N + CH - 1) / CH;
-    if (workspace && workspace_bytes >= chunk_workspace_bytes(a, num_sms) && chunk_workspace_bytes(a, num_sms) > 0)
-        choose_segments(a, num_sms, &nseg, &seg_chunks);
-    float *ws = nseg > 1 ? static_cast<float *>(workspace) : nullptr;
+    const SegPlan plan = choose_plan(a, num_sms, workspace ? workspace_bytes : 0);
+    float *ws = plan.nb > 1 ? static_cast<float *>(workspace) : nullptr;
     *taken = true;
     cudaError_t e;
     if (a.R == 128 && a.d == 128)
-        e = launch_chunk_rd<128, 128>(a, st, mq, mk, mv, mo, nseg, seg_chunks, ws);
+        e = launch_chunk_rd<128, 128>(a, st, mq, mk, mv, mo, plan, ws);
     else if (a.R == 64 && a.d == 64)
-        e = launch_chunk_rd<64, 64>(a, st, mq, mk, mv, mo, nseg, seg_chunks, ws);
+        e = launch_chunk_rd<64, 64>(a, st, mq, mk, mv, mo, plan, ws);
     else if (a.R == 128 && a.d == 64)
-        e = launch_chunk_rd<128, 64>(a, st, mq, mk, mv, mo, nseg, seg_chunks, ws);
+        e = launch_chunk_rd<128, 64>(a, st, mq, mk, mv, mo, plan, ws);
     else
-        e = launch_chunk_rd<64, 128>(a, st, mq, mk, mv, mo, nseg, seg_chunks, ws);
+        e = launch_chunk_rd<64, 128>(a, st, mq, mk, mv, mo, plan, ws);
     if (e != cudaSuccess) {
         why = std::string("chunked prefill launch: ") + cudaGetErrorString(e);
         return IDA_ERR_CUDA;

@@ -31,6 +31,10 @@ struct DecodeArgs {
 };
 
 // Error codes written to the device error word (first writer wins).
+// Largest workspace the prefill asks for (ida_forward_workspace_bytes): sequences are split
+// only as finely as the state slots of that many bytes allow.
+constexpr size_t kPreferredWorkspace = size_t(64) << 20;
+
 enum : unsigned {
     kErrNone = 0,
     kErrWaitTimeout = 1,

@@ -21,11 +21,14 @@ ida_status forward_entry(const void *q, const void *k, const void *v, const floa
                          int B, int H, int N, int d, int R, int M, int dtype, int W, int flags, void *workspace,
                          size_t workspace_bytes, ida_stream_t stream);
 ida_status fail_with(ida_status s, const std::string &why);
+size_t forward_workspace_within(int B, int H, int N, int d, int R, int M, int dtype, int W, int flags,
+                                size_t budget);
 }  // namespace ida
 
-// The shared scratch: 32 MiB per device.  With 152 SMs the segmented prefill
-// needs at most about 20 MB (R = 128), so every supported shape fits; a
-// larger device that would split sequences further gets a clear error instead.
+// The shared scratch: 32 MiB per device.  The prefill splits sequences only as
+// finely as its state slots fit in it (a caller workspace may allow finer splits),
+// so every supported shape runs; a plan that would still need more is refused
+// with a clear error rather than run over the end of the array.
 static constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
@@ -44,7 +47,7 @@ extern "C" ida_status ida_forward_noalloc(const void *q, const void *k, const vo
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return ida::fail_with(IDA_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return ida::fail_with(IDA_ERR_UNSUPPORTED, "device ordinal above 63");
-    const size_t need = ida_forward_workspace_bytes(B, H, N, d, R, M, dtype, W, flags);
+    const size_t need = ida::forward_workspace_within(B, H, N, d, R, M, dtype, W, flags, kStaticScratchBytes);
     if (need > kStaticScratchBytes)
         return ida::fail_with(IDA_ERR_UNSUPPORTED, "this shape needs " + std::to_string(need) +
                                                        " bytes of scratch; the static scratch holds " +

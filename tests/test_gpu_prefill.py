@@ -169,11 +169,14 @@ def test_eta_readout_constant_values_on_gpu(path):
 
 
 @pytest.mark.parametrize("shape", [(1, 64 * 40 + 17, 2, 128, 128), (2, 64 * 33, 1, 64, 128),
-                                   (1, 64 * 24 + 1, 3, 128, 64)],
+                                   (1, 64 * 24 + 1, 3, 128, 64),
+                                   # more blocks than SMs: CTAs run pieces of two or three units
+                                   (4, 64 * 8 - 9, 10, 64, 64), (4, 64 * 9 + 3, 12, 128, 128)],
                          ids=lambda s: "B{}N{}H{}R{}d{}".format(*s))
 def test_segmented_prefill(shape):
-    """Sequences split into segments on separate SMs (workspace path) match the
-    oracle, including a ragged last chunk and the final state."""
+    """Sequences split into blocks whose pieces run on separate SMs (workspace path)
+    match the oracle, including a ragged last chunk, CTAs whose pieces span unit
+    boundaries, and the final state."""
     B, N, H, R, d = shape
     q, k, v, p = problem(B, N, H, R, d, 64, 4, "bf16", seed=300 + N)
     dev = torch.device("cuda")
