@@ -161,27 +161,24 @@ __device__ __forceinline__ uint4 pack_f16x8(const float x[8]) {
     return make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]), pack_h2(x[6], x[7]));
 }
 
-// Work split of a batch of sequences across CTAs.  Each unit's chunks are grouped into
-// nb blocks of fs chunks (the last block may be shorter); the units' blocks, taken in
-// order, are dealt to the readout CTAs q at a time.  A CTA runs its blocks as pieces, one
-// per unit they fall in; every piece not at a sequence start needs the state before its
-// first block, which the block state pass and the block scan provide.
+// Work split of a batch of sequences across CTAs.  Each unit's chunks are grouped into nb
+// blocks of fs chunks (the last block may be shorter) and its blocks into ppu pieces of q
+// blocks; one CTA runs one piece.  A piece not at the sequence start needs the state before
+// its first block: the block state pass computes, from zero, the end state of each of the
+// unit's first (ppu - 1) q blocks and the block scan composes them into start states.
 struct SegPlan {
-    int fs;     // chunks per block
-    int nb;     // blocks per unit
-    int q;      // blocks per readout CTA
-    int total;  // units * nb
+    int fs;   // chunks per block
+    int nb;   // blocks per unit
+    int q;    // blocks per piece
+    int ppu;  // pieces per unit
 };
 
-// Block (within unit u) at which u's last piece starts: the blocks before it are the ones
-// whose local end states the scan composes.
-__host__ __device__ inline int plan_last_start(const SegPlan &p, int u) {
-    const int f_last = (u + 1) * p.nb - 1;
-    const int start = (f_last / p.q) * p.q;
-    return start > u * p.nb ? start - u * p.nb : 0;
-}
+// Blocks per unit whose end states the state pass computes (all but the last piece's).
+__host__ __device__ inline int plan_state_blocks(const SegPlan &p) { return (p.ppu - 1) * p.q; }
 
-template <int R, int D>
+// FACT selects the Gram formulation; a CTA whose head takes the other one returns at once
+// (the other instantiation, launched on the same plan, runs that piece).
+template <int R, int D, bool FACT>
 __global__ void __launch_bounds__(NTH, 1)
     chunk_prefill_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -218,6 +215,47 @@ __global__ void __launch_bounds__(NTH, 1)
         return;
     }
 
+    // ---- this CTA's piece: chunks [c_begin, c_end) of unit `unit` ---------------------
+    const int unit = blockIdx.x / plan.ppu, j0 = (blockIdx.x % plan.ppu) * plan.q;
+    const int j1 = min(plan.nb, j0 + plan.q);
+    const int b = unit / H, h = unit % H;
+    const int c_begin = j0 * plan.fs, c_end = min(nchunks, j1 * plan.fs);
+    const size_t base_qk = ((size_t)b * N * H + h) * R;
+    const float lam_r = a.lambda[((size_t)h * M + mm) * 2], lam_i = a.lambda[((size_t)h * M + mm) * 2 + 1];
+    const float b_r = a.Bvec[((size_t)h * M + mm) * 2], b_i = a.Bvec[((size_t)h * M + mm) * 2 + 1];
+    // Factorised Gram path: lambda^(i-j) = lambda^i lambda^-j, the table T[j] = B lambda^-j
+    // (times 2^-fsc per mode) held in fp16.  Taken when every mode of the head keeps T
+    // within fp16 normals with room for the Ya column scaling: |lambda| <= 1,
+    // |lambda|^-63 <= 2^8 and 2^-8 <= |B| <= 2^8.  Otherwise the skewed-Gram path (tables
+    // lambda^k, bounded by 1 for any stable mode) serves the piece.
+    const float m2 = lam_r * lam_r + lam_i * lam_i, bb2 = b_r * b_r + b_i * b_i;
+    const float lg63 = -31.5f * log2f(m2);  // log2 |lambda|^-63
+    const bool fact = __syncthreads_and(m2 > 0.f && m2 <= 1.001f && lg63 <= 8.f && bb2 >= 1.f / 65536.f &&
+                                        bb2 <= 65536.f) != 0;
+    if (fact != FACT || c_begin >= c_end) return;  // the other instantiation runs this piece
+    // lambda^(32 hsel + 16 is_im + 1): the decay at this lane's first position in the a / Ya stage
+    float w0r = lam_r, w0i = lam_i;
+    {
+        float qr = lam_r, qi = lam_i;
+#pragma unroll
+        for (int sq = 0; sq < 4; ++sq) {  // lambda^16
+            const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
+            qr = nr;
+            qi = ni;
+        }
+        if (is_im) {
+            const float nr = w0r * qr - w0i * qi, ni = w0r * qi + w0i * qr;
+            w0r = nr;
+            w0i = ni;
+        }
+        const float q2r = qr * qr - qi * qi, q2i = 2.f * qr * qi;  // lambda^32
+        if (hsel) {
+            const float nr = w0r * q2r - w0i * q2i, ni = w0r * q2i + w0i * q2r;
+            w0r = nr;
+            w0i = ni;
+        }
+    }
+
     // ---- set-up: barriers, TMEM ---------------------------------------------------
     if (tid == 0) {
         for (int i = 0; i < 8; ++i) mbar_init(&bar[i], 1);
@@ -240,52 +278,40 @@ __global__ void __launch_bounds__(NTH, 1)
     int it = 0;           // chunks this CTA has run so far: the phase parity of every barrier
     int tma_pending = 0;  // TMA copies issued and not yet waited for
     int ci = 0;
-    // This CTA's blocks of the (unit, block) sequence, split at unit boundaries into pieces
-    // that run one after the other; a piece starting past block 0 takes its start state
-    // from the block scan.
-    int fb = blockIdx.x * plan.q;
-    const int fb_end = min(fb + plan.q, plan.total);
-    while (ok && fb < fb_end) {
-        const int unit = fb / plan.nb, j0 = fb % plan.nb;
-        const int j1 = min(plan.nb, j0 + (fb_end - fb));
-        fb += j1 - j0;
-        const int b = unit / H, h = unit % H;
-        const int c_begin = j0 * plan.fs, c_end = min(nchunks, j1 * plan.fs);
-        const size_t base_qk = ((size_t)b * N * H + h) * R;
-        const float lam_r = a.lambda[((size_t)h * M + mm) * 2], lam_i = a.lambda[((size_t)h * M + mm) * 2 + 1];
-        const float b_r = a.Bvec[((size_t)h * M + mm) * 2], b_i = a.Bvec[((size_t)h * M + mm) * 2 + 1];
-        // lambda^(32 hsel + 16 is_im + 1): the decay at this lane's first position in the a / Ya stage
-        float w0r = lam_r, w0i = lam_i;
+    {
+        const int fsc = FACT ? (int)ceilf(0.5f * log2f(bb2) + lg63 + 0.01f) + 1 : 0;  // T max <= 1/2
+        const float fS = pow2i(fsc);
+        // lambda^(2 ib) with ib = 32 hsel + 16 is_im (this lane's first position in the a / Ya
+        // stage) and lambda^2: the running lambda^(2i) of the factorised path
+        float v0r = 1.f, v0i = 0.f;
+        const float l2r = lam_r * lam_r - lam_i * lam_i, l2i = 2.f * lam_r * lam_i;
         {
             float qr = lam_r, qi = lam_i;
-    #pragma unroll
-            for (int sq = 0; sq < 4; ++sq) {  // lambda^16
+#pragma unroll
+            for (int sq = 0; sq < 5; ++sq) {  // lambda^32
                 const float nr = qr * qr - qi * qi, ni = 2.f * qr * qi;
                 qr = nr;
                 qi = ni;
             }
             if (is_im) {
-                const float nr = w0r * qr - w0i * qi, ni = w0r * qi + w0i * qr;
-                w0r = nr;
-                w0i = ni;
+                v0r = qr;
+                v0i = qi;
             }
-            const float q2r = qr * qr - qi * qi, q2i = 2.f * qr * qi;  // lambda^32
             if (hsel) {
-                const float nr = w0r * q2r - w0i * q2i, ni = w0r * q2i + w0i * q2r;
-                w0r = nr;
-                w0i = ni;
+                const float q2r = qr * qr - qi * qi, q2i = 2.f * qr * qi;  // lambda^64
+                const float nr = v0r * q2r - v0i * q2i, ni = v0r * q2i + v0i * q2r;
+                v0r = nr;
+                v0i = ni;
             }
         }
-
-
-        // ---- per-head constants of the piece ----------------------------------------
         for (int x = tid; x < R + D; x += NTH) {
             nws[x] = a.norm_w[(size_t)h * (R + D) + x];
             bss[x] = a.bias[(size_t)h * (R + D) + x];
         }
         if (hsel == 0) {
-            // T_L row (plane tl): component of lambda_m^k, k = 0..63; Coef row: component
-            // of B_m lambda_m^(C-1-j); T_A column tl = T_L row (unscaled).
+            // T_L row (plane tl): component of lambda_m^k, k = 0..63 (skewed path) or of the
+            // factorised table; Coef row: component of B_m lambda_m^(C-1-j); T_A column tl =
+            // T_L row (unscaled).
             float pr = 1.f, pi = 0.f, sr = 0.f, si = 0.f;
             __align__(16) __half tl16[CH], cf[CH];
     #pragma unroll
@@ -311,6 +337,18 @@ __global__ void __launch_bounds__(NTH, 1)
                 laml[mm] = make_float2(qr, qi);  // lambda^C
                 suml[mm] = make_float2(sr, si);  // sum_{k<C} lambda^k
             }
+            if constexpr (FACT) {
+                // factorised table row: component of B lambda^-j 2^-fsc, j = 0..63
+                const float ir = lam_r / m2, ii = -lam_i / m2;  // lambda^-1
+                float wr = b_r * pow2i(-fsc), wi = b_i * pow2i(-fsc);
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                    tl16[j] = __float2half_rn(is_im ? wi : wr);
+                    const float nr = wr * ir - wi * ii, ni = wr * ii + wi * ir;
+                    wr = nr;
+                    wi = ni;
+                }
+            }
     #pragma unroll
             for (int k8 = 0; k8 < CH / 8; ++k8) {
                 *reinterpret_cast<uint4 *>(sm + S::TL16 + kmaj_off(tl, k8 * 8, 2, 128, 1024)) =
@@ -328,7 +366,8 @@ __global__ void __launch_bounds__(NTH, 1)
         {
             // start state: zero at the sequence start, else the state before block j0 from the
             // block scan ([R+128 columns][128 lanes] floats, columns as in TMEM), by column half
-            const float *x0 = j0 > 0 ? seg_start + ((size_t)unit * (plan.nb - 1) + (j0 - 1)) * (size_t)(R + MP) * 128
+            const float *x0 = j0 > 0 ? seg_start + ((size_t)unit * plan_state_blocks(plan) + (j0 - 1)) *
+                                                   (size_t)(R + MP) * 128
                                      : nullptr;
             for (int c0 = hsel * 16; c0 < R + MP; c0 += 32) {
                 float z[16];
@@ -403,22 +442,20 @@ __global__ void __launch_bounds__(NTH, 1)
                 // rows are stored rotated: at step pp this thread writes position i0 + (pp + rot) % PPQ,
                 // so the channel-block threads of one position hit different banks
                 const int rot = cb % PPQ;
-                float tq[32], tk[32];  // taps of my channel block (TMEM lane tl holds block tl % CBQ == cb)
-                tmem_ld16(tb + lane_base + T::TAPS, tq);
-                tmem_ld16(tb + lane_base + T::TAPS + 16, tq + 16);
-                tmem_ld16(tb + lane_base + T::TAPS + 32, tk);
-                tmem_ld16(tb + lane_base + T::TAPS + 48, tk + 16);
                 float nwk[8], bsk[8];
                 *reinterpret_cast<float4 *>(nwk) = *reinterpret_cast<const float4 *>(nws + c0);
                 *reinterpret_cast<float4 *>(nwk + 4) = *reinterpret_cast<const float4 *>(nws + c0 + 4);
                 *reinterpret_cast<float4 *>(bsk) = *reinterpret_cast<const float4 *>(bss + c0);
                 *reinterpret_cast<float4 *>(bsk + 4) = *reinterpret_cast<const float4 *>(bss + c0 + 4);
-                tmem_wait_ld();
                 float fk[PPQ][8];
     #pragma unroll
                 for (int which = 0; which < 2; ++which) {
                     const unsigned char *raw = sm + (which == 0 ? S::RAWQ : S::RAWK);
-                    const float *w8 = which == 0 ? tq : tk;
+                    // taps of my channel block (TMEM lane tl holds block tl % CBQ == cb), q then k
+                    float w8[32];
+                    tmem_ld16(tb + lane_base + T::TAPS + 32 * which, w8);
+                    tmem_ld16(tb + lane_base + T::TAPS + 32 * which + 16, w8 + 16);
+                    tmem_wait_ld();
                     // rows i0 .. i0+PPQ+2 of the staged tile = positions i0-3 .. i0+PPQ-1
                     float f[PPQ][8];
     #pragma unroll
@@ -627,33 +664,50 @@ __global__ void __launch_bounds__(NTH, 1)
             tc_fence_after();
             if (__syncthreads_or(!ok)) break;
 
-            // ---- S3: G' = skewed, masked G -----------------------------------------------
-            // scratch [64][64] rotated by row, over YA16: the raw tile there is consumed and
-            // YA16 is not rewritten before S5 (XQ32 may still be read by the P^T MMA)
+            // ---- S3: G' = skewed, masked G (skewed path); masked G (factorised path) --------
+            // skewed path: scratch [64][64] rotated by row, over YA16: the raw tile there is
+            // consumed and YA16 is not rewritten before S5 (XQ32 may still be read by the P^T MMA)
             float *scr = reinterpret_cast<float *>(sm + S::YA16);
-            if (q4 < 2) {
-                const int i = tl;
-    #pragma unroll
-                for (int c0 = 32 * hsel; c0 < 32 * hsel + 32; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(tb + lane_base + T::G + c0, v);
-                    tmem_wait_ld();
-    #pragma unroll
-                    for (int j = 0; j < 16; ++j) scr[i * 64 + ((c0 + j + i) & 63)] = v[j];
-                }
-            }
-            __syncthreads();
-            {
-                const int i = tid >> 2, p = tid & 3;
-    #pragma unroll
-                for (int h8 = 0; h8 < 2; ++h8) {
-                    float g8[8];
-    #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int k = 16 * p + 8 * h8 + e;
-                        g8[e] = k <= i ? scr[i * 64 + ((2 * i - k) & 63)] : 0.f;
+            if constexpr (!FACT) {
+                if (q4 < 2) {
+                    const int i = tl;
+        #pragma unroll
+                    for (int c0 = 32 * hsel; c0 < 32 * hsel + 32; c0 += 16) {
+                        float v[16];
+                        tmem_ld16(tb + lane_base + T::G + c0, v);
+                        tmem_wait_ld();
+        #pragma unroll
+                        for (int j = 0; j < 16; ++j) scr[i * 64 + ((c0 + j + i) & 63)] = v[j];
                     }
-                    *reinterpret_cast<uint4 *>(sm + S::GP16 + kmaj_off(i, 16 * p + 8 * h8, 2, 128, 1024)) = pack_f16x8(g8);
+                }
+                __syncthreads();
+                {
+                    const int i = tid >> 2, p = tid & 3;
+        #pragma unroll
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        float g8[8];
+        #pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int k = 16 * p + 8 * h8 + e;
+                            g8[e] = k <= i ? scr[i * 64 + ((2 * i - k) & 63)] : 0.f;
+                        }
+                        *reinterpret_cast<uint4 *>(sm + S::GP16 + kmaj_off(i, 16 * p + 8 * h8, 2, 128, 1024)) = pack_f16x8(g8);
+                    }
+                }
+            } else if (q4 < 2) {
+                // row i of G, my half of the columns, masked to j <= i
+                const int i = tl;
+                float v[32];
+                tmem_ld16(tb + lane_base + T::G + 32 * hsel, v);
+                tmem_ld16(tb + lane_base + T::G + 32 * hsel + 16, v + 16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k8 = 0; k8 < 4; ++k8) {
+                    float g8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) g8[e] = 32 * hsel + 8 * k8 + e <= i ? v[8 * k8 + e] : 0.f;
+                    *reinterpret_cast<uint4 *>(sm + S::GP16 + kmaj_off(i, 32 * hsel + 8 * k8, 2, 128, 1024)) =
+                        pack_f16x8(g8);
                 }
             }
             fence_proxy_async_smem();
@@ -691,34 +745,63 @@ __global__ void __launch_bounds__(NTH, 1)
                 tmem_ld16(tb + lane_base + T::PT + 32 * hsel + 16, pv + 16);
                 tmem_ld16(tb + lane_base + T::LT + 32 * hsel, lv);
                 tmem_ld16(tb + lane_base + T::LT + 32 * hsel + 16, lv + 16);
-                float wr = w0r, ws = sg * w0i;  // lambda^(i+1) at my first position, as (Re, s Im)
                 float yo[16], yq[16];           // Ya of my plane / of the partner plane, unscaled
                 float mo = 0.f, mq = 0.f;
                 const int ib = 32 * hsel + 16 * is_im;  // my first position
                 tmem_wait_ld();
-    #pragma unroll
-                for (int p = 0; p < 16; ++p) {
-                    // my plane at my position; the partner needs mine at its position
-                    const float pm = is_im ? pv[16 + p] : pv[p], ps = is_im ? pv[p] : pv[16 + p];
-                    const float lm = is_im ? lv[16 + p] : lv[p], lsd = is_im ? lv[p] : lv[16 + p];
-                    const float po = __shfl_xor_sync(0xffffffffu, ps, 1);
-                    const float lo = __shfl_xor_sync(0xffffffffu, lsd, 1);
-                    // a = lambda^(i+1) P + B L
-                    const float ao = fmaf(pm, wr, fmaf(po, ws, fmaf(lm, b_r, lo * bs)));
-                    const float ap = fmaf(po, wr, fmaf(-pm, ws, fmaf(lo, b_r, -lm * bs)));
-                    // Ya = a B: -s own(a B) = -s b_r ao - b_i ap ; s partner(a B) = s b_r ap - b_i ao
-                    yo[p] = fmaf(ao, -sg * b_r, -b_i * ap);
-                    yq[p] = fmaf(ap, sg * b_r, -b_i * ao);
-                    mo = fmaxf(mo, fabsf(yo[p]));
-                    mq = fmaxf(mq, fabsf(yq[p]));
-                    // a' = a lambda^(i+1), both planes, Re plane first
-                    const float qo = -sg * fmaf(ao, wr, ap * ws), qq = sg * fmaf(ap, wr, -ao * ws);
-                    const uint32_t t_re = tf32_bits(is_im ? qq : qo), t_im = tf32_bits(is_im ? qo : qq);
-                    *reinterpret_cast<uint2 *>(sm + S::AP32 + kmaj_off(ib + p, 2 * mm, 4, PADLBO, S::AP_SBO)) =
-                        make_uint2(t_re, t_im);
-                    const float nr = fmaf(wr, lam_r, -ws * ls), ns = fmaf(wr, ls, ws * lam_r);
-                    wr = nr;
-                    ws = ns;
+                if constexpr (!FACT) {
+                    float wr = w0r, ws = sg * w0i;  // lambda^(i+1) at my first position, as (Re, s Im)
+        #pragma unroll
+                    for (int p = 0; p < 16; ++p) {
+                        // my plane at my position; the partner needs mine at its position
+                        const float pm = is_im ? pv[16 + p] : pv[p], ps = is_im ? pv[p] : pv[16 + p];
+                        const float lm = is_im ? lv[16 + p] : lv[p], lsd = is_im ? lv[p] : lv[16 + p];
+                        const float po = __shfl_xor_sync(0xffffffffu, ps, 1);
+                        const float lo = __shfl_xor_sync(0xffffffffu, lsd, 1);
+                        // a = lambda^(i+1) P + B L
+                        const float ao = fmaf(pm, wr, fmaf(po, ws, fmaf(lm, b_r, lo * bs)));
+                        const float ap = fmaf(po, wr, fmaf(-pm, ws, fmaf(lo, b_r, -lm * bs)));
+                        // Ya = a B: -s own(a B) = -s b_r ao - b_i ap ; s partner(a B) = s b_r ap - b_i ao
+                        yo[p] = fmaf(ao, -sg * b_r, -b_i * ap);
+                        yq[p] = fmaf(ap, sg * b_r, -b_i * ao);
+                        mo = fmaxf(mo, fabsf(yo[p]));
+                        mq = fmaxf(mq, fabsf(yq[p]));
+                        // a' = a lambda^(i+1), both planes, Re plane first
+                        const float qo = -sg * fmaf(ao, wr, ap * ws), qq = sg * fmaf(ap, wr, -ao * ws);
+                        const uint32_t t_re = tf32_bits(is_im ? qq : qo), t_im = tf32_bits(is_im ? qo : qq);
+                        *reinterpret_cast<uint2 *>(sm + S::AP32 + kmaj_off(ib + p, 2 * mm, 4, PADLBO, S::AP_SBO)) =
+                            make_uint2(t_re, t_im);
+                        const float nr = fmaf(wr, lam_r, -ws * ls), ns = fmaf(wr, ls, ws * lam_r);
+                        wr = nr;
+                        ws = ns;
+                    }
+                } else {
+                    // factorised: L'' = 2^-fsc B sum_j G[i,j] lambda^-j, u = lambda P + 2^fsc L'',
+                    // a = lambda^i u, z = a lambda^i; Ya = 2^fsc z (the table is 2^-fsc B lambda^-j),
+                    // a' = a lambda^(i+1) = z lambda
+                    const float l2s = sg * l2i;
+                    float wr = v0r, ws = sg * v0i;  // lambda^(2i) at my first position, as (Re, s Im)
+#pragma unroll
+                    for (int p = 0; p < 16; ++p) {
+                        const float pm = is_im ? pv[16 + p] : pv[p], ps = is_im ? pv[p] : pv[16 + p];
+                        const float lm = is_im ? lv[16 + p] : lv[p], lsd = is_im ? lv[p] : lv[16 + p];
+                        const float po = __shfl_xor_sync(0xffffffffu, ps, 1);
+                        const float lo = __shfl_xor_sync(0xffffffffu, lsd, 1);
+                        const float uo = fmaf(pm, lam_r, fmaf(po, ls, lm * fS));
+                        const float up = fmaf(po, lam_r, fmaf(-pm, ls, lo * fS));
+                        const float zo = fmaf(uo, wr, up * ws), zp = fmaf(up, wr, -uo * ws);
+                        yo[p] = zo * (-sg * fS);
+                        yq[p] = zp * (sg * fS);
+                        mo = fmaxf(mo, fabsf(yo[p]));
+                        mq = fmaxf(mq, fabsf(yq[p]));
+                        const float qo = -sg * fmaf(zo, lam_r, zp * ls), qq = sg * fmaf(zp, lam_r, -zo * ls);
+                        const uint32_t t_re = tf32_bits(is_im ? qq : qo), t_im = tf32_bits(is_im ? qo : qq);
+                        *reinterpret_cast<uint2 *>(sm + S::AP32 + kmaj_off(ib + p, 2 * mm, 4, PADLBO, S::AP_SBO)) =
+                            make_uint2(t_re, t_im);
+                        const float nr = fmaf(wr, l2r, -ws * l2s), ns = fmaf(wr, l2s, ws * l2r);
+                        wr = nr;
+                        ws = ns;
+                    }
                 }
                 // column (plane) maxima over the 64 positions: partner lane, then the other half
                 mo = fmaxf(mo, __shfl_xor_sync(0xffffffffu, mq, 1));
@@ -780,42 +863,76 @@ __global__ void __launch_bounds__(NTH, 1)
             tc_fence_after();
             if (__syncthreads_or(!ok)) break;
 
-            // ---- S7: A2 = unskewed, masked A2' (row-scaled fp16) ------------------------------
-            // scratch over XQ32 (P^T, its last reader, is complete)
-            scr = reinterpret_cast<float *>(sm + S::XQ32);
-            if (q4 < 2) {
+            // ---- S7: A2 = unskewed (skewed path), masked A2' (row-scaled fp16) ----------------
+            // skewed path: scratch over XQ32 (P^T, its last reader, is complete)
+            if constexpr (!FACT) {
+                scr = reinterpret_cast<float *>(sm + S::XQ32);
+                if (q4 < 2) {
+                    const int i = tl;
+        #pragma unroll
+                    for (int c0 = 32 * hsel; c0 < 32 * hsel + 32; c0 += 16) {
+                        float v[16];
+                        tmem_ld16(tb + lane_base + T::G + c0, v);
+                        tmem_wait_ld();
+        #pragma unroll
+                        for (int j = 0; j < 16; ++j) scr[i * 64 + ((c0 + j + i) & 63)] = v[j];
+                    }
+                }
+                __syncthreads();
+                {
+                    const int i = tid >> 2, p = tid & 3;
+                    float v16[16];
+                    float amax = 0.f;
+        #pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int j = 16 * p + u;
+                        v16[u] = j <= i ? scr[i * 64 + ((2 * i - j) & 63)] : 0.f;
+                        amax = fmaxf(amax, fabsf(v16[u]));
+                    }
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                    const int e = down_exp(amax);
+                    const float sdown = pow2i(-e);
+                    if (p == 0) osc[i] = pow2i(e);
+        #pragma unroll
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        float g8[8];
+        #pragma unroll
+                        for (int u = 0; u < 8; ++u) g8[u] = v16[8 * h8 + u] * sdown;
+                        *reinterpret_cast<uint4 *>(sm + S::A216 + kmaj_off(i, 16 * p + 8 * h8, 2, 128, 1024)) = pack_f16x8(g8);
+                    }
+                }
+            } else {
+                // row i of A2, my half of the columns, masked to j <= i; the row maximum of both
+                // halves via GP16 (consumed)
+                float *xch = reinterpret_cast<float *>(sm + S::GP16);
                 const int i = tl;
-    #pragma unroll
-                for (int c0 = 32 * hsel; c0 < 32 * hsel + 32; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(tb + lane_base + T::G + c0, v);
+                float v[32];
+                if (q4 < 2) {
+                    tmem_ld16(tb + lane_base + T::G + 32 * hsel, v);
+                    tmem_ld16(tb + lane_base + T::G + 32 * hsel + 16, v + 16);
                     tmem_wait_ld();
-    #pragma unroll
-                    for (int j = 0; j < 16; ++j) scr[i * 64 + ((c0 + j + i) & 63)] = v[j];
+                    float amax = 0.f;
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        v[u] = 32 * hsel + u <= i ? v[u] : 0.f;
+                        amax = fmaxf(amax, fabsf(v[u]));
+                    }
+                    xch[hsel * 64 + i] = amax;
                 }
-            }
-            __syncthreads();
-            {
-                const int i = tid >> 2, p = tid & 3;
-                float v16[16];
-                float amax = 0.f;
-    #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int j = 16 * p + u;
-                    v16[u] = j <= i ? scr[i * 64 + ((2 * i - j) & 63)] : 0.f;
-                    amax = fmaxf(amax, fabsf(v16[u]));
-                }
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                const int e = down_exp(amax);
-                const float sdown = pow2i(-e);
-                if (p == 0) osc[i] = pow2i(e);
-    #pragma unroll
-                for (int h8 = 0; h8 < 2; ++h8) {
-                    float g8[8];
-    #pragma unroll
-                    for (int u = 0; u < 8; ++u) g8[u] = v16[8 * h8 + u] * sdown;
-                    *reinterpret_cast<uint4 *>(sm + S::A216 + kmaj_off(i, 16 * p + 8 * h8, 2, 128, 1024)) = pack_f16x8(g8);
+                __syncthreads();
+                if (q4 < 2) {
+                    const int e = down_exp(fmaxf(xch[i], xch[64 + i]));
+                    const float sdown = pow2i(-e);
+                    if (hsel == 0) osc[i] = pow2i(e);
+#pragma unroll
+                    for (int k8 = 0; k8 < 4; ++k8) {
+                        float g8[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) g8[u] = v[8 * k8 + u] * sdown;
+                        *reinterpret_cast<uint4 *>(sm + S::A216 + kmaj_off(i, 32 * hsel + 8 * k8, 2, 128, 1024)) =
+                            pack_f16x8(g8);
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -1003,10 +1120,6 @@ __global__ void __launch_bounds__(NTH, 1)
             const size_t used = 2 * plane + 2 * M + 2 * (size_t)(W - 1) * R;
             for (size_t x = used + tid; x < a.state_floats; x += NTH) fs[x] = 0.f;
         }
-        // the next piece rewrites the tables, the TMEM state and the taps
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
     }
     tc_fence_before();
     __syncthreads();
@@ -1063,9 +1176,8 @@ __global__ void __launch_bounds__(NTH, 2)
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const int H = a.H, M = 64, W = a.W;
     // block sgi of unit `unit` (blocks before the unit's last piece are full)
-    const int nloc = plan.nb - 1;
+    const int nloc = plan_state_blocks(plan);
     const int unit = blockIdx.x / nloc, sgi = blockIdx.x % nloc, b = unit / H, h = unit % H;
-    if (sgi >= plan_last_start(plan, unit)) return;  // no piece starts after this block
     const int c_begin = sgi * plan.fs, c_end = c_begin + plan.fs;
     const uint32_t raw_bytes = (uint32_t)(CH + HALO) * R * 2 + (uint32_t)CH * D * 2;
     const int mm = tl >> 1, is_im = tl & 1;
@@ -1314,8 +1426,8 @@ __global__ void __launch_bounds__(NTH, 2)
     if (warp == 0) tmem_dealloc(tb, 256);
 }
 
-// In place over [unit][block][R+128][128]: slot j becomes the state before block j + 1, for
-// the blocks before the unit's last piece.  Threads walk consecutive floats of one column
+// In place over [unit][block][R+128][128], the end states of the unit's first
+// plan_state_blocks() blocks: slot j becomes the state before block j + 1.  Threads walk consecutive floats of one column
 // (U: a complex pair per thread, adjacent lanes; Gamma^T: one value lane, Re and Im in two
 // columns), and each loads a batch of slots before running the recurrence through them.
 __global__ void segment_scan_kernel(const float *lambda, int H, int R, int D, int units, SegPlan plan,
@@ -1324,8 +1436,7 @@ __global__ void segment_scan_kernel(const float *lambda, int H, int R, int D, in
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long long)units * pairs) return;
     const int unit = (int)(idx / pairs), r = (int)(idx % pairs), h = unit % H;
-    const int nscan = plan_last_start(plan, unit);
-    if (nscan == 0) return;
+    const int nscan = plan_state_blocks(plan);
     int m;
     size_t re, im;
     if (r < upairs) {  // U column c, lanes 2m (Re) and 2m+1 (Im)
@@ -1354,7 +1465,7 @@ __global__ void segment_scan_kernel(const float *lambda, int H, int R, int D, in
     }
     constexpr int BATCH = 8;
     const size_t slot = (size_t)(R + MP) * 128;
-    float *base = seg_state + (size_t)unit * (plan.nb - 1) * slot;
+    float *base = seg_state + (size_t)unit * nscan * slot;
     float xr = 0.f, xi = 0.f;
     for (int j0 = 0; j0 < nscan; j0 += BATCH) {
         float lr[BATCH], li[BATCH];
@@ -1420,12 +1531,12 @@ static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const 
                                    const SegPlan &plan, float *ws) {
     const unsigned units = (unsigned)(a.B * a.H);
     cudaError_t e;
-    if (plan.nb > 1) {
+    if (plan.ppu > 1) {
         using SS = StateSmem<R, D>;
         auto sk = chunk_state_kernel<R, D>;
         e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::TOTAL);
         if (e != cudaSuccess) return e;
-        sk<<<units * (unsigned)(plan.nb - 1), NTH, SS::TOTAL, st>>>(a, mk, mv, plan, ws);
+        sk<<<units * (unsigned)plan_state_blocks(plan), NTH, SS::TOTAL, st>>>(a, mk, mv, plan, ws);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const long long pairs = (long long)units * 64 * (R + D);
         segment_scan_kernel<<<(unsigned)((pairs + 255) / 256), 256, 0, st>>>(a.lambda, a.H, R, D, (int)units, plan,
@@ -1433,11 +1544,16 @@ static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const 
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     using S = ChunkSmem<R, D>;
-    auto kern = chunk_prefill_kernel<R, D>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
-    if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((plan.total + plan.q - 1) / plan.q);
-    kern<<<grid, NTH, S::TOTAL, st>>>(a, mq, mk, mv, mo, plan, ws);
+    const unsigned grid = units * (unsigned)plan.ppu;
+    // factorised-Gram heads first, then (usually none) the skewed-Gram ones
+    auto kf = chunk_prefill_kernel<R, D, true>;
+    auto ks = chunk_prefill_kernel<R, D, false>;
+    if ((e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL)) != cudaSuccess)
+        return e;
+    kf<<<grid, NTH, S::TOTAL, st>>>(a, mq, mk, mv, mo, plan, ws);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ks<<<grid, NTH, S::TOTAL, st>>>(a, mq, mk, mv, mo, plan, ws);
     return cudaGetLastError();
 }
 
@@ -1447,60 +1563,70 @@ static bool chunk_path_takes(const PrefillArgs &a) {
 }
 
 // One CTA per unit, whole sequences: the plan without a workspace.
-static SegPlan whole_plan(long long units, int nchunks) {
+static SegPlan whole_plan(int nchunks) {
     SegPlan p;
-    p.fs = nchunks;
+    p.fs = nchunks > 0 ? nchunks : 1;
     p.nb = 1;
     p.q = 1;
-    p.total = (int)units;
+    p.ppu = 1;
     return p;
 }
 
-static SegPlan block_plan(long long units, int nchunks, int fs, int num_sms) {
+// Blocks of fs chunks, at most ppu pieces per unit (fewer if the blocks run out).
+static SegPlan block_plan(int nchunks, int fs, int ppu) {
     SegPlan p;
     p.fs = fs;
     p.nb = (nchunks + fs - 1) / fs;
-    p.total = (int)(units * p.nb);
-    p.q = (p.total + num_sms - 1) / num_sms;
+    p.q = (p.nb + ppu - 1) / ppu;
+    p.ppu = (p.nb + p.q - 1) / p.q;
     return p;
 }
 
 static size_t plan_workspace_bytes(const SegPlan &p, long long units, int R) {
-    return p.nb > 1 ? (size_t)units * (size_t)(p.nb - 1) * (size_t)(R + MP) * 128 * sizeof(float) : 0;
+    return (size_t)units * (size_t)plan_state_blocks(p) * (size_t)(R + MP) * 128 * sizeof(float);
 }
 
-// Modelled time of a plan in readout chunk times (a readout chunk is about 8 us): the
-// busiest readout CTA's chunks, plus, when sequences are split, the block state pass
-// (blocks of fs chunks, two CTAs per SM, a block chunk costing about kStateChunk of a
-// readout chunk), the scan (reads and writes the workspace once, about kScanBytes per
-// readout chunk time) and the two extra launches.
-constexpr double kStateChunk = 0.35;
-constexpr double kScanBytes = 40e6;
-constexpr double kSplitOverhead = 0.5;
-static double plan_cost(const SegPlan &p, long long units, int nchunks, int num_sms, int R) {
-    if (p.nb == 1) return (double)((units + num_sms - 1) / num_sms) * nchunks;
-    long long nstate = 0;
-    for (long long u = 0; u < units; ++u) nstate += plan_last_start(p, (int)u);
-    const long long waves = (nstate + 2LL * num_sms - 1) / (2LL * num_sms);
-    const double scan = 2.0 * (double)nstate * (R + MP) * 128 * sizeof(float) / kScanBytes;
-    return (double)p.q * p.fs + (double)waves * p.fs * kStateChunk + scan + kSplitOverhead;
+// Modelled time of a plan in readout chunk times (a readout chunk takes 7 to 10 us): the
+// readout waves times a piece's chunks, plus, when sequences are split, the block state
+// pass (fs chunks per CTA, one or two CTAs per SM: about kState1 / kState2 of a readout
+// chunk per chunk), the scan (about kScanBytes of workspace traffic per readout chunk
+// time) and the two extra launches.
+constexpr double kState1 = 0.4, kState2 = 0.6;
+constexpr double kScanBytes = 25e6;
+constexpr double kSplitOverhead = 0.8;
+static double plan_cost(const SegPlan &p, long long units, int num_sms, int R) {
+    const long long ctas = units * p.ppu;
+    const double readout = (double)((ctas + num_sms - 1) / num_sms) * p.q * p.fs;
+    if (p.ppu == 1) return readout;
+    const long long nstate = units * plan_state_blocks(p);
+    const double state = nstate <= num_sms ? p.fs * kState1
+                                           : (double)((nstate + 2LL * num_sms - 1) / (2LL * num_sms)) * p.fs * kState2;
+    const double scan = 2.0 * (double)plan_workspace_bytes(p, units, R) / kScanBytes;
+    return readout + state + scan + kSplitOverhead;
 }
 
-// The cheapest plan whose workspace fits `budget` bytes (block sizes 1, 2, 4, ... chunks;
-// ties go to the larger block, i.e. the smaller workspace).
+// The cheapest plan whose workspace fits `budget` bytes: pieces per unit up to one wave of
+// CTAs, any block size; ties go to the smaller workspace.
 static SegPlan choose_plan(const PrefillArgs &a, int num_sms, size_t budget) {
     const int nchunks = (a.N + CH - 1) / CH;
     const long long units = (long long)a.B * a.H;
-    SegPlan best = whole_plan(units, nchunks);
-    double best_cost = plan_cost(best, units, nchunks, num_sms, a.R);
-    if (units <= 0 || nchunks < 2 || units * (long long)nchunks > (1LL << 30)) return best;
-    for (int fs = 1; fs < nchunks; fs *= 2) {
-        const SegPlan p = block_plan(units, nchunks, fs, num_sms);
-        if (p.nb < 2 || plan_workspace_bytes(p, units, a.R) > budget) continue;
-        const double c = plan_cost(p, units, nchunks, num_sms, a.R);
-        if (c <= best_cost) {
-            best = p;
-            best_cost = c;
+    SegPlan best = whole_plan(nchunks);
+    if (units <= 0 || nchunks < 2 || units >= num_sms) return best;
+    double best_cost = plan_cost(best, units, num_sms, a.R);
+    size_t best_ws = 0;
+    const int max_ppu = (int)(num_sms / units);
+    for (int ppu = 2; ppu <= max_ppu && ppu <= nchunks; ++ppu) {
+        for (int fs = 1; fs <= (nchunks + ppu - 1) / ppu; ++fs) {
+            const SegPlan p = block_plan(nchunks, fs, ppu);
+            if (p.ppu < 2) continue;
+            const size_t ws = plan_workspace_bytes(p, units, a.R);
+            if (ws > budget) continue;
+            const double c = plan_cost(p, units, num_sms, a.R);
+            if (c < best_cost - 1e-9 || (c < best_cost + 1e-9 && ws < best_ws)) {
+                best = p;
+                best_cost = c;
+                best_ws = ws;
+            }
         }
     }
     return best;
@@ -1533,7 +1659,7 @@ ida_status launch_chunk_prefill(const PrefillArgs &a, cudaStream_t st, int num_s
         return IDA_OK;
     }
     const SegPlan plan = choose_plan(a, num_sms, workspace ? workspace_bytes : 0);
-    float *ws = plan.nb > 1 ? static_cast<float *>(workspace) : nullptr;
+    float *ws = plan.ppu > 1 ? static_cast<float *>(workspace) : nullptr;
     *taken = true;
     cudaError_t e;
     if (a.R == 128 && a.d == 128)

@@ -170,13 +170,13 @@ def test_eta_readout_constant_values_on_gpu(path):
 
 @pytest.mark.parametrize("shape", [(1, 64 * 40 + 17, 2, 128, 128), (2, 64 * 33, 1, 64, 128),
                                    (1, 64 * 24 + 1, 3, 128, 64),
-                                   # more blocks than SMs: CTAs run pieces of two or three units
+                                   # many units: a few pieces per unit, blocks of several chunks
                                    (4, 64 * 8 - 9, 10, 64, 64), (4, 64 * 9 + 3, 12, 128, 128)],
                          ids=lambda s: "B{}N{}H{}R{}d{}".format(*s))
 def test_segmented_prefill(shape):
-    """Sequences split into blocks whose pieces run on separate SMs (workspace path)
-    match the oracle, including a ragged last chunk, CTAs whose pieces span unit
-    boundaries, and the final state."""
+    """Sequences split into pieces that run on separate SMs, their start states from the
+    block state pass and scan (workspace path), match the oracle, including a ragged last
+    chunk and the final state."""
     B, N, H, R, d = shape
     q, k, v, p = problem(B, N, H, R, d, 64, 4, "bf16", seed=300 + N)
     dev = torch.device("cuda")
@@ -198,3 +198,44 @@ def test_segmented_prefill(shape):
     out2, _ = binding.ida_forward(qd, kd, vd, pd, workspace=ws[:16])
     torch.cuda.synchronize()
     assert rel_l2(to_np(out2), to_np(out1)) == 0.0
+
+
+@pytest.mark.parametrize("rd", [(64, 64), (128, 128)], ids=lambda t: "R{}d{}".format(*t))
+@pytest.mark.parametrize("split", [False, True], ids=["whole", "split"])
+def test_chunk_paths_per_head(rd, split):
+    """The tensor-core prefill picks its Gram formulation per head: the factorised one
+    (decay lambda^(i-j) as lambda^i lambda^-j, needs |lambda|^-63 and |B| in range) or the
+    skewed one (any stable mode).  Heads of both kinds, with complex B, in one call, whole
+    or split into pieces, match the oracle."""
+    R, d = rd
+    B, N, H, M, W = 2, 64 * 5 + 13, 4, 64, 4
+    q, k, v, p = problem(B, N, H, R, d, M, W, "bf16", seed=77 + R)
+    rng = np.random.default_rng(5)
+    m = np.arange(M)
+    lam = p["lambda"][..., 0] + 1j * p["lambda"][..., 1]
+    bvec = np.ones((H, M), dtype=np.complex128)
+    # head 0: slow modes, complex B of modulus 0.5 .. 2 (factorised)
+    bvec[0] = rng.uniform(0.5, 2.0, M) * np.exp(1j * rng.uniform(-np.pi, np.pi, M))
+    # head 1: fast decay, |lambda| = e^-0.5 (skewed)
+    lam[1] = np.exp(1.0 * (-0.5 + 1j * np.pi * m))
+    # head 2: |B| = 400 (skewed)
+    bvec[2] = 400.0 * np.exp(1j * rng.uniform(-np.pi, np.pi, M))
+    # head 3: one fast mode among slow ones, complex B (skewed for the whole head)
+    lam[3, 5] = np.exp(2.0 * (-0.5 + 0.2j))
+    bvec[3] = 1.5 * np.exp(1j * rng.uniform(-np.pi, np.pi, M))
+    p["lambda"] = np.ascontiguousarray(np.stack([lam.real, lam.imag], -1), dtype=np.float32)
+    p["Bvec"] = np.ascontiguousarray(np.stack([bvec.real, bvec.imag], -1), dtype=np.float32)
+    dev = torch.device("cuda")
+    pd = binding.params_to_device(p)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    ws = binding.forward_workspace(qd, vd, pd) if split else None
+    if split:
+        assert ws is not None, "this shape should be split"
+    out, fs = binding.ida_forward(qd, kd, vd, pd, final_state=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.ida_device_error() == 0
+    ref = orc.forward(q, k, v, p, final_state=True)
+    got = to_np(out)
+    for h in range(H):
+        assert rel_l2(got[:, :, h], ref["out"][:, :, h]) <= BF16_REL_L2, (h, rel_l2(got[:, :, h], ref["out"][:, :, h]))
+    assert rel_l2(unpadded_state(to_np(fs), d, R, M, W), ref["final_state"]) <= BF16_REL_L2
