@@ -48,7 +48,11 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <vector>
 #include <string>
 
 #include "ida_common.cuh"
@@ -162,19 +166,24 @@ __device__ __forceinline__ uint4 pack_f16x8(const float x[8]) {
 }
 
 // Work split of a batch of sequences across CTAs.  Each unit's chunks are grouped into nb
-// blocks of fs chunks (the last block may be shorter) and its blocks into ppu pieces of q
-// blocks; one CTA runs one piece.  A piece not at the sequence start needs the state before
-// its first block: the block state pass computes, from zero, the end state of each of the
-// unit's first (ppu - 1) q blocks and the block scan composes them into start states.
+// blocks of fs chunks (the last block may be shorter) and its blocks into ppu pieces: the
+// first of q0 blocks, the others of q blocks; one CTA runs one piece.  The grid lists the
+// later pieces of every unit before the first pieces, so that when there are more pieces
+// than SMs the short first pieces fill in behind.  A piece not at the sequence start needs
+// the state before its first block: the block state pass computes, from zero, the end
+// state of each block before the unit's last piece and the block scan composes them.
 struct SegPlan {
     int fs;   // chunks per block
     int nb;   // blocks per unit
-    int q;    // blocks per piece
+    int q0;   // blocks in a unit's first piece
+    int q;    // blocks in each later piece
     int ppu;  // pieces per unit
 };
 
-// Blocks per unit whose end states the state pass computes (all but the last piece's).
-__host__ __device__ inline int plan_state_blocks(const SegPlan &p) { return (p.ppu - 1) * p.q; }
+// Blocks per unit whose end states the state pass computes (all before the last piece).
+__host__ __device__ inline int plan_state_blocks(const SegPlan &p) {
+    return p.ppu > 1 ? p.q0 + (p.ppu - 2) * p.q : 0;
+}
 
 // FACT selects the Gram formulation; a CTA whose head takes the other one returns at once
 // (the other instantiation, launched on the same plan, runs that piece).
@@ -216,8 +225,11 @@ __global__ void __launch_bounds__(NTH, 1)
     }
 
     // ---- this CTA's piece: chunks [c_begin, c_end) of unit `unit` ---------------------
-    const int unit = blockIdx.x / plan.ppu, j0 = (blockIdx.x % plan.ppu) * plan.q;
-    const int j1 = min(plan.nb, j0 + plan.q);
+    const int nlater = a.B * a.H * (plan.ppu - 1);  // later pieces come first in the grid
+    const int unit = (int)blockIdx.x < nlater ? (int)blockIdx.x / (plan.ppu - 1) : (int)blockIdx.x - nlater;
+    const int pc = (int)blockIdx.x < nlater ? 1 + (int)blockIdx.x % (plan.ppu - 1) : 0;
+    const int j0 = pc == 0 ? 0 : plan.q0 + (pc - 1) * plan.q;
+    const int j1 = min(plan.nb, pc == 0 ? plan.q0 : j0 + plan.q);
     const int b = unit / H, h = unit % H;
     const int c_begin = j0 * plan.fs, c_end = min(nchunks, j1 * plan.fs);
     const size_t base_qk = ((size_t)b * N * H + h) * R;
@@ -1427,9 +1439,10 @@ __global__ void __launch_bounds__(NTH, 2)
 }
 
 // In place over [unit][block][R+128][128], the end states of the unit's first
-// plan_state_blocks() blocks: slot j becomes the state before block j + 1.  Threads walk consecutive floats of one column
-// (U: a complex pair per thread, adjacent lanes; Gamma^T: one value lane, Re and Im in two
-// columns), and each loads a batch of slots before running the recurrence through them.
+// plan_state_blocks() blocks: slot j becomes the state before block j + 1.  Threads walk
+// consecutive floats of one column (U: a complex pair per thread, adjacent lanes; Gamma^T:
+// one value lane, Re and Im in two columns), and each loads a batch of slots before running
+// the recurrence through them.
 __global__ void segment_scan_kernel(const float *lambda, int H, int R, int D, int units, SegPlan plan,
                                     float *seg_state) {
     const int upairs = 64 * R, pairs = upairs + 64 * D;  // complex pairs of one state image
@@ -1567,18 +1580,31 @@ static SegPlan whole_plan(int nchunks) {
     SegPlan p;
     p.fs = nchunks > 0 ? nchunks : 1;
     p.nb = 1;
+    p.q0 = 1;
     p.q = 1;
     p.ppu = 1;
     return p;
 }
 
-// Blocks of fs chunks, at most ppu pieces per unit (fewer if the blocks run out).
+// Blocks of fs chunks, at most ppu equal pieces per unit (fewer if the blocks run out).
 static SegPlan block_plan(int nchunks, int fs, int ppu) {
     SegPlan p;
     p.fs = fs;
     p.nb = (nchunks + fs - 1) / fs;
     p.q = (p.nb + ppu - 1) / ppu;
+    p.q0 = p.q;
     p.ppu = (p.nb + p.q - 1) / p.q;
+    return p;
+}
+
+// Two pieces per unit: the first c1 = q0 fs chunks, the second the rest.
+static SegPlan two_piece_plan(int nchunks, int fs, int q0) {
+    SegPlan p;
+    p.fs = fs;
+    p.nb = q0 + (nchunks - q0 * fs + fs - 1) / fs;
+    p.q0 = q0;
+    p.q = p.nb - q0;
+    p.ppu = 2;
     return p;
 }
 
@@ -1587,16 +1613,36 @@ static size_t plan_workspace_bytes(const SegPlan &p, long long units, int R) {
 }
 
 // Modelled time of a plan in readout chunk times (a readout chunk takes 7 to 10 us): the
-// readout waves times a piece's chunks, plus, when sequences are split, the block state
-// pass (fs chunks per CTA, one or two CTAs per SM: about kState1 / kState2 of a readout
-// chunk per chunk), the scan (about kScanBytes of workspace traffic per readout chunk
-// time) and the two extra launches.
+// readout's makespan (pieces dealt in grid order to the SMs, one CTA each), plus, when
+// sequences are split, the block state pass (fs chunks per CTA, one or two CTAs per SM:
+// about kState1 / kState2 of a readout chunk per chunk), the scan (about kScanBytes of
+// workspace traffic per readout chunk time) and the two extra launches.
 constexpr double kState1 = 0.4, kState2 = 0.6;
 constexpr double kScanBytes = 25e6;
 constexpr double kSplitOverhead = 0.8;
-static double plan_cost(const SegPlan &p, long long units, int num_sms, int R) {
-    const long long ctas = units * p.ppu;
-    const double readout = (double)((ctas + num_sms - 1) / num_sms) * p.q * p.fs;
+static double plan_cost(const SegPlan &p, long long units, int nchunks, int num_sms, int R) {
+    double readout;
+    if (p.ppu == 1) {
+        readout = (double)((units + num_sms - 1) / num_sms) * nchunks;
+    } else {
+        // later pieces (the last one may be short) first, then the first pieces
+        std::vector<double> free_at((size_t)num_sms, 0.0);
+        std::priority_queue<double, std::vector<double>, std::greater<double>> sms(free_at.begin(), free_at.end());
+        double makespan = 0.0;
+        auto deal = [&](double len) {
+            const double t = sms.top() + len;
+            sms.pop();
+            sms.push(t);
+            makespan = std::max(makespan, t);
+        };
+        for (long long u = 0; u < units; ++u)
+            for (int pc = 1; pc < p.ppu; ++pc) {
+                const int j0 = p.q0 + (pc - 1) * p.q, j1 = std::min(p.nb, j0 + p.q);
+                deal((double)(std::min(nchunks, j1 * p.fs) - j0 * p.fs));
+            }
+        for (long long u = 0; u < units; ++u) deal((double)std::min(nchunks, p.q0 * p.fs));
+        readout = makespan;
+    }
     if (p.ppu == 1) return readout;
     const long long nstate = units * plan_state_blocks(p);
     const double state = nstate <= num_sms ? p.fs * kState1
@@ -1605,30 +1651,57 @@ static double plan_cost(const SegPlan &p, long long units, int num_sms, int R) {
     return readout + state + scan + kSplitOverhead;
 }
 
-// The cheapest plan whose workspace fits `budget` bytes: pieces per unit up to one wave of
-// CTAs, any block size; ties go to the smaller workspace.
+// The cheapest plan whose workspace fits `budget` bytes, among equal pieces (up to one wave
+// of CTAs, any block size) and, with fewer than two SMs per unit, two unequal pieces; ties
+// go to the smaller workspace.  Plans are remembered per shape.
 static SegPlan choose_plan(const PrefillArgs &a, int num_sms, size_t budget) {
     const int nchunks = (a.N + CH - 1) / CH;
     const long long units = (long long)a.B * a.H;
     SegPlan best = whole_plan(nchunks);
     if (units <= 0 || nchunks < 2 || units >= num_sms) return best;
-    double best_cost = plan_cost(best, units, num_sms, a.R);
-    size_t best_ws = 0;
-    const int max_ppu = (int)(num_sms / units);
-    for (int ppu = 2; ppu <= max_ppu && ppu <= nchunks; ++ppu) {
-        for (int fs = 1; fs <= (nchunks + ppu - 1) / ppu; ++fs) {
-            const SegPlan p = block_plan(nchunks, fs, ppu);
-            if (p.ppu < 2) continue;
-            const size_t ws = plan_workspace_bytes(p, units, a.R);
-            if (ws > budget) continue;
-            const double c = plan_cost(p, units, num_sms, a.R);
-            if (c < best_cost - 1e-9 || (c < best_cost + 1e-9 && ws < best_ws)) {
-                best = p;
-                best_cost = c;
-                best_ws = ws;
-            }
+
+    struct Key {
+        long long units;
+        int nchunks, R, num_sms;
+        size_t budget;
+        bool operator==(const Key &o) const {
+            return units == o.units && nchunks == o.nchunks && R == o.R && num_sms == o.num_sms && budget == o.budget;
         }
+    };
+    static std::mutex mu;
+    static std::vector<std::pair<Key, SegPlan>> memo;
+    const Key key{units, nchunks, a.R, num_sms, budget};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const auto &e : memo)
+            if (e.first == key) return e.second;
     }
+
+    // a split must model at least 3% faster than whole sequences to be taken
+    double best_cost = 0.97 * plan_cost(best, units, nchunks, num_sms, a.R);
+    size_t best_ws = 0;
+    auto consider = [&](const SegPlan &p) {
+        if (p.ppu < 2) return;
+        const size_t ws = plan_workspace_bytes(p, units, a.R);
+        if (ws > budget) return;
+        const double c = plan_cost(p, units, nchunks, num_sms, a.R);
+        if (c < best_cost - 1e-9 || (c < best_cost + 1e-9 && ws < best_ws)) {
+            best = p;
+            best_cost = c;
+            best_ws = ws;
+        }
+    };
+    const int max_ppu = (int)(num_sms / units);
+    for (int ppu = 2; ppu <= max_ppu && ppu <= nchunks; ++ppu)
+        for (int fs = 1; fs <= (nchunks + ppu - 1) / ppu; ++fs) consider(block_plan(nchunks, fs, ppu));
+    if (2 * units > num_sms)
+        for (int c1 = 1; c1 < nchunks; ++c1)
+            for (int fs = 1; fs <= c1; ++fs)
+                if (c1 % fs == 0) consider(two_piece_plan(nchunks, fs, c1 / fs));
+
+    std::lock_guard<std::mutex> lock(mu);
+    if (memo.size() >= 64) memo.erase(memo.begin());
+    memo.emplace_back(key, best);
     return best;
 }
 

@@ -171,7 +171,9 @@ def test_eta_readout_constant_values_on_gpu(path):
 @pytest.mark.parametrize("shape", [(1, 64 * 40 + 17, 2, 128, 128), (2, 64 * 33, 1, 64, 128),
                                    (1, 64 * 24 + 1, 3, 128, 64),
                                    # many units: a few pieces per unit, blocks of several chunks
-                                   (4, 64 * 8 - 9, 10, 64, 64), (4, 64 * 9 + 3, 12, 128, 128)],
+                                   (4, 64 * 8 - 9, 10, 64, 64), (4, 64 * 9 + 3, 12, 128, 128),
+                                   # fewer than two SMs per unit: a short first piece and a long second
+                                   (8, 64 * 11 + 7, 12, 64, 64)],
                          ids=lambda s: "B{}N{}H{}R{}d{}".format(*s))
 def test_segmented_prefill(shape):
     """Sequences split into pieces that run on separate SMs, their start states from the
