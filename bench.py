@@ -178,11 +178,11 @@ class Prefill:
         self.ws = binding.forward_workspace(self.q, self.v, self.pd, flags)
         self.in_bytes = sum(t.numel() * t.element_size() for t in self.host)
         # tensor-core path: readout kernels for the factorised- and the skewed-Gram heads, plus the
-        # block state pass and scan when split; the eta readout runs one sequential kernel
+        # block state pass when split; the eta readout runs one sequential kernel
         if flags & binding.IDA_READOUT_ETA:
             self.launches_per_step = 1
         else:
-            self.launches_per_step = 2 if self.ws is None else 4
+            self.launches_per_step = 2 if self.ws is None else 3
 
     def step(self):
         self.b.ida_forward(self.q, self.k, self.v, self.pd, out=self.out, final_state=self.fs,

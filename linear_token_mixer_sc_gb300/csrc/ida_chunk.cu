@@ -100,7 +100,8 @@ struct ChunkSmem {
     static constexpr int OSC = TSLOT + 16;                       // [64] float: row scales of A2
     static constexpr int LAML = OSC + CH * 4;                    // [64] float2: lambda^L per mode
     static constexpr int SUML = LAML + 64 * 8;                   // [64] float2: sum_{k<L} lambda^k per mode
-    static constexpr int NWS = SUML + 64 * 8;                    // [R+D] float RMSNorm weights
+    static constexpr int GBLK = SUML + 64 * 8;                   // [64] float2: lambda^(64 fs), one block's decay
+    static constexpr int NWS = GBLK + 64 * 8;                    // [R+D] float RMSNorm weights
     static constexpr int BSS = NWS + (R + D) * 4;                // [R+D] float RMSNorm biases
     static constexpr int TOTAL = BSS + (R + D) * 4;
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
@@ -171,7 +172,8 @@ __device__ __forceinline__ uint4 pack_f16x8(const float x[8]) {
 // later pieces of every unit before the first pieces, so that when there are more pieces
 // than SMs the short first pieces fill in behind.  A piece not at the sequence start needs
 // the state before its first block: the block state pass computes, from zero, the end
-// state of each block before the unit's last piece and the block scan composes them.
+// state of each block before the unit's last piece, and the piece's CTA composes those of
+// the blocks before it as it loads its start state.
 struct SegPlan {
     int fs;   // chunks per block
     int nb;   // blocks per unit
@@ -202,6 +204,7 @@ __global__ void __launch_bounds__(NTH, 1)
     float *osc = reinterpret_cast<float *>(sm + S::OSC);
     float2 *laml = reinterpret_cast<float2 *>(sm + S::LAML);
     float2 *suml = reinterpret_cast<float2 *>(sm + S::SUML);
+    float2 *gblk = reinterpret_cast<float2 *>(sm + S::GBLK);
     float *nws = reinterpret_cast<float *>(sm + S::NWS);
     float *bss = reinterpret_cast<float *>(sm + S::BSS);
 
@@ -348,6 +351,19 @@ __global__ void __launch_bounds__(NTH, 1)
             if (!is_im) {
                 laml[mm] = make_float2(qr, qi);  // lambda^C
                 suml[mm] = make_float2(sr, si);  // sum_{k<C} lambda^k
+                // lambda^(C fs) = (lambda^C)^fs, the decay across one block
+                float gr = 1.f, gi = 0.f, pr = qr, pi = qi;
+                for (unsigned e = (unsigned)plan.fs; e; e >>= 1) {
+                    if (e & 1u) {
+                        const float nr = gr * pr - gi * pi, ni = gr * pi + gi * pr;
+                        gr = nr;
+                        gi = ni;
+                    }
+                    const float nr = pr * pr - pi * pi, ni = 2.f * pr * pi;
+                    pr = nr;
+                    pi = ni;
+                }
+                gblk[mm] = make_float2(gr, gi);
             }
             if constexpr (FACT) {
                 // factorised table row: component of B lambda^-j 2^-fsc, j = 0..63
@@ -376,15 +392,36 @@ __global__ void __launch_bounds__(NTH, 1)
         __syncthreads();
         tc_fence_after();
         {
-            // start state: zero at the sequence start, else the state before block j0 from the
-            // block scan ([R+128 columns][128 lanes] floats, columns as in TMEM), by column half
-            const float *x0 = j0 > 0 ? seg_start + ((size_t)unit * plan_state_blocks(plan) + (j0 - 1)) *
-                                                   (size_t)(R + MP) * 128
-                                     : nullptr;
+            // start state: zero at the sequence start, else the state before block j0,
+            //   X = sum_{j < j0} g^(j0-1-j) X_local(j),  g = lambda^(C fs) per mode,
+            // by Horner over the block end states ([R+128 columns][128 lanes] floats, columns as
+            // in TMEM); U columns pair Re / Im across lanes 2m, 2m+1, Gamma^T columns across
+            // columns R+2m, R+2m+1.  By column half.
+            const float *xs = seg_start + (size_t)unit * plan_state_blocks(plan) * (size_t)(R + MP) * 128;
+            const float2 gu = gblk[mm];
+            const float gus = is_im ? gu.y : -gu.y;  // own(g z) = z_own Re g + z_partner s Im g
             for (int c0 = hsel * 16; c0 < R + MP; c0 += 32) {
                 float z[16];
     #pragma unroll
-                for (int i = 0; i < 16; ++i) z[i] = x0 ? x0[(size_t)(c0 + i) * 128 + tl] : 0.f;
+                for (int i = 0; i < 16; ++i) z[i] = 0.f;
+                for (int j = 0; j < j0; ++j) {
+                    const float *x = xs + (size_t)j * (R + MP) * 128 + (size_t)c0 * 128 + tl;
+                    if (c0 < R) {
+    #pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float zp = __shfl_xor_sync(0xffffffffu, z[i], 1);
+                            z[i] = fmaf(z[i], gu.x, fmaf(zp, gus, x[(size_t)i * 128]));
+                        }
+                    } else {
+    #pragma unroll
+                        for (int i = 0; i < 16; i += 2) {
+                            const float2 g = gblk[(c0 - R + i) >> 1];
+                            const float zr = z[i], zi = z[i + 1];
+                            z[i] = fmaf(g.x, zr, fmaf(-g.y, zi, x[(size_t)i * 128]));
+                            z[i + 1] = fmaf(g.x, zi, fmaf(g.y, zr, x[(size_t)(i + 1) * 128]));
+                        }
+                    }
+                }
                 tmem_st16(tb + lane_base + c0, z);
             }
             if (hsel == 0) {
@@ -1146,9 +1183,9 @@ __global__ void __launch_bounds__(NTH, 1)
 //   X_start(j) = sum_{j' < j} lambda^(P (j - 1 - j')) X_local(j')
 // where X_local(j') = sum_{t in j'} B lambda^(P - 1 - t') z_t (t' the position inside the
 // block) is the state block j' reaches from zero.  chunk_state_kernel computes X_local of
-// every block before the unit's last piece, segment_scan_kernel turns them into start
-// states in place, and chunk_prefill_kernel then runs all pieces in parallel.  States are
-// kept as [R + 128 columns][128 lanes] floats, the TMEM image of U and Gamma^T.
+// every block before the unit's last piece; chunk_prefill_kernel then runs all pieces in
+// parallel, each composing its start state from the X_local before it.  States are kept
+// as [R + 128 columns][128 lanes] floats, the TMEM image of U and Gamma^T.
 //
 // X_local is one contraction over the block's positions: per chunk c of the block, the
 // state-update MMAs accumulate Coef_c . Kt_c and Vt_c^T . Coef_c^T with
@@ -1438,70 +1475,6 @@ __global__ void __launch_bounds__(NTH, 2)
     if (warp == 0) tmem_dealloc(tb, 256);
 }
 
-// In place over [unit][block][R+128][128], the end states of the unit's first
-// plan_state_blocks() blocks: slot j becomes the state before block j + 1.  Threads walk
-// consecutive floats of one column (U: a complex pair per thread, adjacent lanes; Gamma^T:
-// one value lane, Re and Im in two columns), and each loads a batch of slots before running
-// the recurrence through them.
-__global__ void segment_scan_kernel(const float *lambda, int H, int R, int D, int units, SegPlan plan,
-                                    float *seg_state) {
-    const int upairs = 64 * R, pairs = upairs + 64 * D;  // complex pairs of one state image
-    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (long long)units * pairs) return;
-    const int unit = (int)(idx / pairs), r = (int)(idx % pairs), h = unit % H;
-    const int nscan = plan_state_blocks(plan);
-    int m;
-    size_t re, im;
-    if (r < upairs) {  // U column c, lanes 2m (Re) and 2m+1 (Im)
-        const int c = r / 64;
-        m = r % 64;
-        re = (size_t)c * 128 + 2 * m;
-        im = re + 1;
-    } else {  // Gamma^T lane jv, columns R+2m (Re) and R+2m+1 (Im)
-        const int r2 = r - upairs;
-        m = r2 / D;
-        const int jv = r2 % D;
-        re = (size_t)(R + 2 * m) * 128 + jv;
-        im = re + 128;
-    }
-    // g = lambda^(C * fs), the decay across one block, by binary exponentiation
-    float gr = 1.f, gi = 0.f, pr = lambda[((size_t)h * 64 + m) * 2], pi = lambda[((size_t)h * 64 + m) * 2 + 1];
-    for (unsigned e = (unsigned)(CH * plan.fs); e; e >>= 1) {
-        if (e & 1u) {
-            const float nr = gr * pr - gi * pi, ni = gr * pi + gi * pr;
-            gr = nr;
-            gi = ni;
-        }
-        const float nr = pr * pr - pi * pi, ni = 2.f * pr * pi;
-        pr = nr;
-        pi = ni;
-    }
-    constexpr int BATCH = 8;
-    const size_t slot = (size_t)(R + MP) * 128;
-    float *base = seg_state + (size_t)unit * nscan * slot;
-    float xr = 0.f, xi = 0.f;
-    for (int j0 = 0; j0 < nscan; j0 += BATCH) {
-        float lr[BATCH], li[BATCH];
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            if (j0 + u < nscan) {
-                lr[u] = base[(j0 + u) * slot + re];
-                li[u] = base[(j0 + u) * slot + im];
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            if (j0 + u < nscan) {
-                const float nr = gr * xr - gi * xi + lr[u], ni = gr * xi + gi * xr + li[u];
-                xr = nr;
-                xi = ni;
-                base[(j0 + u) * slot + re] = xr;
-                base[(j0 + u) * slot + im] = xi;
-            }
-        }
-    }
-}
-
 // ---- host side ---------------------------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -1550,10 +1523,6 @@ static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const 
         e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::TOTAL);
         if (e != cudaSuccess) return e;
         sk<<<units * (unsigned)plan_state_blocks(plan), NTH, SS::TOTAL, st>>>(a, mk, mv, plan, ws);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        const long long pairs = (long long)units * 64 * (R + D);
-        segment_scan_kernel<<<(unsigned)((pairs + 255) / 256), 256, 0, st>>>(a.lambda, a.H, R, D, (int)units, plan,
-                                                                          ws);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     using S = ChunkSmem<R, D>;
@@ -1613,13 +1582,14 @@ static size_t plan_workspace_bytes(const SegPlan &p, long long units, int R) {
 }
 
 // Modelled time of a plan in readout chunk times (a readout chunk takes 7 to 10 us): the
-// readout's makespan (pieces dealt in grid order to the SMs, one CTA each), plus, when
-// sequences are split, the block state pass (fs chunks per CTA, one or two CTAs per SM:
-// about kState1 / kState2 of a readout chunk per chunk), the scan (about kScanBytes of
-// workspace traffic per readout chunk time) and the two extra launches.
+// readout's makespan (pieces dealt in grid order to the SMs, one CTA each) and, when
+// sequences are split, the readout CTAs' loads of the block end states they compose (about
+// kLoadBytes per readout chunk time), the block state pass before it (fs chunks per CTA,
+// one or two CTAs per SM: about kState1 / kState2 of a readout chunk per chunk) and the
+// extra launch.
 constexpr double kState1 = 0.4, kState2 = 0.6;
-constexpr double kScanBytes = 25e6;
-constexpr double kSplitOverhead = 0.8;
+constexpr double kLoadBytes = 40e6;
+constexpr double kSplitOverhead = 0.5;
 static double plan_cost(const SegPlan &p, long long units, int nchunks, int num_sms, int R) {
     double readout;
     if (p.ppu == 1) {
@@ -1647,8 +1617,10 @@ static double plan_cost(const SegPlan &p, long long units, int nchunks, int num_
     const long long nstate = units * plan_state_blocks(p);
     const double state = nstate <= num_sms ? p.fs * kState1
                                            : (double)((nstate + 2LL * num_sms - 1) / (2LL * num_sms)) * p.fs * kState2;
-    const double scan = 2.0 * (double)plan_workspace_bytes(p, units, R) / kScanBytes;
-    return readout + state + scan + kSplitOverhead;
+    long long loads = 0;  // block end states read by all later pieces
+    for (int pc = 1; pc < p.ppu; ++pc) loads += p.q0 + (long long)(pc - 1) * p.q;
+    const double load = (double)units * loads * (R + MP) * 128 * sizeof(float) / kLoadBytes;
+    return readout + load + state + kSplitOverhead;
 }
 
 // The cheapest plan whose workspace fits `budget` bytes, among equal pieces (up to one wave
