@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Nominal GB300 unit counts for the FP32 CUDA-core peak (decode arithmetic):
 # 152 SMs x 128 FP32 lanes x 2 flops (FMA) x 2.07 GHz max SM clock.
 FP32_TFLOPS_NOMINAL = 152 * 128 * 2 * 2.07e9 / 1e12
-PREFILL_SOURCES = ["ida_chunk.cu", "ida_seq.cu", "ida_common.cuh", "ida_api.cu"]
+PREFILL_SOURCES = ["ida_chunk.cu", "ida_seq.cu", "ida_common.cuh", "tc_sm103.cuh", "ida_api.cu"]
 DECODE_SOURCES = ["ida_decode.cu", "ida_common.cuh", "ida_api.cu"]
 
 
