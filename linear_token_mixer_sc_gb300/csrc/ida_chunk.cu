@@ -1206,11 +1206,15 @@ struct StateSmem {
     static constexpr int NWS = TSLOT + 16;                            // [R+D] float
     static constexpr int BSS = NWS + (R + D) * 4;                     // [R+D] float
     static constexpr int TOTAL = BSS + (R + D) * 4;
-    static_assert(RAWV % 1024 == 0 && TOTAL <= 113 * 1024, "two state-pass CTAs per SM");
+    static_assert(RAWV % 1024 == 0 && TOTAL <= 116 * 1024, "shared memory budget");
+    // Launched with LAUNCH bytes so that one CTA runs per SM: with two co-resident CTAs the
+    // Gamma^T accumulator of the second one was intermittently wrong (seen on GB300, cause
+    // not identified), and one CTA per SM is always right.
+    static constexpr int LAUNCH = 116 * 1024;
 };
 
 template <int R, int D>
-__global__ void __launch_bounds__(NTH, 2)
+__global__ void __launch_bounds__(NTH, 1)
     chunk_state_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, SegPlan plan, float *seg_state) {
     using S = StateSmem<R, D>;
@@ -1520,9 +1524,9 @@ static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const 
     if (plan.ppu > 1) {
         using SS = StateSmem<R, D>;
         auto sk = chunk_state_kernel<R, D>;
-        e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::TOTAL);
+        e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::LAUNCH);
         if (e != cudaSuccess) return e;
-        sk<<<units * (unsigned)plan_state_blocks(plan), NTH, SS::TOTAL, st>>>(a, mk, mv, plan, ws);
+        sk<<<units * (unsigned)plan_state_blocks(plan), NTH, SS::LAUNCH, st>>>(a, mk, mv, plan, ws);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     using S = ChunkSmem<R, D>;
@@ -1584,10 +1588,9 @@ static size_t plan_workspace_bytes(const SegPlan &p, long long units, int R) {
 // Modelled time of a plan in readout chunk times (a readout chunk takes 7 to 10 us): the
 // readout's makespan (pieces dealt in grid order to the SMs, one CTA each) and, when
 // sequences are split, the readout CTAs' loads of the block end states they compose (about
-// kLoadBytes per readout chunk time), the block state pass before it (fs chunks per CTA,
-// one or two CTAs per SM: about kState1 / kState2 of a readout chunk per chunk) and the
-// extra launch.
-constexpr double kState1 = 0.4, kState2 = 0.6;
+// kLoadBytes per readout chunk time), the block state pass before it (waves of one CTA per
+// SM, fs chunks per CTA, about kState1 of a readout chunk per chunk) and the extra launch.
+constexpr double kState1 = 0.4;
 constexpr double kLoadBytes = 40e6;
 constexpr double kSplitOverhead = 0.5;
 static double plan_cost(const SegPlan &p, long long units, int nchunks, int num_sms, int R) {
@@ -1615,8 +1618,7 @@ static double plan_cost(const SegPlan &p, long long units, int nchunks, int num_
     }
     if (p.ppu == 1) return readout;
     const long long nstate = units * plan_state_blocks(p);
-    const double state = nstate <= num_sms ? p.fs * kState1
-                                           : (double)((nstate + 2LL * num_sms - 1) / (2LL * num_sms)) * p.fs * kState2;
+    const double state = (double)((nstate + num_sms - 1) / num_sms) * p.fs * kState1;
     long long loads = 0;  // block end states read by all later pieces
     for (int pc = 1; pc < p.ppu; ++pc) loads += p.q0 + (long long)(pc - 1) * p.q;
     const double load = (double)units * loads * (R + MP) * 128 * sizeof(float) / kLoadBytes;

@@ -30,11 +30,11 @@ struct DecodeArgs {
     unsigned *err;
 };
 
-// Error codes written to the device error word (first writer wins).
 // Largest workspace the prefill asks for (ida_forward_workspace_bytes): sequences are split
 // only as finely as the state slots of that many bytes allow.
 constexpr size_t kPreferredWorkspace = size_t(64) << 20;
 
+// Error codes written to the device error word (first writer wins).
 enum : unsigned {
     kErrNone = 0,
     kErrWaitTimeout = 1,

@@ -241,3 +241,26 @@ def test_chunk_paths_per_head(rd, split):
     for h in range(H):
         assert rel_l2(got[:, :, h], ref["out"][:, :, h]) <= BF16_REL_L2, (h, rel_l2(got[:, :, h], ref["out"][:, :, h]))
     assert rel_l2(unpadded_state(to_np(fs), d, R, M, W), ref["final_state"]) <= BF16_REL_L2
+
+
+@pytest.mark.parametrize("name", ["prefill_125m_bf16", "prefill_1p3b_bf16"])
+def test_split_prefill_is_deterministic(name):
+    """The split path (block state pass, then pieces that compose their start states) gives
+    the same bytes on every call, with the workspace left dirty by the previous call and by
+    calls that do not split in between."""
+    w = configs.ALL[name]
+    dev = torch.device("cuda")
+    pd = binding.params_to_device(inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed))
+    q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed, device=dev)
+    ws = binding.forward_workspace(q, v, pd)
+    assert ws is not None
+    outs = []
+    for r in range(6):
+        o, _ = binding.ida_forward(q, k, v, pd, workspace=ws if r % 2 == 0 else None)
+        outs.append(o.clone())
+    torch.cuda.synchronize()
+    assert binding.ida_device_error() == 0
+    for r in (2, 4):
+        assert torch.equal(outs[0], outs[r]), f"split call {r} differs from the first"
+    for r in (3, 5):
+        assert torch.equal(outs[1], outs[r]), f"whole call {r} differs from the first"
