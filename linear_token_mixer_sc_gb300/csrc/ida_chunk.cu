@@ -397,32 +397,47 @@ __global__ void __launch_bounds__(NTH, 1)
             // by Horner over the block end states ([R+128 columns][128 lanes] floats, columns as
             // in TMEM); U columns pair Re / Im across lanes 2m, 2m+1, Gamma^T columns across
             // columns R+2m, R+2m+1.  By column half.
+            // The loads of one block state are issued together (the groups' values land in
+            // registers, so one memory latency per block); the running sum lives in TMEM.
+            constexpr int NG = (R + MP) / 32;  // my 16-column groups: columns 32 g + 16 hsel
             const float *xs = seg_start + (size_t)unit * plan_state_blocks(plan) * (size_t)(R + MP) * 128;
             const float2 gu = gblk[mm];
             const float gus = is_im ? gu.y : -gu.y;  // own(g z) = z_own Re g + z_partner s Im g
-            for (int c0 = hsel * 16; c0 < R + MP; c0 += 32) {
-                float z[16];
+            for (int j = 0; j < (j0 > 0 ? j0 : 1); ++j) {
+                float x[NG][16];
     #pragma unroll
-                for (int i = 0; i < 16; ++i) z[i] = 0.f;
-                for (int j = 0; j < j0; ++j) {
-                    const float *x = xs + (size_t)j * (R + MP) * 128 + (size_t)c0 * 128 + tl;
-                    if (c0 < R) {
+                for (int g = 0; g < NG; ++g) {
+                    const float *xg = xs + (size_t)j * (R + MP) * 128 + (size_t)(32 * g + 16 * hsel) * 128 + tl;
     #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float zp = __shfl_xor_sync(0xffffffffu, z[i], 1);
-                            z[i] = fmaf(z[i], gu.x, fmaf(zp, gus, x[(size_t)i * 128]));
-                        }
-                    } else {
+                    for (int i = 0; i < 16; ++i) x[g][i] = j0 > 0 ? xg[(size_t)i * 128] : 0.f;
+                }
+                if (j > 0) {
     #pragma unroll
-                        for (int i = 0; i < 16; i += 2) {
-                            const float2 g = gblk[(c0 - R + i) >> 1];
-                            const float zr = z[i], zi = z[i + 1];
-                            z[i] = fmaf(g.x, zr, fmaf(-g.y, zi, x[(size_t)i * 128]));
-                            z[i + 1] = fmaf(g.x, zi, fmaf(g.y, zr, x[(size_t)(i + 1) * 128]));
+                    for (int g = 0; g < NG; ++g) {
+                        const int c0 = 32 * g + 16 * hsel;
+                        float z[16];
+                        tmem_ld16(tb + lane_base + c0, z);
+                        tmem_wait_ld();
+                        if (c0 < R) {
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float zp = __shfl_xor_sync(0xffffffffu, z[i], 1);
+                                x[g][i] = fmaf(z[i], gu.x, fmaf(zp, gus, x[g][i]));
+                            }
+                        } else {
+    #pragma unroll
+                            for (int i = 0; i < 16; i += 2) {
+                                const float2 gg = gblk[(c0 - R + i) >> 1];
+                                const float zr = z[i], zi = z[i + 1];
+                                x[g][i] = fmaf(gg.x, zr, fmaf(-gg.y, zi, x[g][i]));
+                                x[g][i + 1] = fmaf(gg.x, zi, fmaf(gg.y, zr, x[g][i + 1]));
+                            }
                         }
                     }
                 }
-                tmem_st16(tb + lane_base + c0, z);
+    #pragma unroll
+                for (int g = 0; g < NG; ++g) tmem_st16(tb + lane_base + 32 * g + 16 * hsel, x[g]);
+                tmem_wait_st();
             }
             if (hsel == 0) {
                 // conv taps of channels 8*(tl % (R/8)) .. +7, right-aligned: column 32*which + 4*e + jj
@@ -1585,44 +1600,38 @@ static size_t plan_workspace_bytes(const SegPlan &p, long long units, int R) {
     return (size_t)units * (size_t)plan_state_blocks(p) * (size_t)(R + MP) * 128 * sizeof(float);
 }
 
-// Modelled time of a plan in readout chunk times (a readout chunk takes 7 to 10 us): the
-// readout's makespan (pieces dealt in grid order to the SMs, one CTA each) and, when
-// sequences are split, the readout CTAs' loads of the block end states they compose (about
-// kLoadBytes per readout chunk time), the block state pass before it (waves of one CTA per
-// SM, fs chunks per CTA, about kState1 of a readout chunk per chunk) and the extra launch.
-constexpr double kState1 = 0.4;
-constexpr double kLoadBytes = 40e6;
-constexpr double kSplitOverhead = 0.5;
+// Modelled time of a plan in microseconds, fitted to GB300 timings of the 125M-, 1.3B- and
+// 14K-like workloads under forced plans: the readout's makespan (pieces dealt in grid order
+// to the SMs, one CTA each) at kChunkUs per chunk, and, when sequences are split, the block
+// state pass (waves of one CTA per SM, each kStateWaveUs plus kStateChunk readout chunks
+// per chunk), the start-state loads (kLoadUs per block state a piece composes) and the
+// extra launch and set-up (kSplitUs).
+constexpr double kStateWaveUs = 4.9, kStateChunk = 0.22, kLoadUs = 0.7, kSplitUs = 13.0;
+static double chunk_us(int R) { return R > 64 ? 8.9 : 7.4; }
 static double plan_cost(const SegPlan &p, long long units, int nchunks, int num_sms, int R) {
-    double readout;
-    if (p.ppu == 1) {
-        readout = (double)((units + num_sms - 1) / num_sms) * nchunks;
-    } else {
-        // later pieces (the last one may be short) first, then the first pieces
-        std::vector<double> free_at((size_t)num_sms, 0.0);
-        std::priority_queue<double, std::vector<double>, std::greater<double>> sms(free_at.begin(), free_at.end());
-        double makespan = 0.0;
-        auto deal = [&](double len) {
-            const double t = sms.top() + len;
-            sms.pop();
-            sms.push(t);
-            makespan = std::max(makespan, t);
-        };
-        for (long long u = 0; u < units; ++u)
-            for (int pc = 1; pc < p.ppu; ++pc) {
-                const int j0 = p.q0 + (pc - 1) * p.q, j1 = std::min(p.nb, j0 + p.q);
-                deal((double)(std::min(nchunks, j1 * p.fs) - j0 * p.fs));
-            }
-        for (long long u = 0; u < units; ++u) deal((double)std::min(nchunks, p.q0 * p.fs));
-        readout = makespan;
-    }
-    if (p.ppu == 1) return readout;
+    const double tc = chunk_us(R);
+    if (p.ppu == 1) return (double)((units + num_sms - 1) / num_sms) * nchunks * tc;
+    // later pieces (the last one may be short) first, then the first pieces
+    std::vector<double> free_at((size_t)num_sms, 0.0);
+    std::priority_queue<double, std::vector<double>, std::greater<double>> sms(free_at.begin(), free_at.end());
+    double makespan = 0.0;
+    auto deal = [&](double len) {
+        const double t = sms.top() + len;
+        sms.pop();
+        sms.push(t);
+        makespan = std::max(makespan, t);
+    };
+    for (long long u = 0; u < units; ++u)
+        for (int pc = 1; pc < p.ppu; ++pc) {
+            const int j0 = p.q0 + (pc - 1) * p.q, j1 = std::min(p.nb, j0 + p.q);
+            deal((double)(std::min(nchunks, j1 * p.fs) - j0 * p.fs));
+        }
+    for (long long u = 0; u < units; ++u) deal((double)std::min(nchunks, p.q0 * p.fs));
     const long long nstate = units * plan_state_blocks(p);
-    const double state = (double)((nstate + num_sms - 1) / num_sms) * p.fs * kState1;
-    long long loads = 0;  // block end states read by all later pieces
-    for (int pc = 1; pc < p.ppu; ++pc) loads += p.q0 + (long long)(pc - 1) * p.q;
-    const double load = (double)units * loads * (R + MP) * 128 * sizeof(float) / kLoadBytes;
-    return readout + load + state + kSplitOverhead;
+    const long long waves = (nstate + num_sms - 1) / num_sms;
+    const double state = (double)waves * (kStateWaveUs + p.fs * kStateChunk * tc);
+    const double load = plan_state_blocks(p) * kLoadUs * (R + MP) / 192.0;
+    return makespan * tc + state + load + kSplitUs;
 }
 
 // The cheapest plan whose workspace fits `budget` bytes, among equal pieces (up to one wave
