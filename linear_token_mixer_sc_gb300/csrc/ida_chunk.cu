@@ -94,7 +94,8 @@ struct ChunkSmem {
     static constexpr int RAWK = RAWQ + RAWQ_BYTES;               // [67][R] bf16
     static constexpr int RAWV = RAWK + RAWQ_BYTES;               // [64][D] bf16
     static_assert(YA16 % 1024 == 0 && RAWV + CH * D * 2 <= MISC, "raw staging must fit over YA16/AP32");
-    static_assert(XQ32 % 1024 == 0 && CH * D * 2 <= CH * R * 4, "the [64][D] output tile is staged over XQ32");
+    static_assert(GP16 % 128 == 0 && A216 == GP16 + CH * CH * 2 && CH * D * 2 <= 2 * CH * CH * 2,
+                  "the [64][D] output tile is staged over GP16 / A216");
     static constexpr int BARS = MISC;                            // 8 mbarriers
     static constexpr int TSLOT = BARS + 64;
     static constexpr int OSC = TSLOT + 16;                       // [64] float: row scales of A2
@@ -494,7 +495,6 @@ __global__ void __launch_bounds__(NTH, 1)
             // CF16, are waited for inside the prologue, just before ZT16 is rewritten)
             ok = mbar_wait(&bar[5], par);
             if (ok) tma_pending = 0;
-            if (tid == 0) bulk_wait_read_all();  // the previous output tile has left XQ32
             tc_fence_after();
             if (__syncthreads_or(!ok)) break;
 
@@ -725,6 +725,7 @@ __global__ void __launch_bounds__(NTH, 1)
             }
             __syncwarp();
             ok = mbar_wait(&bar[0], par);
+            if (tid == 0) bulk_wait_read_all();  // the previous output tile has left GP16 / A216
             tc_fence_after();
             if (__syncthreads_or(!ok)) break;
 
@@ -1032,10 +1033,11 @@ __global__ void __launch_bounds__(NTH, 1)
                 }
             }
             {
-                // outputs o[i][jv] into the [64][D] bf16 store tile over XQ32 (free until the next
-                // prologue; thread 0 waits for the tile's bulk store before that prologue starts)
+                // outputs o[i][jv] into the [64][D] bf16 store tile over GP16 / A216 (dead from
+                // here to the next chunk's masked Gram; thread 0 waits for the tile's bulk store
+                // just before that)
                 const int jv = tl;
-                __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + S::XQ32);
+                __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + S::GP16);
     #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c0 = 32 * hsel + 16 * cc;
@@ -1108,8 +1110,8 @@ __global__ void __launch_bounds__(NTH, 1)
             // ---- S10: U += Coef . Kt ; Gamma^T += Vt^T . Coef^T -----------------------------------
             if (tid == 0) {
                 // the chunk's output rows; rows past N are clipped by the copy (thread 0 owns the
-                // bulk group it waits on before the next prologue)
-                tma_store_4d(&tm_o, 0, h, t0, b, sm + S::XQ32);
+                // bulk group it waits on before the next masked Gram)
+                tma_store_4d(&tm_o, 0, h, t0, b, sm + S::GP16);
                 bulk_commit();
             }
             if (warp == 0 && elect_one()) {
