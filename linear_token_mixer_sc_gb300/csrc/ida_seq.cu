@@ -316,10 +316,16 @@ static ida_status launch_seq_t(const PrefillArgs &a, cudaStream_t st, int num_sm
     return IDA_OK;
 }
 
-// Chooses the cluster size: the smallest G whose per-CTA state fits in shared
-// memory, then doubled while the grid stays within one wave of SMs.
+bool launch_seq_modes(const PrefillArgs &a, cudaStream_t st, int num_sms, ida_status &s, std::string &why);
+
+// fp32 inputs: this kernel in fp64.  bf16 inputs: the register-resident kernel of
+// ida_seq_modes.cu where it takes the shape, else this kernel in fp32.  The cluster size
+// here is the smallest G whose per-CTA state fits in shared memory, then doubled while
+// the grid stays within one wave of SMs.
 ida_status launch_seq_prefill(const PrefillArgs &a, cudaStream_t st, int num_sms, std::string &why) {
     if (a.dtype == IDA_F32) return launch_seq_t<double>(a, st, num_sms, why);
+    ida_status s;
+    if (launch_seq_modes(a, st, num_sms, s, why)) return s;
     return launch_seq_t<float>(a, st, num_sms, why);
 }
 

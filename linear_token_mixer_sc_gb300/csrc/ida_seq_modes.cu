@@ -1,0 +1,554 @@
+// ida_seq_modes.cu -- token-sequential prefill for bf16 inputs with the state in registers.
+//
+// The recurrence X_t = lambda X_{t-1} + B z_t and the readouts o_t = Re(a_t Gamma_t) and
+// o_t = Re(a_t Gamma_t) / Re(a_t eta_t), a_t = xi(q_t) U_t^T, of "Interdomain Attention:
+// Beyond Token-Level Key-Value Memory" (German technical summary, "Skalierbare
+// Implementierung" for the recurrent core, "Theoretische Herleitung" for the ratio form),
+// walked one position at a time in fp32 on the CUDA cores.  This is the path of the eta
+// readout for bf16 inputs (whose denominator can cancel far below the rounding of the
+// tensor-core operands) and of bf16 shapes the chunked kernel does not take.
+//
+// Arithmetic in the scaled state Y = X / B (per mode).  Since B is constant over time,
+// Y_t = lambda Y_{t-1} + z_t, so an update costs four fp32 operations per complex element
+// instead of six; with alpha_t[m] = xi(q_t) . Y^U_t[m] and beta = B^2 alpha,
+//   o_t = Re sum_m beta_t[m] Y^Gamma_t[m],   den_t = Re sum_m beta_t[m] e_t[m],
+// where e_t = lambda e_{t-1} + 1 (eta = B e).  The final state is written as X = B Y.
+// A mode with B = 0 keeps X = 0 and contributes nothing, as in the unscaled recurrence.
+//
+// Work split: the modes of a unit are split over a cluster of G CTAs and, inside a CTA,
+// over NWC compute warps.  A compute warp owns MPW modes; its lanes form 32/LG groups of
+// LG = R/4 lanes, each group owns 4 modes, and a lane owns 4 consecutive key columns and
+// 4 consecutive value columns (d = R) of those 4 modes: 64 fp32 state registers per lane.
+// a_t needs a sum over the key columns, done per position by a reduce-scatter plus
+// all-gather over the LG lanes of the group (17 shuffles at R = 128).
+//
+// Positions are processed in tiles of TT.  Three helper warps per CTA run beside the
+// compute warps: two compute the feature prologue (conv, SiLU feature map, RMSNorm) of
+// the CTA's share of the next tile and store it into the shared memory of every CTA of
+// the cluster; one sums the per-warp partial readouts of the previous tile over the
+// cluster (fixed order, so the result does not depend on scheduling), divides by the
+// denominator for the eta readout and writes the outputs.  One cluster barrier per tile
+// orders all of it; inputs and partials are double-buffered.
+#include <cooperative_groups.h>
+
+#include <string>
+
+#include "ida_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace ida {
+
+namespace {
+
+constexpr int SM_TT = 16;    // positions per tile
+constexpr int SM_NPRO = 2;   // prologue warps per CTA
+constexpr int SM_HELP = 3;   // helper warps per CTA (prologue + output)
+constexpr int SM_MAXW = 4 + SM_HELP;
+constexpr unsigned FULL = 0xffffffffu;
+
+struct ModesLayout {
+    int nwc;       // compute warps per CTA
+    size_t xq;     // [2][TT][R]       xi(q) of the tile
+    size_t zb;     // [2][TT][2R]      [kt ; vt] of the tile
+    size_t op;     // [2][nwc][TT][R]  per-warp partial outputs
+    size_t dp;     // [2][nwc][TT]     per-warp partial denominators
+    size_t bytes;
+};
+
+__host__ __device__ inline ModesLayout modes_layout(int R, int nwc) {
+    ModesLayout L;
+    L.nwc = nwc;
+    L.xq = 0;
+    L.zb = L.xq + (size_t)2 * SM_TT * R;
+    L.op = L.zb + (size_t)2 * SM_TT * 2 * R;
+    L.dp = L.op + (size_t)2 * nwc * SM_TT * R;
+    L.bytes = (L.dp + (size_t)2 * nwc * SM_TT) * sizeof(float);
+    return L;
+}
+
+// Sum of p[0..8) over the LG lanes of a group, returned to every lane of the group:
+// three halving exchanges leave each lane one eighth of the values summed over eight
+// lanes, butterflies finish the sum, and eight broadcasts gather the results.
+template <int LG>
+__device__ __forceinline__ void group_allreduce8(float (&p)[8], int lane) {
+    {
+        constexpr int o = LG / 2;
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float send = hi ? p[i] : p[i + 4];
+            const float keep = hi ? p[i + 4] : p[i];
+            p[i] = keep + __shfl_xor_sync(FULL, send, o);
+        }
+    }
+    {
+        constexpr int o = LG / 4;
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float send = hi ? p[i] : p[i + 2];
+            const float keep = hi ? p[i + 2] : p[i];
+            p[i] = keep + __shfl_xor_sync(FULL, send, o);
+        }
+    }
+    {
+        constexpr int o = LG / 8;
+        const bool hi = (lane & o) != 0;
+        const float send = hi ? p[0] : p[1];
+        const float keep = hi ? p[1] : p[0];
+        p[0] = keep + __shfl_xor_sync(FULL, send, o);
+    }
+#pragma unroll
+    for (int o = LG / 16; o > 0; o >>= 1) p[0] += __shfl_xor_sync(FULL, p[0], o);
+    const float s = p[0];
+    // value v sits in the lanes whose bits LG/2, LG/4, LG/8 spell v
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+        p[v] = __shfl_sync(FULL, s, ((v >> 2) & 1) * (LG / 2) + ((v >> 1) & 1) * (LG / 4) + (v & 1) * (LG / 8), LG);
+}
+
+template <int CPL>
+__device__ __forceinline__ void load_bf16_row(const __nv_bfloat16 *p, float (&x)[CPL]) {
+    if constexpr (CPL == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        x[0] = __uint_as_float(u.x << 16);
+        x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        x[2] = __uint_as_float(u.y << 16);
+        x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else if constexpr (CPL == 2) {
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+        x[0] = __uint_as_float(u << 16);
+        x[1] = __uint_as_float(u & 0xFFFF0000u);
+    } else {
+        x[0] = __bfloat162float(*p);
+    }
+}
+
+template <int CPL>
+__device__ __forceinline__ void store_f32(float *p, const float (&x)[CPL]) {
+    if constexpr (CPL == 4)
+        *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    else if constexpr (CPL == 2)
+        *reinterpret_cast<float2 *>(p) = make_float2(x[0], x[1]);
+    else
+        *p = x[0];
+}
+
+template <int CPL>
+__device__ __forceinline__ void load_f32(const float *p, float (&x)[CPL]) {
+    if constexpr (CPL == 4) {
+        const float4 u = *reinterpret_cast<const float4 *>(p);
+        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    } else if constexpr (CPL == 2) {
+        const float2 u = *reinterpret_cast<const float2 *>(p);
+        x[0] = u.x; x[1] = u.y;
+    } else {
+        x[0] = *p;
+    }
+}
+
+template <int CPL>
+__device__ __forceinline__ void store_bf16_row(__nv_bfloat16 *p, const float (&x)[CPL]) {
+    if constexpr (CPL == 4) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t *>(&a);
+        u.y = *reinterpret_cast<const uint32_t *>(&b);
+        *reinterpret_cast<uint2 *>(p) = u;
+    } else if constexpr (CPL == 2) {
+        *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(x[0], x[1]);
+    } else {
+        *p = __float2bfloat16_rn(x[0]);
+    }
+}
+
+}  // namespace
+
+// R = d in {32, 64, 128}, bf16 inputs.  Block: nwc compute warps, then SM_NPRO prologue
+// warps, then the output warp.
+template <int R, bool ETA>
+__global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs a, int G, int nwc) {
+    constexpr int LG = R / 4;      // lanes per mode group
+    constexpr int GPW = 32 / LG;   // mode groups per warp
+    constexpr int MPW = 4 * GPW;   // modes per compute warp
+    constexpr int CPL = R / 32;    // channels per lane in the prologue and output warps
+    constexpr int TT = SM_TT;
+    extern __shared__ __align__(16) float smf[];
+    cg::cluster_group cluster = cg::this_cluster();
+    const ModesLayout L = modes_layout(R, nwc);
+    float *xq = smf + L.xq, *zb = smf + L.zb, *op = smf + L.op, *dp = smf + L.dp;
+
+    const int rank = G > 1 ? (int)cluster.block_rank() : 0;
+    const int unit = blockIdx.x / G;
+    const int H = a.H, N = a.N, M = a.M, W = a.W;
+    const int b = unit / H, h = unit % H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nt = (N + TT - 1) / TT;
+    const int PT = (TT + G - 1) / G;  // positions of a tile whose prologue and output this CTA runs
+    const size_t row_qk = (size_t)H * R;  // elements between consecutive positions (d = R)
+    const size_t base = ((size_t)b * N * H + h) * R;
+    const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q) + base;
+    const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k) + base;
+    const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v) + base;
+
+    auto csync = [&]() {
+        if (G > 1)
+            cluster.sync();
+        else
+            __syncthreads();
+    };
+
+    // ---- prologue warps: features of the CTA's share of tile kk into every CTA's buffer kk & 1
+    const int pw = warp - nwc;
+    float cwq[CPL][4], cwk[CPL][4], nwk[CPL], bsk[CPL], nwv[CPL], bsv[CPL];
+    if (pw >= 0 && pw < SM_NPRO) {
+        const float *cq = a.conv_w + ((size_t)h * R + CPL * lane) * W;
+        const float *ck = a.conv_w + ((size_t)(H + h) * R + CPL * lane) * W;
+        const float *nw = a.norm_w + (size_t)h * 2 * R, *bs = a.bias + (size_t)h * 2 * R;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // right-aligned: tap j sits at window row 4 - W + j
+                cwq[i][j] = j >= 4 - W ? cq[i * W + j - (4 - W)] : 0.f;
+                cwk[i][j] = j >= 4 - W ? ck[i * W + j - (4 - W)] : 0.f;
+            }
+            nwk[i] = nw[CPL * lane + i];
+            bsk[i] = bs[CPL * lane + i];
+            nwv[i] = nw[R + CPL * lane + i];
+            bsv[i] = bs[R + CPL * lane + i];
+        }
+    }
+    auto prologue = [&](int kk) {
+        // this warp's part of the CTA's positions [rank PT, rank PT + PT) of the tile
+        const int pper = (PT + SM_NPRO - 1) / SM_NPRO;
+        const int l0 = min(TT, rank * PT + pw * pper);
+        const int l1 = min(TT, min(rank * PT + PT, rank * PT + pw * pper + pper));
+        const int lo = kk * TT + l0, hi = min(N, kk * TT + l1);
+        if (lo >= hi) return;
+        // window rows t-3 .. t of raw q and k (zero before position 0)
+        float wq[4][CPL], wk[4][CPL];
+#pragma unroll
+        for (int r = 1; r < 4; ++r) {
+            const int p = lo - 4 + r;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) wq[r][i] = wk[r][i] = 0.f;
+            if (p >= 0) {
+                load_bf16_row<CPL>(qg + (size_t)p * row_qk + CPL * lane, wq[r]);
+                load_bf16_row<CPL>(kg + (size_t)p * row_qk + CPL * lane, wk[r]);
+            }
+        }
+        for (int t = lo; t < hi; ++t) {
+#pragma unroll
+            for (int r = 0; r < 3; ++r)
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) {
+                    wq[r][i] = wq[r + 1][i];
+                    wk[r][i] = wk[r + 1][i];
+                }
+            float vv[CPL];
+            load_bf16_row<CPL>(qg + (size_t)t * row_qk + CPL * lane, wq[3]);
+            load_bf16_row<CPL>(kg + (size_t)t * row_qk + CPL * lane, wk[3]);
+            load_bf16_row<CPL>(vg + (size_t)t * row_qk + CPL * lane, vv);
+            // causal conv over window rows t-3 .. t (the taps before the first are zero)
+            float fq[CPL], fk[CPL], ssq = 0.f, ssk = 0.f, ssv = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                float sq = 0.f, sk = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    sq = fmaf(cwq[i][j], wq[j][i], sq);
+                    sk = fmaf(cwk[i][j], wk[j][i], sk);
+                }
+                fq[i] = silu(sq);
+                fk[i] = silu(sk);
+                ssq = fmaf(fq[i], fq[i], ssq);
+                ssk = fmaf(fk[i], fk[i], ssk);
+                ssv = fmaf(vv[i], vv[i], ssv);
+            }
+            const float iq = 1.f / (warp_sum(ssq) + (float)IDA_EPS_FEAT);
+            const float ik = 1.f / (warp_sum(ssk) + (float)IDA_EPS_FEAT);
+            float msk = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                fq[i] *= iq;
+                fk[i] *= ik;
+                msk = fmaf(fk[i], fk[i], msk);
+            }
+            const float rk = rsqrtf(warp_sum(msk) / R + (float)IDA_EPS_RMS);
+            const float rv = rsqrtf(warp_sum(ssv) / R + (float)IDA_EPS_RMS);
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                fk[i] = fmaf(fk[i] * rk, nwk[i], bsk[i]);
+                vv[i] = fmaf(vv[i] * rv, nwv[i], bsv[i]);
+            }
+            const int tt = t - kk * TT;
+            const size_t oq = (size_t)(kk & 1) * TT * R + (size_t)tt * R + CPL * lane;
+            const size_t oz = (size_t)(kk & 1) * TT * 2 * R + (size_t)tt * 2 * R + CPL * lane;
+            for (int r = 0; r < G; ++r) {
+                float *dq = G > 1 ? cluster.map_shared_rank(xq, r) : xq;
+                float *dz = G > 1 ? cluster.map_shared_rank(zb, r) : zb;
+                store_f32<CPL>(dq + oq, fq);
+                store_f32<CPL>(dz + oz, fk);
+                store_f32<CPL>(dz + oz + R, vv);
+            }
+        }
+    };
+
+    // ---- output warp: sum the partials of tile kk over the cluster, in a fixed order
+    auto output = [&](int kk) {
+        const int lo = kk * TT + min(TT, rank * PT);
+        const int hi = min(N, kk * TT + min(TT, rank * PT + PT));
+        const int nsl = G * nwc;
+        for (int t = lo; t < hi; ++t) {
+            const int tt = t - kk * TT;
+            float o[CPL];
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) o[i] = 0.f;
+            float dn = 0.f;
+            for (int s0 = 0; s0 < nsl; s0 += 8) {
+                float part[8][CPL], dpart[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int s = s0 + u;
+#pragma unroll
+                    for (int i = 0; i < CPL; ++i) part[u][i] = 0.f;
+                    dpart[u] = 0.f;
+                    if (s < nsl) {
+                        const int r = s / nwc, w = s % nwc;
+                        const float *src = G > 1 ? cluster.map_shared_rank(op, r) : op;
+                        const float *srd = G > 1 ? cluster.map_shared_rank(dp, r) : dp;
+                        load_f32<CPL>(src + (((size_t)(kk & 1) * nwc + w) * TT + tt) * R + CPL * lane, part[u]);
+                        if (ETA) dpart[u] = srd[((size_t)(kk & 1) * nwc + w) * TT + tt];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+#pragma unroll
+                    for (int i = 0; i < CPL; ++i) o[i] += part[u][i];
+                    dn += dpart[u];
+                }
+            }
+            if (ETA) {
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) o[i] = o[i] / dn;
+            }
+            store_bf16_row<CPL>(reinterpret_cast<__nv_bfloat16 *>(a.out) + base + (size_t)t * row_qk + CPL * lane, o);
+        }
+    };
+
+    // ---- compute warps: the state of MPW modes in registers
+    const int g = lane / LG, gl = lane % LG;
+    const int mbase = (rank * nwc + warp) * MPW + 4 * g;
+    float ur[4][4], ui[4][4], gr[4][4], gi[4][4];
+    float lr[4], li[4], b2r[4], b2i[4], er[4], ei[4];
+    if (warp < nwc) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int m = mbase + j;
+            float2 lam = make_float2(0.f, 0.f), bb = make_float2(0.f, 0.f);
+            if (m < M) {
+                lam = *reinterpret_cast<const float2 *>(a.lambda + ((size_t)h * M + m) * 2);
+                bb = *reinterpret_cast<const float2 *>(a.Bvec + ((size_t)h * M + m) * 2);
+            }
+            lr[j] = lam.x;
+            li[j] = lam.y;
+            b2r[j] = bb.x * bb.x - bb.y * bb.y;
+            b2i[j] = 2.f * bb.x * bb.y;
+            er[j] = ei[j] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ur[j][i] = ui[j][i] = gr[j][i] = gi[j][i] = 0.f;
+        }
+    }
+    auto compute = [&](int kk) {
+        const int tn = min(TT, N - kk * TT);
+        const float *xqb = xq + (size_t)(kk & 1) * TT * R + 4 * gl;
+        const float *zbb = zb + (size_t)(kk & 1) * TT * 2 * R + 4 * gl;
+        float *opb = op + ((size_t)(kk & 1) * nwc + warp) * TT * R + 4 * gl;
+        float *dpb = dp + ((size_t)(kk & 1) * nwc + warp) * TT;
+        for (int tt = 0; tt < tn; ++tt) {
+            const float4 x4 = *reinterpret_cast<const float4 *>(xqb + (size_t)tt * R);
+            const float4 k4 = *reinterpret_cast<const float4 *>(zbb + (size_t)tt * 2 * R);
+            const float4 v4 = *reinterpret_cast<const float4 *>(zbb + (size_t)tt * 2 * R + R);
+            const float x[4] = {x4.x, x4.y, x4.z, x4.w};
+            const float zk[4] = {k4.x, k4.y, k4.z, k4.w};
+            const float zv[4] = {v4.x, v4.y, v4.z, v4.w};
+            float p[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float sr = 0.f, si = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float nr = fmaf(lr[j], ur[j][i], fmaf(-li[j], ui[j][i], zk[i]));
+                    const float ni = fmaf(lr[j], ui[j][i], li[j] * ur[j][i]);
+                    ur[j][i] = nr;
+                    ui[j][i] = ni;
+                    sr = fmaf(x[i], nr, sr);
+                    si = fmaf(x[i], ni, si);
+                }
+                p[2 * j] = sr;
+                p[2 * j + 1] = si;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float nr = fmaf(lr[j], gr[j][i], fmaf(-li[j], gi[j][i], zv[i]));
+                    const float ni = fmaf(lr[j], gi[j][i], li[j] * gr[j][i]);
+                    gr[j][i] = nr;
+                    gi[j][i] = ni;
+                }
+                const float nr = fmaf(lr[j], er[j], fmaf(-li[j], ei[j], 1.f));
+                const float ni = fmaf(lr[j], ei[j], li[j] * er[j]);
+                er[j] = nr;
+                ei[j] = ni;
+            }
+            group_allreduce8<LG>(p, lane);
+            float o[4] = {0.f, 0.f, 0.f, 0.f}, dn = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float br = fmaf(b2r[j], p[2 * j], -b2i[j] * p[2 * j + 1]);
+                const float bi = fmaf(b2r[j], p[2 * j + 1], b2i[j] * p[2 * j]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[i] = fmaf(br, gr[j][i], fmaf(-bi, gi[j][i], o[i]));
+                if (ETA) dn = fmaf(br, er[j], fmaf(-bi, ei[j], dn));
+            }
+#pragma unroll
+            for (int off = LG; off < 32; off <<= 1) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[i] += __shfl_xor_sync(FULL, o[i], off);
+                if (ETA) dn += __shfl_xor_sync(FULL, dn, off);
+            }
+            if (lane < LG) *reinterpret_cast<float4 *>(opb + (size_t)tt * R) = make_float4(o[0], o[1], o[2], o[3]);
+            if (ETA && lane == 0) dpb[tt] = dn;
+        }
+    };
+
+    // Each role runs its own loop (so that no role's registers stay live in another's);
+    // all of them pass the same nt + 2 barriers.
+    if (warp < nwc) {
+        csync();
+        for (int kk = 0; kk <= nt; ++kk) {
+            if (kk < nt) compute(kk);
+            csync();
+        }
+    } else if (pw < SM_NPRO) {
+        prologue(0);
+        csync();
+        for (int kk = 0; kk <= nt; ++kk) {
+            if (kk + 1 < nt) prologue(kk + 1);
+            csync();
+        }
+    } else {
+        csync();
+        for (int kk = 0; kk <= nt; ++kk) {
+            if (kk >= 1) output(kk - 1);
+            csync();
+        }
+    }
+
+    // ---- final state: X = B Y and eta = B e for this warp's modes; rank 0 adds the conv tails
+    if (a.final_state) {
+        float *fs = a.final_state + (size_t)unit * a.state_floats;
+        const size_t RD = 2 * (size_t)R, plane = (size_t)M * RD;
+        if (warp < nwc) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int m = mbase + j;
+                if (m >= M) continue;
+                const float2 bb = *reinterpret_cast<const float2 *>(a.Bvec + ((size_t)h * M + m) * 2);
+                float xr[4], xi[4], yr[4], yi[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    xr[i] = bb.x * ur[j][i] - bb.y * ui[j][i];
+                    xi[i] = bb.x * ui[j][i] + bb.y * ur[j][i];
+                    yr[i] = bb.x * gr[j][i] - bb.y * gi[j][i];
+                    yi[i] = bb.x * gi[j][i] + bb.y * gr[j][i];
+                }
+                float *rr = fs + (size_t)m * RD + 4 * gl, *ri = fs + plane + (size_t)m * RD + 4 * gl;
+                *reinterpret_cast<float4 *>(rr) = make_float4(xr[0], xr[1], xr[2], xr[3]);
+                *reinterpret_cast<float4 *>(ri) = make_float4(xi[0], xi[1], xi[2], xi[3]);
+                *reinterpret_cast<float4 *>(rr + R) = make_float4(yr[0], yr[1], yr[2], yr[3]);
+                *reinterpret_cast<float4 *>(ri + R) = make_float4(yi[0], yi[1], yi[2], yi[3]);
+                if (gl == 0) {
+                    fs[2 * plane + m] = bb.x * er[j] - bb.y * ei[j];
+                    fs[2 * plane + M + m] = bb.x * ei[j] + bb.y * er[j];
+                }
+            }
+        } else if (warp == nwc + SM_NPRO && rank == 0) {
+            float *tq = fs + 2 * plane + 2 * M;
+            float *tk = tq + (size_t)(W - 1) * R;
+            for (int i = lane; i < (W - 1) * R; i += 32) {
+                const int r = i / R, c = i % R, p = N - (W - 1) + r;
+                tq[i] = p >= 0 ? __bfloat162float(qg[(size_t)p * row_qk + c]) : 0.f;
+                tk[i] = p >= 0 ? __bfloat162float(kg[(size_t)p * row_qk + c]) : 0.f;
+            }
+            const size_t used = 2 * plane + 2 * (size_t)M + 2 * (size_t)(W - 1) * R;
+            for (size_t i = used + lane; i < a.state_floats; i += 32) fs[i] = 0.f;
+        }
+    }
+}
+
+namespace {
+
+template <int R, bool ETA>
+cudaError_t launch_modes_t(const PrefillArgs &a, int G, int nwc, cudaStream_t st) {
+    auto kern = seq_modes_kernel<R, ETA>;
+    const size_t smem = modes_layout(R, nwc).bytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)G * (unsigned)(a.B * a.H), 1, 1);
+    cfg.blockDim = dim3((unsigned)(nwc + SM_HELP) * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, G, nwc);
+}
+
+template <int R>
+cudaError_t launch_modes_r(const PrefillArgs &a, int G, int nwc, cudaStream_t st) {
+    return (a.flags & IDA_READOUT_ETA) ? launch_modes_t<R, true>(a, G, nwc, st)
+                                       : launch_modes_t<R, false>(a, G, nwc, st);
+}
+
+}  // namespace
+
+// Takes bf16 inputs with R = d in {32, 64, 128} and M <= 8 * 4 * (modes per warp).  Picks
+// the compute warps per CTA (4, else 2 or 1 when the grid would not fill the SMs) and the
+// cluster size G (a power of two) covering the modes.  Returns false (nothing launched)
+// for other shapes.
+bool launch_seq_modes(const PrefillArgs &a, cudaStream_t st, int num_sms, ida_status &s, std::string &why) {
+    if (a.dtype != IDA_BF16 || a.R != a.d || (a.R != 32 && a.R != 64 && a.R != 128) || a.W > 4) return false;
+    const int mpw = 4 * (32 / (a.R / 4));
+    const int wpu = (a.M + mpw - 1) / mpw;  // compute warps per unit
+    const long units = (long)a.B * a.H;
+    int nwc = 4;
+    while (nwc > 1 && units * ((wpu + nwc - 1) / nwc) < num_sms && (wpu + nwc / 2 - 1) / (nwc / 2) <= 8) nwc /= 2;
+    int G = 1;  // a power of two; CTAs past the last mode carry only inert modes
+    while (G * nwc < wpu) G *= 2;
+    if (G > 8) return false;
+    if (units * G > 0x7fffffffL) return false;
+    cudaError_t e;
+    if (a.R == 32)
+        e = launch_modes_r<32>(a, G, nwc, st);
+    else if (a.R == 64)
+        e = launch_modes_r<64>(a, G, nwc, st);
+    else
+        e = launch_modes_r<128>(a, G, nwc, st);
+    if (e != cudaSuccess) {
+        s = IDA_ERR_CUDA;
+        why = std::string("sequential prefill launch: ") + cudaGetErrorString(e);
+    } else {
+        s = IDA_OK;
+    }
+    return true;
+}
+
+}  // namespace ida
