@@ -22,13 +22,16 @@
 // a_t needs a sum over the key columns, done per position by a reduce-scatter plus
 // all-gather over the LG lanes of the group (17 shuffles at R = 128).
 //
-// Positions are processed in tiles of TT.  Three helper warps per CTA run beside the
-// compute warps: two compute the feature prologue (conv, SiLU feature map, RMSNorm) of
-// the CTA's share of the next tile and store it into the shared memory of every CTA of
-// the cluster; one sums the per-warp partial readouts of the previous tile over the
-// cluster (fixed order, so the result does not depend on scheduling), divides by the
-// denominator for the eta readout and writes the outputs.  One cluster barrier per tile
-// orders all of it; inputs and partials are double-buffered.
+// Positions are processed in tiles of TT; CTA r of the cluster owns positions
+// [r PT, r PT + PT) of every tile, split between its two helper warps, which run beside
+// the compute warps.  A helper warp computes the feature prologue (conv, SiLU feature
+// map, RMSNorm) of its positions of the next tile and stores it into the shared memory of
+// every CTA of the cluster; then it sums the partial readouts of its positions of the
+// previous tile, which every compute warp of the cluster has stored into this CTA's
+// shared memory (in a fixed order, so the result does not depend on scheduling), divides
+// by the denominator for the eta readout and writes the outputs.  All traffic between
+// CTAs is stores; one cluster barrier per tile orders it, and inputs and partials are
+// double-buffered.
 #include <cooperative_groups.h>
 
 #include <string>
@@ -42,28 +45,31 @@ namespace ida {
 namespace {
 
 constexpr int SM_TT = 16;    // positions per tile
-constexpr int SM_NPRO = 2;   // prologue warps per CTA
-constexpr int SM_HELP = 3;   // helper warps per CTA (prologue + output)
+constexpr int SM_HELP = 2;   // helper warps per CTA (prologue and output)
 constexpr int SM_MAXW = 4 + SM_HELP;
 constexpr unsigned FULL = 0xffffffffu;
 
+// Shared memory of one CTA, in floats.  S = G * nwc compute warps of the cluster each
+// store their partial readout of a position into the CTA that writes that position's
+// output (CTA r writes positions [r PT, r PT + PT) of every tile).
 struct ModesLayout {
-    int nwc;       // compute warps per CTA
-    size_t xq;     // [2][TT][R]       xi(q) of the tile
-    size_t zb;     // [2][TT][2R]      [kt ; vt] of the tile
-    size_t op;     // [2][nwc][TT][R]  per-warp partial outputs
-    size_t dp;     // [2][nwc][TT]     per-warp partial denominators
+    size_t xq;     // [2][TT][R]        xi(q) of the tile
+    size_t zb;     // [2][TT][2R]       [kt ; vt] of the tile
+    size_t op;     // [2][S][PT][R]     partial outputs of this CTA's positions, per warp
+    size_t dp;     // [2][S][PT]        partial denominators, per warp
     size_t bytes;
 };
 
-__host__ __device__ inline ModesLayout modes_layout(int R, int nwc) {
+__host__ __device__ inline int modes_pt(int G) { return (SM_TT + G - 1) / G; }
+
+__host__ __device__ inline ModesLayout modes_layout(int R, int nwc, int G) {
+    const size_t S = (size_t)G * nwc, PT = modes_pt(G);
     ModesLayout L;
-    L.nwc = nwc;
     L.xq = 0;
     L.zb = L.xq + (size_t)2 * SM_TT * R;
     L.op = L.zb + (size_t)2 * SM_TT * 2 * R;
-    L.dp = L.op + (size_t)2 * nwc * SM_TT * R;
-    L.bytes = (L.dp + (size_t)2 * nwc * SM_TT) * sizeof(float);
+    L.dp = L.op + 2 * S * PT * R;
+    L.bytes = (L.dp + 2 * S * PT) * sizeof(float);
     return L;
 }
 
@@ -108,6 +114,55 @@ __device__ __forceinline__ void group_allreduce8(float (&p)[8], int lane) {
         p[v] = __shfl_sync(FULL, s, ((v >> 2) & 1) * (LG / 2) + ((v >> 1) & 1) * (LG / 4) + (v & 1) * (LG / 8), LG);
 }
 
+typedef unsigned long long f2_t;  // two fp32 in one 64-bit register
+
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f2_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+    f2_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+    f2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// 32-bit shared-memory addresses: this CTA's, the same offset in CTA r of the cluster,
+// and stores through them (a CTA's own shared::cta address is valid in the cluster window)
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t a, uint32_t r) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(r));
+    return d;
+}
+__device__ __forceinline__ void st_cluster(uint32_t a, float x) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(x) : "memory");
+}
+__device__ __forceinline__ void st_cluster(uint32_t a, float x, float y) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
+}
+__device__ __forceinline__ void st_cluster(uint32_t a, float x, float y, float z, float w) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w)
+                 : "memory");
+}
+template <int CPL>
+__device__ __forceinline__ void st_cluster_row(uint32_t a, const float (&x)[CPL]) {
+    if constexpr (CPL == 4)
+        st_cluster(a, x[0], x[1], x[2], x[3]);
+    else if constexpr (CPL == 2)
+        st_cluster(a, x[0], x[1]);
+    else
+        st_cluster(a, x[0]);
+}
+
 template <int CPL>
 __device__ __forceinline__ void load_bf16_row(const __nv_bfloat16 *p, float (&x)[CPL]) {
     if constexpr (CPL == 4) {
@@ -123,16 +178,6 @@ __device__ __forceinline__ void load_bf16_row(const __nv_bfloat16 *p, float (&x)
     } else {
         x[0] = __bfloat162float(*p);
     }
-}
-
-template <int CPL>
-__device__ __forceinline__ void store_f32(float *p, const float (&x)[CPL]) {
-    if constexpr (CPL == 4)
-        *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
-    else if constexpr (CPL == 2)
-        *reinterpret_cast<float2 *>(p) = make_float2(x[0], x[1]);
-    else
-        *p = x[0];
 }
 
 template <int CPL>
@@ -165,8 +210,7 @@ __device__ __forceinline__ void store_bf16_row(__nv_bfloat16 *p, const float (&x
 
 }  // namespace
 
-// R = d in {32, 64, 128}, bf16 inputs.  Block: nwc compute warps, then SM_NPRO prologue
-// warps, then the output warp.
+// R = d in {32, 64, 128}, bf16 inputs.  Block: nwc compute warps, then SM_HELP helper warps.
 template <int R, bool ETA>
 __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs a, int G, int nwc) {
     constexpr int LG = R / 4;      // lanes per mode group
@@ -176,7 +220,7 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
     constexpr int TT = SM_TT;
     extern __shared__ __align__(16) float smf[];
     cg::cluster_group cluster = cg::this_cluster();
-    const ModesLayout L = modes_layout(R, nwc);
+    const ModesLayout L = modes_layout(R, nwc, G);
     float *xq = smf + L.xq, *zb = smf + L.zb, *op = smf + L.op, *dp = smf + L.dp;
 
     const int rank = G > 1 ? (int)cluster.block_rank() : 0;
@@ -185,7 +229,8 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
     const int b = unit / H, h = unit % H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nt = (N + TT - 1) / TT;
-    const int PT = (TT + G - 1) / G;  // positions of a tile whose prologue and output this CTA runs
+    const int PT = modes_pt(G);  // positions of a tile whose prologue and output this CTA runs
+    const int S = G * nwc;       // partial-readout slices per position
     const size_t row_qk = (size_t)H * R;  // elements between consecutive positions (d = R)
     const size_t base = ((size_t)b * N * H + h) * R;
     const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q) + base;
@@ -199,10 +244,13 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
             __syncthreads();
     };
 
-    // ---- prologue warps: features of the CTA's share of tile kk into every CTA's buffer kk & 1
+    // ---- helper warps: this warp's positions of a tile are [hlo, hhi) (tile-local)
     const int pw = warp - nwc;
+    const int hper = (PT + SM_HELP - 1) / SM_HELP;
+    const int hlo = min(TT, rank * PT + pw * hper);
+    const int hhi = min(TT, min(rank * PT + PT, rank * PT + pw * hper + hper));
     float cwq[CPL][4], cwk[CPL][4], nwk[CPL], bsk[CPL], nwv[CPL], bsv[CPL];
-    if (pw >= 0 && pw < SM_NPRO) {
+    if (pw >= 0) {
         const float *cq = a.conv_w + ((size_t)h * R + CPL * lane) * W;
         const float *ck = a.conv_w + ((size_t)(H + h) * R + CPL * lane) * W;
         const float *nw = a.norm_w + (size_t)h * 2 * R, *bs = a.bias + (size_t)h * 2 * R;
@@ -219,15 +267,13 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
             bsv[i] = bs[R + CPL * lane + i];
         }
     }
+    // features of tile kk into every CTA's buffer kk & 1
     auto prologue = [&](int kk) {
-        // this warp's part of the CTA's positions [rank PT, rank PT + PT) of the tile
-        const int pper = (PT + SM_NPRO - 1) / SM_NPRO;
-        const int l0 = min(TT, rank * PT + pw * pper);
-        const int l1 = min(TT, min(rank * PT + PT, rank * PT + pw * pper + pper));
-        const int lo = kk * TT + l0, hi = min(N, kk * TT + l1);
+        const int lo = kk * TT + hlo, hi = min(N, kk * TT + hhi);
         if (lo >= hi) return;
-        // window rows t-3 .. t of raw q and k (zero before position 0)
-        float wq[4][CPL], wk[4][CPL];
+        // window rows t-3 .. t of raw q and k (zero before position 0); the rows of the next
+        // position are loaded one position ahead
+        float wq[4][CPL], wk[4][CPL], nq[CPL], nk[CPL], nv[CPL];
 #pragma unroll
         for (int r = 1; r < 4; ++r) {
             const int p = lo - 4 + r;
@@ -238,18 +284,27 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
                 load_bf16_row<CPL>(kg + (size_t)p * row_qk + CPL * lane, wk[r]);
             }
         }
+        load_bf16_row<CPL>(qg + (size_t)lo * row_qk + CPL * lane, nq);
+        load_bf16_row<CPL>(kg + (size_t)lo * row_qk + CPL * lane, nk);
+        load_bf16_row<CPL>(vg + (size_t)lo * row_qk + CPL * lane, nv);
         for (int t = lo; t < hi; ++t) {
+            float vv[CPL];
 #pragma unroll
-            for (int r = 0; r < 3; ++r)
+            for (int i = 0; i < CPL; ++i) {
 #pragma unroll
-                for (int i = 0; i < CPL; ++i) {
+                for (int r = 0; r < 3; ++r) {
                     wq[r][i] = wq[r + 1][i];
                     wk[r][i] = wk[r + 1][i];
                 }
-            float vv[CPL];
-            load_bf16_row<CPL>(qg + (size_t)t * row_qk + CPL * lane, wq[3]);
-            load_bf16_row<CPL>(kg + (size_t)t * row_qk + CPL * lane, wk[3]);
-            load_bf16_row<CPL>(vg + (size_t)t * row_qk + CPL * lane, vv);
+                wq[3][i] = nq[i];
+                wk[3][i] = nk[i];
+                vv[i] = nv[i];
+            }
+            if (t + 1 < hi) {
+                load_bf16_row<CPL>(qg + (size_t)(t + 1) * row_qk + CPL * lane, nq);
+                load_bf16_row<CPL>(kg + (size_t)(t + 1) * row_qk + CPL * lane, nk);
+                load_bf16_row<CPL>(vg + (size_t)(t + 1) * row_qk + CPL * lane, nv);
+            }
             // causal conv over window rows t-3 .. t (the taps before the first are zero)
             float fq[CPL], fk[CPL], ssq = 0.f, ssk = 0.f, ssv = 0.f;
 #pragma unroll
@@ -283,43 +338,39 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
                 vv[i] = fmaf(vv[i] * rv, nwv[i], bsv[i]);
             }
             const int tt = t - kk * TT;
-            const size_t oq = (size_t)(kk & 1) * TT * R + (size_t)tt * R + CPL * lane;
-            const size_t oz = (size_t)(kk & 1) * TT * 2 * R + (size_t)tt * 2 * R + CPL * lane;
+            const uint32_t aq = smem_u32(xq + (size_t)(kk & 1) * TT * R + (size_t)tt * R + CPL * lane);
+            const uint32_t az = smem_u32(zb + (size_t)(kk & 1) * TT * 2 * R + (size_t)tt * 2 * R + CPL * lane);
             for (int r = 0; r < G; ++r) {
-                float *dq = G > 1 ? cluster.map_shared_rank(xq, r) : xq;
-                float *dz = G > 1 ? cluster.map_shared_rank(zb, r) : zb;
-                store_f32<CPL>(dq + oq, fq);
-                store_f32<CPL>(dz + oz, fk);
-                store_f32<CPL>(dz + oz + R, vv);
+                const uint32_t dq = G > 1 ? mapa_u32(aq, r) : aq, dz = G > 1 ? mapa_u32(az, r) : az;
+                st_cluster_row<CPL>(dq, fq);
+                st_cluster_row<CPL>(dz, fk);
+                st_cluster_row<CPL>(dz + 4 * R, vv);
             }
         }
     };
 
-    // ---- output warp: sum the partials of tile kk over the cluster, in a fixed order
+    // outputs of tile kk: the S partials of each position (all in this CTA's shared
+    // memory), summed in a fixed order
     auto output = [&](int kk) {
-        const int lo = kk * TT + min(TT, rank * PT);
-        const int hi = min(N, kk * TT + min(TT, rank * PT + PT));
-        const int nsl = G * nwc;
+        const int lo = kk * TT + hlo, hi = min(N, kk * TT + hhi);
         for (int t = lo; t < hi; ++t) {
-            const int tt = t - kk * TT;
+            const int pl = t - kk * TT - rank * PT;
+            const float *src = op + ((size_t)(kk & 1) * S * PT + pl) * R + CPL * lane;
+            const float *srd = dp + (size_t)(kk & 1) * S * PT + pl;
             float o[CPL];
 #pragma unroll
             for (int i = 0; i < CPL; ++i) o[i] = 0.f;
             float dn = 0.f;
-            for (int s0 = 0; s0 < nsl; s0 += 8) {
+            for (int s0 = 0; s0 < S; s0 += 8) {
                 float part[8][CPL], dpart[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const int s = s0 + u;
 #pragma unroll
                     for (int i = 0; i < CPL; ++i) part[u][i] = 0.f;
                     dpart[u] = 0.f;
-                    if (s < nsl) {
-                        const int r = s / nwc, w = s % nwc;
-                        const float *src = G > 1 ? cluster.map_shared_rank(op, r) : op;
-                        const float *srd = G > 1 ? cluster.map_shared_rank(dp, r) : dp;
-                        load_f32<CPL>(src + (((size_t)(kk & 1) * nwc + w) * TT + tt) * R + CPL * lane, part[u]);
-                        if (ETA) dpart[u] = srd[((size_t)(kk & 1) * nwc + w) * TT + tt];
+                    if (s0 + u < S) {
+                        load_f32<CPL>(src + (size_t)(s0 + u) * PT * R, part[u]);
+                        if (ETA) dpart[u] = srd[(size_t)(s0 + u) * PT];
                     }
                 }
 #pragma unroll
@@ -340,8 +391,9 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
     // ---- compute warps: the state of MPW modes in registers
     const int g = lane / LG, gl = lane % LG;
     const int mbase = (rank * nwc + warp) * MPW + 4 * g;
-    float ur[4][4], ui[4][4], gr[4][4], gi[4][4];
-    float lr[4], li[4], b2r[4], b2i[4], er[4], ei[4];
+    f2_t ur[4][2], ui[4][2], gr[4][2], gi[4][2];
+    f2_t lr2[4], li2[4], nli2[4];
+    float b2r[4], b2i[4], er[4], ei[4];
     if (warp < nwc) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -351,76 +403,96 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
                 lam = *reinterpret_cast<const float2 *>(a.lambda + ((size_t)h * M + m) * 2);
                 bb = *reinterpret_cast<const float2 *>(a.Bvec + ((size_t)h * M + m) * 2);
             }
-            lr[j] = lam.x;
-            li[j] = lam.y;
             b2r[j] = bb.x * bb.x - bb.y * bb.y;
             b2i[j] = 2.f * bb.x * bb.y;
             er[j] = ei[j] = 0.f;
+            lr2[j] = f2_pack(lam.x, lam.x);
+            li2[j] = f2_pack(lam.y, lam.y);
+            nli2[j] = f2_pack(-lam.y, -lam.y);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) ur[j][i] = ui[j][i] = gr[j][i] = gi[j][i] = 0.f;
+            for (int i = 0; i < 2; ++i) ur[j][i] = ui[j][i] = gr[j][i] = gi[j][i] = 0ull;
         }
     }
     auto compute = [&](int kk) {
         const int tn = min(TT, N - kk * TT);
-        const float *xqb = xq + (size_t)(kk & 1) * TT * R + 4 * gl;
-        const float *zbb = zb + (size_t)(kk & 1) * TT * 2 * R + 4 * gl;
-        float *opb = op + ((size_t)(kk & 1) * nwc + warp) * TT * R + 4 * gl;
-        float *dpb = dp + ((size_t)(kk & 1) * nwc + warp) * TT;
-        for (int tt = 0; tt < tn; ++tt) {
-            const float4 x4 = *reinterpret_cast<const float4 *>(xqb + (size_t)tt * R);
-            const float4 k4 = *reinterpret_cast<const float4 *>(zbb + (size_t)tt * 2 * R);
-            const float4 v4 = *reinterpret_cast<const float4 *>(zbb + (size_t)tt * 2 * R + R);
-            const float x[4] = {x4.x, x4.y, x4.z, x4.w};
-            const float zk[4] = {k4.x, k4.y, k4.z, k4.w};
-            const float zv[4] = {v4.x, v4.y, v4.z, v4.w};
+        const float *xp = xq + (size_t)(kk & 1) * TT * R + 4 * gl;
+        const float *zp = zb + (size_t)(kk & 1) * TT * 2 * R + 4 * gl;
+        const uint32_t slice = (uint32_t)((kk & 1) * S + rank * nwc + warp);  // this warp's slice
+        const uint32_t ao = smem_u32(op + (size_t)slice * PT * R + 4 * gl), ad = smem_u32(dp + (size_t)slice * PT);
+        // uo, ud: where this position's partials go, in the CTA that writes its output
+        auto step = [&](uint32_t uo, uint32_t ud) {
+            const ulonglong2 x4 = *reinterpret_cast<const ulonglong2 *>(xp);
+            const ulonglong2 k4 = *reinterpret_cast<const ulonglong2 *>(zp);
+            const ulonglong2 v4 = *reinterpret_cast<const ulonglong2 *>(zp + R);
+            const f2_t x[2] = {x4.x, x4.y}, zk[2] = {k4.x, k4.y}, zv[2] = {v4.x, v4.y};
             float p[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float sr = 0.f, si = 0.f;
+                f2_t sr = 0ull, si = 0ull;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float nr = fmaf(lr[j], ur[j][i], fmaf(-li[j], ui[j][i], zk[i]));
-                    const float ni = fmaf(lr[j], ui[j][i], li[j] * ur[j][i]);
-                    ur[j][i] = nr;
-                    ui[j][i] = ni;
-                    sr = fmaf(x[i], nr, sr);
-                    si = fmaf(x[i], ni, si);
+                for (int i = 0; i < 2; ++i) {
+                    const f2_t t1 = f2_mul(li2[j], ur[j][i]);
+                    const f2_t t2 = f2_fma(nli2[j], ui[j][i], zk[i]);
+                    ui[j][i] = f2_fma(lr2[j], ui[j][i], t1);
+                    ur[j][i] = f2_fma(lr2[j], ur[j][i], t2);
+                    sr = i == 0 ? f2_mul(x[i], ur[j][i]) : f2_fma(x[i], ur[j][i], sr);
+                    si = i == 0 ? f2_mul(x[i], ui[j][i]) : f2_fma(x[i], ui[j][i], si);
                 }
-                p[2 * j] = sr;
-                p[2 * j + 1] = si;
+                float a0, a1, b0, b1;
+                f2_unpack(sr, a0, a1);
+                f2_unpack(si, b0, b1);
+                p[2 * j] = a0 + a1;
+                p[2 * j + 1] = b0 + b1;
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float nr = fmaf(lr[j], gr[j][i], fmaf(-li[j], gi[j][i], zv[i]));
-                    const float ni = fmaf(lr[j], gi[j][i], li[j] * gr[j][i]);
-                    gr[j][i] = nr;
-                    gi[j][i] = ni;
+                for (int i = 0; i < 2; ++i) {
+                    const f2_t t1 = f2_mul(li2[j], gr[j][i]);
+                    const f2_t t2 = f2_fma(nli2[j], gi[j][i], zv[i]);
+                    gi[j][i] = f2_fma(lr2[j], gi[j][i], t1);
+                    gr[j][i] = f2_fma(lr2[j], gr[j][i], t2);
                 }
-                const float nr = fmaf(lr[j], er[j], fmaf(-li[j], ei[j], 1.f));
-                const float ni = fmaf(lr[j], ei[j], li[j] * er[j]);
-                er[j] = nr;
-                ei[j] = ni;
+                float lrj, lrh, lij, lih;
+                f2_unpack(lr2[j], lrj, lrh);
+                f2_unpack(li2[j], lij, lih);
+                const float t1 = lij * er[j];
+                const float t2 = fmaf(-lij, ei[j], 1.f);
+                ei[j] = fmaf(lrj, ei[j], t1);
+                er[j] = fmaf(lrj, er[j], t2);
             }
             group_allreduce8<LG>(p, lane);
-            float o[4] = {0.f, 0.f, 0.f, 0.f}, dn = 0.f;
+            f2_t o2[2] = {0ull, 0ull};
+            float dn = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float br = fmaf(b2r[j], p[2 * j], -b2i[j] * p[2 * j + 1]);
-                const float bi = fmaf(b2r[j], p[2 * j + 1], b2i[j] * p[2 * j]);
+                const float nbi = fmaf(-b2r[j], p[2 * j + 1], -b2i[j] * p[2 * j]);  // -Im beta
+                const f2_t br2 = f2_pack(br, br), nbi2 = f2_pack(nbi, nbi);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) o[i] = fmaf(br, gr[j][i], fmaf(-bi, gi[j][i], o[i]));
-                if (ETA) dn = fmaf(br, er[j], fmaf(-bi, ei[j], dn));
+                for (int i = 0; i < 2; ++i) o2[i] = f2_fma(br2, gr[j][i], f2_fma(nbi2, gi[j][i], o2[i]));
+                if (ETA) dn = fmaf(br, er[j], fmaf(nbi, ei[j], dn));
             }
+            float o[4];
+            f2_unpack(o2[0], o[0], o[1]);
+            f2_unpack(o2[1], o[2], o[3]);
 #pragma unroll
             for (int off = LG; off < 32; off <<= 1) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) o[i] += __shfl_xor_sync(FULL, o[i], off);
                 if (ETA) dn += __shfl_xor_sync(FULL, dn, off);
             }
-            if (lane < LG) *reinterpret_cast<float4 *>(opb + (size_t)tt * R) = make_float4(o[0], o[1], o[2], o[3]);
-            if (ETA && lane == 0) dpb[tt] = dn;
+            if (LG == 32 || lane < LG) st_cluster(uo, o[0], o[1], o[2], o[3]);
+            if (ETA && lane == 0) st_cluster(ud, dn);
+            xp += R;
+            zp += 2 * R;
+        };
+        // positions [ow PT, ow PT + PT) of the tile are written by CTA ow: their partials are
+        // asynchronous stores into its shared memory
+        for (int ow = 0; ow * PT < tn; ++ow) {
+            uint32_t uo = G > 1 ? mapa_u32(ao, ow) : ao, ud = G > 1 ? mapa_u32(ad, ow) : ad;
+            const int te = min(tn, ow * PT + PT);
+            for (int tt = ow * PT; tt < te; ++tt, uo += 4 * R, ud += 4) step(uo, ud);
         }
     };
 
@@ -432,16 +504,11 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
             if (kk < nt) compute(kk);
             csync();
         }
-    } else if (pw < SM_NPRO) {
+    } else {
         prologue(0);
         csync();
         for (int kk = 0; kk <= nt; ++kk) {
             if (kk + 1 < nt) prologue(kk + 1);
-            csync();
-        }
-    } else {
-        csync();
-        for (int kk = 0; kk <= nt; ++kk) {
             if (kk >= 1) output(kk - 1);
             csync();
         }
@@ -460,10 +527,17 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
                 float xr[4], xi[4], yr[4], yi[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    xr[i] = bb.x * ur[j][i] - bb.y * ui[j][i];
-                    xi[i] = bb.x * ui[j][i] + bb.y * ur[j][i];
-                    yr[i] = bb.x * gr[j][i] - bb.y * gi[j][i];
-                    yi[i] = bb.x * gi[j][i] + bb.y * gr[j][i];
+                    float a0, a1, b0, b1, c0, c1, d0, d1;
+                    f2_unpack(ur[j][i / 2], a0, a1);
+                    f2_unpack(ui[j][i / 2], b0, b1);
+                    f2_unpack(gr[j][i / 2], c0, c1);
+                    f2_unpack(gi[j][i / 2], d0, d1);
+                    const float yu_r = i & 1 ? a1 : a0, yu_i = i & 1 ? b1 : b0;
+                    const float yg_r = i & 1 ? c1 : c0, yg_i = i & 1 ? d1 : d0;
+                    xr[i] = bb.x * yu_r - bb.y * yu_i;
+                    xi[i] = bb.x * yu_i + bb.y * yu_r;
+                    yr[i] = bb.x * yg_r - bb.y * yg_i;
+                    yi[i] = bb.x * yg_i + bb.y * yg_r;
                 }
                 float *rr = fs + (size_t)m * RD + 4 * gl, *ri = fs + plane + (size_t)m * RD + 4 * gl;
                 *reinterpret_cast<float4 *>(rr) = make_float4(xr[0], xr[1], xr[2], xr[3]);
@@ -475,7 +549,7 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
                     fs[2 * plane + M + m] = bb.x * ei[j] + bb.y * er[j];
                 }
             }
-        } else if (warp == nwc + SM_NPRO && rank == 0) {
+        } else if (pw == 0 && rank == 0) {
             float *tq = fs + 2 * plane + 2 * M;
             float *tk = tq + (size_t)(W - 1) * R;
             for (int i = lane; i < (W - 1) * R; i += 32) {
@@ -494,7 +568,7 @@ namespace {
 template <int R, bool ETA>
 cudaError_t launch_modes_t(const PrefillArgs &a, int G, int nwc, cudaStream_t st) {
     auto kern = seq_modes_kernel<R, ETA>;
-    const size_t smem = modes_layout(R, nwc).bytes;
+    const size_t smem = modes_layout(R, nwc, G).bytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
