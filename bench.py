@@ -41,10 +41,12 @@ METRIC = "mixer tokens/s (prefill & decode) at 1 GB300; % of roofline (HBM/TC)"
 L2_BYTES = 126 * 1024 * 1024
 FLUSH_BYTES = 512 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# Nominal GB300 unit counts for the FP32 CUDA-core peak (decode arithmetic):
-# 152 SMs x 128 FP32 lanes x 2 flops (FMA) x 2.07 GHz max SM clock.
+# Nominal GB300 unit counts for the FP32 CUDA-core peak (the bound of the eta readout, which
+# computes in fp32 on the CUDA cores): 152 SMs x 128 FP32 lanes x 2 flops (FMA) x 2.07 GHz
+# maximum SM clock.
 FP32_TFLOPS_NOMINAL = 152 * 128 * 2 * 2.07e9 / 1e12
 PREFILL_SOURCES = ["ida_chunk.cu", "ida_seq.cu", "ida_common.cuh", "tc_sm103.cuh", "ida_api.cu"]
+ETA_SOURCES = ["ida_seq_modes.cu", "ida_seq.cu", "ida_common.cuh", "ida_api.cu"]
 DECODE_SOURCES = ["ida_decode.cu", "ida_common.cuh", "ida_api.cu"]
 
 
@@ -290,6 +292,12 @@ def roofline(runner, ms_avg, peaks, peak_kind, traffic, kernel_bound=None):
     t_b = alg_b / (peaks["hbm_gbs"] * 1e9)
     t_f = fl / (peaks["bf16_tflops"] * 1e12)
     bound = kernel_bound or ("hbm" if t_b >= t_f else "tensor")
+    if bound == "alu":  # fp32 CUDA-core arithmetic (eta readout): algorithmic flops at the FMA peak
+        ach = fl / (ms_avg * 1e-3) / 1e12
+        return {"bound": "alu", "achieved": round(ach, 2), "peak": round(FP32_TFLOPS_NOMINAL, 1),
+                "unit": "TFLOP/s", "frac": round(ach / FP32_TFLOPS_NOMINAL, 4), "traffic": traffic,
+                "algorithmic_flops": fl,
+                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x 2.07 GHz (nominal unit counts)"}
     if bound == "hbm":
         ach = alg_b / (ms_avg * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -389,7 +397,9 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e
     value = job_value(ws, runner.tokens(), ms_all)
     res = {"value": value, "ms_per_step": ms_all, "tokens_per_step": runner.tokens(),
            "flush_l2": flush, "wall_s": wall,
-           "roofline": roofline(runner, ms, peaks, peak_kind, traffic_record(w.name, sources)),
+           "roofline": roofline(runner, ms, peaks, peak_kind,
+                                traffic_record(w.name + (":eta" if flags & 1 else ""), sources),
+                                kernel_bound="alu" if flags & 1 else None),
            "gpu_launches": runner.launches_per_step * steps}
     if e2e:
         et = time_steps(runner, max(3, steps // 2), 2, dev, False, e2e=True)
@@ -461,7 +471,8 @@ def main():
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     main_res = measure(w, dev, args.steps, args.warmup, flags, dist, ws, peaks, peak_kind,
-                       DECODE_SOURCES if w.decode_steps else PREFILL_SOURCES, seed_len=args.seed_len)
+                       DECODE_SOURCES if w.decode_steps else (ETA_SOURCES if flags else PREFILL_SOURCES),
+                       seed_len=args.seed_len)
     clocks = sampler.stop()
     decode_res = None
     if not w.decode_steps and not args.no_decode:

@@ -13,7 +13,9 @@
 // coalesced accesses.  One CTA per (b,h) unit; each warp owns a strided set
 // of modes, lanes own 4-float column slices, the per-mode dot product is a
 // warp-shuffle reduction and the per-warp partial outputs are summed through
-// shared memory at the end.  Arithmetic is fp64 for fp32 inputs (see the
+// shared memory at the end.  lambda, B and eta of a warp's modes are read once,
+// one mode per lane, and broadcast by shuffles, so no mode waits on a load
+// issued after the previous mode's stores.  Arithmetic is fp64 for fp32 inputs (see the
 // sequential prefill for why) and fp32 for bf16 inputs; the state is stored
 // as fp32 either way.
 #include <string>
@@ -26,9 +28,10 @@ constexpr int DEC_WARPS = 4;
 constexpr int DEC_THREADS = DEC_WARPS * 32;
 constexpr int DEC_UNROLL = 2;  // modes in flight per warp
 
-// Features of one new position for one unit, one warp each (q, k, v).
-// Shifts the raw conv tails of q and k in the state.
-template <typename T>
+// Features of one new position for one unit, one warp each (q, k, v); a lane handles
+// channels lane + 32 i, i < 4 NV (R, d <= 128 NV).  Shifts the raw conv tails of q and k in
+// the state.
+template <int NV, typename T>
 __device__ __forceinline__ void decode_prologue(const DecodeArgs &a, int unit, int h, float *st,
                                                 T *xq_s, T *z_s, int warp, int lane) {
     const int R = a.R, d = a.d, W = a.W, H = a.H, M = a.M, RD = R + d;
@@ -39,10 +42,10 @@ __device__ __forceinline__ void decode_prologue(const DecodeArgs &a, int unit, i
         const void *x = which == 0 ? a.q : a.k;
         const float *cw = a.conv_w + ((size_t)which * H + h) * R * W;
         float *tail = st + 2 * (size_t)M * RD + 2 * M + (size_t)which * (W - 1) * R;
-        T f[8];
+        T f[4 * NV];
         T ss = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 4 * NV; ++i) {
             int c = lane + 32 * i;
             f[i] = 0;
             if (c < R) {
@@ -59,36 +62,36 @@ __device__ __forceinline__ void decode_prologue(const DecodeArgs &a, int unit, i
         T inv = T(1) / (warp_sum(ss) + (T)IDA_EPS_FEAT);
         if (which == 0) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 4 * NV; ++i) {
                 int c = lane + 32 * i;
                 if (c < R) xq_s[c] = f[i] * inv;
             }
         } else {
             T ms = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 4 * NV; ++i) {
                 f[i] *= inv;
                 ms = fma(f[i], f[i], ms);
             }
             T r = rsqrt_t(warp_sum(ms) / R + (T)IDA_EPS_RMS);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 4 * NV; ++i) {
                 int c = lane + 32 * i;
                 if (c < R) z_s[c] = fma(f[i] * r, (T)nw[c], (T)bs[c]);
             }
         }
     } else if (warp == 2) {
-        T vv[8];
+        T vv[4 * NV];
         T ms = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 4 * NV; ++i) {
             int j = lane + 32 * i;
             vv[i] = j < d ? (T)load_in(a.v, a.dtype, (size_t)unit * d + j) : T(0);
             ms = fma(vv[i], vv[i], ms);
         }
         T r = rsqrt_t(warp_sum(ms) / d + (T)IDA_EPS_RMS);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 4 * NV; ++i) {
             int j = lane + 32 * i;
             if (j < d) z_s[R + j] = fma(vv[i] * r, (T)nw[R + j], (T)bs[R + j]);
         }
@@ -137,19 +140,27 @@ __device__ __forceinline__ void load_group(ModeGroup<NV> &g, const float *st, in
     }
 }
 
+// lambda, B and eta of the warp's modes, one mode per lane: lane i holds mode warp + DEC_WARPS i
+// (at most 32 modes per warp since M <= 128)
+template <typename T>
+struct ModeRegs {
+    T lr, li, br, bi, er, ei;
+};
+
 // Update the group's modes, store them, accumulate the readout.
 template <int NV, typename T>
 __device__ __forceinline__ void step_group(const ModeGroup<NV> &g, float *st, int mb, const DecodeArgs &a,
-                                           int h, int RD, size_t plane, int lane, const T (&xq)[NV][4],
+                                           int warp, int RD, size_t plane, int lane, const T (&xq)[NV][4],
                                            const T (&zk)[NV][4], const T (&zv)[NV][4], T (&oacc)[NV][4],
-                                           T &dacc) {
+                                           T &dacc, ModeRegs<T> &mr) {
     const int M = a.M, R = a.R, d = a.d;
 #pragma unroll
     for (int u = 0; u < DEC_UNROLL; ++u) {
         const int m = mb + u * DEC_WARPS;
         if (m >= M) break;
-        const T lr = a.lambda[((size_t)h * M + m) * 2], li = a.lambda[((size_t)h * M + m) * 2 + 1];
-        const T br = a.Bvec[((size_t)h * M + m) * 2], bi = a.Bvec[((size_t)h * M + m) * 2 + 1];
+        const int mi = (m - warp) / DEC_WARPS;  // the lane holding this mode's parameters
+        const T lr = __shfl_sync(0xffffffffu, mr.lr, mi), li = __shfl_sync(0xffffffffu, mr.li, mi);
+        const T br = __shfl_sync(0xffffffffu, mr.br, mi), bi = __shfl_sync(0xffffffffu, mr.bi, mi);
         T ar = 0, ai = 0;
         T yr[NV][4], yi[NV][4];
 #pragma unroll
@@ -182,13 +193,12 @@ __device__ __forceinline__ void step_group(const ModeGroup<NV> &g, float *st, in
         for (int iv = 0; iv < NV; ++iv)
 #pragma unroll
             for (int e = 0; e < 4; ++e) oacc[iv][e] += ar * yr[iv][e] - ai * yi[iv][e];
-        T er = st[2 * plane + m], ei = st[2 * plane + M + m];
+        T er = __shfl_sync(0xffffffffu, mr.er, mi), ei = __shfl_sync(0xffffffffu, mr.ei, mi);
         cstep_t(er, ei, lr, li, br, bi, T(1));
         dacc += ar * er - ai * ei;
-        __syncwarp();
-        if (lane == 0) {
-            st[2 * plane + m] = (float)er;
-            st[2 * plane + M + m] = (float)ei;
+        if (lane == mi) {
+            mr.er = er;
+            mr.ei = ei;
         }
     }
 }
@@ -200,7 +210,7 @@ __device__ __forceinline__ void step_group(const ModeGroup<NV> &g, float *st, in
 // is loaded while the previous one is being updated, so that each warp keeps
 // its next loads in flight through the arithmetic.
 template <int NV, typename T>
-__global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(DEC_THREADS, 3) decode_kernel(DecodeArgs a) {
     __shared__ __align__(16) T xq_s[256];
     __shared__ __align__(16) T z_s[512];
     __shared__ __align__(16) T ored[DEC_WARPS][256];
@@ -215,8 +225,15 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(DecodeArgs a) {
 
     ModeGroup<NV> ga, gb;
     load_group(ga, st, warp, M, R, d, RD, plane, lane);
+    ModeRegs<T> mr = {T(0), T(0), T(0), T(0), T(0), T(0)};
+    const int mlane = warp + DEC_WARPS * lane;  // this lane's mode
+    if (mlane < M) {
+        const float2 lam = *reinterpret_cast<const float2 *>(a.lambda + ((size_t)h * M + mlane) * 2);
+        const float2 bb = *reinterpret_cast<const float2 *>(a.Bvec + ((size_t)h * M + mlane) * 2);
+        mr = {(T)lam.x, (T)lam.y, (T)bb.x, (T)bb.y, (T)st[2 * plane + mlane], (T)st[2 * plane + M + mlane]};
+    }
 
-    decode_prologue<T>(a, unit, h, st, xq_s, z_s, warp, lane);
+    decode_prologue<NV, T>(a, unit, h, st, xq_s, z_s, warp, lane);
     __syncthreads();
 
     // Per-lane slices of xi(q) and z, reused for every mode.
@@ -236,10 +253,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(DecodeArgs a) {
 
     for (int mb = warp; mb < M; mb += 2 * STRIDE) {
         if (mb + STRIDE < M) load_group(gb, st, mb + STRIDE, M, R, d, RD, plane, lane);
-        step_group<NV, T>(ga, st, mb, a, h, RD, plane, lane, xq, zk, zv, oacc, dacc);
+        step_group<NV, T>(ga, st, mb, a, warp, RD, plane, lane, xq, zk, zv, oacc, dacc, mr);
         if (mb + STRIDE >= M) break;
         if (mb + 2 * STRIDE < M) load_group(ga, st, mb + 2 * STRIDE, M, R, d, RD, plane, lane);
-        step_group<NV, T>(gb, st, mb + STRIDE, a, h, RD, plane, lane, xq, zk, zv, oacc, dacc);
+        step_group<NV, T>(gb, st, mb + STRIDE, a, warp, RD, plane, lane, xq, zk, zv, oacc, dacc, mr);
     }
 #pragma unroll
     for (int iv = 0; iv < NV; ++iv) {
@@ -249,6 +266,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(DecodeArgs a) {
             for (int e = 0; e < 4; ++e) ored[warp][c + e] = oacc[iv][e];
     }
     if (lane == 0) dred[warp] = dacc;
+    if (mlane < M) {
+        st[2 * plane + mlane] = (float)mr.er;
+        st[2 * plane + M + mlane] = (float)mr.ei;
+    }
     __syncthreads();
     const bool eta_ro = (a.flags & IDA_READOUT_ETA) != 0;
     T dn = 0;
