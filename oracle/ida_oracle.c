@@ -391,17 +391,20 @@ void orc_unit_forward_chunked(const double *xq, const double *kt,
  * Prefill over [B,N,H,*] inputs (q,k: [B,N,H,R], v: [B,N,H,d]) in fp32 or
  * bf16, parameters in fp32 as the device library takes them:
  * conv_w [2,H,R,W] (0 = q, 1 = k), norm_w/bias [H,R+d], lambda/Bvec [H,M,2].
+ * state_in: nullable [B,H][orc_state_doubles], the state before position 0
+ * (planar X, eta, and the raw conv tails, which stand for the inputs of
+ * positions -(W-1) .. -1); NULL is the zero state.
  * out: [B,N,H,d] float64.  final_state: nullable [B,H][orc_state_doubles].
  * den: nullable [B,N,H].  units: nullable list of unit ids (b*H+h) to
  * compute (others untouched); n_units ignored when units is NULL.
  * nthreads <= 0 uses the OpenMP default.  Returns 0.
  */
-int orc_forward(const void *q, const void *k, const void *v, int dtype,
-                const float *conv_w, const float *norm_w, const float *bias,
-                const float *lambda, const float *Bvec, double *out,
-                double *final_state, double *den, int B, int H, int N, int d,
-                int R, int M, int W, int flags, const int *units, int n_units,
-                int nthreads)
+int orc_forward_from(const void *q, const void *k, const void *v, int dtype,
+                     const float *conv_w, const float *norm_w, const float *bias,
+                     const float *lambda, const float *Bvec, const double *state_in,
+                     double *out, double *final_state, double *den, int B, int H,
+                     int N, int d, int R, int M, int W, int flags,
+                     const int *units, int n_units, int nthreads)
 {
     int total = units ? n_units : B * H;
     size_t SD = orc_state_doubles(d, R, M, W);
@@ -424,6 +427,11 @@ int orc_forward(const void *q, const void *k, const void *v, int dtype,
         double *lr = malloc((size_t)2 * M * sizeof(double));
         double *br = malloc((size_t)2 * M * sizeof(double));
         double *st = calloc(SD, sizeof(double));
+        const double *sin = state_in ? state_in + (size_t)id * SD : NULL;
+        const double *tin_q = sin ? sin + (size_t)2 * M * (RD + 1) : NULL;
+        const double *tin_k = sin ? tin_q + (size_t)(W - 1) * R : NULL;
+        if (sin)
+            memcpy(st, sin, (size_t)2 * M * (RD + 1) * sizeof(double));
         double *o = malloc(((size_t)N * d + 1) * sizeof(double));
         double *dn = malloc(((size_t)N + 1) * sizeof(double));
         for (int t = 0; t < N; ++t) {
@@ -450,7 +458,7 @@ int orc_forward(const void *q, const void *k, const void *v, int dtype,
             br[m] = Bvec[(size_t)h * 2 * M + m];
         }
         orc_unit_forward(qr, kr, vr, N, R, d, M, W, wq, wk, nw, bs, lr, br,
-                         flags, st, NULL, NULL, o, dn);
+                         flags, st, tin_q, tin_k, o, dn);
         for (int t = 0; t < N; ++t) {
             for (int j = 0; j < d; ++j)
                 out[(((size_t)b * N + t) * H + h) * d + j] = o[(size_t)t * d + j];
@@ -460,14 +468,23 @@ int orc_forward(const void *q, const void *k, const void *v, int dtype,
         if (final_state) {
             double *fs = final_state + (size_t)id * SD;
             memcpy(fs, st, (size_t)2 * M * (RD + 1) * sizeof(double));
-            /* conv tails: the raw inputs of the last W-1 positions, oldest first */
+            /* conv tails: the raw inputs of the last W-1 positions, oldest first
+             * (positions before 0 from the starting tails, or zero) */
             double *tq = fs + (size_t)2 * M * (RD + 1);
             double *tk = tq + (size_t)(W - 1) * R;
             for (int r = 0; r < W - 1; ++r) {
                 int p = N - (W - 1) + r;
                 for (int c = 0; c < R; ++c) {
-                    tq[(size_t)r * R + c] = p >= 0 ? qr[(size_t)p * R + c] : 0.0;
-                    tk[(size_t)r * R + c] = p >= 0 ? kr[(size_t)p * R + c] : 0.0;
+                    double xq0 = 0.0, xk0 = 0.0;
+                    if (p >= 0) {
+                        xq0 = qr[(size_t)p * R + c];
+                        xk0 = kr[(size_t)p * R + c];
+                    } else if (sin) {
+                        xq0 = tin_q[(size_t)(p + W - 1) * R + c];
+                        xk0 = tin_k[(size_t)(p + W - 1) * R + c];
+                    }
+                    tq[(size_t)r * R + c] = xq0;
+                    tk[(size_t)r * R + c] = xk0;
                 }
             }
         }
@@ -475,6 +492,19 @@ int orc_forward(const void *q, const void *k, const void *v, int dtype,
         free(lr); free(br); free(st); free(o); free(dn);
     }
     return 0;
+}
+
+/* Prefill from the zero state. */
+int orc_forward(const void *q, const void *k, const void *v, int dtype,
+                const float *conv_w, const float *norm_w, const float *bias,
+                const float *lambda, const float *Bvec, double *out,
+                double *final_state, double *den, int B, int H, int N, int d,
+                int R, int M, int W, int flags, const int *units, int n_units,
+                int nthreads)
+{
+    return orc_forward_from(q, k, v, dtype, conv_w, norm_w, bias, lambda, Bvec,
+                            NULL, out, final_state, den, B, H, N, d, R, M, W,
+                            flags, units, n_units, nthreads);
 }
 
 /*

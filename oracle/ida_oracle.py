@@ -72,6 +72,9 @@ def lib():
             L.orc_forward.restype = _i
             L.orc_forward.argtypes = [_vp, _vp, _vp, _i, _fp, _fp, _fp, _fp, _fp, _dp, _dp,
                                       _dp, _i, _i, _i, _i, _i, _i, _i, _i, _ip, _i, _i]
+            L.orc_forward_from.restype = _i
+            L.orc_forward_from.argtypes = [_vp, _vp, _vp, _i, _fp, _fp, _fp, _fp, _fp, _dp, _dp,
+                                           _dp, _dp, _i, _i, _i, _i, _i, _i, _i, _i, _ip, _i, _i]
             L.orc_decode_step.restype = _i
             L.orc_decode_step.argtypes = [_vp, _vp, _vp, _i, _fp, _fp, _fp, _fp, _fp, _dp,
                                           _dp, _dp, _i, _i, _i, _i, _i, _i, _i, _ip, _i, _i]
@@ -202,13 +205,15 @@ def unit_forward_chunked(xq, kt, vt, lam, Bv, C, flags=0, state=None):
 # ---- batched entry points on the library's own argument layout -----------
 
 def forward(q, k, v, params: dict, flags: int = 0, final_state: bool = False,
-            units=None, nthreads: int = 0, want_den: bool = False):
+            units=None, nthreads: int = 0, want_den: bool = False, state_in=None):
     """Prefill of [B,N,H,*] fp32/bf16 tensors (CPU) with fp32 parameters.
 
     params: conv_w [2,H,R,W], norm_w [H,R+d], bias [H,R+d], lambda [H,M,2],
-    Bvec [H,M,2].  Returns dict(out [B,N,H,d] float64, den [B,N,H] or None,
-    final_state [B,H,S] float64 or None).  With ``units`` (ids b*H+h) only
-    those units are computed; other entries stay NaN.
+    Bvec [H,M,2].  state_in: optional [B,H,S] state before position 0 (planar
+    X, eta, raw conv tails; S = state_doubles), zero when None.  Returns
+    dict(out [B,N,H,d] float64, den [B,N,H] or None, final_state [B,H,S]
+    float64 or None).  With ``units`` (ids b*H+h) only those units are
+    computed; other entries stay NaN.
     """
     qp, dt, qk = _raw(q)
     kp, dt2, kk = _raw(k)
@@ -224,10 +229,14 @@ def forward(q, k, v, params: dict, flags: int = 0, final_state: bool = False,
     S = state_doubles(d, R, M, W)
     fs = np.full((B, H, S), np.nan) if final_state else None
     uarr = None if units is None else np.ascontiguousarray(units, dtype=np.int32)
-    rc = lib().orc_forward(qp, kp, vp, dt, _ptr(conv_w, _fp), _ptr(norm_w, _fp), _ptr(bias, _fp),
-                           _ptr(lam, _fp), _ptr(Bv, _fp), _ptr(out), _ptr(fs), _ptr(den),
-                           B, H, N, d, R, M, W, int(flags), _ptr(uarr, _ip),
-                           0 if uarr is None else len(uarr), int(nthreads))
+    sin = None
+    if state_in is not None:
+        sin = _d(state_in)
+        assert sin.shape == (B, H, S), (sin.shape, (B, H, S))
+    rc = lib().orc_forward_from(qp, kp, vp, dt, _ptr(conv_w, _fp), _ptr(norm_w, _fp),
+                                _ptr(bias, _fp), _ptr(lam, _fp), _ptr(Bv, _fp), _ptr(sin),
+                                _ptr(out), _ptr(fs), _ptr(den), B, H, N, d, R, M, W, int(flags),
+                                _ptr(uarr, _ip), 0 if uarr is None else len(uarr), int(nthreads))
     assert rc == 0
     return {"out": out, "den": den, "final_state": fs}
 

@@ -30,6 +30,10 @@ MUTATIONS = [
     ("eta driven without B", "eta[m] = lam[m] * eta[m] + Bv[m];", "eta[m] = lam[m] * eta[m] + 1.0;"),
     ("query RMS-normed like the key", "    orc_feature_map(s, N, R, xq);\n",
      "    orc_feature_map(s, N, R, xq);\n    orc_rmsnorm_affine(xq, N, R, norm_w, bias, xq);\n"),
+    ("starting tails ignored", "flags, st, tin_q, tin_k, o, dn);", "flags, st, NULL, NULL, o, dn);"),
+    ("final tails not reaching into the starting tails", "} else if (sin) {", "} else if (0) {"),
+    ("starting eta ignored", "memcpy(st, sin, (size_t)2 * M * (RD + 1) * sizeof(double));",
+     "memcpy(st, sin, (size_t)2 * M * RD * sizeof(double));"),
 ]
 
 PIN_TESTS = [
@@ -42,6 +46,7 @@ PIN_TESTS = [
     pins.test_lambda_one_single_mode_is_cumulative_sums,
     pins.test_lambda_zero_is_memoryless,
     pins.test_eta_readout_returns_constant_values,
+    pins.test_prefill_from_state_one_position_is_decode_step,
 ]
 
 

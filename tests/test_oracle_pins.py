@@ -339,3 +339,36 @@ def test_short_prefill_tail_is_zero_padded():
     np.testing.assert_array_equal(tail_q[:, :, 0], 0.0)
     np.testing.assert_array_equal(tail_q[:, :, 1:], q.double().numpy().transpose(0, 2, 1, 3))
     assert S == 2 * M * (R + d) + 2 * M + 2 * 3 * R
+
+
+# ---- prefill from an initial state ------------------------------------------
+
+@pytest.mark.parametrize("N1,W", [(1, 4), (2, 4), (7, 4), (5, 2), (3, 1)])
+def test_prefill_from_state_equals_one_longer_prefill(N1, W):
+    """prefill(N1) then prefill(rest, state_in = its final state) == prefill(N):
+    the state, eta and raw conv tails carry everything the recurrence and the
+    causal conv need, so the outputs after N1 and the final state agree exactly.
+
+    Catches a starting state that is ignored, tails taken at the wrong offset or
+    in the wrong order, and final tails that do not reach back into the starting
+    tails when the second part is shorter than W-1."""
+    for N in (N1 + 1, N1 + 2, N1 + 9):
+        q, k, v, p = _small_problem(N=N, W=W)
+        full = orc.forward(q, k, v, p, flags=orc.READOUT_ETA, final_state=True)
+        a = orc.forward(q[:, :N1], k[:, :N1], v[:, :N1], p, flags=orc.READOUT_ETA, final_state=True)
+        b = orc.forward(q[:, N1:], k[:, N1:], v[:, N1:], p, flags=orc.READOUT_ETA, final_state=True,
+                        state_in=a["final_state"])
+        np.testing.assert_array_equal(b["out"], full["out"][:, N1:])
+        np.testing.assert_array_equal(b["final_state"], full["final_state"])
+
+
+def test_prefill_from_state_one_position_is_decode_step():
+    """A one-position prefill from a state equals one decode step from it (the
+    decode step is a separate code path: in-place state, tail shift)."""
+    q, k, v, p = _small_problem(N=6, W=4)
+    st = orc.forward(q[:, :5], k[:, :5], v[:, :5], p, final_state=True)["final_state"]
+    r = orc.forward(q[:, 5:], k[:, 5:], v[:, 5:], p, flags=orc.READOUT_ETA, final_state=True, state_in=st)
+    st2 = st.copy()
+    dec = orc.decode_step(q[:, 5], k[:, 5], v[:, 5], p, st2, flags=orc.READOUT_ETA)
+    np.testing.assert_allclose(r["out"][:, 0], dec["out"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(r["final_state"], st2, rtol=1e-12, atol=1e-14)
