@@ -133,6 +133,34 @@ IDA_API ida_status ida_forward_ws(const void *q, const void *k, const void *v,
                           size_t workspace_bytes, ida_stream_t stream);
 
 /*
+ * Prefill that continues from a given state: the recurrence starts from
+ * state_in instead of zero, and the causal conv of the first positions reads
+ * the raw q, k rows carried in its conv tails (the positions before 0).
+ * Chunked prefill and serving can resume a sequence this way.  The pages
+ * state the recurrence and the fixed-size state it carries ("Interdomain
+ * Attention: Beyond Token-Level Key-Value Memory", German technical summary,
+ * "Rekurrenter Kern"); resuming from a stored state is this library's use of
+ * it.  Same arguments and results as ida_forward_ws, plus:
+ *   state_in  NULL (the zero state: then this is ida_forward_ws), or a
+ *             16-byte aligned device buffer of [B, H] x ida_state_floats(...)
+ *             floats in the layout above (a final_state of an earlier
+ *             prefill, or a decode state).  Read only.  It must not overlap
+ *             final_state (IDA_ERR_ARG).  For bf16 inputs the tails are
+ *             rounded to bf16 where the tensor-core path stages them.
+ * N == 0 copies state_in to final_state (if given).  The eta readout and
+ * other shapes that run token by token take a slower fp32 kernel from a
+ * non-zero state.
+ */
+IDA_API ida_status ida_forward_from(const void *q, const void *k, const void *v,
+                            const float *conv_w, const float *norm_w,
+                            const float *bias, const float *lambda,
+                            const float *Bvec, const float *state_in,
+                            void *out, float *final_state,
+                            int B, int H, int N, int d, int R, int M, int dtype,
+                            int W, int flags, void *workspace,
+                            size_t workspace_bytes, ida_stream_t stream);
+
+/*
  * Workspace bytes that let ida_forward_ws split sequences across the SMs of
  * the current device for this shape; 0 when no split applies (the call then
  * needs no workspace).  Queries the device (no other CUDA work).

@@ -19,7 +19,7 @@ IDA_F32, IDA_BF16 = 0, 1
 IDA_READOUT_ETA = 1
 IDA_PATH_SEQUENTIAL = 256
 
-EXPORTED = ("ida_state_floats", "ida_forward", "ida_forward_ws", "ida_forward_workspace_bytes",
+EXPORTED = ("ida_state_floats", "ida_forward", "ida_forward_ws", "ida_forward_from", "ida_forward_workspace_bytes",
             "ida_forward_noalloc", "ida_decode_step", "ida_device_error", "ida_status_str",
             "ida_last_error")
 
@@ -51,6 +51,9 @@ def load() -> ctypes.CDLL:
             L.ida_forward_ws.restype = _i
             L.ida_forward_ws.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _fp,
                                          _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp]
+            L.ida_forward_from.restype = _i
+            L.ida_forward_from.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _fp, _vp, _fp,
+                                           _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp]
             L.ida_forward_workspace_bytes.restype = ctypes.c_size_t
             L.ida_forward_workspace_bytes.argtypes = [_i] * 9
             L.ida_forward_noalloc.restype = _i
@@ -129,13 +132,16 @@ def ida_forward_workspace_bytes(B: int, H: int, N: int, d: int, R: int, M: int, 
 
 def ida_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,
                 out: torch.Tensor | None = None, final_state: torch.Tensor | bool | None = None,
-                flags: int = 0, stream=None, workspace: torch.Tensor | None = None):
+                flags: int = 0, stream=None, workspace: torch.Tensor | None = None,
+                state_in: torch.Tensor | None = None):
     """Prefill.  q, k [B,N,H,R], v [B,N,H,d] CUDA tensors (fp32/bf16, contiguous).
 
     ``params``: dict of float32 CUDA tensors conv_w [2,H,R,W], norm_w/bias
     [H,R+d], lambda/Bvec [H,M,2].  ``final_state``: a [B,H,S] float32 tensor to
     fill, True to allocate one, or None.  ``workspace``: optional CUDA tensor
-    (any dtype) handed to ``ida_forward_ws``.  Returns (out, final_state).
+    (any dtype) handed to ``ida_forward_ws``.  ``state_in``: optional [B,H,S]
+    float32 CUDA tensor, the state before position 0 (``ida_forward_from``).
+    Returns (out, final_state).
     """
     for t in (q, k, v):
         if not (t.is_cuda and t.is_contiguous()):
@@ -158,7 +164,20 @@ def ida_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,
         final_state = None
     if final_state is not None and (final_state.dtype != torch.float32 or final_state.numel() < B * H * S):
         raise ValueError("final_state must be float32 with B*H*ida_state_floats elements")
-    if workspace is None:
+    if state_in is not None:
+        if not (state_in.is_cuda and state_in.is_contiguous() and state_in.dtype == torch.float32
+                and state_in.numel() >= B * H * S):
+            raise ValueError("state_in must be a contiguous float32 CUDA tensor with B*H*ida_state_floats elements")
+        wp, nbytes = None, 0
+        if workspace is not None:
+            if not workspace.is_cuda:
+                raise ValueError("workspace must be a CUDA tensor")
+            wp, nbytes = workspace, workspace.numel() * workspace.element_size()
+        st = load().ida_forward_from(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv),
+                                     _p(state_in), _p(out), _p(final_state), B, H, N, d, R, M, dt, W,
+                                     int(flags), _p(wp), nbytes, _stream_handle(stream))
+        _check(st, "ida_forward_from")
+    elif workspace is None:
         st = load().ida_forward(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv), _p(out),
                                 _p(final_state), B, H, N, d, R, M, dt, W, int(flags),
                                 _stream_handle(stream))

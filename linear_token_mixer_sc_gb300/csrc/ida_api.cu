@@ -91,9 +91,9 @@ ida_status check_shape(int d, int R, int M, int W, int dtype, int flags, std::st
 namespace ida {
 // Library-internal hooks for entry points defined in other files.
 ida_status forward_entry(const void *q, const void *k, const void *v, const float *conv_w, const float *norm_w,
-                         const float *bias, const float *lambda, const float *Bvec, void *out, float *final_state,
-                         int B, int H, int N, int d, int R, int M, int dtype, int W, int flags, void *workspace,
-                         size_t workspace_bytes, ida_stream_t stream);
+                         const float *bias, const float *lambda, const float *Bvec, const float *state_in, void *out,
+                         float *final_state, int B, int H, int N, int d, int R, int M, int dtype, int W, int flags,
+                         void *workspace, size_t workspace_bytes, ida_stream_t stream);
 ida_status fail_with(ida_status s, const std::string &why) { return fail(s, why); }
 }  // namespace ida
 
@@ -132,8 +132,9 @@ ida_status ida_device_error(unsigned *code) {
 
 ida_status ida::forward_entry(const void *q, const void *k, const void *v, const float *conv_w,
                               const float *norm_w, const float *bias, const float *lambda, const float *Bvec,
-                              void *out, float *final_state, int B, int H, int N, int d, int R, int M, int dtype,
-                              int W, int flags, void *workspace, size_t workspace_bytes, ida_stream_t stream) {
+                              const float *state_in, void *out, float *final_state, int B, int H, int N, int d,
+                              int R, int M, int dtype, int W, int flags, void *workspace, size_t workspace_bytes,
+                              ida_stream_t stream) {
     std::string why;
     if (B < 0 || H < 0 || N < 0) return fail(IDA_ERR_ARG, "B, H and N must be >= 0");
     ida_status s = check_shape(d, R, M, W, dtype, flags, why);
@@ -149,22 +150,31 @@ ida_status ida::forward_entry(const void *q, const void *k, const void *v, const
             if (!aligned16(p)) return fail(IDA_ERR_ARG, "pointers must be 16-byte aligned");
     }
     if (final_state && !aligned16(final_state)) return fail(IDA_ERR_ARG, "final_state must be 16-byte aligned");
+    if (state_in && !aligned16(state_in)) return fail(IDA_ERR_ARG, "state_in must be 16-byte aligned");
     if (workspace && !aligned16(workspace)) return fail(IDA_ERR_ARG, "workspace must be 16-byte aligned");
+    if (state_in && final_state) {
+        // the kernels read state_in after some units' final states are written
+        const size_t bytes = (size_t)B * H * ida_state_floats(d, R, M, W) * sizeof(float);
+        const char *si = reinterpret_cast<const char *>(state_in), *fo = reinterpret_cast<const char *>(final_state);
+        if (si < fo + bytes && fo < si + bytes) return fail(IDA_ERR_ARG, "state_in and final_state must not overlap");
+    }
     if ((long long)B * H == 0 || (N == 0 && !final_state)) return IDA_OK;
     int num_sms = 0;
     s = device_setup(&num_sms, why);
     if (s != IDA_OK) return fail(s, why);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t SF = ida_state_floats(d, R, M, W);
-    if (N == 0) {  // zero positions: the final state is the zero start state
-        cudaError_t e = cudaMemsetAsync(final_state, 0, (size_t)B * H * SF * sizeof(float), st);
+    if (N == 0) {  // zero positions: the final state is the start state
+        const size_t bytes = (size_t)B * H * SF * sizeof(float);
+        cudaError_t e = state_in ? cudaMemcpyAsync(final_state, state_in, bytes, cudaMemcpyDeviceToDevice, st)
+                                 : cudaMemsetAsync(final_state, 0, bytes, st);
         if (e != cudaSuccess) return fail(IDA_ERR_CUDA, cudaGetErrorString(e));
         return IDA_OK;
     }
     ida::PrefillArgs a;
     a.q = q; a.k = k; a.v = v;
     a.conv_w = conv_w; a.norm_w = norm_w; a.bias = bias; a.lambda = lambda; a.Bvec = Bvec;
-    a.out = out; a.final_state = final_state;
+    a.out = out; a.final_state = final_state; a.state_in = state_in;
     a.B = B; a.H = H; a.N = N; a.d = d; a.R = R; a.M = M; a.W = W; a.dtype = dtype; a.flags = flags;
     a.state_floats = SF;
     a.err = g_err_dev;
@@ -183,8 +193,8 @@ ida_status ida_forward(const void *q, const void *k, const void *v, const float 
                        const float *norm_w, const float *bias, const float *lambda,
                        const float *Bvec, void *out, float *final_state, int B, int H, int N,
                        int d, int R, int M, int dtype, int W, int flags, ida_stream_t stream) {
-    return ida::forward_entry(q, k, v, conv_w, norm_w, bias, lambda, Bvec, out, final_state, B, H, N, d, R, M,
-                              dtype, W, flags, nullptr, 0, stream);
+    return ida::forward_entry(q, k, v, conv_w, norm_w, bias, lambda, Bvec, nullptr, out, final_state, B, H, N, d,
+                              R, M, dtype, W, flags, nullptr, 0, stream);
 }
 
 ida_status ida_forward_ws(const void *q, const void *k, const void *v, const float *conv_w,
@@ -192,8 +202,17 @@ ida_status ida_forward_ws(const void *q, const void *k, const void *v, const flo
                           const float *Bvec, void *out, float *final_state, int B, int H, int N,
                           int d, int R, int M, int dtype, int W, int flags, void *workspace,
                           size_t workspace_bytes, ida_stream_t stream) {
-    return ida::forward_entry(q, k, v, conv_w, norm_w, bias, lambda, Bvec, out, final_state, B, H, N, d, R, M,
-                              dtype, W, flags, workspace, workspace_bytes, stream);
+    return ida::forward_entry(q, k, v, conv_w, norm_w, bias, lambda, Bvec, nullptr, out, final_state, B, H, N, d,
+                              R, M, dtype, W, flags, workspace, workspace_bytes, stream);
+}
+
+ida_status ida_forward_from(const void *q, const void *k, const void *v, const float *conv_w,
+                            const float *norm_w, const float *bias, const float *lambda, const float *Bvec,
+                            const float *state_in, void *out, float *final_state, int B, int H, int N, int d,
+                            int R, int M, int dtype, int W, int flags, void *workspace, size_t workspace_bytes,
+                            ida_stream_t stream) {
+    return ida::forward_entry(q, k, v, conv_w, norm_w, bias, lambda, Bvec, state_in, out, final_state, B, H, N, d,
+                              R, M, dtype, W, flags, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

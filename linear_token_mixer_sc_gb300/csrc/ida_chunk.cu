@@ -393,8 +393,9 @@ __global__ void __launch_bounds__(NTH, 1)
         __syncthreads();
         tc_fence_after();
         {
-            // start state: zero at the sequence start, else the state before block j0,
-            //   X = sum_{j < j0} g^(j0-1-j) X_local(j),  g = lambda^(C fs) per mode,
+            // start state: X_in (zero, or the caller's state before position 0) at the sequence
+            // start, else the state before block j0,
+            //   X = g^j0 X_in + sum_{j < j0} g^(j0-1-j) X_local(j),  g = lambda^(C fs) per mode,
             // by Horner over the block end states ([R+128 columns][128 lanes] floats, columns as
             // in TMEM); U columns pair Re / Im across lanes 2m, 2m+1, Gamma^T columns across
             // columns R+2m, R+2m+1.  By column half.
@@ -404,7 +405,32 @@ __global__ void __launch_bounds__(NTH, 1)
             const float *xs = seg_start + (size_t)unit * plan_state_blocks(plan) * (size_t)(R + MP) * 128;
             const float2 gu = gblk[mm];
             const float gus = is_im ? gu.y : -gu.y;  // own(g z) = z_own Re g + z_partner s Im g
-            for (int j = 0; j < (j0 > 0 ? j0 : 1); ++j) {
+            const bool has_in = a.state_in != nullptr;
+            if (has_in) {
+                // X_in in the same layout: U[m][c] of plane tl at column c; Gamma^T (value lane
+                // tl) at column R + 2m (Re) / R + 2m + 1 (Im)
+                const float *xin = a.state_in + (size_t)unit * a.state_floats;
+                const size_t RDs = R + D, plane = (size_t)64 * RDs;
+                float x[NG][16];
+    #pragma unroll
+                for (int g = 0; g < NG; ++g) {
+                    const int c0 = 32 * g + 16 * hsel;
+    #pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int c = c0 + i;
+                        if (c < R) {
+                            x[g][i] = xin[(is_im ? plane : 0) + (size_t)mm * RDs + c];
+                        } else {
+                            const int pl = c - R;
+                            x[g][i] = tl < D ? xin[((pl & 1) ? plane : 0) + (size_t)(pl >> 1) * RDs + R + tl] : 0.f;
+                        }
+                    }
+                }
+    #pragma unroll
+                for (int g = 0; g < NG; ++g) tmem_st16(tb + lane_base + 32 * g + 16 * hsel, x[g]);
+                tmem_wait_st();
+            }
+            for (int j = 0; j < (j0 > 0 ? j0 : (has_in ? 0 : 1)); ++j) {
                 float x[NG][16];
     #pragma unroll
                 for (int g = 0; g < NG; ++g) {
@@ -412,7 +438,7 @@ __global__ void __launch_bounds__(NTH, 1)
     #pragma unroll
                     for (int i = 0; i < 16; ++i) x[g][i] = j0 > 0 ? xg[(size_t)i * 128] : 0.f;
                 }
-                if (j > 0) {
+                if (j > 0 || has_in) {
     #pragma unroll
                     for (int g = 0; g < NG; ++g) {
                         const int c0 = 32 * g + 16 * hsel;
@@ -472,9 +498,15 @@ __global__ void __launch_bounds__(NTH, 1)
         }
 
 
-        // eta of my mode at the piece start, B sum_{k < t_begin} lambda^k (hsel == 0, Re thread)
+        // eta of my mode at the piece start, lambda^t_begin eta_in + B sum_{k < t_begin} lambda^k
+        // (hsel == 0, Re thread)
         float eta_r = 0.f, eta_i = 0.f;
         if (hsel == 0 && !is_im) {
+            if (a.state_in) {
+                const float *ein = a.state_in + (size_t)unit * a.state_floats + (size_t)2 * 64 * (R + D);
+                eta_r = ein[mm];
+                eta_i = ein[64 + mm];
+            }
             const float2 ll = laml[mm], sl = suml[mm];
             for (int c = 0; c < c_begin; ++c) {
                 const float er = ll.x * eta_r - ll.y * eta_i + b_r * sl.x - b_i * sl.y;
@@ -497,6 +529,22 @@ __global__ void __launch_bounds__(NTH, 1)
             if (ok) tma_pending = 0;
             tc_fence_after();
             if (__syncthreads_or(!ok)) break;
+            if (ci == 0 && a.state_in) {
+                // conv halo of the first chunk: the raw rows before position 0 are the initial
+                // state's tails (the copy zero-filled them)
+                const float *tq = a.state_in + (size_t)unit * a.state_floats + (size_t)2 * 64 * (R + D + 1);
+                const float *tk = tq + (size_t)(W - 1) * R;
+                __nv_bfloat16 *rq = reinterpret_cast<__nv_bfloat16 *>(sm + S::RAWQ);
+                __nv_bfloat16 *rk = reinterpret_cast<__nv_bfloat16 *>(sm + S::RAWK);
+                for (int x = tid; x < HALO * R; x += NTH) {
+                    const int r = x / R, c = x % R, j = r - HALO + (W - 1);  // tail row of position r - 3
+                    if (j >= 0) {
+                        rq[x] = __float2bfloat16_rn(tq[(size_t)j * R + c]);
+                        rk[x] = __float2bfloat16_rn(tk[(size_t)j * R + c]);
+                    }
+                }
+                __syncthreads();
+            }
 
             // ---- S1: prologue, thread = (8-channel block, block of consecutive positions)
             {
@@ -1177,11 +1225,14 @@ __global__ void __launch_bounds__(NTH, 1)
             }
             float *tq = fs + 2 * plane + 2 * M;
             float *tk = tq + (size_t)(W - 1) * R;
+            const float *tin = a.state_in ? a.state_in + (size_t)unit * a.state_floats + (tq - fs) : nullptr;
             for (int x = tid; x < (W - 1) * R; x += NTH) {
                 const int r = x / R, c = x % R;
-                const int p = N - (W - 1) + r;
-                tq[x] = p >= 0 ? __bfloat162float(gq[base_qk + (size_t)p * sqk + c]) : 0.f;
-                tk[x] = p >= 0 ? __bfloat162float(gk[base_qk + (size_t)p * sqk + c]) : 0.f;
+                const int p = N - (W - 1) + r;  // before position 0: the initial state's tails
+                const size_t tx = (size_t)(p + W - 1) * R + c;
+                tq[x] = p >= 0 ? __bfloat162float(gq[base_qk + (size_t)p * sqk + c]) : (tin ? tin[tx] : 0.f);
+                tk[x] = p >= 0 ? __bfloat162float(gk[base_qk + (size_t)p * sqk + c])
+                               : (tin ? tin[(size_t)(W - 1) * R + tx] : 0.f);
             }
             const size_t used = 2 * plane + 2 * M + 2 * (size_t)(W - 1) * R;
             for (size_t x = used + tid; x < a.state_floats; x += NTH) fs[x] = 0.f;
@@ -1331,6 +1382,17 @@ __global__ void __launch_bounds__(NTH, 1)
         ok = mbar_wait(&bar[0], par);
         if (ok) tma_pending = 0;
         if (__syncthreads_or(!ok)) break;
+        if (ci == 0 && a.state_in) {
+            // conv halo of the first chunk: the initial state's key tails (the copy zero-filled them)
+            const float *tk = a.state_in + (size_t)unit * a.state_floats + (size_t)2 * 64 * (R + D + 1) +
+                              (size_t)(W - 1) * R;
+            __nv_bfloat16 *rk = reinterpret_cast<__nv_bfloat16 *>(sm + S::RAWK);
+            for (int x = tid; x < HALO * R; x += NTH) {
+                const int r = x / R, c = x % R, j = r - HALO + (W - 1);
+                if (j >= 0) rk[x] = __float2bfloat16_rn(tk[(size_t)j * R + c]);
+            }
+            __syncthreads();
+        }
         // key conv and the raw value rows: the staged tiles are then free for the next chunk
         float fk[PPQ][8];
 #pragma unroll

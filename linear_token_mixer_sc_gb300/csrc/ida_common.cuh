@@ -15,6 +15,7 @@ struct PrefillArgs {
     const float *conv_w, *norm_w, *bias, *lambda, *Bvec;
     void *out;
     float *final_state;
+    const float *state_in;  // NULL: the zero state; else [B,H] x state_floats, the state before position 0
     int B, H, N, d, R, M, W, dtype, flags;
     size_t state_floats;
     unsigned *err;  // device-visible error word (host-mapped)

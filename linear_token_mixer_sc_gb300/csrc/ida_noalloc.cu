@@ -17,9 +17,9 @@
 
 namespace ida {
 ida_status forward_entry(const void *q, const void *k, const void *v, const float *conv_w, const float *norm_w,
-                         const float *bias, const float *lambda, const float *Bvec, void *out, float *final_state,
-                         int B, int H, int N, int d, int R, int M, int dtype, int W, int flags, void *workspace,
-                         size_t workspace_bytes, ida_stream_t stream);
+                         const float *bias, const float *lambda, const float *Bvec, const float *state_in, void *out,
+                         float *final_state, int B, int H, int N, int d, int R, int M, int dtype, int W, int flags,
+                         void *workspace, size_t workspace_bytes, ida_stream_t stream);
 ida_status fail_with(ida_status s, const std::string &why);
 size_t forward_workspace_within(int B, int H, int N, int d, int R, int M, int dtype, int W, int flags,
                                 size_t budget);
@@ -67,6 +67,6 @@ extern "C" ida_status ida_forward_noalloc(const void *q, const void *k, const vo
     }
     // Nothing in the scratch has to start at zero: each call writes every slot
     // it reads (segment end states, then start states) before reading it.
-    return ida::forward_entry(q, k, v, conv_w, norm_w, bias, lambda, Bvec, out, final_state, B, H, N, d, R, M, dtype,
-                              W, flags, scratch, kStaticScratchBytes, stream);
+    return ida::forward_entry(q, k, v, conv_w, norm_w, bias, lambda, Bvec, nullptr, out, final_state, B, H, N, d, R,
+                              M, dtype, W, flags, scratch, kStaticScratchBytes, stream);
 }

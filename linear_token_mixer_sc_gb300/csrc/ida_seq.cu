@@ -50,11 +50,12 @@ static size_t seq_smem_bytes(int Mg, int R, int d) {
            + TT * e;                // partial denominators
 }
 
-// Prologue of one position (one warp): xi(q) -> xq_row, [kt ; vt] -> z_row.
+// Prologue of one position (one warp): xi(q) -> xq_row, [kt ; vt] -> z_row.  tails: NULL, or
+// the raw q rows [W-1][R] then k rows of the positions before 0 (oldest first).
 template <int NC, typename T>
 __device__ __forceinline__ void seq_prologue(const PrefillArgs &a, int h, size_t base_qk,
                                              size_t base_v, int t, T *xq_row,
-                                             T *z_row, int lane) {
+                                             T *z_row, int lane, const float *tails) {
     const int R = a.R, d = a.d, W = a.W, H = a.H;
     const size_t sqk = (size_t)H * R, sv = (size_t)H * d;
     const float *nw = a.norm_w + (size_t)h * (R + d);
@@ -75,6 +76,9 @@ __device__ __forceinline__ void seq_prologue(const PrefillArgs &a, int h, size_t
                     int p = t - (W - 1) + j;
                     if (p >= 0)
                         s = fma((T)cw[(size_t)c * W + j], (T)load_in(x, a.dtype, base_qk + (size_t)p * sqk + c), s);
+                    else if (tails)
+                        s = fma((T)cw[(size_t)c * W + j],
+                                (T)tails[((size_t)which * (W - 1) + (p + W - 1)) * R + c], s);
                 }
                 f[i] = silu(s);
                 ss = fma(f[i], f[i], ss);
@@ -142,13 +146,28 @@ __global__ void __launch_bounds__(SEQ_THREADS, 1) seq_prefill_kernel(PrefillArgs
     const size_t base_v = ((size_t)b * N * H + h) * d;
     const bool eta_ro = (a.flags & IDA_READOUT_ETA) != 0;
 
+    const float *sin = a.state_in ? a.state_in + (size_t)unit * a.state_floats : nullptr;
+    const size_t gplane = (size_t)M * RD;
     for (int i = threadIdx.x; i < 2 * Mg * RD + 2 * Mg; i += SEQ_THREADS) Xr[i] = T(0);
+    __syncthreads();
+    if (sin) {  // the caller's state before position 0, my modes
+        for (int i = threadIdx.x; i < mcount * RD; i += SEQ_THREADS) {
+            const int ml = i / RD, c = i % RD;
+            Xr[i] = (T)sin[(size_t)(m0 + ml) * RD + c];
+            Xi[i] = (T)sin[gplane + (size_t)(m0 + ml) * RD + c];
+        }
+        for (int ml = threadIdx.x; ml < mcount; ml += SEQ_THREADS) {
+            etr[ml] = (T)sin[2 * gplane + m0 + ml];
+            eti[ml] = (T)sin[2 * gplane + M + m0 + ml];
+        }
+    }
+    const float *tails = sin ? sin + 2 * gplane + 2 * M : nullptr;
 
     for (int t0 = 0; t0 < N; t0 += TT) {
         const int tn = min(TT, N - t0);
         // Phase A: prologue, one warp per position; clear the partials.
         if (warp < tn) {
-            seq_prologue<NC, T>(a, h, base_qk, base_v, t0 + warp, xq + warp * R, z + warp * RD, lane);
+            seq_prologue<NC, T>(a, h, base_qk, base_v, t0 + warp, xq + warp * R, z + warp * RD, lane, tails);
             for (int j = lane; j < d; j += 32) opart[warp * d + j] = T(0);
             if (lane == 0) dpart[warp] = T(0);
         }
@@ -256,9 +275,11 @@ __global__ void __launch_bounds__(SEQ_THREADS, 1) seq_prefill_kernel(PrefillArgs
             float *tk = tq + (size_t)(W - 1) * R;
             for (int i = threadIdx.x; i < (W - 1) * R; i += SEQ_THREADS) {
                 int r = i / R, c = i % R;
-                int p = N - (W - 1) + r;
-                tq[i] = p >= 0 ? load_in(a.q, a.dtype, base_qk + (size_t)p * sqk + c) : 0.f;
-                tk[i] = p >= 0 ? load_in(a.k, a.dtype, base_qk + (size_t)p * sqk + c) : 0.f;
+                int p = N - (W - 1) + r;  // before position 0: the initial state's tails
+                const size_t tx = (size_t)(p + W - 1) * R + c;
+                tq[i] = p >= 0 ? load_in(a.q, a.dtype, base_qk + (size_t)p * sqk + c) : (tails ? tails[tx] : 0.f);
+                tk[i] = p >= 0 ? load_in(a.k, a.dtype, base_qk + (size_t)p * sqk + c)
+                               : (tails ? tails[(size_t)(W - 1) * R + tx] : 0.f);
             }
             size_t used = 2 * plane + 2 * M + 2 * (size_t)(W - 1) * R;
             for (size_t i = used + threadIdx.x; i < a.state_floats; i += SEQ_THREADS) fs[i] = 0.f;
@@ -325,7 +346,9 @@ bool launch_seq_modes(const PrefillArgs &a, cudaStream_t st, int num_sms, ida_st
 ida_status launch_seq_prefill(const PrefillArgs &a, cudaStream_t st, int num_sms, std::string &why) {
     if (a.dtype == IDA_F32) return launch_seq_t<double>(a, st, num_sms, why);
     ida_status s;
-    if (launch_seq_modes(a, st, num_sms, s, why)) return s;
+    // the register-resident kernel runs in the scaled state X / B, which a caller's state
+    // cannot always be brought into (B = 0 with X != 0): from a given state this kernel runs
+    if (!a.state_in && launch_seq_modes(a, st, num_sms, s, why)) return s;
     return launch_seq_t<float>(a, st, num_sms, why);
 }
 

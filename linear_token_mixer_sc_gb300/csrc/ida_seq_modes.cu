@@ -492,6 +492,7 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
         for (int ow = 0; ow * PT < tn; ++ow) {
             uint32_t uo = G > 1 ? mapa_u32(ao, ow) : ao, ud = G > 1 ? mapa_u32(ad, ow) : ad;
             const int te = min(tn, ow * PT + PT);
+#pragma unroll 2
             for (int tt = ow * PT; tt < te; ++tt, uo += 4 * R, ud += 4) step(uo, ud);
         }
     };

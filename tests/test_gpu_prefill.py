@@ -264,3 +264,70 @@ def test_split_prefill_is_deterministic(name):
         assert torch.equal(outs[0], outs[r]), f"split call {r} differs from the first"
     for r in (3, 5):
         assert torch.equal(outs[1], outs[r]), f"whole call {r} differs from the first"
+
+
+# ---- prefill from an initial state (ida_forward_from) -------------------------
+
+ETA = binding.IDA_READOUT_ETA
+# (B, N1, N2, H, R, d, M, W, dtype, flags): the first N1 positions are a GPU prefill whose final
+# state starts the remaining N2; ragged lengths, a second part shorter than the conv tails, d != R,
+# W < 4, a split plan (few units, long second part), the token-sequential paths and eta
+FROM_STATE = [
+    (2, 70, 131, 3, 64, 64, 64, 4, "bf16", 0),
+    (1, 64 * 5 + 7, 64 * 9 + 3, 2, 128, 128, 64, 4, "bf16", 0),
+    (1, 64 * 3, 64 * 12, 1, 64, 64, 64, 4, "bf16", 0),
+    (2, 2, 1, 2, 64, 64, 64, 4, "bf16", 0),
+    (1, 50, 40, 2, 128, 64, 64, 3, "bf16", 0),
+    (1, 33, 20, 2, 32, 32, 16, 4, "f32", 0),
+    (1, 33, 20, 2, 32, 32, 16, 4, "f32", ETA),
+    (2, 40, 25, 2, 64, 64, 64, 4, "bf16", ETA),
+    (1, 1, 3, 2, 64, 64, 64, 2, "bf16", 0),
+]
+
+
+@pytest.mark.parametrize("case", FROM_STATE, ids=lambda c: "B{}N{}+{}H{}R{}d{}M{}W{}{}f{}".format(*c))
+def test_prefill_from_state(case):
+    """The second part, started from the GPU's state after the first, against the oracle started
+    from that same state (and, end to end, against the oracle's single run over all positions)."""
+    B, N1, N2, H, R, d, M, W, dt, flags = case
+    q, k, v, p = problem(B, N1 + N2, H, R, d, M, W, dt, seed=300 + N1 + N2)
+    dev = torch.device("cuda")
+    pd = binding.params_to_device(p)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    q1, k1, v1 = qd[:, :N1].contiguous(), kd[:, :N1].contiguous(), vd[:, :N1].contiguous()
+    q2, k2, v2 = qd[:, N1:].contiguous(), kd[:, N1:].contiguous(), vd[:, N1:].contiguous()
+    _, fs1 = binding.ida_forward(q1, k1, v1, pd, flags=flags, final_state=True,
+                                 workspace=binding.forward_workspace(q1, v1, pd, flags))
+    ws2 = binding.forward_workspace(q2, v2, pd, flags)
+    out2, fs2 = binding.ida_forward(q2, k2, v2, pd, flags=flags, final_state=True, workspace=ws2,
+                                    state_in=fs1)
+    torch.cuda.synchronize()
+    assert binding.ida_device_error() == 0
+    st1 = unpadded_state(to_np(fs1), d, R, M, W)
+    ref = orc.forward(q[:, N1:], k[:, N1:], v[:, N1:], p, flags=flags, final_state=True, state_in=st1)
+    _check(to_np(out2), ref["out"], dt)
+    tol = F32_REL_L2 if dt == "f32" else BF16_REL_L2
+    assert rel_l2(unpadded_state(to_np(fs2), d, R, M, W), ref["final_state"]) <= tol
+    full = orc.forward(q, k, v, p, flags=flags, final_state=True)
+    _check(to_np(out2), full["out"][:, N1:], dt)
+    assert rel_l2(unpadded_state(to_np(fs2), d, R, M, W), full["final_state"]) <= tol
+
+
+def test_prefill_from_state_zero_length_copies_state():
+    q, k, v, p = problem(1, 9, 2, 64, 64, 64, 4, "bf16", seed=31)
+    dev = torch.device("cuda")
+    pd = binding.params_to_device(p)
+    _, fs1 = binding.ida_forward(q.to(dev), k.to(dev), v.to(dev), pd, final_state=True)
+    e = torch.empty((1, 0, 2, 64), dtype=torch.bfloat16, device=dev)
+    _, fs2 = binding.ida_forward(e, e.clone(), e.clone(), pd, final_state=True, state_in=fs1)
+    torch.cuda.synchronize()
+    assert torch.equal(fs1, fs2)
+
+
+def test_prefill_from_state_rejects_overlap():
+    q, k, v, p = problem(1, 8, 2, 64, 64, 64, 4, "bf16", seed=32)
+    dev = torch.device("cuda")
+    pd = binding.params_to_device(p)
+    _, fs = binding.ida_forward(q.to(dev), k.to(dev), v.to(dev), pd, final_state=True)
+    with pytest.raises(binding.IdaError, match="overlap"):
+        binding.ida_forward(q.to(dev), k.to(dev), v.to(dev), pd, final_state=fs, state_in=fs)
