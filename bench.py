@@ -162,7 +162,7 @@ class ClockSampler:
 # ---------------------------------------------------------------- our arm
 
 class Prefill:
-    def __init__(self, w, dev, flags=0):
+    def __init__(self, w, dev, flags=0, from_state=False):
         from linear_token_mixer_sc_gb300 import binding
         self.b = binding
         self.w, self.dev, self.flags = w, dev, flags
@@ -185,10 +185,16 @@ class Prefill:
             self.launches_per_step = 1
         else:
             self.launches_per_step = 2 if self.ws is None else 3
+        # continuing a sequence: the state after this same batch of positions (set-up, untimed)
+        self.state_in = None
+        if from_state:
+            _, self.state_in = binding.ida_forward(self.q, self.k, self.v, self.pd, flags=flags,
+                                                   final_state=True, workspace=self.ws)
+            torch.cuda.synchronize(dev)
 
     def step(self):
         self.b.ida_forward(self.q, self.k, self.v, self.pd, out=self.out, final_state=self.fs,
-                           flags=self.flags, workspace=self.ws)
+                           flags=self.flags, workspace=self.ws, state_in=self.state_in)
 
     def step_e2e(self):
         for src, dst in zip(self.host, (self.q, self.k, self.v)):
@@ -203,7 +209,8 @@ class Prefill:
         return self.w.B * self.w.N
 
     def alg_bytes(self):
-        return prefill_bytes(self.w)
+        extra = 0 if self.state_in is None else self.state_in.numel() * 4  # the start state, read once
+        return prefill_bytes(self.w) + extra
 
     def flops(self):
         return mixer_flops(self.w, self.w.B * self.w.H * self.w.N)
@@ -380,8 +387,9 @@ def job_value(world_size: int, tokens_per_rank: int, ms_max: float) -> float:
     return world_size * tokens_per_rank / (ms_max * 1e-3)
 
 
-def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e2e=True, seed_len=None):
-    runner = Decode(w, dev, flags, seed_len) if w.decode_steps else Prefill(w, dev, flags)
+def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e2e=True, seed_len=None,
+            from_state=False):
+    runner = Decode(w, dev, flags, seed_len) if w.decode_steps else Prefill(w, dev, flags, from_state)
     flush = runner.resident_bytes() < 2 * L2_BYTES
     if dist is not None:
         dist.barrier()
@@ -398,7 +406,8 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e
     res = {"value": value, "ms_per_step": ms_all, "tokens_per_step": runner.tokens(),
            "flush_l2": flush, "wall_s": wall,
            "roofline": roofline(runner, ms, peaks, peak_kind,
-                                traffic_record(w.name + (":eta" if flags & 1 else ""), sources),
+                                traffic_record(w.name + (":eta" if flags & 1 else "") +
+                                               (":from_state" if from_state else ""), sources),
                                 kernel_bound="alu" if flags & 1 else None),
            "gpu_launches": runner.launches_per_step * steps}
     if e2e:
@@ -419,6 +428,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=configs.PREFILL_125M.name, choices=sorted(configs.ALL))
     ap.add_argument("--eta", action="store_true", help="eta-normalised readout")
+    ap.add_argument("--from-state", action="store_true",
+                    help="prefill continuing from a given state (ida_forward_from)")
     ap.add_argument("--no-decode", action="store_true", help="skip the secondary decode line")
     ap.add_argument("--seed-len", type=int, default=None,
                     help="decode workload: length of the seeding prefill (default: the workload's 4096)")
@@ -432,6 +443,7 @@ def main():
     cores = os.cpu_count() or 1
     config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "R": w.R, "d": w.d, "M": w.M,
               "W": w.W, "readout": "eta" if args.eta else "denominator-free",
+              "start": "from a given state" if args.from_state else "zero state",
               "parallelism": f"replicas x{ws} (independent (b,h) units, no collective)"}
 
     if args.impl == "reference":
@@ -472,7 +484,7 @@ def main():
     sampler.start()
     main_res = measure(w, dev, args.steps, args.warmup, flags, dist, ws, peaks, peak_kind,
                        DECODE_SOURCES if w.decode_steps else (ETA_SOURCES if flags else PREFILL_SOURCES),
-                       seed_len=args.seed_len)
+                       seed_len=args.seed_len, from_state=args.from_state and not w.decode_steps)
     clocks = sampler.stop()
     decode_res = None
     if not w.decode_steps and not args.no_decode:
