@@ -22,6 +22,8 @@
  *   a1  s_t[c]  = sum_{j<W} w[c][j] * x_{t-W+1+j}[c], x_{<0} = 0 (or the
  *                 carried tail), for x = q and x = k separately.   [de] feature map
  *   a2  xi(x)_t = SiLU(s_t) / (sum_c SiLU(s_t)[c]^2 + EPS_FEAT).  [de] feature map
+ *       With ORC_FEAT_L2 (the "SiLU/l_2" wording of the Chinese summary's
+ *       introduction): xi(x)_t = SiLU(s_t) / (||SiLU(s_t)||_2 + EPS_FEAT).
  *   a3  kt_t    = xi(k)_t / sqrt(mean_c xi(k)_t^2 + EPS_RMS) * w_k + b_k,
  *       vt_t    = v_t     / sqrt(mean_c v_t^2     + EPS_RMS) * w_v + b_v.
  *                                                            [de] normalisation
@@ -64,7 +66,7 @@
 #define EPS_RMS 1e-6
 
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
-enum { ORC_READOUT_ETA = 1 };
+enum { ORC_READOUT_ETA = 1, ORC_FEAT_L2 = 2 };
 
 /* ---- element access -------------------------------------------------- */
 
@@ -130,6 +132,21 @@ void orc_feature_map(const double *s, int N, int C, double *xi)
     }
 }
 
+/* The l_2 reading: SiLU(s) over its Euclidean norm (plus EPS_FEAT). */
+void orc_feature_map_l2(const double *s, int N, int C, double *xi)
+{
+    for (int t = 0; t < N; ++t) {
+        const double *row = s + (size_t)t * C;
+        double sq = 0.0;
+        for (int c = 0; c < C; ++c) {
+            double f = orc_silu(row[c]);
+            sq += f * f;
+        }
+        for (int c = 0; c < C; ++c)
+            xi[(size_t)t * C + c] = orc_silu(row[c]) / (sqrt(sq) + EPS_FEAT);
+    }
+}
+
 /* ---- a3: RMSNorm with per-channel weight and bias --------------------- */
 
 void orc_rmsnorm_affine(const double *x, int N, int C, const double *w,
@@ -152,6 +169,27 @@ void orc_rmsnorm_affine(const double *x, int N, int C, const double *w,
  * [R][W], norm weight/bias [R+d] (key half first).  Outputs xq = xi(q) [N][R],
  * kt [N][R], vt [N][d].  Tails (raw inputs before position 0) may be NULL.
  */
+static void unit_features(const double *q, const double *k, const double *v,
+                          int N, int R, int d, int W,
+                          const double *wq, const double *wk,
+                          const double *norm_w, const double *bias,
+                          const double *tail_q, const double *tail_k, int feat_l2,
+                          double *xq, double *kt, double *vt)
+{
+    size_t nr = (size_t)N * R;
+    double *s = malloc(nr * sizeof(double));
+    double *xk = malloc(nr * sizeof(double));
+    void (*fmap)(const double *, int, int, double *) = feat_l2 ? orc_feature_map_l2 : orc_feature_map;
+    orc_causal_conv(q, N, R, wq, W, tail_q, s);
+    fmap(s, N, R, xq);
+    orc_causal_conv(k, N, R, wk, W, tail_k, s);
+    fmap(s, N, R, xk);
+    orc_rmsnorm_affine(xk, N, R, norm_w, bias, kt);
+    orc_rmsnorm_affine(v, N, d, norm_w + R, bias + R, vt);
+    free(s);
+    free(xk);
+}
+
 void orc_unit_features(const double *q, const double *k, const double *v,
                        int N, int R, int d, int W,
                        const double *wq, const double *wk,
@@ -159,17 +197,7 @@ void orc_unit_features(const double *q, const double *k, const double *v,
                        const double *tail_q, const double *tail_k,
                        double *xq, double *kt, double *vt)
 {
-    size_t nr = (size_t)N * R;
-    double *s = malloc(nr * sizeof(double));
-    double *xk = malloc(nr * sizeof(double));
-    orc_causal_conv(q, N, R, wq, W, tail_q, s);
-    orc_feature_map(s, N, R, xq);
-    orc_causal_conv(k, N, R, wk, W, tail_k, s);
-    orc_feature_map(s, N, R, xk);
-    orc_rmsnorm_affine(xk, N, R, norm_w, bias, kt);
-    orc_rmsnorm_affine(v, N, d, norm_w + R, bias + R, vt);
-    free(s);
-    free(xk);
+    unit_features(q, k, v, N, R, d, W, wq, wk, norm_w, bias, tail_q, tail_k, 0, xq, kt, vt);
 }
 
 /* ---- a4-a7: the S4D recurrence and the query-conditioned readout ------ */
@@ -276,8 +304,8 @@ void orc_unit_forward(const double *q, const double *k, const double *v,
     }
     if (state)
         state_unpack(state, M, RD, X, eta);
-    orc_unit_features(q, k, v, N, R, d, W, wq, wk, norm_w, bias, tail_q,
-                      tail_k, xq, kt, vt);
+    unit_features(q, k, v, N, R, d, W, wq, wk, norm_w, bias, tail_q, tail_k,
+                  flags & ORC_FEAT_L2, xq, kt, vt);
     scan_readout(xq, kt, vt, N, R, d, M, lam, Bv, flags & ORC_READOUT_ETA, X,
                  eta, out, den);
     if (state)

@@ -28,6 +28,7 @@ _lock = threading.Lock()
 _lib = None
 
 READOUT_ETA = 1
+FEAT_L2 = 2  # the "SiLU/l_2" reading of the feature map
 F32, BF16 = 0, 1
 
 _dp = ctypes.POINTER(ctypes.c_double)
@@ -62,6 +63,7 @@ def lib():
             L.orc_silu.argtypes = [ctypes.c_double]
             L.orc_causal_conv.argtypes = [_dp, _i, _i, _dp, _i, _dp, _dp]
             L.orc_feature_map.argtypes = [_dp, _i, _i, _dp]
+            L.orc_feature_map_l2.argtypes = [_dp, _i, _i, _dp]
             L.orc_rmsnorm_affine.argtypes = [_dp, _i, _i, _dp, _dp, _dp]
             L.orc_unit_features.argtypes = [_dp, _dp, _dp, _i, _i, _i, _i, _dp, _dp,
                                             _dp, _dp, _dp, _dp, _dp, _dp, _dp]
@@ -129,10 +131,11 @@ def causal_conv(x, w, tail=None) -> np.ndarray:
     return s
 
 
-def feature_map(s) -> np.ndarray:
+def feature_map(s, l2: bool = False) -> np.ndarray:
     s = _d(s)
     xi = np.empty_like(s)
-    lib().orc_feature_map(_ptr(s), s.shape[0], s.shape[1], _ptr(xi))
+    fn = lib().orc_feature_map_l2 if l2 else lib().orc_feature_map
+    fn(_ptr(s), s.shape[0], s.shape[1], _ptr(xi))
     return xi
 
 

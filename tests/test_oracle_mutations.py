@@ -28,8 +28,10 @@ MUTATIONS = [
      "xi[(size_t)t * C + c] = orc_silu(row[c]) / (sqrt(sq) + EPS_FEAT);"),
     ("RMS over the sum, not the mean", "        ms /= C;\n", "\n"),
     ("eta driven without B", "eta[m] = lam[m] * eta[m] + Bv[m];", "eta[m] = lam[m] * eta[m] + 1.0;"),
-    ("query RMS-normed like the key", "    orc_feature_map(s, N, R, xq);\n",
-     "    orc_feature_map(s, N, R, xq);\n    orc_rmsnorm_affine(xq, N, R, norm_w, bias, xq);\n"),
+    ("query RMS-normed like the key", "    fmap(s, N, R, xq);\n",
+     "    fmap(s, N, R, xq);\n    orc_rmsnorm_affine(xq, N, R, norm_w, bias, xq);\n"),
+    ("l_2 map with the squared norm", "/ (sqrt(sq) + EPS_FEAT);", "/ (sq + EPS_FEAT);"),
+    ("l_2 flag ignored", "flags & ORC_FEAT_L2, xq, kt, vt);", "0, xq, kt, vt);"),
     ("starting tails ignored", "flags, st, tin_q, tin_k, o, dn);", "flags, st, NULL, NULL, o, dn);"),
     ("final tails not reaching into the starting tails", "} else if (sin) {", "} else if (0) {"),
     ("starting eta ignored", "memcpy(st, sin, (size_t)2 * M * (RD + 1) * sizeof(double));",
@@ -47,6 +49,8 @@ PIN_TESTS = [
     pins.test_lambda_zero_is_memoryless,
     pins.test_eta_readout_returns_constant_values,
     pins.test_prefill_from_state_one_position_is_decode_step,
+    pins.test_feature_map_l2_invariants,
+    pins.test_feature_map_l2_flag_reaches_both_feature_maps,
 ]
 
 

@@ -96,6 +96,40 @@ def test_feature_map_squared_norm_invariants():
     np.testing.assert_allclose(cos, 1.0, rtol=1e-13)
 
 
+def test_feature_map_l2_invariants():
+    """The l_2 reading, xi = f / (|f| + eps): parallel to f with |xi| = |f| / (|f| + eps).
+
+    With the squared norm |xi| would be ~1/|f|; without the epsilon or with it under
+    a square root the norm identity breaks at small |f|."""
+    rng = np.random.default_rng(21)
+    s = rng.standard_normal((20, 16)) * 2.0
+    s[3] *= 1e-4  # a row with tiny |f|, where the epsilon placement shows
+    xi = orc.feature_map(s, l2=True)
+    f = s * expit(s)
+    n = np.sqrt((f * f).sum(1))
+    np.testing.assert_allclose(np.linalg.norm(xi, axis=1), n / (n + 1e-6), rtol=1e-12)
+    cos = (xi * f).sum(1) / (np.linalg.norm(xi, axis=1) * n)
+    np.testing.assert_allclose(cos, 1.0, rtol=1e-12)
+
+
+def test_feature_map_l2_flag_reaches_both_feature_maps():
+    """With FEAT_L2 the forward uses the l_2 map for q (the readout scales with it) and for
+    k (only through the RMSNorm epsilon); lambda = 1, B = 1, M = 1 reduces the readout to
+    cumulative sums of those features."""
+    rng = np.random.default_rng(22)
+    N, R, d, W = 25, 4, 3, 3
+    q, k, v, wq, wk, nw, bs = _rand_unit(rng, N, R, d, W)
+    one = np.array([1.0 + 0j])
+    out, _, _ = orc.unit_forward(q, k, v, wq, wk, nw, bs, one, one, flags=orc.FEAT_L2)
+    xq = orc.feature_map(orc.causal_conv(q, wq), l2=True)
+    kt = orc.rmsnorm_affine(orc.feature_map(orc.causal_conv(k, wk), l2=True), nw[:R], bs[:R])
+    vt = orc.rmsnorm_affine(v, nw[R:], bs[R:])
+    ref = (xq * np.cumsum(kt, 0)).sum(1)[:, None] * np.cumsum(vt, 0)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-11)
+    plain, _, _ = orc.unit_forward(q, k, v, wq, wk, nw, bs, one, one)
+    assert np.abs(plain - out).max() > 1e-3 * np.abs(out).max()
+
+
 def test_rmsnorm_unit_mean_square_and_affine():
     """mean(y^2) = ms/(ms+eps) with w=1,b=0; affine applied after the norm."""
     rng = np.random.default_rng(3)
