@@ -70,6 +70,9 @@ enum { IDA_F32 = 0, IDA_BF16 = 1 };            /* dtype of q, k, v and out */
 
 enum {
     IDA_READOUT_ETA = 1,        /* eta-normalised readout instead of denominator-free */
+    IDA_FEAT_L2 = 2,            /* feature map SiLU(s) / (||SiLU(s)||_2 + IDA_EPS_FEAT), the "SiLU/l_2"
+                                   wording of the Chinese summary's introduction, instead of the
+                                   squared norm of the German and Dutch summaries' feature map */
     IDA_PATH_SEQUENTIAL = 256   /* force the token-sequential CUDA-core prefill kernel */
 };
 
@@ -102,7 +105,7 @@ IDA_API size_t ida_state_floats(int d, int R, int M, int W);
  *   out     [B, N, H, d]  dtype; written
  *   final_state  NULL, or [B, H] x ida_state_floats(d, R, M, W) floats:
  *           receives the state after the last position.
- *   flags   IDA_READOUT_ETA and/or IDA_PATH_SEQUENTIAL.
+ *   flags   IDA_READOUT_ETA, IDA_FEAT_L2 and/or IDA_PATH_SEQUENTIAL.
  * N == 0 writes nothing but the zero final_state (if given).
  */
 IDA_API ida_status ida_forward(const void *q, const void *k, const void *v,

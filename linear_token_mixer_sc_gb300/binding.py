@@ -17,6 +17,7 @@ LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libida.so"
 IDA_OK, IDA_ERR_ARG, IDA_ERR_UNSUPPORTED, IDA_ERR_CUDA, IDA_ERR_DEVICE = range(5)
 IDA_F32, IDA_BF16 = 0, 1
 IDA_READOUT_ETA = 1
+IDA_FEAT_L2 = 2
 IDA_PATH_SEQUENTIAL = 256
 
 EXPORTED = ("ida_state_floats", "ida_forward", "ida_forward_ws", "ida_forward_from", "ida_forward_workspace_bytes",

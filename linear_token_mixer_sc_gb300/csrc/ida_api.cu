@@ -75,7 +75,7 @@ ida_status check_shape(int d, int R, int M, int W, int dtype, int flags, std::st
         why = "dtype must be IDA_F32 or IDA_BF16";
         return IDA_ERR_ARG;
     }
-    if (flags & ~(IDA_READOUT_ETA | IDA_PATH_SEQUENTIAL)) {
+    if (flags & ~(IDA_READOUT_ETA | IDA_FEAT_L2 | IDA_PATH_SEQUENTIAL)) {
         why = "unknown flag bits";
         return IDA_ERR_ARG;
     }

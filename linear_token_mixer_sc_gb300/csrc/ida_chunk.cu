@@ -189,8 +189,10 @@ __host__ __device__ inline int plan_state_blocks(const SegPlan &p) {
 }
 
 // FACT selects the Gram formulation; a CTA whose head takes the other one returns at once
-// (the other instantiation, launched on the same plan, runs that piece).
-template <int R, int D, bool FACT>
+// (the other instantiation, launched on the same plan, runs that piece).  EXT compiles in the
+// options that the default call does not use: a given start state (state_in) and the l_2
+// feature map; without it the kernel carries no code for them.
+template <int R, int D, bool FACT, bool EXT>
 __global__ void __launch_bounds__(NTH, 1)
     chunk_prefill_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(NTH, 1)
             const float *xs = seg_start + (size_t)unit * plan_state_blocks(plan) * (size_t)(R + MP) * 128;
             const float2 gu = gblk[mm];
             const float gus = is_im ? gu.y : -gu.y;  // own(g z) = z_own Re g + z_partner s Im g
-            const bool has_in = a.state_in != nullptr;
+            const bool has_in = EXT && a.state_in != nullptr;
             if (has_in) {
                 // X_in in the same layout: U[m][c] of plane tl at column c; Gamma^T (value lane
                 // tl) at column R + 2m (Re) / R + 2m + 1 (Im)
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(NTH, 1)
         // (hsel == 0, Re thread)
         float eta_r = 0.f, eta_i = 0.f;
         if (hsel == 0 && !is_im) {
-            if (a.state_in) {
+            if (EXT && a.state_in) {
                 const float *ein = a.state_in + (size_t)unit * a.state_floats + (size_t)2 * 64 * (R + D);
                 eta_r = ein[mm];
                 eta_i = ein[64 + mm];
@@ -517,7 +519,6 @@ __global__ void __launch_bounds__(NTH, 1)
         }
         int ya_exp = 0;  // scale exponent of my T_A column currently stored
         ci = c_begin;
-
         for (; ci < c_end; ++ci, ++it) {
             const int t0 = ci * CH;
             const int L = min(CH, N - t0);
@@ -529,7 +530,7 @@ __global__ void __launch_bounds__(NTH, 1)
             if (ok) tma_pending = 0;
             tc_fence_after();
             if (__syncthreads_or(!ok)) break;
-            if (ci == 0 && a.state_in) {
+            if (EXT && ci == 0 && a.state_in) {
                 // conv halo of the first chunk: the raw rows before position 0 are the initial
                 // state's tails (the copy zero-filled them)
                 const float *tq = a.state_in + (size_t)unit * a.state_floats + (size_t)2 * 64 * (R + D + 1);
@@ -601,7 +602,11 @@ __global__ void __launch_bounds__(NTH, 1)
                     for (int pp = 0; pp < PPQ; ++pp) {
     #pragma unroll
                         for (int o = 1; o < CBQ; o <<= 1) acc[pp] += __shfl_xor_sync(0xffffffffu, acc[pp], o);
-                        const float inv = (i0 + pp < L) ? __fdividef(1.f, acc[pp] + IDA_EPS_FEAT) : 0.f;
+                        // squared norm, or the l_2 norm (acc rsqrt(acc), zero for a zero row)
+                        const float nrm = (EXT && (a.flags & IDA_FEAT_L2))
+                                              ? (acc[pp] > 0.f ? acc[pp] * rsqrtf(acc[pp]) : 0.f)
+                                              : acc[pp];
+                        const float inv = (i0 + pp < L) ? __fdividef(1.f, nrm + IDA_EPS_FEAT) : 0.f;
     #pragma unroll
                         for (int e = 0; e < 8; ++e) f[pp][e] *= inv;
                     }
@@ -1225,7 +1230,7 @@ __global__ void __launch_bounds__(NTH, 1)
             }
             float *tq = fs + 2 * plane + 2 * M;
             float *tk = tq + (size_t)(W - 1) * R;
-            const float *tin = a.state_in ? a.state_in + (size_t)unit * a.state_floats + (tq - fs) : nullptr;
+            const float *tin = (EXT && a.state_in) ? a.state_in + (size_t)unit * a.state_floats + (tq - fs) : nullptr;
             for (int x = tid; x < (W - 1) * R; x += NTH) {
                 const int r = x / R, c = x % R;
                 const int p = N - (W - 1) + r;  // before position 0: the initial state's tails
@@ -1281,7 +1286,7 @@ struct StateSmem {
     static constexpr int LAUNCH = 116 * 1024;
 };
 
-template <int R, int D>
+template <int R, int D, bool EXT>
 __global__ void __launch_bounds__(NTH, 1)
     chunk_state_kernel(PrefillArgs a, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, SegPlan plan, float *seg_state) {
@@ -1302,6 +1307,7 @@ __global__ void __launch_bounds__(NTH, 1)
     const int c_begin = sgi * plan.fs, c_end = c_begin + plan.fs;
     const uint32_t raw_bytes = (uint32_t)(CH + HALO) * R * 2 + (uint32_t)CH * D * 2;
     const int mm = tl >> 1, is_im = tl & 1;
+    const bool feat_l2 = EXT && (a.flags & IDA_FEAT_L2) != 0;
     const float lam_r = a.lambda[((size_t)h * M + mm) * 2], lam_i = a.lambda[((size_t)h * M + mm) * 2 + 1];
     const float b_r = a.Bvec[((size_t)h * M + mm) * 2], b_i = a.Bvec[((size_t)h * M + mm) * 2 + 1];
     constexpr uint32_t TU = 0, TG = R;  // TMEM columns of U and Gamma^T
@@ -1382,7 +1388,7 @@ __global__ void __launch_bounds__(NTH, 1)
         ok = mbar_wait(&bar[0], par);
         if (ok) tma_pending = 0;
         if (__syncthreads_or(!ok)) break;
-        if (ci == 0 && a.state_in) {
+        if (EXT && ci == 0 && a.state_in) {
             // conv halo of the first chunk: the initial state's key tails (the copy zero-filled them)
             const float *tk = a.state_in + (size_t)unit * a.state_floats + (size_t)2 * 64 * (R + D + 1) +
                               (size_t)(W - 1) * R;
@@ -1434,7 +1440,7 @@ __global__ void __launch_bounds__(NTH, 1)
             }
 #pragma unroll
             for (int o = 1; o < CBQ; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            const float inv = __fdividef(1.f, acc + IDA_EPS_FEAT);
+            const float inv = __fdividef(1.f, (feat_l2 ? sqrtf(acc) : acc) + IDA_EPS_FEAT);
             float ms = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -1594,15 +1600,15 @@ static bool make_map(EncodeTiledFn fn, CUtensorMap *m, const void *ptr, int B, i
     return r == CUDA_SUCCESS;
 }
 
-template <int R, int D>
-static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const CUtensorMap &mq,
-                                   const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
-                                   const SegPlan &plan, float *ws) {
+template <int R, int D, bool EXT>
+static cudaError_t launch_chunk_rd_e(const PrefillArgs &a, cudaStream_t st, const CUtensorMap &mq,
+                                     const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+                                     const SegPlan &plan, float *ws) {
     const unsigned units = (unsigned)(a.B * a.H);
     cudaError_t e;
     if (plan.ppu > 1) {
         using SS = StateSmem<R, D>;
-        auto sk = chunk_state_kernel<R, D>;
+        auto sk = chunk_state_kernel<R, D, EXT>;
         e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::LAUNCH);
         if (e != cudaSuccess) return e;
         sk<<<units * (unsigned)plan_state_blocks(plan), NTH, SS::LAUNCH, st>>>(a, mk, mv, plan, ws);
@@ -1611,8 +1617,8 @@ static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const 
     using S = ChunkSmem<R, D>;
     const unsigned grid = units * (unsigned)plan.ppu;
     // factorised-Gram heads first, then (usually none) the skewed-Gram ones
-    auto kf = chunk_prefill_kernel<R, D, true>;
-    auto ks = chunk_prefill_kernel<R, D, false>;
+    auto kf = chunk_prefill_kernel<R, D, true, EXT>;
+    auto ks = chunk_prefill_kernel<R, D, false, EXT>;
     if ((e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL)) != cudaSuccess)
         return e;
@@ -1620,6 +1626,15 @@ static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const 
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ks<<<grid, NTH, S::TOTAL, st>>>(a, mq, mk, mv, mo, plan, ws);
     return cudaGetLastError();
+}
+
+// The instantiation with the state_in / l_2 code only when the call uses either.
+template <int R, int D>
+static cudaError_t launch_chunk_rd(const PrefillArgs &a, cudaStream_t st, const CUtensorMap &mq,
+                                   const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+                                   const SegPlan &plan, float *ws) {
+    if (a.state_in || (a.flags & IDA_FEAT_L2)) return launch_chunk_rd_e<R, D, true>(a, st, mq, mk, mv, mo, plan, ws);
+    return launch_chunk_rd_e<R, D, false>(a, st, mq, mk, mv, mo, plan, ws);
 }
 
 static bool chunk_path_takes(const PrefillArgs &a) {

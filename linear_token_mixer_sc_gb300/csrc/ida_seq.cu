@@ -84,7 +84,9 @@ __device__ __forceinline__ void seq_prologue(const PrefillArgs &a, int h, size_t
                 ss = fma(f[i], f[i], ss);
             }
         }
-        T inv = T(1) / (warp_sum(ss) + (T)IDA_EPS_FEAT);
+        T nrm = warp_sum(ss);  // squared norm, or its square root for the l_2 reading
+        if (a.flags & IDA_FEAT_L2) nrm = sqrt(nrm);
+        T inv = T(1) / (nrm + (T)IDA_EPS_FEAT);
         if (which == 0) {
 #pragma unroll
             for (int i = 0; i < NC; ++i) {

@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
 
     // ---- helper warps: this warp's positions of a tile are [hlo, hhi) (tile-local)
     const int pw = warp - nwc;
+    const bool feat_l2 = (a.flags & IDA_FEAT_L2) != 0;
     const int hper = (PT + SM_HELP - 1) / SM_HELP;
     const int hlo = min(TT, rank * PT + pw * hper);
     const int hhi = min(TT, min(rank * PT + PT, rank * PT + pw * hper + hper));
@@ -321,8 +322,13 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
                 ssk = fmaf(fk[i], fk[i], ssk);
                 ssv = fmaf(vv[i], vv[i], ssv);
             }
-            const float iq = 1.f / (warp_sum(ssq) + (float)IDA_EPS_FEAT);
-            const float ik = 1.f / (warp_sum(ssk) + (float)IDA_EPS_FEAT);
+            float nq = warp_sum(ssq), nk = warp_sum(ssk);  // squared norms, or l_2 norms
+            if (feat_l2) {
+                nq = sqrtf(nq);
+                nk = sqrtf(nk);
+            }
+            const float iq = 1.f / (nq + (float)IDA_EPS_FEAT);
+            const float ik = 1.f / (nk + (float)IDA_EPS_FEAT);
             float msk = 0.f;
 #pragma unroll
             for (int i = 0; i < CPL; ++i) {

@@ -82,7 +82,7 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(lib, b, N=-1) == binding.IDA_ERR_ARG
     assert _fwd(lib, b, B=-2) == binding.IDA_ERR_ARG
     assert _fwd(lib, b, dtype=7) == binding.IDA_ERR_ARG
-    assert _fwd(lib, b, flags=2) == binding.IDA_ERR_ARG
+    assert _fwd(lib, b, flags=4) == binding.IDA_ERR_ARG  # no such flag bit
     assert _fwd(lib, b, M=0) == binding.IDA_ERR_ARG
     assert "pointer" in binding.ida_last_error() or "must" in binding.ida_last_error()
 

@@ -35,7 +35,8 @@ def _pad_state(st64: np.ndarray, S: int) -> torch.Tensor:
                                    (2, 3, 128, 128, 64, 4, "bf16"), (1, 1, 256, 256, 128, 4, "f32"),
                                    (2, 2, 16, 8, 5, 1, "f32")],
                          ids=lambda s: "B{}H{}d{}R{}M{}W{}{}".format(*s))
-@pytest.mark.parametrize("eta", [0, binding.IDA_READOUT_ETA])
+@pytest.mark.parametrize("eta", [0, binding.IDA_READOUT_ETA, binding.IDA_FEAT_L2,
+                                 binding.IDA_READOUT_ETA | binding.IDA_FEAT_L2])
 def test_decode_from_oracle_state(shape, eta):
     """Decode kernel alone: same fp32 state in, compare out and state over 6 steps."""
     B, H, d, R, M, W, dt = shape

@@ -331,3 +331,38 @@ def test_prefill_from_state_rejects_overlap():
     _, fs = binding.ida_forward(q.to(dev), k.to(dev), v.to(dev), pd, final_state=True)
     with pytest.raises(binding.IdaError, match="overlap"):
         binding.ida_forward(q.to(dev), k.to(dev), v.to(dev), pd, final_state=fs, state_in=fs)
+
+
+# ---- the l_2 reading of the feature map (IDA_FEAT_L2) on every prefill path ------------------
+
+L2 = binding.IDA_FEAT_L2
+# (B, N, H, R, d, M, W, dtype, flags)
+FEAT_L2_CASES = [
+    (2, 200, 3, 64, 64, 64, 4, "bf16", L2),                          # tensor cores, whole sequences
+    (1, 64 * 9 + 5, 2, 128, 128, 64, 4, "bf16", L2),                 # tensor cores, split plan
+    (1, 70, 2, 32, 32, 16, 4, "f32", L2 | ETA),                      # fp64 sequential kernel
+    (2, 90, 2, 128, 128, 64, 4, "bf16", L2 | ETA),                   # register-resident sequential kernel
+    (1, 77, 2, 64, 64, 64, 3, "bf16", L2 | binding.IDA_PATH_SEQUENTIAL),
+]
+
+
+@pytest.mark.parametrize("case", FEAT_L2_CASES, ids=lambda c: "B{}N{}H{}R{}d{}M{}W{}{}f{}".format(*c))
+def test_feature_map_l2(case):
+    B, N, H, R, d, M, W, dt, flags = case
+    q, k, v, p = problem(B, N, H, R, d, M, W, dt, seed=400 + N)
+    dev = torch.device("cuda")
+    pd = binding.params_to_device(p)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out, fs = binding.ida_forward(qd, kd, vd, pd, flags=flags, final_state=True,
+                                  workspace=binding.forward_workspace(qd, vd, pd, flags))
+    torch.cuda.synchronize()
+    assert binding.ida_device_error() == 0
+    oflags = flags & ~binding.IDA_PATH_SEQUENTIAL
+    ref = orc.forward(q, k, v, p, flags=oflags, final_state=True)
+    _check(to_np(out), ref["out"], dt)
+    tol = F32_REL_L2 if dt == "f32" else BF16_REL_L2
+    assert rel_l2(unpadded_state(to_np(fs), d, R, M, W), ref["final_state"]) <= tol
+    # the reading matters: the squared-norm oracle is far from this output (under the eta
+    # readout the scale of xi(q) cancels and only the key RMSNorm epsilon tells them apart)
+    sq = orc.forward(q, k, v, p, flags=oflags & ~L2)
+    assert rel_l2(to_np(out), sq["out"]) > 3 * tol
