@@ -114,3 +114,25 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         binding.load()
+
+
+def _from(lib, b, sin, fs, B=1, H=2, N=8, d=32, R=32, M=16, dtype=0, W=4, flags=0):
+    return lib.ida_forward_from(b.p, b.p, b.p, b.p, b.p, b.p, b.p, b.p, sin, b.p, fs, B, H, N, d, R, M,
+                                dtype, W, flags, None, 0, None)
+
+
+def test_forward_from_rejects_bad_states(lib):
+    """ida_forward_from: a misaligned start state, or one overlapping final_state, is refused
+    before any device work."""
+    S = binding.ida_state_floats(32, 32, 16, 4)
+    mem = np.zeros(4 * 2 * S + 64, dtype=np.float32)
+    base = (mem.ctypes.data + 15) // 16 * 16
+    b = _Bufs()
+    p0 = ctypes.c_void_p(base)
+    assert _from(lib, b, ctypes.c_void_p(base + 4), None) == binding.IDA_ERR_ARG
+    assert "state_in" in binding.ida_last_error()
+    # the same buffer, and a start state ending inside the final state (2 units x S floats each)
+    assert _from(lib, b, p0, p0) == binding.IDA_ERR_ARG
+    assert "overlap" in binding.ida_last_error()
+    assert _from(lib, b, ctypes.c_void_p(base + 16 * ((S * 4) // 16)), p0) == binding.IDA_ERR_ARG
+    assert _from(lib, b, p0, p0, flags=4) == binding.IDA_ERR_ARG  # no such flag bit
