@@ -163,6 +163,10 @@ __device__ __forceinline__ void st_cluster_row(uint32_t a, const float (&x)[CPL]
         st_cluster(a, x[0]);
 }
 
+// SiLU with the hardware exponential and divide (a few ulp; the inputs of this kernel are bf16,
+// rounded at 2^-8, so the feature map's own rounding is far below theirs)
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
 template <int CPL>
 __device__ __forceinline__ void load_bf16_row(const __nv_bfloat16 *p, float (&x)[CPL]) {
     if constexpr (CPL == 4) {
@@ -316,8 +320,8 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
                     sq = fmaf(cwq[i][j], wq[j][i], sq);
                     sk = fmaf(cwk[i][j], wk[j][i], sk);
                 }
-                fq[i] = silu(sq);
-                fk[i] = silu(sk);
+                fq[i] = silu_fast(sq);
+                fk[i] = silu_fast(sk);
                 ssq = fmaf(fq[i], fq[i], ssq);
                 ssk = fmaf(fk[i], fk[i], ssk);
                 ssv = fmaf(vv[i], vv[i], ssv);
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
             }
             if (ETA) {
 #pragma unroll
-                for (int i = 0; i < CPL; ++i) o[i] = o[i] / dn;
+                for (int i = 0; i < CPL; ++i) o[i] = __fdividef(o[i], dn);
             }
             store_bf16_row<CPL>(reinterpret_cast<__nv_bfloat16 *>(a.out) + base + (size_t)t * row_qk + CPL * lane, o);
         }
