@@ -408,7 +408,7 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e
            "roofline": roofline(runner, ms, peaks, peak_kind,
                                 traffic_record(w.name + (":eta" if flags & 1 else "") +
                                                (":from_state" if from_state else ""), sources),
-                                kernel_bound="alu" if flags & 1 else None),
+                                kernel_bound="alu" if (flags & 1 and not w.decode_steps) else None),
            "gpu_launches": runner.launches_per_step * steps}
     if e2e:
         et = time_steps(runner, max(3, steps // 2), 2, dev, False, e2e=True)
@@ -443,8 +443,10 @@ def main():
     cores = os.cpu_count() or 1
     config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "R": w.R, "d": w.d, "M": w.M,
               "W": w.W, "readout": "eta" if args.eta else "denominator-free",
-              "start": "from a given state" if args.from_state else "zero state",
+
               "parallelism": f"replicas x{ws} (independent (b,h) units, no collective)"}
+    if not w.decode_steps:
+        config["start"] = "from a given state" if args.from_state else "zero state"
 
     if args.impl == "reference":
         if rank != 0:

@@ -93,9 +93,11 @@ def test_prefill_then_decode_chain_tiny():
     assert rel_l2(got_st, st_ref) <= F32_REL_L2
 
 
-def test_decode_full_workload_sampled():
+@pytest.mark.parametrize("eta", [0, binding.IDA_READOUT_ETA])
+def test_decode_full_workload_sampled(eta):
     """Batch 256 x 16 heads: GPU prefill of 4096 positions, then 512 GPU decode
-    steps; sampled units checked step by step against the oracle."""
+    steps (denominator-free or eta readout; the state is the same either way);
+    sampled units checked step by step against the oracle."""
     w = configs.DECODE
     dev = torch.device("cuda")
     p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
@@ -118,11 +120,11 @@ def test_decode_full_workload_sampled():
     sq = {u: [] for u in units}
     for step in range(w.decode_steps):
         qt, kt, vt = inputs.make_tokens(w.B, w.H, w.R, w.d, w.dtype, w.seed, step, device=dev)
-        out = binding.ida_decode_step(qt, kt, vt, pd, st)
+        out = binding.ida_decode_step(qt, kt, vt, pd, st, flags=eta)
         o = to_np(out)
         for (b, h) in units:
             r = orc.decode_step(qt[b:b + 1, h:h + 1].cpu(), kt[b:b + 1, h:h + 1].cpu(),
-                                vt[b:b + 1, h:h + 1].cpu(), hp[(b, h)], ref_states[(b, h)])
+                                vt[b:b + 1, h:h + 1].cpu(), hp[(b, h)], ref_states[(b, h)], flags=eta)
             diff = o[b, h] - r["out"][0, 0]
             errs[(b, h)].append(float(diff @ diff))
             sq[(b, h)].append(float(r["out"][0, 0] @ r["out"][0, 0]))

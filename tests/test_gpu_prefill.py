@@ -366,3 +366,16 @@ def test_feature_map_l2(case):
     # readout the scale of xi(q) cancels and only the key RMSNorm epsilon tells them apart)
     sq = orc.forward(q, k, v, p, flags=oflags & ~L2)
     assert rel_l2(to_np(out), sq["out"]) > 3 * tol
+
+
+def test_eta_prefill_is_deterministic():
+    """The register-resident sequential kernel sums its partial readouts in a fixed order:
+    repeated calls give the same bits."""
+    q, k, v, p = problem(2, 300, 4, 128, 128, 64, 4, "bf16", seed=41)
+    dev = torch.device("cuda")
+    pd = binding.params_to_device(p)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    outs = [binding.ida_forward(qd, kd, vd, pd, flags=ETA)[0] for _ in range(4)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
