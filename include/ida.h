@@ -205,7 +205,10 @@ IDA_API ida_status ida_forward_noalloc(const void *q, const void *k, const void 
  *   q, k [B, H, R], v [B, H, d] in dtype; parameters as for ida_forward;
  *   state_inout [B, H] x ida_state_floats(...) floats, read and updated in
  *   place (state, eta and the conv tails); out [B, H, d] in dtype.
- * A prefill's final_state is a valid state_inout.
+ *   flags: IDA_READOUT_ETA and/or IDA_FEAT_L2 (IDA_PATH_SEQUENTIAL is
+ *   accepted and has no effect: a step is always one position).
+ * A prefill's final_state is a valid state_inout; use the same IDA_FEAT_L2
+ * setting for the prefill and the steps that continue it.
  */
 IDA_API ida_status ida_decode_step(const void *q, const void *k, const void *v,
                            const float *conv_w, const float *norm_w,
