@@ -4,15 +4,18 @@
 
 One step is one pass of the mixer over one batch of synthetic input: a
 prefill (``ida_forward``) for the prefill workloads, one ``ida_decode_step``
-over the whole batch for the decode workload.  The default workload is the
-125M-like prefill (B=8, H=12, N=2048, R=d=64, M=64, bf16); the JSON line also
-carries a ``decode`` object measured in the same run on the recurrent decode
-workload (batch 256, H=16, R=d=128, M=64, state seeded by a 4096-position
-prefill).
+over the whole batch for the decode workload.  The headline workload is the
+largest single-GPU one, the 1.3B-like prefill at training context (B=4, H=16,
+N=4096, R=d=128, M=64, bf16, denominator-free readout).  The same JSON line
+carries, under ``workloads``, every other workload measured in the same run,
+each with its own clocks and roofline: the tiny fp32 check, the 125M-like
+prefill, the 1.3B-like prefill with the eta readout, the 14K-position prefill
+returning its final state, and the recurrent decode step (batch 256, H=16,
+state seeded by a 4096-position prefill).
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
 on the launching stream; between timed steps the L2 is flushed (a 512 MB
-write) when the step's inputs fit in L2.  ``value`` is whole-job tokens/s
+write outside the timed region).  ``value`` is whole-job tokens/s
 (a token is one position of one batch row, through all H heads).
 ``--impl reference`` times the CPU oracle instead (bounded sample per step).
 """
@@ -67,15 +70,17 @@ def sources_sha(names) -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_record(workload: str, names):
-    """DRAM bytes per launch from the committed ncu summary, if still current."""
+def traffic_record(key: str, names):
+    """DRAM bytes of one step (every launch of the step) from the committed ncu
+    record, if the kernels' sources still hash to the profiled version; also the
+    per-kernel figures it sums."""
     p = ROOT / "profiles" / "traffic.json"
     if not p.exists():
-        return None
-    rec = json.loads(p.read_text()).get(workload)
+        return None, None
+    rec = json.loads(p.read_text()).get(key)
     if not rec or rec.get("source_sha") != sources_sha(names):
-        return None
-    return rec.get("dram_bytes_per_launch")
+        return None, None
+    return rec.get("step_bytes"), rec.get("kernels")
 
 
 def elem_bytes(dtype: str) -> int:
@@ -101,6 +106,12 @@ def decode_bytes(w) -> int:
     """One decode step: state read + write, q, k, v read, out written."""
     s = elem_bytes(w.dtype)
     return w.B * w.H * (2 * state_floats(w) * 4 + (2 * w.R + w.d) * s + w.d * s)
+
+
+def l2_note(w) -> str:
+    """Every workload flushes the L2 between timed steps (a 512 MB write outside the
+    timed region), whether or not its inputs exceed the L2."""
+    return "flushed between timed steps"
 
 
 def mixer_flops(w, positions: int) -> float:
@@ -181,7 +192,7 @@ class Prefill:
         self.in_bytes = sum(t.numel() * t.element_size() for t in self.host)
         # tensor-core path: readout kernels for the factorised- and the skewed-Gram heads, plus the
         # block state pass when split; the eta readout runs one sequential kernel
-        if flags & binding.IDA_READOUT_ETA:
+        if flags & binding.IDA_READOUT_ETA or w.dtype == "f32":
             self.launches_per_step = 1
         else:
             self.launches_per_step = 2 if self.ws is None else 3
@@ -214,9 +225,6 @@ class Prefill:
 
     def flops(self):
         return mixer_flops(self.w, self.w.B * self.w.H * self.w.N)
-
-    def resident_bytes(self):
-        return self.in_bytes + self.out.numel() * self.out.element_size()
 
 
 class Decode:
@@ -269,9 +277,6 @@ class Decode:
     def flops(self):
         return mixer_flops(self.w, self.w.B * self.w.H)
 
-    def resident_bytes(self):
-        return self.state.numel() * 4
-
 
 def time_steps(runner, steps, warmup, dev, flush, e2e=False):
     """Per-step CUDA-event times (ms) on the launching stream."""
@@ -293,27 +298,34 @@ def time_steps(runner, steps, warmup, dev, flush, e2e=False):
     return [s.elapsed_time(e) for s, e in evs]
 
 
-def roofline(runner, ms_avg, peaks, peak_kind, traffic, kernel_bound=None):
+def roofline(runner, ms_avg, peaks, peak_kind, traffic, fp32_fma=False):
+    """The roofline record of one step: the slower of the algorithmic bytes at the
+    measured HBM bandwidth and the algorithmic flops at the measured dense bf16
+    tensor peak decides the bound; achieved = that quantity / the event-timed step.
+    With ``fp32_fma`` (a path that computes on the CUDA cores in fp32 by design) the
+    same flops are also set against the nominal fp32 FMA peak, as an extra field."""
     alg_b = runner.alg_bytes()
     fl = runner.flops()
     t_b = alg_b / (peaks["hbm_gbs"] * 1e9)
     t_f = fl / (peaks["bf16_tflops"] * 1e12)
-    bound = kernel_bound or ("hbm" if t_b >= t_f else "tensor")
-    if bound == "alu":  # fp32 CUDA-core arithmetic (eta readout): algorithmic flops at the FMA peak
-        ach = fl / (ms_avg * 1e-3) / 1e12
-        return {"bound": "alu", "achieved": round(ach, 2), "peak": round(FP32_TFLOPS_NOMINAL, 1),
-                "unit": "TFLOP/s", "frac": round(ach / FP32_TFLOPS_NOMINAL, 4), "traffic": traffic,
-                "algorithmic_flops": fl,
-                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x 2.07 GHz (nominal unit counts)"}
-    if bound == "hbm":
+    if t_b >= t_f:
         ach = alg_b / (ms_avg * 1e-3) / 1e9
-        return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "algorithmic_bytes": alg_b, "peak_source": f"hbm_gbs ({peak_kind})"}
-    ach = fl / (ms_avg * 1e-3) / 1e12
-    return {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
-            "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
-            "algorithmic_flops": fl, "peak_source": f"bf16_tflops ({peak_kind})"}
+        rec = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+               "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
+               "algorithmic_bytes": alg_b, "peak_source": f"hbm_gbs ({peak_kind})"}
+    else:
+        ach = fl / (ms_avg * 1e-3) / 1e12
+        rec = {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
+               "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
+               "algorithmic_flops": fl, "peak_source": f"bf16_tflops ({peak_kind})"}
+    rec["bound_ms"] = round(1e3 * max(t_b, t_f), 5)
+    if fp32_fma:
+        a32 = fl / (ms_avg * 1e-3) / 1e12
+        rec["fp32_fma"] = {"achieved": round(a32, 2), "peak": round(FP32_TFLOPS_NOMINAL, 1),
+                           "unit": "TFLOP/s", "frac": round(a32 / FP32_TFLOPS_NOMINAL, 4),
+                           "algorithmic_flops": fl,
+                           "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x 2.07 GHz (nominal)"}
+    return rec
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -387,29 +399,56 @@ def job_value(world_size: int, tokens_per_rank: int, ms_max: float) -> float:
     return world_size * tokens_per_rank / (ms_max * 1e-3)
 
 
-def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e2e=True, seed_len=None,
+def line_key(w, flags=0, from_state=False) -> str:
+    """Name of a measured line: the workload, with the readout and start noted."""
+    return w.name + ("_eta" if flags & 1 else "") + ("_from_state" if from_state else "")
+
+
+def sources_of(w, flags) -> list:
+    if w.decode_steps:
+        return DECODE_SOURCES
+    if flags & 1 or w.dtype == "f32":
+        return ETA_SOURCES
+    return PREFILL_SOURCES
+
+
+def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, seed_len=None,
             from_state=False):
     runner = Decode(w, dev, flags, seed_len) if w.decode_steps else Prefill(w, dev, flags, from_state)
-    flush = runner.resident_bytes() < 2 * L2_BYTES
+    flush = True
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
     wall0 = time.perf_counter()
     times = time_steps(runner, steps, warmup, dev, flush)
     torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
     if dist is not None:
         dist.barrier()
-    wall = time.perf_counter() - wall0
     ms = sum(times) / len(times)
     ms_all = max_over_ranks(dist, ms, dev)
     value = job_value(ws, runner.tokens(), ms_all)
-    res = {"value": value, "ms_per_step": ms_all, "tokens_per_step": runner.tokens(),
-           "flush_l2": flush, "wall_s": wall,
-           "roofline": roofline(runner, ms, peaks, peak_kind,
-                                traffic_record(w.name + (":eta" if flags & 1 else "") +
-                                               (":from_state" if from_state else ""), sources),
-                                kernel_bound="alu" if (flags & 1 and not w.decode_steps) else None),
-           "gpu_launches": runner.launches_per_step * steps}
+    key = line_key(w, flags, from_state)
+    traffic, per_kernel = traffic_record(key, sources_of(w, flags))
+    rl = roofline(runner, ms, peaks, peak_kind, traffic,
+                  fp32_fma=bool(flags & 1 and not w.decode_steps) or w.dtype == "f32")
+    if per_kernel:
+        rl["traffic_kernels"] = per_kernel
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "R": w.R, "d": w.d, "M": w.M, "W": w.W,
+           "dtype": w.dtype, "readout": "eta" if flags & 1 else "denominator-free",
+           "l2": l2_note(w)}
+    if w.decode_steps:
+        cfg["seed_prefill_N"] = w.N if seed_len is None else seed_len
+        del cfg["N"]
+    else:
+        cfg["start"] = "from a given state" if from_state else "zero state"
+        cfg["final_state"] = bool(w.final_state)
+    res = {"value": value, "unit": "tokens/s", "ms_per_step": ms_all, "steps": steps,
+           "tokens_per_step": runner.tokens(), "wall_s": wall, "roofline": rl,
+           "gpu_launches": runner.launches_per_step * steps, "clocks": clocks, "config": cfg}
     if e2e:
         et = time_steps(runner, max(3, steps // 2), 2, dev, False, e2e=True)
         ems = max_over_ranks(dist, sum(et) / len(et), dev)
@@ -417,7 +456,15 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, sources, e
         res["e2e"] = {"value": job_value(ws, runner.tokens(), ems), "unit": "tokens/s",
                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                       "ms_per_step": ems}
+    del runner
+    torch.cuda.empty_cache()
     return res
+
+
+# The other workloads measured beside the headline one, in the same JSON line:
+# (workload, flags).  Flag 1 is the eta readout.
+SECONDARY = [(configs.TINY_F32, 0), (configs.PREFILL_125M, 0), (configs.PREFILL_1P3B, 1),
+             (configs.PREFILL_14K, 0), (configs.DECODE, 0)]
 
 
 def main():
@@ -426,11 +473,12 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=configs.PREFILL_125M.name, choices=sorted(configs.ALL))
+    ap.add_argument("--workload", default=configs.PREFILL_1P3B.name, choices=sorted(configs.ALL))
     ap.add_argument("--eta", action="store_true", help="eta-normalised readout")
     ap.add_argument("--from-state", action="store_true",
                     help="prefill continuing from a given state (ida_forward_from)")
-    ap.add_argument("--no-decode", action="store_true", help="skip the secondary decode line")
+    ap.add_argument("--only", "--no-decode", dest="only", action="store_true",
+                    help="measure the selected workload alone (no secondary lines)")
     ap.add_argument("--seed-len", type=int, default=None,
                     help="decode workload: length of the seeding prefill (default: the workload's 4096)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
@@ -438,15 +486,15 @@ def main():
     args = ap.parse_args()
     w = configs.ALL[args.workload]
     flags = 1 if args.eta else 0
+    from_state = args.from_state and not w.decode_steps
 
     dist, rank, ws, lr = dist_setup(args.gpus)
     cores = os.cpu_count() or 1
     config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "R": w.R, "d": w.d, "M": w.M,
               "W": w.W, "readout": "eta" if args.eta else "denominator-free",
-
               "parallelism": f"replicas x{ws} (independent (b,h) units, no collective)"}
     if not w.decode_steps:
-        config["start"] = "from a given state" if args.from_state else "zero state"
+        config["start"] = "from a given state" if from_state else "zero state"
 
     if args.impl == "reference":
         if rank != 0:
@@ -459,6 +507,7 @@ def main():
                 vals.append(v)
                 spent += dt
         value = sum(vals) / len(vals)
+        config["l2"] = l2_note(w)
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * spent / max(1, len(vals)), "higher_is_better": True,
@@ -482,22 +531,18 @@ def main():
     binding.load()
     peaks, peak_kind = load_peaks()
 
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    sampler.start()
     main_res = measure(w, dev, args.steps, args.warmup, flags, dist, ws, peaks, peak_kind,
-                       DECODE_SOURCES if w.decode_steps else (ETA_SOURCES if flags else PREFILL_SOURCES),
-                       seed_len=args.seed_len, from_state=args.from_state and not w.decode_steps)
-    clocks = sampler.stop()
-    decode_res = None
-    if not w.decode_steps and not args.no_decode:
-        dw = configs.DECODE
-        sampler2 = ClockSampler(dev.index if dev.index is not None else 0)
-        sampler2.start()
-        decode_res = measure(dw, dev, max(args.steps, 64), args.warmup, 0, dist, ws, peaks,
-                             peak_kind, DECODE_SOURCES, e2e=True, seed_len=args.seed_len)
-        decode_res["clocks"] = sampler2.stop()
-        decode_res["config"] = {"workload": dw.name, "B": dw.B, "H": dw.H, "R": dw.R, "d": dw.d,
-                                "M": dw.M, "seed_prefill_N": dw.N}
+                       seed_len=args.seed_len, from_state=from_state)
+    others = {}
+    if not args.only:
+        for ow, of in SECONDARY:
+            if (ow.name, of) == (w.name, flags) and not from_state:
+                continue
+            steps = max(args.steps, 64) if ow.decode_steps else args.steps
+            r = measure(ow, dev, steps, args.warmup, of, dist, ws, peaks, peak_kind,
+                        seed_len=args.seed_len)
+            others[line_key(ow, of)] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps", "roofline",
+                                                          "e2e", "gpu_launches", "clocks", "config")}
     if binding.ida_device_error() != 0:
         raise RuntimeError("a kernel reported a device error")
 
@@ -508,18 +553,16 @@ def main():
         cv, desc, _ = oracle_sample(w, args.cpu_budget, cores, flags)
         cpu = {"value": cv, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
                "host": f"{platform.machine()} x{cores}"}
-    config["l2"] = ("flushed between timed steps" if main_res["flush_l2"]
-                    else "inputs larger than L2")
+    config["l2"] = l2_note(w)
     line = {"metric": METRIC, "value": main_res["value"], "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": main_res["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded; shapes of the pages' workloads)",
             "config": config, "roofline": main_res["roofline"], "cpu_baseline": cpu,
-            "e2e": main_res["e2e"], "gpu_launches": main_res["gpu_launches"], "clocks": clocks}
-    if decode_res is not None:
-        line["decode"] = {k: decode_res[k] for k in ("value", "ms_per_step", "roofline", "e2e",
-                                                     "gpu_launches", "clocks", "config")}
-        line["decode"]["unit"] = "tokens/s"
+            "e2e": main_res["e2e"], "gpu_launches": main_res["gpu_launches"],
+            "clocks": main_res["clocks"]}
+    if others:
+        line["workloads"] = others
     print(json.dumps(line))
 
 

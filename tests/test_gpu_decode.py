@@ -3,7 +3,7 @@
 The decode kernel is checked on its own (starting from the oracle's state
 rounded to fp32), chained after a GPU prefill, and at the full recurrent
 decode workload (batch 256, 16 heads, R = d = 128, M = 64: a 4096-position
-prefill then 512 steps) on sampled (b,h) units.
+prefill then 512 steps) on 64 (b,h) units spread over the batch.
 """
 import numpy as np
 import pytest
@@ -11,7 +11,7 @@ import torch
 
 from linear_token_mixer_sc_gb300 import binding, build, configs, inputs
 from oracle import ida_oracle as orc
-from tests.helpers import (BF16_REL_L2, F32_MAX_ABS, F32_REL_L2, head_params,
+from tests.helpers import (BF16_REL_L2, F32_MAX_ABS, F32_REL_L2,
                            max_abs_beyond_rounding, problem,
                            rel_l2, to_np, unpadded_state)
 
@@ -97,38 +97,32 @@ def test_prefill_then_decode_chain_tiny():
 def test_decode_full_workload_sampled(eta):
     """Batch 256 x 16 heads: GPU prefill of 4096 positions, then 512 GPU decode
     steps (denominator-free or eta readout; the state is the same either way);
-    sampled units checked step by step against the oracle."""
+    64 units (every head of four batch rows spread over the batch) checked step by
+    step against the oracle, one rel-L2 over all of their outputs."""
     w = configs.DECODE
     dev = torch.device("cuda")
     p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
     pd = binding.params_to_device(p)
     q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed, device=dev)
     _, st = binding.ida_forward(q, k, v, pd, final_state=True)
-    units = [(0, 0), (77, 5), (255, 15)]
-    ref_states, hp = {}, {}
-    for (b, h) in units:
-        hp[(b, h)] = head_params(p, h)
-        r = orc.forward(q[b:b + 1, :, h:h + 1].cpu(), k[b:b + 1, :, h:h + 1].cpu(),
-                        v[b:b + 1, :, h:h + 1].cpu(), hp[(b, h)], final_state=True)
-        ref_states[(b, h)] = r["final_state"]
+    rows = [0, 77, 170, 255]
+    r = orc.forward(q[rows].cpu(), k[rows].cpu(), v[rows].cpu(), p, final_state=True)
+    ref_state = r["final_state"]
     del q, k, v
     torch.cuda.synchronize()
-    for (b, h) in units:
-        got = unpadded_state(to_np(st[b, h]), w.d, w.R, w.M, w.W)
-        assert rel_l2(got, ref_states[(b, h)][0, 0]) <= BF16_REL_L2
-    errs = {u: [] for u in units}
-    sq = {u: [] for u in units}
+    got = unpadded_state(to_np(st[rows]), w.d, w.R, w.M, w.W)
+    assert rel_l2(got, ref_state) <= BF16_REL_L2
+    err = np.zeros((len(rows), w.H))
+    sq = np.zeros((len(rows), w.H))
     for step in range(w.decode_steps):
         qt, kt, vt = inputs.make_tokens(w.B, w.H, w.R, w.d, w.dtype, w.seed, step, device=dev)
         out = binding.ida_decode_step(qt, kt, vt, pd, st, flags=eta)
-        o = to_np(out)
-        for (b, h) in units:
-            r = orc.decode_step(qt[b:b + 1, h:h + 1].cpu(), kt[b:b + 1, h:h + 1].cpu(),
-                                vt[b:b + 1, h:h + 1].cpu(), hp[(b, h)], ref_states[(b, h)], flags=eta)
-            diff = o[b, h] - r["out"][0, 0]
-            errs[(b, h)].append(float(diff @ diff))
-            sq[(b, h)].append(float(r["out"][0, 0] @ r["out"][0, 0]))
+        o = to_np(out)[rows]
+        ro = orc.decode_step(qt[rows].cpu(), kt[rows].cpu(), vt[rows].cpu(), p, ref_state, flags=eta)["out"]
+        err += ((o - ro) ** 2).sum(-1)
+        sq += (ro ** 2).sum(-1)
     assert binding.ida_device_error() == 0
-    for u in units:
-        rl = (sum(errs[u]) / sum(sq[u])) ** 0.5
-        assert rl <= BF16_REL_L2, (u, rl)
+    total = (err.sum() / sq.sum()) ** 0.5
+    per_unit = np.sqrt(err / sq)
+    worst = np.unravel_index(np.argmax(per_unit), per_unit.shape)
+    assert total <= BF16_REL_L2, (total, (rows[worst[0]], worst[1]), per_unit.max())
