@@ -15,7 +15,7 @@ state seeded by a 4096-position prefill).
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
 on the launching stream; between timed steps the L2 is flushed (a 512 MB
-write outside the timed region).  ``value`` is whole-job tokens/s
+write and read-back outside the timed region).  ``value`` is whole-job tokens/s
 (a token is one position of one batch row, through all H heads).
 ``--impl reference`` times the CPU oracle instead (bounded sample per step).
 """
@@ -109,8 +109,8 @@ def decode_bytes(w) -> int:
 
 
 def l2_note(w) -> str:
-    """Every workload flushes the L2 between timed steps (a 512 MB write outside the
-    timed region), whether or not its inputs exceed the L2."""
+    """Every workload flushes the L2 between timed steps (a 512 MB write and read-back
+    outside the timed region), whether or not its inputs exceed the L2."""
     return "flushed between timed steps"
 
 
@@ -122,37 +122,58 @@ def mixer_flops(w, positions: int) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling around the timed region: started (and its
+    first sample awaited) before the warm-up, stopped after one more sample once the
+    timed steps are done, so the samples bracket the timed region."""
 
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, device_index: int):
         self.proc = None
         self.idx = device_index
+        self.lines = []
+        self.thread = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
+
+    def _wait_for(self, n, timeout_s):
+        t0 = time.perf_counter()
+        while len(self.lines) < n and time.perf_counter() - t0 < timeout_s:
+            time.sleep(0.005)
 
     def start(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-i", str(self.idx), "-lms", "100"],
+                 "-i", str(self.idx), "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        self._wait_for(1, 3.0)
 
     def stop(self):
         if self.proc is None:
             return None
+        self._wait_for(len(self.lines) + 1, 1.0)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
+        for line in self.lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 7:
                 continue
@@ -278,11 +299,18 @@ class Decode:
         return mixer_flops(self.w, self.w.B * self.w.H)
 
 
-def time_steps(runner, steps, warmup, dev, flush, e2e=False):
-    """Per-step CUDA-event times (ms) on the launching stream."""
+def time_steps(runner, steps, warmup, dev, flush, e2e=False, sampler=None):
+    """Per-step CUDA-event times (ms) on the launching stream.  With ``flush`` the L2
+    is flushed before every timed step, outside the timed region, by writing a 512 MB
+    buffer and then reading it back: the write evicts the step's inputs, the read
+    evicts the write's own dirty lines (their write-back happens there), so the timed
+    step neither finds its inputs in L2 nor pays for another buffer's write-back."""
     stream = torch.cuda.current_stream(dev)
     fn = runner.step_e2e if e2e else runner.step
-    scratch = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    scratch = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    if sampler is not None:
+        sampler.start()
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize(dev)
@@ -291,11 +319,13 @@ def time_steps(runner, steps, warmup, dev, flush, e2e=False):
     for s, e in evs:
         if scratch is not None:
             scratch.fill_(1.0)
+            torch.sum(scratch, dim=0, out=sink)
         s.record(stream)
         fn()
         e.record(stream)
     torch.cuda.synchronize(dev)
-    return [s.elapsed_time(e) for s, e in evs]
+    clocks = sampler.stop() if sampler is not None else None
+    return [s.elapsed_time(e) for s, e in evs], clocks
 
 
 def roofline(runner, ms_avg, peaks, peak_kind, traffic, fp32_fma=False):
@@ -420,12 +450,10 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, 
         dist.barrier()
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    sampler.start()
     wall0 = time.perf_counter()
-    times = time_steps(runner, steps, warmup, dev, flush)
+    times, clocks = time_steps(runner, steps, warmup, dev, flush, sampler=sampler)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
-    clocks = sampler.stop()
     if dist is not None:
         dist.barrier()
     ms = sum(times) / len(times)
@@ -450,7 +478,7 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, 
            "tokens_per_step": runner.tokens(), "wall_s": wall, "roofline": rl,
            "gpu_launches": runner.launches_per_step * steps, "clocks": clocks, "config": cfg}
     if e2e:
-        et = time_steps(runner, max(3, steps // 2), 2, dev, False, e2e=True)
+        et, _ = time_steps(runner, max(3, steps // 2), 2, dev, False, e2e=True)
         ems = max_over_ranks(dist, sum(et) / len(et), dev)
         bi, bo = runner.e2e_bytes()
         res["e2e"] = {"value": job_value(ws, runner.tokens(), ems), "unit": "tokens/s",

@@ -176,19 +176,28 @@ IDA_API size_t ida_forward_workspace_bytes(int B, int H, int N, int d, int R,
  * counterpart: this is a property of the library, not of the method.)
  *
  * Same arguments and results as ida_forward; it runs what ida_forward_ws
- * runs with a sufficient workspace, but takes that workspace from one array
- * of static device memory built into this library instead of from the
- * caller.  Use it where the calling code may not allocate: a plug-in that a
- * host framework hands only its input and output buffers, a serving loop
- * that must not touch the allocator after start-up, code with no allocator
- * in reach.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ * runs with a workspace, but takes that workspace from one array of static
+ * device memory built into this library instead of from the caller.  Use it
+ * where the calling code may not allocate: a plug-in that a host framework
+ * hands only its input and output buffers, a serving loop that must not
+ * touch the allocator after start-up, code with no allocator in reach.
+ *   - It calls no cudaMalloc, cudaFree or other device-memory allocator.
+ *     One thing is set up once per process by whichever entry point runs
+ *     first (this one included): a pinned, mapped host word (cudaHostAlloc,
+ *     4 bytes) where kernels report device-side errors.  A caller that may
+ *     not do even that makes any other prefill or decode call first.
  *   - Limit: the array holds 32 MiB on every GPU that loads the library,
- *     kept until the process exits.  A shape whose scratch need
- *     (ida_forward_workspace_bytes) exceeds it returns IDA_ERR_UNSUPPORTED
- *     with the sizes in ida_last_error().
+ *     kept until the process exits.  Every supported shape runs: sequences
+ *     are split across SMs only as finely as 32 MiB of segment states allow
+ *     (ida_forward_ws with a larger workspace may split more finely; with a
+ *     workspace of ida_forward_workspace_bytes(...) <= 32 MiB both run the
+ *     same plan and give the same bytes).
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current and keeps it for the
+ *     process; make that first call before any stream capture.  A
+ *     cudaDeviceReset (or anything else that tears down the device's primary
+ *     context) invalidates the kept address: do not call this entry point on
+ *     that device afterwards.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; nothing in it needs to start at zero, but calls that overlap
  *     on the GPU (e.g. on two streams) race on it.
@@ -201,7 +210,11 @@ IDA_API ida_status ida_forward_noalloc(const void *q, const void *k, const void 
                                int dtype, int W, int flags, ida_stream_t stream);
 
 /*
- * One recurrent decode step (one new position per (b,h) unit).
+ * One recurrent decode step (one new position per (b,h) unit): the fixed-size
+ * state is updated in O(1) work per position, independent of the number of
+ * positions before it ("Interdomain Attention: Beyond Token-Level Key-Value
+ * Memory", translated paper text, section 1, on constant-cost recurrent
+ * inference; German technical summary, "Problemstellung").
  *   q, k [B, H, R], v [B, H, d] in dtype; parameters as for ida_forward;
  *   state_inout [B, H] x ida_state_floats(...) floats, read and updated in
  *   place (state, eta and the conv tails); out [B, H, d] in dtype.
@@ -216,6 +229,19 @@ IDA_API ida_status ida_decode_step(const void *q, const void *k, const void *v,
                            const float *Bvec, float *state_inout, void *out,
                            int B, int H, int d, int R, int M, int dtype,
                            int W, int flags, ida_stream_t stream);
+
+/*
+ * Self-test of the failure reporting (no counterpart in the paper: a property
+ * of the library).  Launches one warp on `stream` that waits, through the
+ * bounded-wait helper every prefill kernel uses, on an mbarrier nothing
+ * arrives on; after about limit_cycles SM clock cycles (1 .. 4e9) the wait
+ * gives up and the kernel records the wait-timeout code (1) in the device
+ * error word and returns.  The GPU and the context stay usable: the next
+ * call returns IDA_ERR_DEVICE, or ida_device_error() reports and clears the
+ * word, once the stream has reached the kernel.  Allocates nothing beyond the
+ * once-per-process error word.
+ */
+IDA_API ida_status ida_selftest_bounded_wait(long long limit_cycles, ida_stream_t stream);
 
 /* Reads and clears the device error word without synchronising; returns
  * IDA_OK or IDA_ERR_DEVICE.  *code (nullable) receives the raw word. */

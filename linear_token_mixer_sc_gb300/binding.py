@@ -22,7 +22,7 @@ IDA_PATH_SEQUENTIAL = 256
 
 EXPORTED = ("ida_state_floats", "ida_forward", "ida_forward_ws", "ida_forward_from", "ida_forward_workspace_bytes",
             "ida_forward_noalloc", "ida_decode_step", "ida_device_error", "ida_status_str",
-            "ida_last_error")
+            "ida_last_error", "ida_selftest_bounded_wait")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +63,8 @@ def load() -> ctypes.CDLL:
             L.ida_decode_step.restype = _i
             L.ida_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _fp, _vp,
                                           _i, _i, _i, _i, _i, _i, _i, _i, _vp]
+            L.ida_selftest_bounded_wait.restype = _i
+            L.ida_selftest_bounded_wait.argtypes = [ctypes.c_longlong, _vp]
             L.ida_device_error.restype = _i
             L.ida_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
             L.ida_status_str.restype = ctypes.c_char_p
@@ -245,6 +247,12 @@ def ida_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: d
                                 _stream_handle(stream))
     _check(st, "ida_decode_step")
     return out
+
+
+def ida_selftest_bounded_wait(limit_cycles: int, stream=None) -> None:
+    """Launch the library's bounded-wait self-test (a wait that runs out on purpose)."""
+    _check(load().ida_selftest_bounded_wait(int(limit_cycles), _stream_handle(stream)),
+           "ida_selftest_bounded_wait")
 
 
 def params_to_device(p: dict, device="cuda") -> dict:

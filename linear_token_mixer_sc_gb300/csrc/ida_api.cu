@@ -34,7 +34,8 @@ ida_status fail(ida_status s, const std::string &why) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-ida_status device_setup(int *num_sms, std::string &why) {
+// The host-mapped error word, set up once per process.
+ida_status ensure_error_word(std::string &why) {
     std::call_once(g_err_once, [] {
         void *h = nullptr;
         g_err_init = cudaHostAlloc(&h, sizeof(unsigned), cudaHostAllocMapped);
@@ -50,6 +51,12 @@ ida_status device_setup(int *num_sms, std::string &why) {
         why = std::string("device error word setup: ") + cudaGetErrorString(g_err_init);
         return IDA_ERR_CUDA;
     }
+    return IDA_OK;
+}
+
+ida_status device_setup(int *num_sms, std::string &why) {
+    ida_status s = ensure_error_word(why);
+    if (s != IDA_OK) return s;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -95,6 +102,12 @@ ida_status forward_entry(const void *q, const void *k, const void *v, const floa
                          float *final_state, int B, int H, int N, int d, int R, int M, int dtype, int W, int flags,
                          void *workspace, size_t workspace_bytes, ida_stream_t stream);
 ida_status fail_with(ida_status s, const std::string &why) { return fail(s, why); }
+// The device address of the error word (set up on first use), without reading it.
+ida_status device_error_word(unsigned **err, std::string &why) {
+    ida_status s = ensure_error_word(why);
+    *err = s == IDA_OK ? g_err_dev : nullptr;
+    return s;
+}
 }  // namespace ida
 
 extern "C" {

@@ -25,16 +25,18 @@ size_t forward_workspace_within(int B, int H, int N, int d, int R, int M, int dt
                                 size_t budget);
 }  // namespace ida
 
-// The shared scratch: 32 MiB per device.  The prefill splits sequences only as
-// finely as its state slots fit in it (a caller workspace may allow finer splits),
-// so every supported shape runs; a plan that would still need more is refused
-// with a clear error rather than run over the end of the array.
+// The shared scratch: 32 MiB per device.  The prefill planner never picks a plan
+// whose segment states exceed the budget it is given (it falls back to coarser
+// splits, or to whole sequences), so every supported shape runs; the size check
+// below guards that invariant rather than a case a caller can reach.
 static constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 // Device address of the scratch, looked up once per device.  In host code
 // g_static_scratch names a host-side stand-in, not device memory, so the
-// kernels are only ever handed the address cudaGetSymbolAddress returns.
+// kernels are only ever handed the address cudaGetSymbolAddress returns.  The
+// address stays valid while the device's primary context lives; a
+// cudaDeviceReset invalidates it (the header says so).
 static std::mutex g_scratch_mu;
 static constexpr int kMaxDevices = 64;
 static void *g_scratch_dev[kMaxDevices];
@@ -48,9 +50,9 @@ extern "C" ida_status ida_forward_noalloc(const void *q, const void *k, const vo
     if (e != cudaSuccess) return ida::fail_with(IDA_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return ida::fail_with(IDA_ERR_UNSUPPORTED, "device ordinal above 63");
     const size_t need = ida::forward_workspace_within(B, H, N, d, R, M, dtype, W, flags, kStaticScratchBytes);
-    if (need > kStaticScratchBytes)
-        return ida::fail_with(IDA_ERR_UNSUPPORTED, "this shape needs " + std::to_string(need) +
-                                                       " bytes of scratch; the static scratch holds " +
+    if (need > kStaticScratchBytes)  // the planner keeps within its budget: not reached
+        return ida::fail_with(IDA_ERR_UNSUPPORTED, "internal: a plan of " + std::to_string(need) +
+                                                       " bytes of scratch exceeds the static " +
                                                        std::to_string(kStaticScratchBytes));
     void *scratch = nullptr;
     {

@@ -136,3 +136,9 @@ def test_forward_from_rejects_bad_states(lib):
     assert "overlap" in binding.ida_last_error()
     assert _from(lib, b, ctypes.c_void_p(base + 16 * ((S * 4) // 16)), p0) == binding.IDA_ERR_ARG
     assert _from(lib, b, p0, p0, flags=4) == binding.IDA_ERR_ARG  # no such flag bit
+
+
+def test_selftest_rejects_bad_limits(lib):
+    """The bounded-wait self-test checks its limit on the host, before touching CUDA."""
+    for bad in (0, -5, 5_000_000_000):
+        assert lib.ida_selftest_bounded_wait(bad, None) == binding.IDA_ERR_ARG
