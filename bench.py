@@ -15,7 +15,8 @@ state seeded by a 4096-position prefill).
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
 on the launching stream; between timed steps the L2 is flushed (a 512 MB
-write and read-back outside the timed region).  ``value`` is whole-job tokens/s
+write and read-back outside the timed region), except where a step streams
+more than four times the L2 (the decode state).  ``value`` is whole-job tokens/s
 (a token is one position of one batch row, through all H heads).
 ``--impl reference`` times the CPU oracle instead (bounded sample per step).
 """
@@ -108,10 +109,24 @@ def decode_bytes(w) -> int:
     return w.B * w.H * (2 * state_floats(w) * 4 + (2 * w.R + w.d) * s + w.d * s)
 
 
+def resident_bytes(w) -> int:
+    """Bytes a step touches that stay on the device between steps: the prefill's
+    inputs and output, or the decode state."""
+    if w.decode_steps:
+        return w.B * w.H * state_floats(w) * 4
+    s = elem_bytes(w.dtype)
+    return w.B * w.H * w.N * (2 * w.R + 2 * w.d) * s
+
+
+def flushes_l2(w) -> bool:
+    """The L2 is flushed between timed steps unless a step streams more than four
+    times the L2 (the decode state), where at most a quarter of it could be reused."""
+    return resident_bytes(w) < 4 * L2_BYTES
+
+
 def l2_note(w) -> str:
-    """Every workload flushes the L2 between timed steps (a 512 MB write and read-back
-    outside the timed region), whether or not its inputs exceed the L2."""
-    return "flushed between timed steps"
+    return ("flushed between timed steps (512 MB write and read-back, outside the timed region)"
+            if flushes_l2(w) else "inputs larger than L2 (the step streams more than 4x the L2)")
 
 
 def mixer_flops(w, positions: int) -> float:
@@ -445,7 +460,7 @@ def sources_of(w, flags) -> list:
 def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, seed_len=None,
             from_state=False):
     runner = Decode(w, dev, flags, seed_len) if w.decode_steps else Prefill(w, dev, flags, from_state)
-    flush = True
+    flush = flushes_l2(w)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)

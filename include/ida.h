@@ -231,6 +231,46 @@ IDA_API ida_status ida_decode_step(const void *q, const void *k, const void *v,
                            int W, int flags, ida_stream_t stream);
 
 /*
+ * Backward pass of ida_forward (from the zero state): the gradients of a loss
+ * L with respect to the inputs and every parameter, given dL/d out.  The
+ * pages train the layer in models of 125M to 1.3B parameters ("Interdomain
+ * Attention: Beyond Token-Level Key-Value Memory", German technical summary,
+ * "Hauptbeiträge"), which takes these gradients; the forward it differentiates
+ * is the one ida_forward computes, readings included.
+ *   q, k, v, conv_w, norm_w, bias, lambda, Bvec  as for ida_forward;
+ *   dout    [B, N, H, d] dtype: dL/d out;
+ *   dq, dk  [B, N, H, R] dtype, dv [B, N, H, d] dtype: written;
+ *   dconv_w [2, H, R, W], dnorm_w / dbias [H, R + d], dlambda / dBvec [H, M, 2]:
+ *           float, written (not accumulated), summed over the batch rows;
+ *           complex parameters get (dL/d Re, dL/d Im);
+ *   flags   IDA_READOUT_ETA and/or IDA_FEAT_L2, as given to the forward;
+ *   workspace  a 16-byte aligned device buffer of at least
+ *           ida_backward_workspace_bytes(...) bytes (required when N > 0;
+ *           contents on entry ignored): feature rows, their gradients, the
+ *           state every 64 positions and the states of one 64-position chunk
+ *           per unit.
+ * The arithmetic is fp64 for fp32 inputs and fp32 for bf16 inputs; sums run
+ * in a fixed order, so the results are deterministic.  N == 0 writes zero
+ * parameter gradients (q, k, v, dout, dq, dk, dv may then be NULL).  Same
+ * shape support as ida_forward.
+ */
+IDA_API ida_status ida_backward(const void *q, const void *k, const void *v,
+                        const float *conv_w, const float *norm_w,
+                        const float *bias, const float *lambda,
+                        const float *Bvec, const void *dout,
+                        void *dq, void *dk, void *dv,
+                        float *dconv_w, float *dnorm_w, float *dbias,
+                        float *dlambda, float *dBvec,
+                        int B, int H, int N, int d, int R, int M, int dtype,
+                        int W, int flags, void *workspace,
+                        size_t workspace_bytes, ida_stream_t stream);
+
+/* Workspace bytes ida_backward needs for this shape (0 for invalid sizes or
+ * N == 0).  Host-only arithmetic: queries nothing. */
+IDA_API size_t ida_backward_workspace_bytes(int B, int H, int N, int d, int R,
+                                            int M, int dtype, int W, int flags);
+
+/*
  * Self-test of the failure reporting (no counterpart in the paper: a property
  * of the library).  Launches one warp on `stream` that waits, through the
  * bounded-wait helper every prefill kernel uses, on an mbarrier nothing

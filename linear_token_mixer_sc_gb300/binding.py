@@ -22,7 +22,7 @@ IDA_PATH_SEQUENTIAL = 256
 
 EXPORTED = ("ida_state_floats", "ida_forward", "ida_forward_ws", "ida_forward_from", "ida_forward_workspace_bytes",
             "ida_forward_noalloc", "ida_decode_step", "ida_device_error", "ida_status_str",
-            "ida_last_error", "ida_selftest_bounded_wait")
+            "ida_last_error", "ida_selftest_bounded_wait", "ida_backward", "ida_backward_workspace_bytes")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +63,12 @@ def load() -> ctypes.CDLL:
             L.ida_decode_step.restype = _i
             L.ida_decode_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _fp, _vp,
                                           _i, _i, _i, _i, _i, _i, _i, _i, _vp]
+            L.ida_backward.restype = _i
+            L.ida_backward.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _vp, _vp, _vp,
+                                       _fp, _fp, _fp, _fp, _fp,
+                                       _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp]
+            L.ida_backward_workspace_bytes.restype = ctypes.c_size_t
+            L.ida_backward_workspace_bytes.argtypes = [_i] * 9
             L.ida_selftest_bounded_wait.restype = _i
             L.ida_selftest_bounded_wait.argtypes = [ctypes.c_longlong, _vp]
             L.ida_device_error.restype = _i
@@ -247,6 +253,44 @@ def ida_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: d
                                 _stream_handle(stream))
     _check(st, "ida_decode_step")
     return out
+
+
+def ida_backward_workspace_bytes(B: int, H: int, N: int, d: int, R: int, M: int, dtype: int,
+                                 W: int, flags: int = 0) -> int:
+    return int(load().ida_backward_workspace_bytes(B, H, N, d, R, M, dtype, W, flags))
+
+
+def ida_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict, dout: torch.Tensor,
+                 flags: int = 0, workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Gradients of the prefill.  q, k [B,N,H,R], v and dout [B,N,H,d] CUDA tensors of one
+    dtype.  Returns dict q, k, v (input dtype) and conv_w, norm_w, bias, lambda, Bvec
+    (float32, the parameters' shapes).  ``workspace``: a CUDA tensor of at least
+    ``ida_backward_workspace_bytes`` bytes (allocated here when None)."""
+    for t in (q, k, v, dout):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("q, k, v and dout must be contiguous CUDA tensors")
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype or dout.dtype != q.dtype:
+        raise TypeError("q, k, v and dout must share a dtype")
+    B, N, H, R = q.shape
+    d = v.shape[3]
+    cw, nw, bs, lam, bv = _params(params)
+    M, W = lam.shape[1], cw.shape[3]
+    if tuple(dout.shape) != (B, N, H, d):
+        raise ValueError("dout must have the shape of out")
+    nbytes = ida_backward_workspace_bytes(B, H, N, d, R, M, dt, W, flags)
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    g = {"q": torch.empty_like(q), "k": torch.empty_like(k), "v": torch.empty_like(v),
+         "conv_w": torch.empty_like(cw), "norm_w": torch.empty_like(nw), "bias": torch.empty_like(bs),
+         "lambda": torch.empty_like(lam), "Bvec": torch.empty_like(bv)}
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().ida_backward(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv), _p(dout),
+                             _p(g["q"]), _p(g["k"]), _p(g["v"]), _p(g["conv_w"]), _p(g["norm_w"]),
+                             _p(g["bias"]), _p(g["lambda"]), _p(g["Bvec"]), B, H, N, d, R, M, dt, W,
+                             int(flags), _p(workspace), wbytes, _stream_handle(stream))
+    _check(st, "ida_backward")
+    return g
 
 
 def ida_selftest_bounded_wait(limit_cycles: int, stream=None) -> None:

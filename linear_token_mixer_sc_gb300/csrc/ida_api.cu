@@ -102,6 +102,13 @@ ida_status forward_entry(const void *q, const void *k, const void *v, const floa
                          float *final_state, int B, int H, int N, int d, int R, int M, int dtype, int W, int flags,
                          void *workspace, size_t workspace_bytes, ida_stream_t stream);
 ida_status fail_with(ida_status s, const std::string &why) { return fail(s, why); }
+// Shape and flag checks of a call; with num_sms, also the device set-up (the error word,
+// where a pending device error is reported).
+ida_status check_call(int d, int R, int M, int W, int dtype, int flags, int *num_sms, std::string &why) {
+    ida_status s = check_shape(d, R, M, W, dtype, flags, why);
+    if (s != IDA_OK || !num_sms) return s;
+    return device_setup(num_sms, why);
+}
 // The device address of the error word (set up on first use), without reading it.
 ida_status device_error_word(unsigned **err, std::string &why) {
     ida_status s = ensure_error_word(why);

@@ -548,9 +548,10 @@ __global__ void __launch_bounds__(NTH, 1)
             }
 
             // ---- S1: prologue, thread = (8-channel block, block of consecutive positions)
+            // query / key: R/8 channel blocks x (64 R/8 / 256) positions per thread
+            constexpr int CBQ = R / 8, PPQ = CH * CBQ / NTH;
+            uint32_t hk[PPQ][4];  // this thread's key rows (fp16 pairs), kept for the Z^T rows
             {
-                // query / key: R/8 channel blocks x (64 R/8 / 256) positions per thread
-                constexpr int CBQ = R / 8, PPQ = CH * CBQ / NTH;
                 const int cb = tid % CBQ, i0 = (tid / CBQ) * PPQ, c0 = 8 * cb;
                 // rows are stored rotated: at step pp this thread writes position i0 + (pp + rot) % PPQ,
                 // so the channel-block threads of one position hit different banks
@@ -654,7 +655,6 @@ __global__ void __launch_bounds__(NTH, 1)
                 }
                 // key RMSNorm + affine, packed to fp16 once for the Kt rows (rotated) and the
                 // transposed key rows of Z^T
-                uint32_t hk[PPQ][4];
     #pragma unroll
                 for (int pp = 0; pp < PPQ; ++pp) {
                     float ms = 0.f;
@@ -683,7 +683,37 @@ __global__ void __launch_bounds__(NTH, 1)
                     *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) =
                         make_uint4(hs[0], hs[1], hs[2], hs[3]);
                 }
-                if (it > 0 && !mbar_wait(&bar[4], par ^ 1)) ok = false;
+            }
+            // The previous chunk's state update read U (which P^T reads next) and Z^T, CF16
+            // (rewritten below): wait for it before issuing this chunk's MMAs.
+            if (it > 0 && !mbar_wait(&bar[4], par ^ 1)) ok = false;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (__syncthreads_or(!ok)) break;
+            tc_fence_after();
+
+            // ---- S2: G and P^T ------------------------------------------------------
+            if (warp == 0 && elect_one()) {
+                const uint32_t idg = idesc(128, 64, 0, 0);
+    #pragma unroll
+                for (int s = 0; s < R / 16; ++s)
+                    mma_f16(tb + T::G, sdesc_at(s16, S::XQ16 + s * 256, 128, 16 * R),
+                               sdesc_at(s16, S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
+                mma_commit(&bar[0]);
+            } else if (warp == 1 && elect_one()) {
+                // P^T from a second issuing thread, so that G's completion is not queued behind it
+                const uint32_t idp = idesc(128, 64, 2, 2);
+    #pragma unroll
+                for (int s = 0; s < R / 8; ++s)
+                    mma_tf32_t(tb + T::PT, tb + T::U + 8 * s, sdesc_at(s16, S::XQ32 + s * 256, 128, 32 * R), idp, s > 0);
+                mma_commit(&bar[6]);
+            }
+            __syncwarp();
+
+            // ---- S1b, under the G / P^T MMAs: Z^T key rows, the value rows, a ragged Coef --------
+            // (read by the O1 and state-update MMAs, after later proxy fences and barriers)
+            {
+                const int cb = tid % CBQ, i0 = (tid / CBQ) * PPQ, c0 = 8 * cb;
     #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     // channel c0 + e at positions i0 .. i0 + PPQ - 1: pairs of halves from hk
@@ -755,28 +785,6 @@ __global__ void __launch_bounds__(NTH, 1)
                     suml[mm] = make_float2(sr, si);  // sum_{k<L} lambda^k
                 }
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (__syncthreads_or(!ok)) break;  // also carries a timeout of the in-prologue wait
-            tc_fence_after();
-
-            // ---- S2: G and P^T ------------------------------------------------------
-            if (warp == 0 && elect_one()) {
-                const uint32_t idg = idesc(128, 64, 0, 0);
-    #pragma unroll
-                for (int s = 0; s < R / 16; ++s)
-                    mma_f16(tb + T::G, sdesc_at(s16, S::XQ16 + s * 256, 128, 16 * R),
-                               sdesc_at(s16, S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
-                mma_commit(&bar[0]);
-            } else if (warp == 1 && elect_one()) {
-                // P^T from a second issuing thread, so that G's completion is not queued behind it
-                const uint32_t idp = idesc(128, 64, 2, 2);
-    #pragma unroll
-                for (int s = 0; s < R / 8; ++s)
-                    mma_tf32_t(tb + T::PT, tb + T::U + 8 * s, sdesc_at(s16, S::XQ32 + s * 256, 128, 32 * R), idp, s > 0);
-                mma_commit(&bar[6]);
-            }
-            __syncwarp();
             ok = mbar_wait(&bar[0], par);
             if (tid == 0) bulk_wait_read_all();  // the previous output tile has left GP16 / A216
             tc_fence_after();
@@ -977,6 +985,29 @@ __global__ void __launch_bounds__(NTH, 1)
                 mma_commit(&bar[3]);
             }
             __syncwarp();
+            // under the A2' / O2 MMAs: U scaled by lambda^L (its last reader, P^T, is complete;
+            // the next one is this chunk's state update)
+            {
+                // U (lanes = mode planes): the partner lane holds the other component
+                const float2 lm = laml[mm];
+                constexpr int NB = R / 32;  // 16-column blocks in my half of U
+                float v[NB][16];
+    #pragma unroll
+                for (int bb = 0; bb < NB; ++bb) tmem_ld16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
+                tmem_wait_ld();
+                // own(lambda^L x) = own(x) Re lambda^L + partner(x) s Im lambda^L, s = +1 on Im planes
+                const float lms = is_im ? lm.y : -lm.y;
+    #pragma unroll
+                for (int bb = 0; bb < NB; ++bb) {
+    #pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float o = __shfl_xor_sync(0xffffffffu, v[bb][j], 1);
+                        v[bb][j] = fmaf(v[bb][j], lm.x, o * lms);
+                    }
+                    tmem_st16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
+                }
+                tmem_wait_st();
+            }
             ok = mbar_wait(&bar[2], par);
             tc_fence_after();
             if (__syncthreads_or(!ok)) break;
@@ -1069,11 +1100,33 @@ __global__ void __launch_bounds__(NTH, 1)
                 mma_commit(&bar[7]);
             }
             __syncwarp();
-            ok = mbar_wait(&bar[7], par) && mbar_wait(&bar[3], par);
+            // under the O1 MMA: Gamma^T scaled by lambda^L once O2, its reader, is complete
+            ok = mbar_wait(&bar[3], par);
+            tc_fence_after();
+            if (ok) {
+                // Gamma^T (lanes = value channels, columns = (Re, Im) per mode)
+                float v[4][16];
+    #pragma unroll
+                for (int bb = 0; bb < 4; ++bb) tmem_ld16(tb + lane_base + T::GT + 64 * hsel + 16 * bb, v[bb]);
+                tmem_wait_ld();
+    #pragma unroll
+                for (int bb = 0; bb < 4; ++bb) {
+    #pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        const float2 l2 = laml[(64 * hsel + 16 * bb + j) >> 1];
+                        const float xr = v[bb][j], xi = v[bb][j + 1];
+                        v[bb][j] = l2.x * xr - l2.y * xi;
+                        v[bb][j + 1] = l2.x * xi + l2.y * xr;
+                    }
+                    tmem_st16(tb + lane_base + T::GT + 64 * hsel + 16 * bb, v[bb]);
+                }
+                tmem_wait_st();
+            }
+            ok = ok && mbar_wait(&bar[7], par);
             tc_fence_after();
             if (__syncthreads_or(!ok)) break;
 
-            // ---- S9: next chunk's raw rows; outputs; state scaled by lambda^L -------------------
+            // ---- S9: next chunk's raw rows; outputs; eta -----------------------------------------
             if (ci + 1 < c_end) {
                 tma_pending = 1;
                 if (tid == 0) {
@@ -1116,45 +1169,6 @@ __global__ void __launch_bounds__(NTH, 1)
                     eta_r = er;
                     eta_i = ei;
                 }
-                // U (lanes = mode planes): the partner lane holds the other component
-                const float2 lm = laml[mm];
-                {
-                    constexpr int NB = R / 32;  // 16-column blocks in my half of U
-                    float v[NB][16];
-    #pragma unroll
-                    for (int bb = 0; bb < NB; ++bb) tmem_ld16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
-                    tmem_wait_ld();
-                    // own(lambda^L x) = own(x) Re lambda^L + partner(x) s Im lambda^L, s = +1 on Im planes
-                    const float lms = is_im ? lm.y : -lm.y;
-    #pragma unroll
-                    for (int bb = 0; bb < NB; ++bb) {
-    #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float o = __shfl_xor_sync(0xffffffffu, v[bb][j], 1);
-                            v[bb][j] = fmaf(v[bb][j], lm.x, o * lms);
-                        }
-                        tmem_st16(tb + lane_base + T::U + hsel * (R / 2) + 16 * bb, v[bb]);
-                    }
-                }
-                // Gamma^T (lanes = value channels, columns = (Re, Im) per mode)
-                {
-                    float v[4][16];
-    #pragma unroll
-                    for (int bb = 0; bb < 4; ++bb) tmem_ld16(tb + lane_base + T::GT + 64 * hsel + 16 * bb, v[bb]);
-                    tmem_wait_ld();
-    #pragma unroll
-                    for (int bb = 0; bb < 4; ++bb) {
-    #pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            const float2 l2 = laml[(64 * hsel + 16 * bb + j) >> 1];
-                            const float xr = v[bb][j], xi = v[bb][j + 1];
-                            v[bb][j] = l2.x * xr - l2.y * xi;
-                            v[bb][j + 1] = l2.x * xi + l2.y * xr;
-                        }
-                        tmem_st16(tb + lane_base + T::GT + 64 * hsel + 16 * bb, v[bb]);
-                    }
-                }
-                tmem_wait_st();
             }
             tc_fence_before();
             __syncthreads();

@@ -142,3 +142,39 @@ def test_selftest_rejects_bad_limits(lib):
     """The bounded-wait self-test checks its limit on the host, before touching CUDA."""
     for bad in (0, -5, 5_000_000_000):
         assert lib.ida_selftest_bounded_wait(bad, None) == binding.IDA_ERR_ARG
+
+
+def test_backward_workspace_bytes(lib):
+    """Feature rows and their gradients, checkpoints every 64 positions, one chunk of
+    states and the adjoint state per unit, plus per-tile partials: host arithmetic only."""
+    n = binding.ida_backward_workspace_bytes(2, 3, 100, 32, 32, 16, binding.IDA_BF16, 4)
+    assert n > 0 and n % 4 == 0
+    assert binding.ida_backward_workspace_bytes(2, 3, 100, 32, 32, 16, binding.IDA_F32, 4) == 2 * n
+    assert binding.ida_backward_workspace_bytes(2, 3, 0, 32, 32, 16, binding.IDA_BF16, 4) == 0
+    assert binding.ida_backward_workspace_bytes(2, 3, 100, 32, 32, 200, binding.IDA_BF16, 4) == 0
+
+
+def test_backward_rejects_bad_arguments_on_the_host(lib):
+    b = _Bufs()
+    p, mis = b.p, b.mis
+    args = [p] * 17
+    ok = dict(B=1, H=2, N=8, d=32, R=32, M=16, dtype=1, W=4, flags=0)
+
+    def call(ptrs, ws=None, ws_bytes=0, **over):
+        kw = dict(ok, **over)
+        return lib.ida_backward(*ptrs, kw["B"], kw["H"], kw["N"], kw["d"], kw["R"], kw["M"], kw["dtype"],
+                                kw["W"], kw["flags"], ws, ws_bytes, None)
+
+    for i in range(17):
+        bad = list(args)
+        bad[i] = None
+        assert call(bad) == binding.IDA_ERR_ARG
+        bad[i] = mis
+        assert call(bad) == binding.IDA_ERR_ARG
+    # missing or short workspace
+    assert call(args) == binding.IDA_ERR_ARG
+    assert call(args, ws=p, ws_bytes=16) == binding.IDA_ERR_ARG
+    assert call(args, B=-1) == binding.IDA_ERR_ARG
+    assert call(args, flags=binding.IDA_PATH_SEQUENTIAL) == binding.IDA_ERR_ARG
+    assert call(args, M=200) == binding.IDA_ERR_UNSUPPORTED
+    assert call(args, W=5) == binding.IDA_ERR_UNSUPPORTED
