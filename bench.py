@@ -52,6 +52,7 @@ FP32_TFLOPS_NOMINAL = 152 * 128 * 2 * 2.07e9 / 1e12
 PREFILL_SOURCES = ["ida_chunk.cu", "ida_seq.cu", "ida_common.cuh", "tc_sm103.cuh", "ida_api.cu"]
 ETA_SOURCES = ["ida_seq_modes.cu", "ida_seq.cu", "ida_common.cuh", "ida_api.cu"]
 DECODE_SOURCES = ["ida_decode.cu", "ida_common.cuh", "ida_api.cu"]
+BACKWARD_SOURCES = ["ida_backward.cu", "ida_common.cuh", "ida_api.cu"]
 
 
 # ---------------------------------------------------------------- helpers
@@ -314,6 +315,57 @@ class Decode:
         return mixer_flops(self.w, self.w.B * self.w.H)
 
 
+class Backward:
+    """One ida_backward call (the gradients of a prefill with respect to q, k, v and every
+    parameter) over the workload's batch, from a seeded output gradient."""
+
+    def __init__(self, w, dev, flags=0):
+        from linear_token_mixer_sc_gb300 import binding
+        self.b = binding
+        self.w, self.dev, self.flags = w, dev, flags
+        self.pd = binding.params_to_device(inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed), dev)
+        q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed)
+        g = torch.Generator().manual_seed(w.seed + 1000)
+        dout = torch.randn(w.B, w.N, w.H, w.d, generator=g).to(q.dtype)
+        self.host = [t.pin_memory() for t in (q, k, v, dout)]
+        self.q, self.k, self.v, self.dout = (t.to(dev) for t in self.host)
+        nb = binding.ida_backward_workspace_bytes(w.B, w.H, w.N, w.d, w.R, w.M,
+                                                  binding.IDA_BF16 if w.dtype == "bf16" else binding.IDA_F32,
+                                                  w.W, flags)
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        self.grads = {"q": torch.empty_like(self.q), "k": torch.empty_like(self.k), "v": torch.empty_like(self.v)}
+        self.grads.update({n: torch.empty_like(self.pd[n]) for n in ("conv_w", "norm_w", "bias", "lambda", "Bvec")})
+        self.gq_host = torch.empty(self.q.shape, dtype=self.q.dtype).pin_memory()
+        self.launches_per_step = 4  # features, scan, position-local backward, parameter reduction
+
+    def step(self):
+        self.b.ida_backward(self.q, self.k, self.v, self.pd, self.dout, flags=self.flags, workspace=self.ws,
+                            grads=self.grads)
+
+    def step_e2e(self):
+        for src, dst in zip(self.host, (self.q, self.k, self.v, self.dout)):
+            dst.copy_(src, non_blocking=True)
+        self.step()
+        self.gq_host.copy_(self.grads["q"], non_blocking=True)
+
+    def e2e_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host), self.gq_host.numel() * self.gq_host.element_size()
+
+    def tokens(self):
+        return self.w.B * self.w.N
+
+    def alg_bytes(self):
+        """q, k, v and dout read once; dq, dk, dv written once."""
+        s = elem_bytes(self.w.dtype)
+        w = self.w
+        return w.B * w.H * w.N * ((2 * w.R + 2 * w.d) * s + (2 * w.R + w.d) * s)
+
+    def flops(self):
+        """The forward recurrence recomputed plus its adjoint: three times the forward's
+        12 M (R + d) per position and head."""
+        return 3 * mixer_flops(self.w, self.w.B * self.w.H * self.w.N)
+
+
 def time_steps(runner, steps, warmup, dev, flush, e2e=False, sampler=None):
     """Per-step CUDA-event times (ms) on the launching stream.  With ``flush`` the L2
     is flushed before every timed step, outside the timed region, by writing a 512 MB
@@ -458,8 +510,13 @@ def sources_of(w, flags) -> list:
 
 
 def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, seed_len=None,
-            from_state=False):
-    runner = Decode(w, dev, flags, seed_len) if w.decode_steps else Prefill(w, dev, flags, from_state)
+            from_state=False, backward=False):
+    if backward:
+        runner = Backward(w, dev, flags)
+    elif w.decode_steps:
+        runner = Decode(w, dev, flags, seed_len)
+    else:
+        runner = Prefill(w, dev, flags, from_state)
     flush = flushes_l2(w)
     if dist is not None:
         dist.barrier()
@@ -474,15 +531,17 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, 
     ms = sum(times) / len(times)
     ms_all = max_over_ranks(dist, ms, dev)
     value = job_value(ws, runner.tokens(), ms_all)
-    key = line_key(w, flags, from_state)
-    traffic, per_kernel = traffic_record(key, sources_of(w, flags))
+    key = line_key(w, flags, from_state) + ("_backward" if backward else "")
+    traffic, per_kernel = traffic_record(key, BACKWARD_SOURCES if backward else sources_of(w, flags))
     rl = roofline(runner, ms, peaks, peak_kind, traffic,
-                  fp32_fma=bool(flags & 1 and not w.decode_steps) or w.dtype == "f32")
+                  fp32_fma=backward or bool(flags & 1 and not w.decode_steps) or w.dtype == "f32")
     if per_kernel:
         rl["traffic_kernels"] = per_kernel
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "R": w.R, "d": w.d, "M": w.M, "W": w.W,
            "dtype": w.dtype, "readout": "eta" if flags & 1 else "denominator-free",
            "l2": l2_note(w)}
+    if backward:
+        cfg["pass"] = "backward (gradients of q, k, v and every parameter)"
     if w.decode_steps:
         cfg["seed_prefill_N"] = w.N if seed_len is None else seed_len
         del cfg["N"]
@@ -586,6 +645,12 @@ def main():
                         seed_len=args.seed_len)
             others[line_key(ow, of)] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps", "roofline",
                                                           "e2e", "gpu_launches", "clocks", "config")}
+        # the backward pass of the 125M-like prefill (gradients for training the layer)
+        bw = configs.PREFILL_125M
+        r = measure(bw, dev, max(3, args.steps // 4), args.warmup, 0, dist, ws, peaks, peak_kind, backward=True)
+        others[line_key(bw) + "_backward"] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps",
+                                                                 "roofline", "e2e", "gpu_launches", "clocks",
+                                                                 "config")}
     if binding.ida_device_error() != 0:
         raise RuntimeError("a kernel reported a device error")
 

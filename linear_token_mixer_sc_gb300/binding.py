@@ -261,11 +261,12 @@ def ida_backward_workspace_bytes(B: int, H: int, N: int, d: int, R: int, M: int,
 
 
 def ida_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict, dout: torch.Tensor,
-                 flags: int = 0, workspace: torch.Tensor | None = None, stream=None) -> dict:
+                 flags: int = 0, workspace: torch.Tensor | None = None, stream=None,
+                 grads: dict | None = None) -> dict:
     """Gradients of the prefill.  q, k [B,N,H,R], v and dout [B,N,H,d] CUDA tensors of one
     dtype.  Returns dict q, k, v (input dtype) and conv_w, norm_w, bias, lambda, Bvec
-    (float32, the parameters' shapes).  ``workspace``: a CUDA tensor of at least
-    ``ida_backward_workspace_bytes`` bytes (allocated here when None)."""
+    (float32, the parameters' shapes), written into ``grads`` when given.  ``workspace``: a
+    CUDA tensor of at least ``ida_backward_workspace_bytes`` bytes (allocated here when None)."""
     for t in (q, k, v, dout):
         if not (t.is_cuda and t.is_contiguous()):
             raise ValueError("q, k, v and dout must be contiguous CUDA tensors")
@@ -281,9 +282,10 @@ def ida_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict
     nbytes = ida_backward_workspace_bytes(B, H, N, d, R, M, dt, W, flags)
     if workspace is None and nbytes > 0:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    g = {"q": torch.empty_like(q), "k": torch.empty_like(k), "v": torch.empty_like(v),
-         "conv_w": torch.empty_like(cw), "norm_w": torch.empty_like(nw), "bias": torch.empty_like(bs),
-         "lambda": torch.empty_like(lam), "Bvec": torch.empty_like(bv)}
+    g = grads if grads is not None else {
+        "q": torch.empty_like(q), "k": torch.empty_like(k), "v": torch.empty_like(v),
+        "conv_w": torch.empty_like(cw), "norm_w": torch.empty_like(nw), "bias": torch.empty_like(bs),
+        "lambda": torch.empty_like(lam), "Bvec": torch.empty_like(bv)}
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().ida_backward(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv), _p(dout),
                              _p(g["q"]), _p(g["k"]), _p(g["v"]), _p(g["conv_w"]), _p(g["norm_w"]),

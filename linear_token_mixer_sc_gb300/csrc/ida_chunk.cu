@@ -148,6 +148,53 @@ __device__ __forceinline__ float silu_tanh(float x) {
 // x rounded to the tf32 grid (10 mantissa bits), nearest with ties away from zero, as bits
 __device__ __forceinline__ uint32_t tf32_bits(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
 
+// the hardware tanh approximation (relative error about 2^-11)
+__device__ __forceinline__ float tanh_approx(float x) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
+    return t;
+}
+
+// two fp32 in one 64-bit register for the packed fp32x2 instructions (each lane rounded
+// like the scalar instruction)
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f2_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+    f2_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+    f2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// v[pp] <- v[(pp + rot) % P] for all pp, by log2(P) conditional shifts (P a power of two)
+template <int P, int Wd>
+__device__ __forceinline__ void rotate_rows(uint32_t (&v)[P][Wd], int rot) {
+#pragma unroll
+    for (int sh = 1; sh < P; sh <<= 1) {
+        const bool on = (rot & sh) != 0;
+        uint32_t t[P][Wd];
+#pragma unroll
+        for (int pp = 0; pp < P; ++pp)
+#pragma unroll
+            for (int e = 0; e < Wd; ++e) t[pp][e] = on ? v[(pp + sh) % P][e] : v[pp][e];
+#pragma unroll
+        for (int pp = 0; pp < P; ++pp)
+#pragma unroll
+            for (int e = 0; e < Wd; ++e) v[pp][e] = t[pp][e];
+    }
+}
+
 // two floats as one fp16 pair (lo in the low half), one conversion instruction
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
@@ -562,43 +609,72 @@ __global__ void __launch_bounds__(NTH, 1)
                 *reinterpret_cast<float4 *>(bsk) = *reinterpret_cast<const float4 *>(bss + c0);
                 *reinterpret_cast<float4 *>(bsk + 4) = *reinterpret_cast<const float4 *>(bss + c0 + 4);
                 float fk[PPQ][8];
+                // taps of my channel block (TMEM lane tl holds block tl % CBQ == cb), q then k, as
+                // channel pairs: tp[which][e2][jj] = (tap jj of channel 2 e2, of channel 2 e2 + 1)
+                f2_t tp[2][4][4];
+                {
+                    float w8[2][32];
+    #pragma unroll
+                    for (int which = 0; which < 2; ++which) {
+                        tmem_ld16(tb + lane_base + T::TAPS + 32 * which, w8[which]);
+                        tmem_ld16(tb + lane_base + T::TAPS + 32 * which + 16, w8[which] + 16);
+                    }
+                    tmem_wait_ld();
+    #pragma unroll
+                    for (int which = 0; which < 2; ++which)
+    #pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2)
+    #pragma unroll
+                            for (int jj = 0; jj < 4; ++jj)
+                                tp[which][e2][jj] = f2_pack(w8[which][8 * e2 + jj], w8[which][8 * e2 + 4 + jj]);
+                }
     #pragma unroll
                 for (int which = 0; which < 2; ++which) {
                     const unsigned char *raw = sm + (which == 0 ? S::RAWQ : S::RAWK);
-                    // taps of my channel block (TMEM lane tl holds block tl % CBQ == cb), q then k
-                    float w8[32];
-                    tmem_ld16(tb + lane_base + T::TAPS + 32 * which, w8);
-                    tmem_ld16(tb + lane_base + T::TAPS + 32 * which + 16, w8 + 16);
-                    tmem_wait_ld();
-                    // rows i0 .. i0+PPQ+2 of the staged tile = positions i0-3 .. i0+PPQ-1
-                    float f[PPQ][8];
+                    // rows i0 .. i0+PPQ+2 of the staged tile = positions i0-3 .. i0+PPQ-1; the conv
+                    // of channel pairs in packed fp32x2 arithmetic
+                    f2_t g[PPQ][4];
     #pragma unroll
                     for (int pp = 0; pp < PPQ; ++pp)
     #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[pp][e] = 0.f;
+                        for (int e2 = 0; e2 < 4; ++e2) g[pp][e2] = 0ull;
     #pragma unroll
                     for (int r = 0; r < PPQ + HALO; ++r) {
-                        float x8[8];
-                        unpack_bf16x8(*reinterpret_cast<const uint4 *>(raw + ((size_t)(i0 + r) * R + c0) * 2), x8);
+                        const uint4 u = *reinterpret_cast<const uint4 *>(raw + ((size_t)(i0 + r) * R + c0) * 2);
+                        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+                        f2_t x2[4];
+    #pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2)
+                            x2[e2] = f2_pack(__uint_as_float(wv[e2] << 16), __uint_as_float(wv[e2] & 0xFFFF0000u));
                         // tile row r holds position i0 + r - 3: right-aligned tap jj = r - pp of position pp
     #pragma unroll
                         for (int pp = 0; pp < PPQ; ++pp) {
                             const int jj = r - pp;
                             if (jj >= 0 && jj < 4)
     #pragma unroll
-                                for (int e = 0; e < 8; ++e) f[pp][e] = fmaf(w8[4 * e + jj], x8[e], f[pp][e]);
+                                for (int e2 = 0; e2 < 4; ++e2) g[pp][e2] = f2_fma(tp[which][e2][jj], x2[e2], g[pp][e2]);
                         }
                     }
+                    // SiLU (x sigmoid x = h + h tanh h, h = x / 2) and the squared norm, pairwise
                     float acc[PPQ];
+                    const f2_t half2 = f2_pack(0.5f, 0.5f);
     #pragma unroll
                     for (int pp = 0; pp < PPQ; ++pp) {
-                        acc[pp] = 0.f;
+                        f2_t s2 = 0ull;
     #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            f[pp][e] = silu_tanh(f[pp][e]);
-                            acc[pp] = fmaf(f[pp][e], f[pp][e], acc[pp]);
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const f2_t h2 = f2_mul(g[pp][e2], half2);
+                            float hl, hh;
+                            f2_unpack(h2, hl, hh);
+                            const f2_t t2 = f2_pack(tanh_approx(hl), tanh_approx(hh));
+                            g[pp][e2] = f2_fma(h2, t2, h2);
+                            s2 = f2_fma(g[pp][e2], g[pp][e2], s2);
                         }
+                        float sl, sh;
+                        f2_unpack(s2, sl, sh);
+                        acc[pp] = sl + sh;
                     }
+                    float f[PPQ][8];
     #pragma unroll
                     for (int pp = 0; pp < PPQ; ++pp) {
     #pragma unroll
@@ -608,43 +684,31 @@ __global__ void __launch_bounds__(NTH, 1)
                                               ? (acc[pp] > 0.f ? acc[pp] * rsqrtf(acc[pp]) : 0.f)
                                               : acc[pp];
                         const float inv = (i0 + pp < L) ? __fdividef(1.f, nrm + IDA_EPS_FEAT) : 0.f;
+                        const f2_t inv2 = f2_pack(inv, inv);
     #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[pp][e] *= inv;
+                        for (int e2 = 0; e2 < 4; ++e2) f2_unpack(f2_mul(g[pp][e2], inv2), f[pp][2 * e2], f[pp][2 * e2 + 1]);
                     }
                     if (which == 0) {
-                        // xi(q) rows: fp16 for the Gram MMA, tf32 for the state read-out MMA
-                        uint32_t h16[PPQ][4], t32[PPQ][8];
+                        // xi(q) rows: fp16 for the Gram MMA, tf32 for the state read-out MMA; row pp
+                        // of the rotated set is position i0 + (pp + rot) % PPQ
+                        uint32_t w12[PPQ][12];
     #pragma unroll
                         for (int pp = 0; pp < PPQ; ++pp) {
     #pragma unroll
-                            for (int e = 0; e < 4; ++e) h16[pp][e] = pack_h2(f[pp][2 * e], f[pp][2 * e + 1]);
+                            for (int e = 0; e < 4; ++e) w12[pp][e] = pack_h2(f[pp][2 * e], f[pp][2 * e + 1]);
     #pragma unroll
-                            for (int e = 0; e < 8; ++e) t32[pp][e] = tf32_bits(f[pp][e]);
+                            for (int e = 0; e < 8; ++e) w12[pp][4 + e] = tf32_bits(f[pp][e]);
                         }
+                        rotate_rows<PPQ, 12>(w12, rot);
     #pragma unroll
                         for (int pp = 0; pp < PPQ; ++pp) {
-                            const int q = (pp + rot) % PPQ, i = i0 + q;
-                            uint32_t hs[4], ts[8];
-    #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                uint32_t v = h16[0][e];
-    #pragma unroll
-                                for (int u = 1; u < PPQ; ++u) v = q == u ? h16[u][e] : v;
-                                hs[e] = v;
-                            }
-    #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                uint32_t v = t32[0][e];
-    #pragma unroll
-                                for (int u = 1; u < PPQ; ++u) v = q == u ? t32[u][e] : v;
-                                ts[e] = v;
-                            }
+                            const int i = i0 + (pp + rot) % PPQ;
                             *reinterpret_cast<uint4 *>(sm + S::XQ16 + kmaj_off(i, c0, 2, 128, 16 * R)) =
-                                make_uint4(hs[0], hs[1], hs[2], hs[3]);
+                                make_uint4(w12[pp][0], w12[pp][1], w12[pp][2], w12[pp][3]);
                             *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0, 4, 128, 32 * R)) =
-                                make_uint4(ts[0], ts[1], ts[2], ts[3]);
+                                make_uint4(w12[pp][4], w12[pp][5], w12[pp][6], w12[pp][7]);
                             *reinterpret_cast<uint4 *>(sm + S::XQ32 + kmaj_off(i, c0 + 4, 4, 128, 32 * R)) =
-                                make_uint4(ts[4], ts[5], ts[6], ts[7]);
+                                make_uint4(w12[pp][8], w12[pp][9], w12[pp][10], w12[pp][11]);
                         }
                     } else {
     #pragma unroll
@@ -669,19 +733,19 @@ __global__ void __launch_bounds__(NTH, 1)
     #pragma unroll
                     for (int e = 0; e < 4; ++e) hk[pp][e] = pack_h2(fk[pp][2 * e], fk[pp][2 * e + 1]);
                 }
+                {
+                    uint32_t hr[PPQ][4];
     #pragma unroll
-                for (int pp = 0; pp < PPQ; ++pp) {
-                    const int q = (pp + rot) % PPQ, i = i0 + q;
-                    uint32_t hs[4];
+                    for (int pp = 0; pp < PPQ; ++pp)
     #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint32_t v = hk[0][e];
+                        for (int e = 0; e < 4; ++e) hr[pp][e] = hk[pp][e];
+                    rotate_rows<PPQ, 4>(hr, rot);
     #pragma unroll
-                        for (int u = 1; u < PPQ; ++u) v = q == u ? hk[u][e] : v;
-                        hs[e] = v;
+                    for (int pp = 0; pp < PPQ; ++pp) {
+                        const int i = i0 + (pp + rot) % PPQ;
+                        *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) =
+                            make_uint4(hr[pp][0], hr[pp][1], hr[pp][2], hr[pp][3]);
                     }
-                    *reinterpret_cast<uint4 *>(sm + S::KT16 + kmaj_off(i, c0, 2, 128, 16 * R)) =
-                        make_uint4(hs[0], hs[1], hs[2], hs[3]);
                 }
             }
             // The previous chunk's state update read U (which P^T reads next) and Z^T, CF16
@@ -701,7 +765,8 @@ __global__ void __launch_bounds__(NTH, 1)
                                sdesc_at(s16, S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
                 mma_commit(&bar[0]);
             } else if (warp == 1 && elect_one()) {
-                // P^T from a second issuing thread, so that G's completion is not queued behind it
+                // P^T from a second issuing thread: an issuing thread stalls while the tensor pipe's
+                // queue is full, and one thread issuing both measured slower
                 const uint32_t idp = idesc(128, 64, 2, 2);
     #pragma unroll
                 for (int s = 0; s < R / 8; ++s)
