@@ -1359,10 +1359,17 @@ struct StateSmem {
     static constexpr int BSS = NWS + (R + D) * 4;                     // [R+D] float
     static constexpr int TOTAL = BSS + (R + D) * 4;
     static_assert(RAWV % 1024 == 0 && TOTAL <= 116 * 1024, "shared memory budget");
-    // Launched with LAUNCH bytes so that one CTA runs per SM: with two co-resident CTAs the
-    // Gamma^T accumulator of the second one was intermittently wrong (seen on GB300, cause
-    // not identified), and one CTA per SM is always right.
+    // Launched with LAUNCH bytes so that one CTA runs per SM.  With two co-resident CTAs
+    // that each accumulate two or more chunks into their TMEM state, a few block states
+    // per call came out wrong on GB300 (a part of one block's U or Gamma^T accumulator off
+    // by 0.1 to 13 %, not another block's value, not zero); one chunk per CTA, or one CTA
+    // per SM, was always bitwise reproducible.  tcgen05 and proxy fences after the in-loop
+    // wait, waiting for each chunk's MMAs right after issuing them, moving the wait to the
+    // top of the iteration, issuing the Gamma^T MMAs first and a 128-aligned Gamma^T column
+    // did not remove it; the cause is not identified, so the pass is kept at one CTA per SM.
     static constexpr int LAUNCH = 116 * 1024;
+    // two CTAs of LAUNCH bytes exceed the 228 KB of shared memory of an sm_103a SM
+    static_assert(2 * LAUNCH > 228 * 1024, "the state pass must run one CTA per SM");
 };
 
 template <int R, int D, bool EXT>
