@@ -26,11 +26,15 @@
 //
 // Kernels (all deterministic: every sum runs in a fixed order):
 //   bwd_features   one warp per position: xi(q), kt, vt into the workspace;
-//   bwd_scan       one CTA per unit, one thread per state column: the forward recurrence,
-//                  storing the state before every chunk of BC positions; then, chunk by
-//                  chunk from the end, the chunk's states recomputed from its checkpoint
-//                  and the adjoint recurrence walked backwards through them; writes
-//                  dxi(q), dkt, dvt per position and per-unit lambda / B gradients;
+//   bwd_scan_a     per (unit, slice of modes): the forward recurrence with the state in
+//                  registers, storing the state before every chunk of 64 positions (and,
+//                  for the eta readout, the slice's parts of numerator and denominator);
+//   bwd_scan_nd    eta readout: 1 / den and -(g . o) / den per position;
+//   bwd_scan_b     per (unit, slice of modes): chunk by chunk from the end, the chunk's
+//                  states recomputed from its checkpoint and the adjoint walked backwards
+//                  through them with the adjoint state and its lambda / B sums in
+//                  registers; the slice's dxi(q), dkt, dvt per position and the slice's
+//                  lambda / B gradients; bwd_sum_slices adds the slices' parts;
 //   bwd_local      one CTA per (unit, tile of positions): RMSNorm, feature-map and conv
 //                  backward, dq, dk, dv, and per-tile partial parameter gradients;
 //   bwd_reduce     sums the partials over batch rows and tiles into the parameter gradients.
@@ -56,31 +60,57 @@ struct BackwardArgs {
     unsigned *err;
 };
 
+// Mode slicing of the adjoint scan: a CTA of BWD_THREADS threads holds G groups of RDw threads
+// (one thread per state column, RDw = R + d rounded up to whole warps); each thread keeps the
+// adjoint state of up to BWD_MGT modes of its column in registers, so a CTA covers
+// MC = G * BWD_MGT modes and a unit's M modes are split over S = ceil(M / MC) CTAs.
+constexpr int BWD_MGT = 8;
+
+struct BwdSlicing {
+    int RDw, G, MC, S;
+    __host__ __device__ static BwdSlicing of(int R, int d, int M) {
+        BwdSlicing q;
+        q.RDw = (R + d + 31) / 32 * 32;
+        q.G = BWD_THREADS / q.RDw;
+        q.MC = q.G * BWD_MGT;
+        q.S = (M + q.MC - 1) / q.MC;
+        return q;
+    }
+    // modes of slice s, and the state elements of one slice-local state (planar Re rows,
+    // Im rows, then eta Re, eta Im)
+    __host__ __device__ int ms(int s, int M) const { return M - s * MC < MC ? M - s * MC : MC; }
+    __host__ __device__ size_t sds(int RD) const { return 2 * (size_t)MC * RD + 2 * (size_t)MC; }
+};
+
 // Workspace layout (elements of T), per unit unless noted.
 struct BwdLayout {
-    size_t feat;   // [N][2R + d]: xi(q), kt, vt
-    size_t gfeat;  // [N][2R + d]: dxi(q), dkt, dvt
-    size_t sd;     // state elements: 2M (R + d) planar X, then 2M eta
-    size_t ckpt;   // [nck][sd]
-    size_t xbuf;   // [BWD_CHUNK + 1][sd]
-    size_t adj;    // [3][sd]: Y, lambda-bar terms, B-bar terms (per element, summed over t)
-    size_t pscan;  // [4M]: lambda-bar (re, im), B-bar (re, im)
+    size_t feat;    // [N][2R + d]: xi(q), kt, vt
+    size_t gfeat;   // [S][N][2R + d]: per mode slice, its part of dxi(q), dkt, dvt (summed into slice 0)
+    size_t nd;      // [S][N][d + 1]: eta readout, per slice: partial numerator and denominator
+    size_t gsc;     // [N][2]: eta readout: 1 / den and -(g . o) / den
+    size_t ckpt;    // [S][nck][sds]
+    size_t xbuf;    // [S][BWD_CHUNK + 1][sds]
+    size_t pscan;   // [4M]: lambda-bar (re, im), B-bar (re, im)
     size_t per_unit;
+    size_t sds;
     size_t plocal_each;  // per (unit, tile): [2][R][W] conv, [R + d] norm weight, [R + d] bias
-    int nck, ntile;
+    int nck, ntile, S;
     size_t total;  // elements of T
-    static BwdLayout of(int B, int H, int N, int d, int R, int M, int W) {
+    static BwdLayout of(int B, int H, int N, int d, int R, int M, int W, bool eta) {
         BwdLayout L;
+        const BwdSlicing q = BwdSlicing::of(R, d, M);
         const size_t units = (size_t)B * H, F = 2 * (size_t)R + d;
+        L.S = q.S;
         L.nck = (N + BWD_CHUNK - 1) / BWD_CHUNK;
         L.ntile = (N + BWD_TILE - 1) / BWD_TILE;
-        L.sd = 2 * (size_t)M * (R + d) + 2 * (size_t)M;
+        L.sds = q.sds(R + d);
         L.feat = 0;
         L.gfeat = L.feat + (size_t)N * F;
-        L.ckpt = L.gfeat + (size_t)N * F;
-        L.xbuf = L.ckpt + (size_t)L.nck * L.sd;
-        L.adj = L.xbuf + (size_t)(BWD_CHUNK + 1) * L.sd;
-        L.pscan = L.adj + 3 * L.sd;
+        L.nd = L.gfeat + (size_t)q.S * N * F;
+        L.gsc = L.nd + (eta ? (size_t)q.S * N * (d + 1) : 0);
+        L.ckpt = L.gsc + (eta ? 2 * (size_t)N : 0);
+        L.xbuf = L.ckpt + (size_t)q.S * L.nck * L.sds;
+        L.pscan = L.xbuf + (size_t)q.S * (BWD_CHUNK + 1) * L.sds;
         L.per_unit = (L.pscan + 4 * (size_t)M + 1) & ~(size_t)1;
         L.plocal_each = 2 * (size_t)R * W + 2 * ((size_t)R + d);
         L.total = units * L.per_unit + units * L.ntile * L.plocal_each;
@@ -173,277 +203,448 @@ __global__ void __launch_bounds__(256) bwd_features_kernel(BackwardArgs a, T *ws
 
 // ---- bwd_scan: the recurrence and its adjoint ---------------------------------------------
 //
-// Thread c owns state column c (c < R: U, R <= c < R + d: Gamma) of every mode; threads
-// c < M also own mode c's eta entry.  Planar layout of a state (sd elements): Re rows
-// [m][R + d], Im rows, then eta Re [M], eta Im [M].
+// Grid: units x S mode slices.  Thread (group g, column c) owns state column c (c < R: U,
+// R <= c < R + d: Gamma) of the slice-local modes g, g + G, g + 2G, ...; thread j < ms also
+// owns the eta entry of slice-local mode j.
 
+// Sum of each of NV values over the 32 lanes of a warp by recursive halving: afterwards lane
+// l holds the full sum of value index vidx(l) (lanes l and l ^ 1 hold the same one).  NV is a
+// power of two <= 16; 2 NV - 1 shuffles instead of 5 NV.
+template <int NV, typename T>
+__device__ __forceinline__ T warp_reduce_scatter(T (&v)[NV], int lane) {
+    int n = NV;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        if (n > 1) {
+            const bool hi = (lane & off) != 0;
+            const int hn = n >> 1;
+#pragma unroll
+            for (int k = 0; k < NV / 2; ++k) {
+                if (k < hn) {
+                    const T send = hi ? v[k] : v[k + hn];
+                    const T keep = hi ? v[k + hn] : v[k];
+                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            n = hn;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        }
+    }
+    return v[0];
+}
+// the value index lane l holds after warp_reduce_scatter<NV>
+template <int NV>
+__device__ __forceinline__ int rs_index(int lane) {
+    int idx = 0, n = NV;
+#pragma unroll
+    for (int off = 16; off >= 1 && n > 1; off >>= 1) {
+        n >>= 1;
+        if (lane & off) idx += n;
+    }
+    return idx;
+}
+
+// Phase A: the forward recurrence of the slice's modes over all positions, storing the state
+// before every chunk; for the eta readout also the slice's part of the numerator and of the
+// denominator at every position.
 template <typename T>
-__global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_kernel(BackwardArgs a, T *ws, BwdLayout L) {
-    extern __shared__ __align__(16) unsigned char smraw[];
+__global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_a_kernel(BackwardArgs a, T *ws, BwdLayout L) {
+    __shared__ T red[BWD_WARPS][2 * BWD_MGT];
+    __shared__ T am[2][BWD_THREADS / 32 * BWD_MGT];  // a_t of the slice's modes (re, im)
+    __shared__ T part[BWD_THREADS];
     const int R = a.R, d = a.d, H = a.H, N = a.N, M = a.M, RD = R + d;
-    const int unit = blockIdx.x, h = unit % H, b = unit / H;
+    const BwdSlicing q = BwdSlicing::of(R, d, M);
+    const int unit = blockIdx.x / q.S, sl = blockIdx.x % q.S, h = unit % H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = tid / q.RDw, c = tid % q.RDw, ms = q.ms(sl, M);
+    const bool col = g < q.G && c < RD;
     const bool eta_ro = (a.flags & IDA_READOUT_ETA) != 0;
     T *base = ws + (size_t)unit * L.per_unit;
     const T *feat = base + L.feat;
-    T *gfeat = base + L.gfeat;
-    T *ckpt = base + L.ckpt, *xbuf = base + L.xbuf, *Y = base + L.adj, *LB = Y + L.sd, *BB = LB + L.sd;
-    const size_t plane = (size_t)M * RD, F = 2 * (size_t)R + d;
-    // shared: lambda, B [M] complex; a, abar [M] complex; per-warp mode partials
-    T *lam_r = reinterpret_cast<T *>(smraw), *lam_i = lam_r + M, *b_r = lam_i + M, *b_i = b_r + M;
-    T *a_r = b_i + M, *a_i = a_r + M, *ab_r = a_i + M, *ab_i = ab_r + M;
-    T *red = ab_i + M;                 // [BWD_WARPS][2M] partial sums over columns
-    T *scal = red + (size_t)BWD_WARPS * 2 * M;  // [BWD_WARPS + 4]
-    for (int m = tid; m < M; m += BWD_THREADS) {
-        lam_r[m] = (T)a.lambda[((size_t)h * M + m) * 2];
-        lam_i[m] = (T)a.lambda[((size_t)h * M + m) * 2 + 1];
-        b_r[m] = (T)a.Bvec[((size_t)h * M + m) * 2];
-        b_i[m] = (T)a.Bvec[((size_t)h * M + m) * 2 + 1];
+    T *ckpt = base + L.ckpt + (size_t)sl * L.nck * L.sds;
+    T *nd = base + L.nd + (size_t)sl * N * (d + 1);
+    const size_t F = 2 * (size_t)R + d, plane = (size_t)q.MC * RD, eoff = 2 * plane;
+    T lr[BWD_MGT], li[BWD_MGT], br[BWD_MGT], bi[BWD_MGT], xr[BWD_MGT], xi[BWD_MGT];
+#pragma unroll
+    for (int i = 0; i < BWD_MGT; ++i) {
+        const int ml = g + q.G * i, m = sl * q.MC + ml;
+        const bool ok = col && ml < ms;
+        lr[i] = ok ? (T)a.lambda[((size_t)h * M + m) * 2] : T(0);
+        li[i] = ok ? (T)a.lambda[((size_t)h * M + m) * 2 + 1] : T(0);
+        br[i] = ok ? (T)a.Bvec[((size_t)h * M + m) * 2] : T(0);
+        bi[i] = ok ? (T)a.Bvec[((size_t)h * M + m) * 2 + 1] : T(0);
+        xr[i] = 0;
+        xi[i] = 0;
     }
-    __syncthreads();
-    const int c = tid;
-    const bool col = c < RD;
-    const bool has_eta = tid < M;  // thread m also carries eta[m]
-    const size_t zoff = (size_t)R + c;  // z column c in a feature row [xi(q) | kt | vt]
-    const size_t eoff = 2 * plane;
-
-    // Phase A: forward recurrence, storing the state before each chunk.
-    for (int m = 0; m < M && col; ++m) {
-        T xr = 0, xi = 0;
-        const T lr = lam_r[m], li = lam_i[m], br = b_r[m], bi = b_i[m];
-        for (int t = 0; t < N; ++t) {
-            if (t % BWD_CHUNK == 0) {
-                T *ck = ckpt + (size_t)(t / BWD_CHUNK) * L.sd;
-                ck[(size_t)m * RD + c] = xr;
-                ck[plane + (size_t)m * RD + c] = xi;
+    // eta of slice-local mode tid
+    const bool eown = tid < ms;
+    T elr = 0, eli = 0, ebr = 0, ebi = 0, er = 0, ei = 0;
+    if (eown) {
+        const int m = sl * q.MC + tid;
+        elr = (T)a.lambda[((size_t)h * M + m) * 2];
+        eli = (T)a.lambda[((size_t)h * M + m) * 2 + 1];
+        ebr = (T)a.Bvec[((size_t)h * M + m) * 2];
+        ebi = (T)a.Bvec[((size_t)h * M + m) * 2 + 1];
+    }
+    const int gwarps = q.RDw / 32;  // warps per group
+    for (int t = 0; t < N; ++t) {
+        if (t % BWD_CHUNK == 0) {
+            T *ck = ckpt + (size_t)(t / BWD_CHUNK) * L.sds;
+#pragma unroll
+            for (int i = 0; i < BWD_MGT; ++i) {
+                const int ml = g + q.G * i;
+                if (col && ml < ms) {
+                    ck[(size_t)ml * RD + c] = xr[i];
+                    ck[plane + (size_t)ml * RD + c] = xi[i];
+                }
             }
-            const T z = feat[(size_t)t * F + zoff];
-            const T nr = fma(lr, xr, fma(-li, xi, br * z)), ni = fma(lr, xi, fma(li, xr, bi * z));
-            xr = nr;
-            xi = ni;
+            if (eown) {
+                ck[eoff + tid] = er;
+                ck[eoff + q.MC + tid] = ei;
+            }
         }
-    }
-    if (has_eta) {
-        const int m = tid;
-        T er = 0, ei = 0;
-        const T lr = lam_r[m], li = lam_i[m], br = b_r[m], bi = b_i[m];
-        for (int t = 0; t < N; ++t) {
-            if (t % BWD_CHUNK == 0) {
-                T *ck = ckpt + (size_t)(t / BWD_CHUNK) * L.sd;
-                ck[eoff + m] = er;
-                ck[eoff + M + m] = ei;
-            }
-            const T nr = fma(lr, er, fma(-li, ei, br)), ni = fma(lr, ei, fma(li, er, bi));
+        const T z = col ? feat[(size_t)t * F + R + c] : T(0);
+#pragma unroll
+        for (int i = 0; i < BWD_MGT; ++i) {
+            const T nr = fma(lr[i], xr[i], fma(-li[i], xi[i], br[i] * z));
+            const T ni = fma(lr[i], xi[i], fma(li[i], xr[i], bi[i] * z));
+            xr[i] = nr;
+            xi[i] = ni;
+        }
+        if (eown) {
+            const T nr = fma(elr, er, fma(-eli, ei, ebr)), ni = fma(elr, ei, fma(eli, er, ebi));
             er = nr;
             ei = ni;
         }
+        if (eta_ro) {
+            // a_t of the slice's modes: sum over the group's key columns
+            const T xq = (col && c < R) ? feat[(size_t)t * F + c] : T(0);
+            T v[2 * BWD_MGT];
+#pragma unroll
+            for (int i = 0; i < BWD_MGT; ++i) {
+                v[2 * i] = xq * xr[i];
+                v[2 * i + 1] = xq * xi[i];
+            }
+            const T s1 = warp_reduce_scatter<2 * BWD_MGT>(v, lane);
+            if ((lane & 1) == 0) red[warp][rs_index<2 * BWD_MGT>(lane)] = s1;
+            __syncthreads();
+            if (tid < q.G * 2 * BWD_MGT) {
+                const int gg = tid / (2 * BWD_MGT), k = tid % (2 * BWD_MGT);
+                T sum = 0;
+                for (int w = 0; w < gwarps; ++w) sum += red[gg * gwarps + w][k];
+                am[k & 1][gg * BWD_MGT + (k >> 1)] = sum;  // [re/im][group * MGT + i]
+            }
+            __syncthreads();
+            // numerator part of value column c - R, denominator part of the eta entries
+            T pn = 0;
+            if (col && c >= R)
+#pragma unroll
+                for (int i = 0; i < BWD_MGT; ++i) pn += am[0][g * BWD_MGT + i] * xr[i] - am[1][g * BWD_MGT + i] * xi[i];
+            part[tid] = pn;
+            T pd = 0;
+            if (eown) {
+                const int gg = tid % q.G, i = tid / q.G;  // slice-local mode tid = gg + G i
+                pd = am[0][gg * BWD_MGT + i] * er - am[1][gg * BWD_MGT + i] * ei;
+            }
+            pd = warp_sum_t(pd);
+            __syncthreads();
+            if (tid < d) {
+                T sum = 0;
+                for (int gg = 0; gg < q.G; ++gg) sum += part[gg * q.RDw + R + tid];
+                nd[(size_t)t * (d + 1) + tid] = sum;
+            }
+            if (lane == 0) red[warp][0] = pd;
+            __syncthreads();
+            if (tid == 0) {
+                T sum = 0;
+                for (int w = 0; w < BWD_WARPS; ++w) sum += red[w][0];
+                nd[(size_t)t * (d + 1) + d] = sum;
+            }
+            __syncthreads();
+        }
     }
-    // adjoint accumulators start at zero
-    for (size_t e = tid; e < L.sd; e += BWD_THREADS) {
-        Y[e] = 0;
-        LB[e] = 0;
-        BB[e] = 0;
-    }
-    __syncthreads();
+}
 
-    const size_t sdout = (size_t)a.H * d;
-    const size_t base_o = ((size_t)b * N * H + h) * d;
+// eta readout: per position, the numerator and denominator over all slices, then
+// 1 / den and gd = -(g . num) / den^2 (one warp per position)
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_scan_nd_kernel(BackwardArgs a, T *ws, BwdLayout L) {
+    const int d = a.d, H = a.H, N = a.N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles = (N + 7) / 8;
+    const int unit = blockIdx.x / tiles, t = (blockIdx.x % tiles) * 8 + warp;
+    if (t >= N) return;
+    const int b = unit / H, h = unit % H;
+    T *base = ws + (size_t)unit * L.per_unit;
+    const T *nd = base + L.nd;
+    const size_t base_o = ((size_t)b * N * H + h) * d, so = (size_t)H * d;
+    T gn = 0, den = 0;
+    for (int j = lane; j <= d; j += 32) {
+        T sum = 0;
+        for (int s = 0; s < L.S; ++s) sum += nd[((size_t)s * N + t) * (d + 1) + j];
+        if (j < d)
+            gn = fma((T)load_in(a.dout, a.dtype, base_o + (size_t)t * so + j), sum, gn);
+        else
+            den = sum;
+    }
+    gn = warp_sum_t(gn);
+    den = warp_sum_t(den);
+    if (lane == 0) {
+        base[L.gsc + 2 * (size_t)t] = T(1) / den;
+        base[L.gsc + 2 * (size_t)t + 1] = -gn / (den * den);
+    }
+}
+
+// Phase B: the adjoint, chunk by chunk from the end, through the chunk's recomputed states.
+template <typename T>
+__global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_b_kernel(BackwardArgs a, T *ws, BwdLayout L) {
+    __shared__ T red[BWD_WARPS][2 * BWD_MGT];
+    __shared__ T am[2][BWD_THREADS / 32 * BWD_MGT];   // a_t (re, im), [group * MGT + i]
+    __shared__ T abm[2][BWD_THREADS / 32 * BWD_MGT];  // abar_t
+    __shared__ T part[2][BWD_THREADS];                // per-thread dz and dxi(q) parts
+    const int R = a.R, d = a.d, H = a.H, N = a.N, M = a.M, RD = R + d;
+    const BwdSlicing q = BwdSlicing::of(R, d, M);
+    const int unit = blockIdx.x / q.S, sl = blockIdx.x % q.S, h = unit % H, b = unit / H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = tid / q.RDw, c = tid % q.RDw, ms = q.ms(sl, M);
+    const bool col = g < q.G && c < RD;
+    const bool eta_ro = (a.flags & IDA_READOUT_ETA) != 0;
+    const int gwarps = q.RDw / 32;
+    T *base = ws + (size_t)unit * L.per_unit;
+    const T *feat = base + L.feat;
+    T *gfeat = base + L.gfeat + (size_t)sl * N * (2 * (size_t)R + d);
+    const T *ckpt = base + L.ckpt + (size_t)sl * L.nck * L.sds;
+    T *xbuf = base + L.xbuf + (size_t)sl * (BWD_CHUNK + 1) * L.sds;
+    const size_t F = 2 * (size_t)R + d, plane = (size_t)q.MC * RD, eoff = 2 * plane;
+    T lr[BWD_MGT], li[BWD_MGT], br[BWD_MGT], bi[BWD_MGT];
+    T yr[BWD_MGT], yi[BWD_MGT], lbr[BWD_MGT], lbi[BWD_MGT], bbr[BWD_MGT], bbi[BWD_MGT];
+#pragma unroll
+    for (int i = 0; i < BWD_MGT; ++i) {
+        const int ml = g + q.G * i, m = sl * q.MC + ml;
+        const bool ok = col && ml < ms;
+        lr[i] = ok ? (T)a.lambda[((size_t)h * M + m) * 2] : T(0);
+        li[i] = ok ? (T)a.lambda[((size_t)h * M + m) * 2 + 1] : T(0);
+        br[i] = ok ? (T)a.Bvec[((size_t)h * M + m) * 2] : T(0);
+        bi[i] = ok ? (T)a.Bvec[((size_t)h * M + m) * 2 + 1] : T(0);
+        yr[i] = yi[i] = lbr[i] = lbi[i] = bbr[i] = bbi[i] = 0;
+    }
+    const bool eown = tid < ms;
+    const int eg = tid % q.G, ei_ = tid / q.G;  // slice-local mode tid = eg + G ei_
+    T elr = 0, eli = 0, ebr = 0, ebi = 0, yer = 0, yei = 0, lber = 0, lbei = 0, bber = 0, bbei = 0;
+    if (eown) {
+        const int m = sl * q.MC + tid;
+        elr = (T)a.lambda[((size_t)h * M + m) * 2];
+        eli = (T)a.lambda[((size_t)h * M + m) * 2 + 1];
+        ebr = (T)a.Bvec[((size_t)h * M + m) * 2];
+        ebi = (T)a.Bvec[((size_t)h * M + m) * 2 + 1];
+    }
+    const size_t base_o = ((size_t)b * N * H + h) * d, so = (size_t)H * d;
     for (int k = L.nck - 1; k >= 0; --k) {
         const int t0 = k * BWD_CHUNK, len = min(BWD_CHUNK, N - t0);
-        // Phase B1: the chunk's states, xbuf[i] = X_{t0 - 1 + i}
-        const T *ck = ckpt + (size_t)k * L.sd;
-        for (int m = 0; m < M && col; ++m) {
-            T xr = ck[(size_t)m * RD + c], xi = ck[plane + (size_t)m * RD + c];
-            const T lr = lam_r[m], li = lam_i[m], br = b_r[m], bi = b_i[m];
-            xbuf[(size_t)m * RD + c] = xr;
-            xbuf[plane + (size_t)m * RD + c] = xi;
-            for (int i = 0; i < len; ++i) {
-                const T z = feat[(size_t)(t0 + i) * F + zoff];
-                const T nr = fma(lr, xr, fma(-li, xi, br * z)), ni = fma(lr, xi, fma(li, xr, bi * z));
-                xr = nr;
-                xi = ni;
-                T *xb = xbuf + (size_t)(i + 1) * L.sd;
-                xb[(size_t)m * RD + c] = xr;
-                xb[plane + (size_t)m * RD + c] = xi;
+        // the chunk's states: xbuf[i] = X_{t0 - 1 + i} for my elements
+        const T *ck = ckpt + (size_t)k * L.sds;
+        {
+            T xr[BWD_MGT], xi[BWD_MGT];
+#pragma unroll
+            for (int i = 0; i < BWD_MGT; ++i) {
+                const int ml = g + q.G * i;
+                const bool ok = col && ml < ms;
+                xr[i] = ok ? ck[(size_t)ml * RD + c] : T(0);
+                xi[i] = ok ? ck[plane + (size_t)ml * RD + c] : T(0);
+                if (ok) {
+                    xbuf[(size_t)ml * RD + c] = xr[i];
+                    xbuf[plane + (size_t)ml * RD + c] = xi[i];
+                }
             }
-        }
-        if (has_eta) {
-            const int m = tid;
-            T er = ck[eoff + m], ei = ck[eoff + M + m];
-            const T lr = lam_r[m], li = lam_i[m], br = b_r[m], bi = b_i[m];
-            xbuf[eoff + m] = er;
-            xbuf[eoff + M + m] = ei;
-            for (int i = 0; i < len; ++i) {
-                const T nr = fma(lr, er, fma(-li, ei, br)), ni = fma(lr, ei, fma(li, er, bi));
-                er = nr;
-                ei = ni;
-                T *xb = xbuf + (size_t)(i + 1) * L.sd;
-                xb[eoff + m] = er;
-                xb[eoff + M + m] = ei;
+            T er = eown ? ck[eoff + tid] : T(0), e_i = eown ? ck[eoff + q.MC + tid] : T(0);
+            if (eown) {
+                xbuf[eoff + tid] = er;
+                xbuf[eoff + q.MC + tid] = e_i;
+            }
+            for (int j = 0; j < len; ++j) {
+                const T z = col ? feat[(size_t)(t0 + j) * F + R + c] : T(0);
+                T *xb = xbuf + (size_t)(j + 1) * L.sds;
+#pragma unroll
+                for (int i = 0; i < BWD_MGT; ++i) {
+                    const T nr = fma(lr[i], xr[i], fma(-li[i], xi[i], br[i] * z));
+                    const T ni = fma(lr[i], xi[i], fma(li[i], xr[i], bi[i] * z));
+                    xr[i] = nr;
+                    xi[i] = ni;
+                    const int ml = g + q.G * i;
+                    if (col && ml < ms) {
+                        xb[(size_t)ml * RD + c] = nr;
+                        xb[plane + (size_t)ml * RD + c] = ni;
+                    }
+                }
+                if (eown) {
+                    const T nr = fma(elr, er, fma(-eli, e_i, ebr)), ni = fma(elr, e_i, fma(eli, er, ebi));
+                    er = nr;
+                    e_i = ni;
+                    xb[eoff + tid] = nr;
+                    xb[eoff + q.MC + tid] = ni;
+                }
             }
         }
         __syncthreads();
-        // Phase B2: positions of the chunk, last first
-        for (int i = len - 1; i >= 0; --i) {
-            const int t = t0 + i;
-            const T *X = xbuf + (size_t)(i + 1) * L.sd;   // X_t
-            const T *Xp = xbuf + (size_t)i * L.sd;        // X_{t-1}
+        for (int j = len - 1; j >= 0; --j) {
+            const int t = t0 + j;
+            const T *X = xbuf + (size_t)(j + 1) * L.sds, *Xp = xbuf + (size_t)j * L.sds;
             const T *frow = feat + (size_t)t * F;
-            const T xq = c < R ? frow[c] : T(0);
-            // a_t[m] = sum_c xi(q)[c] U_t[m, c]: per-warp partials, then a fixed-order sum
-            for (int m = 0; m < M; ++m) {
-                T pr = 0, pi = 0;
-                if (c < R) {
-                    pr = xq * X[(size_t)m * RD + c];
-                    pi = xq * X[plane + (size_t)m * RD + c];
-                }
-                pr = warp_sum_t(pr);
-                pi = warp_sum_t(pi);
-                if (lane == 0) {
-                    red[(size_t)warp * 2 * M + m] = pr;
-                    red[(size_t)warp * 2 * M + M + m] = pi;
-                }
-            }
-            __syncthreads();
-            for (int m = tid; m < M; m += BWD_THREADS) {
-                T sr = 0, si = 0;
-                for (int w = 0; w < BWD_WARPS; ++w) {
-                    sr += red[(size_t)w * 2 * M + m];
-                    si += red[(size_t)w * 2 * M + M + m];
-                }
-                a_r[m] = sr;
-                a_i[m] = si;
-            }
-            __syncthreads();
-            // gn = g (/ den), gd = -(g . o) / den for the eta readout
-            T g = 0;
-            if (c >= R && col) g = (T)load_in(a.dout, a.dtype, base_o + (size_t)t * sdout + (c - R));
-            T gd = 0;
+            const T xq = (col && c < R) ? frow[c] : T(0);
+            const T zc = col ? frow[R + c] : T(0);
+            T gsn = 1, gd = 0;
             if (eta_ro) {
-                // num[j] (thread j = c - R) and den
-                T num = 0;
-                if (c >= R && col)
-                    for (int m = 0; m < M; ++m)
-                        num += a_r[m] * X[(size_t)m * RD + c] - a_i[m] * X[plane + (size_t)m * RD + c];
-                T dpart = 0;
-                if (has_eta) dpart = a_r[tid] * X[eoff + tid] - a_i[tid] * X[eoff + M + tid];
-                // den (sum over modes) and g . num (sum over value columns), fixed order
-                T s1 = warp_sum_t(dpart), s2 = warp_sum_t(g * num);
-                if (lane == 0) {
-                    scal[warp] = s1;
-                    scal[BWD_WARPS + warp] = s2;
-                }
-                __syncthreads();
-                T den = 0, gnum = 0;
-                for (int w = 0; w < BWD_WARPS; ++w) {
-                    den += scal[w];
-                    gnum += scal[BWD_WARPS + w];
-                }
-                g = g / den;
-                gd = -gnum / (den * den);
-                __syncthreads();  // scal reused below
+                gsn = base[L.gsc + 2 * (size_t)t];
+                gd = base[L.gsc + 2 * (size_t)t + 1];
             }
-            // abar[m] = sum_j conj(Gamma[m, j]) gn[j] + conj(eta[m]) gd
-            for (int m = 0; m < M; ++m) {
-                T pr = 0, pi = 0;
-                if (c >= R && col) {
-                    pr = X[(size_t)m * RD + c] * g;
-                    pi = -X[plane + (size_t)m * RD + c] * g;
+            const T gn = (col && c >= R) ? (T)load_in(a.dout, a.dtype, base_o + (size_t)t * so + (c - R)) * gsn : T(0);
+            T ur[BWD_MGT], ui[BWD_MGT];
+#pragma unroll
+            for (int i = 0; i < BWD_MGT; ++i) {
+                const int ml = g + q.G * i;
+                const bool ok = col && ml < ms;
+                ur[i] = ok ? X[(size_t)ml * RD + c] : T(0);
+                ui[i] = ok ? X[plane + (size_t)ml * RD + c] : T(0);
+            }
+            // a_t (key columns) and the Gamma part of abar_t (value columns), summed over the group
+            {
+                T v[2 * BWD_MGT];
+#pragma unroll
+                for (int i = 0; i < BWD_MGT; ++i) {
+                    v[2 * i] = xq * ur[i];
+                    v[2 * i + 1] = xq * ui[i];
                 }
-                pr = warp_sum_t(pr);
-                pi = warp_sum_t(pi);
-                if (lane == 0) {
-                    red[(size_t)warp * 2 * M + m] = pr;
-                    red[(size_t)warp * 2 * M + M + m] = pi;
-                }
+                const T s1 = warp_reduce_scatter<2 * BWD_MGT>(v, lane);
+                if ((lane & 1) == 0) red[warp][rs_index<2 * BWD_MGT>(lane)] = s1;
             }
             __syncthreads();
-            for (int m = tid; m < M; m += BWD_THREADS) {
-                T sr = 0, si = 0;
-                for (int w = 0; w < BWD_WARPS; ++w) {
-                    sr += red[(size_t)w * 2 * M + m];
-                    si += red[(size_t)w * 2 * M + M + m];
-                }
-                if (eta_ro) {
-                    sr += X[eoff + m] * gd;
-                    si -= X[eoff + M + m] * gd;
-                }
-                ab_r[m] = sr;
-                ab_i[m] = si;
+            if (tid < q.G * 2 * BWD_MGT) {
+                const int gg = tid / (2 * BWD_MGT), kk = tid % (2 * BWD_MGT);
+                T sum = 0;
+                for (int w = 0; w < gwarps; ++w) sum += red[gg * gwarps + w][kk];
+                am[kk & 1][gg * BWD_MGT + (kk >> 1)] = sum;
             }
             __syncthreads();
-            // adjoint update of my column, then the column's gradients
-            if (col) {
-                T dxq = 0, dz = 0;
-                const T zc = frow[zoff];
-                for (int m = 0; m < M; ++m) {
-                    const size_t er = (size_t)m * RD + c, ei = plane + er;
-                    T dr, di;  // direct adjoint of X_t[m, c]
-                    if (c < R) {
-                        dr = ab_r[m] * xq;
-                        di = ab_i[m] * xq;
-                    } else {
-                        dr = a_r[m] * g;
-                        di = -a_i[m] * g;
-                    }
-                    // Y_t = D_t + conj(lambda) Y_{t+1}
-                    const T yr0 = Y[er], yi0 = Y[ei];
-                    const T yr = dr + lam_r[m] * yr0 + lam_i[m] * yi0;
-                    const T yi = di + lam_r[m] * yi0 - lam_i[m] * yr0;
-                    Y[er] = yr;
-                    Y[ei] = yi;
-                    // dz = sum_m Re(conj(B) Y), lambda_bar += conj(X_{t-1}) Y, B_bar += z Y
-                    dz += b_r[m] * yr + b_i[m] * yi;
-                    const T pr = Xp[er], pi = Xp[ei];
-                    LB[er] += pr * yr + pi * yi;
-                    LB[ei] += pr * yi - pi * yr;
-                    BB[er] += zc * yr;
-                    BB[ei] += zc * yi;
-                    if (c < R) dxq += ab_r[m] * X[er] + ab_i[m] * X[ei];  // Re(conj(abar) U)
+            {
+                T v[2 * BWD_MGT];  // conj(Gamma) gn
+#pragma unroll
+                for (int i = 0; i < BWD_MGT; ++i) {
+                    v[2 * i] = ur[i] * gn;
+                    v[2 * i + 1] = -ui[i] * gn;
+                }
+                const T s1 = warp_reduce_scatter<2 * BWD_MGT>(v, lane);
+                if ((lane & 1) == 0) red[warp][rs_index<2 * BWD_MGT>(lane)] = s1;
+            }
+            __syncthreads();
+            if (tid < q.G * 2 * BWD_MGT) {
+                const int gg = tid / (2 * BWD_MGT), kk = tid % (2 * BWD_MGT);
+                T sum = 0;
+                for (int w = 0; w < gwarps; ++w) sum += red[gg * gwarps + w][kk];
+                const int ml = gg + q.G * (kk >> 1);
+                if (eta_ro && ml < ms) {  // + conj(eta_t) gd
+                    sum += (kk & 1) ? -X[eoff + q.MC + ml] * gd : X[eoff + ml] * gd;
+                }
+                abm[kk & 1][gg * BWD_MGT + (kk >> 1)] = sum;
+            }
+            __syncthreads();
+            // adjoint update of my elements; my parts of dz and dxi(q)
+            T dz = 0, dxq = 0;
+#pragma unroll
+            for (int i = 0; i < BWD_MGT; ++i) {
+                const int ml = g + q.G * i;
+                const bool ok = col && ml < ms;
+                const T ar = am[0][g * BWD_MGT + i], aim = am[1][g * BWD_MGT + i];
+                const T abr = abm[0][g * BWD_MGT + i], abi = abm[1][g * BWD_MGT + i];
+                T dr, di;
+                if (c < R) {
+                    dr = abr * xq;
+                    di = abi * xq;
+                } else {
+                    dr = ar * gn;
+                    di = -aim * gn;
+                }
+                if (!ok) dr = di = 0;
+                const T nyr = dr + lr[i] * yr[i] + li[i] * yi[i];
+                const T nyi = di + lr[i] * yi[i] - li[i] * yr[i];
+                yr[i] = nyr;
+                yi[i] = nyi;
+                const T pr = ok ? Xp[(size_t)ml * RD + c] : T(0), pi = ok ? Xp[plane + (size_t)ml * RD + c] : T(0);
+                lbr[i] += pr * nyr + pi * nyi;
+                lbi[i] += pr * nyi - pi * nyr;
+                bbr[i] += zc * nyr;
+                bbi[i] += zc * nyi;
+                dz += br[i] * nyr + bi[i] * nyi;
+                dxq += abr * ur[i] + abi * ui[i];
+            }
+            if (eown && eta_ro) {
+                const T ar = am[0][eg * BWD_MGT + ei_], aim = am[1][eg * BWD_MGT + ei_];
+                const T dr = ar * gd, di = -aim * gd;
+                const T nyr = dr + elr * yer + eli * yei;
+                const T nyi = di + elr * yei - eli * yer;
+                yer = nyr;
+                yei = nyi;
+                const T pr = Xp[eoff + tid], pi = Xp[eoff + q.MC + tid];
+                lber += pr * nyr + pi * nyi;
+                lbei += pr * nyi - pi * nyr;
+                bber += nyr;
+                bbei += nyi;
+            }
+            part[0][tid] = dz;
+            part[1][tid] = (c < R) ? dxq : T(0);
+            __syncthreads();
+            // the slice's dz (all columns) and dxi(q) (key columns): sum over the groups
+            for (int cc = tid; cc < RD; cc += BWD_THREADS) {
+                T sz = 0, sq = 0;
+                for (int gg = 0; gg < q.G; ++gg) {
+                    sz += part[0][gg * q.RDw + cc];
+                    sq += part[1][gg * q.RDw + cc];
                 }
                 T *grow = gfeat + (size_t)t * F;
-                if (c < R) grow[c] = dxq;
-                grow[R + c] = dz;  // dkt for c < R, dvt for c >= R
-            }
-            if (has_eta && eta_ro) {
-                const int m = tid;
-                const size_t er = eoff + m, ei = eoff + M + m;
-                const T dr = a_r[m] * gd, di = -a_i[m] * gd;
-                const T yr0 = Y[er], yi0 = Y[ei];
-                const T yr = dr + lam_r[m] * yr0 + lam_i[m] * yi0;
-                const T yi = di + lam_r[m] * yi0 - lam_i[m] * yr0;
-                Y[er] = yr;
-                Y[ei] = yi;
-                const T pr = Xp[er], pi = Xp[ei];
-                LB[er] += pr * yr + pi * yi;
-                LB[ei] += pr * yi - pi * yr;
-                BB[er] += yr;
-                BB[ei] += yi;
+                grow[R + cc] = sz;  // dkt for cc < R, dvt for cc >= R
+                if (cc < R) grow[cc] = sq;
             }
             __syncthreads();
         }
     }
-    // per-mode sums of the lambda / B terms over the columns (and eta), in column order
+    // lambda-bar and B-bar of my modes: sum over the group's columns, then the eta terms
     T *ps = base + L.pscan;
-    for (int m = tid; m < M; m += BWD_THREADS) {
-        T lr = 0, li = 0, br = 0, bi = 0;
-        for (int cc = 0; cc < RD; ++cc) {
-            lr += LB[(size_t)m * RD + cc];
-            li += LB[plane + (size_t)m * RD + cc];
-            br += BB[(size_t)m * RD + cc];
-            bi += BB[plane + (size_t)m * RD + cc];
+    for (int i = 0; i < BWD_MGT; ++i) {
+        T v[4] = {lbr[i], lbi[i], bbr[i], bbi[i]};
+        const T s1 = warp_reduce_scatter<4>(v, lane);
+        if ((lane & 1) == 0) red[warp][rs_index<4>(lane)] = s1;
+        __syncthreads();
+        if (tid < q.G * 4) {
+            const int gg = tid / 4, kk = tid % 4;
+            const int ml = gg + q.G * i, m = sl * q.MC + ml;
+            T sum = 0;
+            for (int w = 0; w < gwarps; ++w) sum += red[gg * gwarps + w][kk];
+            if (ml < ms) part[0][kk * (BWD_THREADS / 4) + ml] = sum;
+            (void)m;
         }
-        if (eta_ro) {
-            lr += LB[eoff + m];
-            li += LB[eoff + M + m];
-            br += BB[eoff + m];
-            bi += BB[eoff + M + m];
-        }
-        ps[m] = lr;
-        ps[M + m] = li;
-        ps[2 * M + m] = br;
-        ps[3 * M + m] = bi;
+        __syncthreads();
     }
+    if (eown) {
+        const int m = sl * q.MC + tid;
+        ps[m] = part[0][0 * (BWD_THREADS / 4) + tid] + (eta_ro ? lber : T(0));
+        ps[M + m] = part[0][1 * (BWD_THREADS / 4) + tid] + (eta_ro ? lbei : T(0));
+        ps[2 * M + m] = part[0][2 * (BWD_THREADS / 4) + tid] + (eta_ro ? bber : T(0));
+        ps[3 * M + m] = part[0][3 * (BWD_THREADS / 4) + tid] + (eta_ro ? bbei : T(0));
+    }
+}
+
+// The dxi(q), dkt, dvt parts of the mode slices summed into slice 0, in slice order.
+template <typename T>
+__global__ void bwd_sum_slices_kernel(BackwardArgs a, T *ws, BwdLayout L) {
+    const size_t F = 2 * (size_t)a.R + a.d, per = (size_t)a.N * F;
+    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t units = (size_t)a.B * a.H;
+    if (e >= units * per) return;
+    const size_t unit = e / per, i = e % per;
+    T *gp = ws + unit * L.per_unit + L.gfeat;
+    T sum = gp[i];
+    for (int s = 1; s < L.S; ++s) sum += gp[(size_t)s * per + i];
+    gp[i] = sum;
 }
 
 // ---- bwd_local: RMSNorm, feature map and conv backward per position ----------------------
@@ -626,35 +827,38 @@ __global__ void bwd_reduce_kernel(BackwardArgs a, const T *ws, BwdLayout L) {
 }
 
 template <typename T>
-static size_t bwd_scan_smem(int M) {
-    return ((size_t)8 * M + (size_t)BWD_WARPS * 2 * M + BWD_WARPS * 2 + 4) * sizeof(T);
-}
-
-template <typename T>
 static size_t bwd_local_smem(int R, int d) {
     return (2 * (size_t)(BWD_TILE + 3) * R + 2 * 8 * ((size_t)R + d)) * sizeof(T);
 }
 
-size_t backward_workspace_bytes(int B, int H, int N, int d, int R, int M, int dtype, int W) {
+size_t backward_workspace_bytes(int B, int H, int N, int d, int R, int M, int dtype, int W, int flags) {
     if (B <= 0 || H <= 0 || N <= 0) return 0;
     const size_t e = dtype == IDA_F32 ? sizeof(double) : sizeof(float);
-    return BwdLayout::of(B, H, N, d, R, M, W).total * e;
+    return BwdLayout::of(B, H, N, d, R, M, W, (flags & IDA_READOUT_ETA) != 0).total * e;
 }
 
 template <typename T>
 static cudaError_t launch_backward_t(const BackwardArgs &a, void *workspace, cudaStream_t st) {
-    const BwdLayout L = BwdLayout::of(a.B, a.H, a.N, a.d, a.R, a.M, a.W);
+    const bool eta = (a.flags & IDA_READOUT_ETA) != 0;
+    const BwdLayout L = BwdLayout::of(a.B, a.H, a.N, a.d, a.R, a.M, a.W, eta);
     T *ws = static_cast<T *>(workspace);
-    const unsigned units = (unsigned)(a.B * a.H);
+    const unsigned units = (unsigned)(a.B * a.H), tiles8 = (unsigned)((a.N + 7) / 8);
     cudaError_t e;
-    bwd_features_kernel<T><<<units * (unsigned)((a.N + 7) / 8), 256, 0, st>>>(a, ws, L);
+    bwd_features_kernel<T><<<units * tiles8, 256, 0, st>>>(a, ws, L);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t s1 = bwd_scan_smem<T>(a.M);
-    if ((e = cudaFuncSetAttribute(bwd_scan_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1)) !=
-        cudaSuccess)
-        return e;
-    bwd_scan_kernel<T><<<units, BWD_THREADS, s1, st>>>(a, ws, L);
+    bwd_scan_a_kernel<T><<<units * (unsigned)L.S, BWD_THREADS, 0, st>>>(a, ws, L);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (eta) {
+        bwd_scan_nd_kernel<T><<<units * tiles8, 256, 0, st>>>(a, ws, L);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    bwd_scan_b_kernel<T><<<units * (unsigned)L.S, BWD_THREADS, 0, st>>>(a, ws, L);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (L.S > 1) {
+        const size_t n = (size_t)units * a.N * (2 * (size_t)a.R + a.d);
+        bwd_sum_slices_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a, ws, L);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     const size_t s2 = bwd_local_smem<T>(a.R, a.d);
     if ((e = cudaFuncSetAttribute(bwd_local_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2)) !=
         cudaSuccess)
@@ -685,11 +889,10 @@ ida_status check_call(int d, int R, int M, int W, int dtype, int flags, int *num
 
 extern "C" size_t ida_backward_workspace_bytes(int B, int H, int N, int d, int R, int M, int dtype, int W,
                                                int flags) {
-    (void)flags;
     if (B < 0 || H < 0 || N < 0 || d < 1 || R < 1 || M < 1 || W < 1 || W > 4 || R > 256 || d > 256 || M > 128 ||
         (dtype != IDA_F32 && dtype != IDA_BF16))
         return 0;
-    return ida::backward_workspace_bytes(B, H, N, d, R, M, dtype, W);
+    return ida::backward_workspace_bytes(B, H, N, d, R, M, dtype, W, flags);
 }
 
 extern "C" ida_status ida_backward(const void *q, const void *k, const void *v, const float *conv_w,
@@ -719,7 +922,7 @@ extern "C" ida_status ida_backward(const void *q, const void *k, const void *v, 
         return ida::fail_with(IDA_ERR_ARG, "workspace must be 16-byte aligned");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((long long)B * H == 0) return IDA_OK;
-    const size_t need = ida::backward_workspace_bytes(B, H, N, d, R, M, dtype, W);
+    const size_t need = ida::backward_workspace_bytes(B, H, N, d, R, M, dtype, W, flags);
     if (N > 0 && (!workspace || workspace_bytes < need))
         return ida::fail_with(IDA_ERR_ARG, "the backward pass needs a workspace of ida_backward_workspace_bytes(...) = " +
                                                std::to_string(need) + " bytes");

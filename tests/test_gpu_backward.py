@@ -60,7 +60,8 @@ CASES = [
     (1, 130, 1, 32, 16, 8, 2, "f32", L2),         # three chunks, the l_2 feature map
     (1, 1, 2, 8, 8, 3, 4, "f32", 0),              # one position
     (2, 50, 2, 16, 16, 7, 1, "f32", ETA | L2),    # W = 1 (no conv history)
-    (2, 150, 2, 64, 64, 64, 4, "bf16", 0),        # the tensor-core forward's shape class
+    (1, 80, 1, 64, 64, 64, 4, "f32", ETA),        # modes split over two CTAs, eta readout
+    (2, 150, 2, 64, 64, 64, 4, "bf16", 0),        # the tensor-core forward's shape class (two mode slices)
     (1, 90, 2, 64, 32, 16, 4, "bf16", L2),
 ]
 
