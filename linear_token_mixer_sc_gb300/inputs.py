@@ -86,3 +86,12 @@ def make_tokens(B: int, H: int, R: int, d: int, dtype: str, seed: int, step: int
     g.manual_seed(int(seed) * 1000003 + int(step))
     return tuple(torch.randn(s, generator=g, device=dev, dtype=torch.float32).to(tdt)
                  for s in ((B, H, R), (B, H, R), (B, H, d)))
+
+
+def make_omega(H: int, D: int, R_in: int, seed: int) -> np.ndarray:
+    """Random Fourier frequencies for the ideal-derivation workload: [H, D, R_in] drawn
+    from N(0, I / R_in) (the Gaussian kernel at the bandwidth of R_in-dimensional rows
+    with unit-variance entries), stored as float32.  The draw is an input of the layer,
+    read by the library and the oracle alike."""
+    rng = np.random.default_rng([seed, 7])
+    return np.ascontiguousarray(rng.standard_normal((H, D, R_in)) / math.sqrt(R_in), dtype=np.float32)
