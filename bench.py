@@ -53,6 +53,7 @@ PREFILL_SOURCES = ["ida_chunk.cu", "ida_seq.cu", "ida_common.cuh", "tc_sm103.cuh
 ETA_SOURCES = ["ida_seq_modes.cu", "ida_seq.cu", "ida_common.cuh", "ida_api.cu"]
 DECODE_SOURCES = ["ida_decode.cu", "ida_common.cuh", "ida_api.cu"]
 BACKWARD_SOURCES = ["ida_backward.cu", "ida_common.cuh", "ida_api.cu"]
+IDEAL_SOURCES = ["ida_ideal.cu", "ida_common.cuh", "ida_api.cu"]
 
 
 # ---------------------------------------------------------------- helpers
@@ -366,6 +367,51 @@ class Backward:
         return 3 * mixer_flops(self.w, self.w.B * self.w.H * self.w.N)
 
 
+class Ideal:
+    """One ida_forward_ideal call: the ideal interdomain layer on D random Fourier
+    frequencies per head, at the 125M-like shape (R_in = d = 64, D = 32, so the feature
+    width 2D equals R)."""
+
+    D = 32
+
+    def __init__(self, w, dev):
+        from linear_token_mixer_sc_gb300 import binding
+        self.b = binding
+        self.w, self.dev = w, dev
+        self.pd = binding.params_to_device(inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed), dev)
+        q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed)
+        self.host = [t.pin_memory() for t in (q, k, v)]
+        self.q, self.k, self.v = (t.to(dev) for t in self.host)
+        self.omega = torch.from_numpy(inputs.make_omega(w.H, self.D, w.R, w.seed)).to(dev)
+        self.out = torch.empty((w.B, w.N, w.H, w.d), dtype=self.q.dtype, device=dev)
+        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.launches_per_step = 1
+
+    def step(self):
+        self.b.ida_forward_ideal(self.q, self.k, self.v, self.omega, self.pd, out=self.out)
+
+    def step_e2e(self):
+        for src, dst in zip(self.host, (self.q, self.k, self.v)):
+            dst.copy_(src, non_blocking=True)
+        self.step()
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host), self.out.numel() * self.out.element_size()
+
+    def tokens(self):
+        return self.w.B * self.w.N
+
+    def alg_bytes(self):
+        return prefill_bytes(self.w)
+
+    def flops(self):
+        """The recurrent form on feature width 2D plus the Fourier features of q and k
+        (D x R_in products each) per position and head."""
+        w = self.w
+        return (12.0 * w.M * (2 * self.D + w.d) + 4.0 * self.D * w.R) * w.B * w.H * w.N
+
+
 def time_steps(runner, steps, warmup, dev, flush, e2e=False, sampler=None):
     """Per-step CUDA-event times (ms) on the launching stream.  With ``flush`` the L2
     is flushed before every timed step, outside the timed region, by writing a 512 MB
@@ -510,8 +556,10 @@ def sources_of(w, flags) -> list:
 
 
 def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, seed_len=None,
-            from_state=False, backward=False):
-    if backward:
+            from_state=False, backward=False, ideal=False):
+    if ideal:
+        runner = Ideal(w, dev)
+    elif backward:
         runner = Backward(w, dev, flags)
     elif w.decode_steps:
         runner = Decode(w, dev, flags, seed_len)
@@ -531,10 +579,11 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, 
     ms = sum(times) / len(times)
     ms_all = max_over_ranks(dist, ms, dev)
     value = job_value(ws, runner.tokens(), ms_all)
-    key = line_key(w, flags, from_state) + ("_backward" if backward else "")
-    traffic, per_kernel = traffic_record(key, BACKWARD_SOURCES if backward else sources_of(w, flags))
+    key = line_key(w, flags, from_state) + ("_backward" if backward else "") + ("_ideal" if ideal else "")
+    traffic, per_kernel = traffic_record(key, BACKWARD_SOURCES if backward else
+                                         IDEAL_SOURCES if ideal else sources_of(w, flags))
     rl = roofline(runner, ms, peaks, peak_kind, traffic,
-                  fp32_fma=backward or bool(flags & 1 and not w.decode_steps) or w.dtype == "f32")
+                  fp32_fma=backward or ideal or bool(flags & 1 and not w.decode_steps) or w.dtype == "f32")
     if per_kernel:
         rl["traffic_kernels"] = per_kernel
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "R": w.R, "d": w.d, "M": w.M, "W": w.W,
@@ -542,6 +591,9 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, 
            "l2": l2_note(w)}
     if backward:
         cfg["pass"] = "backward (gradients of q, k, v and every parameter)"
+    if ideal:
+        cfg["layer"] = f"ideal: random Fourier features, D = {Ideal.D} frequencies, eta ratio readout"
+        cfg["readout"] = "eta"
     if w.decode_steps:
         cfg["seed_prefill_N"] = w.N if seed_len is None else seed_len
         del cfg["N"]
@@ -651,6 +703,11 @@ def main():
         others[line_key(bw) + "_backward"] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps",
                                                                  "roofline", "e2e", "gpu_launches", "clocks",
                                                                  "config")}
+        # the ideal layer on random Fourier features, at the same shape
+        r = measure(bw, dev, args.steps, args.warmup, 0, dist, ws, peaks, peak_kind, ideal=True)
+        others[line_key(bw) + "_ideal"] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps",
+                                                              "roofline", "e2e", "gpu_launches", "clocks",
+                                                              "config")}
     if binding.ida_device_error() != 0:
         raise RuntimeError("a kernel reported a device error")
 

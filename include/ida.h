@@ -271,6 +271,29 @@ IDA_API size_t ida_backward_workspace_bytes(int B, int H, int N, int d, int R,
                                             int M, int dtype, int W, int flags);
 
 /*
+ * The ideal interdomain layer on random Fourier features: the layer the paper
+ * derives before its scalable form ("Interdomain Attention: Beyond
+ * Token-Level Key-Value Memory", translated paper text, section 3.1: the
+ * finite-feature ratio of Eq. 4 with the Fourier features of Eqs. 5-6, read
+ * out through the recurrent state of Fig. 1b).  Per (b,h) unit:
+ *   xi(x)  = D^-1/2 [cos(Omega_h x); sin(Omega_h x)]  (feature width 2D),
+ *   X_t    = lambda o X_{t-1} + B o [xi(k_t); v_t],  eta_t = lambda o eta_{t-1} + B,
+ *   o_t    = Re(xi(q_t)^T U_t^T Gamma_t) / Re(xi(q_t)^T U_t^T eta_t),
+ * from the zero state, with no conv and no normalisation (the derivation has
+ * neither).
+ *   q, k   [B, N, H, R_in] dtype;  v, out [B, N, H, d] dtype;
+ *   omega  [H, D, R_in] float: the random frequencies (drawn by the caller);
+ *   lambda, Bvec [H, M, 2] float, as for ida_forward.
+ * Supported: R_in <= 256, D <= 128, d <= 256, M <= 128.  fp64 arithmetic for
+ * fp32 inputs, fp32 for bf16; deterministic.  Allocates nothing.
+ */
+IDA_API ida_status ida_forward_ideal(const void *q, const void *k, const void *v,
+                             const float *omega, const float *lambda,
+                             const float *Bvec, void *out,
+                             int B, int H, int N, int d, int R_in, int D,
+                             int M, int dtype, ida_stream_t stream);
+
+/*
  * Self-test of the failure reporting (no counterpart in the paper: a property
  * of the library).  Launches one warp on `stream` that waits, through the
  * bounded-wait helper every prefill kernel uses, on an mbarrier nothing

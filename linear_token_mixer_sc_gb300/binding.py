@@ -22,7 +22,8 @@ IDA_PATH_SEQUENTIAL = 256
 
 EXPORTED = ("ida_state_floats", "ida_forward", "ida_forward_ws", "ida_forward_from", "ida_forward_workspace_bytes",
             "ida_forward_noalloc", "ida_decode_step", "ida_device_error", "ida_status_str",
-            "ida_last_error", "ida_selftest_bounded_wait", "ida_backward", "ida_backward_workspace_bytes")
+            "ida_last_error", "ida_selftest_bounded_wait", "ida_backward", "ida_backward_workspace_bytes",
+            "ida_forward_ideal")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +70,8 @@ def load() -> ctypes.CDLL:
                                        _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp]
             L.ida_backward_workspace_bytes.restype = ctypes.c_size_t
             L.ida_backward_workspace_bytes.argtypes = [_i] * 9
+            L.ida_forward_ideal.restype = _i
+            L.ida_forward_ideal.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp]
             L.ida_selftest_bounded_wait.restype = _i
             L.ida_selftest_bounded_wait.argtypes = [ctypes.c_longlong, _vp]
             L.ida_device_error.restype = _i
@@ -293,6 +296,32 @@ def ida_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict
                              int(flags), _p(workspace), wbytes, _stream_handle(stream))
     _check(st, "ida_backward")
     return g
+
+
+def ida_forward_ideal(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, omega: torch.Tensor, params: dict,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The ideal layer on random Fourier features.  q, k [B,N,H,R_in], v [B,N,H,d] CUDA
+    tensors of one dtype; omega [H,D,R_in] float32 CUDA; ``params`` as for ida_forward (only
+    lambda and Bvec are read).  Returns out [B,N,H,d]."""
+    for t in (q, k, v, omega):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("q, k, v and omega must be contiguous CUDA tensors")
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    if omega.dtype != torch.float32:
+        raise TypeError("omega must be float32")
+    B, N, H, Rin = q.shape
+    d = v.shape[3]
+    D = omega.shape[1]
+    lam, bv = params["lambda"], params["Bvec"]
+    M = lam.shape[1]
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=q.dtype, device=q.device)
+    st = load().ida_forward_ideal(_p(q), _p(k), _p(v), _p(omega), _p(lam), _p(bv), _p(out), B, H, N, d, Rin, D, M,
+                                  dt, _stream_handle(stream))
+    _check(st, "ida_forward_ideal")
+    return out
 
 
 def ida_selftest_bounded_wait(limit_cycles: int, stream=None) -> None:
