@@ -41,3 +41,10 @@ def test_rotations_compose_and_frequencies_follow_the_base():
     # positions advance along axis 1
     y = ro.rope(np.repeat(x, 3, axis=1), pos0=4)
     np.testing.assert_allclose(y[:, 2], ro.rope(x, 6)[:, 0], rtol=1e-14)
+
+
+def test_adjacent_channels_form_the_pairs():
+    """The reading: channels (2i, 2i + 1) rotate together (not i and i + R/2)."""
+    x = np.zeros((1, 1, 1, 4))
+    x[..., 0] = 1.0
+    np.testing.assert_allclose(ro.rope(x, 1)[0, 0, 0], [np.cos(1.0), np.sin(1.0), 0.0, 0.0], atol=1e-15)
