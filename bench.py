@@ -54,6 +54,7 @@ ETA_SOURCES = ["ida_seq_modes.cu", "ida_seq.cu", "ida_common.cuh", "ida_api.cu"]
 DECODE_SOURCES = ["ida_decode.cu", "ida_common.cuh", "ida_api.cu"]
 BACKWARD_SOURCES = ["ida_backward.cu", "ida_common.cuh", "ida_api.cu"]
 IDEAL_SOURCES = ["ida_ideal.cu", "ida_common.cuh", "ida_api.cu"]
+ROPE_SOURCES = ["ida_rope.cu", "ida_common.cuh", "ida_api.cu"]
 
 
 # ---------------------------------------------------------------- helpers
@@ -337,7 +338,11 @@ class Backward:
         self.grads = {"q": torch.empty_like(self.q), "k": torch.empty_like(self.k), "v": torch.empty_like(self.v)}
         self.grads.update({n: torch.empty_like(self.pd[n]) for n in ("conv_w", "norm_w", "bias", "lambda", "Bvec")})
         self.gq_host = torch.empty(self.q.shape, dtype=self.q.dtype).pin_memory()
-        self.launches_per_step = 4  # features, scan, position-local backward, parameter reduction
+        # features, forward scan, adjoint scan, position-local backward and parameter reduction,
+        # plus the eta readout's scaling pass and the sum over mode slices when the modes
+        # are split over CTAs (slices of 8 x floor(512 / (R + d rounded up to 32)) modes)
+        slice_modes = 8 * (512 // ((w.R + w.d + 31) // 32 * 32))
+        self.launches_per_step = 5 + (flags & 1) + (w.M > slice_modes)
 
     def step(self):
         self.b.ida_backward(self.q, self.k, self.v, self.pd, self.dout, flags=self.flags, workspace=self.ws,
@@ -410,6 +415,47 @@ class Ideal:
         (D x R_in products each) per position and head."""
         w = self.w
         return (12.0 * w.M * (2 * self.D + w.d) + 4.0 * self.D * w.R) * w.B * w.H * w.N
+
+
+class Rope:
+    """One ida_rope call: rotary position embeddings on q and k of the prefill workload,
+    in place (HBM-bound: q and k read and written once)."""
+
+    def __init__(self, w, dev):
+        from linear_token_mixer_sc_gb300 import binding
+        self.b = binding
+        self.w, self.dev = w, dev
+        q, k, _ = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed)
+        self.host = [t.pin_memory() for t in (q, k)]
+        self.q, self.k = (t.to(dev) for t in self.host)
+        self.back = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in self.host]
+        self.launches_per_step = 1
+
+    def step(self):
+        self.b.ida_rope(self.q, self.k)
+
+    def step_e2e(self):
+        for src, dst in zip(self.host, (self.q, self.k)):
+            dst.copy_(src, non_blocking=True)
+        self.step()
+        for src, dst in zip((self.q, self.k), self.back):
+            dst.copy_(src, non_blocking=True)
+
+    def e2e_bytes(self):
+        n = sum(t.numel() * t.element_size() for t in self.host)
+        return n, n
+
+    def tokens(self):
+        return self.w.B * self.w.N
+
+    def alg_bytes(self):
+        """q and k read once and written once."""
+        return 2 * sum(t.numel() * t.element_size() for t in self.host)
+
+    def flops(self):
+        """Six flops per channel pair (four products, two sums), q and k."""
+        w = self.w
+        return 2 * 6.0 * (w.R // 2) * w.B * w.N * w.H
 
 
 def time_steps(runner, steps, warmup, dev, flush, e2e=False, sampler=None):
@@ -556,8 +602,10 @@ def sources_of(w, flags) -> list:
 
 
 def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, seed_len=None,
-            from_state=False, backward=False, ideal=False):
-    if ideal:
+            from_state=False, backward=False, ideal=False, rope=False):
+    if rope:
+        runner = Rope(w, dev)
+    elif ideal:
         runner = Ideal(w, dev)
     elif backward:
         runner = Backward(w, dev, flags)
@@ -579,11 +627,13 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, 
     ms = sum(times) / len(times)
     ms_all = max_over_ranks(dist, ms, dev)
     value = job_value(ws, runner.tokens(), ms_all)
-    key = line_key(w, flags, from_state) + ("_backward" if backward else "") + ("_ideal" if ideal else "")
-    traffic, per_kernel = traffic_record(key, BACKWARD_SOURCES if backward else
-                                         IDEAL_SOURCES if ideal else sources_of(w, flags))
+    key = line_key(w, flags, from_state) + ("_backward" if backward else "") + ("_ideal" if ideal else "") + \
+        ("_rope" if rope else "")
+    traffic, per_kernel = traffic_record(key, BACKWARD_SOURCES if backward else IDEAL_SOURCES if ideal else
+                                         ROPE_SOURCES if rope else sources_of(w, flags))
     rl = roofline(runner, ms, peaks, peak_kind, traffic,
-                  fp32_fma=backward or ideal or bool(flags & 1 and not w.decode_steps) or w.dtype == "f32")
+                  fp32_fma=not rope and (backward or ideal or bool(flags & 1 and not w.decode_steps)
+                                         or w.dtype == "f32"))
     if per_kernel:
         rl["traffic_kernels"] = per_kernel
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "R": w.R, "d": w.d, "M": w.M, "W": w.W,
@@ -594,7 +644,11 @@ def measure(w, dev, steps, warmup, flags, dist, ws, peaks, peak_kind, e2e=True, 
     if ideal:
         cfg["layer"] = f"ideal: random Fourier features, D = {Ideal.D} frequencies, eta ratio readout"
         cfg["readout"] = "eta"
-    if w.decode_steps:
+    if rope:
+        cfg = {"workload": w.name, "B": w.B, "N": w.N, "H": w.H, "R": w.R, "dtype": w.dtype,
+               "op": "rotary position embeddings on q and k, in place (base 10000, positions 0..N-1)",
+               "l2": l2_note(w)}
+    elif w.decode_steps:
         cfg["seed_prefill_N"] = w.N if seed_len is None else seed_len
         del cfg["N"]
     else:
@@ -633,6 +687,10 @@ def main():
                     help="prefill continuing from a given state (ida_forward_from)")
     ap.add_argument("--only", "--no-decode", dest="only", action="store_true",
                     help="measure the selected workload alone (no secondary lines)")
+    ap.add_argument("--line", choices=["mixer", "backward", "ideal", "rope"], default="mixer",
+                    help="what the main line measures on --workload: the mixer (default), its backward "
+                         "pass, the ideal layer on Fourier features, or RoPE on q and k (for profiling "
+                         "one of the secondary lines alone; no CPU leg)")
     ap.add_argument("--seed-len", type=int, default=None,
                     help="decode workload: length of the seeding prefill (default: the workload's 4096)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
@@ -686,7 +744,8 @@ def main():
     peaks, peak_kind = load_peaks()
 
     main_res = measure(w, dev, args.steps, args.warmup, flags, dist, ws, peaks, peak_kind,
-                       seed_len=args.seed_len, from_state=from_state)
+                       seed_len=args.seed_len, from_state=from_state, backward=args.line == "backward",
+                       ideal=args.line == "ideal", rope=args.line == "rope")
     others = {}
     if not args.only:
         for ow, of in SECONDARY:
@@ -708,13 +767,19 @@ def main():
         others[line_key(bw) + "_ideal"] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps",
                                                               "roofline", "e2e", "gpu_launches", "clocks",
                                                               "config")}
+        # rotary position embeddings on q and k of the 1.3B-like prefill
+        rw = configs.PREFILL_1P3B
+        r = measure(rw, dev, args.steps, args.warmup, 0, dist, ws, peaks, peak_kind, rope=True)
+        others[line_key(rw) + "_rope"] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps",
+                                                             "roofline", "e2e", "gpu_launches", "clocks",
+                                                             "config")}
     if binding.ida_device_error() != 0:
         raise RuntimeError("a kernel reported a device error")
 
     if rank != 0:
         return
     cpu = None
-    if args.cpu_budget > 0:
+    if args.cpu_budget > 0 and args.line == "mixer":
         cv, desc, _ = oracle_sample(w, args.cpu_budget, cores, flags)
         cpu = {"value": cv, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
                "host": f"{platform.machine()} x{cores}"}
@@ -726,6 +791,9 @@ def main():
             "config": config, "roofline": main_res["roofline"], "cpu_baseline": cpu,
             "e2e": main_res["e2e"], "gpu_launches": main_res["gpu_launches"],
             "clocks": main_res["clocks"]}
+    if args.line != "mixer":
+        line["line"] = args.line
+        line["config"] = main_res["config"]
     if others:
         line["workloads"] = others
     print(json.dumps(line))

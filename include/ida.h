@@ -294,6 +294,29 @@ IDA_API ida_status ida_forward_ideal(const void *q, const void *k, const void *v
                              int M, int dtype, ida_stream_t stream);
 
 /*
+ * Rotary position embeddings on the mixer's queries and keys, in place.  The
+ * pages embed the token mixer in a Llama-style decoder with rotary position
+ * embeddings ("Interdomain Attention: Beyond Token-Level Key-Value Memory",
+ * German technical summary, "Skalierbare Implementierung", "Architektur");
+ * the library reads that as the decoder's usual RoPE on q and k before the
+ * mixer (the pages give no formula).  Channel pairs (2i, 2i+1) of the row at
+ * position p = pos0 + t rotate by the angle p * base^(-2i/R):
+ *   x'_{2i}   = x_{2i} cos(a) - x_{2i+1} sin(a),
+ *   x'_{2i+1} = x_{2i} sin(a) + x_{2i+1} cos(a).
+ *   q, k   [B, N, H, R] dtype, contiguous, 16-byte aligned, rotated in place
+ *          (k may be NULL: only q is rotated; k must not alias q);
+ *   pos0   the position of row t = 0 (>= 0), e.g. the length already decoded;
+ *   base   the frequency base (> 1; 10000 in the Llama decoder).
+ * Supported: 8 <= R <= 256 with R % 8 == 0, H*R <= 2^24.  Angles are formed
+ * and reduced modulo 2 pi in fp64, sin / cos and the rotation in fp32 (bf16
+ * inputs are rounded back to bf16).  N == 0, B == 0 or H == 0 does nothing.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+IDA_API ida_status ida_rope(void *q, void *k, int B, int N, int H, int R,
+                            int pos0, float base, int dtype,
+                            ida_stream_t stream);
+
+/*
  * Self-test of the failure reporting (no counterpart in the paper: a property
  * of the library).  Launches one warp on `stream` that waits, through the
  * bounded-wait helper every prefill kernel uses, on an mbarrier nothing

@@ -23,7 +23,7 @@ IDA_PATH_SEQUENTIAL = 256
 EXPORTED = ("ida_state_floats", "ida_forward", "ida_forward_ws", "ida_forward_from", "ida_forward_workspace_bytes",
             "ida_forward_noalloc", "ida_decode_step", "ida_device_error", "ida_status_str",
             "ida_last_error", "ida_selftest_bounded_wait", "ida_backward", "ida_backward_workspace_bytes",
-            "ida_forward_ideal")
+            "ida_forward_ideal", "ida_rope")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +72,8 @@ def load() -> ctypes.CDLL:
             L.ida_backward_workspace_bytes.argtypes = [_i] * 9
             L.ida_forward_ideal.restype = _i
             L.ida_forward_ideal.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp]
+            L.ida_rope.restype = _i
+            L.ida_rope.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _vp]
             L.ida_selftest_bounded_wait.restype = _i
             L.ida_selftest_bounded_wait.argtypes = [ctypes.c_longlong, _vp]
             L.ida_device_error.restype = _i
@@ -322,6 +324,20 @@ def ida_forward_ideal(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, omega: 
                                   dt, _stream_handle(stream))
     _check(st, "ida_forward_ideal")
     return out
+
+
+def ida_rope(q: torch.Tensor, k: torch.Tensor | None = None, pos0: int = 0, base: float = 10000.0,
+             stream=None) -> None:
+    """Rotary position embeddings on q (and k) [B,N,H,R] CUDA tensors, in place: channel
+    pairs (2i, 2i+1) of the row at position pos0 + t rotate by (pos0 + t) * base^(-2i/R)."""
+    for t in (q, k):
+        if t is not None and not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("q and k must be contiguous CUDA tensors")
+    if k is not None and (k.shape != q.shape or k.dtype != q.dtype):
+        raise ValueError("k must match q in shape and dtype")
+    B, N, H, R = q.shape
+    st = load().ida_rope(_p(q), _p(k), B, N, H, R, int(pos0), float(base), _dtype_code(q), _stream_handle(stream))
+    _check(st, "ida_rope")
 
 
 def ida_selftest_bounded_wait(limit_cycles: int, stream=None) -> None:

@@ -1,0 +1,170 @@
+// ida_rope.cu -- rotary position embeddings on the mixer's q and k, in place.
+//
+// The pages embed the token mixer in a Llama-style decoder with rotary position
+// embeddings ("Interdomain Attention: Beyond Token-Level Key-Value Memory", German
+// technical summary, "Skalierbare Implementierung", "Architektur"); as in that decoder
+// the rotation is applied to the query and key rows before the mixer.  Channel pairs
+// (2i, 2i + 1) of a row at position p rotate by p * base^(-2i / R).
+//
+// One CTA per (batch row, tile of ROPE_TILE positions): the tile's cos / sin table
+// [ROPE_TILE][R / 2] is built in shared memory first, its angles reduced modulo 2 pi in
+// fp64 (positions reach 1e4 radians and more, where an fp32 angle would already be off
+// by 1e-3), then every head of the tile's q rows, and of its k rows with the same
+// table, is rotated with 16-byte loads and stores.  HBM-bound: each element is read and
+// written once.
+#include <cstdint>
+#include <string>
+
+#include "ida_common.cuh"
+
+namespace ida {
+
+constexpr int ROPE_TILE = 8;
+constexpr int ROPE_THREADS = 256;
+constexpr int ROPE_UNROLL = 4;  // 16-byte vectors in flight per thread
+
+template <typename E>
+struct RopeVec;  // 16 bytes of elements
+template <>
+struct RopeVec<float> {
+    static constexpr int n = 4;
+};
+template <>
+struct RopeVec<__nv_bfloat16> {
+    static constexpr int n = 8;
+};
+
+__device__ __forceinline__ void rope_unpack(const uint4 &u, float *x, float) {
+    x[0] = __uint_as_float(u.x);
+    x[1] = __uint_as_float(u.y);
+    x[2] = __uint_as_float(u.z);
+    x[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ uint4 rope_pack(const float *x, float) {
+    return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
+}
+__device__ __forceinline__ void rope_unpack(const uint4 &u, float *x, __nv_bfloat16) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+}
+__device__ __forceinline__ uint4 rope_pack(const float *x, __nv_bfloat16) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        w[e] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename E>
+__device__ __forceinline__ uint4 *rope_vec(void *q, void *k, size_t off, int vecs, int e) {
+    constexpr int V = RopeVec<E>::n;
+    E *x = static_cast<E *>(e < vecs ? q : k);
+    return reinterpret_cast<uint4 *>(x + off + (size_t)(e < vecs ? e : e - vecs) * V);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, int N, int H, int R, int pos0,
+                                                            double log2_base) {
+    __shared__ double inv[128];                   // base^(-2i / R), i < R / 2
+    extern __shared__ __align__(16) float cs[];   // [ROPE_TILE][R / 2][2]: cos, sin
+    constexpr int V = RopeVec<E>::n;
+    const int tiles = (N + ROPE_TILE - 1) / ROPE_TILE;
+    const int b = blockIdx.x / tiles, t0 = (blockIdx.x % tiles) * ROPE_TILE;
+    const int len = min(ROPE_TILE, N - t0), half = R / 2;
+    const size_t row = (size_t)H * R;  // elements of one position
+    const size_t off = ((size_t)b * N + t0) * row;
+    // 16-byte vectors of the tile: q's, then k's; a thread takes ROPE_UNROLL of them per
+    // round, the next round's loads issued before the current round is rotated
+    const int vecs = (int)(len * row / V), total = k ? 2 * vecs : vecs;
+    uint4 cur[ROPE_UNROLL], nxt[ROPE_UNROLL];
+#pragma unroll
+    for (int u = 0; u < ROPE_UNROLL; ++u) {
+        const int e = threadIdx.x + u * ROPE_THREADS;
+        if (e < total) cur[u] = __ldcs(rope_vec<E>(q, k, off, vecs, e));
+    }
+    // the table, built while the first loads are in flight.  fp64 is scarce on this part:
+    // one exp2 per frequency, then a multiply and a reduction to [-pi, pi] per (position,
+    // frequency), before the fp32 sin / cos
+    for (int i = threadIdx.x; i < half; i += ROPE_THREADS) inv[i] = exp2(-2.0 * i / R * log2_base);
+    __syncthreads();
+    const double two_pi = 6.283185307179586476925286766559, inv_two_pi = 0.15915494309189533576888376337251;
+    for (int e = threadIdx.x; e < len * half; e += ROPE_THREADS) {
+        const int tt = e / half, i = e % half;
+        const double ang = ((double)pos0 + (double)(t0 + tt)) * inv[i];
+        const float red = (float)fma(-two_pi, rint(ang * inv_two_pi), ang);
+        float sn, cn;
+        sincosf(red, &sn, &cn);
+        cs[2 * e] = cn;
+        cs[2 * e + 1] = sn;
+    }
+    __syncthreads();
+    for (int e0 = threadIdx.x; e0 < total; e0 += ROPE_UNROLL * ROPE_THREADS) {
+#pragma unroll
+        for (int u = 0; u < ROPE_UNROLL; ++u) {
+            const int e = e0 + (u + ROPE_UNROLL) * ROPE_THREADS;
+            if (e < total) nxt[u] = __ldcs(rope_vec<E>(q, k, off, vecs, e));
+        }
+#pragma unroll
+        for (int u = 0; u < ROPE_UNROLL; ++u) {
+            const int e = e0 + u * ROPE_THREADS;
+            if (e >= total) break;
+            const size_t el = (size_t)(e < vecs ? e : e - vecs) * V;
+            const int tt = (int)(el / row), c0 = (int)(el % R);
+            float v[V];
+            rope_unpack(cur[u], v, E());
+#pragma unroll
+            for (int j = 0; j < V; j += 2) {
+                const float2 t = *reinterpret_cast<const float2 *>(cs + 2 * (tt * half + ((c0 + j) >> 1)));
+                const float x0 = v[j], x1 = v[j + 1];
+                v[j] = fmaf(x0, t.x, -x1 * t.y);
+                v[j + 1] = fmaf(x0, t.y, x1 * t.x);
+            }
+            __stcs(rope_vec<E>(q, k, off, vecs, e), rope_pack(v, E()));
+        }
+#pragma unroll
+        for (int u = 0; u < ROPE_UNROLL; ++u) cur[u] = nxt[u];
+    }
+}
+
+ida_status fail_with(ida_status s, const std::string &why);
+ida_status check_call(int d, int R, int M, int W, int dtype, int flags, int *num_sms, std::string &why);
+
+}  // namespace ida
+
+extern "C" ida_status ida_rope(void *q, void *k, int B, int N, int H, int R, int pos0, float base, int dtype,
+                               ida_stream_t stream) {
+    std::string why;
+    if (B < 0 || N < 0 || H < 0) return ida::fail_with(IDA_ERR_ARG, "B, N and H must be >= 0");
+    if (pos0 < 0) return ida::fail_with(IDA_ERR_ARG, "pos0 must be >= 0");
+    if (!(base > 1.0f) || !(base < 3.0e38f)) return ida::fail_with(IDA_ERR_ARG, "base must be finite and > 1");
+    if (dtype != IDA_F32 && dtype != IDA_BF16) return ida::fail_with(IDA_ERR_ARG, "dtype must be IDA_F32 or IDA_BF16");
+    if (R < 8 || R > 256 || (R % 8)) return ida::fail_with(IDA_ERR_UNSUPPORTED, "supported: 8 <= R <= 256, R % 8 == 0");
+    if ((long long)H * R > (1LL << 24)) return ida::fail_with(IDA_ERR_UNSUPPORTED, "H*R above 2^24");
+    if ((long long)B * N * H == 0) return IDA_OK;
+    if (!q) return ida::fail_with(IDA_ERR_ARG, "null pointer");
+    if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(k) & 15u) != 0)
+        return ida::fail_with(IDA_ERR_ARG, "q and k must be 16-byte aligned");
+    if (k == q) return ida::fail_with(IDA_ERR_ARG, "k must not alias q");
+    const long long tiles = (N + ida::ROPE_TILE - 1) / ida::ROPE_TILE;
+    if ((long long)B * tiles > 0x7FFFFFFFLL) return ida::fail_with(IDA_ERR_UNSUPPORTED, "too many positions");
+    int num_sms = 0;
+    ida_status s = ida::check_call(8, R, 1, 1, dtype, 0, &num_sms, why);  // device set-up, pending errors
+    if (s != IDA_OK) return ida::fail_with(s, why);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const unsigned grid = (unsigned)(B * tiles);
+    const size_t smem = (size_t)ida::ROPE_TILE * (R / 2) * 2 * sizeof(float);
+    const double lb = log2((double)base);
+    if (dtype == IDA_F32)
+        ida::rope_kernel<float><<<grid, ida::ROPE_THREADS, smem, st>>>(q, k, N, H, R, pos0, lb);
+    else
+        ida::rope_kernel<__nv_bfloat16><<<grid, ida::ROPE_THREADS, smem, st>>>(q, k, N, H, R, pos0, lb);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return ida::fail_with(IDA_ERR_CUDA, std::string("rope launch: ") + cudaGetErrorString(e));
+    return IDA_OK;
+}

@@ -178,3 +178,28 @@ def test_backward_rejects_bad_arguments_on_the_host(lib):
     assert call(args, flags=binding.IDA_PATH_SEQUENTIAL) == binding.IDA_ERR_ARG
     assert call(args, M=200) == binding.IDA_ERR_UNSUPPORTED
     assert call(args, W=5) == binding.IDA_ERR_UNSUPPORTED
+
+
+def test_rope_rejects_bad_arguments_on_the_host(lib):
+    b = _Bufs()
+    p, mis = b.p, b.mis
+    F = ctypes.c_float
+
+    def call(q=p, k=None, B=1, N=8, H=2, R=32, pos0=0, base=10000.0, dtype=binding.IDA_BF16):
+        return lib.ida_rope(q, k, B, N, H, R, pos0, F(base), dtype, None)
+
+    assert call(q=None) == binding.IDA_ERR_ARG
+    assert call(q=mis) == binding.IDA_ERR_ARG
+    assert call(k=mis) == binding.IDA_ERR_ARG
+    assert call(k=p) == binding.IDA_ERR_ARG            # k aliasing q
+    assert call(B=-1) == binding.IDA_ERR_ARG
+    assert call(pos0=-1) == binding.IDA_ERR_ARG
+    for base in (1.0, 0.5, -3.0, float("nan"), float("inf")):
+        assert call(base=base) == binding.IDA_ERR_ARG, base
+    assert call(dtype=7) == binding.IDA_ERR_ARG
+    for R in (4, 12, 264):
+        assert call(R=R) == binding.IDA_ERR_UNSUPPORTED, R
+    assert call(H=1 << 20, R=256) == binding.IDA_ERR_UNSUPPORTED
+    # no rows: nothing to do, no pointer read, no CUDA call
+    assert call(q=None, N=0) == binding.IDA_OK
+    assert call(q=None, B=0) == binding.IDA_OK
