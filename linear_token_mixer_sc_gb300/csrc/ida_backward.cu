@@ -46,7 +46,6 @@
 
 namespace ida {
 
-constexpr int BWD_CHUNK = 64;     // positions between checkpoints
 constexpr int BWD_TILE = 32;      // positions per bwd_local CTA
 constexpr int BWD_THREADS = 512;  // bwd_scan threads (one per state column; R + d <= 512)
 constexpr int BWD_WARPS = BWD_THREADS / 32;
@@ -76,10 +75,12 @@ struct BwdSlicing {
         q.S = (M + q.MC - 1) / q.MC;
         return q;
     }
-    // modes of slice s, and the state elements of one slice-local state (planar Re rows,
-    // Im rows, then eta Re, eta Im)
+    // modes of slice s, and the elements of one slice-local state as the scans store it:
+    // [Re, Im][thread][BWD_MGT] (a thread's modes contiguous, so it moves them as 16-byte
+    // vectors; threads without a column hold zeros), then eta [Re, Im][MC]
     __host__ __device__ int ms(int s, int M) const { return M - s * MC < MC ? M - s * MC : MC; }
-    __host__ __device__ size_t sds(int RD) const { return 2 * (size_t)MC * RD + 2 * (size_t)MC; }
+    static constexpr size_t plane = (size_t)BWD_THREADS * BWD_MGT;
+    __host__ __device__ size_t sds() const { return 2 * plane + 2 * (size_t)MC; }
 };
 
 // Workspace layout (elements of T), per unit unless noted.
@@ -89,29 +90,33 @@ struct BwdLayout {
     size_t nd;      // [S][N][d + 1]: eta readout, per slice: partial numerator and denominator
     size_t gsc;     // [N][2]: eta readout: 1 / den and -(g . o) / den
     size_t ckpt;    // [S][nck][sds]
-    size_t xbuf;    // [S][BWD_CHUNK + 1][sds]
+    size_t xbuf;    // [S][chunk + 1][sds]
     size_t pscan;   // [4M]: lambda-bar (re, im), B-bar (re, im)
     size_t per_unit;
     size_t sds;
     size_t plocal_each;  // per (unit, tile): [2][R][W] conv, [R + d] norm weight, [R + d] bias
-    int nck, ntile, S;
+    int nck, ntile, S, chunk;
     size_t total;  // elements of T
-    static BwdLayout of(int B, int H, int N, int d, int R, int M, int W, bool eta) {
+    // chunk: positions between checkpoints (BwdChunk<T>::C of the arithmetic type)
+    static BwdLayout of(int B, int H, int N, int d, int R, int M, int W, bool eta, int chunk) {
         BwdLayout L;
         const BwdSlicing q = BwdSlicing::of(R, d, M);
         const size_t units = (size_t)B * H, F = 2 * (size_t)R + d;
         L.S = q.S;
-        L.nck = (N + BWD_CHUNK - 1) / BWD_CHUNK;
+        L.chunk = chunk;
+        L.nck = (N + chunk - 1) / chunk;
         L.ntile = (N + BWD_TILE - 1) / BWD_TILE;
-        L.sds = q.sds(R + d);
+        L.sds = q.sds();
+        // every region starts on a multiple of 4 elements (16-byte vectors of the states)
+        auto r4 = [](size_t x) { return (x + 3) & ~(size_t)3; };
         L.feat = 0;
-        L.gfeat = L.feat + (size_t)N * F;
-        L.nd = L.gfeat + (size_t)q.S * N * F;
-        L.gsc = L.nd + (eta ? (size_t)q.S * N * (d + 1) : 0);
-        L.ckpt = L.gsc + (eta ? 2 * (size_t)N : 0);
-        L.xbuf = L.ckpt + (size_t)q.S * L.nck * L.sds;
-        L.pscan = L.xbuf + (size_t)q.S * (BWD_CHUNK + 1) * L.sds;
-        L.per_unit = (L.pscan + 4 * (size_t)M + 1) & ~(size_t)1;
+        L.gfeat = r4(L.feat + (size_t)N * F);
+        L.nd = r4(L.gfeat + (size_t)q.S * N * F);
+        L.gsc = r4(L.nd + (eta ? (size_t)q.S * N * (d + 1) : 0));
+        L.ckpt = r4(L.gsc + (eta ? 2 * (size_t)N : 0));
+        L.xbuf = r4(L.ckpt + (size_t)q.S * L.nck * L.sds);
+        L.pscan = r4(L.xbuf + (size_t)q.S * (chunk + 1) * L.sds);
+        L.per_unit = r4(L.pscan + 4 * (size_t)M);
         L.plocal_each = 2 * (size_t)R * W + 2 * ((size_t)R + d);
         L.total = units * L.per_unit + units * L.ntile * L.plocal_each;
         return L;
@@ -140,6 +145,58 @@ __device__ __forceinline__ T conv_at(const void *x, int dtype, size_t base, size
     }
     return s;
 }
+
+// a thread's eight mode values of one state plane, as 16-byte vectors (p 16-byte aligned)
+__device__ __forceinline__ void ldg8(const float *p, float (&o)[8]) {
+    const float4 x = reinterpret_cast<const float4 *>(p)[0], y = reinterpret_cast<const float4 *>(p)[1];
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+    o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
+}
+__device__ __forceinline__ void ldg8(const double *p, double (&o)[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const double2 x = reinterpret_cast<const double2 *>(p)[i];
+        o[2 * i] = x.x;
+        o[2 * i + 1] = x.y;
+    }
+}
+__device__ __forceinline__ void stg8(float *p, const float (&v)[8]) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void stg8(double *p, const double (&v)[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) reinterpret_cast<double2 *>(p)[i] = make_double2(v[2 * i], v[2 * i + 1]);
+}
+
+// eight values from the 16-byte vectors p[0], p[BWD_THREADS], ... (shared memory)
+__device__ __forceinline__ void unpack_vecs(const uint4 *p, float (&o)[8]) {
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+        const uint4 w = p[(size_t)v * BWD_THREADS];
+        o[4 * v] = __uint_as_float(w.x);
+        o[4 * v + 1] = __uint_as_float(w.y);
+        o[4 * v + 2] = __uint_as_float(w.z);
+        o[4 * v + 3] = __uint_as_float(w.w);
+    }
+}
+__device__ __forceinline__ void unpack_vecs(const uint4 *p, double (&o)[8]) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const uint4 w = p[(size_t)v * BWD_THREADS];
+        o[2 * v] = __hiloint2double((int)w.y, (int)w.x);
+        o[2 * v + 1] = __hiloint2double((int)w.w, (int)w.z);
+    }
+}
+
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), and its completion
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 template <typename T>
 __device__ __forceinline__ T warp_sum_t(T x) {
@@ -264,7 +321,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_a_kernel(BackwardArgs
     const T *feat = base + L.feat;
     T *ckpt = base + L.ckpt + (size_t)sl * L.nck * L.sds;
     T *nd = base + L.nd + (size_t)sl * N * (d + 1);
-    const size_t F = 2 * (size_t)R + d, plane = (size_t)q.MC * RD, eoff = 2 * plane;
+    const size_t F = 2 * (size_t)R + d, plane = BwdSlicing::plane, eoff = 2 * plane, mine = (size_t)tid * BWD_MGT;
     T lr[BWD_MGT], li[BWD_MGT], br[BWD_MGT], bi[BWD_MGT], xr[BWD_MGT], xi[BWD_MGT];
 #pragma unroll
     for (int i = 0; i < BWD_MGT; ++i) {
@@ -288,23 +345,32 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_a_kernel(BackwardArgs
         ebi = (T)a.Bvec[((size_t)h * M + m) * 2 + 1];
     }
     const int gwarps = q.RDw / 32;  // warps per group
-    for (int t = 0; t < N; ++t) {
-        if (t % BWD_CHUNK == 0) {
-            T *ck = ckpt + (size_t)(t / BWD_CHUNK) * L.sds;
+    // z and xi(q) of the next ZP positions in flight (fewer in fp64, for registers)
+    constexpr int ZP = sizeof(T) == 8 ? 2 : 8;
+    const bool kq = eta_ro && col && c < R;
+    T zq[ZP], qq[ZP];
 #pragma unroll
-            for (int i = 0; i < BWD_MGT; ++i) {
-                const int ml = g + q.G * i;
-                if (col && ml < ms) {
-                    ck[(size_t)ml * RD + c] = xr[i];
-                    ck[plane + (size_t)ml * RD + c] = xi[i];
-                }
-            }
+    for (int u = 0; u < ZP; ++u) {
+        zq[u] = (col && u < N) ? feat[(size_t)u * F + R + c] : T(0);
+        qq[u] = (kq && u < N) ? feat[(size_t)u * F + c] : T(0);
+    }
+    for (int t0 = 0; t0 < N; t0 += ZP)
+#pragma unroll
+    for (int u = 0; u < ZP; ++u) {
+        const int t = t0 + u;
+        if (t >= N) break;
+        const T z = zq[u], xq = qq[u];
+        zq[u] = (col && t + ZP < N) ? feat[(size_t)(t + ZP) * F + R + c] : T(0);
+        qq[u] = (kq && t + ZP < N) ? feat[(size_t)(t + ZP) * F + c] : T(0);
+        if (t % L.chunk == 0) {
+            T *ck = ckpt + (size_t)(t / L.chunk) * L.sds;
+            stg8(ck + mine, xr);
+            stg8(ck + plane + mine, xi);
             if (eown) {
                 ck[eoff + tid] = er;
                 ck[eoff + q.MC + tid] = ei;
             }
         }
-        const T z = col ? feat[(size_t)t * F + R + c] : T(0);
 #pragma unroll
         for (int i = 0; i < BWD_MGT; ++i) {
             const T nr = fma(lr[i], xr[i], fma(-li[i], xi[i], br[i] * z));
@@ -319,7 +385,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_a_kernel(BackwardArgs
         }
         if (eta_ro) {
             // a_t of the slice's modes: sum over the group's key columns
-            const T xq = (col && c < R) ? feat[(size_t)t * F + c] : T(0);
             T v[2 * BWD_MGT];
 #pragma unroll
             for (int i = 0; i < BWD_MGT; ++i) {
@@ -396,240 +461,337 @@ __global__ void __launch_bounds__(256) bwd_scan_nd_kernel(BackwardArgs a, T *ws,
     }
 }
 
-// Phase B: the adjoint, chunk by chunk from the end, through the chunk's recomputed states.
+// eight consecutive values from 16-byte aligned shared memory
+__device__ __forceinline__ void lds8(const float *p, float (&o)[8]) {
+    const float4 x = reinterpret_cast<const float4 *>(p)[0], y = reinterpret_cast<const float4 *>(p)[1];
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+    o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
+}
+__device__ __forceinline__ void lds4(const float *p, float (&o)[4]) {
+    const float4 x = *reinterpret_cast<const float4 *>(p);
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+}
+__device__ __forceinline__ void lds4(const double *p, double (&o)[4]) {
+    const double2 x = reinterpret_cast<const double2 *>(p)[0], y = reinterpret_cast<const double2 *>(p)[1];
+    o[0] = x.x; o[1] = x.y; o[2] = y.x; o[3] = y.y;
+}
+__device__ __forceinline__ void lds8(const double *p, double (&o)[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const double2 x = reinterpret_cast<const double2 *>(p)[i];
+        o[2 * i] = x.x;
+        o[2 * i + 1] = x.y;
+    }
+}
+
+// Chunk length of the adjoint scan (positions between checkpoints): the shared-memory
+// staging of one chunk (below) fits in an SM at 16 fp32 positions or 8 fp64 ones.
 template <typename T>
+struct BwdChunk {
+    static constexpr int C = sizeof(T) == 8 ? 8 : 16;
+};
+
+// Dynamic shared memory of bwd_scan_b, in elements of T.
+template <typename T, bool SPLIT>
+struct ScanBSmem {
+    static constexpr int C = BwdChunk<T>::C;
+    static constexpr int RV = SPLIT ? 2 * BWD_MGT : 4 * BWD_MGT;  // values a warp sums per position
+    static constexpr int GM = BWD_THREADS / 32 * BWD_MGT;         // >= G * MGT mode entries
+    static constexpr size_t RED = 0;                                   // [C][warp][RV] warp sums
+    static constexpr size_t AM = RED + (size_t)C * BWD_WARPS * RV;     // [C][Re, Im][GM] a_t
+    static constexpr size_t ABM = AM + (size_t)C * 2 * GM;             // [C][Re, Im][GM] abar_t
+    static constexpr size_t PART = ABM + (size_t)C * 2 * GM;           // [C][dz, dxi(q)][thread]
+    static constexpr size_t INP = PART + (size_t)C * 2 * BWD_THREADS;  // [C][s, z][thread]
+    static constexpr size_t ETAS = INP + (size_t)C * 2 * BWD_THREADS;  // [C + 1][Re, Im][GM] eta at t0 - 1 + j
+    static constexpr size_t GD = ETAS + (size_t)(C + 1) * 2 * GM;      // [C] gd
+    static constexpr size_t BYTES = (GD + C) * sizeof(T);
+    static_assert(BYTES + 4 * GM * sizeof(T) + 4 * BWD_WARPS * sizeof(T) <= 227 * 1024, "shared memory budget");
+};
+
+// Phase B: the adjoint, chunk by chunk from the end.  Per chunk of C positions:
+//  1. forward from the chunk's checkpoint: the states X_t (kept for step 3 in the replay
+//     buffer, in L2), eta_t, the inputs of every position staged in shared memory, and
+//     each warp's partial sums of a_t (key columns) and abar_t's Gamma part (value
+//     columns) for every position; none of this depends on the adjoint state;
+//  2. the sums over each group's warps, for every position at once (plus conj(eta_t) gd
+//     for the eta readout);
+//  3. the adjoint walked back through the chunk with no barrier: the adjoint state, its
+//     lambda / B sums, and each thread's parts of dz and dxi(q) per position;
+//  4. the parts summed over the groups into dz and dxi(q) rows.
+// Three block barriers per chunk.
+template <typename T, bool SPLIT, bool ETA>
 __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_b_kernel(BackwardArgs a, T *ws, BwdLayout L) {
-    __shared__ T red[BWD_WARPS][2 * BWD_MGT];
-    __shared__ T am[2][BWD_THREADS / 32 * BWD_MGT];   // a_t (re, im), [group * MGT + i]
-    __shared__ T abm[2][BWD_THREADS / 32 * BWD_MGT];  // abar_t
-    __shared__ T part[2][BWD_THREADS];                // per-thread dz and dxi(q) parts
+    using SM = ScanBSmem<T, SPLIT>;
+    constexpr int C = SM::C, RV = SM::RV, GM = SM::GM, NT = BWD_THREADS;
+    extern __shared__ __align__(16) unsigned char smraw[];
+    T *const sm = reinterpret_cast<T *>(smraw);
+    T *const red = sm + SM::RED, *const am = sm + SM::AM, *const abm = sm + SM::ABM;
+    T *const part = sm + SM::PART, *const inp = sm + SM::INP, *const etas = sm + SM::ETAS, *const gds = sm + SM::GD;
+    __shared__ __align__(16) T lam_s[2][GM];  // lambda, B of the slice's modes, [group * MGT + i],
+    __shared__ __align__(16) T bv_s[2][GM];   // zero past them
+    __shared__ T fred[BWD_WARPS][4];
     const int R = a.R, d = a.d, H = a.H, N = a.N, M = a.M, RD = R + d;
     const BwdSlicing q = BwdSlicing::of(R, d, M);
     const int unit = blockIdx.x / q.S, sl = blockIdx.x % q.S, h = unit % H, b = unit / H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = tid / q.RDw, c = tid % q.RDw, ms = q.ms(sl, M);
-    const bool col = g < q.G && c < RD;
-    const bool eta_ro = (a.flags & IDA_READOUT_ETA) != 0;
-    const int gwarps = q.RDw / 32;
+    const bool col = g < q.G && c < RD, kcol = col && c < R, vcol = col && c >= R;
+    const int gwarps = q.RDw / 32, kwarps = R / 32;  // (SPLIT: R % 32 == 0, warps of one kind)
     T *base = ws + (size_t)unit * L.per_unit;
     const T *feat = base + L.feat;
     T *gfeat = base + L.gfeat + (size_t)sl * N * (2 * (size_t)R + d);
     const T *ckpt = base + L.ckpt + (size_t)sl * L.nck * L.sds;
-    T *xbuf = base + L.xbuf + (size_t)sl * (BWD_CHUNK + 1) * L.sds;
-    const size_t F = 2 * (size_t)R + d, plane = (size_t)q.MC * RD, eoff = 2 * plane;
-    T lr[BWD_MGT], li[BWD_MGT], br[BWD_MGT], bi[BWD_MGT];
+    T *xbuf = base + L.xbuf + (size_t)sl * (C + 1) * L.sds;
+    const size_t F = 2 * (size_t)R + d, plane = BwdSlicing::plane, eoff = 2 * plane, mine = (size_t)tid * BWD_MGT;
+    const size_t base_o = ((size_t)b * N * H + h) * d, so = (size_t)H * d;
+    if (tid < q.G * BWD_MGT) {  // entry gg * MGT + i: slice-local mode gg + G i
+        const int ml = tid / BWD_MGT + q.G * (tid % BWD_MGT), m = sl * q.MC + ml;
+        const bool ok = ml < ms;
+        lam_s[0][tid] = ok ? (T)a.lambda[((size_t)h * M + m) * 2] : T(0);
+        lam_s[1][tid] = ok ? (T)a.lambda[((size_t)h * M + m) * 2 + 1] : T(0);
+        bv_s[0][tid] = ok ? (T)a.Bvec[((size_t)h * M + m) * 2] : T(0);
+        bv_s[1][tid] = ok ? (T)a.Bvec[((size_t)h * M + m) * 2 + 1] : T(0);
+    }
+    __syncthreads();
+    const int gm = (g < q.G ? g : 0) * BWD_MGT;  // my group's mode entries
     T yr[BWD_MGT], yi[BWD_MGT], lbr[BWD_MGT], lbi[BWD_MGT], bbr[BWD_MGT], bbi[BWD_MGT];
 #pragma unroll
-    for (int i = 0; i < BWD_MGT; ++i) {
-        const int ml = g + q.G * i, m = sl * q.MC + ml;
-        const bool ok = col && ml < ms;
-        lr[i] = ok ? (T)a.lambda[((size_t)h * M + m) * 2] : T(0);
-        li[i] = ok ? (T)a.lambda[((size_t)h * M + m) * 2 + 1] : T(0);
-        br[i] = ok ? (T)a.Bvec[((size_t)h * M + m) * 2] : T(0);
-        bi[i] = ok ? (T)a.Bvec[((size_t)h * M + m) * 2 + 1] : T(0);
-        yr[i] = yi[i] = lbr[i] = lbi[i] = bbr[i] = bbi[i] = 0;
-    }
-    const bool eown = tid < ms;
-    const int eg = tid % q.G, ei_ = tid / q.G;  // slice-local mode tid = eg + G ei_
-    T elr = 0, eli = 0, ebr = 0, ebi = 0, yer = 0, yei = 0, lber = 0, lbei = 0, bber = 0, bbei = 0;
-    if (eown) {
-        const int m = sl * q.MC + tid;
-        elr = (T)a.lambda[((size_t)h * M + m) * 2];
-        eli = (T)a.lambda[((size_t)h * M + m) * 2 + 1];
-        ebr = (T)a.Bvec[((size_t)h * M + m) * 2];
-        ebi = (T)a.Bvec[((size_t)h * M + m) * 2 + 1];
-    }
-    const size_t base_o = ((size_t)b * N * H + h) * d, so = (size_t)H * d;
+    for (int i = 0; i < BWD_MGT; ++i) yr[i] = yi[i] = lbr[i] = lbi[i] = bbr[i] = bbi[i] = 0;
+    // eta entry of slice-local mode tid (tid < ms): its lambda / B at entry em
+    const bool eown = ETA && tid < ms;
+    const int em = (tid % q.G) * BWD_MGT + tid / q.G;
+    T yer = 0, yei = 0, lber = 0, lbei = 0, bber = 0, bbei = 0;
+    const int nsum = q.G * 4 * BWD_MGT;  // group sums per position: a (2 MGT) then abar (2 MGT) per group
+
     for (int k = L.nck - 1; k >= 0; --k) {
-        const int t0 = k * BWD_CHUNK, len = min(BWD_CHUNK, N - t0);
-        // the chunk's states: xbuf[i] = X_{t0 - 1 + i} for my elements
+        const int t0 = k * C, len = min(C, N - t0);
+        // ---- 1. forward through the chunk
         const T *ck = ckpt + (size_t)k * L.sds;
-        {
-            T xr[BWD_MGT], xi[BWD_MGT];
+        T ur[BWD_MGT], ui[BWD_MGT];
+        ldg8(ck + mine, ur);
+        ldg8(ck + plane + mine, ui);
+        if (ETA)
+            for (int j = tid; j < len; j += NT) gds[j] = base[L.gsc + 2 * (size_t)(t0 + j) + 1];
+        // my inputs of every position of the chunk, all loads issued together: s = xi(q) (key
+        // column) or g / den (value column), and z
+        if (col) {
+            T sv[C], zv[C];
 #pragma unroll
-            for (int i = 0; i < BWD_MGT; ++i) {
-                const int ml = g + q.G * i;
-                const bool ok = col && ml < ms;
-                xr[i] = ok ? ck[(size_t)ml * RD + c] : T(0);
-                xi[i] = ok ? ck[plane + (size_t)ml * RD + c] : T(0);
-                if (ok) {
-                    xbuf[(size_t)ml * RD + c] = xr[i];
-                    xbuf[plane + (size_t)ml * RD + c] = xi[i];
+            for (int j = 0; j < C; ++j) {
+                const int t = min(t0 + j, N - 1);
+                const T *frow = feat + (size_t)t * F;
+                zv[j] = frow[R + c];
+                if (kcol) {
+                    sv[j] = frow[c];
+                } else {
+                    const T gsn = ETA ? base[L.gsc + 2 * (size_t)t] : T(1);
+                    sv[j] = (T)load_in(a.dout, a.dtype, base_o + (size_t)t * so + (c - R)) * gsn;
                 }
             }
-            T er = eown ? ck[eoff + tid] : T(0), e_i = eown ? ck[eoff + q.MC + tid] : T(0);
-            if (eown) {
-                xbuf[eoff + tid] = er;
-                xbuf[eoff + q.MC + tid] = e_i;
-            }
-            for (int j = 0; j < len; ++j) {
-                const T z = col ? feat[(size_t)(t0 + j) * F + R + c] : T(0);
-                T *xb = xbuf + (size_t)(j + 1) * L.sds;
 #pragma unroll
-                for (int i = 0; i < BWD_MGT; ++i) {
-                    const T nr = fma(lr[i], xr[i], fma(-li[i], xi[i], br[i] * z));
-                    const T ni = fma(lr[i], xi[i], fma(li[i], xr[i], bi[i] * z));
-                    xr[i] = nr;
-                    xi[i] = ni;
-                    const int ml = g + q.G * i;
-                    if (col && ml < ms) {
-                        xb[(size_t)ml * RD + c] = nr;
-                        xb[plane + (size_t)ml * RD + c] = ni;
-                    }
-                }
-                if (eown) {
-                    const T nr = fma(elr, er, fma(-eli, e_i, ebr)), ni = fma(elr, e_i, fma(eli, er, ebi));
-                    er = nr;
-                    e_i = ni;
-                    xb[eoff + tid] = nr;
-                    xb[eoff + q.MC + tid] = ni;
-                }
+            for (int j = 0; j < C; ++j) {
+                inp[(size_t)(2 * j) * NT + tid] = sv[j];
+                inp[(size_t)(2 * j + 1) * NT + tid] = zv[j];
             }
+        } else {
+#pragma unroll
+            for (int j = 0; j < C; ++j) inp[(size_t)(2 * j) * NT + tid] = inp[(size_t)(2 * j + 1) * NT + tid] = T(0);
         }
-        __syncthreads();
-        for (int j = len - 1; j >= 0; --j) {
-            const int t = t0 + j;
-            const T *X = xbuf + (size_t)(j + 1) * L.sds, *Xp = xbuf + (size_t)j * L.sds;
-            const T *frow = feat + (size_t)t * F;
-            const T xq = (col && c < R) ? frow[c] : T(0);
-            const T zc = col ? frow[R + c] : T(0);
-            T gsn = 1, gd = 0;
-            if (eta_ro) {
-                gsn = base[L.gsc + 2 * (size_t)t];
-                gd = base[L.gsc + 2 * (size_t)t + 1];
-            }
-            const T gn = (col && c >= R) ? (T)load_in(a.dout, a.dtype, base_o + (size_t)t * so + (c - R)) * gsn : T(0);
-            T ur[BWD_MGT], ui[BWD_MGT];
+        stg8(xbuf + mine, ur);
+        stg8(xbuf + plane + mine, ui);
+        T er = 0, e_i = 0;
+        if (eown) {
+            er = ck[eoff + tid];
+            e_i = ck[eoff + q.MC + tid];
+            etas[tid] = er;
+            etas[GM + tid] = e_i;
+        }
+        for (int j = 0; j < len; ++j) {
+            const T s = inp[(size_t)(2 * j) * NT + tid], z = inp[(size_t)(2 * j + 1) * NT + tid];
 #pragma unroll
-            for (int i = 0; i < BWD_MGT; ++i) {
-                const int ml = g + q.G * i;
-                const bool ok = col && ml < ms;
-                ur[i] = ok ? X[(size_t)ml * RD + c] : T(0);
-                ui[i] = ok ? X[plane + (size_t)ml * RD + c] : T(0);
+            for (int i0 = 0; i0 < BWD_MGT; i0 += 4) {
+                T lr[4], li[4], br[4], bi[4];
+                lds4(&lam_s[0][gm + i0], lr);
+                lds4(&lam_s[1][gm + i0], li);
+                lds4(&bv_s[0][gm + i0], br);
+                lds4(&bv_s[1][gm + i0], bi);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u;
+                    const T nr = fma(lr[u], ur[i], fma(-li[u], ui[i], br[u] * z));
+                    const T ni = fma(lr[u], ui[i], fma(li[u], ur[i], bi[u] * z));
+                    ur[i] = nr;
+                    ui[i] = ni;
+                }
             }
-            // a_t (key columns) and the Gamma part of abar_t (value columns), summed over the group
-            {
+            T *xb = xbuf + (size_t)(j + 1) * L.sds;
+            stg8(xb + mine, ur);
+            stg8(xb + plane + mine, ui);
+            if (eown) {
+                const T elr = lam_s[0][em], eli = lam_s[1][em], ebr = bv_s[0][em], ebi = bv_s[1][em];
+                const T nr = fma(elr, er, fma(-eli, e_i, ebr)), ni = fma(elr, e_i, fma(eli, er, ebi));
+                er = nr;
+                e_i = ni;
+                etas[(size_t)(j + 1) * 2 * GM + tid] = er;
+                etas[(size_t)(j + 1) * 2 * GM + GM + tid] = e_i;
+            }
+            // warp sums: a_t = xi(q) . U_t over key columns, conj(Gamma_t) g over value columns
+            T *rw = red + ((size_t)j * BWD_WARPS + warp) * RV;
+            if constexpr (SPLIT) {
+                const T sg = kcol ? s : -s;
                 T v[2 * BWD_MGT];
 #pragma unroll
                 for (int i = 0; i < BWD_MGT; ++i) {
-                    v[2 * i] = xq * ur[i];
-                    v[2 * i + 1] = xq * ui[i];
+                    v[2 * i] = s * ur[i];
+                    v[2 * i + 1] = sg * ui[i];
                 }
                 const T s1 = warp_reduce_scatter<2 * BWD_MGT>(v, lane);
-                if ((lane & 1) == 0) red[warp][rs_index<2 * BWD_MGT>(lane)] = s1;
-            }
-            __syncthreads();
-            if (tid < q.G * 2 * BWD_MGT) {
-                const int gg = tid / (2 * BWD_MGT), kk = tid % (2 * BWD_MGT);
-                T sum = 0;
-                for (int w = 0; w < gwarps; ++w) sum += red[gg * gwarps + w][kk];
-                am[kk & 1][gg * BWD_MGT + (kk >> 1)] = sum;
-            }
-            __syncthreads();
-            {
-                T v[2 * BWD_MGT];  // conj(Gamma) gn
+                if ((lane & 1) == 0) rw[rs_index<2 * BWD_MGT>(lane)] = s1;
+            } else {
+                const T sa = kcol ? s : T(0), sb = vcol ? s : T(0);
+                T v[4 * BWD_MGT];
 #pragma unroll
                 for (int i = 0; i < BWD_MGT; ++i) {
-                    v[2 * i] = ur[i] * gn;
-                    v[2 * i + 1] = -ui[i] * gn;
+                    v[2 * i] = sa * ur[i];
+                    v[2 * i + 1] = sa * ui[i];
+                    v[2 * BWD_MGT + 2 * i] = sb * ur[i];
+                    v[2 * BWD_MGT + 2 * i + 1] = -sb * ui[i];
                 }
-                const T s1 = warp_reduce_scatter<2 * BWD_MGT>(v, lane);
-                if ((lane & 1) == 0) red[warp][rs_index<2 * BWD_MGT>(lane)] = s1;
+                rw[rs_index<4 * BWD_MGT>(lane)] = warp_reduce_scatter<4 * BWD_MGT>(v, lane);
             }
-            __syncthreads();
-            if (tid < q.G * 2 * BWD_MGT) {
-                const int gg = tid / (2 * BWD_MGT), kk = tid % (2 * BWD_MGT);
-                T sum = 0;
-                for (int w = 0; w < gwarps; ++w) sum += red[gg * gwarps + w][kk];
-                const int ml = gg + q.G * (kk >> 1);
-                if (eta_ro && ml < ms) {  // + conj(eta_t) gd
-                    sum += (kk & 1) ? -X[eoff + q.MC + ml] * gd : X[eoff + ml] * gd;
+        }
+        __syncthreads();
+        // ---- 2. sums over each group's warps, every position of the chunk
+        for (int e = tid; e < len * nsum; e += NT) {
+            const int j = e / nsum, r = e % nsum, gg = r / (4 * BWD_MGT), kk = r % (4 * BWD_MGT);
+            const int kk2 = kk - 2 * BWD_MGT;
+            const T *rr = red + (size_t)j * BWD_WARPS * RV + (size_t)gg * gwarps * RV;
+            T sum = 0;
+            if constexpr (!SPLIT) {
+                for (int w = 0; w < gwarps; ++w) sum += rr[w * RV + kk];
+            } else if (kk2 < 0) {
+                for (int w = 0; w < kwarps; ++w) sum += rr[w * RV + kk];
+            } else {
+                for (int w = kwarps; w < gwarps; ++w) sum += rr[w * RV + kk2];
+            }
+            if (kk2 < 0) {
+                am[(size_t)(2 * j + (kk & 1)) * GM + gg * BWD_MGT + (kk >> 1)] = sum;
+            } else {
+                const int ml = gg + q.G * (kk2 >> 1);
+                if (ETA && ml < ms) {  // + conj(eta_t) gd
+                    const T ev = etas[(size_t)(j + 1) * 2 * GM + (kk2 & 1) * GM + ml];
+                    sum += ((kk2 & 1) ? -ev : ev) * gds[j];
                 }
-                abm[kk & 1][gg * BWD_MGT + (kk >> 1)] = sum;
+                abm[(size_t)(2 * j + (kk2 & 1)) * GM + gg * BWD_MGT + (kk2 >> 1)] = sum;
             }
-            __syncthreads();
-            // adjoint update of my elements; my parts of dz and dxi(q)
+        }
+        __syncthreads();
+        // ---- 3. the adjoint, back through the chunk (ur, ui hold the chunk's last state).
+        // xi(q) is zero on value columns and g on key columns, so the direct adjoint is
+        // abar xi(q) on key columns and conj(a) g on value columns without a branch; modes
+        // past the slice have a = abar = 0 and stay at zero.
+        for (int j = len - 1; j >= 0; --j) {
+            T pr[BWD_MGT], pi[BWD_MGT];  // X_{t-1}
+            const T *xp = xbuf + (size_t)j * L.sds;
+            ldg8(xp + mine, pr);
+            ldg8(xp + plane + mine, pi);
+            const T s = inp[(size_t)(2 * j) * NT + tid], zc = inp[(size_t)(2 * j + 1) * NT + tid];
+            const T xq = kcol ? s : T(0), gn = vcol ? s : T(0);
+            const T *amj = am + (size_t)(2 * j) * GM + gm, *abj = abm + (size_t)(2 * j) * GM + gm;
             T dz = 0, dxq = 0;
 #pragma unroll
-            for (int i = 0; i < BWD_MGT; ++i) {
-                const int ml = g + q.G * i;
-                const bool ok = col && ml < ms;
-                const T ar = am[0][g * BWD_MGT + i], aim = am[1][g * BWD_MGT + i];
-                const T abr = abm[0][g * BWD_MGT + i], abi = abm[1][g * BWD_MGT + i];
-                T dr, di;
-                if (c < R) {
-                    dr = abr * xq;
-                    di = abi * xq;
-                } else {
-                    dr = ar * gn;
-                    di = -aim * gn;
+            for (int i0 = 0; i0 < BWD_MGT; i0 += 4) {
+                T ar[4], aim[4], abr[4], abi[4], lr[4], li[4], br[4], bi[4];
+                lds4(amj + i0, ar);
+                lds4(amj + GM + i0, aim);
+                lds4(abj + i0, abr);
+                lds4(abj + GM + i0, abi);
+                lds4(&lam_s[0][gm + i0], lr);
+                lds4(&lam_s[1][gm + i0], li);
+                lds4(&bv_s[0][gm + i0], br);
+                lds4(&bv_s[1][gm + i0], bi);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u;
+                    const T dr = fma(abr[u], xq, ar[u] * gn), di = fma(abi[u], xq, -aim[u] * gn);
+                    const T nyr = fma(lr[u], yr[i], fma(li[u], yi[i], dr));
+                    const T nyi = fma(lr[u], yi[i], fma(-li[u], yr[i], di));
+                    yr[i] = nyr;
+                    yi[i] = nyi;
+                    bbr[i] = fma(zc, nyr, bbr[i]);
+                    bbi[i] = fma(zc, nyi, bbi[i]);
+                    dz = fma(br[u], nyr, fma(bi[u], nyi, dz));
+                    dxq = fma(abr[u], ur[i], fma(abi[u], ui[i], dxq));
                 }
-                if (!ok) dr = di = 0;
-                const T nyr = dr + lr[i] * yr[i] + li[i] * yi[i];
-                const T nyi = di + lr[i] * yi[i] - li[i] * yr[i];
-                yr[i] = nyr;
-                yi[i] = nyi;
-                const T pr = ok ? Xp[(size_t)ml * RD + c] : T(0), pi = ok ? Xp[plane + (size_t)ml * RD + c] : T(0);
-                lbr[i] += pr * nyr + pi * nyi;
-                lbi[i] += pr * nyi - pi * nyr;
-                bbr[i] += zc * nyr;
-                bbi[i] += zc * nyi;
-                dz += br[i] * nyr + bi[i] * nyi;
-                dxq += abr * ur[i] + abi * ui[i];
             }
-            if (eown && eta_ro) {
-                const T ar = am[0][eg * BWD_MGT + ei_], aim = am[1][eg * BWD_MGT + ei_];
+            // lambda-bar last: the only use of X_{t-1}, whose loads were issued first
+#pragma unroll
+            for (int i = 0; i < BWD_MGT; ++i) {
+                lbr[i] = fma(pr[i], yr[i], fma(pi[i], yi[i], lbr[i]));
+                lbi[i] = fma(pr[i], yi[i], fma(-pi[i], yr[i], lbi[i]));
+            }
+            if (eown) {
+                const T ar = am[(size_t)(2 * j) * GM + em], aim = am[(size_t)(2 * j + 1) * GM + em];
+                const T elr = lam_s[0][em], eli = lam_s[1][em], gd = gds[j];
                 const T dr = ar * gd, di = -aim * gd;
                 const T nyr = dr + elr * yer + eli * yei;
                 const T nyi = di + elr * yei - eli * yer;
                 yer = nyr;
                 yei = nyi;
-                const T pr = Xp[eoff + tid], pi = Xp[eoff + q.MC + tid];
-                lber += pr * nyr + pi * nyi;
-                lbei += pr * nyi - pi * nyr;
+                const T per = etas[(size_t)j * 2 * GM + tid], pei = etas[(size_t)j * 2 * GM + GM + tid];
+                lber += per * nyr + pei * nyi;
+                lbei += per * nyi - pei * nyr;
                 bber += nyr;
                 bbei += nyi;
             }
-            part[0][tid] = dz;
-            part[1][tid] = (c < R) ? dxq : T(0);
-            __syncthreads();
-            // the slice's dz (all columns) and dxi(q) (key columns): sum over the groups
-            for (int cc = tid; cc < RD; cc += BWD_THREADS) {
-                T sz = 0, sq = 0;
-                for (int gg = 0; gg < q.G; ++gg) {
-                    sz += part[0][gg * q.RDw + cc];
-                    sq += part[1][gg * q.RDw + cc];
-                }
-                T *grow = gfeat + (size_t)t * F;
-                grow[R + cc] = sz;  // dkt for cc < R, dvt for cc >= R
-                if (cc < R) grow[cc] = sq;
+            part[(size_t)(2 * j) * NT + tid] = dz;
+            part[(size_t)(2 * j + 1) * NT + tid] = kcol ? dxq : T(0);
+#pragma unroll
+            for (int i = 0; i < BWD_MGT; ++i) {
+                ur[i] = pr[i];
+                ui[i] = pi[i];
             }
-            __syncthreads();
+        }
+        __syncthreads();
+        // ---- 4. dz (all columns) and dxi(q) (key columns) of the chunk's positions
+        for (int e = tid; e < len * RD; e += NT) {
+            const int j = e / RD, cc = e % RD;
+            T sz = 0, sq = 0;
+            for (int gg = 0; gg < q.G; ++gg) {
+                sz += part[(size_t)(2 * j) * NT + gg * q.RDw + cc];
+                sq += part[(size_t)(2 * j + 1) * NT + gg * q.RDw + cc];
+            }
+            T *grow = gfeat + (size_t)(t0 + j) * F;
+            grow[R + cc] = sz;  // dkt for cc < R, dvt for cc >= R
+            if (cc < R) grow[cc] = sq;
         }
     }
+    __syncthreads();
     // lambda-bar and B-bar of my modes: sum over the group's columns, then the eta terms
     T *ps = base + L.pscan;
-    for (int i = 0; i < BWD_MGT; ++i) {
+    T *pflat = part;  // [4][NT / 4]: lambda-bar re, im, B-bar re, im per mode
+#pragma unroll
+    for (int i = 0; i < BWD_MGT; ++i) {  // unrolled: the per-mode sums stay in registers
         T v[4] = {lbr[i], lbi[i], bbr[i], bbi[i]};
         const T s1 = warp_reduce_scatter<4>(v, lane);
-        if ((lane & 1) == 0) red[warp][rs_index<4>(lane)] = s1;
+        __syncthreads();
+        if ((lane & 1) == 0) fred[warp][rs_index<4>(lane)] = s1;
         __syncthreads();
         if (tid < q.G * 4) {
             const int gg = tid / 4, kk = tid % 4;
-            const int ml = gg + q.G * i, m = sl * q.MC + ml;
+            const int ml = gg + q.G * i;
             T sum = 0;
-            for (int w = 0; w < gwarps; ++w) sum += red[gg * gwarps + w][kk];
-            if (ml < ms) part[0][kk * (BWD_THREADS / 4) + ml] = sum;
-            (void)m;
+            for (int w = 0; w < gwarps; ++w) sum += fred[gg * gwarps + w][kk];
+            if (ml < ms) pflat[kk * (NT / 4) + ml] = sum;
         }
-        __syncthreads();
     }
-    if (eown) {
+    __syncthreads();
+    if (tid < ms) {
         const int m = sl * q.MC + tid;
-        ps[m] = part[0][0 * (BWD_THREADS / 4) + tid] + (eta_ro ? lber : T(0));
-        ps[M + m] = part[0][1 * (BWD_THREADS / 4) + tid] + (eta_ro ? lbei : T(0));
-        ps[2 * M + m] = part[0][2 * (BWD_THREADS / 4) + tid] + (eta_ro ? bber : T(0));
-        ps[3 * M + m] = part[0][3 * (BWD_THREADS / 4) + tid] + (eta_ro ? bbei : T(0));
+        ps[m] = pflat[0 * (NT / 4) + tid] + lber;
+        ps[M + m] = pflat[1 * (NT / 4) + tid] + lbei;
+        ps[2 * M + m] = pflat[2 * (NT / 4) + tid] + bber;
+        ps[3 * M + m] = pflat[3 * (NT / 4) + tid] + bbei;
     }
 }
 
@@ -834,13 +996,14 @@ static size_t bwd_local_smem(int R, int d) {
 size_t backward_workspace_bytes(int B, int H, int N, int d, int R, int M, int dtype, int W, int flags) {
     if (B <= 0 || H <= 0 || N <= 0) return 0;
     const size_t e = dtype == IDA_F32 ? sizeof(double) : sizeof(float);
-    return BwdLayout::of(B, H, N, d, R, M, W, (flags & IDA_READOUT_ETA) != 0).total * e;
+    const int chunk = dtype == IDA_F32 ? BwdChunk<double>::C : BwdChunk<float>::C;
+    return BwdLayout::of(B, H, N, d, R, M, W, (flags & IDA_READOUT_ETA) != 0, chunk).total * e;
 }
 
 template <typename T>
 static cudaError_t launch_backward_t(const BackwardArgs &a, void *workspace, cudaStream_t st) {
     const bool eta = (a.flags & IDA_READOUT_ETA) != 0;
-    const BwdLayout L = BwdLayout::of(a.B, a.H, a.N, a.d, a.R, a.M, a.W, eta);
+    const BwdLayout L = BwdLayout::of(a.B, a.H, a.N, a.d, a.R, a.M, a.W, eta, BwdChunk<T>::C);
     T *ws = static_cast<T *>(workspace);
     const unsigned units = (unsigned)(a.B * a.H), tiles8 = (unsigned)((a.N + 7) / 8);
     cudaError_t e;
@@ -852,7 +1015,14 @@ static cudaError_t launch_backward_t(const BackwardArgs &a, void *workspace, cud
         bwd_scan_nd_kernel<T><<<units * tiles8, 256, 0, st>>>(a, ws, L);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    bwd_scan_b_kernel<T><<<units * (unsigned)L.S, BWD_THREADS, 0, st>>>(a, ws, L);
+    {
+        const bool split = a.R % 32 == 0;
+        auto kb = split ? (eta ? bwd_scan_b_kernel<T, true, true> : bwd_scan_b_kernel<T, true, false>)
+                        : (eta ? bwd_scan_b_kernel<T, false, true> : bwd_scan_b_kernel<T, false, false>);
+        const int sb = (int)(split ? ScanBSmem<T, true>::BYTES : ScanBSmem<T, false>::BYTES);
+        if ((e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, sb)) != cudaSuccess) return e;
+        kb<<<units * (unsigned)L.S, BWD_THREADS, sb, st>>>(a, ws, L);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (L.S > 1) {
         const size_t n = (size_t)units * a.N * (2 * (size_t)a.R + a.d);

@@ -145,11 +145,14 @@ def test_selftest_rejects_bad_limits(lib):
 
 
 def test_backward_workspace_bytes(lib):
-    """Feature rows and their gradients, checkpoints every 64 positions, one chunk of
-    states and the adjoint state per unit, plus per-tile partials: host arithmetic only."""
+    """Feature rows and their gradients, a checkpoint of the state every chunk of positions
+    (16 in fp32 arithmetic for bf16 inputs, 8 in fp64 for fp32 inputs), one chunk of replayed
+    states per unit, plus per-tile partials: host arithmetic only."""
     n = binding.ida_backward_workspace_bytes(2, 3, 100, 32, 32, 16, binding.IDA_BF16, 4)
-    assert n > 0 and n % 4 == 0
-    assert binding.ida_backward_workspace_bytes(2, 3, 100, 32, 32, 16, binding.IDA_F32, 4) == 2 * n
+    assert n > 0 and n % 16 == 0
+    n32 = binding.ida_backward_workspace_bytes(2, 3, 100, 32, 32, 16, binding.IDA_F32, 4)
+    assert n32 > n and n32 % 32 == 0  # fp64 elements
+    assert binding.ida_backward_workspace_bytes(2, 3, 200, 32, 32, 16, binding.IDA_BF16, 4) > n
     assert binding.ida_backward_workspace_bytes(2, 3, 0, 32, 32, 16, binding.IDA_BF16, 4) == 0
     assert binding.ida_backward_workspace_bytes(2, 3, 100, 32, 32, 200, binding.IDA_BF16, 4) == 0
 
