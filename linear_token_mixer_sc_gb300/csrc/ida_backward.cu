@@ -47,6 +47,7 @@
 namespace ida {
 
 constexpr int BWD_TILE = 32;      // positions per bwd_local CTA
+constexpr int BWD_LANE_CH = 8;    // channels per lane in the per-position kernels (R, d <= 256)
 constexpr int BWD_THREADS = 512;  // bwd_scan threads (one per state column; R + d <= 512)
 constexpr int BWD_WARPS = BWD_THREADS / 32;
 
@@ -81,6 +82,13 @@ struct BwdSlicing {
     __host__ __device__ int ms(int s, int M) const { return M - s * MC < MC ? M - s * MC : MC; }
     static constexpr size_t plane = (size_t)BWD_THREADS * BWD_MGT;
     __host__ __device__ size_t sds() const { return 2 * plane + 2 * (size_t)MC; }
+};
+
+// Positions between checkpoints of the state: the adjoint scan stages one such chunk in
+// shared memory, which fits in an SM at 16 fp32 positions or 8 fp64 ones.
+template <typename T>
+struct BwdChunk {
+    static constexpr int C = sizeof(T) == 8 ? 8 : 16;
 };
 
 // Workspace layout (elements of T), per unit unless noted.
@@ -223,26 +231,30 @@ __global__ void __launch_bounds__(256) bwd_features_kernel(BackwardArgs a, T *ws
     for (int which = 0; which < 2; ++which) {
         const void *x = which == 0 ? a.q : a.k;
         const float *cw = a.conv_w + ((size_t)which * H + h) * R * W;
+        T fv[BWD_LANE_CH];  // SiLU of the conv of my channels c = lane + 32 i, computed once
         T ss = 0;
-        for (int c = lane; c < R; c += 32) {
-            const T f = silu(conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c));
-            ss = fma(f, f, ss);
+#pragma unroll
+        for (int i = 0; i < BWD_LANE_CH; ++i) {
+            const int c = lane + 32 * i;
+            fv[i] = c < R ? silu(conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c)) : T(0);
+            ss = fma(fv[i], fv[i], ss);
         }
         T n = warp_sum_t(ss);
         if (l2) n = sqrt(n);
         const T inv = T(1) / (n + (T)IDA_EPS_FEAT);
         if (which == 0) {
-            for (int c = lane; c < R; c += 32) row[c] = silu(conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c)) * inv;
+#pragma unroll
+            for (int i = 0; i < BWD_LANE_CH; ++i)
+                if (lane + 32 * i < R) row[lane + 32 * i] = fv[i] * inv;
         } else {
             T ms = 0;
-            for (int c = lane; c < R; c += 32) {
-                const T xi = silu(conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c)) * inv;
-                ms = fma(xi, xi, ms);
-            }
+#pragma unroll
+            for (int i = 0; i < BWD_LANE_CH; ++i) ms = fma(fv[i] * inv, fv[i] * inv, ms);
             const T r = T(1) / sqrt(warp_sum_t(ms) / R + (T)IDA_EPS_RMS);
-            for (int c = lane; c < R; c += 32) {
-                const T xi = silu(conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c)) * inv;
-                row[R + c] = fma(xi * r, (T)nw[c], (T)bs[c]);
+#pragma unroll
+            for (int i = 0; i < BWD_LANE_CH; ++i) {
+                const int c = lane + 32 * i;
+                if (c < R) row[R + c] = fma(fv[i] * inv * r, (T)nw[c], (T)bs[c]);
             }
         }
     }
@@ -264,48 +276,10 @@ __global__ void __launch_bounds__(256) bwd_features_kernel(BackwardArgs a, T *ws
 // R <= c < R + d: Gamma) of the slice-local modes g, g + G, g + 2G, ...; thread j < ms also
 // owns the eta entry of slice-local mode j.
 
-// Sum of each of NV values over the 32 lanes of a warp by recursive halving: afterwards lane
-// l holds the full sum of value index vidx(l) (lanes l and l ^ 1 hold the same one).  NV is a
-// power of two <= 16; 2 NV - 1 shuffles instead of 5 NV.
-template <int NV, typename T>
-__device__ __forceinline__ T warp_reduce_scatter(T (&v)[NV], int lane) {
-    int n = NV;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        if (n > 1) {
-            const bool hi = (lane & off) != 0;
-            const int hn = n >> 1;
-#pragma unroll
-            for (int k = 0; k < NV / 2; ++k) {
-                if (k < hn) {
-                    const T send = hi ? v[k] : v[k + hn];
-                    const T keep = hi ? v[k + hn] : v[k];
-                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                }
-            }
-            n = hn;
-        } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
-        }
-    }
-    return v[0];
-}
-// the value index lane l holds after warp_reduce_scatter<NV>
-template <int NV>
-__device__ __forceinline__ int rs_index(int lane) {
-    int idx = 0, n = NV;
-#pragma unroll
-    for (int off = 16; off >= 1 && n > 1; off >>= 1) {
-        n >>= 1;
-        if (lane & off) idx += n;
-    }
-    return idx;
-}
-
 // Phase A: the forward recurrence of the slice's modes over all positions, storing the state
 // before every chunk; for the eta readout also the slice's part of the numerator and of the
 // denominator at every position.
-template <typename T>
+template <typename T, bool ETA>
 __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_a_kernel(BackwardArgs a, T *ws, BwdLayout L) {
     __shared__ T red[BWD_WARPS][2 * BWD_MGT];
     __shared__ T am[2][BWD_THREADS / 32 * BWD_MGT];  // a_t of the slice's modes (re, im)
@@ -316,7 +290,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_a_kernel(BackwardArgs
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = tid / q.RDw, c = tid % q.RDw, ms = q.ms(sl, M);
     const bool col = g < q.G && c < RD;
-    const bool eta_ro = (a.flags & IDA_READOUT_ETA) != 0;
+    constexpr bool eta_ro = ETA;
     T *base = ws + (size_t)unit * L.per_unit;
     const T *feat = base + L.feat;
     T *ckpt = base + L.ckpt + (size_t)sl * L.nck * L.sds;
@@ -345,6 +319,33 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_a_kernel(BackwardArgs
         ebi = (T)a.Bvec[((size_t)h * M + m) * 2 + 1];
     }
     const int gwarps = q.RDw / 32;  // warps per group
+    if constexpr (!ETA) {
+        // chunk by chunk: the checkpoint, then the chunk's z loaded together and the recurrence
+        constexpr int C = BwdChunk<T>::C;
+        for (int k = 0; k < L.nck; ++k) {
+            const int t0 = k * C, len = min(C, N - t0);
+            T *ck = ckpt + (size_t)k * L.sds;
+            stg8(ck + mine, xr);
+            stg8(ck + plane + mine, xi);
+            T zv[C];
+#pragma unroll
+            for (int j = 0; j < C; ++j) zv[j] = col ? feat[(size_t)min(t0 + j, N - 1) * F + R + c] : T(0);
+#pragma unroll
+            for (int j = 0; j < C; ++j) {
+                if (j < len) {
+#pragma unroll
+                    for (int i = 0; i < BWD_MGT; ++i) {
+                        const T nr = fma(lr[i], xr[i], fma(-li[i], xi[i], br[i] * zv[j]));
+                        const T ni = fma(lr[i], xi[i], fma(li[i], xr[i], bi[i] * zv[j]));
+                        xr[i] = nr;
+                        xi[i] = ni;
+                    }
+                }
+            }
+        }
+        return;
+    }
+    // eta readout: position by position, with the slice's numerator and denominator parts;
     // z and xi(q) of the next ZP positions in flight (fewer in fp64, for registers)
     constexpr int ZP = sizeof(T) == 8 ? 2 : 8;
     const bool kq = eta_ro && col && c < R;
@@ -483,13 +484,6 @@ __device__ __forceinline__ void lds8(const double *p, double (&o)[8]) {
         o[2 * i + 1] = x.y;
     }
 }
-
-// Chunk length of the adjoint scan (positions between checkpoints): the shared-memory
-// staging of one chunk (below) fits in an SM at 16 fp32 positions or 8 fp64 ones.
-template <typename T>
-struct BwdChunk {
-    static constexpr int C = sizeof(T) == 8 ? 8 : 16;
-};
 
 // Dynamic shared memory of bwd_scan_b, in elements of T.
 template <typename T, bool SPLIT>
@@ -815,7 +809,7 @@ __global__ void bwd_sum_slices_kernel(BackwardArgs a, T *ws, BwdLayout L) {
 // convs is needed at positions [t0, t0 + tile + W - 1) for the input gradients of the tile.
 
 template <typename T>
-__global__ void __launch_bounds__(256) bwd_local_kernel(BackwardArgs a, T *ws, BwdLayout L) {
+__global__ void __launch_bounds__(256, 4) bwd_local_kernel(BackwardArgs a, T *ws, BwdLayout L) {
     extern __shared__ __align__(16) unsigned char smraw[];
     const int R = a.R, d = a.d, H = a.H, N = a.N, W = a.W;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw8 = blockDim.x >> 5;
@@ -844,10 +838,15 @@ __global__ void __launch_bounds__(256) bwd_local_kernel(BackwardArgs a, T *ws, B
         for (int which = 0; which < 2; ++which) {
             const void *x = which == 0 ? a.q : a.k;
             const float *cw = a.conv_w + ((size_t)which * H + h) * R * W;
+            // conv outputs s and SiLU values f of my channels c = lane + 32 i, computed once
+            T sv[BWD_LANE_CH], fv[BWD_LANE_CH];
             T ss = 0;
-            for (int c = lane; c < R; c += 32) {
-                const T f = silu(conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c));
-                ss = fma(f, f, ss);
+#pragma unroll
+            for (int i = 0; i < BWD_LANE_CH; ++i) {
+                const int c = lane + 32 * i;
+                sv[i] = c < R ? conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c) : T(0);
+                fv[i] = c < R ? silu(sv[i]) : T(0);
+                ss = fma(fv[i], fv[i], ss);
             }
             ss = warp_sum_t(ss);
             const T n = l2 ? sqrt(ss) : ss;
@@ -856,64 +855,84 @@ __global__ void __launch_bounds__(256) bwd_local_kernel(BackwardArgs a, T *ws, B
             T r = 0, sdy = 0;
             if (which == 1) {
                 T ms = 0, acc = 0;
-                for (int c = lane; c < R; c += 32) {
-                    const T xi = silu(conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c)) / D;
+#pragma unroll
+                for (int i = 0; i < BWD_LANE_CH; ++i) {
+                    const T xi = fv[i] / D;
                     ms = fma(xi, xi, ms);
                 }
                 r = sqrt(warp_sum_t(ms) / R + (T)IDA_EPS_RMS);
-                for (int c = lane; c < R; c += 32) {
-                    const T xi = silu(conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c)) / D;
-                    const T dkt = grow[R + c];
-                    acc = fma(dkt * (T)nw[c], xi, acc);
-                    if (own) {
-                        pnw[(size_t)warp * (R + d) + c] += dkt * xi / r;
-                        pbs[(size_t)warp * (R + d) + c] += dkt;
+#pragma unroll
+                for (int i = 0; i < BWD_LANE_CH; ++i) {
+                    const int c = lane + 32 * i;
+                    if (c < R) {
+                        const T xi = fv[i] / D;
+                        const T dkt = grow[R + c];
+                        acc = fma(dkt * (T)nw[c], xi, acc);
+                        if (own) {
+                            pnw[(size_t)warp * (R + d) + c] += dkt * xi / r;
+                            pbs[(size_t)warp * (R + d) + c] += dkt;
+                        }
                     }
                 }
                 sdy = warp_sum_t(acc);
             }
             // s = sum_c dxi[c] f[c] / D^2 term of the feature-map backward
+            T dxv[BWD_LANE_CH];
             T sdf = 0;
-            for (int c = lane; c < R; c += 32) {
-                const T f = silu(conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c));
-                const T xi = f / D;
-                const T dxi = which == 0 ? grow[c] : (grow[R + c] * (T)nw[c]) / r - xi * sdy / ((T)R * r * r * r);
-                sdf = fma(dxi, f, sdf);
+#pragma unroll
+            for (int i = 0; i < BWD_LANE_CH; ++i) {
+                const int c = lane + 32 * i;
+                dxv[i] = 0;
+                if (c < R) {
+                    const T xi = fv[i] / D;
+                    dxv[i] = which == 0 ? grow[c] : (grow[R + c] * (T)nw[c]) / r - xi * sdy / ((T)R * r * r * r);
+                    sdf = fma(dxv[i], fv[i], sdf);
+                }
             }
             sdf = warp_sum_t(sdf);
-            for (int c = lane; c < R; c += 32) {
-                const T s = conv_at<T>(x, a.dtype, base_qk, sqk, cw, W, t, c);
-                const T f = silu(s);
-                const T xi = f / D;
-                const T dxi = which == 0 ? grow[c] : (grow[R + c] * (T)nw[c]) / r - xi * sdy / ((T)R * r * r * r);
-                // dn/df = 2 f (squared norm) or f / n (l_2 norm)
-                const T dn = l2 ? (n > T(0) ? f / n : T(0)) : T(2) * f;
-                const T df = dxi / D - sdf / (D * D) * dn;
-                ds[((size_t)which * (BWD_TILE + 3) + p) * R + c] = df * silu_grad(s);
+#pragma unroll
+            for (int i = 0; i < BWD_LANE_CH; ++i) {
+                const int c = lane + 32 * i;
+                if (c < R) {
+                    const T f = fv[i];
+                    // dn/df = 2 f (squared norm) or f / n (l_2 norm)
+                    const T dn = l2 ? (n > T(0) ? f / n : T(0)) : T(2) * f;
+                    const T df = dxv[i] / D - sdf / (D * D) * dn;
+                    ds[((size_t)which * (BWD_TILE + 3) + p) * R + c] = df * silu_grad(sv[i]);
+                }
             }
         }
         if (own) {
-            // value RMSNorm backward
+            // value RMSNorm backward (my channels j = lane + 32 i, loaded once)
+            T xvv[BWD_LANE_CH];
             T ms = 0;
-            for (int j = lane; j < d; j += 32) {
-                const T xv = (T)load_in(a.v, a.dtype, base_v + (size_t)t * sv + j);
-                ms = fma(xv, xv, ms);
+#pragma unroll
+            for (int i = 0; i < BWD_LANE_CH; ++i) {
+                const int j = lane + 32 * i;
+                xvv[i] = j < d ? (T)load_in(a.v, a.dtype, base_v + (size_t)t * sv + j) : T(0);
+                ms = fma(xvv[i], xvv[i], ms);
             }
             const T r = sqrt(warp_sum_t(ms) / d + (T)IDA_EPS_RMS);
             T acc = 0;
-            for (int j = lane; j < d; j += 32) {
-                const T xv = (T)load_in(a.v, a.dtype, base_v + (size_t)t * sv + j);
-                const T dvt = grow[2 * R + j];
-                acc = fma(dvt * (T)nw[R + j], xv, acc);
-                pnw[(size_t)warp * (R + d) + R + j] += dvt * xv / r;
-                pbs[(size_t)warp * (R + d) + R + j] += dvt;
+#pragma unroll
+            for (int i = 0; i < BWD_LANE_CH; ++i) {
+                const int j = lane + 32 * i;
+                if (j < d) {
+                    const T dvt = grow[2 * R + j];
+                    acc = fma(dvt * (T)nw[R + j], xvv[i], acc);
+                    pnw[(size_t)warp * (R + d) + R + j] += dvt * xvv[i] / r;
+                    pbs[(size_t)warp * (R + d) + R + j] += dvt;
+                }
             }
             acc = warp_sum_t(acc);
-            for (int j = lane; j < d; j += 32) {
-                const T xv = (T)load_in(a.v, a.dtype, base_v + (size_t)t * sv + j);
-                const T dvt = grow[2 * R + j];
-                const T dv = (dvt * (T)nw[R + j]) / r - xv * acc / ((T)d * r * r * r);
-                store_out(a.dv, a.dtype, base_v + (size_t)t * sv + j, (float)dv);
+#pragma unroll
+            for (int i = 0; i < BWD_LANE_CH; ++i) {
+                const int j = lane + 32 * i;
+                if (j < d) {
+                    const T dvt = grow[2 * R + j];
+                    const T dv = (dvt * (T)nw[R + j]) / r - xvv[i] * acc / ((T)d * r * r * r);
+                    store_out(a.dv, a.dtype, base_v + (size_t)t * sv + j, (float)dv);
+                }
             }
         }
     }
@@ -1009,7 +1028,10 @@ static cudaError_t launch_backward_t(const BackwardArgs &a, void *workspace, cud
     cudaError_t e;
     bwd_features_kernel<T><<<units * tiles8, 256, 0, st>>>(a, ws, L);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_scan_a_kernel<T><<<units * (unsigned)L.S, BWD_THREADS, 0, st>>>(a, ws, L);
+    if (eta)
+        bwd_scan_a_kernel<T, true><<<units * (unsigned)L.S, BWD_THREADS, 0, st>>>(a, ws, L);
+    else
+        bwd_scan_a_kernel<T, false><<<units * (unsigned)L.S, BWD_THREADS, 0, st>>>(a, ws, L);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (eta) {
         bwd_scan_nd_kernel<T><<<units * tiles8, 256, 0, st>>>(a, ws, L);

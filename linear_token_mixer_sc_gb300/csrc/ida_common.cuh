@@ -73,6 +73,45 @@ __device__ __forceinline__ T warp_sum(T x) {
     return x;
 }
 
+// Sum of each of NV values over the 32 lanes of a warp by recursive halving: afterwards lane
+// l holds the full sum of value index rs_index<NV>(l), and the 32 / NV lanes that differ
+// from l only in their low bits hold the same one.  NV is a power of two <= 32; about
+// NV shuffles instead of 5 NV.
+template <int NV, typename T>
+__device__ __forceinline__ T warp_reduce_scatter(T (&v)[NV], int lane) {
+    int n = NV;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        if (n > 1) {
+            const bool hi = (lane & off) != 0;
+            const int hn = n >> 1;
+#pragma unroll
+            for (int k = 0; k < NV / 2; ++k) {
+                if (k < hn) {
+                    const T send = hi ? v[k] : v[k + hn];
+                    const T keep = hi ? v[k + hn] : v[k];
+                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            n = hn;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        }
+    }
+    return v[0];
+}
+// the value index lane l holds after warp_reduce_scatter<NV>
+template <int NV>
+__device__ __forceinline__ int rs_index(int lane) {
+    int idx = 0, n = NV;
+#pragma unroll
+    for (int off = 16; off >= 1 && n > 1; off >>= 1) {
+        n >>= 1;
+        if (lane & off) idx += n;
+    }
+    return idx;
+}
+
 // x <- lam * x + g * z for complex x, lam, g and real z, in arithmetic type T.
 template <typename T>
 __device__ __forceinline__ void cstep_t(T &xr, T &xi, T lr, T li, T gr, T gi, T z) {

@@ -10,8 +10,8 @@
 // [ROPE_TILE][R / 2] is built in shared memory first, its angles reduced modulo 2 pi in
 // fp64 (positions reach 1e4 radians and more, where an fp32 angle would already be off
 // by 1e-3), then every head of the tile's q rows, and of its k rows with the same
-// table, is rotated with 16-byte loads and stores.  HBM-bound: each element is read and
-// written once.
+// table, is rotated with 16-byte loads and stores, a thread's loads of all the tile's
+// positions issued together.  HBM-bound: each element is read and written once.
 #include <cstdint>
 #include <string>
 
@@ -21,7 +21,6 @@ namespace ida {
 
 constexpr int ROPE_TILE = 8;
 constexpr int ROPE_THREADS = 256;
-constexpr int ROPE_UNROLL = 4;  // 16-byte vectors in flight per thread
 
 template <typename E>
 struct RopeVec;  // 16 bytes of elements
@@ -62,13 +61,6 @@ __device__ __forceinline__ uint4 rope_pack(const float *x, __nv_bfloat16) {
 }
 
 template <typename E>
-__device__ __forceinline__ uint4 *rope_vec(void *q, void *k, size_t off, int vecs, int e) {
-    constexpr int V = RopeVec<E>::n;
-    E *x = static_cast<E *>(e < vecs ? q : k);
-    return reinterpret_cast<uint4 *>(x + off + (size_t)(e < vecs ? e : e - vecs) * V);
-}
-
-template <typename E>
 __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, int N, int H, int R, int pos0,
                                                             double log2_base) {
     __shared__ double inv[128];                   // base^(-2i / R), i < R / 2
@@ -77,20 +69,12 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, in
     const int tiles = (N + ROPE_TILE - 1) / ROPE_TILE;
     const int b = blockIdx.x / tiles, t0 = (blockIdx.x % tiles) * ROPE_TILE;
     const int len = min(ROPE_TILE, N - t0), half = R / 2;
-    const size_t row = (size_t)H * R;  // elements of one position
-    const size_t off = ((size_t)b * N + t0) * row;
-    // 16-byte vectors of the tile: q's, then k's; a thread takes ROPE_UNROLL of them per
-    // round, the next round's loads issued before the current round is rotated
-    const int vecs = (int)(len * row / V), total = k ? 2 * vecs : vecs;
-    uint4 cur[ROPE_UNROLL], nxt[ROPE_UNROLL];
-#pragma unroll
-    for (int u = 0; u < ROPE_UNROLL; ++u) {
-        const int e = threadIdx.x + u * ROPE_THREADS;
-        if (e < total) cur[u] = __ldcs(rope_vec<E>(q, k, off, vecs, e));
-    }
-    // the table, built while the first loads are in flight.  fp64 is scarce on this part:
-    // one exp2 per frequency, then a multiply and a reduction to [-pi, pi] per (position,
-    // frequency), before the fp32 sin / cos
+    // thread -> one 16-byte vector of channels (c0 .. c0 + V) in heads h0, h0 + S, ...: its
+    // cos / sin entries are read once per position and serve every head it rotates
+    const int vpr = R / V, S = ROPE_THREADS / vpr;
+    const int c0 = (threadIdx.x % vpr) * V, h0 = threadIdx.x / vpr;
+    // fp64 is scarce on this part: one exp2 per frequency, then a multiply and a reduction
+    // to [-pi, pi] per (position, frequency), before the fp32 sin / cos
     for (int i = threadIdx.x; i < half; i += ROPE_THREADS) inv[i] = exp2(-2.0 * i / R * log2_base);
     __syncthreads();
     const double two_pi = 6.283185307179586476925286766559, inv_two_pi = 0.15915494309189533576888376337251;
@@ -104,31 +88,34 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, in
         cs[2 * e + 1] = sn;
     }
     __syncthreads();
-    for (int e0 = threadIdx.x; e0 < total; e0 += ROPE_UNROLL * ROPE_THREADS) {
+    if (h0 >= S) return;  // R / V does not divide the block: spare threads
+    const size_t rowstride = (size_t)H * R;  // elements between positions
+    for (int which = 0; which < 2; ++which) {
+        E *x = static_cast<E *>(which == 0 ? q : k);
+        if (!x) break;
+        x += ((size_t)b * N + t0) * rowstride + c0;
+        for (int h = h0; h < H; h += S) {
+            uint4 w[ROPE_TILE];
 #pragma unroll
-        for (int u = 0; u < ROPE_UNROLL; ++u) {
-            const int e = e0 + (u + ROPE_UNROLL) * ROPE_THREADS;
-            if (e < total) nxt[u] = __ldcs(rope_vec<E>(q, k, off, vecs, e));
-        }
+            for (int tt = 0; tt < ROPE_TILE; ++tt)
+                if (tt < len) w[tt] = __ldcs(reinterpret_cast<const uint4 *>(x + tt * rowstride + (size_t)h * R));
 #pragma unroll
-        for (int u = 0; u < ROPE_UNROLL; ++u) {
-            const int e = e0 + u * ROPE_THREADS;
-            if (e >= total) break;
-            const size_t el = (size_t)(e < vecs ? e : e - vecs) * V;
-            const int tt = (int)(el / row), c0 = (int)(el % R);
-            float v[V];
-            rope_unpack(cur[u], v, E());
+            for (int tt = 0; tt < ROPE_TILE; ++tt) {
+                if (tt < len) {
+                    const float *t = cs + (size_t)(tt * half + c0 / 2) * 2;
+                    float v[V];
+                    rope_unpack(w[tt], v, E());
 #pragma unroll
-            for (int j = 0; j < V; j += 2) {
-                const float2 t = *reinterpret_cast<const float2 *>(cs + 2 * (tt * half + ((c0 + j) >> 1)));
-                const float x0 = v[j], x1 = v[j + 1];
-                v[j] = fmaf(x0, t.x, -x1 * t.y);
-                v[j + 1] = fmaf(x0, t.y, x1 * t.x);
+                    for (int j = 0; j < V; j += 2) {
+                        const float2 cn_sn = *reinterpret_cast<const float2 *>(t + j);
+                        const float x0 = v[j], x1 = v[j + 1];
+                        v[j] = fmaf(x0, cn_sn.x, -x1 * cn_sn.y);
+                        v[j + 1] = fmaf(x0, cn_sn.y, x1 * cn_sn.x);
+                    }
+                    __stcs(reinterpret_cast<uint4 *>(x + tt * rowstride + (size_t)h * R), rope_pack(v, E()));
+                }
             }
-            __stcs(rope_vec<E>(q, k, off, vecs, e), rope_pack(v, E()));
         }
-#pragma unroll
-        for (int u = 0; u < ROPE_UNROLL; ++u) cur[u] = nxt[u];
     }
 }
 
