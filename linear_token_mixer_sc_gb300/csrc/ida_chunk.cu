@@ -258,6 +258,14 @@ __global__ void __launch_bounds__(NTH, 1)
     float *nws = reinterpret_cast<float *>(sm + S::NWS);
     float *bss = reinterpret_cast<float *>(sm + S::BSS);
 
+    // The two instantiations are launched back to back, the second (skewed) as a programmatic
+    // dependent of the first: every factorised CTA releases it at once, and every skewed CTA
+    // waits for the factorised grid to complete before it does anything.  The skewed grid's
+    // launch then overlaps the factorised one, and its completion still implies that of both.
+    if constexpr (FACT)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    else
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hsel = warp >> 2;        // TMEM lane quarter, column / position half
     const int tl = 32 * q4 + lane;                    // my TMEM lane
@@ -1710,8 +1718,19 @@ static cudaError_t launch_chunk_rd_e(const PrefillArgs &a, cudaStream_t st, cons
         return e;
     kf<<<grid, NTH, S::TOTAL, st>>>(a, mq, mk, mv, mo, plan, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    ks<<<grid, NTH, S::TOTAL, st>>>(a, mq, mk, mv, mo, plan, ws);
-    return cudaGetLastError();
+    // the skewed instantiation as a programmatic dependent of the factorised one (see the kernel)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(NTH, 1, 1);
+    cfg.dynamicSmemBytes = S::TOTAL;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float *wsc = ws;
+    return cudaLaunchKernelEx(&cfg, ks, a, mq, mk, mv, mo, plan, wsc);
 }
 
 // The instantiation with the state_in / l_2 code only when the call uses either.

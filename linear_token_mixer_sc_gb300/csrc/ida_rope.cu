@@ -6,7 +6,7 @@
 // the rotation is applied to the query and key rows before the mixer.  Channel pairs
 // (2i, 2i + 1) of a row at position p rotate by p * base^(-2i / R).
 //
-// One CTA per (batch row, tile of ROPE_TILE positions): the tile's cos / sin table
+// Per (batch row, tile of ROPE_TILE positions), in a persistent grid: the tile's cos / sin table
 // [ROPE_TILE][R / 2] is built in shared memory first, its angles reduced modulo 2 pi in
 // fp64 (positions reach 1e4 radians and more, where an fp32 angle would already be off
 // by 1e-3), then every head of the tile's q rows, and of its k rows with the same
@@ -60,15 +60,15 @@ __device__ __forceinline__ uint4 rope_pack(const float *x, __nv_bfloat16) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Persistent: a grid of one wave of CTAs, CTA i taking tiles i, i + gridDim.x, ... of the
+// B x ceil(N / ROPE_TILE) tiles (no partly filled last wave).
 template <typename E>
-__global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, int N, int H, int R, int pos0,
+__global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, int B, int N, int H, int R, int pos0,
                                                             double log2_base) {
     __shared__ double inv[128];                   // base^(-2i / R), i < R / 2
     extern __shared__ __align__(16) float cs[];   // [ROPE_TILE][R / 2][2]: cos, sin
     constexpr int V = RopeVec<E>::n;
-    const int tiles = (N + ROPE_TILE - 1) / ROPE_TILE;
-    const int b = blockIdx.x / tiles, t0 = (blockIdx.x % tiles) * ROPE_TILE;
-    const int len = min(ROPE_TILE, N - t0), half = R / 2;
+    const int tiles = (N + ROPE_TILE - 1) / ROPE_TILE, half = R / 2;
     // thread -> one 16-byte vector of channels (c0 .. c0 + V) in heads h0, h0 + S, ...: its
     // cos / sin entries are read once per position and serve every head it rotates
     const int vpr = R / V, S = ROPE_THREADS / vpr;
@@ -76,43 +76,47 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, in
     // fp64 is scarce on this part: one exp2 per frequency, then a multiply and a reduction
     // to [-pi, pi] per (position, frequency), before the fp32 sin / cos
     for (int i = threadIdx.x; i < half; i += ROPE_THREADS) inv[i] = exp2(-2.0 * i / R * log2_base);
-    __syncthreads();
     const double two_pi = 6.283185307179586476925286766559, inv_two_pi = 0.15915494309189533576888376337251;
-    for (int e = threadIdx.x; e < len * half; e += ROPE_THREADS) {
-        const int tt = e / half, i = e % half;
-        const double ang = ((double)pos0 + (double)(t0 + tt)) * inv[i];
-        const float red = (float)fma(-two_pi, rint(ang * inv_two_pi), ang);
-        float sn, cn;
-        sincosf(red, &sn, &cn);
-        cs[2 * e] = cn;
-        cs[2 * e + 1] = sn;
-    }
-    __syncthreads();
-    if (h0 >= S) return;  // R / V does not divide the block: spare threads
-    const size_t rowstride = (size_t)H * R;  // elements between positions
-    for (int which = 0; which < 2; ++which) {
-        E *x = static_cast<E *>(which == 0 ? q : k);
-        if (!x) break;
-        x += ((size_t)b * N + t0) * rowstride + c0;
-        for (int h = h0; h < H; h += S) {
-            uint4 w[ROPE_TILE];
+    for (long long tile = blockIdx.x; tile < (long long)B * tiles; tile += gridDim.x) {
+        const int b = (int)(tile / tiles), t0 = (int)(tile % tiles) * ROPE_TILE;
+        const int len = min(ROPE_TILE, N - t0);
+        __syncthreads();  // inv is written; the previous tile's table is no longer read
+        for (int e = threadIdx.x; e < len * half; e += ROPE_THREADS) {
+            const int tt = e / half, i = e % half;
+            const double ang = ((double)pos0 + (double)(t0 + tt)) * inv[i];
+            const float red = (float)fma(-two_pi, rint(ang * inv_two_pi), ang);
+            float sn, cn;
+            sincosf(red, &sn, &cn);
+            cs[2 * e] = cn;
+            cs[2 * e + 1] = sn;
+        }
+        __syncthreads();
+        if (h0 >= S) continue;  // R / V does not divide the block: spare threads
+        const size_t rowstride = (size_t)H * R;  // elements between positions
+        for (int which = 0; which < 2; ++which) {
+            E *x = static_cast<E *>(which == 0 ? q : k);
+            if (!x) break;
+            x += ((size_t)b * N + t0) * rowstride + c0;
+            for (int h = h0; h < H; h += S) {
+                uint4 w[ROPE_TILE];
 #pragma unroll
-            for (int tt = 0; tt < ROPE_TILE; ++tt)
-                if (tt < len) w[tt] = __ldcs(reinterpret_cast<const uint4 *>(x + tt * rowstride + (size_t)h * R));
+                for (int tt = 0; tt < ROPE_TILE; ++tt)
+                    if (tt < len) w[tt] = __ldcs(reinterpret_cast<const uint4 *>(x + tt * rowstride + (size_t)h * R));
 #pragma unroll
-            for (int tt = 0; tt < ROPE_TILE; ++tt) {
-                if (tt < len) {
-                    const float *t = cs + (size_t)(tt * half + c0 / 2) * 2;
-                    float v[V];
-                    rope_unpack(w[tt], v, E());
+                for (int tt = 0; tt < ROPE_TILE; ++tt) {
+                    if (tt < len) {
+                        const float *t = cs + (size_t)(tt * half + c0 / 2) * 2;
+                        float v[V];
+                        rope_unpack(w[tt], v, E());
 #pragma unroll
-                    for (int j = 0; j < V; j += 2) {
-                        const float2 cn_sn = *reinterpret_cast<const float2 *>(t + j);
-                        const float x0 = v[j], x1 = v[j + 1];
-                        v[j] = fmaf(x0, cn_sn.x, -x1 * cn_sn.y);
-                        v[j + 1] = fmaf(x0, cn_sn.y, x1 * cn_sn.x);
+                        for (int j = 0; j < V; j += 2) {
+                            const float2 cn_sn = *reinterpret_cast<const float2 *>(t + j);
+                            const float x0 = v[j], x1 = v[j + 1];
+                            v[j] = fmaf(x0, cn_sn.x, -x1 * cn_sn.y);
+                            v[j + 1] = fmaf(x0, cn_sn.y, x1 * cn_sn.x);
+                        }
+                        __stcs(reinterpret_cast<uint4 *>(x + tt * rowstride + (size_t)h * R), rope_pack(v, E()));
                     }
-                    __stcs(reinterpret_cast<uint4 *>(x + tt * rowstride + (size_t)h * R), rope_pack(v, E()));
                 }
             }
         }
@@ -144,13 +148,21 @@ extern "C" ida_status ida_rope(void *q, void *k, int B, int N, int H, int R, int
     ida_status s = ida::check_call(8, R, 1, 1, dtype, 0, &num_sms, why);  // device set-up, pending errors
     if (s != IDA_OK) return ida::fail_with(s, why);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const unsigned grid = (unsigned)(B * tiles);
     const size_t smem = (size_t)ida::ROPE_TILE * (R / 2) * 2 * sizeof(float);
     const double lb = log2((double)base);
+    int per_sm = 0;
+    cudaError_t oe = dtype == IDA_F32
+                         ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ida::rope_kernel<float>,
+                                                                          ida::ROPE_THREADS, smem)
+                         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ida::rope_kernel<__nv_bfloat16>,
+                                                                          ida::ROPE_THREADS, smem);
+    if (oe != cudaSuccess || per_sm < 1) per_sm = 1;
+    const long long wave = (long long)per_sm * num_sms, ntiles = (long long)B * tiles;
+    const unsigned grid = (unsigned)(ntiles < wave ? ntiles : wave);
     if (dtype == IDA_F32)
-        ida::rope_kernel<float><<<grid, ida::ROPE_THREADS, smem, st>>>(q, k, N, H, R, pos0, lb);
+        ida::rope_kernel<float><<<grid, ida::ROPE_THREADS, smem, st>>>(q, k, B, N, H, R, pos0, lb);
     else
-        ida::rope_kernel<__nv_bfloat16><<<grid, ida::ROPE_THREADS, smem, st>>>(q, k, N, H, R, pos0, lb);
+        ida::rope_kernel<__nv_bfloat16><<<grid, ida::ROPE_THREADS, smem, st>>>(q, k, B, N, H, R, pos0, lb);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return ida::fail_with(IDA_ERR_CUDA, std::string("rope launch: ") + cudaGetErrorString(e));
     return IDA_OK;
