@@ -5,8 +5,8 @@ with the CUDA library (the seeded input generator aside) and nothing with the C
 oracle: it is a second, independent restatement of the forward pass, written
 with plain PyTorch CPU ops in float64 / complex128, whose gradients come from
 autograd.  It is pinned by agreement with the C oracle's forward and by
-finite differences (torch.autograd.gradcheck).  No library kernel computes
-gradients yet; this is the reference such a kernel will be checked against.
+finite differences (torch.autograd.gradcheck).  The library's backward pass
+(ida_backward) is checked against it.
 
 The forward follows "Interdomain Attention: Beyond Token-Level Key-Value Memory"
 (German technical summary, "Skalierbare Implementierung"; the ratio readout

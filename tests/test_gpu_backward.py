@@ -107,3 +107,34 @@ def test_backward_zero_length_gives_zero_parameter_gradients():
     torch.cuda.synchronize()
     for n in NAMES[3:]:
         assert torch.count_nonzero(g[n]).item() == 0, n
+
+
+def test_backward_full_125m_shape_sampled_head():
+    """The benchmark's backward workload as it launches it (B=8, H=12, N=2048, R=d=64, M=64,
+    bf16, with a caller workspace: two mode slices per unit, 192 CTAs), checked against the
+    autograd reference on every batch row of one head: dq, dk, dv of those 8 units and the
+    head's parameter gradients (sums over the batch rows), each over all positions."""
+    from linear_token_mixer_sc_gb300 import configs
+    w = configs.PREFILL_125M
+    p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
+    q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed)
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    dout = torch.randn(w.B, w.N, w.H, w.d, generator=g).to(q.dtype)
+    dev = torch.device("cuda")
+    nb = binding.ida_backward_workspace_bytes(w.B, w.H, w.N, w.d, w.R, w.M, binding.IDA_BF16, w.W, 0)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    got = binding.ida_backward(q.to(dev), k.to(dev), v.to(dev), binding.params_to_device(p), dout.to(dev),
+                               workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.ida_device_error() == 0
+    h = 5
+    hs = slice(h, h + 1)
+    ps = {"conv_w": p["conv_w"][:, hs], "norm_w": p["norm_w"][hs], "bias": p["bias"][hs],
+          "lambda": p["lambda"][hs], "Bvec": p["Bvec"][hs]}
+    ref = _ref(q[:, :, hs], k[:, :, hs], v[:, :, hs], ps, dout[:, :, hs], 0)
+    gh = {n: got[n].float().cpu().double().numpy() for n in NAMES}
+    sel = {"q": gh["q"][:, :, hs], "k": gh["k"][:, :, hs], "v": gh["v"][:, :, hs],
+           "conv_w": gh["conv_w"][:, hs], "norm_w": gh["norm_w"][hs], "bias": gh["bias"][hs],
+           "lambda": gh["lambda"][hs], "Bvec": gh["Bvec"][hs]}
+    errs = {n: rel_l2(sel[n], ref[n]) for n in NAMES}
+    assert all(e <= BF16_REL_L2 for e in errs.values()), errs

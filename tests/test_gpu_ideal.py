@@ -59,3 +59,28 @@ def test_ideal_layer_is_deterministic():
     o2 = binding.ida_forward_ideal(q.cuda(), k.cuda(), v.cuda(), om, pd)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
+
+
+def test_ideal_layer_full_125m_shape_sampled_units():
+    """The benchmark's ideal-layer workload as it launches it (B=8, H=12, N=2048, R_in = d = 64,
+    D = 32 frequencies, M = 64, bf16: two-CTA clusters over 96 units), checked against the
+    oracle on six (b,h) units spread over the batch and the heads, each over all positions."""
+    from linear_token_mixer_sc_gb300 import configs
+    w = configs.PREFILL_125M
+    D = 32
+    p = inputs.make_params(w.H, w.R, w.d, w.M, w.W, w.seed)
+    q, k, v = inputs.make_qkv(w.B, w.N, w.H, w.R, w.d, w.dtype, w.seed)
+    om = inputs.make_omega(w.H, D, w.R, w.seed)
+    dev = torch.device("cuda")
+    out = binding.ida_forward_ideal(q.to(dev), k.to(dev), v.to(dev), torch.from_numpy(om).to(dev),
+                                    binding.params_to_device(p))
+    torch.cuda.synchronize()
+    assert binding.ida_device_error() == 0
+    got = to_np(out)
+    lam = p["lambda"][..., 0].astype(np.float64) + 1j * p["lambda"][..., 1].astype(np.float64)
+    bc = p["Bvec"][..., 0].astype(np.float64) + 1j * p["Bvec"][..., 1].astype(np.float64)
+    for b, h in [(0, 0), (1, 7), (3, 11), (4, 2), (6, 5), (7, 9)]:
+        ref = ii.ideal_unit(q[b, :, h].double().numpy(), k[b, :, h].double().numpy(), v[b, :, h].double().numpy(),
+                            om[h].astype(np.float64), lam[h], bc[h])
+        err = rel_l2(got[b, :, h], ref)
+        assert err <= BF16_REL_L2, (b, h, err)
