@@ -154,57 +154,40 @@ __device__ __forceinline__ T conv_at(const void *x, int dtype, size_t base, size
     return s;
 }
 
-// a thread's eight mode values of one state plane, as 16-byte vectors (p 16-byte aligned)
-__device__ __forceinline__ void ldg8(const float *p, float (&o)[8]) {
-    const float4 x = reinterpret_cast<const float4 *>(p)[0], y = reinterpret_cast<const float4 *>(p)[1];
-    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
-    o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
-}
-__device__ __forceinline__ void ldg8(const double *p, double (&o)[8]) {
+// a thread's BWD_MGT mode values of one state plane, as 16-byte vectors (p 16-byte aligned)
+template <int K>
+__device__ __forceinline__ void ldgm(const float *p, float (&o)[K]) {
+    static_assert(K % 4 == 0, "whole float4 vectors");
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const double2 x = reinterpret_cast<const double2 *>(p)[i];
-        o[2 * i] = x.x;
-        o[2 * i + 1] = x.y;
+    for (int v = 0; v < K / 4; ++v) {
+        const float4 x = reinterpret_cast<const float4 *>(p)[v];
+        o[4 * v] = x.x;
+        o[4 * v + 1] = x.y;
+        o[4 * v + 2] = x.z;
+        o[4 * v + 3] = x.w;
     }
 }
-__device__ __forceinline__ void stg8(float *p, const float (&v)[8]) {
-    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-}
-__device__ __forceinline__ void stg8(double *p, const double (&v)[8]) {
+template <int K>
+__device__ __forceinline__ void ldgm(const double *p, double (&o)[K]) {
+    static_assert(K % 2 == 0, "whole double2 vectors");
 #pragma unroll
-    for (int i = 0; i < 4; ++i) reinterpret_cast<double2 *>(p)[i] = make_double2(v[2 * i], v[2 * i + 1]);
-}
-
-// eight values from the 16-byte vectors p[0], p[BWD_THREADS], ... (shared memory)
-__device__ __forceinline__ void unpack_vecs(const uint4 *p, float (&o)[8]) {
-#pragma unroll
-    for (int v = 0; v < 2; ++v) {
-        const uint4 w = p[(size_t)v * BWD_THREADS];
-        o[4 * v] = __uint_as_float(w.x);
-        o[4 * v + 1] = __uint_as_float(w.y);
-        o[4 * v + 2] = __uint_as_float(w.z);
-        o[4 * v + 3] = __uint_as_float(w.w);
+    for (int v = 0; v < K / 2; ++v) {
+        const double2 x = reinterpret_cast<const double2 *>(p)[v];
+        o[2 * v] = x.x;
+        o[2 * v + 1] = x.y;
     }
 }
-__device__ __forceinline__ void unpack_vecs(const uint4 *p, double (&o)[8]) {
+template <int K>
+__device__ __forceinline__ void stgm(float *p, const float (&o)[K]) {
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-        const uint4 w = p[(size_t)v * BWD_THREADS];
-        o[2 * v] = __hiloint2double((int)w.y, (int)w.x);
-        o[2 * v + 1] = __hiloint2double((int)w.w, (int)w.z);
-    }
+    for (int v = 0; v < K / 4; ++v)
+        reinterpret_cast<float4 *>(p)[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
 }
-
-// 16-byte asynchronous copy global -> shared (both 16-byte aligned), and its completion
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
-                 "l"(gsrc)
-                 : "memory");
+template <int K>
+__device__ __forceinline__ void stgm(double *p, const double (&o)[K]) {
+#pragma unroll
+    for (int v = 0; v < K / 2; ++v) reinterpret_cast<double2 *>(p)[v] = make_double2(o[2 * v], o[2 * v + 1]);
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 template <typename T>
 __device__ __forceinline__ T warp_sum_t(T x) {
@@ -325,8 +308,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_a_kernel(BackwardArgs
         for (int k = 0; k < L.nck; ++k) {
             const int t0 = k * C, len = min(C, N - t0);
             T *ck = ckpt + (size_t)k * L.sds;
-            stg8(ck + mine, xr);
-            stg8(ck + plane + mine, xi);
+            stgm(ck + mine, xr);
+            stgm(ck + plane + mine, xi);
             T zv[C];
 #pragma unroll
             for (int j = 0; j < C; ++j) zv[j] = col ? feat[(size_t)min(t0 + j, N - 1) * F + R + c] : T(0);
@@ -365,8 +348,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_a_kernel(BackwardArgs
         qq[u] = (kq && t + ZP < N) ? feat[(size_t)(t + ZP) * F + c] : T(0);
         if (t % L.chunk == 0) {
             T *ck = ckpt + (size_t)(t / L.chunk) * L.sds;
-            stg8(ck + mine, xr);
-            stg8(ck + plane + mine, xi);
+            stgm(ck + mine, xr);
+            stgm(ck + plane + mine, xi);
             if (eown) {
                 ck[eoff + tid] = er;
                 ck[eoff + q.MC + tid] = ei;
@@ -462,12 +445,7 @@ __global__ void __launch_bounds__(256) bwd_scan_nd_kernel(BackwardArgs a, T *ws,
     }
 }
 
-// eight consecutive values from 16-byte aligned shared memory
-__device__ __forceinline__ void lds8(const float *p, float (&o)[8]) {
-    const float4 x = reinterpret_cast<const float4 *>(p)[0], y = reinterpret_cast<const float4 *>(p)[1];
-    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
-    o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
-}
+// four consecutive values from 16-byte aligned shared memory
 __device__ __forceinline__ void lds4(const float *p, float (&o)[4]) {
     const float4 x = *reinterpret_cast<const float4 *>(p);
     o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
@@ -475,14 +453,6 @@ __device__ __forceinline__ void lds4(const float *p, float (&o)[4]) {
 __device__ __forceinline__ void lds4(const double *p, double (&o)[4]) {
     const double2 x = reinterpret_cast<const double2 *>(p)[0], y = reinterpret_cast<const double2 *>(p)[1];
     o[0] = x.x; o[1] = x.y; o[2] = y.x; o[3] = y.y;
-}
-__device__ __forceinline__ void lds8(const double *p, double (&o)[8]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const double2 x = reinterpret_cast<const double2 *>(p)[i];
-        o[2 * i] = x.x;
-        o[2 * i + 1] = x.y;
-    }
 }
 
 // Dynamic shared memory of bwd_scan_b, in elements of T.
@@ -562,8 +532,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_b_kernel(BackwardArgs
         // ---- 1. forward through the chunk
         const T *ck = ckpt + (size_t)k * L.sds;
         T ur[BWD_MGT], ui[BWD_MGT];
-        ldg8(ck + mine, ur);
-        ldg8(ck + plane + mine, ui);
+        ldgm(ck + mine, ur);
+        ldgm(ck + plane + mine, ui);
         if (ETA)
             for (int j = tid; j < len; j += NT) gds[j] = base[L.gsc + 2 * (size_t)(t0 + j) + 1];
         // my inputs of every position of the chunk, all loads issued together: s = xi(q) (key
@@ -591,8 +561,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_b_kernel(BackwardArgs
 #pragma unroll
             for (int j = 0; j < C; ++j) inp[(size_t)(2 * j) * NT + tid] = inp[(size_t)(2 * j + 1) * NT + tid] = T(0);
         }
-        stg8(xbuf + mine, ur);
-        stg8(xbuf + plane + mine, ui);
+        stgm(xbuf + mine, ur);
+        stgm(xbuf + plane + mine, ui);
         T er = 0, e_i = 0;
         if (eown) {
             er = ck[eoff + tid];
@@ -619,8 +589,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_b_kernel(BackwardArgs
                 }
             }
             T *xb = xbuf + (size_t)(j + 1) * L.sds;
-            stg8(xb + mine, ur);
-            stg8(xb + plane + mine, ui);
+            stgm(xb + mine, ur);
+            stgm(xb + plane + mine, ui);
             if (eown) {
                 const T elr = lam_s[0][em], eli = lam_s[1][em], ebr = bv_s[0][em], ebi = bv_s[1][em];
                 const T nr = fma(elr, er, fma(-eli, e_i, ebr)), ni = fma(elr, e_i, fma(eli, er, ebi));
@@ -687,8 +657,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_scan_b_kernel(BackwardArgs
         for (int j = len - 1; j >= 0; --j) {
             T pr[BWD_MGT], pi[BWD_MGT];  // X_{t-1}
             const T *xp = xbuf + (size_t)j * L.sds;
-            ldg8(xp + mine, pr);
-            ldg8(xp + plane + mine, pi);
+            ldgm(xp + mine, pr);
+            ldgm(xp + plane + mine, pi);
             const T s = inp[(size_t)(2 * j) * NT + tid], zc = inp[(size_t)(2 * j + 1) * NT + tid];
             const T xq = kcol ? s : T(0), gn = vcol ? s : T(0);
             const T *amj = am + (size_t)(2 * j) * GM + gm, *abj = abm + (size_t)(2 * j) * GM + gm;
