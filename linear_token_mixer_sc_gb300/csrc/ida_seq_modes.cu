@@ -114,6 +114,36 @@ __device__ __forceinline__ void group_allreduce8(float (&p)[8], int lane) {
         p[v] = __shfl_sync(FULL, s, ((v >> 2) & 1) * (LG / 2) + ((v >> 1) & 1) * (LG / 4) + (v & 1) * (LG / 8), LG);
 }
 
+// The same for p[0..16) (two positions' values), LG >= 16: four halving exchanges, then
+// sixteen broadcasts.
+template <int LG>
+__device__ __forceinline__ void group_allreduce16(float (&p)[16], int lane) {
+    static_assert(LG >= 16, "four halving levels need 16 lanes");
+#pragma unroll
+    for (int lvl = 0; lvl < 4; ++lvl) {
+        const int o = LG >> (lvl + 1), n = 8 >> lvl;  // values kept after this level: n
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i < n) {
+                const float send = hi ? p[i] : p[i + n];
+                const float keep = hi ? p[i + n] : p[i];
+                p[i] = keep + __shfl_xor_sync(FULL, send, o);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = LG / 32; o > 0; o >>= 1) p[0] += __shfl_xor_sync(FULL, p[0], o);
+    const float s = p[0];
+    // value v sits in the lanes whose bits LG/2, LG/4, LG/8, LG/16 spell v
+#pragma unroll
+    for (int v = 0; v < 16; ++v)
+        p[v] = __shfl_sync(FULL, s,
+                           ((v >> 3) & 1) * (LG / 2) + ((v >> 2) & 1) * (LG / 4) + ((v >> 1) & 1) * (LG / 8) +
+                               (v & 1) * (LG / 16),
+                           LG);
+}
+
 typedef unsigned long long f2_t;  // two fp32 in one 64-bit register
 
 __device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
@@ -497,13 +527,104 @@ __global__ void __launch_bounds__(SM_MAXW * 32, 2) seq_modes_kernel(PrefillArgs 
             xp += R;
             zp += 2 * R;
         };
+        // Two positions at once (LG >= 16): the key-column updates and a_t parts of both,
+        // one 16-value group all-reduce for both (a_t does not depend on the value columns),
+        // then the value-column updates and readouts in order.
+        auto step2 = [&](uint32_t uo, uint32_t ud) {
+            float p[16];
+#pragma unroll
+            for (int sp = 0; sp < 2; ++sp) {
+                const ulonglong2 x4 = *reinterpret_cast<const ulonglong2 *>(xp + sp * R);
+                const ulonglong2 k4 = *reinterpret_cast<const ulonglong2 *>(zp + sp * 2 * R);
+                const f2_t x[2] = {x4.x, x4.y}, zk[2] = {k4.x, k4.y};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    f2_t sr = 0ull, si = 0ull;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const f2_t t1 = f2_mul(li2[j], ur[j][i]);
+                        const f2_t t2 = f2_fma(nli2[j], ui[j][i], zk[i]);
+                        ui[j][i] = f2_fma(lr2[j], ui[j][i], t1);
+                        ur[j][i] = f2_fma(lr2[j], ur[j][i], t2);
+                        sr = i == 0 ? f2_mul(x[i], ur[j][i]) : f2_fma(x[i], ur[j][i], sr);
+                        si = i == 0 ? f2_mul(x[i], ui[j][i]) : f2_fma(x[i], ui[j][i], si);
+                    }
+                    float a0, a1, b0, b1;
+                    f2_unpack(sr, a0, a1);
+                    f2_unpack(si, b0, b1);
+                    p[8 * sp + 2 * j] = a0 + a1;
+                    p[8 * sp + 2 * j + 1] = b0 + b1;
+                }
+            }
+            if constexpr (LG >= 16) {
+                group_allreduce16<LG>(p, lane);
+            } else {
+                float p0[8], p1[8];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    p0[v] = p[v];
+                    p1[v] = p[8 + v];
+                }
+                group_allreduce8<LG>(p0, lane);
+                group_allreduce8<LG>(p1, lane);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    p[v] = p0[v];
+                    p[8 + v] = p1[v];
+                }
+            }
+#pragma unroll
+            for (int sp = 0; sp < 2; ++sp) {
+                const ulonglong2 v4 = *reinterpret_cast<const ulonglong2 *>(zp + sp * 2 * R + R);
+                const f2_t zv[2] = {v4.x, v4.y};
+                f2_t o2[2] = {0ull, 0ull};
+                float dn = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const f2_t t1 = f2_mul(li2[j], gr[j][i]);
+                        const f2_t t2 = f2_fma(nli2[j], gi[j][i], zv[i]);
+                        gi[j][i] = f2_fma(lr2[j], gi[j][i], t1);
+                        gr[j][i] = f2_fma(lr2[j], gr[j][i], t2);
+                    }
+                    float lrj, lrh, lij, lih;
+                    f2_unpack(lr2[j], lrj, lrh);
+                    f2_unpack(li2[j], lij, lih);
+                    const float t1 = lij * er[j];
+                    const float t2 = fmaf(-lij, ei[j], 1.f);
+                    ei[j] = fmaf(lrj, ei[j], t1);
+                    er[j] = fmaf(lrj, er[j], t2);
+                    const float br = fmaf(b2r[j], p[8 * sp + 2 * j], -b2i[j] * p[8 * sp + 2 * j + 1]);
+                    const float nbi = fmaf(-b2r[j], p[8 * sp + 2 * j + 1], -b2i[j] * p[8 * sp + 2 * j]);  // -Im beta
+                    const f2_t br2 = f2_pack(br, br), nbi2 = f2_pack(nbi, nbi);
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) o2[i] = f2_fma(br2, gr[j][i], f2_fma(nbi2, gi[j][i], o2[i]));
+                    if (ETA) dn = fmaf(br, er[j], fmaf(nbi, ei[j], dn));
+                }
+                float o[4];
+                f2_unpack(o2[0], o[0], o[1]);
+                f2_unpack(o2[1], o[2], o[3]);
+#pragma unroll
+                for (int off = LG; off < 32; off <<= 1) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[i] += __shfl_xor_sync(FULL, o[i], off);
+                    if (ETA) dn += __shfl_xor_sync(FULL, dn, off);
+                }
+                if (LG == 32 || lane < LG) st_cluster(uo + sp * 4 * R, o[0], o[1], o[2], o[3]);
+                if (ETA && lane == 0) st_cluster(ud + sp * 4, dn);
+            }
+            xp += 2 * R;
+            zp += 4 * R;
+        };
         // positions [ow PT, ow PT + PT) of the tile are written by CTA ow: their partials are
         // asynchronous stores into its shared memory
         for (int ow = 0; ow * PT < tn; ++ow) {
             uint32_t uo = G > 1 ? mapa_u32(ao, ow) : ao, ud = G > 1 ? mapa_u32(ad, ow) : ad;
             const int te = min(tn, ow * PT + PT);
-#pragma unroll 2
-            for (int tt = ow * PT; tt < te; ++tt, uo += 4 * R, ud += 4) step(uo, ud);
+            int tt = ow * PT;
+            for (; tt + 1 < te; tt += 2, uo += 8 * R, ud += 8) step2(uo, ud);
+            if (tt < te) step(uo, ud);
         }
     };
 
