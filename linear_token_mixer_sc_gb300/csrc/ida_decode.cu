@@ -26,7 +26,7 @@ namespace ida {
 
 constexpr int DEC_WARPS = 4;
 constexpr int DEC_THREADS = DEC_WARPS * 32;
-constexpr int DEC_UNROLL = 2;  // modes in flight per warp
+constexpr int DEC_UNROLL = 1;  // modes per load group (two groups in flight per warp)
 
 // Features of one new position for one unit, one warp each (q, k, v); a lane handles
 // channels lane + 32 i, i < 4 NV (R, d <= 128 NV).  Shifts the raw conv tails of q and k in
