@@ -7,11 +7,12 @@
 // (2i, 2i + 1) of a row at position p rotate by p * base^(-2i / R).
 //
 // Per (batch row, tile of ROPE_TILE positions), in a persistent grid: the tile's cos / sin table
-// [ROPE_TILE][R / 2] is built in shared memory first, its angles reduced modulo 2 pi in
-// fp64 (positions reach 1e4 radians and more, where an fp32 angle would already be off
-// by 1e-3), then every head of the tile's q rows, and of its k rows with the same
-// table, is rotated with 16-byte loads and stores, a thread's loads of all the tile's
-// positions issued together.  HBM-bound: each element is read and written once.
+// [ROPE_TILE][R / 2] is built in shared memory first, its angles reduced modulo 2 pi exactly
+// in integer arithmetic (positions reach 1e4 radians and more, where an fp32 angle would
+// already be off by 1e-3), then every head of the tile's q rows, and of its k rows with
+// the same table, is rotated with 16-byte loads and stores, a thread's loads of all the
+// tile's positions issued together.
+// HBM-bound: each element is read and written once.
 #include <cstdint>
 #include <string>
 
@@ -66,7 +67,7 @@ __device__ __forceinline__ uint4 rope_pack(const float *x, __nv_bfloat16) {
 template <typename E>
 __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, int B, int N, int H, int R, int pos0,
                                                             double log2_base) {
-    __shared__ double inv[128];                   // base^(-2i / R), i < R / 2
+    __shared__ unsigned long long turn[128];      // base^(-2i / R) / (2 pi), as a 0.64 fixed-point fraction
     extern __shared__ __align__(16) float cs[];   // [ROPE_TILE][R / 2][2]: cos, sin
     constexpr int V = RopeVec<E>::n;
     const int tiles = (N + ROPE_TILE - 1) / ROPE_TILE, half = R / 2;
@@ -74,26 +75,32 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, in
     // cos / sin entries are read once per position and serve every head it rotates
     const int vpr = R / V, S = ROPE_THREADS / vpr;
     const int c0 = (threadIdx.x % vpr) * V, h0 = threadIdx.x / vpr;
-    // fp64 is scarce on this part: one exp2 per frequency, then a multiply and a reduction
-    // to [-pi, pi] per (position, frequency), before the fp32 sin / cos
-    for (int i = threadIdx.x; i < half; i += ROPE_THREADS) inv[i] = exp2(-2.0 * i / R * log2_base);
-    const double two_pi = 6.283185307179586476925286766559, inv_two_pi = 0.15915494309189533576888376337251;
+    // The angle of position p and frequency i is p * base^(-2i/R) radians, i.e. p * turn_i
+    // turns.  turn_i is formed once per CTA in fp64 (fp64 is scarce on this part) and kept
+    // as a 64-bit binary fraction; p * turn_i mod 1 is then an exact integer product mod
+    // 2^64, whose top 32 bits, read as a signed fraction of half a turn, go to sincospif.
+    for (int i = threadIdx.x; i < half; i += ROPE_THREADS) {
+        const double tr = exp2(-2.0 * i / R * log2_base) * 0.15915494309189533576888376337251;  // / (2 pi)
+        turn[i] = __double2ull_rn(ldexp(tr, 64));  // tr < 1 / (2 pi): no overflow
+    }
+    const size_t rowstride = (size_t)H * R;  // elements between positions
+    const bool worker = h0 < S;                // R / V does not divide the block: spare threads
     for (long long tile = blockIdx.x; tile < (long long)B * tiles; tile += gridDim.x) {
         const int b = (int)(tile / tiles), t0 = (int)(tile % tiles) * ROPE_TILE;
         const int len = min(ROPE_TILE, N - t0);
-        __syncthreads();  // inv is written; the previous tile's table is no longer read
+        __syncthreads();  // turn is written; the previous tile's table is no longer read
         for (int e = threadIdx.x; e < len * half; e += ROPE_THREADS) {
             const int tt = e / half, i = e % half;
-            const double ang = ((double)pos0 + (double)(t0 + tt)) * inv[i];
-            const float red = (float)fma(-two_pi, rint(ang * inv_two_pi), ang);
+            const unsigned long long pos = (unsigned long long)pos0 + (unsigned long long)(t0 + tt);
+            const unsigned long long ph = pos * turn[i];  // mod 2^64: the fraction of a turn
+            const float x = (float)(int)(unsigned)(ph >> 32) * 4.656612873077392578125e-10f;  // * 2^-31
             float sn, cn;
-            sincosf(red, &sn, &cn);
+            sincospif(x, &sn, &cn);
             cs[2 * e] = cn;
             cs[2 * e + 1] = sn;
         }
         __syncthreads();
-        if (h0 >= S) continue;  // R / V does not divide the block: spare threads
-        const size_t rowstride = (size_t)H * R;  // elements between positions
+        if (!worker) continue;
         for (int which = 0; which < 2; ++which) {
             E *x = static_cast<E *>(which == 0 ? q : k);
             if (!x) break;
@@ -150,7 +157,7 @@ extern "C" ida_status ida_rope(void *q, void *k, int B, int N, int H, int R, int
     if (s != IDA_OK) return ida::fail_with(s, why);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t smem = (size_t)ida::ROPE_TILE * (R / 2) * 2 * sizeof(float);
-    const double lb = log2((double)base);
+    const double lb = log2((double)base);  // base^(-2i/R) = exp2(-2i/R * lb)
     int per_sm = 0;
     cudaError_t oe = dtype == IDA_F32
                          ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ida::rope_kernel<float>,
