@@ -62,19 +62,40 @@ __device__ __forceinline__ uint4 rope_pack(const float *x, __nv_bfloat16) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// The cos / sin table of the tile starting at t0 (len positions), as float2 slots laid out
+// [position][pair u of a vector][vector cv], pair i = cv (V / 2) + u: for each u the lanes,
+// which own consecutive vectors, read consecutive 8-byte words.
+template <int V>
+__device__ __forceinline__ void rope_table(float2 *tab, const unsigned long long *turn, int pos0, int t0, int len,
+                                           int half) {
+    constexpr int P2 = V / 2;  // channel pairs per vector
+    const int vpr = half / P2;
+    for (int e = threadIdx.x; e < len * half; e += ROPE_THREADS) {
+        const int tt = e / half, i = e % half;
+        const unsigned long long pos = (unsigned long long)pos0 + (unsigned long long)(t0 + tt);
+        const unsigned long long ph = pos * turn[i];  // mod 2^64: the fraction of a turn
+        const float x = (float)(int)(unsigned)(ph >> 32) * 4.656612873077392578125e-10f;  // * 2^-31
+        float sn, cn;
+        sincospif(x, &sn, &cn);
+        tab[(tt * P2 + i % P2) * vpr + i / P2] = make_float2(cn, sn);
+    }
+}
+
 // Persistent: a grid of one wave of CTAs, CTA i taking tiles i, i + gridDim.x, ... of the
-// B x ceil(N / ROPE_TILE) tiles (no partly filled last wave).
+// B x ceil(N / ROPE_TILE) tiles (no partly filled last wave).  Two tables: the next tile's
+// is built while the current tile is rotated, one block barrier per tile.
 template <typename E>
 __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, int B, int N, int H, int R, int pos0,
                                                             double log2_base) {
     __shared__ unsigned long long turn[128];      // base^(-2i / R) / (2 pi), as a 0.64 fixed-point fraction
-    extern __shared__ __align__(16) float cs[];   // [ROPE_TILE][R / 2][2]: cos, sin
-    constexpr int V = RopeVec<E>::n;
+    extern __shared__ __align__(16) float2 cs[];  // [2][ROPE_TILE][R / 2]: the two tables (cos, sin)
+    constexpr int V = RopeVec<E>::n, P2 = V / 2;
     const int tiles = (N + ROPE_TILE - 1) / ROPE_TILE, half = R / 2;
-    // thread -> one 16-byte vector of channels (c0 .. c0 + V) in heads h0, h0 + S, ...: its
-    // cos / sin entries are read once per position and serve every head it rotates
+    const long long ntiles = (long long)B * tiles;
+    // thread -> one 16-byte vector cv of channels (c0 = cv V .. c0 + V) in heads h0, h0 + S,
+    // ...: its cos / sin entries are read once per position and serve every head it rotates
     const int vpr = R / V, S = ROPE_THREADS / vpr;
-    const int c0 = (threadIdx.x % vpr) * V, h0 = threadIdx.x / vpr;
+    const int cv = threadIdx.x % vpr, c0 = cv * V, h0 = threadIdx.x / vpr;
     // The angle of position p and frequency i is p * base^(-2i/R) radians, i.e. p * turn_i
     // turns.  turn_i is formed once per CTA in fp64 (fp64 is scarce on this part) and kept
     // as a 64-bit binary fraction; p * turn_i mod 1 is then an exact integer product mod
@@ -83,25 +104,27 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, in
         const double tr = exp2(-2.0 * i / R * log2_base) * 0.15915494309189533576888376337251;  // / (2 pi)
         turn[i] = __double2ull_rn(ldexp(tr, 64));  // tr < 1 / (2 pi): no overflow
     }
+    __syncthreads();
     const size_t rowstride = (size_t)H * R;  // elements between positions
     const bool worker = h0 < S;                // R / V does not divide the block: spare threads
-    for (long long tile = blockIdx.x; tile < (long long)B * tiles; tile += gridDim.x) {
+    const int tsize = ROPE_TILE * half;        // float2 slots per table
+    long long tile = blockIdx.x;
+    if (tile < ntiles) {
+        const int t0 = (int)(tile % tiles) * ROPE_TILE;
+        rope_table<V>(cs, turn, pos0, t0, min(ROPE_TILE, N - t0), half);
+    }
+    __syncthreads();
+    for (int cur = 0; tile < ntiles; tile += gridDim.x, cur ^= 1) {
         const int b = (int)(tile / tiles), t0 = (int)(tile % tiles) * ROPE_TILE;
         const int len = min(ROPE_TILE, N - t0);
-        __syncthreads();  // turn is written; the previous tile's table is no longer read
-        for (int e = threadIdx.x; e < len * half; e += ROPE_THREADS) {
-            const int tt = e / half, i = e % half;
-            const unsigned long long pos = (unsigned long long)pos0 + (unsigned long long)(t0 + tt);
-            const unsigned long long ph = pos * turn[i];  // mod 2^64: the fraction of a turn
-            const float x = (float)(int)(unsigned)(ph >> 32) * 4.656612873077392578125e-10f;  // * 2^-31
-            float sn, cn;
-            sincospif(x, &sn, &cn);
-            cs[2 * e] = cn;
-            cs[2 * e + 1] = sn;
+        // the next tile's table, into the buffer last read before the previous barrier
+        const long long nxt = tile + gridDim.x;
+        if (nxt < ntiles) {
+            const int t1 = (int)(nxt % tiles) * ROPE_TILE;
+            rope_table<V>(cs + (cur ^ 1) * tsize, turn, pos0, t1, min(ROPE_TILE, N - t1), half);
         }
-        __syncthreads();
-        if (!worker) continue;
-        for (int which = 0; which < 2; ++which) {
+        const float2 *tab = cs + cur * tsize;
+        for (int which = 0; which < 2 && worker; ++which) {
             E *x = static_cast<E *>(which == 0 ? q : k);
             if (!x) break;
             x += ((size_t)b * N + t0) * rowstride + c0;
@@ -113,21 +136,21 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(void *q, void *k, in
 #pragma unroll
                 for (int tt = 0; tt < ROPE_TILE; ++tt) {
                     if (tt < len) {
-                        const float *t = cs + (size_t)(tt * half + c0 / 2) * 2;
                         float v[V];
                         rope_unpack(w[tt], v, E());
 #pragma unroll
-                        for (int j = 0; j < V; j += 2) {
-                            const float2 cn_sn = *reinterpret_cast<const float2 *>(t + j);
-                            const float x0 = v[j], x1 = v[j + 1];
-                            v[j] = fmaf(x0, cn_sn.x, -x1 * cn_sn.y);
-                            v[j + 1] = fmaf(x0, cn_sn.y, x1 * cn_sn.x);
+                        for (int u = 0; u < P2; ++u) {
+                            const float2 cn_sn = tab[(tt * P2 + u) * vpr + cv];
+                            const float x0 = v[2 * u], x1 = v[2 * u + 1];
+                            v[2 * u] = fmaf(x0, cn_sn.x, -x1 * cn_sn.y);
+                            v[2 * u + 1] = fmaf(x0, cn_sn.y, x1 * cn_sn.x);
                         }
                         __stcs(reinterpret_cast<uint4 *>(x + tt * rowstride + (size_t)h * R), rope_pack(v, E()));
                     }
                 }
             }
         }
+        __syncthreads();  // the next table is complete; this one is free after the next build
     }
 }
 
@@ -156,7 +179,7 @@ extern "C" ida_status ida_rope(void *q, void *k, int B, int N, int H, int R, int
     ida_status s = ida::check_call(8, R, 1, 1, dtype, 0, &num_sms, why);  // device set-up, pending errors
     if (s != IDA_OK) return ida::fail_with(s, why);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const size_t smem = (size_t)ida::ROPE_TILE * (R / 2) * 2 * sizeof(float);
+    const size_t smem = 2 * (size_t)ida::ROPE_TILE * (R / 2) * sizeof(float2);
     const double lb = log2((double)base);  // base^(-2i/R) = exp2(-2i/R * lb)
     int per_sm = 0;
     cudaError_t oe = dtype == IDA_F32
