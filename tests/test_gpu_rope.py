@@ -1,11 +1,11 @@
 """GPU parity of ida_rope (rotary position embeddings on q and k, in place) against the
 fp64 oracle ``oracle/ida_rope.py``, itself pinned by closed forms and invariants.
 
-Bars, from the arithmetic: the angle is formed and reduced in fp64, sin / cos and the
-rotation run in fp32, so an fp32 result is within a few fp32 ulps of the exact value
-(max-abs <= 2e-6 on unit-variance inputs, rel-L2 <= 1e-6); a bf16 result is the fp32
-value rounded once to bf16, so each element is within half a bf16 ulp (2^-8 |x|) plus
-that fp32 error of the exact value.
+Bars, from the arithmetic: the angle is reduced modulo 2 pi exactly (a 64-bit fixed-point
+phase), sin / cos and the rotation run in fp32, so an fp32 result is within a few fp32
+ulps of the exact value (max-abs <= 2e-6 on unit-variance inputs, rel-L2 <= 1e-6); a bf16
+result is the fp32 value rounded once to bf16, so each element is within half a bf16 ulp
+(2^-8 |x|) plus that fp32 error of the exact value.
 """
 import numpy as np
 import pytest
@@ -47,11 +47,13 @@ CASES = [
     (2, 37, 3, 32, 0, 10000.0, "f32"),              # a ragged last tile of positions
     (1, 8, 1, 8, 0, 10000.0, "f32"),                # the smallest head width, one tile
     (1, 21, 2, 256, 5, 10000.0, "f32"),             # the widest head
-    (2, 50, 4, 64, 1_000_000, 10000.0, "f32"),      # angles of 1e6 radians (reduced in fp64)
+    (2, 50, 4, 64, 1_000_000, 10000.0, "f32"),      # angles of 1e6 radians
     (1, 20, 2, 128, 2_000_000_000, 10000.0, "f32"),  # positions past 2^31 - 1 within the call
     (2, 33, 2, 128, 17, 500000.0, "f32"),           # another base
     (3, 70, 4, 128, 0, 10000.0, "bf16"),
     (1, 9, 16, 64, 4096, 10000.0, "bf16"),
+    (2, 23, 5, 24, 3, 10000.0, "f32"),              # R / 4 = 6 vectors per row: 4 spare threads per CTA
+    (1, 31, 7, 40, 11, 10000.0, "bf16"),            # R / 8 = 5 vectors per row: 1 spare thread per CTA
 ]
 
 
