@@ -307,9 +307,10 @@ IDA_API ida_status ida_forward_ideal(const void *q, const void *k, const void *v
  *          (k may be NULL: only q is rotated; k must not alias q);
  *   pos0   the position of row t = 0 (>= 0), e.g. the length already decoded;
  *   base   the frequency base (> 1; 10000 in the Llama decoder).
- * Supported: 8 <= R <= 256 with R % 8 == 0, H*R <= 2^24.  Angles are formed
- * and reduced modulo 2 pi in fp64, sin / cos and the rotation in fp32 (bf16
- * inputs are rounded back to bf16).  N == 0, B == 0 or H == 0 does nothing.
+ * Supported: 8 <= R <= 256 with R % 8 == 0, H*R <= 2^24.  Each frequency is
+ * formed in fp64 and the angle reduced modulo 2 pi exactly (a 64-bit
+ * fixed-point phase); sin / cos and the rotation run in fp32 (bf16 inputs
+ * are rounded back to bf16).  N == 0, B == 0 or H == 0 does nothing.
  * Asynchronous on `stream`; allocates nothing.
  */
 IDA_API ida_status ida_rope(void *q, void *k, int B, int N, int H, int R,
