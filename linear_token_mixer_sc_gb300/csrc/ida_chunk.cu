@@ -1366,18 +1366,10 @@ struct StateSmem {
     static constexpr int NWS = TSLOT + 16;                            // [R+D] float
     static constexpr int BSS = NWS + (R + D) * 4;                     // [R+D] float
     static constexpr int TOTAL = BSS + (R + D) * 4;
-    static_assert(RAWV % 1024 == 0 && TOTAL <= 116 * 1024, "shared memory budget");
-    // Launched with LAUNCH bytes so that one CTA runs per SM.  With two co-resident CTAs
-    // that each accumulate two or more chunks into their TMEM state, a few block states
-    // per call came out wrong on GB300 (a part of one block's U or Gamma^T accumulator off
-    // by 0.1 to 13 %, not another block's value, not zero); one chunk per CTA, or one CTA
-    // per SM, was always bitwise reproducible.  tcgen05 and proxy fences after the in-loop
-    // wait, waiting for each chunk's MMAs right after issuing them, moving the wait to the
-    // top of the iteration, issuing the Gamma^T MMAs first and a 128-aligned Gamma^T column
-    // did not remove it; the cause is not identified, so the pass is kept at one CTA per SM.
-    static constexpr int LAUNCH = 116 * 1024;
-    // two CTAs of LAUNCH bytes exceed the 228 KB of shared memory of an sm_103a SM
-    static_assert(2 * LAUNCH > 228 * 1024, "the state pass must run one CTA per SM");
+    // two CTAs fit an SM's shared memory and TMEM (256 columns each); the register count
+    // (__launch_bounds__(NTH, 1)) keeps the pass at one CTA per SM, which timed faster than two
+    // CTAs per SM at 128 registers
+    static_assert(RAWV % 1024 == 0 && 2 * TOTAL <= 227 * 1024, "shared memory budget");
 };
 
 template <int R, int D, bool EXT>
@@ -1515,6 +1507,11 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
         for (int pp = 0; pp < PPV; ++pp)
             vraw[pp] = *reinterpret_cast<const uint4 *>(sm + S::RAWV + ((size_t)(iv0 + pp) * D + j0) * 2);
+        // The TMA below rewrites the tiles just read.  A block barrier orders those generic
+        // reads only against other generic accesses: without a proxy fence a shared-memory load
+        // still in flight can return the TMA's new row (seen on GB300 as the last key row of a
+        // chunk read from the next chunk, in about 3 % of calls at two CTAs per SM).
+        fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0 && ci + 1 < c_end) {
             const int tn = (ci + 1) * CH;
@@ -1703,9 +1700,9 @@ static cudaError_t launch_chunk_rd_e(const PrefillArgs &a, cudaStream_t st, cons
     if (plan.ppu > 1) {
         using SS = StateSmem<R, D>;
         auto sk = chunk_state_kernel<R, D, EXT>;
-        e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::LAUNCH);
+        e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SS::TOTAL);
         if (e != cudaSuccess) return e;
-        sk<<<units * (unsigned)plan_state_blocks(plan), NTH, SS::LAUNCH, st>>>(a, mk, mv, plan, ws);
+        sk<<<units * (unsigned)plan_state_blocks(plan), NTH, SS::TOTAL, st>>>(a, mk, mv, plan, ws);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     using S = ChunkSmem<R, D>;
