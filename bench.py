@@ -241,19 +241,28 @@ class Prefill:
             _, self.state_in = binding.ida_forward(self.q, self.k, self.v, self.pd, flags=flags,
                                                    final_state=True, workspace=self.ws)
             torch.cuda.synchronize(dev)
+        # end to end: the host-memory entry point, its staging allocated once
+        self.state_in_host = None if self.state_in is None else self.state_in.cpu().pin_memory()
+        self.fs_host = None if self.fs is None else torch.empty(self.fs.shape, dtype=torch.float32).pin_memory()
+        nst = binding.ida_forward_host_staging_bytes(w.B, w.H, w.N, w.d, w.R, w.M, binding._dtype_code(self.q),
+                                                     w.W, flags)
+        self.staging = torch.empty(max(nst, 16), dtype=torch.uint8, device=dev)
 
     def step(self):
         self.b.ida_forward(self.q, self.k, self.v, self.pd, out=self.out, final_state=self.fs,
                            flags=self.flags, workspace=self.ws, state_in=self.state_in)
 
     def step_e2e(self):
-        for src, dst in zip(self.host, (self.q, self.k, self.v)):
-            dst.copy_(src, non_blocking=True)
-        self.step()
-        self.out_host.copy_(self.out, non_blocking=True)
+        # host buffers in, host buffers out: slices copied in, run and copied out on the
+        # library's three streams (ida_forward_host)
+        q, k, v = self.host
+        self.b.ida_forward_host(q, k, v, self.pd, out=self.out_host, final_state=self.fs_host,
+                                state_in=self.state_in_host, flags=self.flags, staging=self.staging)
 
     def e2e_bytes(self):
-        return self.in_bytes, self.out.numel() * self.out.element_size()
+        bi = self.in_bytes + (0 if self.state_in_host is None else self.state_in_host.numel() * 4)
+        bo = self.out.numel() * self.out.element_size() + (0 if self.fs_host is None else self.fs_host.numel() * 4)
+        return bi, bo
 
     def tokens(self):
         return self.w.B * self.w.N

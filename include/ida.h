@@ -30,7 +30,8 @@
  *
  * Conventions for every call:
  *   - All data pointers are device pointers owned by the caller, 16-byte
- *     aligned.  The library allocates no device memory per call.
+ *     aligned (ida_forward_host excepted: its sequence buffers are host
+ *     memory).  The library allocates no device memory per call.
  *   - Calls are asynchronous on `stream` and never synchronise.  The return
  *     value reports argument errors (nothing is launched) and launch errors.
  *   - Kernels never trap.  A device-side fault detected by a kernel (e.g. a
@@ -208,6 +209,58 @@ IDA_API ida_status ida_forward_noalloc(const void *q, const void *k, const void 
                                const float *Bvec, void *out, float *final_state,
                                int B, int H, int N, int d, int R, int M,
                                int dtype, int W, int flags, ida_stream_t stream);
+
+/*
+ * Prefill from host memory.  (The paper has no counterpart: this is a property
+ * of the library.)  The same computation as ida_forward_from, with the
+ * sequence data in host memory:
+ *   q, k, v, out             host buffers, shapes and dtype as in ida_forward;
+ *   state_in, final_state    NULL or host buffers of [B, H] x
+ *                            ida_state_floats(d, R, M, W) floats (as in
+ *                            ida_forward_from); they must not overlap;
+ *   conv_w ... Bvec          device pointers, as in ida_forward;
+ *   staging                  16-byte aligned device buffer owned by the
+ *                            caller, not shared with a concurrent call;
+ *   staging_bytes            at least ida_forward_host_staging_bytes(...).
+ * Host buffers need no alignment.  Pinned (page-locked) host memory lets the
+ * copies run at full speed and overlap the kernels; pageable memory works
+ * but the copies then serialise.
+ *
+ * On the tensor-core path (see ida_forward_ws) the positions are cut into
+ * slices of at least 512 (a multiple of 64, the last one shorter).  The copy
+ * of slice i to the device, the prefill of slice i-1 (resumed from the state
+ * after slice i-2, as ida_forward_from does) and the copy of slice i-2's
+ * outputs to the host run at the same time, on three streams the library
+ * creates once per device; the staging buffer holds two slices of q, k, v and
+ * out, two states and a prefill workspace.  Other shapes run as one slice.
+ * The split changes only the rounding of the carried state, within the
+ * path's tolerance of an unsplit call.
+ *
+ * Asynchronous like every call: the copies and kernels are ordered after the
+ * work queued on `stream` before the call, and work queued on `stream` after
+ * it runs after the last copy to the host.  The host buffers must stay valid
+ * and unchanged until then.  Calls on one device are enqueued one at a time
+ * (a mutex per device); their copies and kernels may still overlap on the
+ * GPU, so concurrent calls need separate staging buffers.  A device error
+ * reported while the slices are enqueued stops the enqueueing: the call
+ * returns IDA_ERR_DEVICE and `stream` still waits for what was enqueued.
+ */
+IDA_API ida_status ida_forward_host(const void *q, const void *k, const void *v,
+                            const float *conv_w, const float *norm_w,
+                            const float *bias, const float *lambda,
+                            const float *Bvec, const float *state_in,
+                            void *out, float *final_state,
+                            int B, int H, int N, int d, int R, int M, int dtype,
+                            int W, int flags, void *staging,
+                            size_t staging_bytes, ida_stream_t stream);
+
+/*
+ * Staging bytes ida_forward_host needs for this shape (with or without
+ * state_in / final_state); 0 when B*H == 0 or the arguments are invalid.
+ * Queries the device (no other CUDA work).
+ */
+IDA_API size_t ida_forward_host_staging_bytes(int B, int H, int N, int d, int R,
+                                              int M, int dtype, int W, int flags);
 
 /*
  * One recurrent decode step (one new position per (b,h) unit): the fixed-size

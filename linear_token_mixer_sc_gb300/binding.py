@@ -23,7 +23,7 @@ IDA_PATH_SEQUENTIAL = 256
 EXPORTED = ("ida_state_floats", "ida_forward", "ida_forward_ws", "ida_forward_from", "ida_forward_workspace_bytes",
             "ida_forward_noalloc", "ida_decode_step", "ida_device_error", "ida_status_str",
             "ida_last_error", "ida_selftest_bounded_wait", "ida_backward", "ida_backward_workspace_bytes",
-            "ida_forward_ideal", "ida_rope")
+            "ida_forward_ideal", "ida_rope", "ida_forward_host", "ida_forward_host_staging_bytes")
 
 _lock = threading.Lock()
 _lib = None
@@ -58,6 +58,11 @@ def load() -> ctypes.CDLL:
                                            _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp]
             L.ida_forward_workspace_bytes.restype = ctypes.c_size_t
             L.ida_forward_workspace_bytes.argtypes = [_i] * 9
+            L.ida_forward_host.restype = _i
+            L.ida_forward_host.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _fp, _vp, _fp,
+                                           _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp]
+            L.ida_forward_host_staging_bytes.restype = ctypes.c_size_t
+            L.ida_forward_host_staging_bytes.argtypes = [_i] * 9
             L.ida_forward_noalloc.restype = _i
             L.ida_forward_noalloc.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _fp,
                                               _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]
@@ -142,6 +147,61 @@ def _params(p: dict):
 def ida_forward_workspace_bytes(B: int, H: int, N: int, d: int, R: int, M: int, dtype: int,
                                 W: int, flags: int = 0) -> int:
     return int(load().ida_forward_workspace_bytes(B, H, N, d, R, M, dtype, W, flags))
+
+
+def ida_forward_host_staging_bytes(B: int, H: int, N: int, d: int, R: int, M: int, dtype: int,
+                                   W: int, flags: int = 0) -> int:
+    return int(load().ida_forward_host_staging_bytes(B, H, N, d, R, M, dtype, W, flags))
+
+
+def ida_forward_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,
+                     out: torch.Tensor | None = None, final_state: torch.Tensor | bool | None = None,
+                     state_in: torch.Tensor | None = None, flags: int = 0,
+                     staging: torch.Tensor | None = None, stream=None):
+    """Prefill from host memory (``ida_forward_host``).  q, k [B,N,H,R], v [B,N,H,d]
+    contiguous CPU tensors (fp32/bf16; pinned memory lets the copies overlap the
+    kernels).  ``params`` as for ``ida_forward`` (CUDA).  ``out``: CPU tensor to fill,
+    or None to allocate a pinned one.  ``final_state``: CPU float32 [B,H,S] tensor,
+    True to allocate a pinned one, or None.  ``state_in``: CPU float32 [B,H,S] or None.
+    ``staging``: CUDA tensor of at least ``ida_forward_host_staging_bytes`` bytes, or
+    None to allocate one.  Asynchronous on ``stream``: synchronise it before reading
+    ``out`` / ``final_state``.  Returns (out, final_state).
+    """
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CPU tensors")
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    B, N, H, R = q.shape
+    d = v.shape[3]
+    cw, nw, bs, lam, bv = _params(params)
+    M, W = lam.shape[1], cw.shape[3]
+    if tuple(k.shape) != (B, N, H, R) or tuple(v.shape[:3]) != (B, N, H):
+        raise ValueError("shape mismatch between q, k and v")
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=q.dtype).pin_memory()
+    if out.is_cuda or not out.is_contiguous() or out.dtype != q.dtype or out.numel() != B * N * H * d:
+        raise ValueError("out must be a contiguous CPU tensor of q's dtype with B*N*H*d elements")
+    S = ida_state_floats(d, R, M, W)
+    if final_state is True:
+        final_state = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
+    elif final_state is False:
+        final_state = None
+    for name, t in (("final_state", final_state), ("state_in", state_in)):
+        if t is not None and (t.is_cuda or not t.is_contiguous() or t.dtype != torch.float32
+                              or t.numel() < B * H * S):
+            raise ValueError(f"{name} must be a contiguous float32 CPU tensor with B*H*ida_state_floats elements")
+    if staging is None:
+        nbytes = ida_forward_host_staging_bytes(B, H, N, d, R, M, dt, W, flags)
+        staging = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=cw.device)
+    if not staging.is_cuda:
+        raise ValueError("staging must be a CUDA tensor")
+    st = load().ida_forward_host(_p(q), _p(k), _p(v), _p(cw), _p(nw), _p(bs), _p(lam), _p(bv), _p(state_in),
+                                 _p(out), _p(final_state), B, H, N, d, R, M, dt, W, int(flags), _p(staging),
+                                 staging.numel() * staging.element_size(), _stream_handle(stream))
+    _check(st, "ida_forward_host")
+    return out, final_state
 
 
 def ida_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, params: dict,

@@ -1875,6 +1875,14 @@ size_t chunk_workspace_bytes(const PrefillArgs &a, int num_sms, size_t budget) {
     return plan_workspace_bytes(choose_plan(a, num_sms, budget), (long long)a.B * a.H, a.R);
 }
 
+// Whether the tensor-core path takes a prefill of this shape and flags (for callers that
+// plan around it; the launch below decides with the same test).
+bool chunk_path_shape(int dtype, int M, int R, int d, int W, int flags) {
+    PrefillArgs a = {};
+    a.dtype = dtype; a.M = M; a.R = R; a.d = d; a.W = W; a.flags = flags;
+    return !(flags & IDA_PATH_SEQUENTIAL) && chunk_path_takes(a);
+}
+
 // Takes bf16 prefill with M = 64 modes and R, d in {64, 128}, denominator-free
 // readout.  The eta readout divides by Re(xi(q)^T U^T eta), which on the
 // synthetic workloads comes within 1e-5 of its scale; fp16 / tf32 operand

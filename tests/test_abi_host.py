@@ -9,6 +9,7 @@ from pathlib import Path
 
 import numpy as np
 import pytest
+import torch
 
 from linear_token_mixer_sc_gb300 import binding, build
 
@@ -85,6 +86,39 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(lib, b, flags=4) == binding.IDA_ERR_ARG  # no such flag bit
     assert _fwd(lib, b, M=0) == binding.IDA_ERR_ARG
     assert "pointer" in binding.ida_last_error() or "must" in binding.ida_last_error()
+
+
+def _fwd_host(lib, b, B=1, H=2, N=8, d=32, R=32, M=16, dtype=0, W=4, flags=0, **over):
+    args = dict(q=b.p, k=b.p, v=b.p, cw=b.p, nw=b.p, bs=b.p, lam=b.p, bv=b.p, si=None, out=b.p, fs=None,
+                stg=b.p, nstg=1 << 30)
+    args.update(over)
+    return lib.ida_forward_host(args["q"], args["k"], args["v"], args["cw"], args["nw"], args["bs"],
+                                args["lam"], args["bv"], args["si"], args["out"], args["fs"], B, H, N, d, R,
+                                M, dtype, W, flags, args["stg"], args["nstg"], None)
+
+
+def test_forward_host_rejects_bad_arguments_on_the_host(lib):
+    """Argument errors of the host-memory prefill are found before any CUDA call."""
+    b = _Bufs()
+    assert _fwd_host(lib, b, q=None) == binding.IDA_ERR_ARG
+    assert _fwd_host(lib, b, out=None) == binding.IDA_ERR_ARG
+    assert _fwd_host(lib, b, lam=b.mis) == binding.IDA_ERR_ARG
+    assert _fwd_host(lib, b, stg=None) == binding.IDA_ERR_ARG
+    assert _fwd_host(lib, b, stg=b.mis) == binding.IDA_ERR_ARG
+    assert "staging" in binding.ida_last_error()
+    assert _fwd_host(lib, b, si=b.p, fs=b.p) == binding.IDA_ERR_ARG  # state_in overlaps final_state
+    assert _fwd_host(lib, b, N=-1) == binding.IDA_ERR_ARG
+    assert _fwd_host(lib, b, dtype=3) == binding.IDA_ERR_ARG
+    assert _fwd_host(lib, b, R=264) == binding.IDA_ERR_UNSUPPORTED
+    assert _fwd_host(lib, b, B=0) == binding.IDA_OK
+    assert _fwd_host(lib, b, N=0, q=None, out=None) == binding.IDA_OK  # nothing to do without final_state
+
+
+def test_forward_host_staging_bytes_without_work_or_device(lib):
+    assert lib.ida_forward_host_staging_bytes(0, 2, 64, 64, 64, 64, 1, 4, 0) == 0
+    assert lib.ida_forward_host_staging_bytes(1, 2, 64, 64, 64, 64, 9, 4, 0) == 0  # bad dtype
+    if not torch.cuda.is_available():
+        assert lib.ida_forward_host_staging_bytes(1, 2, 4096, 64, 64, 64, 1, 4, 0) == 0
 
 
 def test_forward_rejects_unsupported_shapes(lib):
