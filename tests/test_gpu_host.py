@@ -39,6 +39,9 @@ HOST_CASES = [
     (1, 300, 3, 64, 64, 64, 4, "bf16", 0),                 # too short to slice
     (2, 64 * 18, 2, 64, 64, 64, 4, "bf16", binding.IDA_READOUT_ETA),  # eta: one slice
     (1, 90, 2, 32, 32, 16, 4, "f32", 0),                   # fp32: one slice
+    (9, 64 * 16 + 9, 2, 64, 64, 64, 4, "bf16", 0),         # many rows: 3 slices, 512, 512, 9
+    (4, 64 * 5 + 3, 3, 128, 128, 64, 2, "bf16", 0),        # many rows, one slice
+    (9, 70, 2, 64, 64, 64, 4, "bf16", binding.IDA_READOUT_ETA),  # eta, many rows: one slice
 ]
 
 
@@ -54,9 +57,10 @@ def test_host_prefill_matches_oracle(case):
     assert rel_l2(unpadded_state(to_np(fs), d, R, M, W), ref["final_state"]) <= tol
 
 
-def test_host_prefill_from_state_matches_oracle():
+@pytest.mark.parametrize("B", [2, 5])
+def test_host_prefill_from_state_matches_oracle(B):
     """A host call resumed from a state (several slices) against the oracle run from that state."""
-    B, N1, N2, H, R, d, M, W = 2, 150, 64 * 19 + 3, 2, 64, 64, 64, 4
+    N1, N2, H, R, d, M, W = 150, 64 * 19 + 3, 2, 64, 64, 64, 4
     q, k, v, p = problem(B, N1 + N2, H, R, d, M, W, "bf16", seed=77)
     pd = binding.params_to_device(p)
     dev = torch.device("cuda")
@@ -74,9 +78,11 @@ def test_host_prefill_from_state_matches_oracle():
     assert rel_l2(to_np(out), full["out"][:, N1:]) <= BF16_REL_L2
 
 
-def test_host_single_slice_equals_device_call_bytewise():
-    """One slice (eta readout) runs exactly what ida_forward runs on the device."""
-    q, k, v, p = problem(2, 64 * 18, 2, 64, 64, 64, 4, "bf16", seed=78)
+@pytest.mark.parametrize("B", [2, 9])
+def test_host_sequential_path_equals_device_call_bytewise(B):
+    """A call the tensor-core path does not take (eta readout) runs as one slice: its bytes
+    are ida_forward's."""
+    q, k, v, p = problem(B, 64 * 18, 2, 64, 64, 64, 4, "bf16", seed=78)
     pd = binding.params_to_device(p)
     flags = binding.IDA_READOUT_ETA
     out_h, fs_h = _host(q, k, v, pd, final_state=True, flags=flags)
@@ -87,8 +93,9 @@ def test_host_single_slice_equals_device_call_bytewise():
     assert torch.equal(fs_h, fs_d.cpu())
 
 
-def test_host_pageable_memory_gives_the_same_bytes():
-    q, k, v, p = problem(2, 64 * 17 + 11, 2, 64, 64, 64, 4, "bf16", seed=79)
+@pytest.mark.parametrize("B", [2, 5])
+def test_host_pageable_memory_gives_the_same_bytes(B):
+    q, k, v, p = problem(B, 64 * 17 + 11, 2, 64, 64, 64, 4, "bf16", seed=79)
     pd = binding.params_to_device(p)
     a, fa = _host(q, k, v, pd, pinned=True, final_state=True)
     b, fb = _host(q, k, v, pd, pinned=False, out=torch.empty_like(a), final_state=torch.empty_like(fa))
@@ -130,11 +137,12 @@ def test_host_call_is_ordered_on_a_side_stream():
     assert torch.equal(out, ref)
 
 
-def test_host_zero_length_copies_state():
-    q, k, v, p = problem(1, 9, 2, 64, 64, 64, 4, "bf16", seed=82)
+@pytest.mark.parametrize("B", [1, 6])
+def test_host_zero_length_copies_state(B):
+    q, k, v, p = problem(B, 9, 2, 64, 64, 64, 4, "bf16", seed=82)
     pd = binding.params_to_device(p)
     _, fs1 = _host(q, k, v, pd, final_state=True)
-    e = torch.empty((1, 0, 2, 64), dtype=torch.bfloat16)
+    e = torch.empty((B, 0, 2, 64), dtype=torch.bfloat16)
     _, fs2 = _host(e, e.clone(), e.clone(), pd, final_state=True, state_in=fs1)
     assert torch.equal(fs1, fs2)
     _, fs3 = _host(e, e.clone(), e.clone(), pd, final_state=torch.full_like(fs1, 3.0))
