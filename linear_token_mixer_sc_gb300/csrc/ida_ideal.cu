@@ -299,8 +299,10 @@ static cudaError_t launch_ideal_nc(const IdealArgs &a, int G, int Mg, size_t sme
 
 template <int NC, typename T>
 static cudaError_t launch_ideal_p(const IdealArgs &a, int num_sms, std::string &why, cudaStream_t st, bool &fits) {
-    // G CTAs per unit (a cluster) split the modes: as few as the state's shared memory
-    // allows, then more while the units' clusters still fit two CTAs per SM
+    // G CTAs per unit (a cluster) split the modes: at least as many as the state's shared
+    // memory needs, then the most (up to 8, two modes or more each) whose clusters still fit
+    // one wave of two CTAs per SM.  Any G works (the last CTA's mode range may be short): at
+    // 96 units on 152 SMs, G = 3 timed 3.98 ms against 4.51 ms for G = 2 and 6.35 ms for G = 4
     constexpr int P = IdlTile<NC>::P;
     const size_t kMaxSmem = 227 * 1024;
     const int F = 2 * a.D;
@@ -311,7 +313,8 @@ static cudaError_t launch_ideal_p(const IdealArgs &a, int num_sms, std::string &
     fits = ideal_smem_bytes<T>((a.M + G - 1) / G, F, a.d, P, a.Rin, om_stage) <= kMaxSmem;
     if (!fits) return cudaSuccess;
     const long units = (long)a.B * a.H;
-    while (G < 8 && 2 * G <= a.M && units * 2 * G <= 2L * num_sms) G *= 2;
+    for (int g = G + 1; g <= 8 && 2 * g <= a.M; ++g)
+        if (units * g <= 2L * num_sms) G = g;
     const int Mg = (a.M + G - 1) / G;
     return launch_ideal_nc<NC, T>(a, G, Mg, ideal_smem_bytes<T>(Mg, F, a.d, P, a.Rin, om_stage), st);
 }
