@@ -135,20 +135,11 @@ __device__ __forceinline__ int down_exp(float x) {
     return e > 15 ? 15 : e;
 }
 
-// SiLU with one special-function op: x sigmoid(x) = h + h tanh(h), h = x / 2, through the
-// hardware tanh approximation (relative error about 2^-11, below the fp16 rounding of every
-// operand built from it)
-__device__ __forceinline__ float silu_tanh(float x) {
-    const float h = 0.5f * x;
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
-    return fmaf(h, t, h);
-}
-
 // x rounded to the tf32 grid (10 mantissa bits), nearest with ties away from zero, as bits
 __device__ __forceinline__ uint32_t tf32_bits(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
 
-// the hardware tanh approximation (relative error about 2^-11)
+// the hardware tanh approximation (relative error about 2^-11, below the fp16 rounding of
+// every operand built from it).  SiLU takes one such op: x sigmoid(x) = h + h tanh(h), h = x / 2
 __device__ __forceinline__ float tanh_approx(float x) {
     float t;
     asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
@@ -1440,13 +1431,17 @@ __global__ void __launch_bounds__(NTH, 1)
     // key conv taps of my channel block, right-aligned (as in the readout kernel)
     constexpr int CBQ = R / 8, PPQ = CH * CBQ / NTH;
     const int cb = tid % CBQ, i0 = (tid / CBQ) * PPQ, c0 = 8 * cb;
-    float tk[32];
+    // as channel pairs for the packed fp32x2 arithmetic: tp[e2][jj] = (tap jj of channel
+    // 2 e2, of channel 2 e2 + 1)
+    f2_t tp[4][4];
     {
         const float *cwg = a.conv_w + ((size_t)(1 * H + h) * R + c0) * W;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
+        for (int e2 = 0; e2 < 4; ++e2)
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) tk[4 * e + jj] = jj >= 4 - W ? cwg[e * W + jj - (4 - W)] : 0.f;
+            for (int jj = 0; jj < 4; ++jj)
+                tp[e2][jj] = jj >= 4 - W ? f2_pack(cwg[(2 * e2) * W + jj - (4 - W)], cwg[(2 * e2 + 1) * W + jj - (4 - W)])
+                                         : 0ull;
     }
     tc_fence_before();
     __syncthreads();
@@ -1457,14 +1452,20 @@ __global__ void __launch_bounds__(NTH, 1)
         tma_load_4d(sm + S::RAWK, &tm_k, 0, h, c_begin * CH - HALO, b, &bar[0]);
         tma_load_4d(sm + S::RAWV, &tm_v, 0, h, c_begin * CH, b, &bar[0]);
     }
-    float nwk[8], bsk[8];
+    f2_t nwk[4], bsk[4];  // key RMSNorm weight and bias of my channel pairs
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        nwk[e] = nws[c0 + e];
-        bsk[e] = bss[c0 + e];
+    for (int e2 = 0; e2 < 4; ++e2) {
+        nwk[e2] = f2_pack(nws[c0 + 2 * e2], nws[c0 + 2 * e2 + 1]);
+        bsk[e2] = f2_pack(bss[c0 + 2 * e2], bss[c0 + 2 * e2 + 1]);
     }
     constexpr int CBV = D / 8, PPV = CH * CBV / NTH;
     const int cbv = tid % CBV, iv0 = (tid / CBV) * PPV, j0 = 8 * cbv;
+    f2_t nwv[4], bsv[4];  // value RMSNorm weight and bias of my channel pairs
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+        nwv[e2] = f2_pack(nws[R + j0 + 2 * e2], nws[R + j0 + 2 * e2 + 1]);
+        bsv[e2] = f2_pack(bss[R + j0 + 2 * e2], bss[R + j0 + 2 * e2 + 1]);
+    }
     bool ok = true;
     int tma_pending = 1;
     int ci = c_begin;
@@ -1485,22 +1486,27 @@ __global__ void __launch_bounds__(NTH, 1)
             }
             __syncthreads();
         }
-        // key conv and the raw value rows: the staged tiles are then free for the next chunk
-        float fk[PPQ][8];
+        // key conv (channel pairs, packed fp32x2) and the raw value rows: the staged tiles
+        // are then free for the next chunk
+        f2_t g[PPQ][4];
 #pragma unroll
         for (int pp = 0; pp < PPQ; ++pp)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) fk[pp][e] = 0.f;
+            for (int e2 = 0; e2 < 4; ++e2) g[pp][e2] = 0ull;
 #pragma unroll
         for (int r = 0; r < PPQ + HALO; ++r) {
-            float x8[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4 *>(sm + S::RAWK + ((size_t)(i0 + r) * R + c0) * 2), x8);
+            const uint4 u = *reinterpret_cast<const uint4 *>(sm + S::RAWK + ((size_t)(i0 + r) * R + c0) * 2);
+            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+            f2_t x2[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2)
+                x2[e2] = f2_pack(__uint_as_float(wv[e2] << 16), __uint_as_float(wv[e2] & 0xFFFF0000u));
 #pragma unroll
             for (int pp = 0; pp < PPQ; ++pp) {
                 const int jj = r - pp;
                 if (jj >= 0 && jj < 4)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) fk[pp][e] = fmaf(tk[4 * e + jj], x8[e], fk[pp][e]);
+                    for (int e2 = 0; e2 < 4; ++e2) g[pp][e2] = f2_fma(tp[e2][jj], x2[e2], g[pp][e2]);
             }
         }
         uint4 vraw[PPV];
@@ -1520,44 +1526,67 @@ __global__ void __launch_bounds__(NTH, 1)
             tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[0]);
         }
         if (ci + 1 < c_end) tma_pending = 1;
-        // key features: SiLU, squared-norm normalisation, RMSNorm + affine
+        // key features, channel pairs in packed fp32x2: SiLU (h + h tanh h, h = x / 2),
+        // squared-norm normalisation, RMSNorm + affine
+        float fk[PPQ][8];
+        {
+            const f2_t half2 = f2_pack(0.5f, 0.5f);
 #pragma unroll
-        for (int pp = 0; pp < PPQ; ++pp) {
-            float acc = 0.f;
+            for (int pp = 0; pp < PPQ; ++pp) {
+                f2_t s2 = 0ull;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                fk[pp][e] = silu_tanh(fk[pp][e]);
-                acc = fmaf(fk[pp][e], fk[pp][e], acc);
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const f2_t h2 = f2_mul(g[pp][e2], half2);
+                    float hl, hh;
+                    f2_unpack(h2, hl, hh);
+                    g[pp][e2] = f2_fma(h2, f2_pack(tanh_approx(hl), tanh_approx(hh)), h2);
+                    s2 = f2_fma(g[pp][e2], g[pp][e2], s2);
+                }
+                float sl, sh;
+                f2_unpack(s2, sl, sh);
+                float acc = sl + sh;
+#pragma unroll
+                for (int o = 1; o < CBQ; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                const float inv = __fdividef(1.f, (feat_l2 ? sqrtf(acc) : acc) + IDA_EPS_FEAT);
+                const f2_t inv2 = f2_pack(inv, inv);
+                f2_t m2 = 0ull;
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    g[pp][e2] = f2_mul(g[pp][e2], inv2);
+                    m2 = f2_fma(g[pp][e2], g[pp][e2], m2);
+                }
+                f2_unpack(m2, sl, sh);
+                float ms = sl + sh;
+#pragma unroll
+                for (int o = 1; o < CBQ; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
+                const float rk = rsqrtf(ms / R + IDA_EPS_RMS);
+                const f2_t rk2 = f2_pack(rk, rk);
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2)
+                    f2_unpack(f2_fma(f2_mul(g[pp][e2], rk2), nwk[e2], bsk[e2]), fk[pp][2 * e2], fk[pp][2 * e2 + 1]);
             }
-#pragma unroll
-            for (int o = 1; o < CBQ; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            const float inv = __fdividef(1.f, (feat_l2 ? sqrtf(acc) : acc) + IDA_EPS_FEAT);
-            float ms = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                fk[pp][e] *= inv;
-                ms = fmaf(fk[pp][e], fk[pp][e], ms);
-            }
-#pragma unroll
-            for (int o = 1; o < CBQ; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
-            const float rk = rsqrtf(ms / R + IDA_EPS_RMS);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) fk[pp][e] = fmaf(fk[pp][e] * rk, nwk[e], bsk[e]);
         }
-        // value RMSNorm + affine
+        // value RMSNorm + affine, channel pairs in packed fp32x2
         float vt[PPV][8];
 #pragma unroll
         for (int pp = 0; pp < PPV; ++pp) {
-            float x8[8];
-            unpack_bf16x8(vraw[pp], x8);
-            float ms = 0.f;
+            const uint32_t wv[4] = {vraw[pp].x, vraw[pp].y, vraw[pp].z, vraw[pp].w};
+            f2_t x2[4], m2 = 0ull;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ms = fmaf(x8[e], x8[e], ms);
+            for (int e2 = 0; e2 < 4; ++e2) {
+                x2[e2] = f2_pack(__uint_as_float(wv[e2] << 16), __uint_as_float(wv[e2] & 0xFFFF0000u));
+                m2 = f2_fma(x2[e2], x2[e2], m2);
+            }
+            float sl, sh;
+            f2_unpack(m2, sl, sh);
+            float ms = sl + sh;
 #pragma unroll
             for (int o = 1; o < CBV; o <<= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
             const float rv = rsqrtf(ms / D + IDA_EPS_RMS);
+            const f2_t rv2 = f2_pack(rv, rv);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) vt[pp][e] = fmaf(x8[e] * rv, nws[R + j0 + e], bss[R + j0 + e]);
+            for (int e2 = 0; e2 < 4; ++e2)
+                f2_unpack(f2_fma(f2_mul(x2[e2], rv2), nwv[e2], bsv[e2]), vt[pp][2 * e2], vt[pp][2 * e2 + 1]);
         }
         // Coef_c row: mu = lambda^(64 (fs - 1 - lc)) by squaring, times B lambda^k
         float mr = 1.f, mi = 0.f;
