@@ -167,13 +167,29 @@ __global__ void __launch_bounds__(SEQ_THREADS, 1) seq_prefill_kernel(PrefillArgs
 
     for (int t0 = 0; t0 < N; t0 += TT) {
         const int tn = min(TT, N - t0);
-        // Phase A: prologue, one warp per position; clear the partials.
-        if (warp < tn) {
-            seq_prologue<NC, T>(a, h, base_qk, base_v, t0 + warp, xq + warp * R, z + warp * RD, lane, tails);
-            for (int j = lane; j < d; j += 32) opart[warp * d + j] = T(0);
-            if (lane == 0) dpart[warp] = T(0);
+        // Phase A: prologue, one warp per position, the tile's positions spread over the
+        // cluster (CTA r computes positions tt = r (mod G) and stores their rows into every
+        // CTA of the cluster); clear the partials.
+        for (int tt = rank + G * warp; tt < tn; tt += G * SEQ_WARPS) {
+            T *xrow = xq + tt * R, *zrow = z + tt * RD;
+            seq_prologue<NC, T>(a, h, base_qk, base_v, t0 + tt, xrow, zrow, lane, tails);
+            if (G > 1) {
+                __syncwarp();
+                for (int r = 0; r < G; ++r) {
+                    if (r == rank) continue;
+                    T *rx = cg::this_cluster().map_shared_rank(xrow, r);
+                    T *rz = cg::this_cluster().map_shared_rank(zrow, r);
+                    for (int c = lane; c < R; c += 32) rx[c] = xrow[c];
+                    for (int c = lane; c < RD; c += 32) rz[c] = zrow[c];
+                }
+            }
         }
-        __syncthreads();
+        for (int i = threadIdx.x; i < tn * d; i += SEQ_THREADS) opart[i] = T(0);
+        for (int i = threadIdx.x; i < tn; i += SEQ_THREADS) dpart[i] = T(0);
+        if (G == 1)
+            __syncthreads();
+        else
+            cg::this_cluster().sync();
         // Phase B: recurrence + per-mode readout, one warp per mode.
         for (int ml = warp; ml < mcount; ml += SEQ_WARPS) {
             const int m = m0 + ml;
