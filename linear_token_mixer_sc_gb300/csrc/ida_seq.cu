@@ -14,7 +14,8 @@
 // [r*Mg, (r+1)*Mg) and produces a partial readout over them; the G partials
 // of each position are summed through distributed shared memory.  Positions
 // are processed in tiles of seq_tile<T>(): the prologue (conv, SiLU feature map,
-// RMSNorm) of a tile runs one warp per position, then every warp walks the
+// RMSNorm) of a tile runs one warp per position, the positions dealt over the
+// cluster's CTAs, each storing its rows into every CTA; then every warp walks the
 // tile's positions for its modes with the mode's state row in registers.
 //
 // Arithmetic type T: double for fp32 inputs, float for bf16 inputs.  With
