@@ -28,6 +28,11 @@ CASES = [
     (1, 200, 2, 64, 32, 64, 64, "f32"),
     (2, 130, 2, 64, 32, 64, 64, "bf16"),
     (1, 90, 4, 128, 64, 128, 64, "bf16"),
+    # unit counts whose clusters fill one wave of two CTAs per SM with G = 5, 6, 7 on 152 SMs:
+    # uneven mode ranges (13 x 4 + 12, 11 x 5 + 9, 10 x 6 + 4 modes)
+    (4, 40, 13, 32, 16, 32, 64, "bf16"),
+    (2, 30, 24, 32, 16, 32, 64, "bf16"),
+    (5, 25, 8, 32, 16, 32, 64, "f32"),
 ]
 
 
