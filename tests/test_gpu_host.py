@@ -42,6 +42,7 @@ HOST_CASES = [
     (9, 64 * 16 + 9, 2, 64, 64, 64, 4, "bf16", 0),         # many rows: 3 slices, 512, 512, 9
     (4, 64 * 5 + 3, 3, 128, 128, 64, 2, "bf16", 0),        # many rows, one slice
     (9, 70, 2, 64, 64, 64, 4, "bf16", binding.IDA_READOUT_ETA),  # eta, many rows: one slice
+    (2, 64 * 17 + 11, 2, 128, 128, 64, 4, "bf16", binding.IDA_FEAT_L2),  # l_2 map, 3 resumed slices
 ]
 
 
@@ -51,7 +52,7 @@ def test_host_prefill_matches_oracle(case):
     q, k, v, p = problem(B, N, H, R, d, M, W, dt, seed=500 + N)
     pd = binding.params_to_device(p)
     out, fs = _host(q, k, v, pd, final_state=True, flags=flags)
-    ref = orc.forward(q, k, v, p, flags=flags & binding.IDA_READOUT_ETA, final_state=True)
+    ref = orc.forward(q, k, v, p, flags=flags & (binding.IDA_READOUT_ETA | binding.IDA_FEAT_L2), final_state=True)
     tol = F32_REL_L2 if dt == "f32" else BF16_REL_L2
     assert rel_l2(to_np(out), ref["out"]) <= tol
     assert rel_l2(unpadded_state(to_np(fs), d, R, M, W), ref["final_state"]) <= tol
