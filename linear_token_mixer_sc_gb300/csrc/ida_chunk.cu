@@ -341,6 +341,7 @@ __global__ void __launch_bounds__(NTH, 1)
     bool ok = true;
     int it = 0;           // chunks this CTA has run so far: the phase parity of every barrier
     int tma_pending = 0;  // TMA copies issued and not yet waited for
+    uint32_t tma_par = 0;  // the bar[5] phase parity that the copy in flight completes
     int ci = 0;
     {
         const int fsc = FACT ? (int)ceilf(0.5f * log2f(bb2) + lg63 + 0.01f) + 1 : 0;  // T max <= 1/2
@@ -1167,6 +1168,18 @@ __global__ void __launch_bounds__(NTH, 1)
             // under the O1 MMA: Gamma^T scaled by lambda^L once O2, its reader, is complete
             ok = mbar_wait(&bar[3], par);
             tc_fence_after();
+            if (ok && tid == 0 && ci + 1 < c_end) {
+                // A2' (S6) and O2, the last readers of YA16 / AP32, are complete, and the generic
+                // writes there were fenced before S6: the next chunk's raw rows land there under
+                // the rest of this chunk
+                tma_pending = 1;
+                tma_par = (uint32_t)((it + 1) & 1);
+                const int tn = t0 + CH;
+                mbar_arrive_expect_tx(&bar[5], raw_bytes);
+                tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, tn - HALO, b, &bar[5]);
+                tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[5]);
+                tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[5]);
+            }
             if (ok) {
                 // Gamma^T (lanes = value channels, columns = (Re, Im) per mode)
                 float v[4][16];
@@ -1190,17 +1203,10 @@ __global__ void __launch_bounds__(NTH, 1)
             tc_fence_after();
             if (__syncthreads_or(!ok)) break;
 
-            // ---- S9: next chunk's raw rows; outputs; eta -----------------------------------------
+            // ---- S9: outputs; eta (the next chunk's raw rows were issued in S8) --------------------
             if (ci + 1 < c_end) {
                 tma_pending = 1;
-                if (tid == 0) {
-                    // YA16 / AP32 were last read by the S6 / S8 MMAs, both complete
-                    const int tn = t0 + CH;
-                    mbar_arrive_expect_tx(&bar[5], raw_bytes);
-                    tma_load_4d(sm + S::RAWQ, &tm_q, 0, h, tn - HALO, b, &bar[5]);
-                    tma_load_4d(sm + S::RAWK, &tm_k, 0, h, tn - HALO, b, &bar[5]);
-                    tma_load_4d(sm + S::RAWV, &tm_v, 0, h, tn, b, &bar[5]);
-                }
+                tma_par = (uint32_t)((it + 1) & 1);
             }
             {
                 // outputs o[i][jv] into the [64][D] bf16 store tile over GP16 / A216 (dead from
@@ -1271,7 +1277,7 @@ __global__ void __launch_bounds__(NTH, 1)
         ok = !__syncthreads_or(!ok);
         if (!ok) {
             // error path: let a copy still in flight land before the CTA exits
-            if (tma_pending) mbar_wait(&bar[5], (uint32_t)(it & 1), 200000000LL);
+            if (tma_pending) mbar_wait(&bar[5], tma_par, 200000000LL);
             if (tid == 0) report_error(a.err, kErrWaitTimeout);
         }
         if (ok && a.final_state && c_end == nchunks) {
