@@ -756,7 +756,7 @@ __global__ void __launch_bounds__(NTH, 1)
             if (__syncthreads_or(!ok)) break;
             tc_fence_after();
 
-            // ---- S2: G and P^T ------------------------------------------------------
+            // ---- S2: G (and P^T on the skewed path; the factorised path issues it in S3) ----------
             if (warp == 0 && elect_one()) {
                 const uint32_t idg = idesc(128, 64, 0, 0);
     #pragma unroll
@@ -764,9 +764,9 @@ __global__ void __launch_bounds__(NTH, 1)
                     mma_f16(tb + T::G, sdesc_at(s16, S::XQ16 + s * 256, 128, 16 * R),
                                sdesc_at(s16, S::KT16 + s * 256, 128, 16 * R), idg, s > 0);
                 mma_commit(&bar[0]);
-            } else if (warp == 1 && elect_one()) {
-                // P^T from a second issuing thread: an issuing thread stalls while the tensor pipe's
-                // queue is full, and one thread issuing both measured slower
+            } else if (!FACT && warp == 1 && elect_one()) {
+                // skewed path: P^T from a second issuing thread (an issuing thread stalls while the
+                // tensor pipe's queue is full, and one thread issuing both measured slower)
                 const uint32_t idp = idesc(128, 64, 2, 2);
     #pragma unroll
                 for (int s = 0; s < R / 8; ++s)
@@ -775,7 +775,8 @@ __global__ void __launch_bounds__(NTH, 1)
             }
             __syncwarp();
 
-            // ---- S1b, under the G / P^T MMAs: Z^T key rows, the value rows, a ragged Coef --------
+            // ---- S1b, under the G MMA (and P^T on the skewed path): Z^T key rows, the value rows,
+            // a ragged Coef
             // (read by the O1 and state-update MMAs, after later proxy fences and barriers)
             {
                 const int cb = tid % CBQ, i0 = (tid / CBQ) * PPQ, c0 = 8 * cb;
@@ -856,6 +857,21 @@ __global__ void __launch_bounds__(NTH, 1)
             if (__syncthreads_or(!ok)) break;
 
             // ---- S3: G' = skewed, masked G (skewed path); masked G (factorised path) --------
+            if constexpr (FACT) {
+                // P^T, first read in S5, issued once G is complete, so that G ran alone on the
+                // tensor pipe and P^T runs under the masking, from a warp the masking leaves idle
+                // (U is final since the previous state update; XQ32 was fenced before S2)
+                if (warp == 2 && elect_one()) {
+                    tc_fence_after();
+                    const uint32_t idp = idesc(128, 64, 2, 2);
+    #pragma unroll
+                    for (int s = 0; s < R / 8; ++s)
+                        mma_tf32_t(tb + T::PT, tb + T::U + 8 * s, sdesc_at(s16, S::XQ32 + s * 256, 128, 32 * R), idp,
+                                   s > 0);
+                    mma_commit(&bar[6]);
+                }
+                __syncwarp();
+            }
             // skewed path: scratch [64][64] rotated by row, over YA16: the raw tile there is
             // consumed and YA16 is not rewritten before S5 (XQ32 may still be read by the P^T MMA)
             float *scr = reinterpret_cast<float *>(sm + S::YA16);
