@@ -1056,8 +1056,8 @@ __global__ void __launch_bounds__(NTH, 1)
                     mma_f16(tb + T::G, sdesc_at(s16, S::YA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO),
                                sdesc_at(s16, S::TA16 + s * 2 * PADLBO, PADLBO, S::TY_SBO), id, s > 0);
                 mma_commit(&bar[2]);
-            } else if (warp == 1 && elect_one()) {
-                // O2 = Gamma^T . a'^T needs only S5's a' and the state: it runs under S7
+            } else if (!FACT && warp == 1 && elect_one()) {
+                // skewed path: O2 = Gamma^T . a'^T needs only S5's a' and the state: it runs under S7
                 const uint32_t id32 = idesc(128, 64, 2, 2);
     #pragma unroll
                 for (int s = 0; s < MP / 8; ++s)
@@ -1066,8 +1066,8 @@ __global__ void __launch_bounds__(NTH, 1)
                 mma_commit(&bar[3]);
             }
             __syncwarp();
-            // under the A2' / O2 MMAs: U scaled by lambda^L (its last reader, P^T, is complete;
-            // the next one is this chunk's state update)
+            // under the A2' MMA (and O2 on the skewed path): U scaled by lambda^L (its last reader,
+            // P^T, is complete; the next one is this chunk's state update)
             {
                 // U (lanes = mode planes): the partner lane holds the other component
                 const float2 lm = laml[mm];
@@ -1094,6 +1094,22 @@ __global__ void __launch_bounds__(NTH, 1)
             if (__syncthreads_or(!ok)) break;
 
             // ---- S7: A2 = unskewed (skewed path), masked A2' (row-scaled fp16) ----------------
+            if constexpr (FACT) {
+                // O2 = Gamma^T . a'^T, first read in S8, issued once A2' is complete, so that A2'
+                // ran alone on the tensor pipe and O2 runs under the masking, from a warp the
+                // masking leaves idle (AP32 was fenced before S6; Gamma^T is rescaled only in S8,
+                // after O2 completes)
+                if (warp == 2 && elect_one()) {
+                    tc_fence_after();
+                    const uint32_t id32 = idesc(128, 64, 2, 2);
+    #pragma unroll
+                    for (int s = 0; s < MP / 8; ++s)
+                        mma_tf32_t(tb + T::LT, tb + T::GT + 8 * s,
+                                   sdesc_at(s16, S::AP32 + s * 2 * PADLBO, PADLBO, S::AP_SBO), id32, s > 0);
+                    mma_commit(&bar[3]);
+                }
+                __syncwarp();
+            }
             // skewed path: scratch over XQ32 (P^T, its last reader, is complete)
             if constexpr (!FACT) {
                 scr = reinterpret_cast<float *>(sm + S::XQ32);
